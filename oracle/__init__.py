@@ -1,0 +1,234 @@
+"""CPU oracle for one Sparse Delta Memory (SDM) layer forward pass.
+
+TEST INFRASTRUCTURE ONLY: only `tests/`, `__graft_entry__.smoke()` and the
+benchmark's CPU-baseline leg may import this package. The CUDA library never
+imports, links or calls it, and it shares no code with the CUDA library.
+
+The arithmetic lives in `sdm_oracle.c` (plain C, fp64, OpenMP over independent
+rows/queries). This module builds it with gcc on first use and wraps it for numpy /
+CPU torch tensors. The steps follow the Sparse Delta Memory blog post ("How does SDM
+work?", "Write & Read") and the frozen readings:
+
+- `project`:  q^w = x W_qw, q^r = x W_qr, v = x W_v, fp64 sums rounded once;
+- `address`:  product-key scores s1, s2, exhaustive top-W of the outer sum with
+  ties broken by smaller slot id, temperature-1 softmax over the kept scores;
+- `scan`:     per token decay then delta rule on the write slots, then the
+  softmax-weighted read of the read slots from the post-write bank.
+
+Every function is pinned by tests/test_oracle_pins.py against closed forms,
+hand-worked values, brute force on tiny inputs and invariants.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+F32, BF16, F64 = 0, 1, 2
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sdm_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile sdm_oracle.c into liboracle.so beside it (gcc, fp-contract off)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+                               "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = ctypes.CDLL(build())
+            P, I, L, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+            _lib.orc_bf16_from_double.argtypes = [D]
+            _lib.orc_bf16_from_double.restype = ctypes.c_uint16
+            _lib.orc_round_store.argtypes = [P, L, I, P]
+            _lib.orc_project.argtypes = [P, P, I, L, I, I, P]
+            _lib.orc_subkey_scores.argtypes = [P, I, I, P, P, I, P, P]
+            _lib.orc_topw.argtypes = [P, P, I, I, P, P, P]
+            _lib.orc_softmax.argtypes = [P, I, P]
+            _lib.orc_address.argtypes = [P, I, L, I, P, P, I, I, P, P, P, P]
+            _lib.orc_scan.argtypes = [I, I, L, I, L, I, P, P, P, P, P, P, P, P, P]
+            _lib.orc_scan.restype = I
+            _lib.orc_init_bank.argtypes = [P, L, I, P]
+    return _lib
+
+
+# ------------------------------------------------------------------ conversions
+
+def storage(a):
+    """Return (contiguous numpy array, storage type) for a numpy array or CPU torch
+    tensor. bf16 tensors become uint16 bit patterns."""
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            a = a.detach().cpu().contiguous()
+            if a.dtype == torch.bfloat16:
+                return a.view(torch.int16).numpy().view(np.uint16), BF16
+            a = a.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return a, BF16
+    if a.dtype == np.float32:
+        return a, F32
+    if a.dtype == np.float64:
+        return a, F64
+    raise TypeError("unsupported dtype %s" % a.dtype)
+
+
+def to_f64(a) -> np.ndarray:
+    """Exact fp64 values of a storage array (numpy/torch; bf16 as uint16 or torch)."""
+    arr, t = storage(a)
+    if t == BF16:
+        return (arr.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return arr.astype(np.float64)
+
+
+def _empty(shape, type_):
+    return np.empty(shape, dtype={F32: np.float32, BF16: np.uint16, F64: np.float64}[type_])
+
+
+def _p(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def round_to(values, type_) -> np.ndarray:
+    """Round fp64 values once to a storage type (bf16 RNE / fp32 / fp64)."""
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    out = _empty(v.shape, type_)
+    lib().orc_round_store(_p(v), v.size, type_, _p(out))
+    return out
+
+
+# ------------------------------------------------------------------- the steps
+
+def project(x, Wm) -> np.ndarray:
+    """x [rows, din] @ Wm [din, dout], fp64 sum, rounded once to the storage type."""
+    xa, t = storage(x)
+    wa, tw = storage(Wm)
+    assert t == tw
+    rows, din = xa.reshape(-1, xa.shape[-1]).shape
+    dout = wa.shape[1]
+    out = _empty((rows, dout), t)
+    lib().orc_project(_p(xa), _p(wa), t, rows, din, dout, _p(out))
+    return out.reshape(xa.shape[:-1] + (dout,))
+
+
+def subkey_scores(q, K1, K2):
+    """Sub-key scores of one query: (s1 [n], s2 [n]) in fp64."""
+    qa, t = storage(q)
+    k1, _ = storage(K1)
+    k2, _ = storage(K2)
+    n = k1.shape[0]
+    s1 = np.empty(n)
+    s2 = np.empty(n)
+    lib().orc_subkey_scores(_p(qa), t, qa.shape[-1], _p(k1), _p(k2), n, _p(s1), _p(s2))
+    return s1, s2
+
+
+def topw(s1, s2, W):
+    """Exhaustive top-W of the outer sum: (slots [W], scores [W], gap)."""
+    s1 = np.ascontiguousarray(s1, dtype=np.float64)
+    s2 = np.ascontiguousarray(s2, dtype=np.float64)
+    slots = np.empty(W, dtype=np.int32)
+    scores = np.empty(W)
+    gap = np.empty(1)
+    lib().orc_topw(_p(s1), _p(s2), len(s1), W, _p(slots), _p(scores), _p(gap))
+    return slots, scores, float(gap[0])
+
+
+def softmax(c) -> np.ndarray:
+    c = np.ascontiguousarray(c, dtype=np.float64)
+    w = np.empty_like(c)
+    lib().orc_softmax(_p(c), len(c), _p(w))
+    return w
+
+
+def address(q, K1, K2, W):
+    """Addressing of queries q [..., dk]: slots, weights, scores ([..., W]) and the
+    boundary gap [...] between the W-th and (W+1)-th combined score."""
+    qa, t = storage(q)
+    k1, t1 = storage(K1)
+    k2, _ = storage(K2)
+    assert t == t1
+    dk = qa.shape[-1]
+    lead = qa.shape[:-1]
+    nq = int(np.prod(lead)) if lead else 1
+    n = k1.shape[0]
+    slots = np.empty((nq, W), dtype=np.int32)
+    weights = np.empty((nq, W))
+    scores = np.empty((nq, W))
+    gaps = np.empty(nq)
+    lib().orc_address(_p(qa), t, nq, dk, _p(k1), _p(k2), n, W, _p(slots), _p(weights),
+                      _p(scores), _p(gaps))
+    return (slots.reshape(lead + (W,)), weights.reshape(lead + (W,)),
+            scores.reshape(lead + (W,)), gaps.reshape(lead))
+
+
+def scan(M, v, alpha, beta, S, k, Rd, r):
+    """Recurrence of one sequence on a subset of rows.
+
+    M [N, R] (storage array, updated IN PLACE; the selected rows of every slot),
+    v [T, R] storage array, alpha/beta [T], S/Rd [T, W] int slot ids, k/r [T, W]
+    weights. Returns y [T, R] (fp64)."""
+    if not (isinstance(M, np.ndarray) and M.flags["C_CONTIGUOUS"]):
+        raise ValueError("M must be a C-contiguous numpy array (it is updated in place)")
+    Ma, tm = storage(M)
+    va, tv = storage(v)
+    N, R = Ma.shape
+    T, W = np.asarray(S).shape
+    al = np.ascontiguousarray(to_f64(alpha).reshape(T))
+    be = np.ascontiguousarray(to_f64(beta).reshape(T))
+    Sa = np.ascontiguousarray(S, dtype=np.int32)
+    Ra = np.ascontiguousarray(Rd, dtype=np.int32)
+    ka = np.ascontiguousarray(to_f64(k).reshape(T, W))
+    ra = np.ascontiguousarray(to_f64(r).reshape(T, W))
+    y = np.empty((T, R))
+    rc = lib().orc_scan(tm, tv, N, R, T, W, _p(Ma), _p(va), _p(al), _p(be), _p(Sa), _p(ka),
+                        _p(Ra), _p(ra), _p(y))
+    if rc != 0:
+        raise ValueError("oracle scan: slot id out of range or repeated within a set")
+    return y
+
+
+def init_bank(M0, B):
+    """B copies of the learned initial state, [B, N, d] (storage array)."""
+    m, t = storage(M0)
+    banks = _empty((B,) + m.shape, t)
+    lib().orc_init_bank(_p(m), m.nbytes, B, _p(banks))
+    return banks
+
+
+def prefill_sequence(x, params, alpha, beta, W, rows=None, M=None):
+    """Whole layer for ONE sequence: project, address, scan.
+
+    x [T, d]; params: W_qw, W_qr, W_v, K1, K2, M0 (storage tensors); alpha, beta [T];
+    W active slots. rows: optional list of bank rows to carry (default all).
+    M: optional starting bank rows [N, len(rows)] (default: M0 restricted to rows),
+    updated in place. Returns q_w, q_r, v, write/read slots, weights and gaps, y, M."""
+    q_w = project(x, params["W_qw"])
+    q_r = project(x, params["W_qr"])
+    v = project(x, params["W_v"])
+    Sw, kw, _, gw = address(q_w, params["K1"], params["K2"], W)
+    Sr, kr, _, gr = address(q_r, params["K1"], params["K2"], W)
+    m0, _ = storage(params["M0"])
+    d = m0.shape[1]
+    rows = np.arange(d) if rows is None else np.asarray(rows)
+    if M is None:
+        M = np.ascontiguousarray(m0[:, rows])
+    y = scan(M, np.ascontiguousarray(v[:, rows]), alpha, beta, Sw, kw, Sr, kr)
+    return {"q_w": q_w, "q_r": q_r, "v": v, "S": Sw, "k": kw, "gap_w": gw,
+            "R": Sr, "r": kr, "gap_r": gr, "y": y, "M": M, "rows": rows}
