@@ -1,0 +1,439 @@
+#!/usr/bin/env python3
+"""Benchmark of one Sparse Delta Memory (SDM) layer forward pass on B300.
+
+Workload (N=1): prefill of 4 sequences x 4096 tokens, d = 2048, N = 480^2 slots,
+W = 64, key width 256, bf16 banks (the 1.4B-scale layer of the pages). One step is
+one pass of the whole hot path over that batch: bank initialisation from M0, the
+projections, product-key addressing, the collision codes and the recurrent scan.
+Inputs are synthetic and seeded (synth/).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--no-decode]
+
+Prints one JSON line (rank 0). `value` is tokens/s over the whole job with inputs
+resident in HBM; `e2e` is the same metric through the public one-call API with the
+inputs copied from pinned host memory and y copied back inside the timed region;
+`roofline` is the scan kernel's algorithmic HBM bytes over its event-timed duration
+against the measured copy bandwidth; `cpu_baseline` is the CPU oracle on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+WORKLOAD = "prefill-d2048-b4"
+DECODE_WORKLOAD = "decode-d2048-b64"
+METRIC = "SDM layer tokens/s (prefill, decode) on 1 B300; scan HBM GB/s vs 8 TB/s"
+ORACLE_SAMPLE_TOKENS = 512
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="sdm", choices=["sdm", "reference"])
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, x: float) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6400.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- the GPU arm
+
+def gpu_arm(args, world, rank):
+    import sparse_memory_linear_key_b300 as sdm
+    from sparse_memory_linear_key_b300 import build
+    build.build()
+    sdm.lib()
+
+    wl = synth.WORKLOADS[WORKLOAD]
+    dev = "cuda"
+    cfg = sdm.make_cfg(wl.d, wl.n, wl.dk, wl.W, wl.dtype)
+    p_cpu = synth.make_params(wl)
+    tok_cpu = synth.make_tokens(wl)
+    p = {k: v.to(dev) for k, v in p_cpu.items()}
+    x = tok_cpu["x"].to(dev)
+    alpha = tok_cpu["alpha"].to(dev)
+    beta = tok_cpu["beta"].to(dev)
+    B, T, d = wl.B, wl.T, wl.d
+    ntok = B * T
+    banks = torch.empty(B, wl.N, d, dtype=torch.bfloat16, device=dev)
+    q_w = torch.empty(ntok, wl.dk, dtype=torch.bfloat16, device=dev)
+    q_r = torch.empty_like(q_w)
+    v = torch.empty(ntok, d, dtype=torch.bfloat16, device=dev)
+    idx = torch.empty(ntok, 2, wl.W, dtype=torch.int32, device=dev)
+    wsel = torch.empty(ntok, 2, wl.W, dtype=torch.float32, device=dev)
+    y = torch.empty(ntok, d, dtype=torch.float32, device=dev)
+    ws_a = sdm.alloc_workspace(sdm.address_workspace_bytes(cfg, ntok))
+    ws_s = sdm.alloc_workspace(sdm.scan_workspace_bytes(cfg, B, T))
+    st = sdm.new_status()
+    stream = torch.cuda.current_stream()
+
+    names = ["init", "project", "address", "codes", "scan"]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+          for _ in range(args.steps)]
+
+    def step(e=None):
+        if e is not None:
+            e[0].record(stream)
+        sdm.sdm_init_bank(cfg, p["M0"], banks)
+        if e is not None:
+            e[1].record(stream)
+        sdm.sdm_project(cfg, p, x, q_w, q_r, v)
+        if e is not None:
+            e[2].record(stream)
+        sdm.sdm_address(cfg, p["K1"], p["K2"], q_w, q_r, idx, wsel, ws_a, st)
+        if e is not None:
+            e[3].record(stream)
+        sdm.sdm_scan_prepare(cfg, idx, B, T, ws_s, st)
+        if e is not None:
+            e[4].record(stream)
+        sdm.sdm_scan_run(cfg, idx, wsel, v, alpha, beta, banks, y, B, T, ws_s, st)
+        if e is not None:
+            e[5].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if sdm.read_status(st) != 0:
+        raise RuntimeError("device status %d" % sdm.read_status(st))
+
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        t0.record(stream)
+        for i in range(args.steps):
+            step(ev[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    status = sdm.read_status(st)
+    if status != 0:
+        raise RuntimeError("device status %d during the timed steps" % status)
+    elapsed_ms = t0.elapsed_time(t1)
+    elapsed_ms = max_over_ranks(world, elapsed_ms)
+    stage_ms = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev)
+                for j, n in enumerate(names)}
+    ms_per_step = elapsed_ms / args.steps
+    value = ntok * world * args.steps / (elapsed_ms / 1e3)
+
+    # roofline of the scan kernel: algorithmic bytes per launch / launch duration
+    s_bytes = 2
+    per_tok = (3 * wl.W * d * s_bytes          # write-set read + write, read-set read
+               + d * s_bytes + d * 4            # v in, y out
+               + 2 * wl.W * (4 + 4 + 2) + 8)    # slot ids, weights, codes, alpha, beta
+    scan_bytes = per_tok * ntok
+    scan_s = stage_ms["scan"] / 1e3
+    peak, peak_kind = measured_peaks()
+    achieved = scan_bytes / scan_s / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.4 TB/s",
+                "kernel": "scan_kernel<bf16,8>", "bytes_per_token": per_tok,
+                "vs_8tbs": round(achieved / 8000.0, 4),
+                "literal_2Wd_count_frac_8tbs": round(
+                    (2 * wl.W * d * s_bytes + 2 * wl.W * 8) * ntok / scan_s / 1e9 / 8000.0, 4)}
+
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; x~N(0,1), weights N(0,1/sqrt(fan_in)), M0~N(0,0.02))",
+        "config": {"workload": WORKLOAD, "B": B, "T": T, "d": d, "N": wl.N, "W": wl.W,
+                   "dk": wl.dk, "state": "bf16", "parallelism": "replicas" if world > 1 else "1gpu",
+                   "l2": "inputs larger than L2: each step writes/reads 3.8 GB of banks",
+                   "step": "bank init + projections + addressing + codes + scan"},
+        "stages_ms": {k: round(v_, 4) for k, v_ in stage_ms.items()},
+        "scan_tokens_per_s": round(ntok / scan_s, 1),
+        "roofline": roofline,
+        "clocks": clocks.summary(),
+        "gpu_launches": 5 * args.steps * 1,
+        "library_launches": {"cublas_gemm": 3 * args.steps},
+    }
+
+    # ---- e2e: the one-call public API with host buffers
+    x_h = tok_cpu["x"].pin_memory()
+    a_h = tok_cpu["alpha"].pin_memory()
+    b_h = tok_cpu["beta"].pin_memory()
+    y_h = torch.empty(B, T, d, dtype=torch.float32).pin_memory()
+    ws_p = sdm.alloc_workspace(sdm.workspace_bytes(cfg, B, T))
+    x_d = torch.empty_like(x)
+    a_d = torch.empty_like(alpha)
+    b_d = torch.empty_like(beta)
+    y_d = torch.empty(B, T, d, dtype=torch.float32, device=dev)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        a_d.copy_(a_h, non_blocking=True)
+        b_d.copy_(b_h, non_blocking=True)
+        sdm.sdm_init_bank(cfg, p["M0"], banks)
+        sdm.sdm_prefill(cfg, p, x_d, a_d, b_d, banks, y_d, ws_p, st)
+        y_h.copy_(y_d, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    n_e2e = max(3, args.steps // 5)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1))
+    if sdm.read_status(st) != 0:
+        raise RuntimeError("device status during e2e")
+    h2d = x_h.numel() * x_h.element_size() + a_h.numel() * 4 + b_h.numel() * 4
+    d2h = y_h.numel() * 4
+    res["e2e"] = {"value": round(ntok * world * n_e2e / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+                  "ms_per_step": round(e2e_ms / n_e2e, 4)}
+    del ws_p, x_d, y_d
+
+    if not args.no_decode:
+        res["decode"] = decode_arm(sdm, args, world)
+
+    del banks, q_w, q_r, v, idx, wsel, y, ws_a, ws_s
+    torch.cuda.empty_cache()
+    return res, p_cpu, tok_cpu
+
+
+def decode_arm(sdm, args, world):
+    """64 sequences, 1024 prior writes by a prefill, then `decode_steps` timed
+    sdm_decode_step calls (one token per sequence per call)."""
+    wl = synth.WORKLOADS[DECODE_WORKLOAD]
+    dev = "cuda"
+    cfg = sdm.make_cfg(wl.d, wl.n, wl.dk, wl.W, wl.dtype)
+    p = {k: v.to(dev) for k, v in synth.make_params(wl).items()}
+    tok = synth.make_tokens(wl)
+    dec = synth.make_decode_tokens(wl)
+    B = wl.B
+    banks = torch.empty(B, wl.N, wl.d, dtype=torch.bfloat16, device=dev)
+    sdm.sdm_init_bank(cfg, p["M0"], banks)
+    st = sdm.new_status()
+    ws = sdm.alloc_workspace(sdm.workspace_bytes(cfg, B, wl.T))
+    y0 = torch.empty(B, wl.T, wl.d, device=dev)
+    sdm.sdm_prefill(cfg, p, tok["x"].to(dev), tok["alpha"].to(dev), tok["beta"].to(dev), banks,
+                    y0, ws, st)
+    del ws, y0
+    wsd = sdm.alloc_workspace(sdm.workspace_bytes(cfg, B, 1))
+    xd = dec["x"].to(dev)
+    ad = dec["alpha"].to(dev)
+    bd = dec["beta"].to(dev)
+    y = torch.empty(wl.decode_steps, B, wl.d, device=dev)
+    S = wl.decode_steps
+    stream = torch.cuda.current_stream()
+    # warm-up on the first steps' inputs (state advances; timing uses all S steps)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(S):
+        sdm.sdm_decode_step(cfg, p, xd[s], ad[s], bd[s], banks, y[s], wsd, st)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(world, e0.elapsed_time(e1))
+    if sdm.read_status(st) != 0:
+        raise RuntimeError("device status during decode")
+    per_step_bytes = 3 * wl.W * wl.d * 2 * B
+    out = {"workload": DECODE_WORKLOAD, "value": round(B * S * world / (ms / 1e3), 1),
+           "unit": "tokens/s", "steps": S, "us_per_step": round(ms * 1e3 / S, 2),
+           "state_hbm_gbs": round(per_step_bytes * S / (ms / 1e3) / 1e9, 1),
+           "note": "each call = projections (cuBLAS) + addressing + codes + scan, no graph"}
+    del banks, p, xd, y
+    torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------- the CPU oracle
+
+def oracle_sample(p_cpu, tok_cpu, n_tokens):
+    """The oracle (as it stands) on sequence 0's first n_tokens of the workload, all
+    rows: projections, exhaustive addressing and the recurrence. Returns seconds."""
+    import oracle
+    wl = synth.WORKLOADS[WORKLOAD]
+    t = time.perf_counter()
+    oracle.prefill_sequence(tok_cpu["x"][0, :n_tokens], p_cpu, tok_cpu["alpha"][0, :n_tokens],
+                            tok_cpu["beta"][0, :n_tokens], wl.W)
+    return time.perf_counter() - t
+
+
+def oracle_threads():
+    v = os.environ.get("OMP_NUM_THREADS")
+    return int(v) if v else (len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+                             else os.cpu_count())
+
+
+def cpu_baseline(p_cpu, tok_cpu):
+    n = ORACLE_SAMPLE_TOKENS
+    secs = oracle_sample(p_cpu, tok_cpu, n)
+    return {"value": round(n / secs, 2), "unit": "tokens/s", "cores": oracle_threads(),
+            "kind": "oracle",
+            "sample": "sequence 0, first %d tokens of %s, all 2048 rows (fp64 C oracle: "
+                      "projections, exhaustive top-W over 230,400 slots, recurrence); %.1f s"
+                      % (n, WORKLOAD, secs)}
+
+
+def reference_arm(args, world, rank):
+    """The oracle as the reference arm: each step one bounded sample of the workload."""
+    if rank != 0:
+        return None
+    wl = synth.WORKLOADS[WORKLOAD]
+    p_cpu = synth.make_params(wl)
+    tok_cpu = synth.make_tokens(wl)
+    n = 128
+    for _ in range(min(args.warmup, 1)):
+        oracle_sample(p_cpu, tok_cpu, 16)
+    times = [oracle_sample(p_cpu, tok_cpu, n) for _ in range(args.steps if args.steps <= 3 else 3)]
+    secs = sum(times)
+    value = n * len(times) / secs
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+        "n_gpus": world, "steps": len(times), "warmup": args.warmup,
+        "ms_per_step": round(1e3 * secs / len(times), 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": WORKLOAD, "B": wl.B, "T": wl.T, "d": wl.d, "N": wl.N, "W": wl.W,
+                   "dk": wl.dk, "state": "bf16"},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": oracle_threads(),
+                         "kind": "oracle",
+                         "sample": "per step: sequence 0, first %d tokens, all rows" % n},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        res = reference_arm(args, world, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    res, p_cpu, tok_cpu = gpu_arm(args, world, rank)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(p_cpu, tok_cpu)
+        print(json.dumps(res), flush=True)
+    barrier(world)
+
+
+if __name__ == "__main__":
+    main()

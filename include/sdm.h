@@ -1,0 +1,163 @@
+/*
+ * sdm.h -- C ABI of the B300 (sm_103a) Sparse Delta Memory layer library, libsdm.so.
+ *
+ * One Sparse Delta Memory (SDM) layer keeps a memory bank M of N = n_sub^2 slot
+ * vectors of width d per sequence. Per token it (A) selects W write slots and W read
+ * slots by product keys, (W) writes the write slots with a gated delta rule and
+ * (R) returns the softmax-weighted sum of the read slots ("Sparse Delta Memory" blog
+ * post, sections "How does SDM work?" and "Write & Read: slot selection, gated update,
+ * and retrieval"; "Sparse Delta Memory: Scaling the State of Linear RNNs through
+ * Sparsity", Abstract: the bank starts from a learned initial state).
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, row-major and
+ *    contiguous, base addresses 16-byte aligned. The library allocates no device
+ *    memory; scratch comes from the caller's workspace `ws` of `ws_bytes` bytes
+ *    (see the *_workspace_bytes queries; ws must be 256-byte aligned).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *    Calls only enqueue work on it and return; they do not synchronise.
+ *  - The return value reports host-side validation and launch errors (sdm_status).
+ *    Errors found on the device (an index out of range, a bounded wait that ran
+ *    out) are written to *dev_status (a device int the caller zeroes; the first
+ *    error wins) and are read by the caller after synchronising.
+ *  - dtype SDM_BF16: x, weights, sub-keys, M0, banks, q and v are bf16; SDM_F32: all
+ *    fp32. alpha, beta, selection weights and y are always fp32, slot ids int32.
+ *  - Supported shapes: d % 16 == 0; w in {8, 16, 32, 64}; w <= n_sub <= 512;
+ *    dk even, dk/2 % 8 == 0, dk/2 <= 128. Others return SDM_EUNSUPPORTED.
+ *    sdm_init_bank and sdm_scan need only d % 16 == 0, w in {8, 16, 32, 64} and
+ *    w <= N (the recurrence does not depend on how the slots were chosen).
+ */
+#ifndef SDM_H_
+#define SDM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SDM_API __attribute__((visibility("default")))
+#else
+#define SDM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SDM_OK = 0,
+    SDM_EINVAL = -1,        /* bad argument: null pointer, misaligned, negative size */
+    SDM_EUNSUPPORTED = -2,  /* valid but outside the supported shapes above */
+    SDM_ECUDA = -3,         /* a CUDA runtime or library call failed */
+    SDM_ETIMEOUT = -4,      /* device: a bounded wait inside a kernel ran out */
+    SDM_EWORKSPACE = -5,    /* ws_bytes smaller than the matching *_workspace_bytes */
+    SDM_ERANGE = -6         /* device: a slot id outside [0, N) reached a kernel */
+} sdm_status;
+
+typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
+
+/* Layer shape. N = n_sub * n_sub slots; the same w is used for writing and reading
+ * (the pages give one active-slot count W = 64 for both). */
+typedef struct sdm_cfg {
+    int d;      /* slot width = model width */
+    int n_sub;  /* rows of each sub-key table */
+    int dk;     /* query width; halves of dk/2 are scored against K1 and K2 */
+    int w;      /* active slots per token, write and read */
+    int dtype;  /* sdm_dtype */
+} sdm_cfg;
+
+/* Layer parameters (device pointers, dtype of the cfg):
+ *   W_qw [d, dk], W_qr [d, dk], W_v [d, d], K1 [n_sub, dk/2], K2 [n_sub, dk/2]. */
+typedef struct sdm_weights {
+    const void* W_qw;
+    const void* W_qr;
+    const void* W_v;
+    const void* K1;
+    const void* K2;
+} sdm_weights;
+
+/* Human-readable name of a status code (static string). */
+SDM_API const char* sdm_status_string(int status);
+
+/* Library version, e.g. "0.1.0". */
+SDM_API const char* sdm_version(void);
+
+/* SDM_OK if the shape is supported, else SDM_EINVAL / SDM_EUNSUPPORTED. */
+SDM_API int sdm_check_cfg(const sdm_cfg* cfg);
+
+/* Workspace needed by sdm_prefill / sdm_decode_step for B sequences of T tokens
+ * (decode: T = 1), by sdm_address for ntok tokens, and by sdm_scan. */
+SDM_API size_t sdm_workspace_bytes(const sdm_cfg* cfg, int B, int T);
+SDM_API size_t sdm_address_workspace_bytes(const sdm_cfg* cfg, int64_t ntok);
+SDM_API size_t sdm_scan_workspace_bytes(const sdm_cfg* cfg, int B, int T);
+
+/* Bank initialisation from the learned initial state ("Sparse Delta Memory",
+ * Abstract: the initial state of the memory is learned and used as parametric
+ * memory): banks[b] = M0 for b < B, a bit copy.
+ *   M0 [N, d], banks [B, N, d] (slot-major: slot s of sequence b at banks + (b*N+s)*d).
+ * M0 and banks must not overlap. */
+SDM_API int sdm_init_bank(const sdm_cfg* cfg, const void* M0, void* banks, int B, void* stream);
+
+/* Projections ("Write & Read": the token embedding is projected to write keys; a
+ * separate query projection selects the read slots): for ntok tokens
+ *   q_w = x W_qw [ntok, dk], q_r = x W_qr [ntok, dk], v = x W_v [ntok, d],
+ * fp32 accumulation, rounded once (bf16 RNE in SDM_BF16). x [ntok, d]. */
+SDM_API int sdm_project(const sdm_cfg* cfg, const sdm_weights* wts, const void* x, int64_t ntok,
+                void* q_w, void* q_r, void* v, void* stream);
+
+/* Product-key addressing ("Write & Read": two sub-keys -> outer sum -> top-k, softmax
+ * weights) of ntok write queries q_w [ntok, dk] and read queries q_r [ntok, dk]:
+ *   s1 = K1 q[0:dk/2], s2 = K2 q[dk/2:dk], c_ij = s1_i + s2_j, slot i*n_sub + j;
+ *   keep the w largest c (ties: smaller slot id), weights = softmax of the kept c.
+ * Outputs, per token t and kind (0 = write, 1 = read):
+ *   idx [ntok, 2, w] int32 slot ids in ascending order, wsel [ntok, 2, w] fp32 weights.
+ * Scores are fp32 (bf16 x bf16 products, fp32 sums). */
+SDM_API int sdm_address(const sdm_cfg* cfg, const void* K1, const void* K2, const void* q_w,
+                const void* q_r, int64_t ntok, int32_t* idx, float* wsel, void* ws,
+                size_t ws_bytes, int* dev_status, void* stream);
+
+/* The recurrence ("Write & Read": selected columns are first decayed, then written
+ * with the delta rule; the output is a weighted sum of the retrieved columns) for B
+ * sequences of T tokens, in token order per sequence:
+ *   u = M_S k;  M[S_j] <- alpha M[S_j] + beta k_j (v - alpha u)  (stored once, rounded)
+ *   y = sum_j r_j M[R_j]                                          (post-write bank)
+ * idx/wsel as produced by sdm_address for the B*T tokens (token b*T+t): each set of
+ * w slot ids distinct and in ascending order. v [B*T, d], alpha, beta [B*T] fp32,
+ * banks [B, N, d] updated in place, y [B*T, d] fp32. A slot id outside [0, N) is
+ * skipped and reported as SDM_ERANGE in *dev_status. */
+SDM_API int sdm_scan(const sdm_cfg* cfg, const int32_t* idx, const float* wsel, const void* v,
+             const float* alpha, const float* beta, void* banks, float* y, int B, int T,
+             void* ws, size_t ws_bytes, int* dev_status, void* stream);
+
+/* sdm_scan in two steps, for callers that time or overlap them separately:
+ * sdm_scan_prepare computes, into ws, the collision codes of the B*T tokens' slot
+ * sets (for each slot reference, the distance to the latest earlier write of the same
+ * slot within a short window, and its position there); sdm_scan_run then runs the
+ * recurrence with those codes. The same ws (sdm_scan_workspace_bytes) and idx must be
+ * passed to both; sdm_scan == sdm_scan_prepare followed by sdm_scan_run. */
+SDM_API int sdm_scan_prepare(const sdm_cfg* cfg, const int32_t* idx, int B, int T, void* ws,
+                             size_t ws_bytes, int* dev_status, void* stream);
+SDM_API int sdm_scan_run(const sdm_cfg* cfg, const int32_t* idx, const float* wsel,
+                         const void* v, const float* alpha, const float* beta, void* banks,
+                         float* y, int B, int T, const void* ws, size_t ws_bytes,
+                         int* dev_status, void* stream);
+
+/* Whole layer over a prefill of B sequences of T tokens: sdm_project, sdm_address and
+ * sdm_scan in one call. x [B, T, d], alpha/beta [B, T], banks [B, N, d] (in place),
+ * y [B, T, d] fp32. idx_out [B, T, 2, w] / w_out [B, T, 2, w] optional (NULL = not
+ * returned). ws: sdm_workspace_bytes(cfg, B, T) bytes. */
+SDM_API int sdm_prefill(const sdm_cfg* cfg, const sdm_weights* wts, const void* x, const float* alpha,
+                const float* beta, void* banks, float* y, int B, int T, int32_t* idx_out,
+                float* w_out, void* ws, size_t ws_bytes, int* dev_status, void* stream);
+
+/* One decode step: advance B independent sequences by one token each.
+ * x [B, d], alpha/beta [B], banks [B, N, d] (in place), y [B, d] fp32.
+ * ws: sdm_workspace_bytes(cfg, B, 1) bytes. */
+SDM_API int sdm_decode_step(const sdm_cfg* cfg, const sdm_weights* wts, const void* x,
+                    const float* alpha, const float* beta, void* banks, float* y, int B,
+                    void* ws, size_t ws_bytes, int* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDM_H_ */

@@ -226,9 +226,11 @@ def prefill_sequence(x, params, alpha, beta, W, rows=None, M=None):
     Sr, kr, _, gr = address(q_r, params["K1"], params["K2"], W)
     m0, _ = storage(params["M0"])
     d = m0.shape[1]
-    rows = np.arange(d) if rows is None else np.asarray(rows)
+    all_rows = rows is None
+    rows = np.arange(d) if all_rows else np.asarray(rows)
     if M is None:
-        M = np.ascontiguousarray(m0[:, rows])
-    y = scan(M, np.ascontiguousarray(v[:, rows]), alpha, beta, Sw, kw, Sr, kr)
+        M = m0.copy() if all_rows else np.ascontiguousarray(m0[:, rows])
+    vr = v if all_rows else np.ascontiguousarray(v[:, rows])
+    y = scan(M, vr, alpha, beta, Sw, kw, Sr, kr)
     return {"q_w": q_w, "q_r": q_r, "v": v, "S": Sw, "k": kw, "gap_w": gw,
             "R": Sr, "r": kr, "gap_r": gr, "y": y, "M": M, "rows": rows}

@@ -1,0 +1,267 @@
+"""Python binding of libsdm.so, the B300 (sm_103a) Sparse Delta Memory layer library.
+
+Argument marshalling only: every function below checks that it got device tensors of
+the right dtype and shape, takes their pointers and calls the C entry point of the
+same name (include/sdm.h). All arithmetic runs in the CUDA kernels of libsdm.so; there
+is no CPU path. If libsdm.so is missing, importing the functions raises.
+
+Layouts (row-major, contiguous): x [B, T, d]; alpha, beta [B, T] fp32; banks
+[B, N, d]; y [B, T, d] fp32; idx [B*T, 2, w] int32; wsel [B*T, 2, w] fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Dict, Optional
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "lib", "libsdm.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "sdm.h")
+
+SDM_OK, SDM_EINVAL, SDM_EUNSUPPORTED, SDM_ECUDA = 0, -1, -2, -3
+SDM_ETIMEOUT, SDM_EWORKSPACE, SDM_ERANGE = -4, -5, -6
+SDM_F32, SDM_BF16 = 0, 1
+
+
+class SdmError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__("%s: %s" % (what, status_string(code) if _lib is not None else code))
+
+
+class Cfg(ctypes.Structure):
+    _fields_ = [("d", ctypes.c_int), ("n_sub", ctypes.c_int), ("dk", ctypes.c_int),
+                ("w", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+    @property
+    def N(self) -> int:
+        return self.n_sub * self.n_sub
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.bfloat16 if self.dtype == SDM_BF16 else torch.float32
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("W_qw", ctypes.c_void_p), ("W_qr", ctypes.c_void_p), ("W_v", ctypes.c_void_p),
+                ("K1", ctypes.c_void_p), ("K2", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def exported_names():
+    """Function names declared in include/sdm.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^SDM_API\s+(?:const\s+)?[a-z_0-9]+\*?\s+\**(sdm_[a-z_0-9]+)\s*\(",
+                                 text, re.M)))
+
+
+def lib():
+    """Load libsdm.so (built in-tree). Raises if it is missing: there is no fallback."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libsdm.so not found at %s; build it with "
+                              "`python -m sparse_memory_linear_key_b300.build`" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, L64, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        CP = ctypes.POINTER(Cfg)
+        WP = ctypes.POINTER(Weights)
+        sig = {
+            "sdm_status_string": ([I], ctypes.c_char_p),
+            "sdm_version": ([], ctypes.c_char_p),
+            "sdm_check_cfg": ([CP], I),
+            "sdm_workspace_bytes": ([CP, I, I], S),
+            "sdm_address_workspace_bytes": ([CP, L64], S),
+            "sdm_scan_workspace_bytes": ([CP, I, I], S),
+            "sdm_init_bank": ([CP, P, P, I, P], I),
+            "sdm_project": ([CP, WP, P, L64, P, P, P, P], I),
+            "sdm_address": ([CP, P, P, P, P, L64, P, P, P, S, P, P], I),
+            "sdm_scan": ([CP, P, P, P, P, P, P, P, I, I, P, S, P, P], I),
+            "sdm_scan_prepare": ([CP, P, I, I, P, S, P, P], I),
+            "sdm_scan_run": ([CP, P, P, P, P, P, P, P, I, I, P, S, P, P], I),
+            "sdm_prefill": ([CP, WP, P, P, P, P, P, I, I, P, P, P, S, P, P], I),
+            "sdm_decode_step": ([CP, WP, P, P, P, P, P, I, P, S, P, P], I),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().sdm_status_string(int(code)).decode()
+
+
+def version() -> str:
+    return lib().sdm_version().decode()
+
+
+def make_cfg(d: int, n_sub: int, dk: int, w: int, dtype) -> Cfg:
+    if isinstance(dtype, torch.dtype):
+        dtype = SDM_BF16 if dtype == torch.bfloat16 else SDM_F32
+    elif isinstance(dtype, str):
+        dtype = SDM_BF16 if dtype == "bf16" else SDM_F32
+    return Cfg(d, n_sub, dk, w, int(dtype))
+
+
+def check_cfg(cfg: Cfg) -> int:
+    return lib().sdm_check_cfg(ctypes.byref(cfg))
+
+
+def workspace_bytes(cfg: Cfg, B: int, T: int) -> int:
+    return int(lib().sdm_workspace_bytes(ctypes.byref(cfg), B, T))
+
+
+def address_workspace_bytes(cfg: Cfg, ntok: int) -> int:
+    return int(lib().sdm_address_workspace_bytes(ctypes.byref(cfg), ntok))
+
+
+def scan_workspace_bytes(cfg: Cfg, B: int, T: int) -> int:
+    return int(lib().sdm_scan_workspace_bytes(ctypes.byref(cfg), B, T))
+
+
+def alloc_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A byte tensor of at least nbytes, 256-byte aligned (torch allocations are)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def new_status(device=None) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def read_status(dev_status: torch.Tensor) -> int:
+    """Synchronises (reads the device int) and returns the first device error or 0."""
+    return int(dev_status.item())
+
+
+# ------------------------------------------------------------------ marshalling
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor (there is no CPU path)" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(rc: int, what: str):
+    if rc != SDM_OK:
+        raise SdmError(rc, what)
+
+
+def _weights(cfg: Cfg, p: Dict[str, torch.Tensor]) -> Weights:
+    dt = cfg.torch_dtype
+    return Weights(*[_ptr(p[k], dt, k) for k in ("W_qw", "W_qr", "W_v", "K1", "K2")])
+
+
+def sdm_init_bank(cfg: Cfg, M0: torch.Tensor, banks: torch.Tensor, stream=None) -> None:
+    B = banks.shape[0]
+    if tuple(banks.shape[1:]) != tuple(M0.shape):
+        raise ValueError("banks must be [B, N, d] with M0 [N, d]")
+    dt = cfg.torch_dtype
+    _check(lib().sdm_init_bank(ctypes.byref(cfg), _ptr(M0, dt, "M0"), _ptr(banks, dt, "banks"),
+                               B, _stream(stream)), "sdm_init_bank")
+
+
+def sdm_project(cfg: Cfg, params: Dict[str, torch.Tensor], x: torch.Tensor, q_w: torch.Tensor,
+                q_r: torch.Tensor, v: torch.Tensor, stream=None) -> None:
+    dt = cfg.torch_dtype
+    ntok = x.numel() // cfg.d
+    w = _weights(cfg, params)
+    _check(lib().sdm_project(ctypes.byref(cfg), ctypes.byref(w), _ptr(x, dt, "x"), ntok,
+                             _ptr(q_w, dt, "q_w"), _ptr(q_r, dt, "q_r"), _ptr(v, dt, "v"),
+                             _stream(stream)), "sdm_project")
+
+
+def sdm_address(cfg: Cfg, K1, K2, q_w, q_r, idx, wsel, ws, dev_status, stream=None) -> None:
+    dt = cfg.torch_dtype
+    ntok = q_w.numel() // cfg.dk
+    _check(lib().sdm_address(ctypes.byref(cfg), _ptr(K1, dt, "K1"), _ptr(K2, dt, "K2"),
+                             _ptr(q_w, dt, "q_w"), _ptr(q_r, dt, "q_r"), ntok,
+                             _ptr(idx, torch.int32, "idx"), _ptr(wsel, torch.float32, "wsel"),
+                             _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+                             _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)),
+           "sdm_address")
+
+
+def sdm_scan(cfg: Cfg, idx, wsel, v, alpha, beta, banks, y, B: int, T: int, ws, dev_status,
+             stream=None) -> None:
+    dt = cfg.torch_dtype
+    _check(lib().sdm_scan(ctypes.byref(cfg), _ptr(idx, torch.int32, "idx"),
+                          _ptr(wsel, torch.float32, "wsel"), _ptr(v, dt, "v"),
+                          _ptr(alpha, torch.float32, "alpha"), _ptr(beta, torch.float32, "beta"),
+                          _ptr(banks, dt, "banks"), _ptr(y, torch.float32, "y"), B, T,
+                          _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+                          _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)),
+           "sdm_scan")
+
+
+def sdm_scan_prepare(cfg: Cfg, idx, B: int, T: int, ws, dev_status, stream=None) -> None:
+    _check(lib().sdm_scan_prepare(ctypes.byref(cfg), _ptr(idx, torch.int32, "idx"), B, T,
+                                  _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+                                  _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)),
+           "sdm_scan_prepare")
+
+
+def sdm_scan_run(cfg: Cfg, idx, wsel, v, alpha, beta, banks, y, B: int, T: int, ws, dev_status,
+                 stream=None) -> None:
+    dt = cfg.torch_dtype
+    _check(lib().sdm_scan_run(ctypes.byref(cfg), _ptr(idx, torch.int32, "idx"),
+                              _ptr(wsel, torch.float32, "wsel"), _ptr(v, dt, "v"),
+                              _ptr(alpha, torch.float32, "alpha"),
+                              _ptr(beta, torch.float32, "beta"), _ptr(banks, dt, "banks"),
+                              _ptr(y, torch.float32, "y"), B, T, _ptr(ws, None, "ws"),
+                              ws.numel() * ws.element_size(),
+                              _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)),
+           "sdm_scan_run")
+
+
+def sdm_prefill(cfg: Cfg, params, x, alpha, beta, banks, y, ws, dev_status, idx_out=None,
+                w_out=None, stream=None) -> None:
+    dt = cfg.torch_dtype
+    B, T = x.shape[0], x.shape[1]
+    w = _weights(cfg, params)
+    _check(lib().sdm_prefill(ctypes.byref(cfg), ctypes.byref(w), _ptr(x, dt, "x"),
+                             _ptr(alpha, torch.float32, "alpha"), _ptr(beta, torch.float32, "beta"),
+                             _ptr(banks, dt, "banks"), _ptr(y, torch.float32, "y"), B, T,
+                             _ptr(idx_out, torch.int32, "idx_out"),
+                             _ptr(w_out, torch.float32, "w_out"),
+                             _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+                             _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)),
+           "sdm_prefill")
+
+
+def sdm_decode_step(cfg: Cfg, params, x, alpha, beta, banks, y, ws, dev_status,
+                    stream=None) -> None:
+    dt = cfg.torch_dtype
+    B = x.shape[0]
+    w = _weights(cfg, params)
+    _check(lib().sdm_decode_step(ctypes.byref(cfg), ctypes.byref(w), _ptr(x, dt, "x"),
+                                 _ptr(alpha, torch.float32, "alpha"),
+                                 _ptr(beta, torch.float32, "beta"), _ptr(banks, dt, "banks"),
+                                 _ptr(y, torch.float32, "y"), B, _ptr(ws, None, "ws"),
+                                 ws.numel() * ws.element_size(),
+                                 _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)),
+           "sdm_decode_step")

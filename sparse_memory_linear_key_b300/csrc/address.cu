@@ -1,0 +1,345 @@
+// address.cu -- product-key addressing of every token, run up front because it
+// depends only on the input ("Sparse Delta Memory" blog, "Write & Read": two sub-keys
+// -> outer sum -> top-k; softmax-weighted).
+//
+//   subkey_topw_kernel     s_h = K_h q_h for both halves of both queries, and the
+//                          top-W of each half, sorted (score desc, row asc).
+//   candidate_select_kernel  outer sums of the pairs of half-ranks (a, b) with
+//                          (a+1)(b+1) <= W -- the only pairs that can reach the top-W
+//                          of all n^2 sums -- their top-W, softmax, and the set in
+//                          ascending slot order.
+//   fwd_codes_kernel       for the scan: for every slot reference, the distance to the
+//                          latest earlier write of the same slot within a window and
+//                          its position there (collision forwarding).
+#include <algorithm>
+
+#include "sdm_common.cuh"
+#include "sdm_internal.h"
+
+namespace sdm {
+
+// ------------------------------------------------------------------ half top-W
+
+// Block: 8 warps; blockIdx.y = half (0: K1 on q[0:h], 1: K2 on q[h:dk]). The half's
+// sub-key table is staged transposed ([h][P], zero-padded to P = 32*E columns) in
+// shared memory; each warp then takes (token, kind) queries in turn.
+template <typename IO, int E>
+__global__ void __launch_bounds__(256) subkey_topw_kernel(
+    const IO* __restrict__ q_w, const IO* __restrict__ q_r, const IO* __restrict__ K1,
+    const IO* __restrict__ K2, int64_t ntok, int dk, int n, int W, float* __restrict__ hv,
+    int32_t* __restrict__ hi)
+{
+    constexpr int P = 32 * E;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int h = dk / 2;
+    const int half = blockIdx.y;
+    IO* KT = reinterpret_cast<IO*>(smem_raw);                     // [h][P]
+    float* qs = reinterpret_cast<float*>(smem_raw + (size_t)h * P * sizeof(IO));  // [8][h]
+    const IO* K = half ? K2 : K1;
+    for (int e = threadIdx.x; e < h * P; e += blockDim.x) {
+        const int k = e / P, r = e % P;
+        KT[e] = (r < n) ? K[(size_t)r * h + k] : IO(0.0f);
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float* qw = qs + warp * h;
+    const int64_t nq = 2 * ntok;
+    for (int64_t qi = (int64_t)blockIdx.x * 8 + warp; qi < nq; qi += (int64_t)gridDim.x * 8) {
+        const int kind = (int)(qi / ntok);
+        const int64_t tok = qi % ntok;
+        const IO* q = (kind ? q_r : q_w) + tok * dk + half * h;
+        __syncwarp();
+        for (int k = lane; k < h; k += 32)
+            qw[k] = to_f32(q[k]);
+        __syncwarp();
+        float acc[E];
+#pragma unroll
+        for (int i = 0; i < E; ++i)
+            acc[i] = 0.0f;
+        for (int k = 0; k < h; ++k) {
+            const float qk = qw[k];
+            const IO* row = KT + (size_t)k * P + lane;
+#pragma unroll
+            for (int i = 0; i < E; ++i)
+                acc[i] = fmaf(to_f32(row[32 * i]), qk, acc[i]);
+        }
+        uint64_t key[E];
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+            const int r = lane + 32 * i;
+            key[i] = (r < n) ? desc_key(acc[i], (uint32_t)r) : ~0ull;
+        }
+        warp_bitonic_sort<E>(key);
+        const size_t base = (((size_t)kind * ntok + tok) * 2 + half) * W;
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+            const int e = lane * E + i;
+            if (e < W) {
+                hv[base + e] = key_score(key[i]);
+                hi[base + e] = (int32_t)key_id(key[i]);
+            }
+        }
+    }
+}
+
+// --------------------------------------------------------- candidates + softmax
+
+// One warp per (token, kind). Candidate pairs (a, b) of half-ranks come from a table
+// built in shared memory at block start.
+template <int EC, int EW>
+__global__ void __launch_bounds__(256) candidate_select_kernel(
+    const float* __restrict__ hv, const int32_t* __restrict__ hi, int64_t ntok, int n, int W,
+    int32_t* __restrict__ idx, float* __restrict__ wsel)
+{
+    __shared__ unsigned short pairs[32 * EC];     // (a << 8) | b
+    __shared__ int npairs;
+    __shared__ float lv[8][2][64];
+    __shared__ int li[8][2][64];
+    __shared__ uint64_t sel[8][64];
+    if (threadIdx.x == 0) {
+        int c = 0;
+        for (int a = 0; a < W; ++a)
+            for (int b = 0; (a + 1) * (b + 1) <= W; ++b)
+                pairs[c++] = (unsigned short)((a << 8) | b);
+        npairs = c;
+    }
+    __syncthreads();
+    const int C = npairs;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t nq = 2 * ntok;
+    for (int64_t qi = (int64_t)blockIdx.x * 8 + warp; qi < nq; qi += (int64_t)gridDim.x * 8) {
+        const int kind = (int)(qi / ntok);
+        const int64_t tok = qi % ntok;
+        const size_t base = ((size_t)kind * ntok + tok) * 2 * W;
+        __syncwarp();
+        for (int e = lane; e < 2 * W; e += 32) {
+            lv[warp][e / W][e % W] = hv[base + e];
+            li[warp][e / W][e % W] = hi[base + e];
+        }
+        __syncwarp();
+        uint64_t key[EC];
+#pragma unroll
+        for (int i = 0; i < EC; ++i) {
+            const int c = lane * EC + i;
+            if (c < C) {
+                const int a = pairs[c] >> 8, b = pairs[c] & 0xFF;
+                const float s = lv[warp][0][a] + lv[warp][1][b];
+                const uint32_t slot = (uint32_t)li[warp][0][a] * (uint32_t)n + (uint32_t)li[warp][1][b];
+                key[i] = desc_key(s, slot);
+            } else {
+                key[i] = ~0ull;
+            }
+        }
+        warp_bitonic_sort<EC>(key);
+        // softmax over the W kept scores (elements 0..W-1); element 0 is the max
+        const float mx = __shfl_sync(0xFFFFFFFFu, key_score(key[0]), 0);
+        float ex[EC];
+        float part = 0.0f;
+#pragma unroll
+        for (int i = 0; i < EC; ++i) {
+            const int e = lane * EC + i;
+            ex[i] = (e < W) ? expf(key_score(key[i]) - mx) : 0.0f;
+            part += ex[i];
+        }
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1)
+            part += __shfl_xor_sync(0xFFFFFFFFu, part, m);
+#pragma unroll
+        for (int i = 0; i < EC; ++i) {
+            const int e = lane * EC + i;
+            if (e < W)
+                sel[warp][e] = ((uint64_t)key_id(key[i]) << 32) | __float_as_uint(ex[i] / part);
+        }
+        __syncwarp();
+        // report the set in ascending slot order, weights alongside
+        uint64_t k2[EW];
+#pragma unroll
+        for (int i = 0; i < EW; ++i) {
+            const int e = lane * EW + i;
+            k2[i] = (e < W) ? sel[warp][e] : ~0ull;
+        }
+        warp_bitonic_sort<EW>(k2);
+        const size_t ob = ((size_t)tok * 2 + kind) * W;
+#pragma unroll
+        for (int i = 0; i < EW; ++i) {
+            const int e = lane * EW + i;
+            if (e < W) {
+                idx[ob + e] = (int32_t)(k2[i] >> 32);
+                wsel[ob + e] = __uint_as_float((uint32_t)k2[i]);
+            }
+        }
+    }
+}
+
+static int candidate_count(int W)
+{
+    int c = 0;
+    for (int a = 1; a <= W; ++a)
+        c += W / a;
+    return c;
+}
+
+size_t address_ws_bytes(const sdm_cfg& c, int64_t ntok)
+{
+    // half lists: [2 kinds][ntok][2 halves][W] x (fp32 score + int32 row)
+    const size_t n = (size_t)2 * ntok * 2 * c.w;
+    return ((n * 8) + 255) / 256 * 256;
+}
+
+template <typename IO, int E>
+static cudaError_t run_topw(const sdm_cfg& c, const void* K1, const void* K2, const void* q_w,
+                            const void* q_r, int64_t ntok, float* hv, int32_t* hi,
+                            cudaStream_t s)
+{
+    const int h = c.dk / 2;
+    const size_t smem = (size_t)h * 32 * E * sizeof(IO) + 8 * h * sizeof(float);
+    auto kern = subkey_topw_kernel<IO, E>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    const int sms = num_sms_current_device();
+    int64_t blocks = (2 * ntok + 7) / 8;
+    if (blocks > (int64_t)sms * 2)
+        blocks = (int64_t)sms * 2;
+    dim3 grid((unsigned)blocks, 2);
+    kern<<<grid, 256, smem, s>>>((const IO*)q_w, (const IO*)q_r, (const IO*)K1, (const IO*)K2,
+                                 ntok, c.dk, c.n_sub, c.w, hv, hi);
+    return cudaGetLastError();
+}
+
+template <typename IO>
+static cudaError_t run_topw_e(const sdm_cfg& c, const void* K1, const void* K2, const void* q_w,
+                              const void* q_r, int64_t ntok, float* hv, int32_t* hi,
+                              cudaStream_t s)
+{
+    const int n = c.n_sub;
+    if (n <= 32) return run_topw<IO, 1>(c, K1, K2, q_w, q_r, ntok, hv, hi, s);
+    if (n <= 64) return run_topw<IO, 2>(c, K1, K2, q_w, q_r, ntok, hv, hi, s);
+    if (n <= 128) return run_topw<IO, 4>(c, K1, K2, q_w, q_r, ntok, hv, hi, s);
+    if (n <= 256) return run_topw<IO, 8>(c, K1, K2, q_w, q_r, ntok, hv, hi, s);
+    return run_topw<IO, 16>(c, K1, K2, q_w, q_r, ntok, hv, hi, s);
+}
+
+template <int EC, int EW>
+static cudaError_t run_cand(const sdm_cfg& c, int64_t ntok, const float* hv, const int32_t* hi,
+                            int32_t* idx, float* wsel, cudaStream_t s)
+{
+    const int sms = num_sms_current_device();
+    int64_t blocks = (2 * ntok + 7) / 8;
+    if (blocks > (int64_t)sms * 4)
+        blocks = (int64_t)sms * 4;
+    candidate_select_kernel<EC, EW><<<(unsigned)blocks, 256, 0, s>>>(hv, hi, ntok, c.n_sub, c.w,
+                                                                    idx, wsel);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_address(const sdm_cfg& c, const void* K1, const void* K2, const void* q_w,
+                           const void* q_r, int64_t ntok, int32_t* idx, float* wsel, void* ws,
+                           int* status, cudaStream_t s)
+{
+    (void)status;
+    if (ntok <= 0)
+        return cudaSuccess;
+    float* hv = (float*)ws;
+    int32_t* hi = (int32_t*)((char*)ws + (size_t)2 * ntok * 2 * c.w * sizeof(float));
+    cudaError_t e = (c.dtype == SDM_BF16)
+                        ? run_topw_e<bf16>(c, K1, K2, q_w, q_r, ntok, hv, hi, s)
+                        : run_topw_e<float>(c, K1, K2, q_w, q_r, ntok, hv, hi, s);
+    if (e != cudaSuccess)
+        return e;
+    const int C = candidate_count(c.w);
+    switch (c.w) {
+    case 8: return run_cand<1, 1>(c, ntok, hv, hi, idx, wsel, s);      // 20 candidates
+    case 16: return run_cand<2, 1>(c, ntok, hv, hi, idx, wsel, s);     // 50
+    case 32: return run_cand<4, 1>(c, ntok, hv, hi, idx, wsel, s);     // 119
+    case 64: return run_cand<16, 2>(c, ntok, hv, hi, idx, wsel, s);    // 280
+    default: (void)C; return cudaErrorInvalidValue;
+    }
+}
+
+// ----------------------------------------------------------- collision codes
+
+// Block: one sequence b, a run of TB tokens. A bitmap over all N slots marks the
+// slots written by the tokens of the window [t0 - kFwdWindow, t0 + TB); a reference
+// whose bit is clear has no earlier write within the window (the common case).
+// Otherwise the sorted write lists of the preceding tokens are binary-searched,
+// newest first. Write references look at tokens t-1, t-2, ...; read references
+// also at t itself (the read follows the write of the same token).
+constexpr int kCodeTB = 64;
+
+__global__ void __launch_bounds__(256) fwd_codes_kernel(const int32_t* __restrict__ idx, int T,
+                                                        int W, int N,
+                                                        uint16_t* __restrict__ codes,
+                                                        int* status)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int nwords = (N + 31) / 32;
+    uint32_t* bits = reinterpret_cast<uint32_t*>(smem_raw);
+    int32_t* lists = reinterpret_cast<int32_t*>(smem_raw + (size_t)nwords * 4);
+    const int b = blockIdx.y;
+    const int t0 = blockIdx.x * kCodeTB;
+    const int t1 = min(T, t0 + kCodeTB);
+    const int base = max(0, t0 - kFwdWindow);
+    const int nlist = t1 - base;
+    for (int i = threadIdx.x; i < nwords; i += blockDim.x)
+        bits[i] = 0u;
+    __syncthreads();
+    for (int e = threadIdx.x; e < nlist * W; e += blockDim.x) {
+        const int lt = e / W, j = e % W;
+        const int32_t s = idx[(((size_t)b * T + base + lt) * 2 + 0) * W + j];
+        lists[e] = s;
+        if (s >= 0 && s < N)
+            atomicOr(&bits[s >> 5], 1u << (s & 31));
+        else
+            report(status, SDM_ERANGE);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < (t1 - t0) * 2 * W; e += blockDim.x) {
+        const int lt = e / (2 * W);
+        const int kind = (e / W) & 1;
+        const int j = e % W;
+        const int t = t0 + lt;
+        const size_t o = (((size_t)b * T + t) * 2 + kind) * W + j;
+        const int32_t s = idx[o];
+        uint16_t code = kNoFwd;
+        if (s >= 0 && s < N && (bits[s >> 5] >> (s & 31)) & 1u) {
+            for (int dt = kind ? 0 : 1; dt <= kFwdWindow; ++dt) {
+                const int tp = t - dt;
+                if (tp < base)
+                    break;
+                const int32_t* L = lists + (tp - base) * W;
+                int lo = 0, hi = W - 1, found = -1;
+                while (lo <= hi) {
+                    const int mid = (lo + hi) >> 1;
+                    const int32_t v = L[mid];
+                    if (v == s) { found = mid; break; }
+                    if (v < s) lo = mid + 1; else hi = mid - 1;
+                }
+                if (found >= 0) {
+                    code = (uint16_t)((dt << 8) | found);
+                    break;
+                }
+            }
+        }
+        codes[o] = code;
+    }
+}
+
+cudaError_t launch_fwd_codes(const sdm_cfg& c, const int32_t* idx, int B, int T,
+                             uint16_t* codes, int* status, cudaStream_t s)
+{
+    if (B <= 0 || T <= 0)
+        return cudaSuccess;
+    const int N = c.n_sub * c.n_sub;
+    const size_t smem = (size_t)((N + 31) / 32) * 4 + (size_t)(kCodeTB + kFwdWindow) * c.w * 4;
+    cudaError_t e = cudaFuncSetAttribute(fwd_codes_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    dim3 grid((T + kCodeTB - 1) / kCodeTB, B);
+    fwd_codes_kernel<<<grid, 256, smem, s>>>(idx, T, c.w, N, codes, status);
+    return cudaGetLastError();
+}
+
+}  // namespace sdm

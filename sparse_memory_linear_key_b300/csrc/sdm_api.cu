@@ -1,0 +1,335 @@
+// sdm_api.cu -- the extern "C" entry points of libsdm.so (declared in include/sdm.h):
+// argument validation, workspace layout and the launch sequence of each operation.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "sdm_common.cuh"
+#include "sdm_internal.h"
+
+namespace sdm {
+
+int num_sms_current_device()
+{
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 148;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            v = 148;
+        cache[dev] = v;
+    }
+    return cache[dev];
+}
+
+static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Shapes the scan alone needs (the recurrence does not care how the slots were
+// chosen, so w <= n_sub is not required here): d % 16, w in {8,16,32,64}, w <= N.
+static int check_scan_cfg(const sdm_cfg* cfg)
+{
+    if (cfg == nullptr)
+        return SDM_EINVAL;
+    const sdm_cfg& c = *cfg;
+    if (c.d <= 0 || c.n_sub <= 0 || c.w <= 0 || (c.dtype != SDM_F32 && c.dtype != SDM_BF16))
+        return SDM_EINVAL;
+    if (c.d % kScanRows != 0 || (c.w != 8 && c.w != 16 && c.w != 32 && c.w != 64))
+        return SDM_EUNSUPPORTED;
+    if ((long long)c.n_sub * c.n_sub < c.w || c.n_sub > 512)
+        return SDM_EUNSUPPORTED;
+    return SDM_OK;
+}
+
+static size_t esize(const sdm_cfg& c) { return c.dtype == SDM_BF16 ? 2 : 4; }
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+static int cuda_status(cudaError_t e) { return e == cudaSuccess ? SDM_OK : SDM_ECUDA; }
+
+// Workspace layout of a prefill / decode call over ntok = B*T tokens.
+struct PrefillWs {
+    size_t q_w, q_r, v, idx, wsel, codes, addr, total;
+};
+
+static PrefillWs prefill_layout(const sdm_cfg& c, int64_t ntok)
+{
+    PrefillWs L;
+    size_t o = 0;
+    const size_t W2 = (size_t)2 * c.w;
+    L.q_w = o; o += align256((size_t)ntok * c.dk * esize(c));
+    L.q_r = o; o += align256((size_t)ntok * c.dk * esize(c));
+    L.v = o; o += align256((size_t)ntok * c.d * esize(c));
+    L.idx = o; o += align256((size_t)ntok * W2 * 4);
+    L.wsel = o; o += align256((size_t)ntok * W2 * 4);
+    L.codes = o; o += align256((size_t)ntok * W2 * 2);
+    L.addr = o; o += address_ws_bytes(c, ntok);
+    L.total = o;
+    return L;
+}
+
+}  // namespace sdm
+
+using namespace sdm;
+
+extern "C" {
+
+const char* sdm_status_string(int status)
+{
+    switch (status) {
+    case SDM_OK: return "SDM_OK";
+    case SDM_EINVAL: return "SDM_EINVAL: invalid argument";
+    case SDM_EUNSUPPORTED: return "SDM_EUNSUPPORTED: shape outside the supported set";
+    case SDM_ECUDA: return "SDM_ECUDA: CUDA runtime or library error";
+    case SDM_ETIMEOUT: return "SDM_ETIMEOUT: a bounded device wait ran out";
+    case SDM_EWORKSPACE: return "SDM_EWORKSPACE: workspace too small";
+    case SDM_ERANGE: return "SDM_ERANGE: slot id out of range on the device";
+    default: return "unknown sdm status";
+    }
+}
+
+const char* sdm_version(void) { return "0.1.0"; }
+
+int sdm_check_cfg(const sdm_cfg* cfg)
+{
+    if (cfg == nullptr)
+        return SDM_EINVAL;
+    const sdm_cfg& c = *cfg;
+    if (c.d <= 0 || c.n_sub <= 0 || c.dk <= 0 || c.w <= 0 ||
+        (c.dtype != SDM_F32 && c.dtype != SDM_BF16))
+        return SDM_EINVAL;
+    if (c.d % kScanRows != 0)
+        return SDM_EUNSUPPORTED;
+    if (c.w != 8 && c.w != 16 && c.w != 32 && c.w != 64)
+        return SDM_EUNSUPPORTED;
+    if (c.n_sub < c.w || c.n_sub > 512)
+        return SDM_EUNSUPPORTED;
+    if (c.dk % 2 != 0 || (c.dk / 2) % 8 != 0 || c.dk / 2 > 128)
+        return SDM_EUNSUPPORTED;
+    // the sub-key table of one half is staged in shared memory, padded to a power of two
+    int P = 32;
+    while (P < c.n_sub)
+        P *= 2;
+    const size_t smem = (size_t)(c.dk / 2) * P * esize(c) + 8 * (c.dk / 2) * 4;
+    if (smem > 200 * 1024)
+        return SDM_EUNSUPPORTED;
+    return SDM_OK;
+}
+
+size_t sdm_address_workspace_bytes(const sdm_cfg* cfg, int64_t ntok)
+{
+    if (sdm_check_cfg(cfg) != SDM_OK || ntok < 0)
+        return 0;
+    return address_ws_bytes(*cfg, ntok);
+}
+
+size_t sdm_scan_workspace_bytes(const sdm_cfg* cfg, int B, int T)
+{
+    if (check_scan_cfg(cfg) != SDM_OK || B < 0 || T < 0)
+        return 0;
+    return align256((size_t)B * T * 2 * cfg->w * 2);
+}
+
+size_t sdm_workspace_bytes(const sdm_cfg* cfg, int B, int T)
+{
+    if (sdm_check_cfg(cfg) != SDM_OK || B < 0 || T < 0)
+        return 0;
+    return prefill_layout(*cfg, (int64_t)B * T).total;
+}
+
+int sdm_init_bank(const sdm_cfg* cfg, const void* M0, void* banks, int B, void* stream)
+{
+    int rc = check_scan_cfg(cfg);
+    if (rc != SDM_OK)
+        return rc;
+    if (B < 0 || (B > 0 && (M0 == nullptr || banks == nullptr)) || !aligned16(M0) ||
+        !aligned16(banks))
+        return SDM_EINVAL;
+    const size_t N = (size_t)cfg->n_sub * cfg->n_sub;
+    const size_t bytes = N * cfg->d * esize(*cfg);
+    const char* a = (const char*)M0;
+    const char* b = (const char*)banks;
+    if (B > 0 && a < b + bytes * B && b < a + bytes)
+        return SDM_EINVAL;  // overlap
+    return cuda_status(launch_bank_init(M0, banks, bytes, B, (cudaStream_t)stream));
+}
+
+int sdm_project(const sdm_cfg* cfg, const sdm_weights* w, const void* x, int64_t ntok,
+                void* q_w, void* q_r, void* v, void* stream)
+{
+    int rc = sdm_check_cfg(cfg);
+    if (rc != SDM_OK)
+        return rc;
+    if (w == nullptr || ntok < 0)
+        return SDM_EINVAL;
+    if (ntok == 0)
+        return SDM_OK;
+    const void* ptrs[] = {x, q_w, q_r, v, w->W_qw, w->W_qr, w->W_v};
+    for (const void* p : ptrs)
+        if (p == nullptr || !aligned16(p))
+            return SDM_EINVAL;
+    return launch_project(*cfg, *w, x, ntok, q_w, q_r, v, (cudaStream_t)stream);
+}
+
+int sdm_address(const sdm_cfg* cfg, const void* K1, const void* K2, const void* q_w,
+                const void* q_r, int64_t ntok, int32_t* idx, float* wsel, void* ws,
+                size_t ws_bytes, int* dev_status, void* stream)
+{
+    int rc = sdm_check_cfg(cfg);
+    if (rc != SDM_OK)
+        return rc;
+    if (ntok < 0)
+        return SDM_EINVAL;
+    if (ntok == 0)
+        return SDM_OK;
+    const void* ptrs[] = {K1, K2, q_w, q_r, idx, wsel, ws};
+    for (const void* p : ptrs)
+        if (p == nullptr || !aligned16(p))
+            return SDM_EINVAL;
+    if (((uintptr_t)ws & 255u) != 0)
+        return SDM_EINVAL;
+    if (ws_bytes < address_ws_bytes(*cfg, ntok))
+        return SDM_EWORKSPACE;
+    return cuda_status(launch_address(*cfg, K1, K2, q_w, q_r, ntok, idx, wsel, ws, dev_status,
+                                      (cudaStream_t)stream));
+}
+
+static int scan_impl(const sdm_cfg& c, const int32_t* idx, const float* wsel, const void* v,
+                     const float* alpha, const float* beta, void* banks, float* y, int B, int T,
+                     uint16_t* codes, int* dev_status, cudaStream_t s)
+{
+    cudaError_t e = launch_fwd_codes(c, idx, B, T, codes, dev_status, s);
+    if (e != cudaSuccess)
+        return SDM_ECUDA;
+    ScanLaunch L = choose_scan_launch(B, T, c.d, num_sms_current_device());
+    e = launch_scan(c, idx, wsel, codes, v, alpha, beta, banks, y, B, T, L, dev_status, s);
+    return cuda_status(e);
+}
+
+int sdm_scan_prepare(const sdm_cfg* cfg, const int32_t* idx, int B, int T, void* ws,
+                     size_t ws_bytes, int* dev_status, void* stream)
+{
+    int rc = check_scan_cfg(cfg);
+    if (rc != SDM_OK)
+        return rc;
+    if (B < 0 || T < 0)
+        return SDM_EINVAL;
+    if (B == 0 || T == 0)
+        return SDM_OK;
+    if (idx == nullptr || ws == nullptr || !aligned16(idx) || ((uintptr_t)ws & 255u) != 0)
+        return SDM_EINVAL;
+    if (ws_bytes < sdm_scan_workspace_bytes(cfg, B, T))
+        return SDM_EWORKSPACE;
+    return cuda_status(launch_fwd_codes(*cfg, idx, B, T, (uint16_t*)ws, dev_status,
+                                       (cudaStream_t)stream));
+}
+
+int sdm_scan_run(const sdm_cfg* cfg, const int32_t* idx, const float* wsel, const void* v,
+                 const float* alpha, const float* beta, void* banks, float* y, int B, int T,
+                 const void* ws, size_t ws_bytes, int* dev_status, void* stream)
+{
+    int rc = check_scan_cfg(cfg);
+    if (rc != SDM_OK)
+        return rc;
+    if (B < 0 || T < 0)
+        return SDM_EINVAL;
+    if (B == 0 || T == 0)
+        return SDM_OK;
+    const void* ptrs[] = {idx, wsel, v, alpha, beta, banks, y, ws, dev_status};
+    for (const void* p : ptrs)
+        if (p == nullptr)
+            return SDM_EINVAL;
+    const void* al[] = {idx, wsel, v, banks, y};
+    for (const void* p : al)
+        if (!aligned16(p))
+            return SDM_EINVAL;
+    if (((uintptr_t)ws & 255u) != 0)
+        return SDM_EINVAL;
+    if (ws_bytes < sdm_scan_workspace_bytes(cfg, B, T))
+        return SDM_EWORKSPACE;
+    ScanLaunch L = choose_scan_launch(B, T, cfg->d, num_sms_current_device());
+    return cuda_status(launch_scan(*cfg, idx, wsel, (const uint16_t*)ws, v, alpha, beta, banks,
+                                   y, B, T, L, dev_status, (cudaStream_t)stream));
+}
+
+int sdm_scan(const sdm_cfg* cfg, const int32_t* idx, const float* wsel, const void* v,
+             const float* alpha, const float* beta, void* banks, float* y, int B, int T,
+             void* ws, size_t ws_bytes, int* dev_status, void* stream)
+{
+    int rc = check_scan_cfg(cfg);
+    if (rc != SDM_OK)
+        return rc;
+    if (B < 0 || T < 0)
+        return SDM_EINVAL;
+    if (B == 0 || T == 0)
+        return SDM_OK;
+    const void* ptrs[] = {idx, wsel, v, alpha, beta, banks, y, ws, dev_status};
+    for (const void* p : ptrs)
+        if (p == nullptr)
+            return SDM_EINVAL;
+    const void* al[] = {idx, wsel, v, banks, y};
+    for (const void* p : al)
+        if (!aligned16(p))
+            return SDM_EINVAL;
+    if (((uintptr_t)ws & 255u) != 0)
+        return SDM_EINVAL;
+    if (ws_bytes < sdm_scan_workspace_bytes(cfg, B, T))
+        return SDM_EWORKSPACE;
+    return scan_impl(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, (uint16_t*)ws, dev_status,
+                     (cudaStream_t)stream);
+}
+
+int sdm_prefill(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const float* alpha,
+                const float* beta, void* banks, float* y, int B, int T, int32_t* idx_out,
+                float* w_out, void* ws, size_t ws_bytes, int* dev_status, void* stream)
+{
+    int rc = sdm_check_cfg(cfg);
+    if (rc != SDM_OK)
+        return rc;
+    if (w == nullptr || B < 0 || T < 0)
+        return SDM_EINVAL;
+    if (B == 0 || T == 0)
+        return SDM_OK;
+    const void* ptrs[] = {x, alpha, beta, banks, y, ws, dev_status, w->K1, w->K2};
+    for (const void* p : ptrs)
+        if (p == nullptr)
+            return SDM_EINVAL;
+    const void* al[] = {x, banks, y, w->K1, w->K2, idx_out, w_out};
+    for (const void* p : al)
+        if (!aligned16(p))
+            return SDM_EINVAL;
+    if (((uintptr_t)ws & 255u) != 0)
+        return SDM_EINVAL;
+    const int64_t ntok = (int64_t)B * T;
+    const PrefillWs L = prefill_layout(*cfg, ntok);
+    if (ws_bytes < L.total)
+        return SDM_EWORKSPACE;
+    char* base = (char*)ws;
+    void* q_w = base + L.q_w;
+    void* q_r = base + L.q_r;
+    void* v = base + L.v;
+    int32_t* idx = idx_out ? idx_out : (int32_t*)(base + L.idx);
+    float* wsel = w_out ? w_out : (float*)(base + L.wsel);
+    uint16_t* codes = (uint16_t*)(base + L.codes);
+    cudaStream_t s = (cudaStream_t)stream;
+    rc = launch_project(*cfg, *w, x, ntok, q_w, q_r, v, s);
+    if (rc != SDM_OK)
+        return rc;
+    if (launch_address(*cfg, w->K1, w->K2, q_w, q_r, ntok, idx, wsel, base + L.addr, dev_status,
+                       s) != cudaSuccess)
+        return SDM_ECUDA;
+    return scan_impl(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, codes, dev_status, s);
+}
+
+int sdm_decode_step(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const float* alpha,
+                    const float* beta, void* banks, float* y, int B, void* ws, size_t ws_bytes,
+                    int* dev_status, void* stream)
+{
+    return sdm_prefill(cfg, w, x, alpha, beta, banks, y, B, 1, nullptr, nullptr, ws, ws_bytes,
+                       dev_status, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,185 @@
+// sdm_common.cuh -- device-side helpers shared by the SDM kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sdm.h"
+
+namespace sdm {
+
+using bf16 = __nv_bfloat16;
+
+// Upper bound for every spin-wait inside a kernel, in SM clock cycles (about one
+// second at 2 GHz). A wait that runs out records SDM_ETIMEOUT and the warp leaves.
+constexpr long long kSpinLimitCycles = 2000000000LL;
+
+__device__ __forceinline__ void report(int* status, int code)
+{
+    if (status != nullptr)
+        atomicCAS(status, 0, code);
+}
+
+// ------------------------------------------------------------ shared-memory flags
+
+__device__ __forceinline__ int ld_acquire_cta(const int* p)
+{
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];"
+                 : "=r"(v)
+                 : "r"((uint32_t)__cvta_generic_to_shared(p))
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_cta(int* p, int v)
+{
+    asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(p)),
+                 "r"(v)
+                 : "memory");
+}
+
+// Spin until *flag >= target (acquire). Returns false if the wait ran out or another
+// warp of the block raised *abort; then the caller must leave.
+__device__ __forceinline__ bool wait_geq(const int* flag, int target, const int* abort,
+                                         int* status)
+{
+    if (ld_acquire_cta(flag) >= target)
+        return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (ld_acquire_cta(flag) >= target)
+            return true;
+        if (*(volatile const int*)abort)
+            return false;
+        if (clock64() - t0 > kSpinLimitCycles) {
+            report(status, SDM_ETIMEOUT);
+            *(volatile int*)abort = 1;
+            return false;
+        }
+    }
+}
+
+// ------------------------------------------------------- 4-row vectors of state
+
+// Four consecutive rows of one slot vector, in the storage type.
+template <typename S>
+struct Row4;
+
+template <>
+struct Row4<float> {
+    using V = float4;
+    static __device__ __forceinline__ V load_cg(const float* p) { return __ldcg((const float4*)p); }
+    static __device__ __forceinline__ void store_cg(float* p, V v) { __stcg((float4*)p, v); }
+    static __device__ __forceinline__ void to_f32(V v, float f[4])
+    {
+        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+    }
+    static __device__ __forceinline__ V from_f32(const float f[4])
+    {
+        return make_float4(f[0], f[1], f[2], f[3]);
+    }
+    static __device__ __forceinline__ V zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+};
+
+template <>
+struct Row4<bf16> {
+    using V = uint2;  // two packed bf16x2 words
+    static __device__ __forceinline__ V load_cg(const bf16* p) { return __ldcg((const uint2*)p); }
+    static __device__ __forceinline__ void store_cg(bf16* p, V v) { __stcg((uint2*)p, v); }
+    static __device__ __forceinline__ void to_f32(V v, float f[4])
+    {
+        f[0] = __uint_as_float(v.x << 16);
+        f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+        f[2] = __uint_as_float(v.y << 16);
+        f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+    }
+    // round-to-nearest-even, once per value
+    static __device__ __forceinline__ V from_f32(const float f[4])
+    {
+        __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]);
+        __nv_bfloat162 b = __floats2bfloat162_rn(f[2], f[3]);
+        V v;
+        v.x = *reinterpret_cast<uint32_t*>(&a);
+        v.y = *reinterpret_cast<uint32_t*>(&b);
+        return v;
+    }
+    static __device__ __forceinline__ V zero() { return make_uint2(0u, 0u); }
+};
+
+// scalar load of the I/O type as fp32
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(bf16 x) { return __bfloat162float(x); }
+
+// ------------------------------------------------------- ordered sort keys
+
+// Monotone map of a float to uint32 (larger float -> larger key); -0 folds to +0.
+__device__ __forceinline__ uint32_t float_order_bits(float f)
+{
+    uint32_t u = __float_as_uint(f + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float float_from_order_bits(uint32_t o)
+{
+    uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+    return __uint_as_float(u);
+}
+
+// 64-bit key, ascending = larger score first, then smaller id.
+__device__ __forceinline__ uint64_t desc_key(float score, uint32_t id)
+{
+    return ((uint64_t)(~float_order_bits(score)) << 32) | id;
+}
+
+__device__ __forceinline__ float key_score(uint64_t k)
+{
+    return float_from_order_bits(~(uint32_t)(k >> 32));
+}
+
+__device__ __forceinline__ uint32_t key_id(uint64_t k) { return (uint32_t)k; }
+
+// Bitonic sort, ascending, of 32*E 64-bit keys held lane-major by one warp (lane l
+// holds elements l*E .. l*E+E-1 in k[0..E-1]). E is a power of two.
+template <int E>
+__device__ __forceinline__ void warp_bitonic_sort(uint64_t (&k)[E])
+{
+    const int lane = threadIdx.x & 31;
+    constexpr int P = 32 * E;
+#pragma unroll
+    for (int size = 2; size <= P; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            if (stride < E) {
+#pragma unroll
+                for (int i = 0; i < E; ++i) {
+                    const int j = i ^ stride;
+                    if (j > i) {
+                        const int e = lane * E + i;
+                        const bool up = (e & size) == 0;
+                        uint64_t a = k[i], b = k[j];
+                        const bool swap = up ? (a > b) : (a < b);
+                        k[i] = swap ? b : a;
+                        k[j] = swap ? a : b;
+                    }
+                }
+            } else {
+                const int lm = stride / E;
+#pragma unroll
+                for (int i = 0; i < E; ++i) {
+                    const int e = lane * E + i;
+                    const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, k[i], lm);
+                    const bool up = (e & size) == 0;
+                    const bool lower = (e & stride) == 0;
+                    const uint64_t mn = k[i] < other ? k[i] : other;
+                    const uint64_t mx = k[i] < other ? other : k[i];
+                    k[i] = (up == lower) ? mn : mx;
+                }
+            }
+        }
+    }
+}
+
+}  // namespace sdm

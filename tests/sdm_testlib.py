@@ -1,0 +1,179 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C-ABI binding
+on seeded inputs, run the oracle on the same input bits, and apply the parity
+criteria of the specification (exact slot sets except near-ties; max-abs 1e-4 for
+fp32 state; per-vector relative 2e-2 for bf16 state)."""
+from __future__ import annotations
+
+import math
+from typing import Dict, Optional
+
+import numpy as np
+import torch
+
+import oracle
+import sparse_memory_linear_key_b300 as sdm
+import synth
+
+NEAR_TIE = 1e-5          # oracle fp64 gap below which a slot-set mismatch is excused
+F32_ATOL = 1e-4          # fp32 state: max-abs on y and bank
+BF16_REL = 2e-2          # bf16 state: per-vector max|a-b| / max|b|
+WEIGHT_ATOL = 1e-5       # selection weights where the sets agree
+
+
+def cfg_of(wl: synth.Workload):
+    return sdm.make_cfg(wl.d, wl.n, wl.dk, wl.W, wl.dtype)
+
+
+def to_dev(d: Dict[str, torch.Tensor], device="cuda") -> Dict[str, torch.Tensor]:
+    return {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+def run_staged(wl: synth.Workload, params: Dict[str, torch.Tensor], tok: Dict[str, torch.Tensor],
+               pool=None, pattern=None, query_hook=None) -> Dict[str, torch.Tensor]:
+    """Whole layer on the GPU through the staged entry points (project, optional query
+    substitution, address, init_bank, scan). Inputs are CPU tensors; returns device
+    tensors and the device status."""
+    cfg = cfg_of(wl)
+    dev = "cuda"
+    p = to_dev(params)
+    x = tok["x"].to(dev)
+    alpha = tok["alpha"].to(dev).contiguous()
+    beta = tok["beta"].to(dev).contiguous()
+    B, T = x.shape[0], x.shape[1]
+    ntok = B * T
+    dt = wl.torch_dtype
+    q_w = torch.empty(ntok, wl.dk, dtype=dt, device=dev)
+    q_r = torch.empty_like(q_w)
+    v = torch.empty(ntok, wl.d, dtype=dt, device=dev)
+    sdm.sdm_project(cfg, p, x, q_w, q_r, v)
+    if pool is not None or pattern is not None:
+        synth.inject_queries(wl, q_w.view(B, T, -1), q_r.view(B, T, -1), v.view(B, T, -1),
+                             pool=pool, pattern=pattern)
+    if query_hook is not None:
+        query_hook(q_w, q_r, v)
+    idx = torch.empty(ntok, 2, wl.W, dtype=torch.int32, device=dev)
+    wsel = torch.empty(ntok, 2, wl.W, dtype=torch.float32, device=dev)
+    st = sdm.new_status()
+    ws = sdm.alloc_workspace(sdm.address_workspace_bytes(cfg, ntok))
+    sdm.sdm_address(cfg, p["K1"], p["K2"], q_w, q_r, idx, wsel, ws, st)
+    del ws
+    banks = torch.empty(B, wl.N, wl.d, dtype=dt, device=dev)
+    sdm.sdm_init_bank(cfg, p["M0"], banks)
+    y = torch.empty(ntok, wl.d, dtype=torch.float32, device=dev)
+    ws = sdm.alloc_workspace(sdm.scan_workspace_bytes(cfg, B, T))
+    sdm.sdm_scan(cfg, idx, wsel, v, alpha, beta, banks, y, B, T, ws, st)
+    torch.cuda.synchronize()
+    return {"q_w": q_w, "q_r": q_r, "v": v, "idx": idx, "wsel": wsel, "banks": banks, "y": y,
+            "status": int(st.item()), "alpha": alpha, "beta": beta}
+
+
+def run_scan_only(cfg, M0: torch.Tensor, idx, wsel, v, alpha, beta, B, T):
+    """sdm_init_bank + sdm_scan on given device tensors; returns (banks, y, status)."""
+    dev = "cuda"
+    banks = torch.empty((B,) + tuple(M0.shape), dtype=M0.dtype, device=dev)
+    sdm.sdm_init_bank(cfg, M0.to(dev), banks)
+    y = torch.empty(B * T, cfg.d, dtype=torch.float32, device=dev)
+    st = sdm.new_status()
+    ws = sdm.alloc_workspace(sdm.scan_workspace_bytes(cfg, B, T))
+    sdm.sdm_scan(cfg, idx.to(dev).contiguous(), wsel.to(dev).contiguous(), v.to(dev).contiguous(),
+                 alpha.to(dev).contiguous(), beta.to(dev).contiguous(), banks, y, B, T, ws, st)
+    torch.cuda.synchronize()
+    return banks, y, int(st.item())
+
+
+# ------------------------------------------------------------------ comparisons
+
+def projection_ok(got: np.ndarray, ref: np.ndarray, x: np.ndarray, Wm: np.ndarray) -> bool:
+    """bf16 projections: the CUDA path rounds an fp32-accumulated sum to bf16, the oracle
+    rounds the fp64 sum. They may differ by one bf16 ulp of the result (the two
+    roundings fall on either side of a rounding boundary) plus the error of fp32
+    accumulation of K products, bounded by K * 2^-24 * sum_k |x_k W_kc|. Also at least
+    99% of the values must agree exactly."""
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 1e-38))) - 7)
+    acc = np.abs(x) @ np.abs(Wm) * (x.shape[-1] * 2.0 ** -24)
+    ok = np.all(np.abs(got - ref) <= ulp + acc)
+    return bool(ok) and float(np.mean(got == ref)) > 0.99
+
+
+def set_parity(gpu_idx: np.ndarray, orc_slots: np.ndarray, orc_gaps: np.ndarray):
+    """Compare slot SETS row by row. Returns (n_mismatch, n_excused, unexcused rows)."""
+    g = np.sort(gpu_idx.reshape(-1, gpu_idx.shape[-1]), axis=1)
+    o = np.sort(orc_slots.reshape(-1, orc_slots.shape[-1]), axis=1)
+    gaps = orc_gaps.reshape(-1)
+    bad = np.nonzero(np.any(g != o, axis=1))[0]
+    excused = bad[gaps[bad] < NEAR_TIE]
+    unexcused = bad[gaps[bad] >= NEAR_TIE]
+    return len(bad), len(excused), unexcused
+
+
+def weights_by_slot(idx_row: np.ndarray, w_row: np.ndarray) -> Dict[int, float]:
+    return {int(s): float(w) for s, w in zip(idx_row, w_row)}
+
+
+def max_weight_err(gpu_idx, gpu_w, orc_slots, orc_w, rows):
+    err = 0.0
+    for i in rows:
+        a = weights_by_slot(gpu_idx[i], gpu_w[i])
+        b = weights_by_slot(orc_slots[i], orc_w[i])
+        if set(a) != set(b):
+            continue
+        err = max(err, max(abs(a[s] - b[s]) for s in a))
+    return err
+
+
+def per_vector_rel(a: np.ndarray, b: np.ndarray) -> float:
+    """max over vectors (last axis) of max_i |a_i - b_i| / max_i |b_i|."""
+    a = a.reshape(-1, a.shape[-1]).astype(np.float64)
+    b = b.reshape(-1, b.shape[-1]).astype(np.float64)
+    den = np.maximum(np.abs(b).max(axis=1), 1e-30)
+    return float((np.abs(a - b).max(axis=1) / den).max())
+
+
+def state_ok(dtype: str, gpu: np.ndarray, ref: np.ndarray):
+    """(ok, measure): fp32 max-abs <= 1e-4, bf16 per-vector relative <= 2e-2."""
+    if dtype == "f32":
+        m = float(np.abs(gpu.astype(np.float64) - ref.astype(np.float64)).max())
+        return m <= F32_ATOL, m
+    m = per_vector_rel(gpu, ref)
+    return m <= BF16_REL, m
+
+
+def bank_rows_cpu(banks: torch.Tensor, b: int, rows) -> np.ndarray:
+    """Selected rows of every slot of bank b as fp64 [N, len(rows)]."""
+    sel = banks[b][:, torch.as_tensor(rows, device=banks.device)].cpu()
+    return oracle.to_f64(sel)
+
+
+def oracle_scan_rows(wl: synth.Workload, M0: torch.Tensor, out: Dict[str, torch.Tensor], b: int,
+                     rows, T: Optional[int] = None):
+    """The oracle's recurrence for sequence b on bank rows `rows`, teacher-forced with
+    the CUDA path's addressing (idx, wsel) and value bits (v). Returns (y [T, R], M)."""
+    T = T or wl.T
+    rows = np.asarray(rows)
+    m0, _ = oracle.storage(M0)
+    M = np.ascontiguousarray(m0[:, rows])
+    lo, hi = b * T, (b + 1) * T
+    idx = out["idx"][lo:hi].cpu().numpy()
+    wsel = out["wsel"][lo:hi].cpu().numpy().astype(np.float64)
+    vv = out["v"][lo:hi][:, torch.as_tensor(rows, device=out["v"].device)].cpu()
+    va, _ = oracle.storage(vv)
+    al = out["alpha"].reshape(-1)[lo:hi].cpu().numpy().astype(np.float64)
+    be = out["beta"].reshape(-1)[lo:hi].cpu().numpy().astype(np.float64)
+    y = oracle.scan(M, np.ascontiguousarray(va), al, be, idx[:, 0], wsel[:, 0], idx[:, 1],
+                    wsel[:, 1])
+    return y, M
+
+
+def sample_rows(d: int, k: int, seed: int = 0) -> np.ndarray:
+    """k rows spread over the machines (16-row slices) and lanes, plus both ends."""
+    rng = np.random.default_rng(seed)
+    r = set([0, d - 1])
+    while len(r) < min(k, d):
+        r.add(int(rng.integers(0, d)))
+    return np.array(sorted(r))
+
+
+def cos(a, b) -> float:
+    a = np.asarray(a, dtype=np.float64).ravel()
+    b = np.asarray(b, dtype=np.float64).ravel()
+    return float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b) + 1e-30))

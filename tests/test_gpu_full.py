@@ -1,0 +1,177 @@
+"""GPU parity at the full sizes of the five workloads, in the launch configuration the
+benchmark times. The oracle checks what it can compute in seconds:
+
+- projections on sampled tokens;
+- addressing on sampled tokens (oracle scoring the CUDA path's own q bits), exact
+  slot sets except counted near-ties;
+- the recurrence on sampled bank rows for the whole sequence (rows evolve
+  independently, so a row subset is exact), teacher-forced with the CUDA path's
+  addressing: y and the final bank on those rows;
+- the workload structure: pool queries give identical slot sets, the inserted pattern
+  is read back from exactly the slots it was written to.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_memory_linear_key_b300 as sdm
+import synth
+from tests import sdm_testlib as tl
+
+pytestmark = pytest.mark.gpu
+
+N_TOK_SAMPLE = 256
+N_ROWS = 8
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    from sparse_memory_linear_key_b300 import build
+    build.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _check_projection(wl, p, tok, out, toks):
+    x = tok["x"].reshape(-1, wl.d)[toks]
+    for key, w in (("q_w", "W_qw"), ("q_r", "W_qr"), ("v", "W_v")):
+        ref = oracle.to_f64(oracle.project(x, p[w]))
+        got = oracle.to_f64(out[key][torch.as_tensor(toks, device="cuda")].cpu())
+        assert tl.projection_ok(got, ref, oracle.to_f64(x), oracle.to_f64(p[w])), key
+
+
+def _check_address(wl, p, out, toks):
+    idx = out["idx"][torch.as_tensor(toks, device="cuda")].cpu().numpy()
+    wsel = out["wsel"][torch.as_tensor(toks, device="cuda")].cpu().numpy()
+    excused = 0
+    for kind, key in ((0, "q_w"), (1, "q_r")):
+        q = out[key][torch.as_tensor(toks, device="cuda")].cpu()
+        S, k, _, gaps = oracle.address(q, p["K1"], p["K2"], wl.W)
+        n_bad, n_exc, unexc = tl.set_parity(idx[:, kind], S, gaps)
+        assert len(unexc) == 0, (kind, n_bad, n_exc)
+        excused += n_exc
+        assert tl.max_weight_err(idx[:, kind], wsel[:, kind], S, k, range(len(S))) <= tl.WEIGHT_ATOL
+    return excused
+
+
+def _check_scan(wl, p, out, b, rows, T=None):
+    T = T or wl.T
+    yr, M = tl.oracle_scan_rows(wl, p["M0"], out, b, rows, T=T)
+    yg = out["y"][b * T:(b + 1) * T][:, torch.as_tensor(rows, device="cuda")].cpu().numpy()
+    ok, m = tl.state_ok(wl.dtype, yg, yr)
+    assert ok, ("y", b, m)
+    ok, mb = tl.state_ok(wl.dtype, tl.bank_rows_cpu(out["banks"], b, rows), oracle.to_f64(M))
+    assert ok, ("bank", b, mb)
+    return m, mb
+
+
+def _run(name):
+    wl = synth.WORKLOADS[name]
+    p = synth.make_params(wl)
+    tok = synth.make_tokens(wl)
+    pool = synth.make_pool(wl)
+    pattern = synth.make_pattern(wl)
+    out = tl.run_staged(wl, p, tok, pool=pool, pattern=pattern)
+    assert out["status"] == 0
+    return wl, p, tok, pool, pattern, out
+
+
+@pytest.mark.parametrize("name", ["prefill-d2048-b4", "prefill-d3840-pool", "long-131k"])
+def test_full_prefill_workload(name):
+    wl, p, tok, pool, pattern, out = _run(name)
+    rng = np.random.default_rng(1)
+    ntok = wl.B * wl.T
+    toks = np.sort(rng.choice(ntok, N_TOK_SAMPLE, replace=False))
+    if pattern is not None:
+        L = wl.pattern_len
+        toks = np.unique(np.concatenate([toks, np.arange(wl.pattern_write_at, wl.pattern_write_at + L),
+                                         np.arange(wl.pattern_read_at, wl.pattern_read_at + L)]))
+    # projections: tokens whose queries were substituted are not projections
+    plain = toks
+    if pool is not None:
+        plain = toks[~pool["mask"].reshape(-1).numpy()[toks]]
+    if pattern is not None:
+        plain = plain[(plain < wl.pattern_write_at) | (plain >= wl.pattern_write_at + wl.pattern_len)]
+        plain = plain[(plain < wl.pattern_read_at) | (plain >= wl.pattern_read_at + wl.pattern_len)]
+    _check_projection(wl, p, tok, out, plain[:64])
+    _check_address(wl, p, out, toks)
+    rows = tl.sample_rows(wl.d, N_ROWS, seed=2)
+    for b in range(wl.B):
+        _check_scan(wl, p, out, b, rows)
+    idx = out["idx"].cpu().numpy()
+    if pool is not None:
+        # tokens that share a pool query share their slot set exactly
+        m = pool["mask"].reshape(-1).numpy()
+        pw = pool["pick_w"].reshape(-1).numpy()
+        for vec in range(4):
+            sel = np.nonzero(m & (pw == vec))[0]
+            assert len(sel) > 1
+            assert (idx[sel, 0] == idx[sel[0], 0]).all()
+    if pattern is not None:
+        L, wa, ra = wl.pattern_len, wl.pattern_write_at, wl.pattern_read_at
+        for i in range(L):
+            assert np.array_equal(idx[ra + i, 1], idx[wa + i, 0])
+
+
+def test_full_decode_workload():
+    """64 sequences: 1024 prior writes by a prefill, then 512 sdm_decode_step calls.
+    Oracle on sequences {0, 17, 42, 63} and sampled rows, teacher-forced with the
+    addressing that the same kernels give for the same inputs."""
+    wl = synth.WORKLOADS["decode-d2048-b64"]
+    cfg = tl.cfg_of(wl)
+    p = synth.make_params(wl)
+    tok = synth.make_tokens(wl)          # the 1024 prior tokens
+    dec = synth.make_decode_tokens(wl)   # [512, 64, d]
+    pd = tl.to_dev(p)
+    dev = "cuda"
+    B, T, S = wl.B, wl.T, wl.decode_steps
+    banks = torch.empty(B, wl.N, wl.d, dtype=torch.bfloat16, device=dev)
+    sdm.sdm_init_bank(cfg, pd["M0"], banks)
+    st = sdm.new_status()
+    ws = sdm.alloc_workspace(sdm.workspace_bytes(cfg, B, T))
+    y0 = torch.empty(B, T, wl.d, device=dev)
+    idx0 = torch.empty(B * T, 2, wl.W, dtype=torch.int32, device=dev)
+    w0 = torch.empty(B * T, 2, wl.W, device=dev)
+    x0 = tok["x"].to(dev)
+    sdm.sdm_prefill(cfg, pd, x0, tok["alpha"].to(dev), tok["beta"].to(dev), banks, y0, ws, st,
+                    idx_out=idx0, w_out=w0)
+    v0 = torch.empty(B * T, wl.d, dtype=torch.bfloat16, device=dev)
+    qtmp = torch.empty(B * T, wl.dk, dtype=torch.bfloat16, device=dev)
+    sdm.sdm_project(cfg, pd, x0, qtmp, torch.empty_like(qtmp), v0)
+    del qtmp, ws
+    wsd = sdm.alloc_workspace(sdm.workspace_bytes(cfg, B, 1))
+    wsa = sdm.alloc_workspace(sdm.address_workspace_bytes(cfg, B))
+    ydec = torch.empty(S, B, wl.d, device=dev)
+    idxd = torch.empty(S, B, 2, wl.W, dtype=torch.int32, device=dev)
+    wd = torch.empty(S, B, 2, wl.W, device=dev)
+    vd = torch.empty(S, B, wl.d, dtype=torch.bfloat16, device=dev)
+    qw = torch.empty(B, wl.dk, dtype=torch.bfloat16, device=dev)
+    qr = torch.empty_like(qw)
+    xd = dec["x"].to(dev)
+    ad = dec["alpha"].to(dev)
+    bd = dec["beta"].to(dev)
+    for s in range(S):
+        sdm.sdm_decode_step(cfg, pd, xd[s], ad[s], bd[s], banks, ydec[s], wsd, st)
+        # the addressing of this step, recomputed with the same kernels for the oracle
+        sdm.sdm_project(cfg, pd, xd[s], qw, qr, vd[s])
+        sdm.sdm_address(cfg, pd["K1"], pd["K2"], qw, qr, idxd[s], wd[s], wsa, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    rows = tl.sample_rows(wl.d, N_ROWS, seed=3)
+    rt = torch.as_tensor(rows, device=dev)
+    for b in (0, 17, 42, 63):
+        idx_b = np.concatenate([idx0[b * T:(b + 1) * T].cpu().numpy(), idxd[:, b].cpu().numpy()])
+        w_b = np.concatenate([w0[b * T:(b + 1) * T].cpu().numpy(),
+                              wd[:, b].cpu().numpy()]).astype(np.float64)
+        v_b = torch.cat([v0[b * T:(b + 1) * T][:, rt], vd[:, b][:, rt]]).cpu()
+        al = np.concatenate([tok["alpha"][b].numpy(), dec["alpha"][:, b].numpy()]).astype(np.float64)
+        be = np.concatenate([tok["beta"][b].numpy(), dec["beta"][:, b].numpy()]).astype(np.float64)
+        M = np.ascontiguousarray(oracle.storage(p["M0"])[0][:, rows])
+        yr = oracle.scan(M, oracle.storage(v_b)[0], al, be, idx_b[:, 0], w_b[:, 0],
+                         idx_b[:, 1], w_b[:, 1])
+        yg = np.concatenate([y0[b][:, rt].cpu().numpy(), ydec[:, b][:, rt].cpu().numpy()])
+        ok, m = tl.state_ok("bf16", yg, yr)
+        assert ok, ("y", b, m)
+        ok, m = tl.state_ok("bf16", tl.bank_rows_cpu(banks, b, rows), oracle.to_f64(M))
+        assert ok, ("bank", b, m)

@@ -1,0 +1,292 @@
+"""GPU parity of the CUDA path (through the C-ABI) against the CPU oracle, element by
+element, on seeded inputs small enough for the oracle to run in seconds but spanning
+several blocks/machines and ragged tails. Full-size workloads: test_gpu_full.py."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_memory_linear_key_b300 as sdm
+import synth
+from tests import sdm_testlib as tl
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    # the tiny fp32 workload itself (B1, T256, d64, n32, W8)
+    "tiny-f32": synth.WORKLOADS["tiny-f32"],
+    # ragged: T not a multiple of the token-parallel width or of the code block,
+    # n not a power of two (padded sort), several machines per sequence
+    "ragged-bf16": synth.Workload("ragged-bf16", B=3, T=333, d=96, n=40, dk=48, W=16,
+                                  dtype="bf16", seed=77),
+    "ragged-f32": synth.Workload("ragged-f32", B=2, T=201, d=48, n=24, dk=32, W=8,
+                                 dtype="f32", seed=78),
+    # W = n (the W = sqrt(N) edge), W = 32
+    "w-eq-n": synth.Workload("w-eq-n", B=2, T=150, d=64, n=32, dk=64, W=32, dtype="bf16",
+                             seed=79),
+    # the pages' W = 64 with the real sub-key width, small bank
+    "w64-small": synth.Workload("w64-small", B=2, T=300, d=128, n=96, dk=256, W=64,
+                                dtype="bf16", seed=80),
+    # the full 480 x 480 product-key grid and key width, small d
+    "n480-small-d": synth.Workload("n480-small-d", B=1, T=257, d=32, n=480, dk=256, W=64,
+                                   dtype="bf16", seed=81),
+}
+
+
+def _inputs(wl):
+    return synth.make_params(wl), synth.make_tokens(wl)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    from sparse_memory_linear_key_b300 import build
+    build.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def test_init_bank_bit_exact():
+    for wl in (synth.WORKLOADS["tiny-f32"], SMALL["w64-small"]):
+        p = synth.make_params(wl)
+        cfg = tl.cfg_of(wl)
+        banks = torch.empty(3, wl.N, wl.d, dtype=wl.torch_dtype, device="cuda")
+        banks.fill_(7)
+        sdm.sdm_init_bank(cfg, p["M0"].cuda(), banks)
+        torch.cuda.synchronize()
+        want = oracle.init_bank(p["M0"], 3)
+        got, _ = oracle.storage(banks.cpu())
+        assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_projection_parity(name):
+    wl = SMALL[name]
+    p, tok = _inputs(wl)
+    out = tl.run_staged(wl, p, tok)
+    x = tok["x"].reshape(-1, wl.d)
+    for key, w in (("q_w", "W_qw"), ("q_r", "W_qr"), ("v", "W_v")):
+        ref = oracle.to_f64(oracle.project(x, p[w]))
+        got = oracle.to_f64(out[key].cpu())
+        if wl.dtype == "f32":
+            np.testing.assert_allclose(got, ref, rtol=2e-5, atol=2e-5)
+        else:
+            assert tl.projection_ok(got, ref, oracle.to_f64(x), oracle.to_f64(p[w])), key
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_address_parity(name):
+    """Slot sets exact (except near-ties) and weights within 1e-5, with the oracle
+    scoring the CUDA path's own q bits."""
+    wl = SMALL[name]
+    p, tok = _inputs(wl)
+    out = tl.run_staged(wl, p, tok)
+    assert out["status"] == 0
+    idx = out["idx"].cpu().numpy()
+    wsel = out["wsel"].cpu().numpy()
+    # ascending, distinct, in range
+    assert np.all(np.diff(idx, axis=-1) > 0)
+    assert idx.min() >= 0 and idx.max() < wl.N
+    for kind, key in ((0, "q_w"), (1, "q_r")):
+        S, k, _, gaps = oracle.address(out[key].cpu(), p["K1"], p["K2"], wl.W)
+        n_bad, n_exc, unexc = tl.set_parity(idx[:, kind], S, gaps)
+        assert len(unexc) == 0, (name, kind, unexc[:5], n_bad, n_exc)
+        err = tl.max_weight_err(idx[:, kind], wsel[:, kind], S, k, range(len(S)))
+        assert err <= tl.WEIGHT_ATOL, (name, kind, err)
+        np.testing.assert_allclose(wsel[:, kind].sum(-1), 1.0, atol=1e-5)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_scan_parity(name):
+    """The recurrence on every row of every sequence, teacher-forced with the CUDA
+    path's addressing, against the oracle: y and the final bank."""
+    wl = SMALL[name]
+    p, tok = _inputs(wl)
+    out = tl.run_staged(wl, p, tok)
+    assert out["status"] == 0
+    rows = np.arange(wl.d)
+    y = out["y"].cpu().numpy().reshape(wl.B, wl.T, wl.d)
+    for b in range(wl.B):
+        yr, M = tl.oracle_scan_rows(wl, p["M0"], out, b, rows)
+        ok, m = tl.state_ok(wl.dtype, y[b], yr)
+        assert ok, (name, b, "y", m)
+        ok, m = tl.state_ok(wl.dtype, tl.bank_rows_cpu(out["banks"], b, rows), oracle.to_f64(M))
+        assert ok, (name, b, "bank", m)
+
+
+def test_prefill_entry_point_matches_staged():
+    """sdm_prefill (one call) gives the same bits as the staged calls."""
+    wl = SMALL["ragged-bf16"]
+    p, tok = _inputs(wl)
+    out = tl.run_staged(wl, p, tok)
+    cfg = tl.cfg_of(wl)
+    pd = tl.to_dev(p)
+    banks = torch.empty(wl.B, wl.N, wl.d, dtype=wl.torch_dtype, device="cuda")
+    sdm.sdm_init_bank(cfg, pd["M0"], banks)
+    y = torch.empty(wl.B, wl.T, wl.d, device="cuda")
+    idx = torch.empty(wl.B * wl.T, 2, wl.W, dtype=torch.int32, device="cuda")
+    wsel = torch.empty(wl.B * wl.T, 2, wl.W, device="cuda")
+    ws = sdm.alloc_workspace(sdm.workspace_bytes(cfg, wl.B, wl.T))
+    st = sdm.new_status()
+    sdm.sdm_prefill(cfg, pd, tok["x"].cuda(), tok["alpha"].cuda(), tok["beta"].cuda(), banks, y,
+                    ws, st, idx_out=idx, w_out=wsel)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(idx, out["idx"]) and torch.equal(wsel, out["wsel"])
+    assert torch.equal(y.reshape(-1, wl.d), out["y"])
+    assert torch.equal(banks, out["banks"])
+
+
+def test_tiny_f32_free_running():
+    """The whole layer with the oracle's own projections and addressing (no teacher
+    forcing) on the tiny fp32 workload."""
+    wl = synth.WORKLOADS["tiny-f32"]
+    p, tok = _inputs(wl)
+    out = tl.run_staged(wl, p, tok)
+    ref = oracle.prefill_sequence(tok["x"][0], p, tok["alpha"][0], tok["beta"][0], wl.W)
+    idx = out["idx"].cpu().numpy()
+    for kind, S, g in ((0, ref["S"], ref["gap_w"]), (1, ref["R"], ref["gap_r"])):
+        n_bad, n_exc, unexc = tl.set_parity(idx[:, kind], S, g)
+        assert n_bad == 0, (kind, n_bad, n_exc)
+    y = out["y"].cpu().numpy()
+    assert np.abs(y - ref["y"]).max() <= tl.F32_ATOL
+    M = oracle.to_f64(out["banks"][0].cpu())
+    assert np.abs(M - ref["M"]).max() <= tl.F32_ATOL
+
+
+# ------------------------------------------------- the scan under heavy collisions
+
+def _random_sets(rng, T, N, W):
+    return np.stack([np.sort(rng.choice(N, W, replace=False)) for _ in range(T)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("B,T,N,W,d,dtype,seed", [
+    (1, 500, 64, 8, 16, "bf16", 1),       # 8 of 64 slots per token: collisions at every dt
+    (1, 700, 16, 8, 16, "f32", 2),        # half the bank written by every token
+    (2, 300, 256, 64, 32, "bf16", 3),     # W = 64 of 256
+    (1, 64, 64, 64, 16, "bf16", 4),       # every token writes and reads ALL slots
+    (3, 97, 1024, 16, 48, "f32", 5),
+])
+def test_scan_collisions(B, T, N, W, d, dtype, seed):
+    """Random ascending slot sets from a tiny bank (so consecutive tokens share many
+    slots, and read sets hit the same token's write set): the collision forwarding
+    of the token-parallel scan must reproduce the sequential oracle."""
+    rng = np.random.default_rng(seed)
+    n = int(round(N ** 0.5))
+    cfg = sdm.make_cfg(d, n, 16, W, dtype)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    ntok = B * T
+    idx = np.zeros((ntok, 2, W), dtype=np.int32)
+    idx[:, 0] = _random_sets(rng, ntok, N, W)
+    idx[:, 1] = _random_sets(rng, ntok, N, W)
+    # some tokens read exactly what they write
+    same = rng.random(ntok) < 0.2
+    idx[same, 1] = idx[same, 0]
+    wts = rng.random((ntok, 2, W)).astype(np.float32) + 0.05
+    wts /= wts.sum(-1, keepdims=True)
+    v = torch.randn(ntok, d, generator=torch.Generator().manual_seed(seed)).to(dt)
+    M0 = (torch.randn(N, d, generator=torch.Generator().manual_seed(seed + 1)) * 0.1).to(dt)
+    alpha = torch.from_numpy(rng.uniform(0.5, 1.0, ntok).astype(np.float32))
+    beta = torch.from_numpy(rng.uniform(0.0, 1.0, ntok).astype(np.float32))
+    banks, y, status = tl.run_scan_only(cfg, M0, torch.from_numpy(idx), torch.from_numpy(wts),
+                                        v, alpha, beta, B, T)
+    assert status == 0
+    yg = y.cpu().numpy().reshape(B, T, d)
+    for b in range(B):
+        M = np.ascontiguousarray(oracle.storage(M0)[0].copy())
+        sl = slice(b * T, (b + 1) * T)
+        yr = oracle.scan(M, oracle.storage(v[sl])[0], alpha[sl].numpy().astype(np.float64),
+                         beta[sl].numpy().astype(np.float64), idx[sl, 0],
+                         wts[sl, 0].astype(np.float64), idx[sl, 1], wts[sl, 1].astype(np.float64))
+        ok, m = tl.state_ok(dtype, yg[b], yr)
+        assert ok, ("y", b, m)
+        ok, m = tl.state_ok(dtype, oracle.to_f64(banks[b].cpu()), oracle.to_f64(M))
+        assert ok, ("bank", b, m)
+
+
+@pytest.mark.parametrize("B", [1, 200, 400, 800, 2000])
+def test_scan_token_parallel_widths(B):
+    """The launch picks 16, 8, 4, 2 or 1 tokens in flight per machine depending on
+    how many machines there are; every width must agree with the oracle."""
+    rng = np.random.default_rng(B)
+    T, N, W, d = 40, 64, 8, 16
+    cfg = sdm.make_cfg(d, 8, 16, W, "bf16")
+    ntok = B * T
+    idx = np.zeros((ntok, 2, W), dtype=np.int32)
+    idx[:, 0] = _random_sets(rng, ntok, N, W)
+    idx[:, 1] = _random_sets(rng, ntok, N, W)
+    wts = (rng.random((ntok, 2, W)) + 0.05).astype(np.float32)
+    wts /= wts.sum(-1, keepdims=True)
+    v = torch.randn(ntok, d, generator=torch.Generator().manual_seed(9)).to(torch.bfloat16)
+    M0 = (torch.randn(N, d, generator=torch.Generator().manual_seed(10)) * 0.1).to(torch.bfloat16)
+    alpha = torch.from_numpy(rng.uniform(0.5, 1.0, ntok).astype(np.float32))
+    beta = torch.from_numpy(rng.uniform(0.0, 1.0, ntok).astype(np.float32))
+    banks, y, status = tl.run_scan_only(cfg, M0, torch.from_numpy(idx), torch.from_numpy(wts),
+                                        v, alpha, beta, B, T)
+    assert status == 0
+    yg = y.cpu().numpy().reshape(B, T, d)
+    bk = banks.cpu()
+    for b in sorted(set([0, B // 2, B - 1])):
+        M = np.ascontiguousarray(oracle.storage(M0)[0].copy())
+        sl = slice(b * T, (b + 1) * T)
+        yr = oracle.scan(M, oracle.storage(v[sl])[0], alpha[sl].numpy().astype(np.float64),
+                         beta[sl].numpy().astype(np.float64), idx[sl, 0],
+                         wts[sl, 0].astype(np.float64), idx[sl, 1], wts[sl, 1].astype(np.float64))
+        assert tl.state_ok("bf16", yg[b], yr)[0]
+        assert tl.state_ok("bf16", oracle.to_f64(bk[b]), oracle.to_f64(M))[0]
+
+
+def test_single_token_and_single_sequence():
+    """T = 1 (the decode shape) and B = 1 through sdm_decode_step and sdm_prefill."""
+    wl = synth.Workload("t1", B=5, T=1, d=64, n=32, dk=64, W=16, dtype="bf16", seed=90)
+    p, tok = _inputs(wl)
+    out = tl.run_staged(wl, p, tok)
+    cfg = tl.cfg_of(wl)
+    pd = tl.to_dev(p)
+    banks = torch.empty(wl.B, wl.N, wl.d, dtype=torch.bfloat16, device="cuda")
+    sdm.sdm_init_bank(cfg, pd["M0"], banks)
+    y = torch.empty(wl.B, wl.d, device="cuda")
+    ws = sdm.alloc_workspace(sdm.workspace_bytes(cfg, wl.B, 1))
+    st = sdm.new_status()
+    sdm.sdm_decode_step(cfg, pd, tok["x"][:, 0].cuda().contiguous(),
+                        tok["alpha"][:, 0].cuda().contiguous(),
+                        tok["beta"][:, 0].cuda().contiguous(), banks, y, ws, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(y, out["y"]) and torch.equal(banks, out["banks"])
+    for b in range(wl.B):
+        yr, M = tl.oracle_scan_rows(wl, p["M0"], out, b, np.arange(wl.d))
+        assert tl.state_ok("bf16", y[b].cpu().numpy()[None], yr)[0]
+
+
+def test_zero_tokens_is_a_no_op():
+    wl = SMALL["ragged-bf16"]
+    cfg = tl.cfg_of(wl)
+    banks = torch.zeros(1, wl.N, wl.d, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(1, wl.d, device="cuda")
+    st = sdm.new_status()
+    ws = sdm.alloc_workspace(256)
+    idx = torch.zeros(1, 2, wl.W, dtype=torch.int32, device="cuda")
+    sdm.sdm_scan(cfg, idx, torch.zeros(1, 2, wl.W, device="cuda"),
+                 torch.zeros(1, wl.d, dtype=torch.bfloat16, device="cuda"),
+                 torch.zeros(1, device="cuda"), torch.zeros(1, device="cuda"), banks, y, 1, 0, ws,
+                 st)
+    torch.cuda.synchronize()
+    assert st.item() == 0 and int(banks.abs().sum().item()) == 0
+
+
+def test_out_of_range_slot_is_reported_not_faulted():
+    """A slot id outside [0, N) reaching the scan is skipped and reported as
+    SDM_ERANGE in the device status word."""
+    B, T, N, W, d = 1, 10, 64, 8, 16
+    cfg = sdm.make_cfg(d, 8, 16, W, "bf16")
+    rng = np.random.default_rng(0)
+    idx = np.zeros((T, 2, W), dtype=np.int32)
+    idx[:, 0] = _random_sets(rng, T, N, W)
+    idx[:, 1] = _random_sets(rng, T, N, W)
+    idx[3, 1, -1] = N + 5          # ascending order kept: the last one is the largest
+    wts = np.full((T, 2, W), 1.0 / W, dtype=np.float32)
+    M0 = torch.zeros(N, d, dtype=torch.bfloat16)
+    banks, y, status = tl.run_scan_only(cfg, M0, torch.from_numpy(idx), torch.from_numpy(wts),
+                                        torch.ones(T, d, dtype=torch.bfloat16),
+                                        torch.full((T,), 0.9), torch.full((T,), 0.5), B, T)
+    assert status == sdm.SDM_ERANGE
