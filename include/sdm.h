@@ -141,6 +141,29 @@ SDM_API int sdm_scan_run(const sdm_cfg* cfg, const int32_t* idx, const float* ws
                          float* y, int B, int T, const void* ws, size_t ws_bytes,
                          int* dev_status, void* stream);
 
+/* Size of the device array that sdm_scan_noalloc uses as its scratch: 8 MiB, i.e.
+ * B * T * w * 4 bytes of collision codes, B * T <= 32768 tokens at w = 64. */
+#define SDM_SCAN_NOALLOC_MAX_BYTES (8u << 20)
+
+/* sdm_scan without a caller workspace, for callers that cannot allocate device
+ * memory: a plugin inside an application that owns all device memory through its own
+ * pool or budget and hands this code no allocator, or a latency-critical loop where a
+ * cudaMalloc/cudaFree would synchronise the device. The pages have no counterpart: it
+ * is the same recurrence as sdm_scan, with the scratch (the collision codes) kept in a
+ * library-owned device array of SDM_SCAN_NOALLOC_MAX_BYTES that every GPU loading the
+ * library holds until the process exits. Arguments as sdm_scan, minus ws / ws_bytes.
+ *  - Returns SDM_EWORKSPACE, before touching the GPU, if B * T * w * 4 bytes exceed
+ *    SDM_SCAN_NOALLOC_MAX_BYTES.
+ *  - Allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ *  - The first call on a device looks up the array's device address (once per device,
+ *    with that device current); make that first call before any stream capture.
+ *  - Every call shares the one array: calls whose work overlaps on the GPU (other
+ *    streams, other host threads) race on it and must be serialised by the caller. */
+SDM_API int sdm_scan_noalloc(const sdm_cfg* cfg, const int32_t* idx, const float* wsel,
+                             const void* v, const float* alpha, const float* beta,
+                             void* banks, float* y, int B, int T, int* dev_status,
+                             void* stream);
+
 /* Whole layer over a prefill of B sequences of T tokens: sdm_project, sdm_address and
  * sdm_scan in one call. x [B, T, d], alpha/beta [B, T], banks [B, N, d] (in place),
  * y [B, T, d] fp32. idx_out [B, T, 2, w] / w_out [B, T, 2, w] optional (NULL = not

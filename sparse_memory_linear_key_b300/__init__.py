@@ -85,6 +85,7 @@ def lib():
             "sdm_scan": ([CP, P, P, P, P, P, P, P, I, I, P, S, P, P], I),
             "sdm_scan_prepare": ([CP, P, I, I, P, S, P, P], I),
             "sdm_scan_run": ([CP, P, P, P, P, P, P, P, I, I, P, S, P, P], I),
+            "sdm_scan_noalloc": ([CP, P, P, P, P, P, P, P, I, I, P, P], I),
             "sdm_prefill": ([CP, WP, P, P, P, P, P, I, I, P, P, P, S, P, P], I),
             "sdm_decode_step": ([CP, WP, P, P, P, P, P, I, P, S, P, P], I),
         }
@@ -236,6 +237,24 @@ def sdm_scan_run(cfg: Cfg, idx, wsel, v, alpha, beta, banks, y, B: int, T: int, 
                               ws.numel() * ws.element_size(),
                               _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)),
            "sdm_scan_run")
+
+
+def sdm_scan_noalloc(cfg: Cfg, idx, wsel, v, alpha, beta, banks, y, B: int, T: int, dev_status,
+                     stream=None) -> None:
+    """sdm_scan with its scratch in a library-owned device array (no workspace, no
+    allocation), for callers that cannot allocate device memory; B * T * w * 4 bytes
+    must not exceed SDM_SCAN_NOALLOC_MAX_BYTES (8 MiB)."""
+    dt = cfg.torch_dtype
+    _check(lib().sdm_scan_noalloc(ctypes.byref(cfg), _ptr(idx, torch.int32, "idx"),
+                                  _ptr(wsel, torch.float32, "wsel"), _ptr(v, dt, "v"),
+                                  _ptr(alpha, torch.float32, "alpha"),
+                                  _ptr(beta, torch.float32, "beta"), _ptr(banks, dt, "banks"),
+                                  _ptr(y, torch.float32, "y"), B, T,
+                                  _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)),
+           "sdm_scan_noalloc")
+
+
+SCAN_NOALLOC_MAX_BYTES = 8 << 20
 
 
 def sdm_prefill(cfg: Cfg, params, x, alpha, beta, banks, y, ws, dev_status, idx_out=None,
