@@ -141,8 +141,11 @@ SDM_API int sdm_scan_run(const sdm_cfg* cfg, const int32_t* idx, const float* ws
                          float* y, int B, int T, const void* ws, size_t ws_bytes,
                          int* dev_status, void* stream);
 
-/* Size of the device array that sdm_scan_noalloc uses as its scratch: 8 MiB, i.e.
- * B * T * w * 4 bytes of collision codes, B * T <= 32768 tokens at w = 64. */
+/* Size of the device array that sdm_scan_noalloc uses as its scratch: 8 MiB. A call
+ * needs sdm_scan_workspace_bytes(cfg, B, T) of it: the collision codes (B * T * w * 4
+ * bytes) and one progress flag per token and 1 KB row block of a slot vector
+ * (B * T * ceil(d * elem / 1024) * 4 bytes), plus under 1 KB of alignment and counters;
+ * at w = 64, d = 2048 bf16 that is B * T <= 30839 tokens. */
 #define SDM_SCAN_NOALLOC_MAX_BYTES (8u << 20)
 
 /* sdm_scan without a caller workspace, for callers that cannot allocate device
@@ -152,9 +155,10 @@ SDM_API int sdm_scan_run(const sdm_cfg* cfg, const int32_t* idx, const float* ws
  * is the same recurrence as sdm_scan, with the scratch (the collision codes) kept in a
  * library-owned device array of SDM_SCAN_NOALLOC_MAX_BYTES that every GPU loading the
  * library holds until the process exits. Arguments as sdm_scan, minus ws / ws_bytes.
- *  - Returns SDM_EWORKSPACE, before touching the GPU, if B * T * w * 4 bytes exceed
- *    SDM_SCAN_NOALLOC_MAX_BYTES.
- *  - Allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ *  - Returns SDM_EWORKSPACE, before touching the GPU, if sdm_scan_workspace_bytes(cfg, B,
+ *    T) exceeds SDM_SCAN_NOALLOC_MAX_BYTES.
+ *  - Allocates nothing (no cudaMalloc, cudaFree or allocating library call); it clears
+ *    the flags it uses with cudaMemsetAsync on `stream`.
  *  - The first call on a device looks up the array's device address (once per device,
  *    with that device current); make that first call before any stream capture.
  *  - Every call shares the one array: calls whose work overlaps on the GPU (other

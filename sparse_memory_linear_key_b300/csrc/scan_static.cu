@@ -4,15 +4,17 @@
 // Some hosts give this code no way to allocate: a plugin inside an application that
 // owns all device memory through its own pool or budget, or a latency-critical loop
 // where cudaMalloc/cudaFree would synchronise the device and stall other work. For
-// them this entry point keeps the scan's only scratch (the collision codes, B*T*w*4
-// bytes) in g_scan_scratch below, a file-scope device array of
-// SDM_SCAN_NOALLOC_MAX_BYTES that every GPU loading the library holds until exit.
+// them this entry point keeps the scan's scratch (the collision codes, B*T*w*4 bytes,
+// and the per-token progress flags of the row blocks, see sdm_scan_workspace_bytes) in
+// g_scan_scratch below, a file-scope device array of SDM_SCAN_NOALLOC_MAX_BYTES that
+// every GPU loading the library holds until exit.
 //
 // The first call on each device looks up the array's device address with
 // cudaGetSymbolAddress (with that device current) and caches it; that first call
 // should come before any stream capture. The array is shared by every call: each call
-// fully rewrites the part it uses before reading it (nothing needs to start at zero),
-// and calls whose work overlaps on the GPU race on it.
+// rewrites the codes it uses and clears the flags it uses (cudaMemsetAsync on the
+// caller's stream) before reading them, and calls whose work overlaps on the GPU race
+// on it.
 #include <cuda_runtime.h>
 
 #include <mutex>

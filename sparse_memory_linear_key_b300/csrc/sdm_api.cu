@@ -37,11 +37,17 @@ static int check_scan_cfg(const sdm_cfg* cfg)
     const sdm_cfg& c = *cfg;
     if (c.d <= 0 || c.n_sub <= 0 || c.w <= 0 || (c.dtype != SDM_F32 && c.dtype != SDM_BF16))
         return SDM_EINVAL;
-    if (c.d % kScanRows != 0 || (c.w != 8 && c.w != 16 && c.w != 32 && c.w != 64))
+    if (c.d % kRowAlign != 0 || (c.w != 8 && c.w != 16 && c.w != 32 && c.w != 64))
         return SDM_EUNSUPPORTED;
     if ((long long)c.n_sub * c.n_sub < c.w || c.n_sub > 512)
         return SDM_EUNSUPPORTED;
     return SDM_OK;
+}
+
+// The scan's workspace: the collision codes, then the progress flags.
+static size_t scan_codes_bytes(const sdm_cfg& c, int B, int T)
+{
+    return align256((size_t)B * T * 2 * c.w * 2);
 }
 
 static size_t esize(const sdm_cfg& c) { return c.dtype == SDM_BF16 ? 2 : 4; }
@@ -52,7 +58,7 @@ static int cuda_status(cudaError_t e) { return e == cudaSuccess ? SDM_OK : SDM_E
 
 // Workspace layout of a prefill / decode call over ntok = B*T tokens.
 struct PrefillWs {
-    size_t q_w, q_r, v, idx, wsel, codes, addr, total;
+    size_t q_w, q_r, v, idx, wsel, codes, flags, addr, total;
 };
 
 static PrefillWs prefill_layout(const sdm_cfg& c, int64_t ntok)
@@ -66,6 +72,7 @@ static PrefillWs prefill_layout(const sdm_cfg& c, int64_t ntok)
     L.idx = o; o += align256((size_t)ntok * W2 * 4);
     L.wsel = o; o += align256((size_t)ntok * W2 * 4);
     L.codes = o; o += align256((size_t)ntok * W2 * 2);
+    L.flags = o; o += scan_flags_bytes(c, 1, (int)ntok);
     L.addr = o; o += address_ws_bytes(c, ntok);
     L.total = o;
     return L;
@@ -101,7 +108,7 @@ int sdm_check_cfg(const sdm_cfg* cfg)
     if (c.d <= 0 || c.n_sub <= 0 || c.dk <= 0 || c.w <= 0 ||
         (c.dtype != SDM_F32 && c.dtype != SDM_BF16))
         return SDM_EINVAL;
-    if (c.d % kScanRows != 0)
+    if (c.d % kRowAlign != 0)
         return SDM_EUNSUPPORTED;
     if (c.w != 8 && c.w != 16 && c.w != 32 && c.w != 64)
         return SDM_EUNSUPPORTED;
@@ -130,7 +137,7 @@ size_t sdm_scan_workspace_bytes(const sdm_cfg* cfg, int B, int T)
 {
     if (check_scan_cfg(cfg) != SDM_OK || B < 0 || T < 0)
         return 0;
-    return align256((size_t)B * T * 2 * cfg->w * 2);
+    return scan_codes_bytes(*cfg, B, T) + scan_flags_bytes(*cfg, B, T);
 }
 
 size_t sdm_workspace_bytes(const sdm_cfg* cfg, int B, int T)
@@ -199,13 +206,12 @@ int sdm_address(const sdm_cfg* cfg, const void* K1, const void* K2, const void* 
 
 static int scan_impl(const sdm_cfg& c, const int32_t* idx, const float* wsel, const void* v,
                      const float* alpha, const float* beta, void* banks, float* y, int B, int T,
-                     uint16_t* codes, int* dev_status, cudaStream_t s)
+                     uint16_t* codes, void* flags, int* dev_status, cudaStream_t s)
 {
     cudaError_t e = launch_fwd_codes(c, idx, B, T, codes, dev_status, s);
     if (e != cudaSuccess)
         return SDM_ECUDA;
-    ScanLaunch L = choose_scan_launch(B, T, c.d, num_sms_current_device());
-    e = launch_scan(c, idx, wsel, codes, v, alpha, beta, banks, y, B, T, L, dev_status, s);
+    e = launch_scan(c, idx, wsel, codes, v, alpha, beta, banks, y, B, T, flags, dev_status, s);
     return cuda_status(e);
 }
 
@@ -250,9 +256,9 @@ int sdm_scan_run(const sdm_cfg* cfg, const int32_t* idx, const float* wsel, cons
         return SDM_EINVAL;
     if (ws_bytes < sdm_scan_workspace_bytes(cfg, B, T))
         return SDM_EWORKSPACE;
-    ScanLaunch L = choose_scan_launch(B, T, cfg->d, num_sms_current_device());
+    void* flags = (char*)ws + scan_codes_bytes(*cfg, B, T);
     return cuda_status(launch_scan(*cfg, idx, wsel, (const uint16_t*)ws, v, alpha, beta, banks,
-                                   y, B, T, L, dev_status, (cudaStream_t)stream));
+                                   y, B, T, flags, dev_status, (cudaStream_t)stream));
 }
 
 int sdm_scan(const sdm_cfg* cfg, const int32_t* idx, const float* wsel, const void* v,
@@ -278,8 +284,8 @@ int sdm_scan(const sdm_cfg* cfg, const int32_t* idx, const float* wsel, const vo
         return SDM_EINVAL;
     if (ws_bytes < sdm_scan_workspace_bytes(cfg, B, T))
         return SDM_EWORKSPACE;
-    return scan_impl(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, (uint16_t*)ws, dev_status,
-                     (cudaStream_t)stream);
+    return scan_impl(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, (uint16_t*)ws,
+                     (char*)ws + scan_codes_bytes(*cfg, B, T), dev_status, (cudaStream_t)stream);
 }
 
 int sdm_prefill(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const float* alpha,
@@ -314,6 +320,7 @@ int sdm_prefill(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const f
     int32_t* idx = idx_out ? idx_out : (int32_t*)(base + L.idx);
     float* wsel = w_out ? w_out : (float*)(base + L.wsel);
     uint16_t* codes = (uint16_t*)(base + L.codes);
+    void* flags = base + L.flags;
     cudaStream_t s = (cudaStream_t)stream;
     rc = launch_project(*cfg, *w, x, ntok, q_w, q_r, v, s);
     if (rc != SDM_OK)
@@ -321,7 +328,7 @@ int sdm_prefill(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const f
     if (launch_address(*cfg, w->K1, w->K2, q_w, q_r, ntok, idx, wsel, base + L.addr, dev_status,
                        s) != cudaSuccess)
         return SDM_ECUDA;
-    return scan_impl(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, codes, dev_status, s);
+    return scan_impl(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, codes, flags, dev_status, s);
 }
 
 int sdm_decode_step(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const float* alpha,

@@ -183,3 +183,147 @@ __device__ __forceinline__ void warp_bitonic_sort(uint64_t (&k)[E])
 }
 
 }  // namespace sdm
+
+// ------------------------------------------------ global flags, mbarriers, bulk copies
+
+namespace sdm {
+
+__device__ __forceinline__ int ld_relaxed_gpu(const int* p)
+{
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(int* p, int v)
+{
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_gpu(int* p, int v)
+{
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// orders this thread's earlier generic-proxy accesses of global memory before its later
+// async-proxy (bulk copy) accesses, and vice versa
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_shared()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbarrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// Declares `bytes` of the current phase's transactions done without a copy (used when
+// copies that were counted will not be issued).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.complete_tx.shared::cta.relaxed.cta.b64 [%0], %1;" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of parity `parity` of an mbarrier. Returns false if the
+// global abort flag is raised (abort may be null: not watched) or the wait ran out;
+// a wait that ran out records SDM_ETIMEOUT and raises the abort flag.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* abort, int* status)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (abort != nullptr && ld_relaxed_gpu(abort) != 0)
+            return false;
+        if (clock64() - t0 > kSpinLimitCycles) {
+            report(status, SDM_ETIMEOUT);
+            if (abort != nullptr)
+                st_relaxed_gpu(abort, 1);
+            return false;
+        }
+    }
+}
+
+// Bounded wait until *f >= target (relaxed reads; the caller follows a successful wait
+// with fence_acq_rel_gpu() to make it an acquire).
+__device__ __forceinline__ bool spin_geq_gpu(const int* f, int target, int* abort, int* status)
+{
+    if (ld_relaxed_gpu(f) >= target)
+        return true;
+    const long long t0 = clock64();
+    while (true) {
+        __nanosleep(100);
+        if (ld_relaxed_gpu(f) >= target)
+            return true;
+        if (ld_relaxed_gpu(abort) != 0)
+            return false;
+        if (clock64() - t0 > kSpinLimitCycles) {
+            report(status, SDM_ETIMEOUT);
+            st_relaxed_gpu(abort, 1);
+            return false;
+        }
+    }
+}
+
+// Bulk copy global -> shared (this CTA), completing `bytes` transactions on `bar`.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+}  // namespace sdm
