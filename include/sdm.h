@@ -85,10 +85,15 @@ SDM_API const char* sdm_version(void);
 SDM_API int sdm_check_cfg(const sdm_cfg* cfg);
 
 /* Workspace needed by sdm_prefill / sdm_decode_step for B sequences of T tokens
- * (decode: T = 1), by sdm_address for ntok tokens, and by sdm_scan. */
+ * (decode: T = 1), by sdm_address for ntok tokens, and by sdm_scan (and its two steps).
+ * sdm_scan_min_workspace_bytes is the smallest workspace the scan accepts: without the
+ * room for its forwarding ring (slot values handed from a writer still in flight to a
+ * later token) it runs, with the same results, but a token whose slot was just written
+ * by another in-flight token waits for that writer's bank store instead. */
 SDM_API size_t sdm_workspace_bytes(const sdm_cfg* cfg, int B, int T);
 SDM_API size_t sdm_address_workspace_bytes(const sdm_cfg* cfg, int64_t ntok);
 SDM_API size_t sdm_scan_workspace_bytes(const sdm_cfg* cfg, int B, int T);
+SDM_API size_t sdm_scan_min_workspace_bytes(const sdm_cfg* cfg, int B, int T);
 
 /* Bank initialisation from the learned initial state ("Sparse Delta Memory",
  * Abstract: the initial state of the memory is learned and used as parametric
@@ -132,8 +137,9 @@ SDM_API int sdm_scan(const sdm_cfg* cfg, const int32_t* idx, const float* wsel, 
  * sdm_scan_prepare computes, into ws, the collision codes of the B*T tokens' slot
  * sets (for each slot reference, the distance to the latest earlier write of the same
  * slot within a short window, and its position there); sdm_scan_run then runs the
- * recurrence with those codes. The same ws (sdm_scan_workspace_bytes) and idx must be
- * passed to both; sdm_scan == sdm_scan_prepare followed by sdm_scan_run. */
+ * recurrence with those codes. The same ws and idx must be passed to both (ws_bytes at
+ * least sdm_scan_min_workspace_bytes, sdm_scan_workspace_bytes for the forwarding
+ * ring); sdm_scan == sdm_scan_prepare followed by sdm_scan_run. */
 SDM_API int sdm_scan_prepare(const sdm_cfg* cfg, const int32_t* idx, int B, int T, void* ws,
                              size_t ws_bytes, int* dev_status, void* stream);
 SDM_API int sdm_scan_run(const sdm_cfg* cfg, const int32_t* idx, const float* wsel,
@@ -142,10 +148,12 @@ SDM_API int sdm_scan_run(const sdm_cfg* cfg, const int32_t* idx, const float* ws
                          int* dev_status, void* stream);
 
 /* Size of the device array that sdm_scan_noalloc uses as its scratch: 8 MiB. A call
- * needs sdm_scan_workspace_bytes(cfg, B, T) of it: the collision codes (B * T * w * 4
- * bytes) and one progress flag per token and 1 KB row block of a slot vector
- * (B * T * ceil(d * elem / 1024) * 4 bytes), plus under 1 KB of alignment and counters;
- * at w = 64, d = 2048 bf16 that is B * T <= 30839 tokens. */
+ * needs sdm_scan_min_workspace_bytes(cfg, B, T) of it: the collision codes (B * T * w * 4
+ * bytes), one forwarding mask per token (B * T * 8 bytes) and one progress flag per
+ * token and 1 KB row block of a slot vector (B * T * ceil(d * elem / 1024) * 4 bytes),
+ * plus under 1 KB of alignment and counters; at w = 64, d = 2048 bf16 that is
+ * B * T <= 29957 tokens. When sdm_scan_workspace_bytes(cfg, B, T) fits too, the call
+ * also uses the forwarding ring. */
 #define SDM_SCAN_NOALLOC_MAX_BYTES (8u << 20)
 
 /* sdm_scan without a caller workspace, for callers that cannot allocate device
@@ -155,8 +163,8 @@ SDM_API int sdm_scan_run(const sdm_cfg* cfg, const int32_t* idx, const float* ws
  * is the same recurrence as sdm_scan, with the scratch (the collision codes) kept in a
  * library-owned device array of SDM_SCAN_NOALLOC_MAX_BYTES that every GPU loading the
  * library holds until the process exits. Arguments as sdm_scan, minus ws / ws_bytes.
- *  - Returns SDM_EWORKSPACE, before touching the GPU, if sdm_scan_workspace_bytes(cfg, B,
- *    T) exceeds SDM_SCAN_NOALLOC_MAX_BYTES.
+ *  - Returns SDM_EWORKSPACE, before touching the GPU, if sdm_scan_min_workspace_bytes(cfg,
+ *    B, T) exceeds SDM_SCAN_NOALLOC_MAX_BYTES.
  *  - Allocates nothing (no cudaMalloc, cudaFree or allocating library call); it clears
  *    the flags it uses with cudaMemsetAsync on `stream`.
  *  - The first call on a device looks up the array's device address (once per device,

@@ -79,6 +79,7 @@ def lib():
             "sdm_workspace_bytes": ([CP, I, I], S),
             "sdm_address_workspace_bytes": ([CP, L64], S),
             "sdm_scan_workspace_bytes": ([CP, I, I], S),
+            "sdm_scan_min_workspace_bytes": ([CP, I, I], S),
             "sdm_init_bank": ([CP, P, P, I, P], I),
             "sdm_project": ([CP, WP, P, L64, P, P, P, P], I),
             "sdm_address": ([CP, P, P, P, P, L64, P, P, P, S, P, P], I),
@@ -127,6 +128,10 @@ def address_workspace_bytes(cfg: Cfg, ntok: int) -> int:
 
 def scan_workspace_bytes(cfg: Cfg, B: int, T: int) -> int:
     return int(lib().sdm_scan_workspace_bytes(ctypes.byref(cfg), B, T))
+
+
+def scan_min_workspace_bytes(cfg: Cfg, B: int, T: int) -> int:
+    return int(lib().sdm_scan_min_workspace_bytes(ctypes.byref(cfg), B, T))
 
 
 def alloc_workspace(nbytes: int, device=None) -> torch.Tensor:

@@ -8,9 +8,6 @@
 //                          (a+1)(b+1) <= W -- the only pairs that can reach the top-W
 //                          of all n^2 sums -- their top-W, softmax, and the set in
 //                          ascending slot order.
-//   fwd_codes_kernel       for the scan: for every slot reference, the distance to the
-//                          latest earlier write of the same slot within a window and
-//                          its position there (collision forwarding).
 #include <algorithm>
 
 #include "sdm_common.cuh"
@@ -256,120 +253,6 @@ cudaError_t launch_address(const sdm_cfg& c, const void* K1, const void* K2, con
     case 64: return run_cand<16, 2>(c, ntok, hv, hi, idx, wsel, s);    // 280
     default: (void)C; return cudaErrorInvalidValue;
     }
-}
-
-// ----------------------------------------------------------- collision codes
-
-// Block: one sequence b, a run of kCodeTB tokens [t0, t1). Two bitmaps over all N slots
-// are built from the write lists of the window [t0 - kFwdWindow, t1): `once` marks
-// slots written by at least one of those tokens, `twice` slots written by at least
-// two. A read reference whose `once` bit is clear, or a write reference whose `twice`
-// bit is clear (its own token accounts for one write), has no earlier writer within
-// the window: that is the common case and is settled at once. The other references
-// are queued and searched: the sorted write lists of the preceding tokens are
-// binary-searched, newest first. Write references look at tokens t-1, t-2, ...; read
-// references also at t itself (the read follows the write of the same token).
-constexpr int kCodeTB = 32;
-
-__global__ void __launch_bounds__(256) fwd_codes_kernel(const int32_t* __restrict__ idx, int T,
-                                                        int W, int N,
-                                                        uint16_t* __restrict__ codes,
-                                                        int* status)
-{
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    const int nwords = (N + 31) / 32;
-    uint32_t* once = reinterpret_cast<uint32_t*>(smem_raw);
-    uint32_t* twice = once + nwords;
-    int32_t* lists = reinterpret_cast<int32_t*>(twice + nwords);
-    int* queue = lists + (kCodeTB + kFwdWindow) * W;       // [kCodeTB * 2 * W]
-    __shared__ int qn;
-    const int b = blockIdx.y;
-    const int t0 = blockIdx.x * kCodeTB;
-    const int t1 = min(T, t0 + kCodeTB);
-    const int base = max(0, t0 - kFwdWindow);
-    const int nlist = t1 - base;
-    for (int i = threadIdx.x; i < 2 * nwords; i += blockDim.x)
-        once[i] = 0u;
-    if (threadIdx.x == 0)
-        qn = 0;
-    __syncthreads();
-    for (int e = threadIdx.x; e < nlist * W; e += blockDim.x) {
-        const int lt = e / W, j = e % W;
-        const int32_t s = idx[(((size_t)b * T + base + lt) * 2 + 0) * W + j];
-        lists[e] = s;
-        if (s >= 0 && s < N) {
-            const uint32_t m = 1u << (s & 31);
-            if (atomicOr(&once[s >> 5], m) & m)
-                atomicOr(&twice[s >> 5], m);
-        } else {
-            report(status, SDM_ERANGE);
-        }
-    }
-    __syncthreads();
-    const int nref = (t1 - t0) * 2 * W;
-    for (int e = threadIdx.x; e < nref; e += blockDim.x) {
-        const int kind = (e / W) & 1;
-        const size_t o = ((size_t)b * T + t0) * 2 * W + e;
-        const int32_t s = idx[o];
-        bool hit = false;
-        if (s >= 0 && s < N)
-            hit = ((kind ? once : twice)[s >> 5] >> (s & 31)) & 1u;
-        if (hit)
-            queue[atomicAdd(&qn, 1)] = e;
-        else
-            codes[o] = kNoFwd;
-    }
-    __syncthreads();
-    const int nq = qn;
-    for (int qi = threadIdx.x; qi < nq; qi += blockDim.x) {
-        const int e = queue[qi];
-        const int t = t0 + e / (2 * W);
-        const int kind = (e / W) & 1;
-        const size_t o = ((size_t)b * T + t0) * 2 * W + e;
-        const int32_t s = idx[o];
-        uint16_t code = kNoFwd;
-        for (int dt = kind ? 0 : 1; dt <= kFwdWindow; ++dt) {
-            const int tp = t - dt;
-            if (tp < base)
-                break;
-            const int32_t* L = lists + (tp - base) * W;
-            int lo = 0, hi = W - 1, found = -1;
-            while (lo <= hi) {
-                const int mid = (lo + hi) >> 1;
-                const int32_t v = L[mid];
-                if (v == s) { found = mid; break; }
-                if (v < s) lo = mid + 1; else hi = mid - 1;
-            }
-            if (found >= 0) {
-                code = (uint16_t)((dt << 8) | found);
-                break;
-            }
-        }
-        codes[o] = code;
-    }
-}
-
-size_t fwd_codes_smem_bytes(const sdm_cfg& c)
-{
-    const int N = c.n_sub * c.n_sub;
-    return (size_t)2 * ((N + 31) / 32) * 4 + (size_t)(kCodeTB + kFwdWindow) * c.w * 4 +
-           (size_t)kCodeTB * 2 * c.w * 4;
-}
-
-cudaError_t launch_fwd_codes(const sdm_cfg& c, const int32_t* idx, int B, int T,
-                             uint16_t* codes, int* status, cudaStream_t s)
-{
-    if (B <= 0 || T <= 0)
-        return cudaSuccess;
-    const int N = c.n_sub * c.n_sub;
-    const size_t smem = fwd_codes_smem_bytes(c);
-    cudaError_t e = cudaFuncSetAttribute(fwd_codes_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess)
-        return e;
-    dim3 grid((T + kCodeTB - 1) / kCodeTB, B);
-    fwd_codes_kernel<<<grid, 256, smem, s>>>(idx, T, c.w, N, codes, status);
-    return cudaGetLastError();
 }
 
 }  // namespace sdm

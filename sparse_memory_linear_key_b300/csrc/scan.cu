@@ -11,32 +11,42 @@
 //
 // Work unit ("item"): one token of one sequence on one row block -- 1 KB of every slot
 // vector (512 rows in bf16, 256 in fp32). Rows evolve independently, so the row blocks
-// of a sequence are independent streams of tokens. Each item moves 2 x W gathered 1 KB
-// chunks in and W chunks out: random 1 KB chunks are what HBM serves near its copy
-// bandwidth (32-byte gathers reach only about a sixth of it).
+// of a sequence are independent streams of tokens. An item gathers W write chunks and
+// W read chunks of 1 KB and scatters W chunks back: random 1 KB chunks are served by
+// HBM near its copy bandwidth, unlike the 32-byte pieces a finer split would give.
 //
 // Persistent kernel, one CTA per SM, items claimed in increasing order from a global
-// counter (t-major, so every stream advances together). Per CTA:
-//  * a producer warp claims the next item and gathers its W write chunks into the write
-//    buffer and its W read chunks (plus weights and v) into one of two read buffers with
-//    cp.async.bulk, while
-//  * 8 consumer warps compute the current item: they copy the write chunks into
-//    registers (freeing the write buffer for the next item at once), form u, wait for
-//    the write-after-read clearance, store the new slot values straight to HBM, and
-//    reduce the read chunks into y.
+// counter (t-major, so all streams advance together). Warp roles in a CTA:
+//  P   claims the next item, reads its slot ids and codes, and gathers the write chunks
+//      (one buffer) and read chunks (two buffers, alternating items) with cp.async.bulk;
+//  D   copies the chunks whose latest writer is still in flight, from that writer's
+//      forwarding-ring entry, once the writer has published it;
+//  C   16 warps: take the write chunks into registers (freeing the buffer for the next
+//      item), form u and the new values, publish the slots later tokens need into the
+//      ring, reduce the read chunks into y, then store the new values to the bank;
+//  F1  marks the item's bank loads done and clears its bank stores (write after read,
+//      write after write);
+//  F2  publishes the ring entries and then the bank stores.
 // Ordering between tokens of one stream, which may run on different SMs, goes through
-// one progress flag per item in global memory (1 = its chunks are loaded, 2 = its
-// writes are visible):
-//  * read after write: a reference whose latest earlier writer lies within the last
-//    kFwdWindow tokens (from the collision codes) waits for that writer's flag = 2
-//    before its chunk is copied; a read of a slot the same token writes (distance 0) is
-//    not loaded but forwarded from the new values in shared memory;
-//  * write after read: the stores of token t wait until tokens t-kFwdWindow .. t-1 have
-//    loaded (flag >= 1);
-//  * window: token t starts only when tokens t-2*kFwdWindow+1 .. t-kFwdWindow are
-//    committed, so every older writer is visible and every older reader done.
-// Every wait is bounded: on time-out the kernel records SDM_ETIMEOUT, raises a global
-// abort flag that all CTAs watch, waits for its own copies in flight and leaves.
+// one progress flag per item in global memory: 1 = its bank loads are done, 2 = its
+// ring entries are visible, 3 = its bank stores are visible (raised with atomic max, so
+// it never goes down whichever role gets there first).
+//  * read after write: a reference whose latest writer lies within the last `win`
+//    tokens (collision codes) is copied from that writer's ring entry once its flag is
+//    >= 2; a read of a slot the same token writes is forwarded in shared memory; older
+//    writers are visible in the bank (window rule below);
+//  * write after read: the bank stores of token t wait until tokens t-win .. t-1 have
+//    flag >= 1 (bank loads happen first, so this never waits on a dependency);
+//  * write after write: they also wait until each in-window writer of a slot t writes
+//    has flag 3;
+//  * window: token t starts only when tokens t-2*win+1 .. t-win have flag 3; the ring
+//    has 2*win entries per stream, so an entry is reused only when all its readers are
+//    done.
+// Without ring space (a workspace of only min_total bytes) dependent references wait
+// for flag 3 and read the bank.
+// Every wait is bounded: on time-out the kernel records SDM_ETIMEOUT and raises a
+// global abort flag that every warp watches; the warps that issued copies wait for
+// them to land before the CTA ends.
 #include "sdm_common.cuh"
 #include "sdm_internal.h"
 
@@ -44,43 +54,53 @@ namespace sdm {
 
 namespace {
 
-constexpr int kChunk = 1024;       // bytes of one slot's row block
-constexpr int kCWarps = 8;         // consumer warps
-constexpr int kScanThreads = 32 * (kCWarps + 1);
+constexpr int kChunk = 1024;       // bytes of a full row block of one slot
+constexpr int kStride = 1088;      // shared-memory stride between chunks (bank spread)
+constexpr int kCWarps = 16;        // consumer warps
+constexpr int kWarpP = kCWarps, kWarpD = kCWarps + 1, kWarpF1 = kCWarps + 2;
+constexpr int kScanThreads = 32 * (kCWarps + 4);
 constexpr int kMaxW = 64;
+constexpr int kSG = 8;             // slot groups (lanes sharing a row group)
 
 struct ScanArgs {
     unsigned char* banks;
     const int32_t* idx;
     const float* wsel;
     const uint16_t* codes;
+    const unsigned long long* fwdmask;
     const unsigned char* v;
     const float* alpha;
     const float* beta;
     float* y;
     int* status;
-    int* flags;                     // [B][nrb][T] progress of each item
+    int* flags;                     // [B][nrb][T]
     unsigned long long* counter;    // next item to claim
     int* abort_flag;
+    unsigned char* ring;            // null: no forwarding ring
     long long items;                // B * T * nrb
-    int B, T, d, N, nrb, rb_rows;
+    int B, T, d, N, nrb, rb_rows, win, ring_entries, chunk_bytes;
 };
 
-// Everything the consumers need about one item besides the chunks.
+// Everything about one item besides the chunks.
 struct __align__(16) Meta {
     float wsel[2 * kMaxW];          // write weights, then read weights (bulk copy target)
     unsigned char v[kChunk];        // v rows of this row block (bulk copy target)
     int wid[kMaxW];                 // write slot ids, -1 if out of range
-    signed char fpos[kMaxW];        // read ref j: its position in the write set if the
-                                    // token writes that slot itself, else -1
-    unsigned long long fmask;       // bit j: read ref j is such a forwarded slot
+    int rid[kMaxW];                 // read slot ids, -1 if out of range
+    uint16_t code[2 * kMaxW];       // collision codes, write refs then read refs
+    signed char fpos[kMaxW];        // read ref j: position in the write set if own write
+    unsigned long long fmask;       // bit j: read ref j is such a slot
+    unsigned long long fwdmask;     // bit j: write slot j goes to the ring
     long long tok;                  // b * T + t
     int b, t, rb, rows;
     float alpha, beta;
     int valid;                      // 0: no more work
 };
 
-enum { kFullW = 0, kEmptyW = 1, kFullR = 2, kEmptyR = 4, kWar = 6, kCbar = 8, kNumBars = 9 };
+enum {
+    kFullW = 0, kEmptyW = 1, kFullR = 2, kEmptyR = 4, kDepB = 6, kPosted = 8, kWar = 10,
+    kFwdw = 12, kStored = 14, kCbar = 16, kNumBars = 17
+};
 
 template <typename S>
 struct Pack16;
@@ -129,108 +149,168 @@ struct Pack16<float> {
 
 __device__ __forceinline__ int warp_sum(int x) { return __reduce_add_sync(0xFFFFFFFFu, x); }
 
-// ------------------------------------------------------------------ producer warp
+__device__ __forceinline__ bool uniform_wait(uint32_t bar, uint32_t parity, const ScanArgs& a)
+{
+    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, a.abort_flag, a.status));
+}
+
+__device__ __forceinline__ int* item_flag(const ScanArgs& a, int b, int rb, int t)
+{
+    return a.flags + ((long long)b * a.nrb + rb) * a.T + t;
+}
+
+__device__ __forceinline__ unsigned char* ring_entry(const ScanArgs& a, int b, int rb, int t, int pos)
+{
+    const long long e = ((long long)b * a.nrb + rb) * a.ring_entries + t % a.ring_entries;
+    return a.ring + ((size_t)e * kMaxW + pos) * a.chunk_bytes;
+}
+
+// Wait (bounded) until every flag of tokens [lo, hi) of one stream is >= target, reading
+// them all first; the caller follows with fence_acq_rel_gpu().
+__device__ __forceinline__ bool window_geq(const ScanArgs& a, const int* fl, int lo, int hi,
+                                           int target)
+{
+    const int lane = threadIdx.x & 31;
+    lo = max(lo, 0);
+    int got[kMaxWindow / 32];
+#pragma unroll
+    for (int q = 0; q < kMaxWindow / 32; ++q) {
+        const int tt = lo + lane + 32 * q;
+        got[q] = tt < hi ? ld_relaxed_gpu(fl + tt) : target;
+    }
+    bool ok = true;
+#pragma unroll
+    for (int q = 0; q < kMaxWindow / 32; ++q) {
+        const int tt = lo + lane + 32 * q;
+        if (ok && got[q] < target && !spin_geq_gpu(fl + tt, target, a.abort_flag, a.status))
+            ok = false;
+    }
+    return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// ------------------------------------------------------------------ P: gathers
+
+// A claimed item and what the producer needs of it, read one item ahead.
+template <int JW>
+struct Ahead {
+    unsigned long long item;
+    int t, b, rb;
+    int wid[JW], rid[JW];
+    uint16_t wc[JW], rc[JW];
+    float alpha, beta;               // lane 0
+    unsigned long long fwdmask;      // lane 0
+};
+
+template <int W, int JW>
+__device__ __forceinline__ void fetch_ahead(const ScanArgs& a, unsigned long long item, Ahead<JW>& n)
+{
+    const int lane = threadIdx.x & 31;
+    n.item = item;
+    if (item >= (unsigned long long)a.items)
+        return;
+    const long long S_ = (long long)a.B * a.nrb;
+    n.t = (int)(item / S_);
+    const int rem = (int)(item % S_);
+    n.b = rem / a.nrb;
+    n.rb = rem % a.nrb;
+    const long long tok = (long long)n.b * a.T + n.t;
+#pragma unroll
+    for (int jj = 0; jj < JW; ++jj) {
+        const int j = lane + 32 * jj;
+        if (j < W) {
+            n.wid[jj] = __ldg(a.idx + tok * 2 * W + j);
+            n.rid[jj] = __ldg(a.idx + tok * 2 * W + W + j);
+            n.wc[jj] = __ldg(a.codes + tok * 2 * W + j);
+            n.rc[jj] = __ldg(a.codes + tok * 2 * W + W + j);
+        } else {
+            n.wid[jj] = n.rid[jj] = -1;
+            n.wc[jj] = n.rc[jj] = kNoFwd;
+        }
+    }
+    if (lane == 0) {
+        n.alpha = __ldg(a.alpha + tok);
+        n.beta = __ldg(a.beta + tok);
+        n.fwdmask = a.ring != nullptr ? __ldg(a.fwdmask + tok) : 0ull;
+    }
+}
 
 template <typename S, int W>
-__device__ void scan_producer(const ScanArgs& a, unsigned char* wbuf, unsigned char* rbuf,
+__device__ void role_producer(const ScanArgs& a, unsigned char* wbuf, unsigned char* rbuf,
                               Meta* meta, uint64_t* bars)
 {
     constexpr int JW = (W + 31) / 32;
     const int lane = threadIdx.x & 31;
     const uint32_t fullW = smem_u32(bars + kFullW), emptyW = smem_u32(bars + kEmptyW);
-    int armedW = -1, armedR[2] = {-1, -1};  // item sequence numbers whose phases were armed
+    int armedW = -1, armedR[2] = {-1, -1};  // item numbers whose full phases were armed
     uint32_t missW = 0, missR = 0;          // this lane's counted-but-unissued bytes
     bool ok = true;
+    Ahead<JW> nx;
+    {
+        unsigned long long item = 0;
+        if (lane == 0)
+            item = atomicAdd(a.counter, 1ull);
+        fetch_ahead<W, JW>(a, __shfl_sync(0xFFFFFFFFu, item, 0), nx);
+    }
     int k = 0;
     for (;; ++k) {
         const int p = k & 1;
         const uint32_t fullR = smem_u32(bars + kFullR + p), emptyR = smem_u32(bars + kEmptyR + p);
         Meta& m = meta[p];
-        unsigned char* rb_buf = rbuf + (size_t)p * W * kChunk;
-        unsigned long long item = 0;
-        int aborted = 0;
-        if (lane == 0) {
-            item = atomicAdd(a.counter, 1ull);
-            aborted = ld_relaxed_gpu(a.abort_flag);
-        }
-        item = __shfl_sync(0xFFFFFFFFu, item, 0);
+        unsigned char* rb_buf = rbuf + (size_t)p * W * kStride;
+        int aborted = lane == 0 ? ld_relaxed_gpu(a.abort_flag) : 0;
         aborted = __shfl_sync(0xFFFFFFFFu, aborted, 0);
-        if (item >= (unsigned long long)a.items || aborted != 0) {
-            // end of work: hand the consumers an empty item
-            ok = mbar_wait(emptyW, (k & 1) ^ 1, a.abort_flag, a.status) &&
-                 mbar_wait(emptyR, ((k >> 1) & 1) ^ 1, a.abort_flag, a.status);
-            ok = __all_sync(0xFFFFFFFFu, ok);
+        if (nx.item >= (unsigned long long)a.items || aborted != 0) {
+            // end of work: hand every role an empty item
+            ok = uniform_wait(emptyW, (k & 1) ^ 1, a) &&
+                 uniform_wait(emptyR, ((k >> 1) & 1) ^ 1, a);
             if (ok && lane == 0) {
                 m.valid = 0;
                 mbar_arrive(fullW);
                 mbar_arrive(fullR);
+                mbar_arrive(smem_u32(bars + kPosted + p));
             }
             break;
         }
-        const long long S_ = (long long)a.B * a.nrb;
-        const int t = (int)(item / S_);
-        const int rem = (int)(item % S_);
-        const int b = rem / a.nrb, rb = rem % a.nrb;
+        const int t = nx.t, b = nx.b, rb = nx.rb;
         const long long tok = (long long)b * a.T + t;
         const int rows = min(a.rb_rows, a.d - rb * a.rb_rows);
         const uint32_t cb = (uint32_t)rows * (uint32_t)sizeof(S);
-        const int* fl = a.flags + ((long long)b * a.nrb + rb) * a.T;
+        const int* fl = item_flag(a, b, rb, 0);
         const unsigned char* bank =
             a.banks + ((size_t)b * a.N * a.d + (size_t)rb * a.rb_rows) * sizeof(S);
         const size_t slot_bytes = (size_t)a.d * sizeof(S);
 
-        // slot ids and collision codes of this token
-        int wid[JW], rid[JW];
-        uint16_t wc[JW], rc[JW];
-        bool has[JW];
-#pragma unroll
-        for (int jj = 0; jj < JW; ++jj) {
-            const int j = lane + 32 * jj;
-            has[jj] = j < W;
-            if (has[jj]) {
-                wid[jj] = __ldg(a.idx + tok * 2 * W + j);
-                rid[jj] = __ldg(a.idx + tok * 2 * W + W + j);
-                wc[jj] = __ldg(a.codes + tok * 2 * W + j);
-                rc[jj] = __ldg(a.codes + tok * 2 * W + W + j);
-            } else {
-                wid[jj] = rid[jj] = -1;
-                wc[jj] = rc[jj] = kNoFwd;
-            }
-        }
-        // window: tokens t-2*win+1 .. t-win of this stream committed
-        {
-            int got[kFwdWindow / 32];
-#pragma unroll
-            for (int q = 0; q < kFwdWindow / 32; ++q) {
-                const int tt = t - kFwdWindow - lane - 32 * q;
-                got[q] = (tt >= 0 && tt > t - 2 * kFwdWindow) ? ld_relaxed_gpu(fl + tt) : 2;
-            }
-#pragma unroll
-            for (int q = 0; q < kFwdWindow / 32; ++q) {
-                const int tt = t - kFwdWindow - lane - 32 * q;
-                if (got[q] < 2 && !spin_geq_gpu(fl + tt, 2, a.abort_flag, a.status))
-                    ok = false;
-            }
-            fence_acq_rel_gpu();
-            fence_proxy_async_global();
-        }
-        if (__any_sync(0xFFFFFFFFu, !ok))
-            break;
-
-        // ---- write chunks
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(emptyW, (k & 1) ^ 1, a.abort_flag, a.status))) {
+        // window: tokens t-2*win+1 .. t-win of this stream are committed
+        if (!window_geq(a, fl, t - 2 * a.win + 1, t - a.win + 1, 3)) {
             ok = false;
             break;
         }
-        bool wval[JW], wdep[JW];
-        int nW = 0;
+        fence_acq_rel_gpu();
+        fence_proxy_async_global();
+
+        bool wval[JW], wdep[JW], rval[JW], rdep[JW], rown[JW];
+        int nW = 0, nR = 0;
+        unsigned long long fmask = 0;
 #pragma unroll
         for (int jj = 0; jj < JW; ++jj) {
-            wval[jj] = has[jj] && wid[jj] >= 0 && wid[jj] < a.N;
-            if (has[jj] && !wval[jj])
+            const bool has = lane + 32 * jj < W;
+            wval[jj] = has && nx.wid[jj] >= 0 && nx.wid[jj] < a.N;
+            rval[jj] = has && nx.rid[jj] >= 0 && nx.rid[jj] < a.N;
+            if ((has && !wval[jj]) || (has && !rval[jj]))
                 report(a.status, SDM_ERANGE);
-            wdep[jj] = wval[jj] && wc[jj] != kNoFwd;  // an earlier writer within the window
-            nW += wval[jj] ? 1 : 0;
+            wdep[jj] = wval[jj] && nx.wc[jj] != kNoFwd;  // an in-window writer: D copies it
+            const int dt = nx.rc[jj] >> 8;
+            rown[jj] = rval[jj] && nx.rc[jj] != kNoFwd && dt == 0;
+            rdep[jj] = rval[jj] && nx.rc[jj] != kNoFwd && dt > 0;
+            nW += (wval[jj] && !wdep[jj]) ? 1 : 0;
+            nR += (rval[jj] && !rown[jj] && !rdep[jj]) ? 1 : 0;
+            fmask |= (unsigned long long)__ballot_sync(0xFFFFFFFFu, rown[jj]) << (32 * jj);
+        }
+
+        // ---- write chunks, as soon as the consumers have taken the previous ones
+        if (!uniform_wait(emptyW, (k & 1) ^ 1, a)) {
+            ok = false;
+            break;
         }
         missW = (uint32_t)nW * cb;
         const int totW = warp_sum(nW);
@@ -241,48 +321,39 @@ __device__ void scan_producer(const ScanArgs& a, unsigned char* wbuf, unsigned c
 #pragma unroll
         for (int jj = 0; jj < JW; ++jj)
             if (wval[jj] && !wdep[jj]) {
-                bulk_g2s(smem_u32(wbuf + (size_t)(lane + 32 * jj) * kChunk),
-                         bank + (size_t)wid[jj] * slot_bytes, cb, fullW);
+                bulk_g2s(smem_u32(wbuf + (size_t)(lane + 32 * jj) * kStride),
+                         bank + (size_t)nx.wid[jj] * slot_bytes, cb, fullW);
                 missW -= cb;
             }
 
-        // ---- read chunks, weights and v
-        if (!__all_sync(0xFFFFFFFFu,
-                        mbar_wait(emptyR, ((k >> 1) & 1) ^ 1, a.abort_flag, a.status))) {
+        // ---- item description, read chunks, weights and v
+        if (!uniform_wait(emptyR, ((k >> 1) & 1) ^ 1, a)) {
             ok = false;
             break;
         }
-        bool rval[JW], rdep[JW], rown[JW];
-        int nR = 0;
-        unsigned long long fmask = 0;
 #pragma unroll
         for (int jj = 0; jj < JW; ++jj) {
             const int j = lane + 32 * jj;
-            rval[jj] = has[jj] && rid[jj] >= 0 && rid[jj] < a.N;
-            if (has[jj] && !rval[jj])
-                report(a.status, SDM_ERANGE);
-            const int dt = rc[jj] >> 8;
-            rown[jj] = rval[jj] && rc[jj] != kNoFwd && dt == 0;
-            rdep[jj] = rval[jj] && rc[jj] != kNoFwd && dt > 0;
-            nR += (rval[jj] && !rown[jj]) ? 1 : 0;
-            if (has[jj]) {
-                m.wid[j] = wval[jj] ? wid[jj] : -1;
-                m.fpos[j] = rown[jj] ? (signed char)(rc[jj] & 0xFF) : (signed char)-1;
+            if (j < W) {
+                m.wid[j] = wval[jj] ? nx.wid[jj] : -1;
+                m.rid[j] = rval[jj] ? nx.rid[jj] : -1;
+                m.code[j] = nx.wc[jj];
+                m.code[W + j] = nx.rc[jj];
+                m.fpos[j] = rown[jj] ? (signed char)(nx.rc[jj] & 0xFF) : (signed char)-1;
             }
-            const unsigned bal = __ballot_sync(0xFFFFFFFFu, rown[jj]);
-            fmask |= (unsigned long long)bal << (32 * jj);
         }
         missR = (uint32_t)nR * cb;
         const int totR = warp_sum(nR);
         if (lane == 0) {
             m.fmask = fmask;
+            m.fwdmask = nx.fwdmask;
             m.tok = tok;
             m.b = b;
             m.t = t;
             m.rb = rb;
             m.rows = rows;
-            m.alpha = __ldg(a.alpha + tok);
-            m.beta = __ldg(a.beta + tok);
+            m.alpha = nx.alpha;
+            m.beta = nx.beta;
             m.valid = 1;
         }
         __syncwarp();
@@ -298,72 +369,26 @@ __device__ void scan_producer(const ScanArgs& a, unsigned char* wbuf, unsigned c
 #pragma unroll
         for (int jj = 0; jj < JW; ++jj)
             if (rval[jj] && !rown[jj] && !rdep[jj]) {
-                bulk_g2s(smem_u32(rb_buf + (size_t)(lane + 32 * jj) * kChunk),
-                         bank + (size_t)rid[jj] * slot_bytes, cb, fullR);
+                bulk_g2s(smem_u32(rb_buf + (size_t)(lane + 32 * jj) * kStride),
+                         bank + (size_t)nx.rid[jj] * slot_bytes, cb, fullR);
                 missR -= cb;
             }
-
-        // ---- chunks whose latest writer is still in the window: wait for its commit
-#pragma unroll
-        for (int jj = 0; jj < JW; ++jj)
-            if (ok && wdep[jj]) {
-                const int tw = t - (wc[jj] >> 8);
-                if (spin_geq_gpu(fl + tw, 2, a.abort_flag, a.status)) {
-                    fence_acq_rel_gpu();
-                    fence_proxy_async_global();
-                    bulk_g2s(smem_u32(wbuf + (size_t)(lane + 32 * jj) * kChunk),
-                             bank + (size_t)wid[jj] * slot_bytes, cb, fullW);
-                    missW -= cb;
-                } else {
-                    ok = false;
-                }
-            }
-#pragma unroll
-        for (int jj = 0; jj < JW; ++jj)
-            if (ok && rdep[jj]) {
-                const int tw = t - (rc[jj] >> 8);
-                if (spin_geq_gpu(fl + tw, 2, a.abort_flag, a.status)) {
-                    fence_acq_rel_gpu();
-                    fence_proxy_async_global();
-                    bulk_g2s(smem_u32(rb_buf + (size_t)(lane + 32 * jj) * kChunk),
-                             bank + (size_t)rid[jj] * slot_bytes, cb, fullR);
-                    missR -= cb;
-                } else {
-                    ok = false;
-                }
-            }
-        if (__any_sync(0xFFFFFFFFu, !ok))
-            break;
-
-        // ---- write after read: tokens t-win .. t-1 of this stream have loaded
-        {
-            int got[kFwdWindow / 32];
-#pragma unroll
-            for (int q = 0; q < kFwdWindow / 32; ++q) {
-                const int tt = t - 1 - lane - 32 * q;
-                got[q] = tt >= 0 ? ld_relaxed_gpu(fl + tt) : 1;
-            }
-#pragma unroll
-            for (int q = 0; q < kFwdWindow / 32; ++q) {
-                const int tt = t - 1 - lane - 32 * q;
-                if (got[q] < 1 && !spin_geq_gpu(fl + tt, 1, a.abort_flag, a.status))
-                    ok = false;
-            }
-            fence_acq_rel_gpu();
-        }
-        if (__any_sync(0xFFFFFFFFu, !ok))
-            break;
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(smem_u32(bars + kWar + p));
+            mbar_arrive(smem_u32(bars + kPosted + p));  // D may start on this item
         missW = missR = 0;
+
+        // ---- the next item
+        unsigned long long next = 0;
+        if (lane == 0)
+            next = atomicAdd(a.counter, 1ull);
+        fetch_ahead<W, JW>(a, __shfl_sync(0xFFFFFFFFu, next, 0), nx);
     }
     if (__all_sync(0xFFFFFFFFu, ok))
         return;
-    // Failure (time-out or abort): declare the bytes that were counted but never
-    // copied, then wait, boundedly, for the copies that are in flight into this CTA's
-    // shared memory before the CTA may end.
-    if (ld_relaxed_gpu(a.abort_flag) == 0)
+    // Failure: declare the bytes that were counted but never copied, then wait
+    // (bounded) for the copies in flight into this CTA's shared memory.
+    if (lane == 0)
         st_relaxed_gpu(a.abort_flag, 1);
     const int mw = warp_sum((int)missW), mr = warp_sum((int)missR);
     const int p = k & 1;
@@ -381,23 +406,184 @@ __device__ void scan_producer(const ScanArgs& a, unsigned char* wbuf, unsigned c
     __syncwarp();
 }
 
-// ---------------------------------------------------------------- consumer warps
+// ------------------------------------------------------- D: in-flight dependencies
 
 template <typename S, int W>
-__device__ void scan_consumer(const ScanArgs& a, const unsigned char* wbuf, unsigned char* rbuf,
+__device__ void role_deps(const ScanArgs& a, unsigned char* wbuf, unsigned char* rbuf,
+                          const Meta* meta, uint64_t* bars)
+{
+    constexpr int JR = (2 * W + 31) / 32;   // references per lane
+    const int lane = threadIdx.x & 31;
+    const int need = a.ring != nullptr ? 2 : 3;
+    for (int k = 0;; ++k) {
+        const int p = k & 1;
+        if (!uniform_wait(smem_u32(bars + kPosted + p), (k >> 1) & 1, a))
+            return;
+        const Meta& m = meta[p];
+        if (!m.valid)
+            return;
+        const uint32_t depB = smem_u32(bars + kDepB + p);
+        const uint32_t cb = (uint32_t)m.rows * (uint32_t)sizeof(S);
+        const int t = m.t, b = m.b, rb = m.rb;
+        const int* fl = item_flag(a, b, rb, 0);
+        bool dep[JR];
+        int n = 0;
+#pragma unroll
+        for (int q = 0; q < JR; ++q) {
+            const int r = lane + 32 * q;
+            dep[q] = false;
+            if (r < 2 * W) {
+                const uint16_t c = m.code[r];
+                const int id = r < W ? m.wid[r] : m.rid[r - W];
+                dep[q] = id >= 0 && c != kNoFwd && (c >> 8) > 0;
+            }
+            n += dep[q] ? 1 : 0;
+        }
+        const int tot = warp_sum(n);
+        if (lane == 0)
+            mbar_arrive_expect_tx(depB, (uint32_t)tot * cb);
+        __syncwarp();
+        uint32_t miss = (uint32_t)n * cb;
+        // read the writers' flags together, then wait for the ones not yet published
+        int got[JR];
+#pragma unroll
+        for (int q = 0; q < JR; ++q)
+            got[q] = dep[q] ? ld_relaxed_gpu(fl + t - (m.code[lane + 32 * q] >> 8)) : need;
+        bool ok = true;
+#pragma unroll
+        for (int q = 0; q < JR; ++q) {
+            if (!dep[q] || !ok)
+                continue;
+            const int r = lane + 32 * q;
+            const uint16_t c = m.code[r];
+            const int tw = t - (c >> 8);
+            if (got[q] < need && !spin_geq_gpu(fl + tw, need, a.abort_flag, a.status)) {
+                ok = false;
+                continue;
+            }
+            fence_acq_rel_gpu();
+            fence_proxy_async_global();
+            const bool is_w = r < W;
+            const int j = is_w ? r : r - W;
+            const unsigned char* src;
+            if (a.ring != nullptr) {
+                src = ring_entry(a, b, rb, tw, c & 0xFF);
+            } else {
+                const int id = is_w ? m.wid[j] : m.rid[j];
+                src = a.banks + (((size_t)b * a.N + id) * a.d + (size_t)rb * a.rb_rows) * sizeof(S);
+            }
+            unsigned char* dst = (is_w ? wbuf : rbuf + (size_t)p * W * kStride) + (size_t)j * kStride;
+            bulk_g2s(smem_u32(dst), src, cb, depB);
+            miss -= cb;
+        }
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+            // declare what was not copied, wait (bounded) for what was, and leave
+            if (lane == 0)
+                st_relaxed_gpu(a.abort_flag, 1);
+            const int mm = warp_sum((int)miss);
+            if (lane == 0) {
+                if (mm > 0)
+                    mbar_complete_tx(depB, (uint32_t)mm);
+                mbar_wait(depB, (k >> 1) & 1, nullptr, a.status);
+            }
+            __syncwarp();
+            return;
+        }
+    }
+}
+
+// ------------------------------------------------------------ F1: loads done, clearance
+
+template <int W>
+__device__ void role_clear(const ScanArgs& a, const Meta* meta, uint64_t* bars)
+{
+    constexpr int JW = (W + 31) / 32;
+    const int lane = threadIdx.x & 31;
+    for (int k = 0;; ++k) {
+        const int p = k & 1;
+        if (!uniform_wait(smem_u32(bars + kFullW), k & 1, a) ||
+            !uniform_wait(smem_u32(bars + kFullR + p), (k >> 1) & 1, a))
+            return;
+        const Meta& m = meta[p];
+        if (!m.valid)
+            return;
+        const int t = m.t;
+        const int* fl = item_flag(a, m.b, m.rb, 0);
+        int wdt[JW];
+#pragma unroll
+        for (int jj = 0; jj < JW; ++jj) {
+            const int j = lane + 32 * jj;
+            const uint16_t c = j < W ? m.code[j] : kNoFwd;
+            wdt[jj] = (j < W && m.wid[j] >= 0 && c != kNoFwd) ? (c >> 8) : 0;
+        }
+        // without the ring, dependent references are bank loads too
+        if (a.ring == nullptr && !uniform_wait(smem_u32(bars + kDepB + p), (k >> 1) & 1, a))
+            return;
+        if (lane == 0)
+            red_max_release_gpu(item_flag(a, m.b, m.rb, t), 1);  // bank loads done
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(bars + kEmptyW));
+        // write after read: tokens t-win .. t-1 have done their bank loads
+        bool ok = window_geq(a, fl, t - a.win, t, 1);
+        // write after write: in-window writers of our write slots have stored
+#pragma unroll
+        for (int jj = 0; jj < JW; ++jj)
+            if (ok && wdt[jj] > 0 && !spin_geq_gpu(fl + t - wdt[jj], 3, a.abort_flag, a.status))
+                ok = false;
+        if (!__all_sync(0xFFFFFFFFu, ok))
+            return;
+        fence_acq_rel_gpu();
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(smem_u32(bars + kWar + p));
+            mbar_arrive(smem_u32(bars + kEmptyR + p));
+        }
+    }
+}
+
+// -------------------------------------------------------------- F2: publication
+
+__device__ void role_publish(const ScanArgs& a, const Meta* meta, uint64_t* bars)
+{
+    const int lane = threadIdx.x & 31;
+    for (int k = 0;; ++k) {
+        const int p = k & 1;
+        if (!uniform_wait(smem_u32(bars + kFullR + p), (k >> 1) & 1, a))
+            return;
+        const Meta& m = meta[p];
+        if (!m.valid)
+            return;
+        int* flag = item_flag(a, m.b, m.rb, m.t);
+        if (!uniform_wait(smem_u32(bars + kFwdw + p), (k >> 1) & 1, a))
+            return;
+        if (lane == 0)
+            red_max_release_gpu(flag, 2);  // ring entries visible
+        if (!uniform_wait(smem_u32(bars + kStored + p), (k >> 1) & 1, a))
+            return;
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(smem_u32(bars + kEmptyR + p));
+            red_max_release_gpu(flag, 3);  // bank stores visible
+        }
+    }
+}
+
+// ---------------------------------------------------------------- C: consumers
+
+template <typename S, int W>
+__device__ void role_consumer(const ScanArgs& a, const unsigned char* wbuf, unsigned char* rbuf,
                               const Meta* meta, uint64_t* bars)
 {
-    constexpr int SPL = W / 4;         // slots of each set per thread
+    constexpr int SPL = W / kSG;       // slots of each set per thread: i*8 + sg
     using P = Pack16<S>;
     constexpr int RPL = P::R;          // rows per thread (16 bytes)
     const int ct = threadIdx.x, w = ct >> 5, lane = ct & 31;
-    const int sg = lane >> 3;          // slot group: slots sg*SPL .. sg*SPL + SPL - 1
-    const int rg = w * 8 + (lane & 7); // row group: rows rg*RPL .. rg*RPL + RPL - 1
-    const uint32_t fullW = smem_u32(bars + kFullW), emptyW = smem_u32(bars + kEmptyW);
+    const int sg = lane >> 2;          // slot group
+    const int rg = w * 4 + (lane & 3); // row group: rows rg*RPL .. rg*RPL + RPL - 1
     const uint32_t cbar = smem_u32(bars + kCbar);
-    // Barrier of the consumer warps (one arrival per warp). Every exit below is taken
-    // by whole warps (the wait outcomes are made warp-uniform), and a warp that is
-    // left waiting here gives up after the bounded wait, so no warp can hang.
+    // Barrier of the consumer warps (one arrival per warp). Exits are taken by whole
+    // warps, and a warp left waiting here gives up after the bounded wait.
     int cuses = 0;
     auto consumer_barrier = [&]() -> bool {
         __syncwarp();
@@ -409,37 +595,34 @@ __device__ void scan_consumer(const ScanArgs& a, const unsigned char* wbuf, unsi
     };
     for (int k = 0;; ++k) {
         const int p = k & 1;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(fullW, k & 1, a.abort_flag, a.status)))
-            return;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(bars + kFullR + p), (k >> 1) & 1,
-                                               a.abort_flag, a.status)))
+        if (!uniform_wait(smem_u32(bars + kFullW), k & 1, a) ||
+            !uniform_wait(smem_u32(bars + kFullR + p), (k >> 1) & 1, a))
             return;
         const Meta& m = meta[p];
         if (!m.valid)
             return;
-        const unsigned char* rb_buf = rbuf + (size_t)p * W * kChunk;
+        if (!uniform_wait(smem_u32(bars + kDepB + p), (k >> 1) & 1, a))
+            return;
+        unsigned char* rb_buf = rbuf + (size_t)p * W * kStride;
         const bool act = rg * 16 < m.rows * (int)sizeof(S);
         uint4 Mv[SPL];
 #pragma unroll
         for (int i = 0; i < SPL; ++i)
-            Mv[i] = act ? *reinterpret_cast<const uint4*>(wbuf + (size_t)(sg * SPL + i) * kChunk +
+            Mv[i] = act ? *reinterpret_cast<const uint4*>(wbuf + (size_t)(i * kSG + sg) * kStride +
                                                           rg * 16)
                         : make_uint4(0, 0, 0, 0);
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(emptyW);
-        int* flag = a.flags + ((long long)m.b * a.nrb + m.rb) * a.T + m.t;
-        if (ct == 0)
-            st_release_gpu(flag, 1);  // this token's chunks are loaded
+            mbar_arrive(smem_u32(bars + kEmptyW));
 
-        // u = M_S k (pre-write), reduced over the four slot groups
+        // u = M_S k (pre-write), reduced over the slot groups
         float u[RPL];
 #pragma unroll
         for (int r = 0; r < RPL; ++r)
             u[r] = 0.f;
 #pragma unroll
         for (int i = 0; i < SPL; ++i) {
-            const float kw = m.wsel[sg * SPL + i];
+            const float kw = m.wsel[i * kSG + sg];
             float f[RPL];
             P::unpack(Mv[i], f);
 #pragma unroll
@@ -448,6 +631,7 @@ __device__ void scan_consumer(const ScanArgs& a, const unsigned char* wbuf, unsi
         }
 #pragma unroll
         for (int r = 0; r < RPL; ++r) {
+            u[r] += __shfl_xor_sync(0xFFFFFFFFu, u[r], 4);
             u[r] += __shfl_xor_sync(0xFFFFFFFFu, u[r], 8);
             u[r] += __shfl_xor_sync(0xFFFFFFFFu, u[r], 16);
         }
@@ -458,39 +642,46 @@ __device__ void scan_consumer(const ScanArgs& a, const unsigned char* wbuf, unsi
 #pragma unroll
         for (int r = 0; r < RPL; ++r)
             c[r] = be * (vv[r] - al * u[r]);
-
-        // M[S_j] <- alpha M[S_j] + k_j beta (v - alpha u), rounded once, stored
-        if (!__all_sync(0xFFFFFFFFu,
-                        mbar_wait(smem_u32(bars + kWar + p), (k >> 1) & 1, a.abort_flag, a.status)))
-            return;
-        S* bank = reinterpret_cast<S*>(a.banks) + (size_t)m.b * a.N * a.d +
-                  (size_t)m.rb * a.rb_rows + rg * RPL;
+        // M[S_j] <- alpha M[S_j] + k_j beta (v - alpha u), rounded once
 #pragma unroll
         for (int i = 0; i < SPL; ++i) {
-            const float kw = m.wsel[sg * SPL + i];
+            const float kw = m.wsel[i * kSG + sg];
             float f[RPL];
             P::unpack(Mv[i], f);
 #pragma unroll
             for (int r = 0; r < RPL; ++r)
                 f[r] = fmaf(kw, c[r], al * f[r]);
             Mv[i] = P::pack(f);
-            const int id = m.wid[sg * SPL + i];
-            if (act && id >= 0)
-                __stcg(reinterpret_cast<uint4*>(bank + (size_t)id * a.d), Mv[i]);
         }
-        // read slots this token writes itself: their new values, from registers
-        const unsigned long long fm0 = m.fmask;
-        if (fm0 != 0) {
-            unsigned long long fm = fm0;
-            while (fm != 0) {
-                const int j = __ffsll((long long)fm) - 1;
-                fm &= fm - 1;
-                const int q = m.fpos[j];
+        // slots that later tokens read while this one may be in flight: to the ring
+        const unsigned long long fw = m.fwdmask;
+        if (fw != 0) {
+            unsigned long long q = fw;
+            while (q != 0) {
+                const int j = __ffsll((long long)q) - 1;
+                q &= q - 1;
 #pragma unroll
                 for (int i = 0; i < SPL; ++i)
-                    if (act && q == sg * SPL + i)
-                        *reinterpret_cast<uint4*>(rbuf + (size_t)p * W * kChunk +
-                                                  (size_t)j * kChunk + rg * 16) = Mv[i];
+                    if (act && j == i * kSG + sg)
+                        __stcg(reinterpret_cast<uint4*>(ring_entry(a, m.b, m.rb, m.t, j) + rg * 16),
+                               Mv[i]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(bars + kFwdw + p));
+        // read slots this token writes itself: their new values, from registers
+        const unsigned long long fm = m.fmask;
+        if (fm != 0) {
+            unsigned long long q = fm;
+            while (q != 0) {
+                const int j = __ffsll((long long)q) - 1;
+                q &= q - 1;
+                const int pos = m.fpos[j];
+#pragma unroll
+                for (int i = 0; i < SPL; ++i)
+                    if (act && pos == i * kSG + sg)
+                        *reinterpret_cast<uint4*>(rb_buf + (size_t)j * kStride + rg * 16) = Mv[i];
             }
             if (!consumer_barrier())
                 return;
@@ -503,9 +694,9 @@ __device__ void scan_consumer(const ScanArgs& a, const unsigned char* wbuf, unsi
             yv[r] = 0.f;
 #pragma unroll
         for (int i = 0; i < SPL; ++i) {
-            const float rw = m.wsel[W + sg * SPL + i];
+            const float rw = m.wsel[W + i * kSG + sg];
             float f[RPL];
-            P::unpack(act ? *reinterpret_cast<const uint4*>(rb_buf + (size_t)(sg * SPL + i) * kChunk +
+            P::unpack(act ? *reinterpret_cast<const uint4*>(rb_buf + (size_t)(i * kSG + sg) * kStride +
                                                             rg * 16)
                           : make_uint4(0, 0, 0, 0),
                       f);
@@ -515,6 +706,7 @@ __device__ void scan_consumer(const ScanArgs& a, const unsigned char* wbuf, unsi
         }
 #pragma unroll
         for (int r = 0; r < RPL; ++r) {
+            yv[r] += __shfl_xor_sync(0xFFFFFFFFu, yv[r], 4);
             yv[r] += __shfl_xor_sync(0xFFFFFFFFu, yv[r], 8);
             yv[r] += __shfl_xor_sync(0xFFFFFFFFu, yv[r], 16);
         }
@@ -525,18 +717,23 @@ __device__ void scan_consumer(const ScanArgs& a, const unsigned char* wbuf, unsi
                 __stcs(reinterpret_cast<float4*>(yp + r),
                        make_float4(yv[r], yv[r + 1], yv[r + 2], yv[r + 3]));
         }
+        if (fm != 0)
+            fence_proxy_async_shared();  // this buffer is refilled by bulk copies later
 
-        // commit: every consumer's stores visible, then the flag
-        __threadfence();
-        if (!consumer_barrier())
+        // bank stores, once cleared
+        if (!uniform_wait(smem_u32(bars + kWar + p), (k >> 1) & 1, a))
             return;
-        if (ct == 0)
-            st_release_gpu(flag, 2);
-        if (fm0 != 0)
-            fence_proxy_async_shared();
+        S* bank = reinterpret_cast<S*>(a.banks) + (size_t)m.b * a.N * a.d +
+                  (size_t)m.rb * a.rb_rows + rg * RPL;
+#pragma unroll
+        for (int i = 0; i < SPL; ++i) {
+            const int id = m.wid[i * kSG + sg];
+            if (act && id >= 0)
+                __stcg(reinterpret_cast<uint4*>(bank + (size_t)id * a.d), Mv[i]);
+        }
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(smem_u32(bars + kEmptyR + p));
+            mbar_arrive(smem_u32(bars + kStored + p));
     }
 }
 
@@ -545,31 +742,42 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a)
 {
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* wbuf = smem;
-    unsigned char* rbuf = smem + (size_t)W * kChunk;
-    Meta* meta = reinterpret_cast<Meta*>(smem + (size_t)3 * W * kChunk);
+    unsigned char* rbuf = smem + (size_t)W * kStride;
+    Meta* meta = reinterpret_cast<Meta*>(smem + (size_t)3 * W * kStride);
     uint64_t* bars = reinterpret_cast<uint64_t*>(meta + 2);
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(bars + kFullW), 1);
-        mbar_init(smem_u32(bars + kEmptyW), kCWarps);
+        mbar_init(smem_u32(bars + kEmptyW), kCWarps + 1);   // consumers + F1
         for (int p = 0; p < 2; ++p) {
             mbar_init(smem_u32(bars + kFullR + p), 1);
-            mbar_init(smem_u32(bars + kEmptyR + p), kCWarps);
+            mbar_init(smem_u32(bars + kEmptyR + p), 2);     // F1 + F2
+            mbar_init(smem_u32(bars + kDepB + p), 1);
+            mbar_init(smem_u32(bars + kPosted + p), 1);
             mbar_init(smem_u32(bars + kWar + p), 1);
+            mbar_init(smem_u32(bars + kFwdw + p), kCWarps);
+            mbar_init(smem_u32(bars + kStored + p), kCWarps);
         }
         mbar_init(smem_u32(bars + kCbar), kCWarps);
         fence_mbarrier_init();
     }
     __syncthreads();
-    if (threadIdx.x >= 32 * kCWarps)
-        scan_producer<S, W>(a, wbuf, rbuf, meta, bars);
+    const int warp = threadIdx.x >> 5;
+    if (warp < kCWarps)
+        role_consumer<S, W>(a, wbuf, rbuf, meta, bars);
+    else if (warp == kWarpP)
+        role_producer<S, W>(a, wbuf, rbuf, meta, bars);
+    else if (warp == kWarpD)
+        role_deps<S, W>(a, wbuf, rbuf, meta, bars);
+    else if (warp == kWarpF1)
+        role_clear<W>(a, meta, bars);
     else
-        scan_consumer<S, W>(a, wbuf, rbuf, meta, bars);
+        role_publish(a, meta, bars);
 }
 
 template <typename S, int W>
 cudaError_t launch_scan_t(const ScanArgs& a, cudaStream_t s)
 {
-    const size_t smem = (size_t)3 * W * kChunk + 2 * sizeof(Meta) + kNumBars * sizeof(uint64_t);
+    const size_t smem = (size_t)3 * W * kStride + 2 * sizeof(Meta) + kNumBars * sizeof(uint64_t);
     auto kern = scan_kernel<S, W>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
@@ -584,55 +792,81 @@ cudaError_t launch_scan_t(const ScanArgs& a, cudaStream_t s)
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
+long long pow2_ceil(long long x)
+{
+    long long p = 1;
+    while (p < x)
+        p *= 2;
+    return p;
+}
+
 }  // namespace
 
-int scan_block_rows(const sdm_cfg& c)
+ScanWs scan_ws_layout(const sdm_cfg& c, int B, int T)
 {
+    ScanWs L{};
     const int es = c.dtype == SDM_BF16 ? 2 : 4;
-    return kChunk / es;
+    L.rb_rows = kChunk / es;
+    L.nrb = (c.d + L.rb_rows - 1) / L.rb_rows;
+    L.chunk_bytes = (c.d < L.rb_rows ? c.d : L.rb_rows) * es;
+    // Window: room for about twice the tokens of one stream the grid keeps in flight
+    // (one CTA per SM, about two items each), between 16 and kMaxWindow tokens.
+    const long long streams = (long long)(B > 0 ? B : 1) * L.nrb;
+    const long long inflight = (2LL * num_sms_current_device() + streams - 1) / streams;
+    long long win = pow2_ceil(2 * inflight);
+    if (win < 16)
+        win = 16;
+    if (win > kMaxWindow)
+        win = kMaxWindow;
+    L.win = (int)win;
+    L.ring_entries = T < 2 * L.win ? (T > 0 ? T : 1) : 2 * L.win;
+    size_t o = 0;
+    L.codes = o; o += align256((size_t)B * T * 2 * c.w * 2);
+    L.fwdmask = o; o += align256((size_t)B * T * 8);
+    L.flags = o; L.flags_bytes = align256((size_t)B * L.nrb * T * 4) + 256; o += L.flags_bytes;
+    L.min_total = o;
+    L.ring = o;
+    L.ring_bytes = (size_t)B * L.nrb * L.ring_entries * kMaxW * L.chunk_bytes;
+    o += align256(L.ring_bytes);
+    L.total = o;
+    return L;
 }
 
-int scan_row_blocks(const sdm_cfg& c)
-{
-    const int r = scan_block_rows(c);
-    return (c.d + r - 1) / r;
-}
-
-size_t scan_flags_bytes(const sdm_cfg& c, int B, int T)
-{
-    return align256((size_t)B * scan_row_blocks(c) * T * sizeof(int)) + 256;
-}
-
-cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel,
-                        const uint16_t* codes, const void* v, const float* alpha,
-                        const float* beta, void* banks, float* y, int B, int T, void* flags,
-                        int* status, cudaStream_t s)
+cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel, const void* v,
+                        const float* alpha, const float* beta, void* banks, float* y, int B,
+                        int T, void* ws, size_t ws_bytes, int* status, cudaStream_t s)
 {
     if (B <= 0 || T <= 0)
         return cudaSuccess;
-    const size_t fb = scan_flags_bytes(c, B, T);
-    cudaError_t e = cudaMemsetAsync(flags, 0, fb, s);
+    const ScanWs L = scan_ws_layout(c, B, T);
+    char* base = (char*)ws;
+    cudaError_t e = cudaMemsetAsync(base + L.flags, 0, L.flags_bytes, s);
     if (e != cudaSuccess)
         return e;
     ScanArgs a;
     a.banks = (unsigned char*)banks;
     a.idx = idx;
     a.wsel = wsel;
-    a.codes = codes;
+    a.codes = (const uint16_t*)(base + L.codes);
+    a.fwdmask = (const unsigned long long*)(base + L.fwdmask);
     a.v = (const unsigned char*)v;
     a.alpha = alpha;
     a.beta = beta;
     a.y = y;
     a.status = status;
-    a.flags = (int*)flags;
-    a.counter = (unsigned long long*)((char*)flags + fb - 256);
-    a.abort_flag = (int*)((char*)flags + fb - 128);
+    a.flags = (int*)(base + L.flags);
+    a.counter = (unsigned long long*)(base + L.flags + L.flags_bytes - 256);
+    a.abort_flag = (int*)(base + L.flags + L.flags_bytes - 128);
+    a.ring = ws_bytes >= L.total ? (unsigned char*)(base + L.ring) : nullptr;
     a.B = B;
     a.T = T;
     a.d = c.d;
     a.N = c.n_sub * c.n_sub;
-    a.nrb = scan_row_blocks(c);
-    a.rb_rows = scan_block_rows(c);
+    a.nrb = L.nrb;
+    a.rb_rows = L.rb_rows;
+    a.win = L.win;
+    a.ring_entries = L.ring_entries;
+    a.chunk_bytes = L.chunk_bytes;
     a.items = (long long)B * T * a.nrb;
     const bool bf = c.dtype == SDM_BF16;
     switch (c.w) {

@@ -4,9 +4,10 @@
 // Some hosts give this code no way to allocate: a plugin inside an application that
 // owns all device memory through its own pool or budget, or a latency-critical loop
 // where cudaMalloc/cudaFree would synchronise the device and stall other work. For
-// them this entry point keeps the scan's scratch (the collision codes, B*T*w*4 bytes,
-// and the per-token progress flags of the row blocks, see sdm_scan_workspace_bytes) in
-// g_scan_scratch below, a file-scope device array of SDM_SCAN_NOALLOC_MAX_BYTES that
+// them this entry point keeps the scan's scratch (the collision codes, the forwarding
+// masks and the per-token progress flags of the row blocks: the minimal scan workspace,
+// sdm_scan_min_workspace_bytes; the forwarding ring too when the whole workspace fits)
+// in g_scan_scratch below, a file-scope device array of SDM_SCAN_NOALLOC_MAX_BYTES that
 // every GPU loading the library holds until exit.
 //
 // The first call on each device looks up the array's device address with
@@ -54,7 +55,7 @@ extern "C" int sdm_scan_noalloc(const sdm_cfg* cfg, const int32_t* idx, const fl
 {
     if (B < 0 || T < 0)
         return SDM_EINVAL;
-    const size_t need = sdm_scan_workspace_bytes(cfg, B, T);
+    const size_t need = sdm_scan_min_workspace_bytes(cfg, B, T);
     if (need == 0)  // the shape itself is not accepted: report why
         return sdm_scan(cfg, idx, wsel, v, alpha, beta, banks, y, B, T, nullptr, 0, dev_status,
                         stream);

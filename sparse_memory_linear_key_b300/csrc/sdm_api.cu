@@ -44,26 +44,21 @@ static int check_scan_cfg(const sdm_cfg* cfg)
     return SDM_OK;
 }
 
-// The scan's workspace: the collision codes, then the progress flags.
-static size_t scan_codes_bytes(const sdm_cfg& c, int B, int T)
-{
-    return align256((size_t)B * T * 2 * c.w * 2);
-}
-
 static size_t esize(const sdm_cfg& c) { return c.dtype == SDM_BF16 ? 2 : 4; }
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 static int cuda_status(cudaError_t e) { return e == cudaSuccess ? SDM_OK : SDM_ECUDA; }
 
-// Workspace layout of a prefill / decode call over ntok = B*T tokens.
+// Workspace layout of a prefill / decode call over B sequences of T tokens.
 struct PrefillWs {
-    size_t q_w, q_r, v, idx, wsel, codes, flags, addr, total;
+    size_t q_w, q_r, v, idx, wsel, scan, addr, total;
 };
 
-static PrefillWs prefill_layout(const sdm_cfg& c, int64_t ntok)
+static PrefillWs prefill_layout(const sdm_cfg& c, int B, int T)
 {
     PrefillWs L;
+    const int64_t ntok = (int64_t)B * T;
     size_t o = 0;
     const size_t W2 = (size_t)2 * c.w;
     L.q_w = o; o += align256((size_t)ntok * c.dk * esize(c));
@@ -71,8 +66,7 @@ static PrefillWs prefill_layout(const sdm_cfg& c, int64_t ntok)
     L.v = o; o += align256((size_t)ntok * c.d * esize(c));
     L.idx = o; o += align256((size_t)ntok * W2 * 4);
     L.wsel = o; o += align256((size_t)ntok * W2 * 4);
-    L.codes = o; o += align256((size_t)ntok * W2 * 2);
-    L.flags = o; o += scan_flags_bytes(c, 1, (int)ntok);
+    L.scan = o; o += scan_ws_layout(c, B, T).total;
     L.addr = o; o += address_ws_bytes(c, ntok);
     L.total = o;
     return L;
@@ -137,14 +131,21 @@ size_t sdm_scan_workspace_bytes(const sdm_cfg* cfg, int B, int T)
 {
     if (check_scan_cfg(cfg) != SDM_OK || B < 0 || T < 0)
         return 0;
-    return scan_codes_bytes(*cfg, B, T) + scan_flags_bytes(*cfg, B, T);
+    return scan_ws_layout(*cfg, B, T).total;
+}
+
+size_t sdm_scan_min_workspace_bytes(const sdm_cfg* cfg, int B, int T)
+{
+    if (check_scan_cfg(cfg) != SDM_OK || B < 0 || T < 0)
+        return 0;
+    return scan_ws_layout(*cfg, B, T).min_total;
 }
 
 size_t sdm_workspace_bytes(const sdm_cfg* cfg, int B, int T)
 {
     if (sdm_check_cfg(cfg) != SDM_OK || B < 0 || T < 0)
         return 0;
-    return prefill_layout(*cfg, (int64_t)B * T).total;
+    return prefill_layout(*cfg, B, T).total;
 }
 
 int sdm_init_bank(const sdm_cfg* cfg, const void* M0, void* banks, int B, void* stream)
@@ -206,12 +207,15 @@ int sdm_address(const sdm_cfg* cfg, const void* K1, const void* K2, const void* 
 
 static int scan_impl(const sdm_cfg& c, const int32_t* idx, const float* wsel, const void* v,
                      const float* alpha, const float* beta, void* banks, float* y, int B, int T,
-                     uint16_t* codes, void* flags, int* dev_status, cudaStream_t s)
+                     void* ws, size_t ws_bytes, int* dev_status, cudaStream_t s)
 {
-    cudaError_t e = launch_fwd_codes(c, idx, B, T, codes, dev_status, s);
+    const ScanWs L = scan_ws_layout(c, B, T);
+    char* base = (char*)ws;
+    cudaError_t e = launch_scan_codes(c, idx, B, T, L.win, (uint16_t*)(base + L.codes),
+                                      (unsigned long long*)(base + L.fwdmask), dev_status, s);
     if (e != cudaSuccess)
         return SDM_ECUDA;
-    e = launch_scan(c, idx, wsel, codes, v, alpha, beta, banks, y, B, T, flags, dev_status, s);
+    e = launch_scan(c, idx, wsel, v, alpha, beta, banks, y, B, T, ws, ws_bytes, dev_status, s);
     return cuda_status(e);
 }
 
@@ -227,65 +231,65 @@ int sdm_scan_prepare(const sdm_cfg* cfg, const int32_t* idx, int B, int T, void*
         return SDM_OK;
     if (idx == nullptr || ws == nullptr || !aligned16(idx) || ((uintptr_t)ws & 255u) != 0)
         return SDM_EINVAL;
-    if (ws_bytes < sdm_scan_workspace_bytes(cfg, B, T))
+    const ScanWs L = scan_ws_layout(*cfg, B, T);
+    if (ws_bytes < L.min_total)
         return SDM_EWORKSPACE;
-    return cuda_status(launch_fwd_codes(*cfg, idx, B, T, (uint16_t*)ws, dev_status,
-                                       (cudaStream_t)stream));
+    char* base = (char*)ws;
+    return cuda_status(launch_scan_codes(*cfg, idx, B, T, L.win, (uint16_t*)(base + L.codes),
+                                         (unsigned long long*)(base + L.fwdmask), dev_status,
+                                         (cudaStream_t)stream));
+}
+
+static int check_scan_args(const sdm_cfg* cfg, const int32_t* idx, const float* wsel,
+                           const void* v, const float* alpha, const float* beta, void* banks,
+                           float* y, int B, int T, const void* ws, size_t ws_bytes,
+                           int* dev_status)
+{
+    int rc = check_scan_cfg(cfg);
+    if (rc != SDM_OK)
+        return rc;
+    if (B < 0 || T < 0)
+        return SDM_EINVAL;
+    if (B == 0 || T == 0)
+        return SDM_OK;
+    const void* ptrs[] = {idx, wsel, v, alpha, beta, banks, y, ws, dev_status};
+    for (const void* p : ptrs)
+        if (p == nullptr)
+            return SDM_EINVAL;
+    const void* al[] = {idx, wsel, v, banks, y};
+    for (const void* p : al)
+        if (!aligned16(p))
+            return SDM_EINVAL;
+    if (((uintptr_t)ws & 255u) != 0)
+        return SDM_EINVAL;
+    if (ws_bytes < scan_ws_layout(*cfg, B, T).min_total)
+        return SDM_EWORKSPACE;
+    return SDM_OK;
 }
 
 int sdm_scan_run(const sdm_cfg* cfg, const int32_t* idx, const float* wsel, const void* v,
                  const float* alpha, const float* beta, void* banks, float* y, int B, int T,
                  const void* ws, size_t ws_bytes, int* dev_status, void* stream)
 {
-    int rc = check_scan_cfg(cfg);
-    if (rc != SDM_OK)
+    const int rc = check_scan_args(cfg, idx, wsel, v, alpha, beta, banks, y, B, T, ws, ws_bytes,
+                                   dev_status);
+    if (rc != SDM_OK || B == 0 || T == 0)
         return rc;
-    if (B < 0 || T < 0)
-        return SDM_EINVAL;
-    if (B == 0 || T == 0)
-        return SDM_OK;
-    const void* ptrs[] = {idx, wsel, v, alpha, beta, banks, y, ws, dev_status};
-    for (const void* p : ptrs)
-        if (p == nullptr)
-            return SDM_EINVAL;
-    const void* al[] = {idx, wsel, v, banks, y};
-    for (const void* p : al)
-        if (!aligned16(p))
-            return SDM_EINVAL;
-    if (((uintptr_t)ws & 255u) != 0)
-        return SDM_EINVAL;
-    if (ws_bytes < sdm_scan_workspace_bytes(cfg, B, T))
-        return SDM_EWORKSPACE;
-    void* flags = (char*)ws + scan_codes_bytes(*cfg, B, T);
-    return cuda_status(launch_scan(*cfg, idx, wsel, (const uint16_t*)ws, v, alpha, beta, banks,
-                                   y, B, T, flags, dev_status, (cudaStream_t)stream));
+    return cuda_status(launch_scan(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T,
+                                   const_cast<void*>(ws), ws_bytes, dev_status,
+                                   (cudaStream_t)stream));
 }
 
 int sdm_scan(const sdm_cfg* cfg, const int32_t* idx, const float* wsel, const void* v,
              const float* alpha, const float* beta, void* banks, float* y, int B, int T,
              void* ws, size_t ws_bytes, int* dev_status, void* stream)
 {
-    int rc = check_scan_cfg(cfg);
-    if (rc != SDM_OK)
+    const int rc = check_scan_args(cfg, idx, wsel, v, alpha, beta, banks, y, B, T, ws, ws_bytes,
+                                   dev_status);
+    if (rc != SDM_OK || B == 0 || T == 0)
         return rc;
-    if (B < 0 || T < 0)
-        return SDM_EINVAL;
-    if (B == 0 || T == 0)
-        return SDM_OK;
-    const void* ptrs[] = {idx, wsel, v, alpha, beta, banks, y, ws, dev_status};
-    for (const void* p : ptrs)
-        if (p == nullptr)
-            return SDM_EINVAL;
-    const void* al[] = {idx, wsel, v, banks, y};
-    for (const void* p : al)
-        if (!aligned16(p))
-            return SDM_EINVAL;
-    if (((uintptr_t)ws & 255u) != 0)
-        return SDM_EINVAL;
-    if (ws_bytes < sdm_scan_workspace_bytes(cfg, B, T))
-        return SDM_EWORKSPACE;
-    return scan_impl(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, (uint16_t*)ws,
-                     (char*)ws + scan_codes_bytes(*cfg, B, T), dev_status, (cudaStream_t)stream);
+    return scan_impl(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, ws, ws_bytes, dev_status,
+                     (cudaStream_t)stream);
 }
 
 int sdm_prefill(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const float* alpha,
@@ -310,7 +314,7 @@ int sdm_prefill(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const f
     if (((uintptr_t)ws & 255u) != 0)
         return SDM_EINVAL;
     const int64_t ntok = (int64_t)B * T;
-    const PrefillWs L = prefill_layout(*cfg, ntok);
+    const PrefillWs L = prefill_layout(*cfg, B, T);
     if (ws_bytes < L.total)
         return SDM_EWORKSPACE;
     char* base = (char*)ws;
@@ -319,8 +323,7 @@ int sdm_prefill(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const f
     void* v = base + L.v;
     int32_t* idx = idx_out ? idx_out : (int32_t*)(base + L.idx);
     float* wsel = w_out ? w_out : (float*)(base + L.wsel);
-    uint16_t* codes = (uint16_t*)(base + L.codes);
-    void* flags = base + L.flags;
+
     cudaStream_t s = (cudaStream_t)stream;
     rc = launch_project(*cfg, *w, x, ntok, q_w, q_r, v, s);
     if (rc != SDM_OK)
@@ -328,7 +331,8 @@ int sdm_prefill(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const f
     if (launch_address(*cfg, w->K1, w->K2, q_w, q_r, ntok, idx, wsel, base + L.addr, dev_status,
                        s) != cudaSuccess)
         return SDM_ECUDA;
-    return scan_impl(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, codes, flags, dev_status, s);
+    return scan_impl(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, base + L.scan,
+                     scan_ws_layout(*cfg, B, T).total, dev_status, s);
 }
 
 int sdm_decode_step(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const float* alpha,

@@ -200,6 +200,12 @@ __device__ __forceinline__ void st_release_gpu(int* p, int v)
     asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// *p = max(*p, v) with release semantics (monotone progress flags)
+__device__ __forceinline__ void red_max_release_gpu(int* p, int v)
+{
+    asm volatile("red.release.gpu.global.max.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void st_relaxed_gpu(int* p, int v)
 {
     asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");

@@ -55,14 +55,23 @@ def test_workspace_sizes(L):
     c = sdm.make_cfg(2048, 480, 256, 64, "bf16")
     ntok = 4 * 4096
     ws = sdm.workspace_bytes(c, 4, 4096)
-    # q_w, q_r, v (bf16), idx + wsel (int32/fp32), codes (uint16), the scan's progress
-    # flags (one int per token and 1 KB row block: 4 blocks at d = 2048 bf16), half lists
-    want = (ntok * (2 * 256 * 2 + 2048 * 2 + 128 * 4 * 2 + 128 * 2 + 4 * 4)
-            + 2 * ntok * 2 * 64 * 8)
-    assert want <= ws <= want + 10 * 256
-    assert sdm.scan_workspace_bytes(c, 4, 4096) >= ntok * (128 * 2 + 4 * 4)
+    # q_w, q_r, v (bf16), idx + wsel (int32/fp32), the scan's workspace, half lists
+    front = ntok * (2 * 256 * 2 + 2048 * 2 + 128 * 4 * 2) + 2 * ntok * 2 * 64 * 8
+    scan = sdm.scan_workspace_bytes(c, 4, 4096)
+    assert front + scan <= ws <= front + scan + 8 * 256
+    # scan: codes (uint16), forwarding masks (uint64), one progress flag per token and
+    # 1 KB row block (4 blocks at d = 2048 bf16), then the forwarding ring (whole 1 KB
+    # chunks of up to 64 slots per ring entry, 4 sequences x 4 blocks, 16..256 entries)
+    small = ntok * (128 * 2 + 8 + 4 * 4)
+    smin = sdm.scan_min_workspace_bytes(c, 4, 4096)
+    assert small <= smin <= small + 4 * 256
+    ring = scan - smin
+    assert ring % (16 * 64 * 1024) == 0 and 16 <= ring // (16 * 64 * 1024) <= 256
     assert sdm.address_workspace_bytes(c, ntok) >= 2 * ntok * 2 * 64 * 8
     assert sdm.workspace_bytes(sdm.make_cfg(2048, 480, 256, 63, "bf16"), 1, 1) == 0
+    # a single decode step: the ring holds one entry per stream
+    assert sdm.scan_workspace_bytes(c, 64, 1) - sdm.scan_min_workspace_bytes(c, 64, 1) == \
+        64 * 4 * 64 * 1024
 
 
 def test_host_validation_before_cuda(L):
