@@ -17,20 +17,23 @@
 //
 // Persistent kernel, one CTA per SM, items claimed in increasing order from a global
 // counter (t-major, so all streams advance together). Warp roles in a CTA:
-//  P   claims the next item, reads its slot ids and codes, and gathers the write chunks
-//      (one buffer) and read chunks (two buffers, alternating items) with cp.async.bulk;
+//  P   claims the next item, reads its slot ids and codes, checks its window and writes
+//      its description (which chunks come from the bank);
+//  C   16 warps: take the write chunks into registers, which frees the write buffer,
+//      then gather the next item's chunks from the bank with cp.async.bulk into it and
+//      into one of two read buffers (alternating items), each warp issuing 1/16 of the
+//      copies (one warp alone issues them too slowly); then form u and the new values,
+//      publish the slots later tokens need into the ring, reduce the read chunks into
+//      y, and store the new values to the bank;
 //  D   copies the chunks whose latest writer is still in flight, from that writer's
 //      forwarding-ring entry, once the writer has published it;
-//  C   16 warps: take the write chunks into registers (freeing the buffer for the next
-//      item), form u and the new values, publish the slots later tokens need into the
-//      ring, reduce the read chunks into y, then store the new values to the bank;
-//  F1  marks the item's bank loads done and clears its bank stores (write after read,
-//      write after write);
-//  F2  publishes the ring entries and then the bank stores.
+//  F1  clears the item's bank stores (write after read, write after write);
+//  M   marks the item's progress: bank loads done, ring entries and bank stores
+//      published.
 // Ordering between tokens of one stream, which may run on different SMs, goes through
 // one progress flag per item in global memory: 1 = its bank loads are done, 2 = its
 // ring entries are visible, 3 = its bank stores are visible (raised with atomic max, so
-// it never goes down whichever role gets there first).
+// it never goes down whichever mark lands first).
 //  * read after write: a reference whose latest writer lies within the last `win`
 //    tokens (collision codes) is copied from that writer's ring entry once its flag is
 //    >= 2; a read of a slot the same token writes is forwarded in shared memory; older
@@ -45,8 +48,8 @@
 // Without ring space (a workspace of only min_total bytes) dependent references wait
 // for flag 3 and read the bank.
 // Every wait is bounded: on time-out the kernel records SDM_ETIMEOUT and raises a
-// global abort flag that every warp watches; the warps that issued copies wait for
-// them to land before the CTA ends.
+// global abort flag that every warp watches. Each warp leaves as a whole, and no warp
+// waits on another without a bound, so none can hang.
 #include "sdm_common.cuh"
 #include "sdm_internal.h"
 
@@ -58,6 +61,7 @@ constexpr int kChunk = 1024;       // bytes of a full row block of one slot
 constexpr int kStride = 1088;      // shared-memory stride between chunks (bank spread)
 constexpr int kCWarps = 16;        // consumer warps
 constexpr int kWarpP = kCWarps, kWarpD = kCWarps + 1, kWarpF1 = kCWarps + 2;
+// 20 warps: five per SM sub-partition, which leaves each thread up to 96 registers
 constexpr int kScanThreads = 32 * (kCWarps + 4);
 constexpr int kMaxW = 64;
 constexpr int kSG = 8;             // slot groups (lanes sharing a row group)
@@ -91,15 +95,24 @@ struct __align__(16) Meta {
     signed char fpos[kMaxW];        // read ref j: position in the write set if own write
     unsigned long long fmask;       // bit j: read ref j is such a slot
     unsigned long long fwdmask;     // bit j: write slot j goes to the ring
+    unsigned long long wload;       // bit j: write chunk j is gathered from the bank
+    unsigned long long rload;       // bit j: read chunk j is gathered from the bank
     long long tok;                  // b * T + t
     int b, t, rb, rows;
     float alpha, beta;
     int valid;                      // 0: no more work
 };
 
+// mbarriers: full* = an item's chunks landed (armed by the consumer warps issuing them),
+// Wfree = the consumers took the write chunks, EmptyR = item description and read
+// buffer free again (F1 and M done), DepB = D's copies landed, Posted = item described,
+// War = bank stores cleared, Fwdw / Stored = consumers wrote the ring / the bank,
+// Cbar = barrier of the consumer warps, Lmark = M marked the item loaded (the consumers
+// arm the next item's FullW only then, so that FullW is never two phases ahead of M).
+// The [2] ones alternate with the items.
 enum {
-    kFullW = 0, kEmptyW = 1, kFullR = 2, kEmptyR = 4, kDepB = 6, kPosted = 8, kWar = 10,
-    kFwdw = 12, kStored = 14, kCbar = 16, kNumBars = 17
+    kFullW = 0, kWfree = 1, kFullR = 2, kEmptyR = 4, kDepB = 6, kPosted = 8, kWar = 10,
+    kFwdw = 12, kStored = 14, kCbar = 16, kLmark = 17, kNumBars = 18
 };
 
 template <typename S>
@@ -147,11 +160,18 @@ struct Pack16<float> {
     }
 };
 
-__device__ __forceinline__ int warp_sum(int x) { return __reduce_add_sync(0xFFFFFFFFu, x); }
-
 __device__ __forceinline__ bool uniform_wait(uint32_t bar, uint32_t parity, const ScanArgs& a)
 {
     return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, a.abort_flag, a.status));
+}
+
+// warp-uniform non-blocking test of an mbarrier phase
+__device__ __forceinline__ bool uniform_test(uint32_t bar, uint32_t parity)
+{
+    int r = 0;
+    if ((threadIdx.x & 31) == 0)
+        r = mbar_test(bar, parity) ? 1 : 0;
+    return __shfl_sync(0xFFFFFFFFu, r, 0) != 0;
 }
 
 __device__ __forceinline__ int* item_flag(const ScanArgs& a, int b, int rb, int t)
@@ -188,7 +208,7 @@ __device__ __forceinline__ bool window_geq(const ScanArgs& a, const int* fl, int
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
-// ------------------------------------------------------------------ P: gathers
+// ------------------------------------------------------------- P: item descriptions
 
 // A claimed item and what the producer needs of it, read one item ahead.
 template <int JW>
@@ -234,16 +254,11 @@ __device__ __forceinline__ void fetch_ahead(const ScanArgs& a, unsigned long lon
     }
 }
 
-template <typename S, int W>
-__device__ void role_producer(const ScanArgs& a, unsigned char* wbuf, unsigned char* rbuf,
-                              Meta* meta, uint64_t* bars)
+template <int W>
+__device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
 {
     constexpr int JW = (W + 31) / 32;
     const int lane = threadIdx.x & 31;
-    const uint32_t fullW = smem_u32(bars + kFullW), emptyW = smem_u32(bars + kEmptyW);
-    int armedW = -1, armedR[2] = {-1, -1};  // item numbers whose full phases were armed
-    uint32_t missW = 0, missR = 0;          // this lane's counted-but-unissued bytes
-    bool ok = true;
     Ahead<JW> nx;
     {
         unsigned long long item = 0;
@@ -251,132 +266,72 @@ __device__ void role_producer(const ScanArgs& a, unsigned char* wbuf, unsigned c
             item = atomicAdd(a.counter, 1ull);
         fetch_ahead<W, JW>(a, __shfl_sync(0xFFFFFFFFu, item, 0), nx);
     }
-    int k = 0;
-    for (;; ++k) {
+    for (int k = 0;; ++k) {
         const int p = k & 1;
-        const uint32_t fullR = smem_u32(bars + kFullR + p), emptyR = smem_u32(bars + kEmptyR + p);
         Meta& m = meta[p];
-        unsigned char* rb_buf = rbuf + (size_t)p * W * kStride;
         int aborted = lane == 0 ? ld_relaxed_gpu(a.abort_flag) : 0;
         aborted = __shfl_sync(0xFFFFFFFFu, aborted, 0);
+        // the description slot (and read buffer) is free once item k-2 is done
+        if (!uniform_wait(smem_u32(bars + kEmptyR + p), ((k >> 1) & 1) ^ 1, a))
+            return;
         if (nx.item >= (unsigned long long)a.items || aborted != 0) {
-            // end of work: hand every role an empty item
-            ok = uniform_wait(emptyW, (k & 1) ^ 1, a) &&
-                 uniform_wait(emptyR, ((k >> 1) & 1) ^ 1, a);
-            if (ok && lane == 0) {
+            // end of work: an empty item tells every role to finish
+            if (lane == 0) {
                 m.valid = 0;
-                mbar_arrive(fullW);
-                mbar_arrive(fullR);
                 mbar_arrive(smem_u32(bars + kPosted + p));
             }
-            break;
+            return;
         }
         const int t = nx.t, b = nx.b, rb = nx.rb;
-        const long long tok = (long long)b * a.T + t;
-        const int rows = min(a.rb_rows, a.d - rb * a.rb_rows);
-        const uint32_t cb = (uint32_t)rows * (uint32_t)sizeof(S);
         const int* fl = item_flag(a, b, rb, 0);
-        const unsigned char* bank =
-            a.banks + ((size_t)b * a.N * a.d + (size_t)rb * a.rb_rows) * sizeof(S);
-        const size_t slot_bytes = (size_t)a.d * sizeof(S);
-
         // window: tokens t-2*win+1 .. t-win of this stream are committed
-        if (!window_geq(a, fl, t - 2 * a.win + 1, t - a.win + 1, 3)) {
-            ok = false;
-            break;
-        }
+        if (!window_geq(a, fl, t - 2 * a.win + 1, t - a.win + 1, 3))
+            return;
         fence_acq_rel_gpu();
-        fence_proxy_async_global();
 
-        bool wval[JW], wdep[JW], rval[JW], rdep[JW], rown[JW];
-        int nW = 0, nR = 0;
-        unsigned long long fmask = 0;
-#pragma unroll
-        for (int jj = 0; jj < JW; ++jj) {
-            const bool has = lane + 32 * jj < W;
-            wval[jj] = has && nx.wid[jj] >= 0 && nx.wid[jj] < a.N;
-            rval[jj] = has && nx.rid[jj] >= 0 && nx.rid[jj] < a.N;
-            if ((has && !wval[jj]) || (has && !rval[jj]))
-                report(a.status, SDM_ERANGE);
-            wdep[jj] = wval[jj] && nx.wc[jj] != kNoFwd;  // an in-window writer: D copies it
-            const int dt = nx.rc[jj] >> 8;
-            rown[jj] = rval[jj] && nx.rc[jj] != kNoFwd && dt == 0;
-            rdep[jj] = rval[jj] && nx.rc[jj] != kNoFwd && dt > 0;
-            nW += (wval[jj] && !wdep[jj]) ? 1 : 0;
-            nR += (rval[jj] && !rown[jj] && !rdep[jj]) ? 1 : 0;
-            fmask |= (unsigned long long)__ballot_sync(0xFFFFFFFFu, rown[jj]) << (32 * jj);
-        }
-
-        // ---- write chunks, as soon as the consumers have taken the previous ones
-        if (!uniform_wait(emptyW, (k & 1) ^ 1, a)) {
-            ok = false;
-            break;
-        }
-        missW = (uint32_t)nW * cb;
-        const int totW = warp_sum(nW);
-        if (lane == 0)
-            mbar_arrive_expect_tx(fullW, (uint32_t)totW * cb);
-        armedW = k;
-        __syncwarp();
-#pragma unroll
-        for (int jj = 0; jj < JW; ++jj)
-            if (wval[jj] && !wdep[jj]) {
-                bulk_g2s(smem_u32(wbuf + (size_t)(lane + 32 * jj) * kStride),
-                         bank + (size_t)nx.wid[jj] * slot_bytes, cb, fullW);
-                missW -= cb;
-            }
-
-        // ---- item description, read chunks, weights and v
-        if (!uniform_wait(emptyR, ((k >> 1) & 1) ^ 1, a)) {
-            ok = false;
-            break;
-        }
+        unsigned long long wload = 0, rload = 0, fmask = 0;
 #pragma unroll
         for (int jj = 0; jj < JW; ++jj) {
             const int j = lane + 32 * jj;
-            if (j < W) {
-                m.wid[j] = wval[jj] ? nx.wid[jj] : -1;
-                m.rid[j] = rval[jj] ? nx.rid[jj] : -1;
+            const bool has = j < W;
+            const bool wval = has && nx.wid[jj] >= 0 && nx.wid[jj] < a.N;
+            const bool rval = has && nx.rid[jj] >= 0 && nx.rid[jj] < a.N;
+            if ((has && !wval) || (has && !rval))
+                report(a.status, SDM_ERANGE);
+            const int dt = nx.rc[jj] >> 8;
+            const bool rown = rval && nx.rc[jj] != kNoFwd && dt == 0;
+            const bool rdep = rval && nx.rc[jj] != kNoFwd && dt > 0;
+            // bank loads: references with no writer within the window (D copies the rest)
+            wload |= (unsigned long long)__ballot_sync(0xFFFFFFFFu, wval && nx.wc[jj] == kNoFwd)
+                     << (32 * jj);
+            rload |= (unsigned long long)__ballot_sync(0xFFFFFFFFu, rval && !rown && !rdep)
+                     << (32 * jj);
+            fmask |= (unsigned long long)__ballot_sync(0xFFFFFFFFu, rown) << (32 * jj);
+            if (has) {
+                m.wid[j] = wval ? nx.wid[jj] : -1;
+                m.rid[j] = rval ? nx.rid[jj] : -1;
                 m.code[j] = nx.wc[jj];
                 m.code[W + j] = nx.rc[jj];
-                m.fpos[j] = rown[jj] ? (signed char)(nx.rc[jj] & 0xFF) : (signed char)-1;
+                m.fpos[j] = rown ? (signed char)(nx.rc[jj] & 0xFF) : (signed char)-1;
             }
         }
-        missR = (uint32_t)nR * cb;
-        const int totR = warp_sum(nR);
         if (lane == 0) {
             m.fmask = fmask;
             m.fwdmask = nx.fwdmask;
-            m.tok = tok;
+            m.wload = wload;
+            m.rload = rload;
+            m.tok = (long long)b * a.T + t;
             m.b = b;
             m.t = t;
             m.rb = rb;
-            m.rows = rows;
+            m.rows = min(a.rb_rows, a.d - rb * a.rb_rows);
             m.alpha = nx.alpha;
             m.beta = nx.beta;
             m.valid = 1;
         }
         __syncwarp();
         if (lane == 0)
-            mbar_arrive_expect_tx(fullR, (uint32_t)totR * cb + 2 * W * 4 + cb);
-        armedR[p] = k;
-        __syncwarp();
-        if (lane == 0)
-            bulk_g2s(smem_u32(m.wsel), a.wsel + tok * 2 * W, 2 * W * 4, fullR);
-        if (lane == 1)
-            bulk_g2s(smem_u32(m.v), a.v + ((size_t)tok * a.d + (size_t)rb * a.rb_rows) * sizeof(S),
-                     cb, fullR);
-#pragma unroll
-        for (int jj = 0; jj < JW; ++jj)
-            if (rval[jj] && !rown[jj] && !rdep[jj]) {
-                bulk_g2s(smem_u32(rb_buf + (size_t)(lane + 32 * jj) * kStride),
-                         bank + (size_t)nx.rid[jj] * slot_bytes, cb, fullR);
-                missR -= cb;
-            }
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(smem_u32(bars + kPosted + p));  // D may start on this item
-        missW = missR = 0;
+            mbar_arrive(smem_u32(bars + kPosted + p));  // consumers and D may start on it
 
         // ---- the next item
         unsigned long long next = 0;
@@ -384,26 +339,6 @@ __device__ void role_producer(const ScanArgs& a, unsigned char* wbuf, unsigned c
             next = atomicAdd(a.counter, 1ull);
         fetch_ahead<W, JW>(a, __shfl_sync(0xFFFFFFFFu, next, 0), nx);
     }
-    if (__all_sync(0xFFFFFFFFu, ok))
-        return;
-    // Failure: declare the bytes that were counted but never copied, then wait
-    // (bounded) for the copies in flight into this CTA's shared memory.
-    if (lane == 0)
-        st_relaxed_gpu(a.abort_flag, 1);
-    const int mw = warp_sum((int)missW), mr = warp_sum((int)missR);
-    const int p = k & 1;
-    if (lane == 0) {
-        if (armedW == k && mw > 0)
-            mbar_complete_tx(fullW, (uint32_t)mw);
-        if (armedR[p] == k && mr > 0)
-            mbar_complete_tx(smem_u32(bars + kFullR + p), (uint32_t)mr);
-        if (armedW >= 0)
-            mbar_wait(fullW, armedW & 1, nullptr, a.status);
-        for (int q = 0; q < 2; ++q)
-            if (armedR[q] >= 0)
-                mbar_wait(smem_u32(bars + kFullR + q), (armedR[q] >> 1) & 1, nullptr, a.status);
-    }
-    __syncwarp();
 }
 
 // ------------------------------------------------------- D: in-flight dependencies
@@ -427,7 +362,7 @@ __device__ void role_deps(const ScanArgs& a, unsigned char* wbuf, unsigned char*
         const int t = m.t, b = m.b, rb = m.rb;
         const int* fl = item_flag(a, b, rb, 0);
         bool dep[JR];
-        int n = 0;
+        int n = 0, nw = 0;
 #pragma unroll
         for (int q = 0; q < JR; ++q) {
             const int r = lane + 32 * q;
@@ -438,18 +373,20 @@ __device__ void role_deps(const ScanArgs& a, unsigned char* wbuf, unsigned char*
                 dep[q] = id >= 0 && c != kNoFwd && (c >> 8) > 0;
             }
             n += dep[q] ? 1 : 0;
+            nw += (dep[q] && r < W) ? 1 : 0;
         }
-        const int tot = warp_sum(n);
+        const int tot = __reduce_add_sync(0xFFFFFFFFu, n);
+        const int totw = __reduce_add_sync(0xFFFFFFFFu, nw);
         if (lane == 0)
             mbar_arrive_expect_tx(depB, (uint32_t)tot * cb);
-        __syncwarp();
+        // write chunks go to the write buffer, free once item k-1 has taken its own
+        bool ok = totw == 0 || k == 0 || uniform_wait(smem_u32(bars + kWfree), (k - 1) & 1, a);
         uint32_t miss = (uint32_t)n * cb;
         // read the writers' flags together, then wait for the ones not yet published
         int got[JR];
 #pragma unroll
         for (int q = 0; q < JR; ++q)
             got[q] = dep[q] ? ld_relaxed_gpu(fl + t - (m.code[lane + 32 * q] >> 8)) : need;
-        bool ok = true;
 #pragma unroll
         for (int q = 0; q < JR; ++q) {
             if (!dep[q] || !ok)
@@ -480,7 +417,7 @@ __device__ void role_deps(const ScanArgs& a, unsigned char* wbuf, unsigned char*
             // declare what was not copied, wait (bounded) for what was, and leave
             if (lane == 0)
                 st_relaxed_gpu(a.abort_flag, 1);
-            const int mm = warp_sum((int)miss);
+            const int mm = __reduce_add_sync(0xFFFFFFFFu, (int)miss);
             if (lane == 0) {
                 if (mm > 0)
                     mbar_complete_tx(depB, (uint32_t)mm);
@@ -492,7 +429,7 @@ __device__ void role_deps(const ScanArgs& a, unsigned char* wbuf, unsigned char*
     }
 }
 
-// ------------------------------------------------------------ F1: loads done, clearance
+// ------------------------------------------------------------------ F1: clearance
 
 template <int W>
 __device__ void role_clear(const ScanArgs& a, const Meta* meta, uint64_t* bars)
@@ -501,8 +438,7 @@ __device__ void role_clear(const ScanArgs& a, const Meta* meta, uint64_t* bars)
     const int lane = threadIdx.x & 31;
     for (int k = 0;; ++k) {
         const int p = k & 1;
-        if (!uniform_wait(smem_u32(bars + kFullW), k & 1, a) ||
-            !uniform_wait(smem_u32(bars + kFullR + p), (k >> 1) & 1, a))
+        if (!uniform_wait(smem_u32(bars + kPosted + p), (k >> 1) & 1, a))
             return;
         const Meta& m = meta[p];
         if (!m.valid)
@@ -516,14 +452,9 @@ __device__ void role_clear(const ScanArgs& a, const Meta* meta, uint64_t* bars)
             const uint16_t c = j < W ? m.code[j] : kNoFwd;
             wdt[jj] = (j < W && m.wid[j] >= 0 && c != kNoFwd) ? (c >> 8) : 0;
         }
-        // without the ring, dependent references are bank loads too
-        if (a.ring == nullptr && !uniform_wait(smem_u32(bars + kDepB + p), (k >> 1) & 1, a))
-            return;
-        if (lane == 0)
-            red_max_release_gpu(item_flag(a, m.b, m.rb, t), 1);  // bank loads done
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(smem_u32(bars + kEmptyW));
+            mbar_arrive(smem_u32(bars + kEmptyR + p));  // done with the item description
         // write after read: tokens t-win .. t-1 have done their bank loads
         bool ok = window_geq(a, fl, t - a.win, t, 1);
         // write after write: in-window writers of our write slots have stored
@@ -535,44 +466,91 @@ __device__ void role_clear(const ScanArgs& a, const Meta* meta, uint64_t* bars)
             return;
         fence_acq_rel_gpu();
         __syncwarp();
-        if (lane == 0) {
+        if (lane == 0)
             mbar_arrive(smem_u32(bars + kWar + p));
-            mbar_arrive(smem_u32(bars + kEmptyR + p));
-        }
     }
 }
 
-// -------------------------------------------------------------- F2: publication
+// ------------------------------------------------------------ M: progress marks
 
-__device__ void role_publish(const ScanArgs& a, const Meta* meta, uint64_t* bars)
+// Raises each item's flag: to 1 as soon as its bank chunks have landed, to 2 once the
+// consumers have written its ring entries, to 3 once they have stored its new slot
+// values (the consumers' arrival, release at CTA scope, followed by this release at GPU
+// scope publishes their global writes). The three marks advance independently: the
+// warp polls whichever is next for each and never blocks one behind another (a later
+// item's bank loads may wait on other tokens' commits, this item's among them).
+__device__ void role_marks(const ScanArgs& a, const Meta* meta, uint64_t* bars)
 {
     const int lane = threadIdx.x & 31;
-    for (int k = 0;; ++k) {
-        const int p = k & 1;
-        if (!uniform_wait(smem_u32(bars + kFullR + p), (k >> 1) & 1, a))
-            return;
-        const Meta& m = meta[p];
-        if (!m.valid)
-            return;
-        int* flag = item_flag(a, m.b, m.rb, m.t);
-        if (!uniform_wait(smem_u32(bars + kFwdw + p), (k >> 1) & 1, a))
-            return;
-        if (lane == 0)
-            red_max_release_gpu(flag, 2);  // ring entries visible
-        if (!uniform_wait(smem_u32(bars + kStored + p), (k >> 1) & 1, a))
-            return;
-        __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(smem_u32(bars + kEmptyR + p));
-            red_max_release_gpu(flag, 3);  // bank stores visible
+    int kl = 0, kp = 0, kc = 0;   // next item to mark loaded, ring-published, committed
+    int end = -1;                 // item number of the empty end item, once seen
+    long long idle = clock64();
+    while (true) {
+        bool progress = false;
+        if (end < 0) {
+            const int p = kl & 1;
+            if (uniform_test(smem_u32(bars + kFullW), kl & 1) &&
+                uniform_test(smem_u32(bars + kFullR + p), (kl >> 1) & 1)) {
+                const Meta& m = meta[p];
+                if (!m.valid) {
+                    end = kl;
+                    progress = true;
+                } else if (a.ring != nullptr ||
+                           uniform_test(smem_u32(bars + kDepB + p), (kl >> 1) & 1)) {
+                    // (without the ring, dependent references are bank loads too)
+                    if (lane == 0) {
+                        red_max_release_gpu(item_flag(a, m.b, m.rb, m.t), 1);
+                        mbar_arrive(smem_u32(bars + kLmark));
+                    }
+                    ++kl;
+                    progress = true;
+                }
+            }
         }
+        if (kp < kl && uniform_test(smem_u32(bars + kFwdw + (kp & 1)), (kp >> 1) & 1)) {
+            const Meta& m = meta[kp & 1];
+            if (lane == 0)
+                red_max_release_gpu(item_flag(a, m.b, m.rb, m.t), 2);  // ring entries visible
+            ++kp;
+            progress = true;
+        }
+        if (kc < kp && uniform_test(smem_u32(bars + kStored + (kc & 1)), (kc >> 1) & 1)) {
+            const Meta& m = meta[kc & 1];
+            int* flag = item_flag(a, m.b, m.rb, m.t);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(smem_u32(bars + kEmptyR + (kc & 1)));
+                red_max_release_gpu(flag, 3);  // bank stores visible
+            }
+            ++kc;
+            progress = true;
+        }
+        if (end >= 0 && kc == end)
+            return;
+        if (progress) {
+            idle = clock64();
+            continue;
+        }
+        int stop = 0;
+        if (lane == 0) {
+            if (ld_relaxed_gpu(a.abort_flag) != 0) {
+                stop = 1;
+            } else if (clock64() - idle > kSpinLimitCycles) {
+                report(a.status, SDM_ETIMEOUT);
+                st_relaxed_gpu(a.abort_flag, 1);
+                stop = 1;
+            }
+        }
+        if (__shfl_sync(0xFFFFFFFFu, stop, 0))
+            return;
+        __nanosleep(20);
     }
 }
 
 // ---------------------------------------------------------------- C: consumers
 
 template <typename S, int W>
-__device__ void role_consumer(const ScanArgs& a, const unsigned char* wbuf, unsigned char* rbuf,
+__device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned char* rbuf,
                               const Meta* meta, uint64_t* bars)
 {
     constexpr int SPL = W / kSG;       // slots of each set per thread: i*8 + sg
@@ -593,6 +571,54 @@ __device__ void role_consumer(const ScanArgs& a, const unsigned char* wbuf, unsi
         ++cuses;
         return __all_sync(0xFFFFFFFFu, okb);
     };
+    // Bank gathers of item kn, split over the consumer warps (8 bulk copies a warp at
+    // W = 64). The full barriers count one arrival per consumer warp: each warp declares
+    // the bytes of its own copies (arrive.expect_tx) before issuing them, so no copy can
+    // land on a phase that does not expect it yet. For the empty end item each warp just
+    // arrives.
+    auto issue = [&](int kn) {
+        const int pn = kn & 1;
+        const Meta& mn = meta[pn];
+        const uint32_t fw = smem_u32(bars + kFullW), fr = smem_u32(bars + kFullR + pn);
+        if (!mn.valid) {
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(fw);
+                mbar_arrive(fr);
+            }
+            return;
+        }
+        const uint32_t cb = (uint32_t)mn.rows * (uint32_t)sizeof(S);
+        const bool is_r = lane >= 4;
+        const int j = w + kCWarps * (lane & 3);
+        const unsigned long long mask = is_r ? mn.rload : mn.wload;
+        const bool chunk = lane < 8 && j < W && ((mask >> j) & 1);
+        const bool wsel_copy = lane == 8 && w == 0, v_copy = lane == 8 && w == 1;
+        const uint32_t wb = __reduce_add_sync(0xFFFFFFFFu, chunk && !is_r ? cb : 0u);
+        const uint32_t rb = __reduce_add_sync(
+            0xFFFFFFFFu, (chunk && is_r ? cb : 0u) + (wsel_copy ? 2u * W * 4 : 0u) + (v_copy ? cb : 0u));
+        if (lane == 0) {
+            mbar_arrive_expect_tx(fw, wb);
+            mbar_arrive_expect_tx(fr, rb);
+        }
+        __syncwarp();
+        fence_proxy_async_global();
+        const unsigned char* bank =
+            a.banks + ((size_t)mn.b * a.N * a.d + (size_t)mn.rb * a.rb_rows) * sizeof(S);
+        if (chunk) {
+            const int id = is_r ? mn.rid[j] : mn.wid[j];
+            unsigned char* dst = (is_r ? rbuf + (size_t)pn * W * kStride : wbuf) + (size_t)j * kStride;
+            bulk_g2s(smem_u32(dst), bank + (size_t)id * a.d * sizeof(S), cb, is_r ? fr : fw);
+        } else if (wsel_copy) {
+            bulk_g2s(smem_u32(mn.wsel), a.wsel + mn.tok * 2 * W, 2 * W * 4, fr);
+        } else if (v_copy) {
+            bulk_g2s(smem_u32(mn.v), a.v + ((size_t)mn.tok * a.d + (size_t)mn.rb * a.rb_rows) * sizeof(S),
+                     cb, fr);
+        }
+    };
+    if (!uniform_wait(smem_u32(bars + kPosted), 0, a))
+        return;
+    issue(0);
     for (int k = 0;; ++k) {
         const int p = k & 1;
         if (!uniform_wait(smem_u32(bars + kFullW), k & 1, a) ||
@@ -611,9 +637,16 @@ __device__ void role_consumer(const ScanArgs& a, const unsigned char* wbuf, unsi
             Mv[i] = act ? *reinterpret_cast<const uint4*>(wbuf + (size_t)(i * kSG + sg) * kStride +
                                                           rg * 16)
                         : make_uint4(0, 0, 0, 0);
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(smem_u32(bars + kEmptyW));
+        // every consumer has taken the write chunks: the buffer is free for item k+1
+        if (!consumer_barrier())
+            return;
+        if (ct == 0)
+            mbar_arrive(smem_u32(bars + kWfree));
+        const uint32_t posted_next = smem_u32(bars + kPosted + ((k + 1) & 1));
+        const uint32_t lmark = smem_u32(bars + kLmark);
+        bool issued = uniform_test(lmark, k & 1) && uniform_test(posted_next, ((k + 1) >> 1) & 1);
+        if (issued)
+            issue(k + 1);
 
         // u = M_S k (pre-write), reduced over the slot groups
         float u[RPL];
@@ -717,8 +750,11 @@ __device__ void role_consumer(const ScanArgs& a, const unsigned char* wbuf, unsi
                 __stcs(reinterpret_cast<float4*>(yp + r),
                        make_float4(yv[r], yv[r + 1], yv[r + 2], yv[r + 3]));
         }
-        if (fm != 0)
-            fence_proxy_async_shared();  // this buffer is refilled by bulk copies later
+        if (!issued && uniform_test(lmark, k & 1) &&
+            uniform_test(posted_next, ((k + 1) >> 1) & 1)) {
+            issue(k + 1);
+            issued = true;
+        }
 
         // bank stores, once cleared
         if (!uniform_wait(smem_u32(bars + kWar + p), (k >> 1) & 1, a))
@@ -734,6 +770,11 @@ __device__ void role_consumer(const ScanArgs& a, const unsigned char* wbuf, unsi
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_u32(bars + kStored + p));
+        if (!issued) {
+            if (!uniform_wait(lmark, k & 1, a) || !uniform_wait(posted_next, ((k + 1) >> 1) & 1, a))
+                return;
+            issue(k + 1);
+        }
     }
 }
 
@@ -746,11 +787,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a)
     Meta* meta = reinterpret_cast<Meta*>(smem + (size_t)3 * W * kStride);
     uint64_t* bars = reinterpret_cast<uint64_t*>(meta + 2);
     if (threadIdx.x == 0) {
-        mbar_init(smem_u32(bars + kFullW), 1);
-        mbar_init(smem_u32(bars + kEmptyW), kCWarps + 1);   // consumers + F1
+        mbar_init(smem_u32(bars + kFullW), kCWarps);
+        mbar_init(smem_u32(bars + kWfree), 1);
         for (int p = 0; p < 2; ++p) {
-            mbar_init(smem_u32(bars + kFullR + p), 1);
-            mbar_init(smem_u32(bars + kEmptyR + p), 2);     // F1 + F2
+            mbar_init(smem_u32(bars + kFullR + p), kCWarps);
+            mbar_init(smem_u32(bars + kEmptyR + p), 2);     // F1 + M
             mbar_init(smem_u32(bars + kDepB + p), 1);
             mbar_init(smem_u32(bars + kPosted + p), 1);
             mbar_init(smem_u32(bars + kWar + p), 1);
@@ -758,6 +799,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a)
             mbar_init(smem_u32(bars + kStored + p), kCWarps);
         }
         mbar_init(smem_u32(bars + kCbar), kCWarps);
+        mbar_init(smem_u32(bars + kLmark), 1);
         fence_mbarrier_init();
     }
     __syncthreads();
@@ -765,13 +807,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a)
     if (warp < kCWarps)
         role_consumer<S, W>(a, wbuf, rbuf, meta, bars);
     else if (warp == kWarpP)
-        role_producer<S, W>(a, wbuf, rbuf, meta, bars);
+        role_producer<W>(a, meta, bars);
     else if (warp == kWarpD)
         role_deps<S, W>(a, wbuf, rbuf, meta, bars);
     else if (warp == kWarpF1)
         role_clear<W>(a, meta, bars);
     else
-        role_publish(a, meta, bars);
+        role_marks(a, meta, bars);
 }
 
 template <typename S, int W>

@@ -273,6 +273,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking: has the phase of parity `parity` completed?
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase of parity `parity` of an mbarrier. Returns false if the
 // global abort flag is raised (abort may be null: not watched) or the wait ran out;
 // a wait that ran out records SDM_ETIMEOUT and raises the abort flag.
@@ -325,6 +339,31 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
             dst),
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+// 16-byte copy global -> shared through the load/store unit (L2 only, no L1).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has completed (the
+// pending count is raised now and dropped on completion, so the phase waits for it).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// One warp copies `bytes` (a multiple of 16, at most 1024) from src to dst.
+__device__ __forceinline__ void warp_copy_chunk(uint32_t dst, const unsigned char* src, uint32_t bytes)
+{
+    const uint32_t lane = threadIdx.x & 31;
+#pragma unroll
+    for (uint32_t off = lane * 16; off < 1024; off += 512)
+        if (off < bytes)
+            cp_async16(dst + off, src + off);
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads)
