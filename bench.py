@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--impl", default="sdm", choices=["sdm", "reference"])
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="tokens per sequence instead of the workload's (for profiling a "
+                         "small case of the same kernels)")
     return ap.parse_args()
 
 
@@ -156,6 +159,8 @@ def gpu_arm(args, world, rank):
     sdm.lib()
 
     wl = synth.WORKLOADS[WORKLOAD]
+    if args.tokens:
+        wl = wl.with_(T=args.tokens)
     dev = "cuda"
     cfg = sdm.make_cfg(wl.d, wl.n, wl.dk, wl.W, wl.dtype)
     p_cpu = synth.make_params(wl)

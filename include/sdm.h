@@ -149,10 +149,10 @@ SDM_API int sdm_scan_run(const sdm_cfg* cfg, const int32_t* idx, const float* ws
 
 /* Size of the device array that sdm_scan_noalloc uses as its scratch: 8 MiB. A call
  * needs sdm_scan_min_workspace_bytes(cfg, B, T) of it: the collision codes (B * T * w * 4
- * bytes), one forwarding mask per token (B * T * 8 bytes) and one progress flag per
+ * bytes), four ordering masks per token (B * T * 32 bytes) and one progress flag per
  * token and 1 KB row block of a slot vector (B * T * ceil(d * elem / 1024) * 4 bytes),
  * plus under 1 KB of alignment and counters; at w = 64, d = 2048 bf16 that is
- * B * T <= 29957 tokens. When sdm_scan_workspace_bytes(cfg, B, T) fits too, the call
+ * B * T <= 27592 tokens. When sdm_scan_workspace_bytes(cfg, B, T) fits too, the call
  * also uses the forwarding ring. */
 #define SDM_SCAN_NOALLOC_MAX_BYTES (8u << 20)
 

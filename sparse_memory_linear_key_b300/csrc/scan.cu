@@ -27,7 +27,7 @@
 //      y, and store the new values to the bank;
 //  D   copies the chunks whose latest writer is still in flight, from that writer's
 //      forwarding-ring entry, once the writer has published it;
-//  F1  clears the item's bank stores (write after read, write after write);
+//  F1  clears the item's bank stores (write after read);
 //  M   marks the item's progress: bank loads done, ring entries and bank stores
 //      published.
 // Ordering between tokens of one stream, which may run on different SMs, goes through
@@ -38,10 +38,12 @@
 //    tokens (collision codes) is copied from that writer's ring entry once its flag is
 //    >= 2; a read of a slot the same token writes is forwarded in shared memory; older
 //    writers are visible in the bank (window rule below);
-//  * write after read: the bank stores of token t wait until tokens t-win .. t-1 have
-//    flag >= 1 (bank loads happen first, so this never waits on a dependency);
-//  * write after write: they also wait until each in-window writer of a slot t writes
-//    has flag 3;
+//  * write after read: the bank stores of token t wait until each token within the
+//    window that references a slot t writes has flag >= 1 (the codes mark them; bank
+//    loads happen first, so this never waits on a dependency);
+//  * write after write: a write that a later token within the window overwrites is
+//    not stored at all (dead store: readers in between take the ring entry, readers
+//    after it the newer value), so two stores of one slot are always a window apart;
 //  * window: token t starts only when tokens t-2*win+1 .. t-win have flag 3; the ring
 //    has 2*win entries per stream, so an entry is reused only when all its readers are
 //    done.
@@ -71,7 +73,7 @@ struct ScanArgs {
     const int32_t* idx;
     const float* wsel;
     const uint16_t* codes;
-    const unsigned long long* fwdmask;
+    const unsigned long long* masks;  // per token: fwdmask [B*T], deadmask [B*T], warmask [B*T][2]
     const unsigned char* v;
     const float* alpha;
     const float* beta;
@@ -95,6 +97,8 @@ struct __align__(16) Meta {
     signed char fpos[kMaxW];        // read ref j: position in the write set if own write
     unsigned long long fmask;       // bit j: read ref j is such a slot
     unsigned long long fwdmask;     // bit j: write slot j goes to the ring
+    unsigned long long deadmask;    // bit j: write slot j is rewritten within the window
+    unsigned long long war[2];      // bit dt-1: token t-dt must have loaded before our stores
     unsigned long long wload;       // bit j: write chunk j is gathered from the bank
     unsigned long long rload;       // bit j: read chunk j is gathered from the bank
     long long tok;                  // b * T + t
@@ -105,14 +109,15 @@ struct __align__(16) Meta {
 
 // mbarriers: full* = an item's chunks landed (armed by the consumer warps issuing them),
 // Wfree = the consumers took the write chunks, EmptyR = item description and read
-// buffer free again (F1 and M done), DepB = D's copies landed, Posted = item described,
+// buffer free again (F1 and M done), DepB / DepR = D's write / read chunk copies landed
+// (read chunks are needed only after u and the new values), Posted = item described,
 // War = bank stores cleared, Fwdw / Stored = consumers wrote the ring / the bank,
 // Cbar = barrier of the consumer warps, Lmark = M marked the item loaded (the consumers
 // arm the next item's FullW only then, so that FullW is never two phases ahead of M).
 // The [2] ones alternate with the items.
 enum {
     kFullW = 0, kWfree = 1, kFullR = 2, kEmptyR = 4, kDepB = 6, kPosted = 8, kWar = 10,
-    kFwdw = 12, kStored = 14, kCbar = 16, kLmark = 17, kNumBars = 18
+    kFwdw = 12, kStored = 14, kCbar = 16, kLmark = 17, kDepR = 18, kNumBars = 20
 };
 
 template <typename S>
@@ -218,7 +223,7 @@ struct Ahead {
     int wid[JW], rid[JW];
     uint16_t wc[JW], rc[JW];
     float alpha, beta;               // lane 0
-    unsigned long long fwdmask;      // lane 0
+    unsigned long long fwdmask, deadmask, war0, war1;  // lane 0
 };
 
 template <int W, int JW>
@@ -250,7 +255,12 @@ __device__ __forceinline__ void fetch_ahead(const ScanArgs& a, unsigned long lon
     if (lane == 0) {
         n.alpha = __ldg(a.alpha + tok);
         n.beta = __ldg(a.beta + tok);
-        n.fwdmask = a.ring != nullptr ? __ldg(a.fwdmask + tok) : 0ull;
+        const size_t BT = (size_t)a.B * a.T;
+        // without the ring, nothing is handed over and every store is needed
+        n.fwdmask = a.ring != nullptr ? __ldg(a.masks + tok) : 0ull;
+        n.deadmask = a.ring != nullptr ? __ldg(a.masks + BT + tok) : 0ull;
+        n.war0 = __ldg(a.masks + 2 * BT + 2 * tok);
+        n.war1 = __ldg(a.masks + 2 * BT + 2 * tok + 1);
     }
 }
 
@@ -318,6 +328,9 @@ __device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
         if (lane == 0) {
             m.fmask = fmask;
             m.fwdmask = nx.fwdmask;
+            m.deadmask = nx.deadmask;
+            m.war[0] = nx.war0;
+            m.war[1] = nx.war1;
             m.wload = wload;
             m.rload = rload;
             m.tok = (long long)b * a.T + t;
@@ -357,12 +370,14 @@ __device__ void role_deps(const ScanArgs& a, unsigned char* wbuf, unsigned char*
         const Meta& m = meta[p];
         if (!m.valid)
             return;
-        const uint32_t depB = smem_u32(bars + kDepB + p);
+        const uint32_t depB = smem_u32(bars + kDepB + p), depR = smem_u32(bars + kDepR + p);
         const uint32_t cb = (uint32_t)m.rows * (uint32_t)sizeof(S);
         const int t = m.t, b = m.b, rb = m.rb;
         const int* fl = item_flag(a, b, rb, 0);
+        // references whose latest writer lies within the window: write chunks first
+        // (q < JW), then read chunks
         bool dep[JR];
-        int n = 0, nw = 0;
+        int nw = 0, nr = 0;
 #pragma unroll
         for (int q = 0; q < JR; ++q) {
             const int r = lane + 32 * q;
@@ -372,16 +387,18 @@ __device__ void role_deps(const ScanArgs& a, unsigned char* wbuf, unsigned char*
                 const int id = r < W ? m.wid[r] : m.rid[r - W];
                 dep[q] = id >= 0 && c != kNoFwd && (c >> 8) > 0;
             }
-            n += dep[q] ? 1 : 0;
             nw += (dep[q] && r < W) ? 1 : 0;
+            nr += (dep[q] && r >= W) ? 1 : 0;
         }
-        const int tot = __reduce_add_sync(0xFFFFFFFFu, n);
         const int totw = __reduce_add_sync(0xFFFFFFFFu, nw);
-        if (lane == 0)
-            mbar_arrive_expect_tx(depB, (uint32_t)tot * cb);
+        const int totr = __reduce_add_sync(0xFFFFFFFFu, nr);
+        if (lane == 0) {
+            mbar_arrive_expect_tx(depB, (uint32_t)totw * cb);
+            mbar_arrive_expect_tx(depR, (uint32_t)totr * cb);
+        }
         // write chunks go to the write buffer, free once item k-1 has taken its own
         bool ok = totw == 0 || k == 0 || uniform_wait(smem_u32(bars + kWfree), (k - 1) & 1, a);
-        uint32_t miss = (uint32_t)n * cb;
+        uint32_t missw = (uint32_t)nw * cb, missr = (uint32_t)nr * cb;
         // read the writers' flags together, then wait for the ones not yet published
         int got[JR];
 #pragma unroll
@@ -410,18 +427,22 @@ __device__ void role_deps(const ScanArgs& a, unsigned char* wbuf, unsigned char*
                 src = a.banks + (((size_t)b * a.N + id) * a.d + (size_t)rb * a.rb_rows) * sizeof(S);
             }
             unsigned char* dst = (is_w ? wbuf : rbuf + (size_t)p * W * kStride) + (size_t)j * kStride;
-            bulk_g2s(smem_u32(dst), src, cb, depB);
-            miss -= cb;
+            bulk_g2s(smem_u32(dst), src, cb, is_w ? depB : depR);
+            (is_w ? missw : missr) -= cb;
         }
         if (!__all_sync(0xFFFFFFFFu, ok)) {
             // declare what was not copied, wait (bounded) for what was, and leave
             if (lane == 0)
                 st_relaxed_gpu(a.abort_flag, 1);
-            const int mm = __reduce_add_sync(0xFFFFFFFFu, (int)miss);
+            const int mw = __reduce_add_sync(0xFFFFFFFFu, (int)missw);
+            const int mr = __reduce_add_sync(0xFFFFFFFFu, (int)missr);
             if (lane == 0) {
-                if (mm > 0)
-                    mbar_complete_tx(depB, (uint32_t)mm);
+                if (mw > 0)
+                    mbar_complete_tx(depB, (uint32_t)mw);
+                if (mr > 0)
+                    mbar_complete_tx(depR, (uint32_t)mr);
                 mbar_wait(depB, (k >> 1) & 1, nullptr, a.status);
+                mbar_wait(depR, (k >> 1) & 1, nullptr, a.status);
             }
             __syncwarp();
             return;
@@ -434,7 +455,6 @@ __device__ void role_deps(const ScanArgs& a, unsigned char* wbuf, unsigned char*
 template <int W>
 __device__ void role_clear(const ScanArgs& a, const Meta* meta, uint64_t* bars)
 {
-    constexpr int JW = (W + 31) / 32;
     const int lane = threadIdx.x & 31;
     for (int k = 0;; ++k) {
         const int p = k & 1;
@@ -445,23 +465,22 @@ __device__ void role_clear(const ScanArgs& a, const Meta* meta, uint64_t* bars)
             return;
         const int t = m.t;
         const int* fl = item_flag(a, m.b, m.rb, 0);
-        int wdt[JW];
-#pragma unroll
-        for (int jj = 0; jj < JW; ++jj) {
-            const int j = lane + 32 * jj;
-            const uint16_t c = j < W ? m.code[j] : kNoFwd;
-            wdt[jj] = (j < W && m.wid[j] >= 0 && c != kNoFwd) ? (c >> 8) : 0;
-        }
+        const unsigned long long war[2] = {m.war[0], m.war[1]};
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_u32(bars + kEmptyR + p));  // done with the item description
-        // write after read: tokens t-win .. t-1 have done their bank loads
-        bool ok = window_geq(a, fl, t - a.win, t, 1);
-        // write after write: in-window writers of our write slots have stored
+        // write after read: the tokens that reference a slot this token writes have done
+        // their bank loads (lane q watches dt = q+1, q+33, q+65, q+97). A token's
+        // in-window earlier writer of a slot never stores it (dead store), so there is
+        // no write-after-write wait.
+        bool ok = true;
 #pragma unroll
-        for (int jj = 0; jj < JW; ++jj)
-            if (ok && wdt[jj] > 0 && !spin_geq_gpu(fl + t - wdt[jj], 3, a.abort_flag, a.status))
+        for (int q = 0; q < 4; ++q) {
+            const int dt = lane + 32 * q + 1;
+            const bool need = (war[q >> 1] >> ((dt - 1) & 63)) & 1;
+            if (ok && need && !spin_geq_gpu(fl + t - dt, 1, a.abort_flag, a.status))
                 ok = false;
+        }
         if (!__all_sync(0xFFFFFFFFu, ok))
             return;
         fence_acq_rel_gpu();
@@ -496,7 +515,8 @@ __device__ void role_marks(const ScanArgs& a, const Meta* meta, uint64_t* bars)
                     end = kl;
                     progress = true;
                 } else if (a.ring != nullptr ||
-                           uniform_test(smem_u32(bars + kDepB + p), (kl >> 1) & 1)) {
+                           (uniform_test(smem_u32(bars + kDepB + p), (kl >> 1) & 1) &&
+                            uniform_test(smem_u32(bars + kDepR + p), (kl >> 1) & 1))) {
                     // (without the ring, dependent references are bank loads too)
                     if (lane == 0) {
                         red_max_release_gpu(item_flag(a, m.b, m.rb, m.t), 1);
@@ -703,6 +723,9 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_u32(bars + kFwdw + p));
+        // the read chunks D copies (writer still in flight when this item was described)
+        if (!uniform_wait(smem_u32(bars + kDepR + p), (k >> 1) & 1, a))
+            return;
         // read slots this token writes itself: their new values, from registers
         const unsigned long long fm = m.fmask;
         if (fm != 0) {
@@ -762,9 +785,11 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
         S* bank = reinterpret_cast<S*>(a.banks) + (size_t)m.b * a.N * a.d +
                   (size_t)m.rb * a.rb_rows + rg * RPL;
 #pragma unroll
+        const unsigned long long dead = m.deadmask;
+#pragma unroll
         for (int i = 0; i < SPL; ++i) {
             const int id = m.wid[i * kSG + sg];
-            if (act && id >= 0)
+            if (act && id >= 0 && !((dead >> (i * kSG + sg)) & 1))
                 __stcg(reinterpret_cast<uint4*>(bank + (size_t)id * a.d), Mv[i]);
         }
         __syncwarp();
@@ -793,6 +818,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a)
             mbar_init(smem_u32(bars + kFullR + p), kCWarps);
             mbar_init(smem_u32(bars + kEmptyR + p), 2);     // F1 + M
             mbar_init(smem_u32(bars + kDepB + p), 1);
+            mbar_init(smem_u32(bars + kDepR + p), 1);
             mbar_init(smem_u32(bars + kPosted + p), 1);
             mbar_init(smem_u32(bars + kWar + p), 1);
             mbar_init(smem_u32(bars + kFwdw + p), kCWarps);
@@ -864,7 +890,7 @@ ScanWs scan_ws_layout(const sdm_cfg& c, int B, int T)
     L.ring_entries = T < 2 * L.win ? (T > 0 ? T : 1) : 2 * L.win;
     size_t o = 0;
     L.codes = o; o += align256((size_t)B * T * 2 * c.w * 2);
-    L.fwdmask = o; o += align256((size_t)B * T * 8);
+    L.masks = o; o += align256((size_t)B * T * 32);
     L.flags = o; L.flags_bytes = align256((size_t)B * L.nrb * T * 4) + 256; o += L.flags_bytes;
     L.min_total = o;
     L.ring = o;
@@ -890,7 +916,7 @@ cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel,
     a.idx = idx;
     a.wsel = wsel;
     a.codes = (const uint16_t*)(base + L.codes);
-    a.fwdmask = (const unsigned long long*)(base + L.fwdmask);
+    a.masks = (const unsigned long long*)(base + L.masks);
     a.v = (const unsigned char*)v;
     a.alpha = alpha;
     a.beta = beta;

@@ -212,7 +212,7 @@ static int scan_impl(const sdm_cfg& c, const int32_t* idx, const float* wsel, co
     const ScanWs L = scan_ws_layout(c, B, T);
     char* base = (char*)ws;
     cudaError_t e = launch_scan_codes(c, idx, B, T, L.win, (uint16_t*)(base + L.codes),
-                                      (unsigned long long*)(base + L.fwdmask), dev_status, s);
+                                      (unsigned long long*)(base + L.masks), dev_status, s);
     if (e != cudaSuccess)
         return SDM_ECUDA;
     e = launch_scan(c, idx, wsel, v, alpha, beta, banks, y, B, T, ws, ws_bytes, dev_status, s);
@@ -236,7 +236,7 @@ int sdm_scan_prepare(const sdm_cfg* cfg, const int32_t* idx, int B, int T, void*
         return SDM_EWORKSPACE;
     char* base = (char*)ws;
     return cuda_status(launch_scan_codes(*cfg, idx, B, T, L.win, (uint16_t*)(base + L.codes),
-                                         (unsigned long long*)(base + L.fwdmask), dev_status,
+                                         (unsigned long long*)(base + L.masks), dev_status,
                                          (cudaStream_t)stream));
 }
 

@@ -34,19 +34,19 @@ cudaError_t launch_address(const sdm_cfg& c, const void* K1, const void* K2, con
 // ---- scan (scan.cu, scan_codes.cu)
 // Layout of the scan's workspace for B sequences of T tokens (byte offsets):
 //   codes    [B*T, 2, w] uint16  collision codes
-//   fwdmask  [B*T] uint64        write positions handed over through the ring
+//   masks    [4][B*T] uint64     per token: fwdmask, deadmask, warmask (2 words)
 //   flags    [B, nrb, T] int     progress of each (token, row block) item, then a
 //                                work counter and an abort flag (256 bytes)
 //   ring     [B*nrb, R, w, chunk] forwarding ring (R = min(T, 2*win) entries)
 // `min_total` covers codes..flags: with a workspace that small the scan runs without
 // the ring (a dependent reference then waits for its writer's bank store).
 struct ScanWs {
-    size_t codes, fwdmask, flags, flags_bytes, ring, ring_bytes, min_total, total;
+    size_t codes, masks, flags, flags_bytes, ring, ring_bytes, min_total, total;
     int win, nrb, rb_rows, ring_entries, chunk_bytes;
 };
 ScanWs scan_ws_layout(const sdm_cfg& c, int B, int T);
 cudaError_t launch_scan_codes(const sdm_cfg& c, const int32_t* idx, int B, int T, int win,
-                              uint16_t* codes, unsigned long long* fwdmask, int* status,
+                              uint16_t* codes, unsigned long long* masks, int* status,
                               cudaStream_t s);
 // Runs the recurrence; `ws` holds what launch_scan_codes wrote. ws_bytes >= L.total
 // enables the forwarding ring.

@@ -73,13 +73,13 @@ def test_noalloc_scan_matches_sdm_scan_twice():
 
 def test_noalloc_rejects_oversize_on_the_host():
     """More than SDM_SCAN_NOALLOC_MAX_BYTES of scratch (w = 64, d = 2048 bf16: more than
-    29957 tokens) is refused with SDM_EWORKSPACE before any device work."""
+    27592 tokens) is refused with SDM_EWORKSPACE before any device work."""
     from sparse_memory_linear_key_b300 import build
     build.build()
     L = sdm.lib()
     cfg = sdm.make_cfg(2048, 480, 256, 64, "bf16")
     P = ctypes.c_void_p
-    t_max = 29957
+    t_max = 27592
     assert sdm.scan_min_workspace_bytes(cfg, 1, t_max) <= sdm.SCAN_NOALLOC_MAX_BYTES
     assert sdm.scan_min_workspace_bytes(cfg, 1, t_max + 1) > sdm.SCAN_NOALLOC_MAX_BYTES
     rc = L.sdm_scan_noalloc(ctypes.byref(cfg), P(256), P(256), P(256), P(256), P(256), P(256),
