@@ -12,8 +12,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "lib")
 LIB = os.path.join(OUT_DIR, "libsdm.so")
-SOURCES = ["sdm_api.cu", "bank_init.cu", "project.cu", "address.cu", "scan_codes.cu", "scan.cu",
-           "scan_static.cu"]
+SOURCES = ["sdm_api.cu", "bank_init.cu", "project.cu", "address.cu", "score_tc.cu",
+           "scan_codes.cu", "scan.cu", "scan_static.cu"]
 HEADERS = ["sdm_common.cuh", "sdm_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

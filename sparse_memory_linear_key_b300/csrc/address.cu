@@ -2,9 +2,13 @@
 // depends only on the input ("Sparse Delta Memory" blog, "Write & Read": two sub-keys
 // -> outer sum -> top-k; softmax-weighted).
 //
-//   subkey_topw_kernel     s_h = K_h q_h for both halves of both queries, and the
-//                          top-W of each half, sorted (score desc, row asc).
-//   candidate_select_kernel  outer sums of the pairs of half-ranks (a, b) with
+//   score_tc_kernel        (score_tc.cu) s_h = K_h q_h for both halves of both queries
+//                          on the tensor cores, and the top-W of each half (bf16 layers)
+//   subkey_topw_kernel     the same on the SIMT cores in fp32 (fp32 layers and shapes
+//                          the tensor path does not take), lists sorted
+//                          (score desc, row asc)
+//   candidate_select_kernel  sorts each half's list, then outer sums of the pairs of
+//                          half-ranks (a, b) with
 //                          (a+1)(b+1) <= W -- the only pairs that can reach the top-W
 //                          of all n^2 sums -- their top-W, softmax, and the set in
 //                          ascending slot order.
@@ -83,7 +87,7 @@ __global__ void __launch_bounds__(256) subkey_topw_kernel(
 
 // One warp per (token, kind). Candidate pairs (a, b) of half-ranks come from a table
 // built in shared memory at block start.
-template <int EC, int EW>
+template <int EC, int EW, int EH>
 __global__ void __launch_bounds__(256) candidate_select_kernel(
     const float* __restrict__ hv, const int32_t* __restrict__ hi, int64_t ntok, int n, int W,
     int32_t* __restrict__ idx, float* __restrict__ wsel)
@@ -108,10 +112,26 @@ __global__ void __launch_bounds__(256) candidate_select_kernel(
         const int kind = (int)(qi / ntok);
         const int64_t tok = qi % ntok;
         const size_t base = ((size_t)kind * ntok + tok) * 2 * W;
-        __syncwarp();
-        for (int e = lane; e < 2 * W; e += 32) {
-            lv[warp][e / W][e % W] = hv[base + e];
-            li[warp][e / W][e % W] = hi[base + e];
+        // each half's W best rows, sorted (score desc, row asc): the tensor-core scoring
+        // writes them in row order
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint64_t hk[EH];
+#pragma unroll
+            for (int i = 0; i < EH; ++i) {
+                const int e = lane * EH + i;
+                hk[i] = e < W ? desc_key(hv[base + h * W + e], (uint32_t)hi[base + h * W + e]) : ~0ull;
+            }
+            warp_bitonic_sort<EH>(hk);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < EH; ++i) {
+                const int e = lane * EH + i;
+                if (e < W) {
+                    lv[warp][h][e] = key_score(hk[i]);
+                    li[warp][h][e] = (int)key_id(hk[i]);
+                }
+            }
         }
         __syncwarp();
         uint64_t key[EC];
@@ -218,7 +238,7 @@ static cudaError_t run_topw_e(const sdm_cfg& c, const void* K1, const void* K2, 
     return run_topw<IO, 16>(c, K1, K2, q_w, q_r, ntok, hv, hi, s);
 }
 
-template <int EC, int EW>
+template <int EC, int EW, int EH>
 static cudaError_t run_cand(const sdm_cfg& c, int64_t ntok, const float* hv, const int32_t* hi,
                             int32_t* idx, float* wsel, cudaStream_t s)
 {
@@ -226,7 +246,7 @@ static cudaError_t run_cand(const sdm_cfg& c, int64_t ntok, const float* hv, con
     int64_t blocks = (2 * ntok + 7) / 8;
     if (blocks > (int64_t)sms * 4)
         blocks = (int64_t)sms * 4;
-    candidate_select_kernel<EC, EW><<<(unsigned)blocks, 256, 0, s>>>(hv, hi, ntok, c.n_sub, c.w,
+    candidate_select_kernel<EC, EW, EH><<<(unsigned)blocks, 256, 0, s>>>(hv, hi, ntok, c.n_sub, c.w,
                                                                     idx, wsel);
     return cudaGetLastError();
 }
@@ -235,22 +255,25 @@ cudaError_t launch_address(const sdm_cfg& c, const void* K1, const void* K2, con
                            const void* q_r, int64_t ntok, int32_t* idx, float* wsel, void* ws,
                            int* status, cudaStream_t s)
 {
-    (void)status;
     if (ntok <= 0)
         return cudaSuccess;
     float* hv = (float*)ws;
     int32_t* hi = (int32_t*)((char*)ws + (size_t)2 * ntok * 2 * c.w * sizeof(float));
-    cudaError_t e = (c.dtype == SDM_BF16)
-                        ? run_topw_e<bf16>(c, K1, K2, q_w, q_r, ntok, hv, hi, s)
-                        : run_topw_e<float>(c, K1, K2, q_w, q_r, ntok, hv, hi, s);
+    // bf16 layers score on the tensor cores; fp32 layers (exact fp32 products) and other
+    // shapes on the SIMT kernel
+    cudaError_t e = score_tc_supported(c)
+                        ? launch_score_tc(c, K1, K2, q_w, q_r, ntok, hv, hi, status, s)
+                        : (c.dtype == SDM_BF16)
+                              ? run_topw_e<bf16>(c, K1, K2, q_w, q_r, ntok, hv, hi, s)
+                              : run_topw_e<float>(c, K1, K2, q_w, q_r, ntok, hv, hi, s);
     if (e != cudaSuccess)
         return e;
     const int C = candidate_count(c.w);
     switch (c.w) {
-    case 8: return run_cand<1, 1>(c, ntok, hv, hi, idx, wsel, s);      // 20 candidates
-    case 16: return run_cand<2, 1>(c, ntok, hv, hi, idx, wsel, s);     // 50
-    case 32: return run_cand<4, 1>(c, ntok, hv, hi, idx, wsel, s);     // 119
-    case 64: return run_cand<16, 2>(c, ntok, hv, hi, idx, wsel, s);    // 280
+    case 8: return run_cand<1, 1, 1>(c, ntok, hv, hi, idx, wsel, s);      // 20 candidates
+    case 16: return run_cand<2, 1, 1>(c, ntok, hv, hi, idx, wsel, s);     // 50
+    case 32: return run_cand<4, 1, 1>(c, ntok, hv, hi, idx, wsel, s);     // 119
+    case 64: return run_cand<16, 2, 2>(c, ntok, hv, hi, idx, wsel, s);    // 280
     default: (void)C; return cudaErrorInvalidValue;
     }
 }

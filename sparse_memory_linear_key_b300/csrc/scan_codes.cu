@@ -131,12 +131,15 @@ __global__ void __launch_bounds__(256) codes_kernel(const int32_t* __restrict__ 
                 }
             }
         } else {
-            // write: the latest earlier writer, and every earlier referencing token
+            // write: the latest earlier writer, and every earlier referencing token; only
+            // the lists the bitmaps say can hold the slot are searched
+            const uint32_t mb = 1u << (s & 31);
+            const bool other_w = (twice[s >> 5] & mb) != 0, any_r = (rref[s >> 5] & mb) != 0;
             unsigned long long war0 = 0, war1 = 0;
             for (int dt = 1; dt <= win && t - dt >= base; ++dt) {
                 const int tp = t - dt - base;
-                const int pw = find_sorted(wl + tp * W, W, s);
-                const bool ref = pw >= 0 || find_sorted(rl + tp * W, W, s) >= 0;
+                const int pw = other_w ? find_sorted(wl + tp * W, W, s) : -1;
+                const bool ref = pw >= 0 || (any_r && find_sorted(rl + tp * W, W, s) >= 0);
                 if (pw >= 0 && code == kNoFwd) {
                     code = (uint16_t)((dt << 8) | pw);
                     atomicOr(fwdmask + (size_t)b * T + t - dt, 1ull << pw);

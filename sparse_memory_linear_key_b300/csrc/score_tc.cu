@@ -1,0 +1,451 @@
+// score_tc.cu -- sub-key scores and per-half top-W on the tensor cores (bf16 layers).
+//
+// Product-key addressing ("Sparse Delta Memory" blog, "Write & Read": two sub-keys ->
+// outer sum -> top-k) scores every query half against its sub-key table:
+//   s_h[q][i] = <K_h[i], q_h>   for the n rows of K_h, both halves, write and read queries.
+// Over all tokens that is a dense GEMM [2*ntok, dk/2] x [dk/2, n] per half, and this
+// kernel runs it on the 5th-generation tensor cores:
+//  * one CTA per SM works on one half; the half's sub-key table (n <= 512 rows) is
+//    loaded once by TMA into shared memory in the 128-byte-swizzled K-major layout the
+//    MMA reads, and 128-query tiles stream through two TMA stages;
+//  * one thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M = 128, N = 256
+//    twice) into a 512-column TMEM accumulator: row r of the tile in TMEM lane r;
+//  * four epilogue warps (one per TMEM lane quadrant) keep, per row, the W largest
+//    scores by (score desc, row asc): a first pass replaces each score in TMEM by its
+//    order-preserving integer image (tcgen05.st), a bisection over those keys finds
+//    the W-th largest (stopping early once exactly W keys lie at or above the probe;
+//    one compare per element a pass), and a last pass writes the kept (score, row)
+//    pairs, ties at the threshold by ascending row.
+// The per-half lists are written unsorted; the candidate kernel sorts them.
+// Every wait is bounded (status SDM_ETIMEOUT); on time-out a role stops issuing, the
+// CTA waits (bounded) for its copies and MMAs in flight and frees its TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "sdm_common.cuh"
+#include "sdm_internal.h"
+
+namespace sdm {
+
+namespace {
+
+constexpr int kTileM = 128;               // queries per tile
+constexpr int kKAtom = 64;                // bf16 elements per 128-byte swizzle row
+constexpr int kBRows = 512;               // sub-key rows staged (n padded)
+constexpr int kTmemCols = 512;
+constexpr int kThreads = 192;             // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr uint32_t kBBytes = kBRows * 128 * 2;        // two K atoms of 512 rows
+constexpr uint32_t kABytes = kTileM * 128 * 2;        // two K atoms of 128 rows
+
+struct ScoreArgs {
+    int ntok, n, khalf, W, tiles_per_kind, ctas_per_half;
+    float* hv;
+    int32_t* hi;
+    int* status;
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// the mbarrier arrives once every MMA this thread issued so far has completed
+__device__ __forceinline__ void tc_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]),
+        "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]),
+        "r"(v[30]), "r"(v[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+          "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle layout
+// (8-row groups of 1024 bytes, rows of 128 bytes), start address 16-byte units.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);          // start address
+    d |= (uint64_t)1 << 16;                            // leading byte offset (unused here)
+    d |= (uint64_t)(1024 >> 4) << 32;                  // stride byte offset: 8 rows
+    d |= (uint64_t)1 << 46;                            // descriptor version
+    d |= (uint64_t)2 << 61;                            // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: kind::f16 with bf16 A and B, fp32 D, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// Order-preserving integer image of an fp32 score (larger score, larger key; -0 folds
+// to +0). Every real score maps to a key >= 0x007FFFFF, so 0 marks padding columns.
+__device__ __forceinline__ uint32_t order_key(uint32_t bits)
+{
+    const uint32_t u = __float_as_uint(__uint_as_float(bits) + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_to_score(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// ------------------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
+    const __grid_constant__ CUtensorMap map_qw, const __grid_constant__ CUtensorMap map_qr,
+    const __grid_constant__ CUtensorMap map_k1, const __grid_constant__ CUtensorMap map_k2,
+    ScoreArgs a)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 1024-byte aligned base for the swizzled operands
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char* sp = smem_raw + (base - raw);
+    const uint32_t sB = base, sA0 = base + kBBytes, sA1 = base + kBBytes + kABytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sp + kBBytes + 2 * kABytes);
+    // bars: 0 B loaded, 1..2 A stage full, 3..4 A stage empty, 5 TMEM full, 6 TMEM empty
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+    __shared__ int dead;                 // a role gave up: the others stop at their next wait
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int half = blockIdx.x / a.ctas_per_half;
+    const int cta = blockIdx.x % a.ctas_per_half;
+    const int ntiles = 2 * a.tiles_per_kind;
+    const int my_tiles = cta < ntiles ? (ntiles - cta + a.ctas_per_half - 1) / a.ctas_per_half : 0;
+    const int NP = (a.n + 15) & ~15;     // MMA N over all chunks
+    const int katoms = a.khalf / kKAtom;
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(bars + 0), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(bars + 1 + s), 1);
+            mbar_init(smem_u32(bars + 3 + s), 1);
+        }
+        mbar_init(smem_u32(bars + 5), 1);
+        mbar_init(smem_u32(bars + 6), 4);
+        dead = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    int* stat = a.status;
+    auto waitb = [&](uint32_t bar, uint32_t parity) -> bool {
+        // bounded, and gives up early once another role has given up
+        if (mbar_try_wait(bar, parity))
+            return true;
+        const long long t0 = clock64();
+        while (!mbar_try_wait(bar, parity)) {
+            if (*(volatile int*)&dead)
+                return false;
+            if (clock64() - t0 > kSpinLimitCycles) {
+                report(stat, SDM_ETIMEOUT);
+                *(volatile int*)&dead = 1;
+                return false;
+            }
+        }
+        return true;
+    };
+
+    if (warp == 0) {
+        // ---------------- TMA producer: the sub-key table once, then query tiles
+        if (lane == 0 && my_tiles > 0) {
+            const CUtensorMap* mk = half ? &map_k2 : &map_k1;
+            const uint32_t bB = smem_u32(bars + 0);
+            mbar_arrive_expect_tx(bB, (uint32_t)katoms * 2 * 256 * 128);
+            for (int kb = 0; kb < katoms; ++kb)
+                for (int nc = 0; nc < 2; ++nc)
+                    tma_load_2d(sB + kb * (kBBytes / 2) + nc * 256 * 128, mk, kb * kKAtom, nc * 256, bB);
+            int armed[2] = {-1, -1};
+            for (int i = 0; i < my_tiles; ++i) {
+                const int s = i & 1;
+                if (i >= 2 && !waitb(smem_u32(bars + 3 + s), ((i - 2) >> 1) & 1))
+                    break;
+                const int tl = cta + i * a.ctas_per_half;
+                const int kind = tl / a.tiles_per_kind;
+                const int row0 = (tl % a.tiles_per_kind) * kTileM;
+                const CUtensorMap* mq = kind ? &map_qr : &map_qw;
+                const uint32_t fb = smem_u32(bars + 1 + s);
+                const uint32_t dst = s ? sA1 : sA0;
+                mbar_arrive_expect_tx(fb, (uint32_t)katoms * kTileM * 128);
+                for (int kb = 0; kb < katoms; ++kb)
+                    tma_load_2d(dst + kb * (kABytes / 2), mq, half * a.khalf + kb * kKAtom, row0, fb);
+                armed[s] = i;
+            }
+            // copies in flight land before the CTA may end
+            mbar_wait(bB, 0, nullptr, stat);
+            for (int s = 0; s < 2; ++s)
+                if (armed[s] >= 0)
+                    mbar_wait(smem_u32(bars + 1 + s), (armed[s] >> 1) & 1, nullptr, stat);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0 && my_tiles > 0) {
+            bool ok = waitb(smem_u32(bars + 0), 0);
+            int issued = -1;
+            for (int i = 0; ok && i < my_tiles; ++i) {
+                const int s = i & 1;
+                ok = waitb(smem_u32(bars + 1 + s), (i >> 1) & 1);
+                // the accumulator is free once the epilogue has read the previous tile
+                if (ok && i >= 1)
+                    ok = waitb(smem_u32(bars + 6), (i - 1) & 1);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                const uint32_t aBase = s ? sA1 : sA0;
+                for (int nc = 0; nc * 256 < NP; ++nc) {
+                    const int N = min(256, NP - nc * 256);
+                    const uint32_t idesc = idesc_bf16(kTileM, N);
+                    for (int kb = 0; kb < katoms; ++kb)
+                        for (int kk = 0; kk < kKAtom / 16; ++kk) {
+                            const uint64_t ad = sw128_desc(aBase + kb * (kABytes / 2) + kk * 32);
+                            const uint64_t bd =
+                                sw128_desc(sB + kb * (kBBytes / 2) + nc * 256 * 128 + kk * 32);
+                            tc_mma(tmem + nc * 256, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+                        }
+                }
+                tc_commit(smem_u32(bars + 3 + s));   // the A stage may be refilled
+                tc_commit(smem_u32(bars + 5));       // the scores are in TMEM
+                issued = i;
+            }
+            // MMAs in flight complete before TMEM is freed
+            if (issued >= 0)
+                mbar_wait(smem_u32(bars + 5), issued & 1, nullptr, stat);
+        }
+    } else {
+        // ---------------- epilogue: per-row top-W of the scores
+        const int q = warp & 3;                          // TMEM lane quadrant of this warp
+        const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+        const int W = a.W;
+        for (int i = 0; i < my_tiles; ++i) {
+            if (!__all_sync(0xFFFFFFFFu, waitb(smem_u32(bars + 5), i & 1)))
+                break;
+            tc_fence_after();
+            const int tl = cta + i * a.ctas_per_half;
+            const int kind = tl / a.tiles_per_kind;
+            const int tok = (tl % a.tiles_per_kind) * kTileM + q * 32 + lane;
+            uint32_t v[32];
+            // keys in place of the scores (0 in padding columns), and their range
+            uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+            for (int c0 = 0; c0 < NP; c0 += 32) {
+                tmem_ld32(trow + c0, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const uint32_t k = c0 + j < a.n ? order_key(v[j]) : 0u;
+                    if (c0 + j < a.n) {
+                        kmin = min(kmin, k);
+                        kmax = max(kmax, k);
+                    }
+                    v[j] = k;
+                }
+                tmem_st32(trow + c0, v);
+            }
+            // bisection: at least W keys lie at or above lo, fewer than W at or above hi
+            uint32_t lo = kmin, hi = kmax + 1;
+            int cnt_hi = 0;
+            bool exact = false;
+            while (__any_sync(0xFFFFFFFFu, !exact && hi - lo > 1)) {
+                const bool active = !exact && hi - lo > 1;
+                const uint32_t mid = lo + ((hi - lo) >> 1);
+                int cnt = 0;
+                for (int c0 = 0; c0 < NP; c0 += 32) {
+                    tmem_ld32(trow + c0, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        cnt += v[j] >= mid ? 1 : 0;
+                }
+                if (active) {
+                    if (cnt == W) {
+                        lo = mid;
+                        exact = true;
+                    } else if (cnt > W) {
+                        lo = mid;
+                    } else {
+                        hi = mid;
+                        cnt_hi = cnt;
+                    }
+                }
+            }
+            // keep: keys >= lo when exactly W lie there, else keys >= hi and the
+            // lowest-numbered rows among those equal to lo
+            const int need_ties = exact ? 0 : W - cnt_hi;
+            int pos = 0, ties = 0;
+            const size_t ob = (((size_t)kind * a.ntok + tok) * 2 + half) * W;
+            const bool row_ok = tok < a.ntok;
+            for (int c0 = 0; c0 < NP; c0 += 32) {
+                tmem_ld32(trow + c0, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const uint32_t k = v[j];
+                    bool keep;
+                    if (exact) {
+                        keep = k >= lo;
+                    } else {
+                        keep = k >= hi;
+                        if (!keep && k == lo && ties < need_ties) {
+                            keep = true;
+                            ++ties;
+                        }
+                    }
+                    if (keep && row_ok && pos < W) {
+                        a.hv[ob + pos] = key_to_score(k);
+                        a.hi[ob + pos] = c0 + j;
+                        ++pos;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(bars + 6));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
+}
+
+// ------------------------------------------------------------------------- host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2D bf16 row-major tensor [rows, cols], box {64 columns, box_rows}, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_rows)
+{
+    auto enc = encode_fn();
+    if (enc == nullptr)
+        return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kKAtom, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool score_tc_supported(const sdm_cfg& c)
+{
+    const int h = c.dk / 2;
+    return c.dtype == SDM_BF16 && (h == 64 || h == 128) && c.n_sub <= kBRows && c.w <= 64 &&
+           encode_fn() != nullptr;
+}
+
+cudaError_t launch_score_tc(const sdm_cfg& c, const void* K1, const void* K2, const void* q_w,
+                            const void* q_r, int64_t ntok, float* hv, int32_t* hi, int* status,
+                            cudaStream_t s)
+{
+    if (ntok <= 0)
+        return cudaSuccess;
+    const int h = c.dk / 2;
+    CUtensorMap mqw, mqr, mk1, mk2;
+    if (!make_map(&mqw, q_w, (uint64_t)c.dk, (uint64_t)ntok, kTileM) ||
+        !make_map(&mqr, q_r, (uint64_t)c.dk, (uint64_t)ntok, kTileM) ||
+        !make_map(&mk1, K1, (uint64_t)h, (uint64_t)c.n_sub, 256) ||
+        !make_map(&mk2, K2, (uint64_t)h, (uint64_t)c.n_sub, 256))
+        return cudaErrorInvalidValue;
+    ScoreArgs a;
+    a.ntok = (int)ntok;
+    a.n = c.n_sub;
+    a.khalf = h;
+    a.W = c.w;
+    a.tiles_per_kind = (int)((ntok + kTileM - 1) / kTileM);
+    int per_half = num_sms_current_device() / 2;
+    if (per_half > 2 * a.tiles_per_kind)
+        per_half = 2 * a.tiles_per_kind;
+    if (per_half < 1)
+        per_half = 1;
+    a.ctas_per_half = per_half;
+    a.hv = hv;
+    a.hi = hi;
+    a.status = status;
+    const size_t smem = 1024 + kBBytes + 2 * kABytes + 8 * sizeof(uint64_t) + 16;
+    cudaError_t e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    score_tc_kernel<<<2 * per_half, kThreads, smem, s>>>(mqw, mqr, mk1, mk2, a);
+    return cudaGetLastError();
+}
+
+}  // namespace sdm

@@ -25,7 +25,11 @@ cudaError_t launch_bank_init(const void* M0, void* banks, size_t bank_bytes, int
 int launch_project(const sdm_cfg& c, const sdm_weights& w, const void* x, int64_t ntok,
                    void* q_w, void* q_r, void* v, cudaStream_t s);
 
-// ---- addressing (address.cu)
+// ---- addressing (address.cu, score_tc.cu)
+bool score_tc_supported(const sdm_cfg& c);
+cudaError_t launch_score_tc(const sdm_cfg& c, const void* K1, const void* K2, const void* q_w,
+                            const void* q_r, int64_t ntok, float* hv, int32_t* hi, int* status,
+                            cudaStream_t s);
 size_t address_ws_bytes(const sdm_cfg& c, int64_t ntok);
 cudaError_t launch_address(const sdm_cfg& c, const void* K1, const void* K2, const void* q_w,
                            const void* q_r, int64_t ntok, int32_t* idx, float* wsel, void* ws,
