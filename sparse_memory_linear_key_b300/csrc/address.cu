@@ -7,11 +7,11 @@
 //   subkey_topw_kernel     the same on the SIMT cores in fp32 (fp32 layers and shapes
 //                          the tensor path does not take), lists sorted
 //                          (score desc, row asc)
-//   candidate_select_kernel  sorts each half's list, then outer sums of the pairs of
-//                          half-ranks (a, b) with
-//                          (a+1)(b+1) <= W -- the only pairs that can reach the top-W
-//                          of all n^2 sums -- their top-W, softmax, and the set in
-//                          ascending slot order.
+//   candidate_select_kernel  sorts each half's list, then forms the outer sums of the
+//                          pairs of half-ranks (a, b) with (a+1)(b+1) <= W -- the only
+//                          pairs that can reach the top-W of all n^2 sums -- keeps their
+//                          top-W (bisection over the sums), takes the softmax, and reports
+//                          the set in ascending slot order.
 #include <algorithm>
 
 #include "sdm_common.cuh"
@@ -87,12 +87,20 @@ __global__ void __launch_bounds__(256) subkey_topw_kernel(
 
 // One warp per (token, kind). Candidate pairs (a, b) of half-ranks come from a table
 // built in shared memory at block start.
-template <int EC, int EW, int EH>
+__device__ __forceinline__ float __reduce_add_sync_f(float x)
+{
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1)
+        x += __shfl_xor_sync(0xFFFFFFFFu, x, m);
+    return x;
+}
+
+template <int NC, int EW, int EH>
 __global__ void __launch_bounds__(256) candidate_select_kernel(
     const float* __restrict__ hv, const int32_t* __restrict__ hi, int64_t ntok, int n, int W,
     int32_t* __restrict__ idx, float* __restrict__ wsel)
 {
-    __shared__ unsigned short pairs[32 * EC];     // (a << 8) | b
+    __shared__ unsigned short pairs[32 * NC];     // (a << 8) | b
     __shared__ int npairs;
     __shared__ float lv[8][2][64];
     __shared__ int li[8][2][64];
@@ -134,38 +142,82 @@ __global__ void __launch_bounds__(256) candidate_select_kernel(
             }
         }
         __syncwarp();
-        uint64_t key[EC];
+        // The W largest candidate sums by (sum desc, slot asc): bisection over the
+        // order-preserving keys of the sums (NC candidates a lane), stopping once exactly W
+        // keys lie at or above the probe; equal sums at the threshold go to the lower slot.
+        uint32_t ck[NC], cs[NC];
+        float cv[NC];
+        uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
 #pragma unroll
-        for (int i = 0; i < EC; ++i) {
-            const int c = lane * EC + i;
+        for (int i = 0; i < NC; ++i) {
+            const int c = lane + 32 * i;
+            ck[i] = 0u;                                    // below every real key
+            cv[i] = 0.0f;
+            cs[i] = 0xFFFFFFFFu;
             if (c < C) {
                 const int a = pairs[c] >> 8, b = pairs[c] & 0xFF;
-                const float s = lv[warp][0][a] + lv[warp][1][b];
-                const uint32_t slot = (uint32_t)li[warp][0][a] * (uint32_t)n + (uint32_t)li[warp][1][b];
-                key[i] = desc_key(s, slot);
-            } else {
-                key[i] = ~0ull;
+                cv[i] = lv[warp][0][a] + lv[warp][1][b];
+                cs[i] = (uint32_t)li[warp][0][a] * (uint32_t)n + (uint32_t)li[warp][1][b];
+                ck[i] = float_order_bits(cv[i]);
+                kmin = min(kmin, ck[i]);
+                kmax = max(kmax, ck[i]);
             }
         }
-        warp_bitonic_sort<EC>(key);
-        // softmax over the W kept scores (elements 0..W-1); element 0 is the max
-        const float mx = __shfl_sync(0xFFFFFFFFu, key_score(key[0]), 0);
-        float ex[EC];
+        kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+        kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+        uint32_t lo = kmin, hi = kmax + 1;
+        int cnt_hi = 0;
+        bool exact = false;
+        while (!exact && hi - lo > 1) {
+            const uint32_t mid = lo + ((hi - lo) >> 1);
+            int c = 0;
+#pragma unroll
+            for (int i = 0; i < NC; ++i)
+                c += ck[i] >= mid ? 1 : 0;
+            c = __reduce_add_sync(0xFFFFFFFFu, c);
+            if (c == W) {
+                lo = mid;
+                exact = true;
+            } else if (c > W) {
+                lo = mid;
+            } else {
+                hi = mid;
+                cnt_hi = c;
+            }
+        }
+        bool keep[NC];
+#pragma unroll
+        for (int i = 0; i < NC; ++i)
+            keep[i] = exact ? ck[i] >= lo : ck[i] >= hi;
+        for (int need = exact ? 0 : W - cnt_hi; need > 0; --need) {
+            // the lowest slot among the equal sums not yet kept
+            uint32_t best = 0xFFFFFFFFu;
+#pragma unroll
+            for (int i = 0; i < NC; ++i)
+                if (!keep[i] && ck[i] == lo)
+                    best = min(best, cs[i]);
+            best = __reduce_min_sync(0xFFFFFFFFu, best);
+#pragma unroll
+            for (int i = 0; i < NC; ++i)
+                if (!keep[i] && ck[i] == lo && cs[i] == best)
+                    keep[i] = true;
+        }
+        // softmax over the kept sums (the largest one is the largest of all)
+        const float mx = float_from_order_bits(kmax);
         float part = 0.0f;
 #pragma unroll
-        for (int i = 0; i < EC; ++i) {
-            const int e = lane * EC + i;
-            ex[i] = (e < W) ? expf(key_score(key[i]) - mx) : 0.0f;
-            part += ex[i];
-        }
+        for (int i = 0; i < NC; ++i)
+            part += keep[i] ? expf(cv[i] - mx) : 0.0f;
+        part = __reduce_add_sync_f(part);
+        int base_pos = 0;
 #pragma unroll
-        for (int m = 16; m > 0; m >>= 1)
-            part += __shfl_xor_sync(0xFFFFFFFFu, part, m);
-#pragma unroll
-        for (int i = 0; i < EC; ++i) {
-            const int e = lane * EC + i;
-            if (e < W)
-                sel[warp][e] = ((uint64_t)key_id(key[i]) << 32) | __float_as_uint(ex[i] / part);
+        for (int i = 0; i < NC; ++i) {
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep[i]);
+            if (keep[i]) {
+                const int pos = base_pos + __popc(bal & ((1u << lane) - 1u));
+                sel[warp][pos] = ((uint64_t)cs[i] << 32) | __float_as_uint(expf(cv[i] - mx) / part);
+            }
+            base_pos += __popc(bal);
         }
         __syncwarp();
         // report the set in ascending slot order, weights alongside
@@ -238,7 +290,7 @@ static cudaError_t run_topw_e(const sdm_cfg& c, const void* K1, const void* K2, 
     return run_topw<IO, 16>(c, K1, K2, q_w, q_r, ntok, hv, hi, s);
 }
 
-template <int EC, int EW, int EH>
+template <int NC, int EW, int EH>
 static cudaError_t run_cand(const sdm_cfg& c, int64_t ntok, const float* hv, const int32_t* hi,
                             int32_t* idx, float* wsel, cudaStream_t s)
 {
@@ -246,7 +298,7 @@ static cudaError_t run_cand(const sdm_cfg& c, int64_t ntok, const float* hv, con
     int64_t blocks = (2 * ntok + 7) / 8;
     if (blocks > (int64_t)sms * 4)
         blocks = (int64_t)sms * 4;
-    candidate_select_kernel<EC, EW, EH><<<(unsigned)blocks, 256, 0, s>>>(hv, hi, ntok, c.n_sub, c.w,
+    candidate_select_kernel<NC, EW, EH><<<(unsigned)blocks, 256, 0, s>>>(hv, hi, ntok, c.n_sub, c.w,
                                                                     idx, wsel);
     return cudaGetLastError();
 }
@@ -273,7 +325,7 @@ cudaError_t launch_address(const sdm_cfg& c, const void* K1, const void* K2, con
     case 8: return run_cand<1, 1, 1>(c, ntok, hv, hi, idx, wsel, s);      // 20 candidates
     case 16: return run_cand<2, 1, 1>(c, ntok, hv, hi, idx, wsel, s);     // 50
     case 32: return run_cand<4, 1, 1>(c, ntok, hv, hi, idx, wsel, s);     // 119
-    case 64: return run_cand<16, 2, 2>(c, ntok, hv, hi, idx, wsel, s);    // 280
+    case 64: return run_cand<9, 2, 2>(c, ntok, hv, hi, idx, wsel, s);     // 280
     default: (void)C; return cudaErrorInvalidValue;
     }
 }

@@ -10,8 +10,9 @@
 //    MMA reads, and 128-query tiles stream through two TMA stages;
 //  * one thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M = 128, N = 256
 //    twice) into a 512-column TMEM accumulator: row r of the tile in TMEM lane r;
-//  * four epilogue warps (one per TMEM lane quadrant) keep, per row, the W largest
-//    scores by (score desc, row asc): a first pass replaces each score in TMEM by its
+//  * sixteen epilogue warps (four per TMEM lane quadrant, one column group each) keep,
+//    per row, the W largest scores by (score desc, row asc): a first pass replaces
+//    each score in TMEM by its
 //    order-preserving integer image (tcgen05.st), a bisection over those keys finds
 //    the W-th largest (stopping early once exactly W keys lie at or above the probe;
 //    one compare per element a pass), and a last pass writes the kept (score, row)
@@ -35,7 +36,8 @@ constexpr int kTileM = 128;               // queries per tile
 constexpr int kKAtom = 64;                // bf16 elements per 128-byte swizzle row
 constexpr int kBRows = 512;               // sub-key rows staged (n padded)
 constexpr int kTmemCols = 512;
-constexpr int kThreads = 192;             // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kEpiWarps = 16;             // four per TMEM lane quadrant, one column group each
+constexpr int kThreads = 32 * (2 + kEpiWarps);  // warp 0 TMA, warp 1 MMA, then the epilogue
 constexpr uint32_t kBBytes = kBRows * 128 * 2;        // two K atoms of 512 rows
 constexpr uint32_t kABytes = kTileM * 128 * 2;        // two K atoms of 128 rows
 
@@ -77,6 +79,26 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
+}
+
+__device__ __forceinline__ void bar_sync(int id, int n)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// barrier over n threads that also returns whether `ok` holds in all of them
+__device__ __forceinline__ bool bar_all(int id, int n, bool ok)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.and.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32])
@@ -159,6 +181,12 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
     uint64_t* bars = reinterpret_cast<uint64_t*>(sp + kBBytes + 2 * kABytes);
     // bars: 0 B loaded, 1..2 A stage full, 3..4 A stage empty, 5 TMEM full, 6 TMEM empty
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+    // exchange between the four epilogue warps of a quadrant: [quadrant][group][lane]
+    uint32_t* xmin = tmem_slot + 4;                  // 512 each
+    uint32_t* xmax = xmin + 512;
+    int* xcnt = reinterpret_cast<int*>(xmax + 512);  // [2 parities][512]
+    int* xa = xcnt + 1024;
+    int* xt = xa + 512;
     __shared__ int dead;                 // a role gave up: the others stop at their next wait
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -176,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
             mbar_init(smem_u32(bars + 3 + s), 1);
         }
         mbar_init(smem_u32(bars + 5), 1);
-        mbar_init(smem_u32(bars + 6), 4);
+        mbar_init(smem_u32(bars + 6), kEpiWarps);
         dead = 0;
         fence_mbarrier_init();
     }
@@ -275,12 +303,23 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
                 mbar_wait(smem_u32(bars + 5), issued & 1, nullptr, stat);
         }
     } else {
-        // ---------------- epilogue: per-row top-W of the scores
-        const int q = warp & 3;                          // TMEM lane quadrant of this warp
+        // ---------------- epilogue: per-row top-W of the scores. Warp e = warp - 2 reads
+        // TMEM lane quadrant q = warp % 4 (the quadrant a warp may access) and column
+        // group g = e / 4; the four warps of a quadrant add up their counts per row
+        // through shared memory at a named barrier (id 1 + q). They run the same number
+        // of barrier rounds (same rows, same totals) and leave together, so none can be
+        // left waiting at a barrier.
+        const int q = warp & 3, g = (warp - 2) >> 2;
+        const int bid = 1 + q;
         const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
         const int W = a.W;
+        const int CW = ((NP + 4 * 32 - 1) / (4 * 32)) * 32;       // columns a group reads
+        const int cb = min(NP, g * CW), ce = min(NP, cb + CW);
+        const int xi = (q * 4 + g) * 32 + lane;                     // own exchange slot
+        const int xq = q * 4 * 32 + lane;                           // group 0 of this lane
         for (int i = 0; i < my_tiles; ++i) {
-            if (!__all_sync(0xFFFFFFFFu, waitb(smem_u32(bars + 5), i & 1)))
+            const bool got = waitb(smem_u32(bars + 5), i & 1);
+            if (!bar_all(bid, 128, got))
                 break;
             tc_fence_after();
             const int tl = cta + i * a.ctas_per_half;
@@ -289,12 +328,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
             uint32_t v[32];
             // keys in place of the scores (0 in padding columns), and their range
             uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-            for (int c0 = 0; c0 < NP; c0 += 32) {
+            for (int c0 = cb; c0 < ce; c0 += 32) {
                 tmem_ld32(trow + c0, v);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const uint32_t k = c0 + j < a.n ? order_key(v[j]) : 0u;
-                    if (c0 + j < a.n) {
+                    const bool valid = c0 + j < a.n;
+                    const uint32_t k = valid ? order_key(v[j]) : 0u;
+                    if (valid) {
                         kmin = min(kmin, k);
                         kmax = max(kmax, k);
                     }
@@ -302,20 +342,32 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
                 }
                 tmem_st32(trow + c0, v);
             }
+            xmin[xi] = kmin;
+            xmax[xi] = kmax;
+            bar_sync(bid, 128);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                kmin = min(kmin, xmin[xq + h * 32]);
+                kmax = max(kmax, xmax[xq + h * 32]);
+            }
             // bisection: at least W keys lie at or above lo, fewer than W at or above hi
             uint32_t lo = kmin, hi = kmax + 1;
             int cnt_hi = 0;
             bool exact = false;
-            while (__any_sync(0xFFFFFFFFu, !exact && hi - lo > 1)) {
+            for (int it = 0; __any_sync(0xFFFFFFFFu, !exact && hi - lo > 1); ++it) {
                 const bool active = !exact && hi - lo > 1;
                 const uint32_t mid = lo + ((hi - lo) >> 1);
                 int cnt = 0;
-                for (int c0 = 0; c0 < NP; c0 += 32) {
+                for (int c0 = cb; c0 < ce; c0 += 32) {
                     tmem_ld32(trow + c0, v);
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         cnt += v[j] >= mid ? 1 : 0;
                 }
+                int* xc = xcnt + (it & 1) * 512;
+                xc[xi] = cnt;
+                bar_sync(bid, 128);
+                cnt = xc[xq] + xc[xq + 32] + xc[xq + 64] + xc[xq + 96];
                 if (active) {
                     if (cnt == W) {
                         lo = mid;
@@ -329,25 +381,40 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
                 }
             }
             // keep: keys >= lo when exactly W lie there, else keys >= hi and the
-            // lowest-numbered rows among those equal to lo
-            const int need_ties = exact ? 0 : W - cnt_hi;
-            int pos = 0, ties = 0;
+            // lowest-numbered rows among those equal to lo (taken in column order, so a
+            // group takes ties only after the groups of lower columns)
+            const int need = exact ? 0 : W - cnt_hi;
+            int ka = 0, kt = 0;
+            for (int c0 = cb; c0 < ce; c0 += 32) {
+                tmem_ld32(trow + c0, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    ka += (exact ? v[j] >= lo : v[j] >= hi) ? 1 : 0;
+                    kt += (!exact && v[j] == lo) ? 1 : 0;
+                }
+            }
+            xa[xi] = ka;
+            xt[xi] = kt;
+            bar_sync(bid, 128);
+            int pre_a = 0, pre_t = 0;
+            for (int h = 0; h < g; ++h) {
+                pre_a += xa[xq + h * 32];
+                pre_t += xt[xq + h * 32];
+            }
+            int pos = pre_a + min(pre_t, need);
+            const int allow = max(0, min(kt, need - pre_t));
+            int ties = 0;
             const size_t ob = (((size_t)kind * a.ntok + tok) * 2 + half) * W;
             const bool row_ok = tok < a.ntok;
-            for (int c0 = 0; c0 < NP; c0 += 32) {
+            for (int c0 = cb; c0 < ce; c0 += 32) {
                 tmem_ld32(trow + c0, v);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const uint32_t k = v[j];
-                    bool keep;
-                    if (exact) {
-                        keep = k >= lo;
-                    } else {
-                        keep = k >= hi;
-                        if (!keep && k == lo && ties < need_ties) {
-                            keep = true;
-                            ++ties;
-                        }
+                    bool keep = exact ? k >= lo : k >= hi;
+                    if (!keep && !exact && k == lo && ties < allow) {
+                        keep = true;
+                        ++ties;
                     }
                     if (keep && row_ok && pos < W) {
                         a.hv[ob + pos] = key_to_score(k);
@@ -439,7 +506,7 @@ cudaError_t launch_score_tc(const sdm_cfg& c, const void* K1, const void* K2, co
     a.hv = hv;
     a.hi = hi;
     a.status = status;
-    const size_t smem = 1024 + kBBytes + 2 * kABytes + 8 * sizeof(uint64_t) + 16;
+    const size_t smem = 1024 + kBBytes + 2 * kABytes + 8 * sizeof(uint64_t) + 16 + 4 * 3584;
     cudaError_t e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess)
