@@ -177,7 +177,9 @@ SDM_API int sdm_scan_noalloc(const sdm_cfg* cfg, const int32_t* idx, const float
                              void* stream);
 
 /* Whole layer over a prefill of B sequences of T tokens: sdm_project, sdm_address and
- * sdm_scan in one call. x [B, T, d], alpha/beta [B, T], banks [B, N, d] (in place),
+ * sdm_scan in one call. Everything, cuBLAS's scratch included, lives in ws, so once a
+ * first call on a device has set up its cuBLAS handle, later calls (and
+ * sdm_decode_step) can be captured in a CUDA graph. x [B, T, d], alpha/beta [B, T], banks [B, N, d] (in place),
  * y [B, T, d] fp32. idx_out [B, T, 2, w] / w_out [B, T, 2, w] optional (NULL = not
  * returned). ws: sdm_workspace_bytes(cfg, B, T) bytes. */
 SDM_API int sdm_prefill(const sdm_cfg* cfg, const sdm_weights* wts, const void* x, const float* alpha,

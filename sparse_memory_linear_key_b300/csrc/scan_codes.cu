@@ -17,13 +17,12 @@
 //                writes) a slot that t writes; t's bank stores wait for those tokens'
 //                bank loads.
 //
-// Block: one sequence, a run of kCodeTB tokens [t0, t1). Bitmaps over all N slots are
-// built from the lists of the window [t0 - win, t1): `once` / `twice` mark slots
-// written by at least one / two of those tokens, `rref` slots read by any of them. A
-// read reference whose `once` bit is clear, or a write reference whose `twice` and
-// `rref` bits are clear (its own token accounts for one write), has nothing to find:
-// the common case. The rest are queued and searched in the sorted lists of the
-// preceding tokens, newest first.
+// Block: one sequence, a run of `tb` tokens [t0, t1). The references of the window
+// [t0 - win, t1) (slot ids are one contiguous run of idx) are indexed by slot: a counting
+// sort places them in kBuckets hash buckets of (slot, token, kind, position) entries.
+// Each reference of the block then scans only its slot's bucket -- a handful of entries,
+// more for popular slots -- for the latest earlier writer and the earlier referencing
+// tokens.
 #include "sdm_common.cuh"
 #include "sdm_internal.h"
 
@@ -31,125 +30,127 @@ namespace sdm {
 
 namespace {
 
-constexpr int kCodeTB = 32;
+constexpr int kBuckets = 4096;
+constexpr int kCodeThreads = 256;
 
-__device__ __forceinline__ int find_sorted(const int32_t* L, int W, int32_t s)
+__device__ __forceinline__ uint32_t bucket_of(int32_t s)
 {
-    int lo = 0, hi = W - 1;
-    while (lo <= hi) {
-        const int mid = (lo + hi) >> 1;
-        const int32_t v = L[mid];
-        if (v == s)
-            return mid;
-        if (v < s)
-            lo = mid + 1;
-        else
-            hi = mid - 1;
-    }
-    return -1;
+    return ((uint32_t)s * 0x9E3779B1u) >> 20;   // top 12 bits
 }
 
-__global__ void __launch_bounds__(256) codes_kernel(const int32_t* __restrict__ idx, int T, int W,
-                                                    int N, int win,
-                                                    uint16_t* __restrict__ codes,
-                                                    unsigned long long* __restrict__ fwdmask,
-                                                    unsigned long long* __restrict__ deadmask,
-                                                    unsigned long long* __restrict__ warmask,
-                                                    int* status)
+__global__ void __launch_bounds__(kCodeThreads) codes_kernel(const int32_t* __restrict__ idx, int T,
+                                                             int W, int N, int win, int tb,
+                                                             uint16_t* __restrict__ codes,
+                                                             unsigned long long* __restrict__ fwdmask,
+                                                             unsigned long long* __restrict__ deadmask,
+                                                             unsigned long long* __restrict__ warmask,
+                                                             int* status)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    const int nwords = (N + 31) / 32;
-    uint32_t* once = reinterpret_cast<uint32_t*>(smem_raw);
-    uint32_t* twice = once + nwords;
-    uint32_t* rref = twice + nwords;
-    int32_t* wl = reinterpret_cast<int32_t*>(rref + nwords);       // [(kCodeTB + win) * W]
-    int32_t* rl = wl + (kCodeTB + win) * W;                         // [(kCodeTB + win) * W]
-    int* queue = rl + (kCodeTB + win) * W;                          // [kCodeTB * 2 * W]
-    __shared__ int qn;
+    uint32_t* off = reinterpret_cast<uint32_t*>(smem_raw);           // [kBuckets + 1]
+    uint32_t* cur = off + kBuckets + 4;                               // [kBuckets] counts, cursors
+    int32_t* slot = reinterpret_cast<int32_t*>(cur + kBuckets);       // [nref window]
+    uint32_t* info = reinterpret_cast<uint32_t*>(slot + (tb + win) * 2 * W);  // tloc<<8|kind<<7|pos
+    __shared__ uint32_t wsum[kCodeThreads / 32];
     const int b = blockIdx.y;
-    const int t0 = blockIdx.x * kCodeTB;
-    const int t1 = min(T, t0 + kCodeTB);
+    const int t0 = blockIdx.x * tb;
+    const int t1 = min(T, t0 + tb);
     const int base = max(0, t0 - win);
-    const int nlist = t1 - base;
-    for (int i = threadIdx.x; i < 3 * nwords; i += blockDim.x)
-        once[i] = 0u;
-    if (threadIdx.x == 0)
-        qn = 0;
+    const int nwin = (t1 - base) * 2 * W;
+    const int32_t* wsrc = idx + ((size_t)b * T + base) * 2 * W;     // [token][write, read][W]
+    for (int i = threadIdx.x; i < kBuckets; i += blockDim.x)
+        cur[i] = 0u;
     __syncthreads();
-    for (int e = threadIdx.x; e < nlist * 2 * W; e += blockDim.x) {
-        const int lt = e / (2 * W), kind = (e / W) & 1, j = e % W;
-        const int32_t s = idx[(((size_t)b * T + base + lt) * 2 + kind) * W + j];
-        (kind ? rl : wl)[lt * W + j] = s;
-        if (s >= 0 && s < N) {
-            const uint32_t m = 1u << (s & 31);
-            if (kind)
-                atomicOr(&rref[s >> 5], m);
-            else if (atomicOr(&once[s >> 5], m) & m)
-                atomicOr(&twice[s >> 5], m);
-        } else if (kind == 0) {
+    for (int e = threadIdx.x; e < nwin; e += blockDim.x) {
+        const int32_t s = __ldg(wsrc + e);
+        if (s >= 0 && s < N)
+            atomicAdd(&cur[bucket_of(s)], 1u);
+        else if (((e / W) & 1) == 0)
             report(status, SDM_ERANGE);
+    }
+    __syncthreads();
+    // exclusive prefix sum of the bucket sizes (16 buckets a thread)
+    {
+        constexpr int PER = kBuckets / kCodeThreads;
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        uint32_t v[PER], tot = 0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            v[i] = cur[threadIdx.x * PER + i];
+            tot += v[i];
+        }
+        uint32_t inc = tot;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+            if (lane >= d)
+                inc += o;
+        }
+        if (lane == 31)
+            wsum[warp] = inc;
+        __syncthreads();
+        uint32_t pre = 0;
+        for (int w = 0; w < warp; ++w)
+            pre += wsum[w];
+        uint32_t run = pre + inc - tot;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            off[threadIdx.x * PER + i] = run;
+            cur[threadIdx.x * PER + i] = run;
+            run += v[i];
+        }
+        if (threadIdx.x == blockDim.x - 1)
+            off[kBuckets] = run;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < nwin; e += blockDim.x) {
+        const int32_t s = __ldg(wsrc + e);
+        if (s >= 0 && s < N) {
+            const uint32_t at = atomicAdd(&cur[bucket_of(s)], 1u);
+            slot[at] = s;
+            info[at] = ((uint32_t)(e / (2 * W)) << 8) | ((uint32_t)((e / W) & 1) << 7) | (uint32_t)(e % W);
         }
     }
     __syncthreads();
     const int nref = (t1 - t0) * 2 * W;
     for (int e = threadIdx.x; e < nref; e += blockDim.x) {
         const int kind = (e / W) & 1;
+        const int t = t0 + e / (2 * W);
         const size_t o = ((size_t)b * T + t0) * 2 * W + e;
-        const int32_t s = idx[o];
-        bool hit = false;
-        if (s >= 0 && s < N) {
-            const uint32_t m = 1u << (s & 31);
-            // a write is searched if another write of the slot or a read of it lies in
-            // the window
-            hit = kind ? (once[s >> 5] & m) != 0
-                       : ((twice[s >> 5] & m) != 0 || (rref[s >> 5] & m) != 0);
-        }
-        if (hit)
-            queue[atomicAdd(&qn, 1)] = e;
-        else
-            codes[o] = kNoFwd;
-    }
-    __syncthreads();
-    const int nq = qn;
-    for (int qi = threadIdx.x; qi < nq; qi += blockDim.x) {
-        const int e = queue[qi];
-        const int lt = e / (2 * W);
-        const int t = t0 + lt;
-        const int kind = (e / W) & 1;
-        const size_t o = ((size_t)b * T + t0) * 2 * W + e;
-        const int32_t s = idx[o];
+        const int32_t s = __ldg(idx + o);
         uint16_t code = kNoFwd;
-        if (kind) {
-            // read: the latest writer, this token's own write included
-            for (int dt = 0; dt <= win && t - dt >= base; ++dt) {
-                const int pos = find_sorted(wl + (t - dt - base) * W, W, s);
-                if (pos >= 0) {
-                    code = (uint16_t)((dt << 8) | pos);
-                    if (dt > 0)
-                        atomicOr(fwdmask + (size_t)b * T + t - dt, 1ull << pos);
-                    break;
-                }
-            }
-        } else {
-            // write: the latest earlier writer, and every earlier referencing token; only
-            // the lists the bitmaps say can hold the slot are searched
-            const uint32_t mb = 1u << (s & 31);
-            const bool other_w = (twice[s >> 5] & mb) != 0, any_r = (rref[s >> 5] & mb) != 0;
+        if (s >= 0 && s < N) {
+            const uint32_t bk = bucket_of(s);
+            int best_dt = 1 << 30, best_pos = 0;
             unsigned long long war0 = 0, war1 = 0;
-            for (int dt = 1; dt <= win && t - dt >= base; ++dt) {
-                const int tp = t - dt - base;
-                const int pw = other_w ? find_sorted(wl + tp * W, W, s) : -1;
-                const bool ref = pw >= 0 || (any_r && find_sorted(rl + tp * W, W, s) >= 0);
-                if (pw >= 0 && code == kNoFwd) {
-                    code = (uint16_t)((dt << 8) | pw);
-                    atomicOr(fwdmask + (size_t)b * T + t - dt, 1ull << pw);
-                    atomicOr(deadmask + (size_t)b * T + t - dt, 1ull << pw);
+            for (uint32_t q = off[bk]; q < off[bk + 1]; ++q) {
+                if (slot[q] != s)
+                    continue;
+                const uint32_t in = info[q];
+                const int dt = t - (base + (int)(in >> 8));
+                if (dt < 0 || dt > win)
+                    continue;
+                const bool is_w = ((in >> 7) & 1) == 0;
+                // writers: the latest one at or before t (a read sees its own token's
+                // write), strictly before t for a write
+                if (is_w && dt < best_dt && (kind ? dt >= 0 : dt >= 1)) {
+                    best_dt = dt;
+                    best_pos = (int)(in & 0x7F);
                 }
-                if (ref) {
+                // a write waits for the bank loads of every earlier referencing token
+                if (!kind && dt >= 1) {
                     if (dt <= 64)
                         war0 |= 1ull << (dt - 1);
                     else
                         war1 |= 1ull << (dt - 65);
+                }
+            }
+            if (best_dt <= win) {
+                code = (uint16_t)((best_dt << 8) | best_pos);
+                if (best_dt > 0) {
+                    atomicOr(fwdmask + (size_t)b * T + t - best_dt, 1ull << best_pos);
+                    if (!kind)
+                        atomicOr(deadmask + (size_t)b * T + t - best_dt, 1ull << best_pos);
                 }
             }
             if (war0)
@@ -177,14 +178,18 @@ cudaError_t launch_scan_codes(const sdm_cfg& c, const int32_t* idx, int B, int T
     unsigned long long* deadmask = masks + (size_t)B * T;
     unsigned long long* warmask = masks + (size_t)B * T * 2;
     const int N = c.n_sub * c.n_sub;
-    const size_t smem = (size_t)3 * ((N + 31) / 32) * 4 + (size_t)2 * (kCodeTB + win) * c.w * 4 +
-                        (size_t)kCodeTB * 2 * c.w * 4;
+    // tokens a block: keep the indexed window (tb + win tokens, 8 bytes a reference) near
+    // 80 KB, so that two blocks share an SM where the window allows
+    int tb = 32;
+    while (tb > 8 && (size_t)(tb + win) * 2 * c.w * 8 > 80 * 1024)
+        tb /= 2;
+    const size_t smem = (size_t)(2 * kBuckets + 4) * 4 + (size_t)(tb + win) * 2 * c.w * 8;
     e = cudaFuncSetAttribute(codes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    dim3 grid((T + kCodeTB - 1) / kCodeTB, B);
-    codes_kernel<<<grid, 256, smem, s>>>(idx, T, c.w, N, win, codes, fwdmask, deadmask, warmask,
-                                         status);
+    dim3 grid((T + tb - 1) / tb, B);
+    codes_kernel<<<grid, kCodeThreads, smem, s>>>(idx, T, c.w, N, win, tb, codes, fwdmask, deadmask,
+                                                  warmask, status);
     return cudaGetLastError();
 }
 

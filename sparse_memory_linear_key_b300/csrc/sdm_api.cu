@@ -52,7 +52,7 @@ static int cuda_status(cudaError_t e) { return e == cudaSuccess ? SDM_OK : SDM_E
 
 // Workspace layout of a prefill / decode call over B sequences of T tokens.
 struct PrefillWs {
-    size_t q_w, q_r, v, idx, wsel, scan, addr, total;
+    size_t q_w, q_r, v, idx, wsel, scan, addr, blas, total;
 };
 
 static PrefillWs prefill_layout(const sdm_cfg& c, int B, int T)
@@ -67,7 +67,8 @@ static PrefillWs prefill_layout(const sdm_cfg& c, int B, int T)
     L.idx = o; o += align256((size_t)ntok * W2 * 4);
     L.wsel = o; o += align256((size_t)ntok * W2 * 4);
     L.scan = o; o += scan_ws_layout(c, B, T).total;
-    L.addr = o; o += address_ws_bytes(c, ntok);
+    L.addr = o; o += align256(address_ws_bytes(c, ntok));
+    L.blas = o; o += kBlasWsBytes;
     L.total = o;
     return L;
 }
@@ -325,7 +326,7 @@ int sdm_prefill(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const f
     float* wsel = w_out ? w_out : (float*)(base + L.wsel);
 
     cudaStream_t s = (cudaStream_t)stream;
-    rc = launch_project(*cfg, *w, x, ntok, q_w, q_r, v, s);
+    rc = launch_project(*cfg, *w, x, ntok, q_w, q_r, v, s, base + L.blas, kBlasWsBytes);
     if (rc != SDM_OK)
         return rc;
     if (launch_address(*cfg, w->K1, w->K2, q_w, q_r, ntok, idx, wsel, base + L.addr, dev_status,

@@ -22,8 +22,11 @@ cudaError_t launch_bank_init(const void* M0, void* banks, size_t bank_bytes, int
                              cudaStream_t s);
 
 // ---- projections (project.cu)
+// blas_ws (may be null: cuBLAS's own workspace) is a region of the caller's workspace
+constexpr size_t kBlasWsBytes = (size_t)32 << 20;
 int launch_project(const sdm_cfg& c, const sdm_weights& w, const void* x, int64_t ntok,
-                   void* q_w, void* q_r, void* v, cudaStream_t s);
+                   void* q_w, void* q_r, void* v, cudaStream_t s, void* blas_ws = nullptr,
+                   size_t blas_ws_bytes = 0);
 
 // ---- addressing (address.cu, score_tc.cu)
 bool score_tc_supported(const sdm_cfg& c);

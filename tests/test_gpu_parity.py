@@ -290,3 +290,39 @@ def test_out_of_range_slot_is_reported_not_faulted():
                                         torch.ones(T, d, dtype=torch.bfloat16),
                                         torch.full((T,), 0.9), torch.full((T,), 0.5), B, T)
     assert status == sdm.SDM_ERANGE
+
+
+def test_decode_steps_captured_in_a_graph_match_eager():
+    """sdm_decode_step allocates nothing (cuBLAS works in the caller's workspace), so a
+    sequence of decode steps can be captured in a CUDA graph after a first call; the
+    replay gives the same bits as the eager calls."""
+    wl = synth.Workload("g", B=8, T=6, d=64, n=32, dk=64, W=16, dtype="bf16", seed=77)
+    p, tok = _inputs(wl)
+    cfg = tl.cfg_of(wl)
+    pd = tl.to_dev(p)
+    x = tok["x"].cuda()
+    al = tok["alpha"].cuda()
+    be = tok["beta"].cuda()
+    ws = sdm.alloc_workspace(sdm.workspace_bytes(cfg, wl.B, 1))
+    st = sdm.new_status()
+
+    def run(banks, y):
+        for t in range(wl.T):
+            sdm.sdm_decode_step(cfg, pd, x[:, t].contiguous(), al[:, t].contiguous(),
+                                be[:, t].contiguous(), banks, y[t], ws, st)
+
+    banks_e = torch.empty(wl.B, wl.N, wl.d, dtype=torch.bfloat16, device="cuda")
+    sdm.sdm_init_bank(cfg, pd["M0"], banks_e)
+    y_e = torch.empty(wl.T, wl.B, wl.d, device="cuda")
+    run(banks_e, y_e)                       # eager (also the first call)
+    banks_g = torch.empty_like(banks_e)
+    sdm.sdm_init_bank(cfg, pd["M0"], banks_g)
+    y_g = torch.zeros_like(y_e)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run(banks_g, y_g)
+    sdm.sdm_init_bank(cfg, pd["M0"], banks_g)   # capture did not run the work
+    g.replay()
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(y_g, y_e) and torch.equal(banks_g, banks_e)
