@@ -105,12 +105,16 @@ __global__ void __launch_bounds__(256) candidate_select_kernel(
     __shared__ float lv[8][2][64];
     __shared__ int li[8][2][64];
     __shared__ uint64_t sel[8][64];
-    if (threadIdx.x == 0) {
-        int c = 0;
-        for (int a = 0; a < W; ++a)
-            for (int b = 0; (a + 1) * (b + 1) <= W; ++b)
-                pairs[c++] = (unsigned short)((a << 8) | b);
-        npairs = c;
+    // pairs (a, b) with (a+1)(b+1) <= W, row a's run starting after the runs of rows < a
+    if (threadIdx.x < W) {
+        const int a = threadIdx.x;
+        int start = 0;
+        for (int a2 = 0; a2 < a; ++a2)
+            start += W / (a2 + 1);
+        for (int b = 0; b < W / (a + 1); ++b)
+            pairs[start + b] = (unsigned short)((a << 8) | b);
+        if (a == W - 1)
+            npairs = start + W / (a + 1);
     }
     __syncthreads();
     const int C = npairs;

@@ -13,16 +13,19 @@
 //  * sixteen epilogue warps (four per TMEM lane quadrant, one column group each) keep,
 //    per row, the W largest scores by (score desc, row asc): a first pass replaces
 //    each score in TMEM by its
-//    order-preserving integer image (tcgen05.st), a bisection over those keys finds
-//    the W-th largest (stopping early once exactly W keys lie at or above the probe;
-//    one compare per element a pass), and a last pass writes the kept (score, row)
-//    pairs, ties at the threshold by ascending row.
+//    order-preserving integer image (tcgen05.st) and sums the row's scores and squares;
+//    a bracket around mean + z sd (the scores of a row are near normal; z is the normal
+//    quantile of 1 - W/n) is checked in one counting pass, and a bisection over the keys
+//    inside what holds of the bracket (the whole range otherwise) finds the W-th
+//    largest, stopping early once exactly W keys lie at or above the probe; a last pass
+//    writes the kept (score, row) pairs, ties at the threshold by ascending row.
 // The per-half lists are written unsorted; the candidate kernel sorts them.
 // Every wait is bounded (status SDM_ETIMEOUT); on time-out a role stops issuing, the
 // CTA waits (bounded) for its copies and MMAs in flight and frees its TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <mutex>
 
 #include "sdm_common.cuh"
@@ -43,6 +46,7 @@ constexpr uint32_t kABytes = kTileM * 128 * 2;        // two K atoms of 128 rows
 
 struct ScoreArgs {
     int ntok, n, khalf, W, tiles_per_kind, ctas_per_half;
+    float z;               // standard normal quantile of 1 - W/n (bracket of the W-th score)
     float* hv;
     int32_t* hi;
     int* status;
@@ -187,6 +191,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
     int* xcnt = reinterpret_cast<int*>(xmax + 512);  // [2 parities][512]
     int* xa = xcnt + 1024;
     int* xt = xa + 512;
+    float* xs = reinterpret_cast<float*>(xt + 512);   // [512] row sums, then [512] squares
+    float* xs2 = xs + 512;
+    int* xb1 = reinterpret_cast<int*>(xs2 + 512);      // bracket counts
+    int* xb2 = xb1 + 512;
     __shared__ int dead;                 // a role gave up: the others stop at their next wait
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -326,17 +334,22 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
             const int kind = tl / a.tiles_per_kind;
             const int tok = (tl % a.tiles_per_kind) * kTileM + q * 32 + lane;
             uint32_t v[32];
-            // keys in place of the scores (0 in padding columns), and their range
+            // keys in place of the scores (0 in padding columns), their range, and the
+            // row's mean and spread
             uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+            float sum = 0.f, sum2 = 0.f;
             for (int c0 = cb; c0 < ce; c0 += 32) {
                 tmem_ld32(trow + c0, v);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const bool valid = c0 + j < a.n;
+                    const float f = __uint_as_float(v[j]);
                     const uint32_t k = valid ? order_key(v[j]) : 0u;
                     if (valid) {
                         kmin = min(kmin, k);
                         kmax = max(kmax, k);
+                        sum += f;
+                        sum2 = fmaf(f, f, sum2);
                     }
                     v[j] = k;
                 }
@@ -344,17 +357,67 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
             }
             xmin[xi] = kmin;
             xmax[xi] = kmax;
+            xs[xi] = sum;
+            xs2[xi] = sum2;
             bar_sync(bid, 128);
+            sum = 0.f;
+            sum2 = 0.f;
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
                 kmin = min(kmin, xmin[xq + h * 32]);
                 kmax = max(kmax, xmax[xq + h * 32]);
+                sum += xs[xq + h * 32];
+                sum2 += xs2[xq + h * 32];
             }
-            // bisection: at least W keys lie at or above lo, fewer than W at or above hi
+            // bracket the W-th largest score around mean + z sd (scores are near normal);
+            // one counting pass checks it, and the bisection starts from whatever of the
+            // bracket holds: at least W keys lie at or above lo, fewer than W at or above hi
+            const float mean = sum / a.n;
+            const float sd = sqrtf(fmaxf(sum2 / a.n - mean * mean, 0.f));
+            const uint32_t bl = order_key(__float_as_uint(mean + (a.z - 0.5f) * sd));
+            const uint32_t bh = order_key(__float_as_uint(mean + (a.z + 0.5f) * sd));
             uint32_t lo = kmin, hi = kmax + 1;
             int cnt_hi = 0;
             bool exact = false;
-            for (int it = 0; __any_sync(0xFFFFFFFFu, !exact && hi - lo > 1); ++it) {
+            {
+                int cl = 0, ch = 0;
+                for (int c0 = cb; c0 < ce; c0 += 32) {
+                    tmem_ld32(trow + c0, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        cl += v[j] >= bl ? 1 : 0;
+                        ch += v[j] >= bh ? 1 : 0;
+                    }
+                }
+                xb1[xi] = cl;
+                xb2[xi] = ch;
+                bar_sync(bid, 128);
+                cl = xb1[xq] + xb1[xq + 32] + xb1[xq + 64] + xb1[xq + 96];
+                ch = xb2[xq] + xb2[xq + 32] + xb2[xq + 64] + xb2[xq + 96];
+                if (bl > lo && bl < hi) {
+                    if (cl == W) {
+                        lo = bl;
+                        exact = true;
+                    } else if (cl > W) {
+                        lo = bl;
+                    } else {
+                        hi = bl;
+                        cnt_hi = cl;
+                    }
+                }
+                if (!exact && bh > lo && bh < hi) {
+                    if (ch == W) {
+                        lo = bh;
+                        exact = true;
+                    } else if (ch > W) {
+                        lo = bh;
+                    } else {
+                        hi = bh;
+                        cnt_hi = ch;
+                    }
+                }
+            }
+            for (int it = 1; __any_sync(0xFFFFFFFFu, !exact && hi - lo > 1); ++it) {
                 const bool active = !exact && hi - lo > 1;
                 const uint32_t mid = lo + ((hi - lo) >> 1);
                 int cnt = 0;
@@ -455,6 +518,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 // 2D bf16 row-major tensor [rows, cols], box {64 columns, box_rows}, 128-byte swizzle.
+// z with P(Z > z) = p for a standard normal Z: bisection on the upper tail
+// 0.5 erfc(z / sqrt 2), which falls as z grows. Only a starting bracket for an exact
+// search, so a float is plenty.
+float normal_upper_quantile(double p)
+{
+    if (p <= 0.0 || p >= 1.0)
+        return 0.0f;
+    double lo = -10.0, hi = 10.0;
+    for (int i = 0; i < 60; ++i) {
+        const double mid = 0.5 * (lo + hi);
+        if (0.5 * std::erfc(mid / std::sqrt(2.0)) > p)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return (float)(0.5 * (lo + hi));
+}
+
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_rows)
 {
     auto enc = encode_fn();
@@ -496,6 +577,7 @@ cudaError_t launch_score_tc(const sdm_cfg& c, const void* K1, const void* K2, co
     a.n = c.n_sub;
     a.khalf = h;
     a.W = c.w;
+    a.z = normal_upper_quantile((double)c.w / c.n_sub);
     a.tiles_per_kind = (int)((ntok + kTileM - 1) / kTileM);
     int per_half = num_sms_current_device() / 2;
     if (per_half > 2 * a.tiles_per_kind)
@@ -506,7 +588,7 @@ cudaError_t launch_score_tc(const sdm_cfg& c, const void* K1, const void* K2, co
     a.hv = hv;
     a.hi = hi;
     a.status = status;
-    const size_t smem = 1024 + kBBytes + 2 * kABytes + 8 * sizeof(uint64_t) + 16 + 4 * 3584;
+    const size_t smem = 1024 + kBBytes + 2 * kABytes + 8 * sizeof(uint64_t) + 16 + 4 * 5632;
     cudaError_t e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess)
