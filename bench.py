@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--tokens", type=int, default=None,
                     help="tokens per sequence instead of the workload's (for profiling a "
                          "small case of the same kernels)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="sequences instead of the workload's (for profiling a small case)")
     return ap.parse_args()
 
 
@@ -161,6 +163,8 @@ def gpu_arm(args, world, rank):
     wl = synth.WORKLOADS[WORKLOAD]
     if args.tokens:
         wl = wl.with_(T=args.tokens)
+    if args.batch:
+        wl = wl.with_(B=args.batch)
     dev = "cuda"
     cfg = sdm.make_cfg(wl.d, wl.n, wl.dk, wl.W, wl.dtype)
     p_cpu = synth.make_params(wl)
