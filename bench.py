@@ -86,6 +86,25 @@ def max_over_ranks(world, x: float) -> float:
     return float(t.item())
 
 
+# DRAM bytes (read + write) of one scan_kernel launch on this workload, from one ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum, 1 pass, full size). They hold
+# for the kernel sources they were taken on; any change to those makes them stale.
+SCAN_TRAFFIC = {"B": 4, "T": 4096, "bytes": 8439312e3 + 4480697e3,
+                "sources_sha256": {"scan.cu": "f49881c6490422ca", "sdm_common.cuh": "a8376df91a89808f"}}
+
+
+def scan_traffic(B, T):
+    import hashlib
+    if (B, T) != (SCAN_TRAFFIC["B"], SCAN_TRAFFIC["T"]):
+        return None
+    csrc = os.path.join(ROOT, "sparse_memory_linear_key_b300", "csrc")
+    for name, want in SCAN_TRAFFIC["sources_sha256"].items():
+        with open(os.path.join(csrc, name), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest()[:16] != want:
+                return None
+    return SCAN_TRAFFIC["bytes"]
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -247,7 +266,7 @@ def gpu_arm(args, world, rank):
     peak, peak_kind = measured_peaks()
     achieved = scan_bytes / scan_s / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
+                "frac": round(achieved / peak, 4), "traffic": scan_traffic(B, T),
                 "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.4 TB/s",
                 "kernel": "scan_kernel<bf16,64>", "bytes_per_token": per_tok,
