@@ -65,6 +65,11 @@ constexpr int kCWarps = 16;        // consumer warps
 constexpr int kWarpP = kCWarps, kWarpD = kCWarps + 1, kWarpF1 = kCWarps + 2;
 // 20 warps: five per SM sub-partition, which leaves each thread up to 96 registers
 constexpr int kScanThreads = 32 * (kCWarps + 4);
+constexpr int kLaunchRegs = 96;    // registers a thread at launch (__launch_bounds__)
+constexpr int kConsumerRegs = 104, kRoleRegs = 64;
+static_assert(kCWarps * 32 * kConsumerRegs + 4 * 32 * kRoleRegs <= kScanThreads * kLaunchRegs,
+              "register split exceeds the block's launch allocation");
+static_assert(kCWarps % 4 == 0, "consumer warps must form whole warpgroups");
 constexpr int kMaxW = 64;
 constexpr int kSG = 8;             // slot groups (lanes sharing a row group)
 
@@ -101,6 +106,7 @@ struct __align__(16) Meta {
     unsigned long long war[2];      // bit dt-1: token t-dt must have loaded before our stores
     unsigned long long wload;       // bit j: write chunk j is gathered from the bank
     unsigned long long rload;       // bit j: read chunk j is gathered from the bank
+    unsigned long long rdmask;      // bit j: read chunk j is copied by D (writer in flight)
     long long tok;                  // b * T + t
     int b, t, rb, rows;
     float alpha, beta;
@@ -120,28 +126,29 @@ enum {
     kFwdw = 12, kStored = 14, kCbar = 16, kLmark = 17, kDepR = 18, kNumBars = 20
 };
 
+// 16 bytes of one slot vector (8 rows in bf16, 4 in fp32) as fp32 pairs, the operand
+// of the packed two-lane fp32 FMA.
 template <typename S>
 struct Pack16;
 
 template <>
 struct Pack16<bf16> {
-    static constexpr int R = 8;
-    static __device__ __forceinline__ void unpack(const uint4& q, float (&f)[8])
+    static constexpr int R = 8;   // rows
+    static constexpr int H = 4;   // fp32 pairs
+    static __device__ __forceinline__ void unpack(const uint4& q, float2 (&f)[H])
     {
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            f[2 * i] = __uint_as_float(w[i] << 16);
-            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-        }
+        for (int i = 0; i < 4; ++i)
+            f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
     }
     // round-to-nearest-even, once per value
-    static __device__ __forceinline__ uint4 pack(const float (&f)[8])
+    static __device__ __forceinline__ uint4 pack(const float2 (&f)[H])
     {
         uint32_t w[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+            __nv_bfloat162 h = __float22bfloat162_rn(f[i]);
             w[i] = *reinterpret_cast<uint32_t*>(&h);
         }
         return make_uint4(w[0], w[1], w[2], w[3]);
@@ -151,19 +158,28 @@ struct Pack16<bf16> {
 template <>
 struct Pack16<float> {
     static constexpr int R = 4;
-    static __device__ __forceinline__ void unpack(const uint4& q, float (&f)[4])
+    static constexpr int H = 2;
+    static __device__ __forceinline__ void unpack(const uint4& q, float2 (&f)[H])
     {
-        f[0] = __uint_as_float(q.x);
-        f[1] = __uint_as_float(q.y);
-        f[2] = __uint_as_float(q.z);
-        f[3] = __uint_as_float(q.w);
+        f[0] = make_float2(__uint_as_float(q.x), __uint_as_float(q.y));
+        f[1] = make_float2(__uint_as_float(q.z), __uint_as_float(q.w));
     }
-    static __device__ __forceinline__ uint4 pack(const float (&f)[4])
+    static __device__ __forceinline__ uint4 pack(const float2 (&f)[H])
     {
-        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
-                          __float_as_uint(f[3]));
+        return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y), __float_as_uint(f[1].x),
+                          __float_as_uint(f[1].y));
     }
 };
+
+// sum of a pair over the eight slot groups of a row group (lanes 4 apart)
+__device__ __forceinline__ float2 slot_group_sum(float2 v)
+{
+#pragma unroll
+    for (int o = 4; o <= 16; o <<= 1)
+        v = __fadd2_rn(v, make_float2(__shfl_xor_sync(0xFFFFFFFFu, v.x, o),
+                                      __shfl_xor_sync(0xFFFFFFFFu, v.y, o)));
+    return v;
+}
 
 __device__ __forceinline__ bool uniform_wait(uint32_t bar, uint32_t parity, const ScanArgs& a)
 {
@@ -299,7 +315,7 @@ __device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
             return;
         fence_acq_rel_gpu();
 
-        unsigned long long wload = 0, rload = 0, fmask = 0;
+        unsigned long long wload = 0, rload = 0, fmask = 0, rdmask = 0;
 #pragma unroll
         for (int jj = 0; jj < JW; ++jj) {
             const int j = lane + 32 * jj;
@@ -317,6 +333,7 @@ __device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
             rload |= (unsigned long long)__ballot_sync(0xFFFFFFFFu, rval && !rown && !rdep)
                      << (32 * jj);
             fmask |= (unsigned long long)__ballot_sync(0xFFFFFFFFu, rown) << (32 * jj);
+            rdmask |= (unsigned long long)__ballot_sync(0xFFFFFFFFu, rdep) << (32 * jj);
             if (has) {
                 m.wid[j] = wval ? nx.wid[jj] : -1;
                 m.rid[j] = rval ? nx.rid[jj] : -1;
@@ -333,6 +350,7 @@ __device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
             m.war[1] = nx.war1;
             m.wload = wload;
             m.rload = rload;
+            m.rdmask = rdmask;
             m.tok = (long long)b * a.T + t;
             m.b = b;
             m.t = t;
@@ -576,6 +594,7 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
     constexpr int SPL = W / kSG;       // slots of each set per thread: i*8 + sg
     using P = Pack16<S>;
     constexpr int RPL = P::R;          // rows per thread (16 bytes)
+    constexpr int HPL = P::H;          // fp32 pairs per thread
     const int ct = threadIdx.x, w = ct >> 5, lane = ct & 31;
     const int sg = lane >> 2;          // slot group
     const int rg = w * 4 + (lane & 3); // row group: rows rg*RPL .. rg*RPL + RPL - 1
@@ -647,10 +666,37 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
         const Meta& m = meta[p];
         if (!m.valid)
             return;
-        if (!uniform_wait(smem_u32(bars + kDepB + p), (k >> 1) & 1, a))
-            return;
         unsigned char* rb_buf = rbuf + (size_t)p * W * kStride;
         const bool act = rg * 16 < m.rows * (int)sizeof(S);
+        // y = sum_j r_j M[R_j] (post-write), accumulated per thread over its read slots
+        // i*8 + sg in a fixed order -- chunks gathered from the bank, then the chunks D
+        // copied from the ring, then this token's own writes -- and then over the slot
+        // groups. The bank chunks need nothing of the write, so they are taken while a
+        // write-side dependency is still in flight, else after the write.
+        float2 yv[HPL];
+#pragma unroll
+        for (int h = 0; h < HPL; ++h)
+            yv[h] = make_float2(0.f, 0.f);
+        auto y_add = [&](unsigned long long sel) {
+#pragma unroll
+            for (int i = 0; i < SPL; ++i) {
+                if (!act || !((sel >> (i * kSG + sg)) & 1))
+                    continue;
+                const float rw = m.wsel[W + i * kSG + sg];
+                float2 f[HPL];
+                P::unpack(*reinterpret_cast<const uint4*>(rb_buf + (size_t)(i * kSG + sg) * kStride +
+                                                          rg * 16),
+                          f);
+#pragma unroll
+                for (int h = 0; h < HPL; ++h)
+                    yv[h] = __ffma2_rn(make_float2(rw, rw), f[h], yv[h]);
+            }
+        };
+        const bool bank_first = !uniform_test(smem_u32(bars + kDepB + p), (k >> 1) & 1);
+        if (bank_first)
+            y_add(m.rload);
+        if (!uniform_wait(smem_u32(bars + kDepB + p), (k >> 1) & 1, a))
+            return;
         uint4 Mv[SPL];
 #pragma unroll
         for (int i = 0; i < SPL; ++i)
@@ -668,110 +714,92 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
         if (issued)
             issue(k + 1);
 
-        // u = M_S k (pre-write), reduced over the slot groups
-        float u[RPL];
+        // u = M_S k (pre-write), reduced over the slot groups; fp32 pairs throughout
+        float2 u[HPL];
 #pragma unroll
-        for (int r = 0; r < RPL; ++r)
-            u[r] = 0.f;
+        for (int h = 0; h < HPL; ++h)
+            u[h] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < SPL; ++i) {
             const float kw = m.wsel[i * kSG + sg];
-            float f[RPL];
+            float2 f[HPL];
             P::unpack(Mv[i], f);
 #pragma unroll
-            for (int r = 0; r < RPL; ++r)
-                u[r] = fmaf(kw, f[r], u[r]);
+            for (int h = 0; h < HPL; ++h)
+                u[h] = __ffma2_rn(make_float2(kw, kw), f[h], u[h]);
         }
-#pragma unroll
-        for (int r = 0; r < RPL; ++r) {
-            u[r] += __shfl_xor_sync(0xFFFFFFFFu, u[r], 4);
-            u[r] += __shfl_xor_sync(0xFFFFFFFFu, u[r], 8);
-            u[r] += __shfl_xor_sync(0xFFFFFFFFu, u[r], 16);
-        }
-        float vv[RPL];
+        float2 vv[HPL];
         P::unpack(act ? *reinterpret_cast<const uint4*>(m.v + rg * 16) : make_uint4(0, 0, 0, 0), vv);
         const float al = m.alpha, be = m.beta;
-        float c[RPL];
+        const float2 al2 = make_float2(al, al), be2 = make_float2(be, be);
+        float2 c[HPL];   // beta (v - alpha u)
 #pragma unroll
-        for (int r = 0; r < RPL; ++r)
-            c[r] = be * (vv[r] - al * u[r]);
+        for (int h = 0; h < HPL; ++h)
+            c[h] = __fmul2_rn(be2, __ffma2_rn(make_float2(-al, -al), slot_group_sum(u[h]), vv[h]));
         // M[S_j] <- alpha M[S_j] + k_j beta (v - alpha u), rounded once
 #pragma unroll
         for (int i = 0; i < SPL; ++i) {
             const float kw = m.wsel[i * kSG + sg];
-            float f[RPL];
+            float2 f[HPL];
             P::unpack(Mv[i], f);
 #pragma unroll
-            for (int r = 0; r < RPL; ++r)
-                f[r] = fmaf(kw, c[r], al * f[r]);
+            for (int h = 0; h < HPL; ++h)
+                f[h] = __ffma2_rn(make_float2(kw, kw), c[h], __fmul2_rn(al2, f[h]));
             Mv[i] = P::pack(f);
         }
         // slots that later tokens read while this one may be in flight: to the ring
-        const unsigned long long fw = m.fwdmask;
-        if (fw != 0) {
-            unsigned long long q = fw;
-            while (q != 0) {
-                const int j = __ffsll((long long)q) - 1;
-                q &= q - 1;
+        // (this thread holds slots i*8 + sg: its bits of the mask are sg, sg+8, ...)
+        const unsigned long long fw = (m.fwdmask >> sg) & 0x0101010101010101ull;
+        if (fw != 0 && act) {
+            unsigned char* re = ring_entry(a, m.b, m.rb, m.t, 0) + rg * 16;
 #pragma unroll
-                for (int i = 0; i < SPL; ++i)
-                    if (act && j == i * kSG + sg)
-                        __stcg(reinterpret_cast<uint4*>(ring_entry(a, m.b, m.rb, m.t, j) + rg * 16),
-                               Mv[i]);
-            }
+            for (int i = 0; i < SPL; ++i)
+                if ((fw >> (8 * i)) & 1)
+                    __stcg(reinterpret_cast<uint4*>(re + (size_t)(i * kSG + sg) * a.chunk_bytes), Mv[i]);
         }
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_u32(bars + kFwdw + p));
+        if (!bank_first)
+            y_add(m.rload);
         // the read chunks D copies (writer still in flight when this item was described)
         if (!uniform_wait(smem_u32(bars + kDepR + p), (k >> 1) & 1, a))
             return;
-        // read slots this token writes itself: their new values, from registers
+        y_add(m.rdmask);
+        // read slots this token writes itself: the new values are in the registers of
+        // the thread holding write position pos; the slot-group sum below gathers them
         const unsigned long long fm = m.fmask;
-        if (fm != 0) {
+        if (fm != 0 && act) {
             unsigned long long q = fm;
             while (q != 0) {
                 const int j = __ffsll((long long)q) - 1;
                 q &= q - 1;
                 const int pos = m.fpos[j];
+                if ((pos & (kSG - 1)) != sg)
+                    continue;
+                const float rw = m.wsel[W + j];
+                const int ip = pos / kSG;
 #pragma unroll
-                for (int i = 0; i < SPL; ++i)
-                    if (act && pos == i * kSG + sg)
-                        *reinterpret_cast<uint4*>(rb_buf + (size_t)j * kStride + rg * 16) = Mv[i];
+                for (int i = 0; i < SPL; ++i) {
+                    if (i != ip)
+                        continue;
+                    float2 f[HPL];
+                    P::unpack(Mv[i], f);
+#pragma unroll
+                    for (int h = 0; h < HPL; ++h)
+                        yv[h] = __ffma2_rn(make_float2(rw, rw), f[h], yv[h]);
+                }
             }
-            if (!consumer_barrier())
-                return;
-        }
-
-        // y = sum_j r_j M[R_j] (post-write)
-        float yv[RPL];
-#pragma unroll
-        for (int r = 0; r < RPL; ++r)
-            yv[r] = 0.f;
-#pragma unroll
-        for (int i = 0; i < SPL; ++i) {
-            const float rw = m.wsel[W + i * kSG + sg];
-            float f[RPL];
-            P::unpack(act ? *reinterpret_cast<const uint4*>(rb_buf + (size_t)(i * kSG + sg) * kStride +
-                                                            rg * 16)
-                          : make_uint4(0, 0, 0, 0),
-                      f);
-#pragma unroll
-            for (int r = 0; r < RPL; ++r)
-                yv[r] = fmaf(rw, f[r], yv[r]);
         }
 #pragma unroll
-        for (int r = 0; r < RPL; ++r) {
-            yv[r] += __shfl_xor_sync(0xFFFFFFFFu, yv[r], 4);
-            yv[r] += __shfl_xor_sync(0xFFFFFFFFu, yv[r], 8);
-            yv[r] += __shfl_xor_sync(0xFFFFFFFFu, yv[r], 16);
-        }
+        for (int h = 0; h < HPL; ++h)
+            yv[h] = slot_group_sum(yv[h]);
         if (sg == 0 && act) {
             float* yp = a.y + (size_t)m.tok * a.d + (size_t)m.rb * a.rb_rows + rg * RPL;
 #pragma unroll
-            for (int r = 0; r < RPL; r += 4)
-                __stcs(reinterpret_cast<float4*>(yp + r),
-                       make_float4(yv[r], yv[r + 1], yv[r + 2], yv[r + 3]));
+            for (int h = 0; h < HPL; h += 2)
+                __stcs(reinterpret_cast<float4*>(yp + 2 * h),
+                       make_float4(yv[h].x, yv[h].y, yv[h + 1].x, yv[h + 1].y));
         }
         if (!issued && uniform_test(lmark, k & 1) &&
             uniform_test(posted_next, ((k + 1) >> 1) & 1)) {
@@ -830,9 +858,16 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a)
     }
     __syncthreads();
     const int warp = threadIdx.x >> 5;
-    if (warp < kCWarps)
+    // Register split: the block is launched with 96 registers a thread (640 x 96 =
+    // 61,440). The four consumer warpgroups take 104 (4 x 128 x 104 = 53,248), the role
+    // warpgroup (warps 16..19) gives back down to 64 (128 x 64 = 8,192): 61,440 in all.
+    if (warp < kCWarps) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kConsumerRegs) : "memory");
         role_consumer<S, W>(a, wbuf, rbuf, meta, bars);
-    else if (warp == kWarpP)
+        return;
+    }
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRoleRegs) : "memory");
+    if (warp == kWarpP)
         role_producer<W>(a, meta, bars);
     else if (warp == kWarpD)
         role_deps<S, W>(a, wbuf, rbuf, meta, bars);
