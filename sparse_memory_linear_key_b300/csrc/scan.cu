@@ -589,7 +589,7 @@ __device__ void role_marks(const ScanArgs& a, const Meta* meta, uint64_t* bars)
 
 template <typename S, int W>
 __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned char* rbuf,
-                              const Meta* meta, uint64_t* bars)
+                              const Meta* meta, uint64_t* bars, float* ybuf)
 {
     constexpr int SPL = W / kSG;       // slots of each set per thread: i*8 + sg
     using P = Pack16<S>;
@@ -599,16 +599,15 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
     const int sg = lane >> 2;          // slot group
     const int rg = w * 4 + (lane & 3); // row group: rows rg*RPL .. rg*RPL + RPL - 1
     const uint32_t cbar = smem_u32(bars + kCbar);
-    // Barrier of the consumer warps (one arrival per warp). Exits are taken by whole
-    // warps, and a warp left waiting here gives up after the bounded wait.
-    int cuses = 0;
-    auto consumer_barrier = [&]() -> bool {
+    // Split barrier of the consumer warps (one arrival per warp, waited for later). Exits
+    // are taken by whole warps, and a warp left waiting gives up after the bounded wait.
+    auto consumer_arrive = [&]() {
         __syncwarp();
         if (lane == 0)
             mbar_arrive(cbar);
-        const bool okb = mbar_wait(cbar, cuses & 1, a.abort_flag, a.status);
-        ++cuses;
-        return __all_sync(0xFFFFFFFFu, okb);
+    };
+    auto consumer_wait = [&](int k) -> bool {
+        return __all_sync(0xFFFFFFFFu, mbar_wait(cbar, k & 1, a.abort_flag, a.status));
     };
     // Bank gathers of item kn, split over the consumer warps (8 bulk copies a warp at
     // W = 64). The full barriers count one arrival per consumer warp: each warp declares
@@ -668,16 +667,19 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
             return;
         unsigned char* rb_buf = rbuf + (size_t)p * W * kStride;
         const bool act = rg * 16 < m.rows * (int)sizeof(S);
-        // y = sum_j r_j M[R_j] (post-write), accumulated per thread over its read slots
-        // i*8 + sg in a fixed order -- chunks gathered from the bank, then the chunks D
-        // copied from the ring, then this token's own writes -- and then over the slot
-        // groups. The bank chunks need nothing of the write, so they are taken while a
-        // write-side dependency is still in flight, else after the write.
-        float2 yv[HPL];
+        // y = sum_j r_j M[R_j] (post-write). The chunks gathered from the bank need nothing
+        // of the write: each thread reduces its read slots i*8 + sg, then the slot groups
+        // are summed. Chunks D copies from the ring and this token's own writes are few;
+        // the lane of slot group 0 adds them afterwards to the partial, which waits in
+        // shared memory.
+        float* ypart = ybuf + (w * 4 + (lane & 3)) * RPL;
+        const bool y_rest = (m.rdmask | m.fmask) != 0;   // same for every thread
+        auto y_bank = [&]() {
+            float2 yv[HPL];
 #pragma unroll
-        for (int h = 0; h < HPL; ++h)
-            yv[h] = make_float2(0.f, 0.f);
-        auto y_add = [&](unsigned long long sel) {
+            for (int h = 0; h < HPL; ++h)
+                yv[h] = make_float2(0.f, 0.f);
+            const unsigned long long sel = m.rload;
 #pragma unroll
             for (int i = 0; i < SPL; ++i) {
                 if (!act || !((sel >> (i * kSG + sg)) & 1))
@@ -691,10 +693,29 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
                 for (int h = 0; h < HPL; ++h)
                     yv[h] = __ffma2_rn(make_float2(rw, rw), f[h], yv[h]);
             }
+#pragma unroll
+            for (int h = 0; h < HPL; ++h)
+                yv[h] = slot_group_sum(yv[h]);
+            if (sg == 0 && act) {
+                if (y_rest) {
+#pragma unroll
+                    for (int h = 0; h < HPL; h += 2)
+                        *reinterpret_cast<float4*>(ypart + 2 * h) =
+                            make_float4(yv[h].x, yv[h].y, yv[h + 1].x, yv[h + 1].y);
+                } else {
+                    float* yp = a.y + (size_t)m.tok * a.d + (size_t)m.rb * a.rb_rows + rg * RPL;
+#pragma unroll
+                    for (int h = 0; h < HPL; h += 2)
+                        __stcs(reinterpret_cast<float4*>(yp + 2 * h),
+                               make_float4(yv[h].x, yv[h].y, yv[h + 1].x, yv[h + 1].y));
+                }
+            }
         };
+        // while a write-side dependency is still in flight, the bank chunks of the read
+        // go first; otherwise the write goes first (later tokens wait for its ring entries)
         const bool bank_first = !uniform_test(smem_u32(bars + kDepB + p), (k >> 1) & 1);
         if (bank_first)
-            y_add(m.rload);
+            y_bank();
         if (!uniform_wait(smem_u32(bars + kDepB + p), (k >> 1) & 1, a))
             return;
         uint4 Mv[SPL];
@@ -703,16 +724,7 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
             Mv[i] = act ? *reinterpret_cast<const uint4*>(wbuf + (size_t)(i * kSG + sg) * kStride +
                                                           rg * 16)
                         : make_uint4(0, 0, 0, 0);
-        // every consumer has taken the write chunks: the buffer is free for item k+1
-        if (!consumer_barrier())
-            return;
-        if (ct == 0)
-            mbar_arrive(smem_u32(bars + kWfree));
-        const uint32_t posted_next = smem_u32(bars + kPosted + ((k + 1) & 1));
-        const uint32_t lmark = smem_u32(bars + kLmark);
-        bool issued = uniform_test(lmark, k & 1) && uniform_test(posted_next, ((k + 1) >> 1) & 1);
-        if (issued)
-            issue(k + 1);
+        consumer_arrive();   // this warp has taken its write chunks
 
         // u = M_S k (pre-write), reduced over the slot groups; fp32 pairs throughout
         float2 u[HPL];
@@ -728,6 +740,16 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
             for (int h = 0; h < HPL; ++h)
                 u[h] = __ffma2_rn(make_float2(kw, kw), f[h], u[h]);
         }
+        // every consumer has taken the write chunks: the buffer is free for item k+1
+        if (!consumer_wait(k))
+            return;
+        if (ct == 0)
+            mbar_arrive(smem_u32(bars + kWfree));
+        const uint32_t posted_next = smem_u32(bars + kPosted + ((k + 1) & 1));
+        const uint32_t lmark = smem_u32(bars + kLmark);
+        bool issued = uniform_test(lmark, k & 1) && uniform_test(posted_next, ((k + 1) >> 1) & 1);
+        if (issued)
+            issue(k + 1);
         float2 vv[HPL];
         P::unpack(act ? *reinterpret_cast<const uint4*>(m.v + rg * 16) : make_uint4(0, 0, 0, 0), vv);
         const float al = m.alpha, be = m.beta;
@@ -761,45 +783,65 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
         if (lane == 0)
             mbar_arrive(smem_u32(bars + kFwdw + p));
         if (!bank_first)
-            y_add(m.rload);
-        // the read chunks D copies (writer still in flight when this item was described)
-        if (!uniform_wait(smem_u32(bars + kDepR + p), (k >> 1) & 1, a))
-            return;
-        y_add(m.rdmask);
-        // read slots this token writes itself: the new values are in the registers of
-        // the thread holding write position pos; the slot-group sum below gathers them
-        const unsigned long long fm = m.fmask;
-        if (fm != 0 && act) {
-            unsigned long long q = fm;
-            while (q != 0) {
-                const int j = __ffsll((long long)q) - 1;
-                q &= q - 1;
-                const int pos = m.fpos[j];
-                if ((pos & (kSG - 1)) != sg)
-                    continue;
-                const float rw = m.wsel[W + j];
-                const int ip = pos / kSG;
+            y_bank();
+        if (y_rest) {
+            // the read chunks D copies (writer still in flight when this item was described)
+            if (!uniform_wait(smem_u32(bars + kDepR + p), (k >> 1) & 1, a))
+                return;
+            // own writes: the new value of write position pos is in the registers of slot
+            // group pos % 8; that lane adds it, and a slot-group sum collects the terms
+            float2 ye[HPL];
 #pragma unroll
-                for (int i = 0; i < SPL; ++i) {
-                    if (i != ip)
+            for (int h = 0; h < HPL; ++h)
+                ye[h] = make_float2(0.f, 0.f);
+            const unsigned long long fm = m.fmask;
+            if (fm != 0) {
+                unsigned long long q = fm;
+                while (q != 0) {
+                    const int j = __ffsll((long long)q) - 1;
+                    q &= q - 1;
+                    const int pos = m.fpos[j];
+                    if (!act || pos % kSG != sg)
                         continue;
+                    const float rw = m.wsel[W + j];
+                    // every register slot, weighted 0 but the one at pos (a selected
+                    // register index would move Mv to local memory)
+#pragma unroll
+                    for (int i = 0; i < SPL; ++i) {
+                        const float sc = i == pos / kSG ? rw : 0.f;
+                        float2 f[HPL];
+                        P::unpack(Mv[i], f);
+#pragma unroll
+                        for (int h = 0; h < HPL; ++h)
+                            ye[h] = __ffma2_rn(make_float2(sc, sc), f[h], ye[h]);
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < HPL; ++h)
+                    ye[h] = slot_group_sum(ye[h]);
+            }
+            if (sg == 0 && act) {
+                // chunks copied by D, all of them, by this lane alone
+                unsigned long long rd = m.rdmask;
+                while (rd != 0) {
+                    const int j = __ffsll((long long)rd) - 1;
+                    rd &= rd - 1;
+                    const float rw = m.wsel[W + j];
                     float2 f[HPL];
-                    P::unpack(Mv[i], f);
+                    P::unpack(*reinterpret_cast<const uint4*>(rb_buf + (size_t)j * kStride + rg * 16), f);
 #pragma unroll
                     for (int h = 0; h < HPL; ++h)
-                        yv[h] = __ffma2_rn(make_float2(rw, rw), f[h], yv[h]);
+                        ye[h] = __ffma2_rn(make_float2(rw, rw), f[h], ye[h]);
+                }
+                float* yp = a.y + (size_t)m.tok * a.d + (size_t)m.rb * a.rb_rows + rg * RPL;
+#pragma unroll
+                for (int h = 0; h < HPL; h += 2) {
+                    const float4 pp = *reinterpret_cast<const float4*>(ypart + 2 * h);
+                    __stcs(reinterpret_cast<float4*>(yp + 2 * h),
+                           make_float4(pp.x + ye[h].x, pp.y + ye[h].y, pp.z + ye[h + 1].x,
+                                       pp.w + ye[h + 1].y));
                 }
             }
-        }
-#pragma unroll
-        for (int h = 0; h < HPL; ++h)
-            yv[h] = slot_group_sum(yv[h]);
-        if (sg == 0 && act) {
-            float* yp = a.y + (size_t)m.tok * a.d + (size_t)m.rb * a.rb_rows + rg * RPL;
-#pragma unroll
-            for (int h = 0; h < HPL; h += 2)
-                __stcs(reinterpret_cast<float4*>(yp + 2 * h),
-                       make_float4(yv[h].x, yv[h].y, yv[h + 1].x, yv[h + 1].y));
         }
         if (!issued && uniform_test(lmark, k & 1) &&
             uniform_test(posted_next, ((k + 1) >> 1) & 1)) {
@@ -839,6 +881,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a)
     unsigned char* rbuf = smem + (size_t)W * kStride;
     Meta* meta = reinterpret_cast<Meta*>(smem + (size_t)3 * W * kStride);
     uint64_t* bars = reinterpret_cast<uint64_t*>(meta + 2);
+    float* ybuf = reinterpret_cast<float*>(bars + kNumBars);   // [64 row groups][8 rows]
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(bars + kFullW), kCWarps);
         mbar_init(smem_u32(bars + kWfree), 1);
@@ -863,7 +906,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a)
     // warpgroup (warps 16..19) gives back down to 64 (128 x 64 = 8,192): 61,440 in all.
     if (warp < kCWarps) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kConsumerRegs) : "memory");
-        role_consumer<S, W>(a, wbuf, rbuf, meta, bars);
+        role_consumer<S, W>(a, wbuf, rbuf, meta, bars, ybuf);
         return;
     }
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRoleRegs) : "memory");
@@ -880,7 +923,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a)
 template <typename S, int W>
 cudaError_t launch_scan_t(const ScanArgs& a, cudaStream_t s)
 {
-    const size_t smem = (size_t)3 * W * kStride + 2 * sizeof(Meta) + kNumBars * sizeof(uint64_t);
+    const size_t smem = (size_t)3 * W * kStride + 2 * sizeof(Meta) + kNumBars * sizeof(uint64_t) +
+                        (size_t)(kChunk / 16) * 8 * sizeof(float);   // partial y: 64 row groups x 8 rows
     auto kern = scan_kernel<S, W>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
