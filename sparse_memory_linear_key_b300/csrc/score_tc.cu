@@ -46,6 +46,9 @@ constexpr uint32_t kABytes = kTileM * 128 * 2;        // two K atoms of 128 rows
 
 struct ScoreArgs {
     int ntok, n, khalf, W, tiles_per_kind, ctas_per_half;
+    int rep;               // 1: a tile holds 128 queries; 4: 32 queries, each in all four
+                           // TMEM lane quadrants, so all 16 epilogue warps share its rows
+    int qrows;             // queries a tile: 128 / rep
     float z;               // standard normal quantile of 1 - W/n (bracket of the W-th score)
     float* hv;
     int32_t* hi;
@@ -261,13 +264,17 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
                     break;
                 const int tl = cta + i * a.ctas_per_half;
                 const int kind = tl / a.tiles_per_kind;
-                const int row0 = (tl % a.tiles_per_kind) * kTileM;
+                const int row0 = (tl % a.tiles_per_kind) * a.qrows;
                 const CUtensorMap* mq = kind ? &map_qr : &map_qw;
                 const uint32_t fb = smem_u32(bars + 1 + s);
                 const uint32_t dst = s ? sA1 : sA0;
                 mbar_arrive_expect_tx(fb, (uint32_t)katoms * kTileM * 128);
+                // (the 1024-byte swizzle period divides a 32-row slice, so slices of
+                // a replicated tile land exactly as rows of a full one would)
                 for (int kb = 0; kb < katoms; ++kb)
-                    tma_load_2d(dst + kb * (kABytes / 2), mq, half * a.khalf + kb * kKAtom, row0, fb);
+                    for (int r = 0; r < a.rep; ++r)
+                        tma_load_2d(dst + kb * (kABytes / 2) + r * a.qrows * 128, mq,
+                                    half * a.khalf + kb * kKAtom, row0, fb);
                 armed[s] = i;
             }
             // copies in flight land before the CTA may end
@@ -312,27 +319,33 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
         }
     } else {
         // ---------------- epilogue: per-row top-W of the scores. Warp e = warp - 2 reads
-        // TMEM lane quadrant q = warp % 4 (the quadrant a warp may access) and column
-        // group g = e / 4; the four warps of a quadrant add up their counts per row
-        // through shared memory at a named barrier (id 1 + q). They run the same number
-        // of barrier rounds (same rows, same totals) and leave together, so none can be
-        // left waiting at a barrier.
-        const int q = warp & 3, g = (warp - 2) >> 2;
-        const int bid = 1 + q;
+        // TMEM lane quadrant q = warp % 4 (the quadrant a warp may access). With 128
+        // queries a tile, the four warps of a quadrant share its 32 rows, one column group
+        // g = e / 4 each, and add up their counts per row through shared memory at a
+        // named barrier (id 1 + q, 128 threads). With replicated queries every quadrant
+        // holds the same 32 rows, and all 16 warps share them, column group g = e, at one
+        // barrier of 512 threads. The warps at a barrier run the same number of rounds
+        // (same rows, same totals) and leave together, so none can be left waiting.
+        const int q = warp & 3;
+        const int G = a.rep == 1 ? 4 : 16;                          // column groups a row
+        const int g = a.rep == 1 ? (warp - 2) >> 2 : warp - 2;
+        const int xs0 = a.rep == 1 ? q : 0;                         // exchange block
+        const int bid = a.rep == 1 ? 1 + q : 1;
+        const int bn = 32 * G;                                      // threads at the barrier
         const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
         const int W = a.W;
-        const int CW = ((NP + 4 * 32 - 1) / (4 * 32)) * 32;       // columns a group reads
+        const int CW = ((NP + G * 32 - 1) / (G * 32)) * 32;         // columns a group reads
         const int cb = min(NP, g * CW), ce = min(NP, cb + CW);
-        const int xi = (q * 4 + g) * 32 + lane;                     // own exchange slot
-        const int xq = q * 4 * 32 + lane;                           // group 0 of this lane
+        const int xi = (xs0 * G + g) * 32 + lane;                   // own exchange slot
+        const int xq = xs0 * G * 32 + lane;                         // group 0 of this lane
         for (int i = 0; i < my_tiles; ++i) {
             const bool got = waitb(smem_u32(bars + 5), i & 1);
-            if (!bar_all(bid, 128, got))
+            if (!bar_all(bid, bn, got))
                 break;
             tc_fence_after();
             const int tl = cta + i * a.ctas_per_half;
             const int kind = tl / a.tiles_per_kind;
-            const int tok = (tl % a.tiles_per_kind) * kTileM + q * 32 + lane;
+            const int tok = (tl % a.tiles_per_kind) * a.qrows + (a.rep == 1 ? q * 32 : 0) + lane;
             uint32_t v[32];
             // keys in place of the scores (0 in padding columns), their range, and the
             // row's mean and spread
@@ -359,11 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
             xmax[xi] = kmax;
             xs[xi] = sum;
             xs2[xi] = sum2;
-            bar_sync(bid, 128);
+            bar_sync(bid, bn);
             sum = 0.f;
             sum2 = 0.f;
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
+            for (int h = 0; h < G; ++h) {
                 kmin = min(kmin, xmin[xq + h * 32]);
                 kmax = max(kmax, xmax[xq + h * 32]);
                 sum += xs[xq + h * 32];
@@ -391,9 +403,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
                 }
                 xb1[xi] = cl;
                 xb2[xi] = ch;
-                bar_sync(bid, 128);
-                cl = xb1[xq] + xb1[xq + 32] + xb1[xq + 64] + xb1[xq + 96];
-                ch = xb2[xq] + xb2[xq + 32] + xb2[xq + 64] + xb2[xq + 96];
+                bar_sync(bid, bn);
+                cl = 0;
+                ch = 0;
+                for (int h = 0; h < G; ++h) {
+                    cl += xb1[xq + h * 32];
+                    ch += xb2[xq + h * 32];
+                }
                 if (bl > lo && bl < hi) {
                     if (cl == W) {
                         lo = bl;
@@ -429,8 +445,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
                 }
                 int* xc = xcnt + (it & 1) * 512;
                 xc[xi] = cnt;
-                bar_sync(bid, 128);
-                cnt = xc[xq] + xc[xq + 32] + xc[xq + 64] + xc[xq + 96];
+                bar_sync(bid, bn);
+                cnt = 0;
+                for (int h = 0; h < G; ++h)
+                    cnt += xc[xq + h * 32];
                 if (active) {
                     if (cnt == W) {
                         lo = mid;
@@ -458,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
             }
             xa[xi] = ka;
             xt[xi] = kt;
-            bar_sync(bid, 128);
+            bar_sync(bid, bn);
             int pre_a = 0, pre_t = 0;
             for (int h = 0; h < g; ++h) {
                 pre_a += xa[xq + h * 32];
@@ -566,9 +584,15 @@ cudaError_t launch_score_tc(const sdm_cfg& c, const void* K1, const void* K2, co
     if (ntok <= 0)
         return cudaSuccess;
     const int h = c.dk / 2;
+    // Replicated queries when the tiles of 128 would leave most SMs idle: four times the
+    // CTAs, a quarter of the columns per epilogue thread.
+    const int sms = num_sms_current_device();
+    const int64_t full_tiles = 2 * 2 * ((ntok + kTileM - 1) / kTileM);
+    const int rep_ = full_tiles * 2 < sms ? 4 : 1;
+    const int qrows = kTileM / rep_;
     CUtensorMap mqw, mqr, mk1, mk2;
-    if (!make_map(&mqw, q_w, (uint64_t)c.dk, (uint64_t)ntok, kTileM) ||
-        !make_map(&mqr, q_r, (uint64_t)c.dk, (uint64_t)ntok, kTileM) ||
+    if (!make_map(&mqw, q_w, (uint64_t)c.dk, (uint64_t)ntok, (uint32_t)qrows) ||
+        !make_map(&mqr, q_r, (uint64_t)c.dk, (uint64_t)ntok, (uint32_t)qrows) ||
         !make_map(&mk1, K1, (uint64_t)h, (uint64_t)c.n_sub, 256) ||
         !make_map(&mk2, K2, (uint64_t)h, (uint64_t)c.n_sub, 256))
         return cudaErrorInvalidValue;
@@ -578,8 +602,10 @@ cudaError_t launch_score_tc(const sdm_cfg& c, const void* K1, const void* K2, co
     a.khalf = h;
     a.W = c.w;
     a.z = normal_upper_quantile((double)c.w / c.n_sub);
-    a.tiles_per_kind = (int)((ntok + kTileM - 1) / kTileM);
-    int per_half = num_sms_current_device() / 2;
+    a.rep = rep_;
+    a.qrows = qrows;
+    a.tiles_per_kind = (int)((ntok + qrows - 1) / qrows);
+    int per_half = sms / 2;
     if (per_half > 2 * a.tiles_per_kind)
         per_half = 2 * a.tiles_per_kind;
     if (per_half < 1)

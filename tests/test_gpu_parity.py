@@ -30,6 +30,10 @@ SMALL = {
     # the full 480 x 480 product-key grid and key width, small d
     "n480-small-d": synth.Workload("n480-small-d", B=1, T=257, d=32, n=480, dk=256, W=64,
                                    dtype="bf16", seed=81),
+    # enough tokens for the scorer's tiles of 128 queries (fewer take replicated tiles
+    # of 32), with a ragged last tile
+    "n480-full-tiles": synth.Workload("n480-full-tiles", B=4, T=700, d=32, n=480, dk=256,
+                                      W=64, dtype="bf16", seed=82),
 }
 
 
@@ -93,6 +97,37 @@ def test_address_parity(name):
         err = tl.max_weight_err(idx[:, kind], wsel[:, kind], S, k, range(len(S)))
         assert err <= tl.WEIGHT_ATOL, (name, kind, err)
         np.testing.assert_allclose(wsel[:, kind].sum(-1), 1.0, atol=1e-5)
+
+
+def test_address_tile_modes_agree():
+    """The tensor-core scorer takes tiles of 128 queries for large batches and tiles of
+    32 replicated queries for small ones. Each score is the same dot product either way
+    and the selection is exact, so the addressing of a token must not depend on the
+    batch it came in: bits of a 2,800-token call against calls on slices of it."""
+    wl = SMALL["n480-full-tiles"]
+    cfg = tl.cfg_of(wl)
+    p = tl.to_dev(synth.make_params(wl, with_m0=False))
+    g = torch.Generator().manual_seed(5)
+    ntok = wl.B * wl.T
+    q_w = torch.randn(ntok, wl.dk, generator=g).to(torch.bfloat16).cuda()
+    q_r = torch.randn(ntok, wl.dk, generator=g).to(torch.bfloat16).cuda()
+    st = sdm.new_status()
+
+    def address(lo, hi):
+        n = hi - lo
+        idx = torch.empty(n, 2, wl.W, dtype=torch.int32, device="cuda")
+        w = torch.empty(n, 2, wl.W, device="cuda")
+        ws = sdm.alloc_workspace(sdm.address_workspace_bytes(cfg, n))
+        sdm.sdm_address(cfg, p["K1"], p["K2"], q_w[lo:hi].contiguous(), q_r[lo:hi].contiguous(),
+                        idx, w, ws, st)
+        return idx.cpu(), w.cpu()
+
+    idx_all, w_all = address(0, ntok)
+    for lo, hi in ((0, 64), (1000, 1257), (ntok - 33, ntok)):
+        idx, w = address(lo, hi)
+        assert torch.equal(idx, idx_all[lo:hi]), (lo, hi)
+        assert torch.equal(w, w_all[lo:hi]), (lo, hi)
+    assert sdm.read_status(st) == 0
 
 
 @pytest.mark.parametrize("name", list(SMALL))
