@@ -70,4 +70,85 @@ int launch_project(const sdm_cfg& c, const sdm_weights& w, const void* x, int64_
     return SDM_OK;
 }
 
+// ---------------------------------------------------------- forked projections
+
+// Per device: two side streams with a cuBLAS handle each, and the events that fork them
+// off the caller's stream and join them back. q_w runs on the caller's stream, q_r and v
+// on the side streams; the caller's stream waits for q_r before the addressing, and only
+// the scan waits for v. Everything is recorded with events, so the three GEMMs overlap
+// in eager use and become parallel branches when the caller captures a graph.
+struct Fork {
+    bool ready = false;
+    cudaStream_t side[2] = {nullptr, nullptr};
+    cublasHandle_t h[2] = {nullptr, nullptr};
+    cudaEvent_t ev_fork = nullptr, ev_q = nullptr, ev_v = nullptr;
+};
+static Fork g_fork[64];
+
+static Fork* fork_state()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return nullptr;
+    Fork& f = g_fork[dev];
+    if (f.ready)
+        return &f;
+    for (int i = 0; i < 2; ++i) {
+        if (f.side[i] == nullptr &&
+            cudaStreamCreateWithFlags(&f.side[i], cudaStreamNonBlocking) != cudaSuccess)
+            return nullptr;
+        if (f.h[i] == nullptr && cublasCreate(&f.h[i]) != CUBLAS_STATUS_SUCCESS)
+            return nullptr;
+        if (cublasSetStream(f.h[i], f.side[i]) != CUBLAS_STATUS_SUCCESS)
+            return nullptr;
+    }
+    cudaEvent_t* evs[3] = {&f.ev_fork, &f.ev_q, &f.ev_v};
+    for (cudaEvent_t* e : evs)
+        if (*e == nullptr && cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess)
+            return nullptr;
+    f.ready = true;
+    return &f;
+}
+
+int launch_project_forked(const sdm_cfg& c, const sdm_weights& w, const void* x, int64_t ntok,
+                          void* q_w, void* q_r, void* v, cudaStream_t s, void* blas_ws,
+                          size_t blas_ws_bytes, std::unique_lock<std::mutex>& lock,
+                          cudaEvent_t* v_ready)
+{
+    *v_ready = nullptr;
+    if (ntok <= 0)
+        return SDM_OK;
+    if (ntok > 0x7FFFFFFF)
+        return SDM_EUNSUPPORTED;
+    lock = std::unique_lock<std::mutex>(g_blas_mu);
+    cublasHandle_t h = blas_handle(1);
+    Fork* f = fork_state();
+    if (h == nullptr || f == nullptr)
+        return SDM_ECUDA;
+    // the workspace region in three parts, one per concurrent GEMM
+    const size_t part = (blas_ws_bytes / 3) & ~(size_t)255;
+    char* wsb = (char*)blas_ws;
+    const bool bf = c.dtype == SDM_BF16;
+    if (cudaEventRecord(f->ev_fork, s) != cudaSuccess ||
+        cudaStreamWaitEvent(f->side[0], f->ev_fork, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(f->side[1], f->ev_fork, 0) != cudaSuccess)
+        return SDM_ECUDA;
+    const bool ok =
+        cublasSetStream(h, s) == CUBLAS_STATUS_SUCCESS &&
+        cublasSetWorkspace(h, wsb, part) == CUBLAS_STATUS_SUCCESS &&
+        cublasSetWorkspace(f->h[0], wsb + part, part) == CUBLAS_STATUS_SUCCESS &&
+        cublasSetWorkspace(f->h[1], wsb + 2 * part, part) == CUBLAS_STATUS_SUCCESS &&
+        gemm(f->h[1], bf, x, w.W_v, v, ntok, c.d, c.d) == CUBLAS_STATUS_SUCCESS &&
+        gemm(f->h[0], bf, x, w.W_qr, q_r, ntok, c.d, c.dk) == CUBLAS_STATUS_SUCCESS &&
+        gemm(h, bf, x, w.W_qw, q_w, ntok, c.d, c.dk) == CUBLAS_STATUS_SUCCESS;
+    // both side streams join back whatever happened (a forked capture must rejoin)
+    const bool joined = cudaEventRecord(f->ev_q, f->side[0]) == cudaSuccess &&
+                        cudaStreamWaitEvent(s, f->ev_q, 0) == cudaSuccess &&
+                        cudaEventRecord(f->ev_v, f->side[1]) == cudaSuccess;
+    if (!joined)
+        return SDM_ECUDA;
+    *v_ready = f->ev_v;
+    return ok ? SDM_OK : SDM_ECUDA;
+}
+
 }  // namespace sdm

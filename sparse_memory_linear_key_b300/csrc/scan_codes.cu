@@ -162,6 +162,43 @@ __global__ void __launch_bounds__(kCodeThreads) codes_kernel(const int32_t* __re
     }
 }
 
+// One token per sequence (a decode step): no earlier token exists, so every write code
+// is "no writer" and a read's only possible writer is its own token (dt = 0). One warp
+// per token matches the read set against the write set; the masks are all zero.
+__global__ void __launch_bounds__(256) codes_single_kernel(const int32_t* __restrict__ idx, int B,
+                                                           int W, int N, uint16_t* __restrict__ codes,
+                                                           unsigned long long* __restrict__ masks,
+                                                           int* status)
+{
+    const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (b >= B)
+        return;
+    const int32_t* wr = idx + (size_t)b * 2 * W;
+    const int32_t* rd = wr + W;
+    uint16_t* cw = codes + (size_t)b * 2 * W;
+    uint16_t* cr = cw + W;
+    for (int j0 = 0; j0 < W; j0 += 32) {
+        const int j = j0 + lane;
+        const int32_t r = j < W ? __ldg(rd + j) : -1;
+        int pos = -1;
+        for (int i = 0; i < W; ++i) {
+            const int32_t wv = __ldg(wr + i);   // same address in every lane: one load
+            if (wv == r && pos < 0)
+                pos = i;
+        }
+        if (j < W) {
+            const int32_t wv = __ldg(wr + j);
+            if (wv < 0 || wv >= N)
+                report(status, SDM_ERANGE);
+            cw[j] = kNoFwd;
+            cr[j] = (r >= 0 && r < N && pos >= 0) ? (uint16_t)pos : kNoFwd;
+        }
+    }
+    if (lane < 4)
+        masks[(size_t)lane * B + b] = 0ull;   // the 4*B mask words (B*T = B), all zero
+}
+
 }  // namespace
 
 cudaError_t launch_scan_codes(const sdm_cfg& c, const int32_t* idx, int B, int T, int win,
@@ -170,6 +207,11 @@ cudaError_t launch_scan_codes(const sdm_cfg& c, const int32_t* idx, int B, int T
 {
     if (B <= 0 || T <= 0)
         return cudaSuccess;
+    if (T == 1) {
+        codes_single_kernel<<<(B + 7) / 8, 256, 0, s>>>(idx, B, c.w, c.n_sub * c.n_sub, codes, masks,
+                                                         status);
+        return cudaGetLastError();
+    }
     // masks: fwdmask [B*T], deadmask [B*T], warmask [B*T][2], all cleared first
     cudaError_t e = cudaMemsetAsync(masks, 0, (size_t)B * T * 4 * sizeof(unsigned long long), s);
     if (e != cudaSuccess)

@@ -208,12 +208,16 @@ int sdm_address(const sdm_cfg* cfg, const void* K1, const void* K2, const void* 
 
 static int scan_impl(const sdm_cfg& c, const int32_t* idx, const float* wsel, const void* v,
                      const float* alpha, const float* beta, void* banks, float* y, int B, int T,
-                     void* ws, size_t ws_bytes, int* dev_status, cudaStream_t s)
+                     void* ws, size_t ws_bytes, int* dev_status, cudaStream_t s,
+                     cudaEvent_t v_ready = nullptr)
 {
     const ScanWs L = scan_ws_layout(c, B, T);
     char* base = (char*)ws;
     cudaError_t e = launch_scan_codes(c, idx, B, T, L.win, (uint16_t*)(base + L.codes),
                                       (unsigned long long*)(base + L.masks), dev_status, s);
+    // v comes from a projection forked off the stream: the scan is its first reader
+    if (v_ready != nullptr && cudaStreamWaitEvent(s, v_ready, 0) != cudaSuccess)
+        return SDM_ECUDA;
     if (e != cudaSuccess)
         return SDM_ECUDA;
     e = launch_scan(c, idx, wsel, v, alpha, beta, banks, y, B, T, ws, ws_bytes, dev_status, s);
@@ -326,14 +330,24 @@ int sdm_prefill(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const f
     float* wsel = w_out ? w_out : (float*)(base + L.wsel);
 
     cudaStream_t s = (cudaStream_t)stream;
-    rc = launch_project(*cfg, *w, x, ntok, q_w, q_r, v, s, base + L.blas, kBlasWsBytes);
-    if (rc != SDM_OK)
+    // the projections fork off the stream and join it again (v before the scan); the
+    // lock keeps another thread's call off the fork's events until the join is enqueued
+    std::unique_lock<std::mutex> lock;
+    cudaEvent_t v_ready = nullptr;
+    rc = launch_project_forked(*cfg, *w, x, ntok, q_w, q_r, v, s, base + L.blas, kBlasWsBytes, lock,
+                               &v_ready);
+    if (rc != SDM_OK) {
+        if (v_ready != nullptr)
+            cudaStreamWaitEvent(s, v_ready, 0);
         return rc;
+    }
     if (launch_address(*cfg, w->K1, w->K2, q_w, q_r, ntok, idx, wsel, base + L.addr, dev_status,
-                       s) != cudaSuccess)
+                       s) != cudaSuccess) {
+        cudaStreamWaitEvent(s, v_ready, 0);
         return SDM_ECUDA;
+    }
     return scan_impl(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, base + L.scan,
-                     scan_ws_layout(*cfg, B, T).total, dev_status, s);
+                     scan_ws_layout(*cfg, B, T).total, dev_status, s, v_ready);
 }
 
 int sdm_decode_step(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const float* alpha,

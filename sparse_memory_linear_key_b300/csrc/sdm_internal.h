@@ -1,6 +1,7 @@
 // sdm_internal.h -- launchers shared between the C-ABI layer and the kernel files.
 #pragma once
 
+#include <mutex>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -27,6 +28,13 @@ constexpr size_t kBlasWsBytes = (size_t)32 << 20;
 int launch_project(const sdm_cfg& c, const sdm_weights& w, const void* x, int64_t ntok,
                    void* q_w, void* q_r, void* v, cudaStream_t s, void* blas_ws = nullptr,
                    size_t blas_ws_bytes = 0);
+// The same three GEMMs forked over two side streams (sdm_prefill / sdm_decode_step):
+// returns with `lock` held and *v_ready the event that v is done on; the caller makes its
+// stream wait for it before the scan, then releases the lock (the events are per device).
+int launch_project_forked(const sdm_cfg& c, const sdm_weights& w, const void* x, int64_t ntok,
+                          void* q_w, void* q_r, void* v, cudaStream_t s, void* blas_ws,
+                          size_t blas_ws_bytes, std::unique_lock<std::mutex>& lock,
+                          cudaEvent_t* v_ready);
 
 // ---- addressing (address.cu, score_tc.cu)
 bool score_tc_supported(const sdm_cfg& c);
