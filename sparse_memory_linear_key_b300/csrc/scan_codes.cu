@@ -178,22 +178,28 @@ __global__ void __launch_bounds__(256) codes_single_kernel(const int32_t* __rest
     const int32_t* rd = wr + W;
     uint16_t* cw = codes + (size_t)b * 2 * W;
     uint16_t* cr = cw + W;
-    for (int j0 = 0; j0 < W; j0 += 32) {
-        const int j = j0 + lane;
-        const int32_t r = j < W ? __ldg(rd + j) : -1;
-        int pos = -1;
-        for (int i = 0; i < W; ++i) {
-            const int32_t wv = __ldg(wr + i);   // same address in every lane: one load
-            if (wv == r && pos < 0)
-                pos = i;
-        }
-        if (j < W) {
-            const int32_t wv = __ldg(wr + j);
-            if (wv < 0 || wv >= N)
-                report(status, SDM_ERANGE);
-            cw[j] = kNoFwd;
-            cr[j] = (r >= 0 && r < N && pos >= 0) ? (uint16_t)pos : kNoFwd;
-        }
+    // the write set in registers (lane l holds positions l and l + 32), read set likewise
+    const int32_t w0 = lane < W ? __ldg(wr + lane) : -1;
+    const int32_t w1 = lane + 32 < W ? __ldg(wr + lane + 32) : -1;
+    const int32_t r0 = lane < W ? __ldg(rd + lane) : -1;
+    const int32_t r1 = lane + 32 < W ? __ldg(rd + lane + 32) : -1;
+    int p0 = -1, p1 = -1;
+    for (int i = 0; i < W; ++i) {
+        const int32_t wv = __shfl_sync(0xFFFFFFFFu, i < 32 ? w0 : w1, i & 31);
+        if (wv == r0 && p0 < 0)
+            p0 = i;
+        if (wv == r1 && p1 < 0)
+            p1 = i;
+    }
+    if ((lane < W && (w0 < 0 || w0 >= N)) || (lane + 32 < W && (w1 < 0 || w1 >= N)))
+        report(status, SDM_ERANGE);
+    if (lane < W) {
+        cw[lane] = kNoFwd;
+        cr[lane] = (r0 >= 0 && r0 < N && p0 >= 0) ? (uint16_t)p0 : kNoFwd;
+    }
+    if (lane + 32 < W) {
+        cw[lane + 32] = kNoFwd;
+        cr[lane + 32] = (r1 >= 0 && r1 < N && p1 >= 0) ? (uint16_t)p1 : kNoFwd;
     }
     if (lane < 4)
         masks[(size_t)lane * B + b] = 0ull;   // the 4*B mask words (B*T = B), all zero
