@@ -3,9 +3,11 @@
 
 Workload (N=1): prefill of 4 sequences x 4096 tokens, d = 2048, N = 480^2 slots,
 W = 64, key width 256, bf16 banks (the 1.4B-scale layer of the pages). One step is
-one pass of the whole hot path over that batch: bank initialisation from M0, the
-projections, product-key addressing, the collision codes and the recurrent scan.
-Inputs are synthetic and seeded (synth/).
+one pass of the whole hot path over that batch: the projections, product-key
+addressing, the collision codes, and the recurrent scan with the bank initialisation
+from M0 fused into it (first touch: the scan reads M0 for slots its sequence has not
+written yet, and never-written slots get M0's row afterwards; bit-identical to a copy
+of M0 into every bank first). Inputs are synthetic and seeded (synth/).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--no-decode]
 
@@ -203,31 +205,39 @@ def gpu_arm(args, world, rank):
     y = torch.empty(ntok, d, dtype=torch.float32, device=dev)
     ws_a = sdm.alloc_workspace(sdm.address_workspace_bytes(cfg, ntok))
     ws_s = sdm.alloc_workspace(sdm.scan_workspace_bytes(cfg, B, T))
+    first_write = torch.empty(B, wl.N, dtype=torch.int32, device=dev)
     st = sdm.new_status()
     stream = torch.cuda.current_stream()
 
-    names = ["init", "project", "address", "codes", "scan"]
+    # Bank initialisation is fused: the scan reads M0 for slots not yet written in the
+    # sequence (first-touch table), and the slots a sequence never writes get M0's row
+    # afterwards -- bit-identical to copying M0 into every bank first.
+    names = ["project", "address", "codes", "first_touch", "scan", "fill"]
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
           for _ in range(args.steps)]
 
     def step(e=None):
         if e is not None:
             e[0].record(stream)
-        sdm.sdm_init_bank(cfg, p["M0"], banks)
-        if e is not None:
-            e[1].record(stream)
         sdm.sdm_project(cfg, p, x, q_w, q_r, v)
         if e is not None:
-            e[2].record(stream)
+            e[1].record(stream)
         sdm.sdm_address(cfg, p["K1"], p["K2"], q_w, q_r, idx, wsel, ws_a, st)
         if e is not None:
-            e[3].record(stream)
+            e[2].record(stream)
         sdm.sdm_scan_prepare(cfg, idx, B, T, ws_s, st)
         if e is not None:
+            e[3].record(stream)
+        sdm.sdm_first_touch(cfg, idx, B, T, first_write)
+        if e is not None:
             e[4].record(stream)
-        sdm.sdm_scan_run(cfg, idx, wsel, v, alpha, beta, banks, y, B, T, ws_s, st)
+        sdm.sdm_scan_run_m0(cfg, idx, wsel, v, alpha, beta, p["M0"], first_write, banks, y, B, T,
+                            ws_s, st)
         if e is not None:
             e[5].record(stream)
+        sdm.sdm_fill_untouched(cfg, p["M0"], first_write, banks, B, T)
+        if e is not None:
+            e[6].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -281,13 +291,15 @@ def gpu_arm(args, world, rank):
         "data": "synthetic (seeded; x~N(0,1), weights N(0,1/sqrt(fan_in)), M0~N(0,0.02))",
         "config": {"workload": WORKLOAD, "B": B, "T": T, "d": d, "N": wl.N, "W": wl.W,
                    "dk": wl.dk, "state": "bf16", "parallelism": "replicas" if world > 1 else "1gpu",
-                   "l2": "inputs larger than L2: each step writes/reads 3.8 GB of banks",
-                   "step": "bank init + projections + addressing + codes + scan"},
+                   "l2": "inputs larger than L2: each step moves > 15 GB of bank and M0 rows",
+                   "step": "projections + addressing + codes + bank init fused as first touch "
+                           "(M0 read by the scan for slots not yet written, never-written slots "
+                           "filled from M0) + scan"},
         "stages_ms": {k: round(v_, 4) for k, v_ in stage_ms.items()},
         "scan_tokens_per_s": round(ntok / scan_s, 1),
         "roofline": roofline,
         "clocks": clocks.summary(),
-        "gpu_launches": 5 * args.steps * 1,
+        "gpu_launches": 6 * args.steps,
         "library_launches": {"cublas_gemm": 3 * args.steps},
     }
 
@@ -296,7 +308,7 @@ def gpu_arm(args, world, rank):
     a_h = tok_cpu["alpha"].pin_memory()
     b_h = tok_cpu["beta"].pin_memory()
     y_h = torch.empty(B, T, d, dtype=torch.float32).pin_memory()
-    ws_p = sdm.alloc_workspace(sdm.workspace_bytes(cfg, B, T))
+    ws_p = sdm.alloc_workspace(sdm.prefill_m0_workspace_bytes(cfg, B, T))
     x_d = torch.empty_like(x)
     a_d = torch.empty_like(alpha)
     b_d = torch.empty_like(beta)
@@ -306,8 +318,7 @@ def gpu_arm(args, world, rank):
         x_d.copy_(x_h, non_blocking=True)
         a_d.copy_(a_h, non_blocking=True)
         b_d.copy_(b_h, non_blocking=True)
-        sdm.sdm_init_bank(cfg, p["M0"], banks)
-        sdm.sdm_prefill(cfg, p, x_d, a_d, b_d, banks, y_d, ws_p, st)
+        sdm.sdm_prefill_m0(cfg, p, p["M0"], x_d, a_d, b_d, banks, y_d, ws_p, st)
         y_h.copy_(y_d, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):

@@ -186,6 +186,40 @@ SDM_API int sdm_prefill(const sdm_cfg* cfg, const sdm_weights* wts, const void* 
                 const float* beta, void* banks, float* y, int B, int T, int32_t* idx_out,
                 float* w_out, void* ws, size_t ws_bytes, int* dev_status, void* stream);
 
+/* Bank initialisation fused into the recurrence. The learned initial state
+ * ("Sparse Delta Memory: Scaling the State of Linear RNNs through Sparsity", Abstract)
+ * is the same M0 for every sequence, and before token t a slot still holds M0 unless an
+ * earlier token of its sequence wrote it. So instead of copying M0 into every bank
+ * (sdm_init_bank, 2 * B * N * d elements of traffic), the scan loads M0 for those
+ * references, and afterwards only the slots a sequence never wrote get M0's row. The
+ * result is bit-identical to sdm_init_bank followed by the same calls without M0.
+ *
+ * sdm_first_touch: first_write [B, N] int32 <- for each sequence b and slot s, the first
+ *   token t whose write set (idx[b*T+t][0][:]) holds s, or a value >= T if none;
+ *   sdm_first_touch_bytes(cfg, B) = B * N * 4 bytes, 16-byte aligned, caller-owned.
+ * sdm_scan_run_m0: sdm_scan_run with banks that start as M0 (their content on entry is
+ *   read only for slots written earlier in the same call); M0 [N, d] must not overlap
+ *   banks, first_write from sdm_first_touch on the same idx, B and T.
+ * sdm_fill_untouched: banks[b][s] <- M0[s] wherever first_write[b][s] >= T.
+ * sdm_prefill_m0: sdm_prefill from M0: the banks' content on entry is ignored; on
+ *   return they hold the state after the T tokens, as after sdm_init_bank + sdm_prefill.
+ *   ws: sdm_prefill_m0_workspace_bytes(cfg, B, T) (the prefill workspace plus the
+ *   first-touch table). T = 0 copies M0 into the banks. */
+SDM_API size_t sdm_first_touch_bytes(const sdm_cfg* cfg, int B);
+SDM_API int sdm_first_touch(const sdm_cfg* cfg, const int32_t* idx, int B, int T,
+                            int32_t* first_write, void* stream);
+SDM_API int sdm_scan_run_m0(const sdm_cfg* cfg, const int32_t* idx, const float* wsel,
+                            const void* v, const float* alpha, const float* beta, const void* M0,
+                            const int32_t* first_write, void* banks, float* y, int B, int T,
+                            const void* ws, size_t ws_bytes, int* dev_status, void* stream);
+SDM_API int sdm_fill_untouched(const sdm_cfg* cfg, const void* M0, const int32_t* first_write,
+                               void* banks, int B, int T, void* stream);
+SDM_API size_t sdm_prefill_m0_workspace_bytes(const sdm_cfg* cfg, int B, int T);
+SDM_API int sdm_prefill_m0(const sdm_cfg* cfg, const sdm_weights* wts, const void* M0,
+                           const void* x, const float* alpha, const float* beta, void* banks,
+                           float* y, int B, int T, int32_t* idx_out, float* w_out, void* ws,
+                           size_t ws_bytes, int* dev_status, void* stream);
+
 /* One decode step: advance B independent sequences by one token each.
  * x [B, d], alpha/beta [B], banks [B, N, d] (in place), y [B, d] fp32.
  * ws: sdm_workspace_bytes(cfg, B, 1) bytes. */

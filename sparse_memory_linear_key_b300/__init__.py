@@ -89,6 +89,12 @@ def lib():
             "sdm_scan_noalloc": ([CP, P, P, P, P, P, P, P, I, I, P, P], I),
             "sdm_prefill": ([CP, WP, P, P, P, P, P, I, I, P, P, P, S, P, P], I),
             "sdm_decode_step": ([CP, WP, P, P, P, P, P, I, P, S, P, P], I),
+            "sdm_first_touch_bytes": ([CP, I], S),
+            "sdm_first_touch": ([CP, P, I, I, P, P], I),
+            "sdm_scan_run_m0": ([CP, P, P, P, P, P, P, P, P, P, I, I, P, S, P, P], I),
+            "sdm_fill_untouched": ([CP, P, P, P, I, I, P], I),
+            "sdm_prefill_m0_workspace_bytes": ([CP, I, I], S),
+            "sdm_prefill_m0": ([CP, WP, P, P, P, P, P, P, I, I, P, P, P, S, P, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -275,6 +281,60 @@ def sdm_prefill(cfg: Cfg, params, x, alpha, beta, banks, y, ws, dev_status, idx_
                              _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
                              _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)),
            "sdm_prefill")
+
+
+def first_touch_bytes(cfg: Cfg, B: int) -> int:
+    return int(lib().sdm_first_touch_bytes(ctypes.byref(cfg), B))
+
+
+def prefill_m0_workspace_bytes(cfg: Cfg, B: int, T: int) -> int:
+    return int(lib().sdm_prefill_m0_workspace_bytes(ctypes.byref(cfg), B, T))
+
+
+def sdm_first_touch(cfg: Cfg, idx, B: int, T: int, first_write, stream=None) -> None:
+    _check(lib().sdm_first_touch(ctypes.byref(cfg), _ptr(idx, torch.int32, "idx"), B, T,
+                                 _ptr(first_write, torch.int32, "first_write"), _stream(stream)),
+           "sdm_first_touch")
+
+
+def sdm_scan_run_m0(cfg: Cfg, idx, wsel, v, alpha, beta, M0, first_write, banks, y, B: int,
+                    T: int, ws, dev_status, stream=None) -> None:
+    dt = cfg.torch_dtype
+    _check(lib().sdm_scan_run_m0(ctypes.byref(cfg), _ptr(idx, torch.int32, "idx"),
+                                 _ptr(wsel, torch.float32, "wsel"), _ptr(v, dt, "v"),
+                                 _ptr(alpha, torch.float32, "alpha"),
+                                 _ptr(beta, torch.float32, "beta"), _ptr(M0, dt, "M0"),
+                                 _ptr(first_write, torch.int32, "first_write"),
+                                 _ptr(banks, dt, "banks"), _ptr(y, torch.float32, "y"), B, T,
+                                 _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+                                 _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)),
+           "sdm_scan_run_m0")
+
+
+def sdm_fill_untouched(cfg: Cfg, M0, first_write, banks, B: int, T: int, stream=None) -> None:
+    dt = cfg.torch_dtype
+    _check(lib().sdm_fill_untouched(ctypes.byref(cfg), _ptr(M0, dt, "M0"),
+                                    _ptr(first_write, torch.int32, "first_write"),
+                                    _ptr(banks, dt, "banks"), B, T, _stream(stream)),
+           "sdm_fill_untouched")
+
+
+def sdm_prefill_m0(cfg: Cfg, params, M0, x, alpha, beta, banks, y, ws, dev_status, idx_out=None,
+                   w_out=None, stream=None) -> None:
+    """sdm_prefill with banks that start as M0 without a copy (their content on entry is
+    ignored); ws: prefill_m0_workspace_bytes(cfg, B, T) bytes."""
+    dt = cfg.torch_dtype
+    B, T = x.shape[0], x.shape[1]
+    w = _weights(cfg, params)
+    _check(lib().sdm_prefill_m0(ctypes.byref(cfg), ctypes.byref(w), _ptr(M0, dt, "M0"),
+                                _ptr(x, dt, "x"), _ptr(alpha, torch.float32, "alpha"),
+                                _ptr(beta, torch.float32, "beta"), _ptr(banks, dt, "banks"),
+                                _ptr(y, torch.float32, "y"), B, T,
+                                _ptr(idx_out, torch.int32, "idx_out"),
+                                _ptr(w_out, torch.float32, "w_out"),
+                                _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+                                _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)),
+           "sdm_prefill_m0")
 
 
 def sdm_decode_step(cfg: Cfg, params, x, alpha, beta, banks, y, ws, dev_status,

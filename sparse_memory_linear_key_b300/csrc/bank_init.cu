@@ -4,7 +4,8 @@
 //
 // HBM-bound copy: M0 is read once and written B times. Every thread moves 16-byte
 // chunks, four per iteration, with streaming stores; the grid is a multiple of the
-// SM count.
+// SM count. The first-touch kernels below give the same initial state without the
+// copy of slots the sequence writes.
 #include "sdm_common.cuh"
 #include "sdm_internal.h"
 
@@ -48,6 +49,94 @@ cudaError_t launch_bank_init(const void* M0, void* banks, size_t bank_bytes, int
     if (blocks > cap)
         blocks = cap;
     bank_init_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint4*)M0, (uint4*)banks, n16, B);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- first touch
+//
+// The same initial state without the copy. Before token t a slot holds M0 unless an
+// earlier token of its sequence wrote it, so the scan reads M0 for those references
+// (scan.cu) and only the slots a sequence never writes need M0 in its bank afterwards.
+// first_write[b][s] is the first token of sequence b whose write set holds s.
+
+__global__ void __launch_bounds__(256) first_touch_kernel(const int32_t* __restrict__ idx,
+                                                          int64_t nref, int T, int W, int N,
+                                                          int32_t* __restrict__ first_write)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nref; e += stride) {
+        const int64_t tok = e / W;                  // b * T + t
+        const int32_t s = __ldg(idx + tok * 2 * W + e % W);
+        if (s >= 0 && s < N)
+            atomicMin(first_write + (tok / T) * N + s, (int32_t)(tok % T));
+    }
+}
+
+// One warp per slot: the sequences that never wrote it (first_write >= T) get M0's row,
+// read once. Each lane moves 16 bytes a step, four steps in flight.
+__global__ void __launch_bounds__(256) fill_untouched_kernel(const uint4* __restrict__ M0,
+                                                             const int32_t* __restrict__ first_write,
+                                                             uint4* __restrict__ banks, int B, int T,
+                                                             int N, int row16)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t sl = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); sl < N;
+         sl += warps) {
+        for (int b0 = 0; b0 < B; b0 += 32) {
+            const int b = b0 + lane;
+            const bool fresh = b < B && __ldg(first_write + (int64_t)b * N + sl) >= T;
+            unsigned mask = __ballot_sync(0xFFFFFFFFu, fresh);
+            if (mask == 0)
+                continue;
+            const uint4* src = M0 + sl * row16;
+            for (int c0 = lane; c0 < row16; c0 += 4 * 32) {
+                uint4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (c0 + u * 32 < row16)
+                        v[u] = __ldg(src + c0 + u * 32);
+                for (unsigned m = mask; m != 0; m &= m - 1) {
+                    uint4* dst = banks + ((int64_t)(b0 + __ffs(m) - 1) * N + sl) * row16;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (c0 + u * 32 < row16)
+                            __stcs(dst + c0 + u * 32, v[u]);
+                }
+            }
+        }
+    }
+}
+
+cudaError_t launch_first_touch(const sdm_cfg& c, const int32_t* idx, int B, int T,
+                               int32_t* first_write, cudaStream_t s)
+{
+    if (B <= 0)
+        return cudaSuccess;
+    const int N = c.n_sub * c.n_sub;
+    // 0x7F7F7F7F: above every token index
+    cudaError_t e = cudaMemsetAsync(first_write, 0x7F, (size_t)B * N * sizeof(int32_t), s);
+    if (e != cudaSuccess || T <= 0)
+        return e;
+    const int64_t nref = (int64_t)B * T * c.w;
+    int64_t blocks = (nref + 255) / 256;
+    const int64_t cap = (int64_t)num_sms_current_device() * 8;
+    if (blocks > cap)
+        blocks = cap;
+    first_touch_kernel<<<(unsigned)blocks, 256, 0, s>>>(idx, nref, T, c.w, N, first_write);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fill_untouched(const sdm_cfg& c, const void* M0, const int32_t* first_write,
+                                  void* banks, int B, int T, cudaStream_t s)
+{
+    if (B <= 0)
+        return cudaSuccess;
+    const int N = c.n_sub * c.n_sub;
+    const int row16 = c.d * (c.dtype == SDM_BF16 ? 2 : 4) / 16;
+    const int64_t blocks = (int64_t)num_sms_current_device() * 8;
+    fill_untouched_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint4*)M0, first_write,
+                                                            (uint4*)banks, B, T, N, row16);
     return cudaGetLastError();
 }
 

@@ -88,6 +88,10 @@ struct ScanArgs {
     unsigned long long* counter;    // next item to claim
     int* abort_flag;
     unsigned char* ring;            // null: no forwarding ring
+    const unsigned char* m0;        // non-null: banks start as M0 without a copy; the
+                                    // first write of a slot in a sequence, and every
+                                    // read before it, loads the slot from M0
+    const int* first_write;         // [B][N] first token writing each slot (>= T: none)
     long long items;                // B * T * nrb
     int B, T, d, N, nrb, rb_rows, win, ring_entries, chunk_bytes;
 };
@@ -107,6 +111,7 @@ struct __align__(16) Meta {
     unsigned long long wload;       // bit j: write chunk j is gathered from the bank
     unsigned long long rload;       // bit j: read chunk j is gathered from the bank
     unsigned long long rdmask;      // bit j: read chunk j is copied by D (writer in flight)
+    unsigned long long m0w, m0r;    // bit j: write / read chunk j is gathered from M0
     long long tok;                  // b * T + t
     int b, t, rb, rows;
     float alpha, beta;
@@ -237,6 +242,7 @@ struct Ahead {
     unsigned long long item;
     int t, b, rb;
     int wid[JW], rid[JW];
+    int ftw[JW], ftr[JW];            // first writer of the slot in the sequence (M0 mode)
     uint16_t wc[JW], rc[JW];
     float alpha, beta;               // lane 0
     unsigned long long fwdmask, deadmask, war0, war1;  // lane 0
@@ -266,6 +272,18 @@ __device__ __forceinline__ void fetch_ahead(const ScanArgs& a, unsigned long lon
         } else {
             n.wid[jj] = n.rid[jj] = -1;
             n.wc[jj] = n.rc[jj] = kNoFwd;
+        }
+    }
+    // M0 mode: the first writer of each referenced slot in this sequence
+#pragma unroll
+    for (int jj = 0; jj < JW; ++jj) {
+        n.ftw[jj] = n.ftr[jj] = 0;
+        if (a.m0 != nullptr) {
+            const int* fw = a.first_write + (size_t)n.b * a.N;
+            if (n.wid[jj] >= 0 && n.wid[jj] < a.N)
+                n.ftw[jj] = __ldg(fw + n.wid[jj]);
+            if (n.rid[jj] >= 0 && n.rid[jj] < a.N)
+                n.ftr[jj] = __ldg(fw + n.rid[jj]);
         }
     }
     if (lane == 0) {
@@ -315,7 +333,7 @@ __device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
             return;
         fence_acq_rel_gpu();
 
-        unsigned long long wload = 0, rload = 0, fmask = 0, rdmask = 0;
+        unsigned long long wload = 0, rload = 0, fmask = 0, rdmask = 0, m0w = 0, m0r = 0;
 #pragma unroll
         for (int jj = 0; jj < JW; ++jj) {
             const int j = lane + 32 * jj;
@@ -334,6 +352,14 @@ __device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
                      << (32 * jj);
             fmask |= (unsigned long long)__ballot_sync(0xFFFFFFFFu, rown) << (32 * jj);
             rdmask |= (unsigned long long)__ballot_sync(0xFFFFFFFFu, rdep) << (32 * jj);
+            // M0 mode: a bank load of a slot no earlier token of the sequence wrote reads
+            // M0 (a write is the first when its token is the first writer)
+            m0w |= (unsigned long long)__ballot_sync(
+                       0xFFFFFFFFu, a.m0 != nullptr && wval && nx.wc[jj] == kNoFwd && nx.ftw[jj] >= t)
+                   << (32 * jj);
+            m0r |= (unsigned long long)__ballot_sync(
+                       0xFFFFFFFFu, a.m0 != nullptr && rval && !rown && !rdep && nx.ftr[jj] > t)
+                   << (32 * jj);
             if (has) {
                 m.wid[j] = wval ? nx.wid[jj] : -1;
                 m.rid[j] = rval ? nx.rid[jj] : -1;
@@ -351,6 +377,8 @@ __device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
             m.wload = wload;
             m.rload = rload;
             m.rdmask = rdmask;
+            m.m0w = m0w;
+            m.m0r = m0r;
             m.tok = (long long)b * a.T + t;
             m.b = b;
             m.t = t;
@@ -646,7 +674,11 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
         if (chunk) {
             const int id = is_r ? mn.rid[j] : mn.wid[j];
             unsigned char* dst = (is_r ? rbuf + (size_t)pn * W * kStride : wbuf) + (size_t)j * kStride;
-            bulk_g2s(smem_u32(dst), bank + (size_t)id * a.d * sizeof(S), cb, is_r ? fr : fw);
+            const bool from_m0 = (((is_r ? mn.m0r : mn.m0w) >> j) & 1) != 0;
+            const unsigned char* src =
+                from_m0 ? a.m0 + ((size_t)id * a.d + (size_t)mn.rb * a.rb_rows) * sizeof(S)
+                        : bank + (size_t)id * a.d * sizeof(S);
+            bulk_g2s(smem_u32(dst), src, cb, is_r ? fr : fw);
         } else if (wsel_copy) {
             bulk_g2s(smem_u32(mn.wsel), a.wsel + mn.tok * 2 * W, 2 * W * 4, fr);
         } else if (v_copy) {
@@ -981,7 +1013,8 @@ ScanWs scan_ws_layout(const sdm_cfg& c, int B, int T)
 
 cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel, const void* v,
                         const float* alpha, const float* beta, void* banks, float* y, int B,
-                        int T, void* ws, size_t ws_bytes, int* status, cudaStream_t s)
+                        int T, void* ws, size_t ws_bytes, int* status, cudaStream_t s,
+                        const void* m0, const int32_t* first_write)
 {
     if (B <= 0 || T <= 0)
         return cudaSuccess;
@@ -1005,6 +1038,8 @@ cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel,
     a.counter = (unsigned long long*)(base + L.flags + L.flags_bytes - 256);
     a.abort_flag = (int*)(base + L.flags + L.flags_bytes - 128);
     a.ring = ws_bytes >= L.total ? (unsigned char*)(base + L.ring) : nullptr;
+    a.m0 = (const unsigned char*)m0;
+    a.first_write = first_write;
     a.B = B;
     a.T = T;
     a.d = c.d;

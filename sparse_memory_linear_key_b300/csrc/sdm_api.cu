@@ -209,7 +209,8 @@ int sdm_address(const sdm_cfg* cfg, const void* K1, const void* K2, const void* 
 static int scan_impl(const sdm_cfg& c, const int32_t* idx, const float* wsel, const void* v,
                      const float* alpha, const float* beta, void* banks, float* y, int B, int T,
                      void* ws, size_t ws_bytes, int* dev_status, cudaStream_t s,
-                     cudaEvent_t v_ready = nullptr)
+                     cudaEvent_t v_ready = nullptr, const void* m0 = nullptr,
+                     const int32_t* first_write = nullptr)
 {
     const ScanWs L = scan_ws_layout(c, B, T);
     char* base = (char*)ws;
@@ -220,7 +221,8 @@ static int scan_impl(const sdm_cfg& c, const int32_t* idx, const float* wsel, co
         return SDM_ECUDA;
     if (e != cudaSuccess)
         return SDM_ECUDA;
-    e = launch_scan(c, idx, wsel, v, alpha, beta, banks, y, B, T, ws, ws_bytes, dev_status, s);
+    e = launch_scan(c, idx, wsel, v, alpha, beta, banks, y, B, T, ws, ws_bytes, dev_status, s, m0,
+                    first_write);
     return cuda_status(e);
 }
 
@@ -297,15 +299,85 @@ int sdm_scan(const sdm_cfg* cfg, const int32_t* idx, const float* wsel, const vo
                      (cudaStream_t)stream);
 }
 
-int sdm_prefill(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const float* alpha,
-                const float* beta, void* banks, float* y, int B, int T, int32_t* idx_out,
-                float* w_out, void* ws, size_t ws_bytes, int* dev_status, void* stream)
+// ------------------------------------------------------------- first-touch init
+
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb)
+{
+    const char* x = (const char*)a;
+    const char* y = (const char*)b;
+    return x < y + nb && y < x + na;
+}
+
+size_t sdm_first_touch_bytes(const sdm_cfg* cfg, int B)
+{
+    if (check_scan_cfg(cfg) != SDM_OK || B < 0)
+        return 0;
+    return (size_t)B * cfg->n_sub * cfg->n_sub * sizeof(int32_t);
+}
+
+int sdm_first_touch(const sdm_cfg* cfg, const int32_t* idx, int B, int T, int32_t* first_write,
+                    void* stream)
+{
+    int rc = check_scan_cfg(cfg);
+    if (rc != SDM_OK)
+        return rc;
+    if (B < 0 || T < 0)
+        return SDM_EINVAL;
+    if (B == 0)
+        return SDM_OK;
+    if (first_write == nullptr || (T > 0 && idx == nullptr) || !aligned16(first_write))
+        return SDM_EINVAL;
+    return cuda_status(launch_first_touch(*cfg, idx, B, T, first_write, (cudaStream_t)stream));
+}
+
+int sdm_scan_run_m0(const sdm_cfg* cfg, const int32_t* idx, const float* wsel, const void* v,
+                    const float* alpha, const float* beta, const void* M0,
+                    const int32_t* first_write, void* banks, float* y, int B, int T, const void* ws,
+                    size_t ws_bytes, int* dev_status, void* stream)
+{
+    const int rc = check_scan_args(cfg, idx, wsel, v, alpha, beta, banks, y, B, T, ws, ws_bytes,
+                                   dev_status);
+    if (rc != SDM_OK || B == 0 || T == 0)
+        return rc;
+    const size_t bank = (size_t)cfg->n_sub * cfg->n_sub * cfg->d * esize(*cfg);
+    if (M0 == nullptr || first_write == nullptr || !aligned16(M0) ||
+        overlaps(M0, bank, banks, bank * B))
+        return SDM_EINVAL;
+    return cuda_status(launch_scan(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T,
+                                   const_cast<void*>(ws), ws_bytes, dev_status,
+                                   (cudaStream_t)stream, M0, first_write));
+}
+
+int sdm_fill_untouched(const sdm_cfg* cfg, const void* M0, const int32_t* first_write,
+                       void* banks, int B, int T, void* stream)
+{
+    int rc = check_scan_cfg(cfg);
+    if (rc != SDM_OK)
+        return rc;
+    if (B < 0 || T < 0)
+        return SDM_EINVAL;
+    if (B == 0)
+        return SDM_OK;
+    const size_t bank = (size_t)cfg->n_sub * cfg->n_sub * cfg->d * esize(*cfg);
+    if (M0 == nullptr || first_write == nullptr || banks == nullptr || !aligned16(M0) ||
+        !aligned16(banks) || overlaps(M0, bank, banks, bank * B))
+        return SDM_EINVAL;
+    return cuda_status(
+        launch_fill_untouched(*cfg, M0, first_write, banks, B, T, (cudaStream_t)stream));
+}
+
+static int prefill_impl(const sdm_cfg* cfg, const sdm_weights* w, const void* M0, const void* x,
+                        const float* alpha, const float* beta, void* banks, float* y, int B, int T,
+                        int32_t* idx_out, float* w_out, void* ws, size_t ws_bytes,
+                        int* dev_status, void* stream)
 {
     int rc = sdm_check_cfg(cfg);
     if (rc != SDM_OK)
         return rc;
     if (w == nullptr || B < 0 || T < 0)
         return SDM_EINVAL;
+    if (B > 0 && T == 0 && M0 != nullptr)   // no tokens: the banks are just M0
+        return sdm_init_bank(cfg, M0, banks, B, stream);
     if (B == 0 || T == 0)
         return SDM_OK;
     const void* ptrs[] = {x, alpha, beta, banks, y, ws, dev_status, w->K1, w->K2};
@@ -320,8 +392,14 @@ int sdm_prefill(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const f
         return SDM_EINVAL;
     const int64_t ntok = (int64_t)B * T;
     const PrefillWs L = prefill_layout(*cfg, B, T);
-    if (ws_bytes < L.total)
+    const size_t bank = (size_t)cfg->n_sub * cfg->n_sub * cfg->d * esize(*cfg);
+    if (M0 != nullptr && (!aligned16(M0) || overlaps(M0, bank, banks, bank * B)))
+        return SDM_EINVAL;
+    // M0 mode: the first-touch table follows the prefill workspace
+    const size_t need = L.total + (M0 != nullptr ? align256((size_t)B * cfg->n_sub * cfg->n_sub * 4) : 0);
+    if (ws_bytes < need)
         return SDM_EWORKSPACE;
+    int32_t* first_write = M0 != nullptr ? (int32_t*)((char*)ws + L.total) : nullptr;
     char* base = (char*)ws;
     void* q_w = base + L.q_w;
     void* q_r = base + L.q_r;
@@ -342,12 +420,43 @@ int sdm_prefill(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const f
         return rc;
     }
     if (launch_address(*cfg, w->K1, w->K2, q_w, q_r, ntok, idx, wsel, base + L.addr, dev_status,
-                       s) != cudaSuccess) {
+                       s) != cudaSuccess ||
+        (M0 != nullptr && launch_first_touch(*cfg, idx, B, T, first_write, s) != cudaSuccess)) {
         cudaStreamWaitEvent(s, v_ready, 0);
         return SDM_ECUDA;
     }
-    return scan_impl(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, base + L.scan,
-                     scan_ws_layout(*cfg, B, T).total, dev_status, s, v_ready);
+    rc = scan_impl(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, base + L.scan,
+                   scan_ws_layout(*cfg, B, T).total, dev_status, s, v_ready, M0, first_write);
+    if (rc != SDM_OK || M0 == nullptr)
+        return rc;
+    return cuda_status(launch_fill_untouched(*cfg, M0, first_write, banks, B, T, s));
+}
+
+int sdm_prefill(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const float* alpha,
+                const float* beta, void* banks, float* y, int B, int T, int32_t* idx_out,
+                float* w_out, void* ws, size_t ws_bytes, int* dev_status, void* stream)
+{
+    return prefill_impl(cfg, w, nullptr, x, alpha, beta, banks, y, B, T, idx_out, w_out, ws,
+                        ws_bytes, dev_status, stream);
+}
+
+size_t sdm_prefill_m0_workspace_bytes(const sdm_cfg* cfg, int B, int T)
+{
+    const size_t base = sdm_workspace_bytes(cfg, B, T);
+    if (base == 0)
+        return 0;
+    return base + align256((size_t)B * cfg->n_sub * cfg->n_sub * 4);
+}
+
+int sdm_prefill_m0(const sdm_cfg* cfg, const sdm_weights* w, const void* M0, const void* x,
+                   const float* alpha, const float* beta, void* banks, float* y, int B, int T,
+                   int32_t* idx_out, float* w_out, void* ws, size_t ws_bytes, int* dev_status,
+                   void* stream)
+{
+    if (M0 == nullptr)
+        return SDM_EINVAL;
+    return prefill_impl(cfg, w, M0, x, alpha, beta, banks, y, B, T, idx_out, w_out, ws, ws_bytes,
+                        dev_status, stream);
 }
 
 int sdm_decode_step(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const float* alpha,

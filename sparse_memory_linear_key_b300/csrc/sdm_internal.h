@@ -65,9 +65,19 @@ cudaError_t launch_scan_codes(const sdm_cfg& c, const int32_t* idx, int B, int T
                               cudaStream_t s);
 // Runs the recurrence; `ws` holds what launch_scan_codes wrote. ws_bytes >= L.total
 // enables the forwarding ring.
+// m0 / first_write non-null: the banks start as M0 without a copy (first_touch below)
 cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel, const void* v,
                         const float* alpha, const float* beta, void* banks, float* y, int B,
-                        int T, void* ws, size_t ws_bytes, int* status, cudaStream_t s);
+                        int T, void* ws, size_t ws_bytes, int* status, cudaStream_t s,
+                        const void* m0 = nullptr, const int32_t* first_write = nullptr);
+
+// first_write [B][N] <- the first token of each sequence that writes each slot, or a
+// value >= T if none (bank_init.cu)
+cudaError_t launch_first_touch(const sdm_cfg& c, const int32_t* idx, int B, int T,
+                               int32_t* first_write, cudaStream_t s);
+// banks[b][s] <- M0[s] for every slot sequence b never wrote (first_write >= T)
+cudaError_t launch_fill_untouched(const sdm_cfg& c, const void* M0, const int32_t* first_write,
+                                  void* banks, int B, int T, cudaStream_t s);
 
 int num_sms_current_device();
 
