@@ -91,8 +91,8 @@ def max_over_ranks(world, x: float) -> float:
 # DRAM bytes (read + write) of one scan_kernel launch on this workload, from one ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum, 1 pass, full size). They hold
 # for the kernel sources they were taken on; any change to those makes them stale.
-SCAN_TRAFFIC = {"B": 4, "T": 4096, "bytes": 8439312e3 + 4480697e3,
-                "sources_sha256": {"scan.cu": "f49881c6490422ca", "sdm_common.cuh": "a8376df91a89808f"}}
+SCAN_TRAFFIC = {"B": 4, "T": 4096, "bytes": 8459700e3 + 4488772e3,
+                "sources_sha256": {"scan.cu": "fd3510bb4ffa4e40", "sdm_common.cuh": "a8376df91a89808f"}}
 
 
 def scan_traffic(B, T):
