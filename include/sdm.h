@@ -220,6 +220,26 @@ SDM_API int sdm_prefill_m0(const sdm_cfg* cfg, const sdm_weights* wts, const voi
                            float* y, int B, int T, int32_t* idx_out, float* w_out, void* ws,
                            size_t ws_bytes, int* dev_status, void* stream);
 
+/* Slot-access statistics, the pages' diagnostic of how the memory is used ("Sparse
+ * Delta Memory" blog, "Memory Access Patterns on a Needle-in-a-Haystack Task": which
+ * slots are written and read at each token position, and whether the slots written at
+ * the needle are the ones read at the query). idx [B, T, 2, w] as from sdm_address.
+ * Slot ids outside [0, N) are not counted.
+ * sdm_slot_counts: counts [B, N] uint32 (overwritten) <- for each sequence b and slot s,
+ *   the number of tokens t in [t0, t1) whose write (kind 0) or read (kind 1) set holds
+ *   s. Counts over [0, t) are the pages' cumulative writes up to position t.
+ * sdm_slot_overlap: out [B, 3] uint32 <- per sequence: the distinct slots written by the
+ *   tokens in [w0, w1), the distinct slots read by the tokens in [r0, r1), and the
+ *   distinct slots in both (the write-read bucket overlap). ws:
+ *   sdm_slot_overlap_workspace_bytes(cfg, B) (two N-bit maps per sequence).
+ * Windows must satisfy 0 <= lo <= hi <= T (SDM_EINVAL otherwise). */
+SDM_API int sdm_slot_counts(const sdm_cfg* cfg, const int32_t* idx, int B, int T, int kind,
+                            int t0, int t1, uint32_t* counts, void* stream);
+SDM_API size_t sdm_slot_overlap_workspace_bytes(const sdm_cfg* cfg, int B);
+SDM_API int sdm_slot_overlap(const sdm_cfg* cfg, const int32_t* idx, int B, int T, int w0, int w1,
+                             int r0, int r1, uint32_t* out, void* ws, size_t ws_bytes,
+                             void* stream);
+
 /* One decode step: advance B independent sequences by one token each.
  * x [B, d], alpha/beta [B], banks [B, N, d] (in place), y [B, d] fp32.
  * ws: sdm_workspace_bytes(cfg, B, 1) bytes. */

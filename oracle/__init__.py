@@ -234,3 +234,33 @@ def prefill_sequence(x, params, alpha, beta, W, rows=None, M=None):
     y = scan(M, vr, alpha, beta, Sw, kw, Sr, kr)
     return {"q_w": q_w, "q_r": q_r, "v": v, "S": Sw, "k": kw, "gap_w": gw,
             "R": Sr, "r": kr, "gap_r": gr, "y": y, "M": M, "rows": rows}
+
+
+# --------------------------------------------------------- slot-access statistics
+# The pages' diagnostic of memory use (Sparse Delta Memory blog, "Memory Access Patterns
+# on a Needle-in-a-Haystack Task": the slots written and read at each token position,
+# and the write-read bucket overlap). Written as the set definitions, with numpy.
+
+def slot_counts(idx, B, T, N, kind, t0, t1) -> np.ndarray:
+    """counts[b, s] = number of tokens t in [t0, t1) of sequence b whose write (kind 0)
+    or read (kind 1) set holds slot s. idx: [B*T, 2, W] int."""
+    idx = np.asarray(idx).reshape(B, T, 2, -1)
+    counts = np.zeros((B, N), np.int64)
+    for b in range(B):
+        for t in range(t0, t1):
+            for s in set(int(v) for v in idx[b, t, kind]):
+                if 0 <= s < N:
+                    counts[b, s] += 1
+    return counts
+
+
+def slot_overlap(idx, B, T, N, w0, w1, r0, r1) -> np.ndarray:
+    """Per sequence: [|written in [w0, w1)|, |read in [r0, r1)|, |both|] over distinct
+    slot ids in [0, N)."""
+    idx = np.asarray(idx).reshape(B, T, 2, -1)
+    out = np.zeros((B, 3), np.int64)
+    for b in range(B):
+        wr = {int(s) for s in idx[b, w0:w1, 0].ravel() if 0 <= s < N}
+        rd = {int(s) for s in idx[b, r0:r1, 1].ravel() if 0 <= s < N}
+        out[b] = (len(wr), len(rd), len(wr & rd))
+    return out

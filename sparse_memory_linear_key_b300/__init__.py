@@ -95,6 +95,9 @@ def lib():
             "sdm_fill_untouched": ([CP, P, P, P, I, I, P], I),
             "sdm_prefill_m0_workspace_bytes": ([CP, I, I], S),
             "sdm_prefill_m0": ([CP, WP, P, P, P, P, P, P, I, I, P, P, P, S, P, P], I),
+            "sdm_slot_counts": ([CP, P, I, I, I, I, I, P, P], I),
+            "sdm_slot_overlap_workspace_bytes": ([CP, I], S),
+            "sdm_slot_overlap": ([CP, P, I, I, I, I, I, I, P, P, S, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -335,6 +338,28 @@ def sdm_prefill_m0(cfg: Cfg, params, M0, x, alpha, beta, banks, y, ws, dev_statu
                                 _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
                                 _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)),
            "sdm_prefill_m0")
+
+
+def sdm_slot_counts(cfg: Cfg, idx, B: int, T: int, kind: int, t0: int, t1: int, counts,
+                    stream=None) -> None:
+    """counts [B, N] int32 (uint32 bits) <- per slot, the tokens in [t0, t1) whose write
+    (kind 0) or read (kind 1) set holds it."""
+    _check(lib().sdm_slot_counts(ctypes.byref(cfg), _ptr(idx, torch.int32, "idx"), B, T, kind,
+                                 t0, t1, _ptr(counts, torch.int32, "counts"), _stream(stream)),
+           "sdm_slot_counts")
+
+
+def slot_overlap_workspace_bytes(cfg: Cfg, B: int) -> int:
+    return int(lib().sdm_slot_overlap_workspace_bytes(ctypes.byref(cfg), B))
+
+
+def sdm_slot_overlap(cfg: Cfg, idx, B: int, T: int, w0: int, w1: int, r0: int, r1: int, out, ws,
+                     stream=None) -> None:
+    """out [B, 3] int32 <- distinct slots written in [w0, w1), read in [r0, r1), and in both."""
+    _check(lib().sdm_slot_overlap(ctypes.byref(cfg), _ptr(idx, torch.int32, "idx"), B, T, w0, w1,
+                                  r0, r1, _ptr(out, torch.int32, "out"), _ptr(ws, None, "ws"),
+                                  ws.numel() * ws.element_size(), _stream(stream)),
+           "sdm_slot_overlap")
 
 
 def sdm_decode_step(cfg: Cfg, params, x, alpha, beta, banks, y, ws, dev_status,

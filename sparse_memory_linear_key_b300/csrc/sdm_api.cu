@@ -459,6 +459,52 @@ int sdm_prefill_m0(const sdm_cfg* cfg, const sdm_weights* w, const void* M0, con
                         dev_status, stream);
 }
 
+// ------------------------------------------------------ slot-access statistics
+
+static bool window_ok(int lo, int hi, int T) { return 0 <= lo && lo <= hi && hi <= T; }
+
+int sdm_slot_counts(const sdm_cfg* cfg, const int32_t* idx, int B, int T, int kind, int t0, int t1,
+                    uint32_t* counts, void* stream)
+{
+    int rc = check_scan_cfg(cfg);
+    if (rc != SDM_OK)
+        return rc;
+    if (B < 0 || T < 0 || (kind != 0 && kind != 1) || !window_ok(t0, t1, T))
+        return SDM_EINVAL;
+    if (B == 0)
+        return SDM_OK;
+    if (counts == nullptr || (t1 > t0 && idx == nullptr) || !aligned16(counts))
+        return SDM_EINVAL;
+    return cuda_status(
+        launch_slot_counts(*cfg, idx, B, T, kind, t0, t1, counts, (cudaStream_t)stream));
+}
+
+size_t sdm_slot_overlap_workspace_bytes(const sdm_cfg* cfg, int B)
+{
+    if (check_scan_cfg(cfg) != SDM_OK || B < 0)
+        return 0;
+    return slot_overlap_ws_bytes(*cfg, B);
+}
+
+int sdm_slot_overlap(const sdm_cfg* cfg, const int32_t* idx, int B, int T, int w0, int w1, int r0,
+                     int r1, uint32_t* out, void* ws, size_t ws_bytes, void* stream)
+{
+    int rc = check_scan_cfg(cfg);
+    if (rc != SDM_OK)
+        return rc;
+    if (B < 0 || T < 0 || !window_ok(w0, w1, T) || !window_ok(r0, r1, T))
+        return SDM_EINVAL;
+    if (B == 0)
+        return SDM_OK;
+    if (out == nullptr || ws == nullptr || ((w1 > w0 || r1 > r0) && idx == nullptr) ||
+        ((uintptr_t)ws & 15u) != 0)
+        return SDM_EINVAL;
+    if (ws_bytes < slot_overlap_ws_bytes(*cfg, B))
+        return SDM_EWORKSPACE;
+    return cuda_status(
+        launch_slot_overlap(*cfg, idx, B, T, w0, w1, r0, r1, out, ws, (cudaStream_t)stream));
+}
+
 int sdm_decode_step(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const float* alpha,
                     const float* beta, void* banks, float* y, int B, void* ws, size_t ws_bytes,
                     int* dev_status, void* stream)

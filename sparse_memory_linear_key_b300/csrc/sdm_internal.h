@@ -75,6 +75,13 @@ cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel,
 // value >= T if none (bank_init.cu)
 cudaError_t launch_first_touch(const sdm_cfg& c, const int32_t* idx, int B, int T,
                                int32_t* first_write, cudaStream_t s);
+// slot-access statistics (slot_stats.cu)
+size_t slot_overlap_ws_bytes(const sdm_cfg& c, int B);
+cudaError_t launch_slot_counts(const sdm_cfg& c, const int32_t* idx, int B, int T, int kind,
+                               int t0, int t1, uint32_t* counts, cudaStream_t s);
+cudaError_t launch_slot_overlap(const sdm_cfg& c, const int32_t* idx, int B, int T, int w0, int w1,
+                                int r0, int r1, uint32_t* out, void* ws, cudaStream_t s);
+
 // banks[b][s] <- M0[s] for every slot sequence b never wrote (first_write >= T)
 cudaError_t launch_fill_untouched(const sdm_cfg& c, const void* M0, const int32_t* first_write,
                                   void* banks, int B, int T, cudaStream_t s);

@@ -112,6 +112,20 @@ def test_full_prefill_workload(name):
         L, wa, ra = wl.pattern_len, wl.pattern_write_at, wl.pattern_read_at
         for i in range(L):
             assert np.array_equal(idx[ra + i, 1], idx[wa + i, 0])
+        # the pages' write-read bucket overlap at full size: every slot read at the
+        # query was written at the needle (and the read sets equal the write sets)
+        cfg = tl.cfg_of(wl)
+        o = torch.empty(wl.B, 3, dtype=torch.int32, device="cuda")
+        ws = sdm.alloc_workspace(sdm.slot_overlap_workspace_bytes(cfg, wl.B))
+        sdm.sdm_slot_overlap(cfg, out["idx"], wl.B, wl.T, wa, wa + L, ra, ra + L, o, ws)
+        got = o.cpu().numpy()[0]
+        assert got[2] == got[1] == got[0] and got[0] >= wl.W
+        # a wider write window around the needle, against the oracle's set definition
+        w0, w1 = wa - 64, wa + L + 64
+        sdm.sdm_slot_overlap(cfg, out["idx"], wl.B, wl.T, w0, w1, ra, ra + L, o, ws)
+        want = oracle.slot_overlap(np.concatenate([idx[w0:w1], idx[ra:ra + L]]), 1,
+                                   w1 - w0 + L, wl.N, 0, w1 - w0, w1 - w0, w1 - w0 + L)
+        assert np.array_equal(o.cpu().numpy()[0], want[0])
 
 
 def test_full_decode_workload():

@@ -396,3 +396,42 @@ def test_init_bank_is_a_copy():
     assert banks.shape == (3, 30, 8)
     for b in range(3):
         assert np.array_equal(banks[b], M0)
+
+
+# ------------------------------------------------------------ slot-access statistics
+
+def test_slot_stats_hand_example():
+    """Three tokens, two slots each (blog, "Memory Access Patterns": cumulative writes,
+    current reads, write-read bucket overlap), worked by hand:
+    writes {1,2}, {2,4}, {6,7}; reads {2,3}, {1,5}, {7,1}."""
+    idx = np.array([[[1, 2], [2, 3]], [[2, 4], [1, 5]], [[6, 7], [7, 1]]])
+    w = oracle.slot_counts(idx, 1, 3, 8, 0, 0, 3)
+    assert w.tolist() == [[0, 1, 2, 0, 1, 0, 1, 1]]
+    r = oracle.slot_counts(idx, 1, 3, 8, 1, 1, 3)
+    assert r.tolist() == [[0, 2, 0, 0, 0, 1, 0, 1]]
+    # written in tokens 0-1: {1,2,4}; read in tokens 1-2: {1,5,7}; both: {1}
+    assert oracle.slot_overlap(idx, 1, 3, 8, 0, 2, 1, 3).tolist() == [[3, 3, 1]]
+    # an empty write window; all reads: {2,3} | {1,5} | {7,1} = {1,2,3,5,7}
+    assert oracle.slot_overlap(idx, 1, 3, 8, 1, 1, 0, 3).tolist() == [[0, 5, 0]]
+
+
+def test_slot_stats_invariants():
+    rng = np.random.default_rng(11)
+    B, T, W, N = 3, 40, 4, 64
+    idx = np.stack([np.stack([rng.choice(N, W, replace=False) for _ in range(2)])
+                    for _ in range(B * T)])
+    c = oracle.slot_counts(idx, B, T, N, 0, 5, 30)
+    assert np.all(c.sum(1) == 25 * W)          # distinct ids: one count per reference
+    o = oracle.slot_overlap(idx, B, T, N, 5, 30, 10, 40)
+    assert np.all(o[:, 2] <= np.minimum(o[:, 0], o[:, 1]))
+    # the distinct written slots are exactly the slots with a nonzero count
+    assert np.array_equal(o[:, 0], (c > 0).sum(1))
+    # a window against itself with the read sets equal to the write sets: full overlap
+    same = idx.copy()
+    same[:, 1] = same[:, 0]
+    o2 = oracle.slot_overlap(same, B, T, N, 0, T, 0, T)
+    assert np.array_equal(o2[:, 0], o2[:, 2]) and np.array_equal(o2[:, 1], o2[:, 2])
+    # out-of-range ids are not counted
+    bad = idx.copy()
+    bad[0, 0, 0] = N
+    assert oracle.slot_counts(bad, B, T, N, 0, 0, 1)[0].sum() == W - 1
