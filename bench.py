@@ -303,6 +303,39 @@ def gpu_arm(args, world, rank):
         "library_launches": {"cublas_gemm": 3 * args.steps},
     }
 
+    # ---- the dense-state comparator on the same tokens: the gated delta rule on a
+    # dense [d, 64] state per sequence, with this step's write / read weights, v and gates
+    y_g = torch.empty(ntok, d, dtype=torch.float32, device=dev)
+
+    def gdn():
+        sdm.sdm_gdn_dense_scan(cfg, wsel, wsel[:, 1], 2 * wl.W, v, alpha, beta, y_g, B, T)
+
+    for _ in range(3):
+        gdn()
+    torch.cuda.synchronize()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    n_g = max(3, args.steps // 5)
+    g0.record(stream)
+    for _ in range(n_g):
+        gdn()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    g_ms = g0.elapsed_time(g1) / n_g
+    res["dense_comparator"] = {
+        "what": "gated delta rule on a dense [d, 64] fp32 state per sequence (the state size "
+                "of SDM's 64 active slots), same tokens, weights, v and gates, iso-FLOP",
+        "ms": round(g_ms, 4), "tokens_per_s": round(ntok / (g_ms / 1e3), 1),
+        "vs_sdm_scan": round(g_ms / stage_ms["scan"], 4),
+        "state_bytes_per_sequence": d * 64 * 4,
+        "sdm_state_bytes_per_sequence": wl.N * d * 2,
+        # HBM bytes a token moves: v in, y out, both weight vectors, gates (the state
+        # stays on chip) against the SDM scan's 800,008
+        "hbm_bytes_per_token": d * 2 + d * 4 + 2 * 64 * 4 + 8,
+        "kernel": "gdn_dense_kernel: sequential in t per row, state in registers",
+        "gpu_launches_per_call": 1}
+    del y_g
+
     # ---- e2e: the one-call public API with host buffers
     x_h = tok_cpu["x"].pin_memory()
     a_h = tok_cpu["alpha"].pin_memory()

@@ -220,6 +220,22 @@ SDM_API int sdm_prefill_m0(const sdm_cfg* cfg, const sdm_weights* wts, const voi
                            float* y, int B, int T, int32_t* idx_out, float* w_out, void* ws,
                            size_t ws_bytes, int* dev_status, void* stream);
 
+/* Dense-state comparator (NOT the method: a measured reference point). The pages set
+ * SDM against gated-delta-net: SDM's W = 64 active slot vectors per token are exactly the
+ * size of GDN's whole dense state, at identical FLOPs per token ("Sparse Delta Memory"
+ * blog, "Background", "How does SDM work?"). This runs the same gated delta rule on a
+ * dense state of W columns that every token updates, per sequence:
+ *   u = S k;  S <- alpha S + beta (v - alpha u) k^T;  y = S r     (fp32 throughout)
+ * S0 / S_out [B, d, W] fp32 (row-major per row; S0 NULL = zeros, S_out NULL = not
+ * returned), kw / kr: write / read weights of token b*T+t at kw + (b*T+t)*k_stride
+ * (W fp32 each; e.g. the wsel of sdm_address with k_stride = 2W, kr = kw + W), v [B*T, d]
+ * in the I/O type, alpha / beta [B*T], y [B*T, d] fp32. cfg: d % 16 == 0, w == 64.
+ * The state never leaves the chip: its traffic is the per-token inputs and y. */
+SDM_API int sdm_gdn_dense_scan(const sdm_cfg* cfg, const float* S0, const float* kw,
+                               const float* kr, int64_t k_stride, const void* v,
+                               const float* alpha, const float* beta, float* S_out, float* y,
+                               int B, int T, void* stream);
+
 /* Slot-access statistics, the pages' diagnostic of how the memory is used ("Sparse
  * Delta Memory" blog, "Memory Access Patterns on a Needle-in-a-Haystack Task": which
  * slots are written and read at each token position, and whether the slots written at

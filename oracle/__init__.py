@@ -264,3 +264,29 @@ def slot_overlap(idx, B, T, N, w0, w1, r0, r1) -> np.ndarray:
         rd = {int(s) for s in idx[b, r0:r1, 1].ravel() if 0 <= s < N}
         out[b] = (len(wr), len(rd), len(wr & rd))
     return out
+
+
+# ------------------------------------------------------- dense-state comparator
+# The same gated delta rule on a dense state of W columns that every token updates
+# (Sparse Delta Memory blog, "Background": SDM's W active slot vectors are the size of a
+# gated-delta-net's whole dense state at identical FLOPs per token). Written out per
+# token in fp64 with numpy, no rounding of the state.
+
+def gdn_dense(S0, kw, kr, v, alpha, beta):
+    """S0 [d, W] initial state (None: zeros); kw, kr [T, W] write / read weights; v [T, d];
+    alpha, beta [T]. Per token: u = S k; S <- alpha S + beta (v - alpha u) k^T; y = S r.
+    Returns (y [T, d], final S [d, W]), fp64."""
+    kw = to_f64(kw)
+    kr = to_f64(kr)
+    v = to_f64(v)
+    al = to_f64(alpha).reshape(-1)
+    be = to_f64(beta).reshape(-1)
+    T, W = kw.shape
+    d = v.shape[1]
+    S = np.zeros((d, W)) if S0 is None else to_f64(S0).reshape(d, W).copy()
+    y = np.empty((T, d))
+    for t in range(T):
+        u = S @ kw[t]
+        S = al[t] * S + be[t] * np.outer(v[t] - al[t] * u, kw[t])
+        y[t] = S @ kr[t]
+    return y, S

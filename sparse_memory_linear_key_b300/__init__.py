@@ -95,6 +95,7 @@ def lib():
             "sdm_fill_untouched": ([CP, P, P, P, I, I, P], I),
             "sdm_prefill_m0_workspace_bytes": ([CP, I, I], S),
             "sdm_prefill_m0": ([CP, WP, P, P, P, P, P, P, I, I, P, P, P, S, P, P], I),
+            "sdm_gdn_dense_scan": ([CP, P, P, P, L64, P, P, P, P, P, I, I, P], I),
             "sdm_slot_counts": ([CP, P, I, I, I, I, I, P, P], I),
             "sdm_slot_overlap_workspace_bytes": ([CP, I], S),
             "sdm_slot_overlap": ([CP, P, I, I, I, I, I, I, P, P, S, P], I),
@@ -338,6 +339,23 @@ def sdm_prefill_m0(cfg: Cfg, params, M0, x, alpha, beta, banks, y, ws, dev_statu
                                 _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
                                 _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)),
            "sdm_prefill_m0")
+
+
+def sdm_gdn_dense_scan(cfg: Cfg, kw, kr, k_stride: int, v, alpha, beta, y, B: int, T: int,
+                       S0=None, S_out=None, stream=None) -> None:
+    """The dense-state comparator: the gated delta rule on a dense [d, 64] fp32 state
+    per sequence (kw, kr: fp32 views whose token rows are k_stride floats apart)."""
+    for name, t in (("kw", kw), ("kr", kr)):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.float32):
+            raise ValueError("%s must be a float32 CUDA tensor (a strided view is fine)" % name)
+    _check(lib().sdm_gdn_dense_scan(ctypes.byref(cfg), _ptr(S0, torch.float32, "S0"),
+                                    ctypes.c_void_p(kw.data_ptr()), ctypes.c_void_p(kr.data_ptr()),
+                                    k_stride, _ptr(v, cfg.torch_dtype, "v"),
+                                    _ptr(alpha, torch.float32, "alpha"),
+                                    _ptr(beta, torch.float32, "beta"),
+                                    _ptr(S_out, torch.float32, "S_out"),
+                                    _ptr(y, torch.float32, "y"), B, T, _stream(stream)),
+           "sdm_gdn_dense_scan")
 
 
 def sdm_slot_counts(cfg: Cfg, idx, B: int, T: int, kind: int, t0: int, t1: int, counts,

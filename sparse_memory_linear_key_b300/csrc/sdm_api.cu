@@ -459,6 +459,31 @@ int sdm_prefill_m0(const sdm_cfg* cfg, const sdm_weights* w, const void* M0, con
                         dev_status, stream);
 }
 
+// ------------------------------------------------------ dense-state comparator
+
+int sdm_gdn_dense_scan(const sdm_cfg* cfg, const float* S0, const float* kw, const float* kr,
+                       int64_t k_stride, const void* v, const float* alpha, const float* beta,
+                       float* S_out, float* y, int B, int T, void* stream)
+{
+    if (cfg == nullptr)
+        return SDM_EINVAL;
+    const sdm_cfg& c = *cfg;
+    if (c.d <= 0 || (c.dtype != SDM_F32 && c.dtype != SDM_BF16) || B < 0 || T < 0)
+        return SDM_EINVAL;
+    if (c.w != 64 || c.d % kRowAlign != 0)
+        return SDM_EUNSUPPORTED;
+    if (B == 0)
+        return SDM_OK;
+    if (T > 0 && (kw == nullptr || kr == nullptr || v == nullptr || alpha == nullptr ||
+                  beta == nullptr || y == nullptr))
+        return SDM_EINVAL;
+    if (k_stride < c.w || k_stride % 4 != 0 || !aligned16(kw) || !aligned16(kr) || !aligned16(S0) ||
+        !aligned16(S_out) || ((uintptr_t)v & (esize(c) - 1)) != 0 || ((uintptr_t)y & 3u) != 0)
+        return SDM_EINVAL;
+    return cuda_status(launch_gdn_dense(c.dtype == SDM_BF16, S0, kw, kr, k_stride, v, alpha, beta,
+                                        S_out, y, B, T, c.d, (cudaStream_t)stream));
+}
+
 // ------------------------------------------------------ slot-access statistics
 
 static bool window_ok(int lo, int hi, int T) { return 0 <= lo && lo <= hi && hi <= T; }

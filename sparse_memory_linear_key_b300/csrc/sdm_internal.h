@@ -75,6 +75,11 @@ cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel,
 // value >= T if none (bank_init.cu)
 cudaError_t launch_first_touch(const sdm_cfg& c, const int32_t* idx, int B, int T,
                                int32_t* first_write, cudaStream_t s);
+// dense-state comparator (gdn_dense.cu): W = 64 columns, d % 16 == 0
+cudaError_t launch_gdn_dense(bool bf_io, const float* S0, const float* kw, const float* kr,
+                             int64_t ks, const void* v, const float* alpha, const float* beta,
+                             float* S_out, float* y, int B, int T, int d, cudaStream_t s);
+
 // slot-access statistics (slot_stats.cu)
 size_t slot_overlap_ws_bytes(const sdm_cfg& c, int B);
 cudaError_t launch_slot_counts(const sdm_cfg& c, const int32_t* idx, int B, int T, int kind,

@@ -435,3 +435,41 @@ def test_slot_stats_invariants():
     bad = idx.copy()
     bad[0, 0, 0] = N
     assert oracle.slot_counts(bad, B, T, N, 0, 0, 1)[0].sum() == W - 1
+
+
+# ------------------------------------------------------- dense-state comparator
+
+def test_gdn_dense_is_the_scan_on_a_fixed_slot_set():
+    """The dense comparator is the SDM recurrence with every token selecting the same
+    W slots of a W-slot bank: the numpy dense form against the C scan (fp64 storage, so
+    no rounding on either side)."""
+    rng = np.random.default_rng(21)
+    T, W, d = 40, 8, 12
+    S0 = rng.normal(size=(d, W))
+    kw = rng.dirichlet(np.ones(W), size=T)
+    kr = rng.dirichlet(np.ones(W), size=T)
+    v = rng.normal(size=(T, d))
+    al = rng.uniform(0.5, 1.0, T)
+    be = rng.uniform(0.0, 1.0, T)
+    y, S = oracle.gdn_dense(S0, kw, kr, v, al, be)
+    M = np.ascontiguousarray(S0.T)                       # [N = W slots, d rows]
+    sets = np.tile(np.arange(W, dtype=np.int32), (T, 1))
+    y2 = oracle.scan(M, v, al, be, sets, kw, sets, kr)
+    np.testing.assert_allclose(y, y2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(S, M.T, rtol=0, atol=1e-12)
+
+
+def test_gdn_dense_closed_forms():
+    d, W = 5, 4
+    rng = np.random.default_rng(22)
+    S0 = rng.normal(size=(d, W))
+    e = np.eye(W)
+    # beta = 0: pure decay, y = alpha S0 r
+    y, S = oracle.gdn_dense(S0, e[[1]], e[[2]], rng.normal(size=(1, d)), [0.5], [0.0])
+    np.testing.assert_allclose(S, 0.5 * S0, atol=1e-15)
+    np.testing.assert_allclose(y[0], 0.5 * S0[:, 2], atol=1e-15)
+    # beta = 1, one-hot k, r = k: the write is read back exactly (idempotence)
+    v = rng.normal(size=(1, d))
+    y, S = oracle.gdn_dense(S0, e[[3]], e[[3]], v, [0.7], [1.0])
+    np.testing.assert_allclose(y[0], v[0], atol=1e-14)
+    np.testing.assert_allclose(S[:, :3], 0.7 * S0[:, :3], atol=1e-15)
