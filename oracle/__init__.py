@@ -290,3 +290,56 @@ def gdn_dense(S0, kw, kr, v, alpha, beta):
         S = al[t] * S + be[t] * np.outer(v[t] - al[t] * u, kw[t])
         y[t] = S @ kr[t]
     return y, S
+
+
+# ------------------------------------------------------------- backward (a5 + a6)
+# Gradients of the recurrence by automatic differentiation of the per-token definition,
+# written with plain PyTorch CPU ops in fp64. The state is stored once per token in the
+# storage type (bf16 RNE or fp32) as the forward does; the rounding passes the gradient
+# through unchanged (its derivative is taken as 1), which is what a backward pass that
+# reuses the stored forward values computes.
+
+def scan_backward(M_init, v, alpha, beta, S, k, Rd, r, dy, dM_final=None, type_=F32):
+    """One sequence, a subset of rows. M_init [N, R] fp64 values, v [T, R], alpha/beta [T],
+    S/Rd [T, W] slot ids, k/r [T, W] weights, dy [T, R]; dM_final [N, R] or None.
+    Returns dict of fp64 numpy arrays: dM_init [N, R], dv [T, R], dalpha [T], dbeta [T],
+    dk [T, W], dr [T, W]."""
+    import torch
+    f = torch.float64
+
+    def store(x):
+        if type_ == F64:
+            return x
+        if type_ == F32:
+            q = x.detach().to(torch.float32).to(f)
+        else:
+            q = x.detach().to(torch.float32).to(torch.bfloat16).to(f)
+        return x + (q - x).detach()
+
+    M0 = torch.tensor(np.asarray(M_init, np.float64), dtype=f, requires_grad=True)
+    vv = torch.tensor(to_f64(v), dtype=f, requires_grad=True)
+    al = torch.tensor(to_f64(alpha).reshape(-1), dtype=f, requires_grad=True)
+    be = torch.tensor(to_f64(beta).reshape(-1), dtype=f, requires_grad=True)
+    kk = torch.tensor(to_f64(k), dtype=f, requires_grad=True)
+    rr = torch.tensor(to_f64(r), dtype=f, requires_grad=True)
+    S = np.asarray(S)
+    Rd = np.asarray(Rd)
+    T = S.shape[0]
+    M = M0.clone()
+    ys = []
+    for t in range(T):
+        s_idx = torch.as_tensor(S[t], dtype=torch.long)
+        r_idx = torch.as_tensor(Rd[t], dtype=torch.long)
+        old = M[s_idx]                                   # [W, R]
+        u = kk[t] @ old                                  # [R]
+        new = al[t] * old + be[t] * kk[t][:, None] * (vv[t] - al[t] * u)[None, :]
+        M = M.index_copy(0, s_idx, store(new))
+        ys.append(rr[t] @ M[r_idx])
+    y = torch.stack(ys)
+    loss = (y * torch.tensor(to_f64(dy), dtype=f)).sum()
+    if dM_final is not None:
+        loss = loss + (M * torch.tensor(np.asarray(dM_final, np.float64), dtype=f)).sum()
+    loss.backward()
+    return {"dM_init": M0.grad.numpy(), "dv": vv.grad.numpy(), "dalpha": al.grad.numpy(),
+            "dbeta": be.grad.numpy(), "dk": kk.grad.numpy(), "dr": rr.grad.numpy(),
+            "y": y.detach().numpy(), "M_final": M.detach().numpy()}

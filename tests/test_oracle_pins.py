@@ -473,3 +473,71 @@ def test_gdn_dense_closed_forms():
     y, S = oracle.gdn_dense(S0, e[[3]], e[[3]], v, [0.7], [1.0])
     np.testing.assert_allclose(y[0], v[0], atol=1e-14)
     np.testing.assert_allclose(S[:, :3], 0.7 * S0[:, :3], atol=1e-15)
+
+
+# ------------------------------------------------------------- backward (a5 + a6)
+
+def _bwd_case(seed, T=6, N=10, W=3, R=4):
+    rng = np.random.default_rng(seed)
+    M0 = rng.normal(size=(N, R))
+    v = rng.normal(size=(T, R))
+    al = rng.uniform(0.5, 1.0, T)
+    be = rng.uniform(0.1, 0.9, T)
+    S = np.stack([np.sort(rng.choice(N, W, replace=False)) for _ in range(T)])
+    Rd = np.stack([np.sort(rng.choice(N, W, replace=False)) for _ in range(T)])
+    S[2] = Rd[2]                      # a token that reads exactly what it writes
+    k = rng.dirichlet(np.ones(W), size=T)
+    r = rng.dirichlet(np.ones(W), size=T)
+    dy = rng.normal(size=(T, R))
+    dMf = rng.normal(size=(N, R))
+    return M0, v, al, be, S, k, Rd, r, dy, dMf
+
+
+def test_scan_backward_forward_values_are_the_scan():
+    M0, v, al, be, S, k, Rd, r, dy, dMf = _bwd_case(31)
+    g = oracle.scan_backward(M0, v, al, be, S, k, Rd, r, dy, dMf, type_=oracle.F64)
+    M = np.ascontiguousarray(M0.copy())
+    y = oracle.scan(M, v, al, be, S, k, Rd, r)
+    np.testing.assert_allclose(g["y"], y, atol=1e-12)
+    np.testing.assert_allclose(g["M_final"], M, atol=1e-12)
+
+
+def test_scan_backward_matches_finite_differences():
+    """Central differences of L = <y, dy> + <M_final, dM> through the C scan (fp64
+    storage), against the autograd gradients, for every input family."""
+    M0, v, al, be, S, k, Rd, r, dy, dMf = _bwd_case(32)
+    g = oracle.scan_backward(M0, v, al, be, S, k, Rd, r, dy, dMf, type_=oracle.F64)
+
+    def loss(M0_, v_, al_, be_, k_, r_):
+        M = np.ascontiguousarray(M0_.copy())
+        y = oracle.scan(M, v_, al_, be_, S, k_, Rd, r_)
+        return float((y * dy).sum() + (M * dMf).sum())
+
+    base = [M0, v, al, be, k, r]
+    names = ["dM_init", "dv", "dalpha", "dbeta", "dk", "dr"]
+    h = 1e-6
+    for a_i, name in enumerate(names):
+        arr = base[a_i]
+        flat = arr.reshape(-1)
+        for e in range(0, flat.size, max(1, flat.size // 7)):
+            plus = [b.copy() for b in base]
+            minus = [b.copy() for b in base]
+            plus[a_i].reshape(-1)[e] += h
+            minus[a_i].reshape(-1)[e] -= h
+            fd = (loss(*plus) - loss(*minus)) / (2 * h)
+            assert abs(fd - g[name].reshape(-1)[e]) <= 1e-6 * max(1.0, abs(fd)), (name, e)
+
+
+def test_scan_backward_closed_form_single_token():
+    """One token, W = 1, R = S: y = alpha m + beta k (v - alpha k m) k-weighted read.
+    With k = r = 1 (W = 1): y = alpha m + beta (v - alpha m) = alpha (1 - beta) m + beta v,
+    so dy/dv = beta, dy/dm = alpha (1 - beta), dy/dalpha = (1 - beta) m,
+    dy/dbeta = v - alpha m."""
+    m, vv, a, b = 0.7, -1.3, 0.8, 0.25
+    g = oracle.scan_backward(np.array([[m]]), np.array([[vv]]), [a], [b], np.array([[0]]),
+                             np.array([[1.0]]), np.array([[0]]), np.array([[1.0]]),
+                             np.array([[1.0]]), None, type_=oracle.F64)
+    assert abs(g["dv"][0, 0] - b) < 1e-14
+    assert abs(g["dM_init"][0, 0] - a * (1 - b)) < 1e-14
+    assert abs(g["dalpha"][0] - (1 - b) * m) < 1e-14
+    assert abs(g["dbeta"][0] - (vv - a * m)) < 1e-14
