@@ -220,6 +220,34 @@ SDM_API int sdm_prefill_m0(const sdm_cfg* cfg, const sdm_weights* wts, const voi
                            float* y, int B, int T, int32_t* idx_out, float* w_out, void* ws,
                            size_t ws_bytes, int* dev_status, void* stream);
 
+/* Backward of the recurrence (the write and the read; the method is trained end to
+ * end, "Sparse Delta Memory: Scaling the State of Linear RNNs through Sparsity",
+ * Abstract). Two calls:
+ * sdm_scan_run_train: sdm_scan_run (or sdm_scan_run_m0 when M0 / first_write are given,
+ *   both or neither) that also records, per token, the pre-write values of its write
+ *   slots: tape [B*T, w, d] in the state type, sdm_tape_bytes(cfg, B, T) bytes.
+ * sdm_scan_backward: given dy [B*T, d] fp32 (the gradient of the loss with respect to y)
+ *   and dbank [B, N, d] fp32 (in: with respect to the banks after the tokens, zeros if
+ *   they do not enter the loss; out: with respect to the banks before the tokens --
+ *   with banks from M0, dL/dM0 = sum over b of dbank[b]), it writes
+ *   dv [B*T, d], dalpha, dbeta [B*T] and dwsel [B*T, 2, w] (write then read weights),
+ *   all fp32. banks (in: the state after the tokens, as the forward left it; out: the
+ *   state before them) are walked back with the tape. idx, wsel, v, alpha, beta as in
+ *   the forward. ws: sdm_scan_backward_workspace_bytes(cfg, B, T) (per-block partial
+ *   sums). The stored state's rounding is differentiated as the identity. */
+SDM_API size_t sdm_tape_bytes(const sdm_cfg* cfg, int B, int T);
+SDM_API int sdm_scan_run_train(const sdm_cfg* cfg, const int32_t* idx, const float* wsel,
+                               const void* v, const float* alpha, const float* beta,
+                               const void* M0, const int32_t* first_write, void* banks, float* y,
+                               int B, int T, const void* ws, size_t ws_bytes, void* tape,
+                               int* dev_status, void* stream);
+SDM_API size_t sdm_scan_backward_workspace_bytes(const sdm_cfg* cfg, int B, int T);
+SDM_API int sdm_scan_backward(const sdm_cfg* cfg, const int32_t* idx, const float* wsel,
+                              const void* v, const float* alpha, const float* beta,
+                              const void* tape, void* banks, const float* dy, float* dbank,
+                              float* dv, float* dalpha, float* dbeta, float* dwsel, int B, int T,
+                              void* ws, size_t ws_bytes, void* stream);
+
 /* Dense-state comparator (NOT the method: a measured reference point). The pages set
  * SDM against gated-delta-net: SDM's W = 64 active slot vectors per token are exactly the
  * size of GDN's whole dense state, at identical FLOPs per token ("Sparse Delta Memory"

@@ -96,6 +96,10 @@ def lib():
             "sdm_prefill_m0_workspace_bytes": ([CP, I, I], S),
             "sdm_prefill_m0": ([CP, WP, P, P, P, P, P, P, I, I, P, P, P, S, P, P], I),
             "sdm_gdn_dense_scan": ([CP, P, P, P, L64, P, P, P, P, P, I, I, P], I),
+            "sdm_tape_bytes": ([CP, I, I], S),
+            "sdm_scan_run_train": ([CP, P, P, P, P, P, P, P, P, P, I, I, P, S, P, P, P], I),
+            "sdm_scan_backward_workspace_bytes": ([CP, I, I], S),
+            "sdm_scan_backward": ([CP, P, P, P, P, P, P, P, P, P, P, P, P, P, I, I, P, S, P], I),
             "sdm_slot_counts": ([CP, P, I, I, I, I, I, P, P], I),
             "sdm_slot_overlap_workspace_bytes": ([CP, I], S),
             "sdm_slot_overlap": ([CP, P, I, I, I, I, I, I, P, P, S, P], I),
@@ -339,6 +343,48 @@ def sdm_prefill_m0(cfg: Cfg, params, M0, x, alpha, beta, banks, y, ws, dev_statu
                                 _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
                                 _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)),
            "sdm_prefill_m0")
+
+
+def tape_bytes(cfg: Cfg, B: int, T: int) -> int:
+    return int(lib().sdm_tape_bytes(ctypes.byref(cfg), B, T))
+
+
+def scan_backward_workspace_bytes(cfg: Cfg, B: int, T: int) -> int:
+    return int(lib().sdm_scan_backward_workspace_bytes(ctypes.byref(cfg), B, T))
+
+
+def sdm_scan_run_train(cfg: Cfg, idx, wsel, v, alpha, beta, banks, y, B: int, T: int, ws, tape,
+                       dev_status, M0=None, first_write=None, stream=None) -> None:
+    """sdm_scan_run (from M0 when M0 and first_write are given) that also records the
+    pre-write values of each token's write slots into tape [B*T, w, d]."""
+    dt = cfg.torch_dtype
+    _check(lib().sdm_scan_run_train(ctypes.byref(cfg), _ptr(idx, torch.int32, "idx"),
+                                    _ptr(wsel, torch.float32, "wsel"), _ptr(v, dt, "v"),
+                                    _ptr(alpha, torch.float32, "alpha"),
+                                    _ptr(beta, torch.float32, "beta"), _ptr(M0, dt, "M0"),
+                                    _ptr(first_write, torch.int32, "first_write"),
+                                    _ptr(banks, dt, "banks"), _ptr(y, torch.float32, "y"), B, T,
+                                    _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+                                    _ptr(tape, dt, "tape"),
+                                    _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)),
+           "sdm_scan_run_train")
+
+
+def sdm_scan_backward(cfg: Cfg, idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, dalpha,
+                      dbeta, dwsel, B: int, T: int, ws, stream=None) -> None:
+    """Gradients of the recurrence; banks walk back from the final to the initial state and
+    dbank from the final to the initial bank's gradient (see include/sdm.h)."""
+    dt = cfg.torch_dtype
+    f = torch.float32
+    _check(lib().sdm_scan_backward(ctypes.byref(cfg), _ptr(idx, torch.int32, "idx"),
+                                   _ptr(wsel, f, "wsel"), _ptr(v, dt, "v"),
+                                   _ptr(alpha, f, "alpha"), _ptr(beta, f, "beta"),
+                                   _ptr(tape, dt, "tape"), _ptr(banks, dt, "banks"),
+                                   _ptr(dy, f, "dy"), _ptr(dbank, f, "dbank"), _ptr(dv, f, "dv"),
+                                   _ptr(dalpha, f, "dalpha"), _ptr(dbeta, f, "dbeta"),
+                                   _ptr(dwsel, f, "dwsel"), B, T, _ptr(ws, None, "ws"),
+                                   ws.numel() * ws.element_size(), _stream(stream)),
+           "sdm_scan_backward")
 
 
 def sdm_gdn_dense_scan(cfg: Cfg, kw, kr, k_stride: int, v, alpha, beta, y, B: int, T: int,

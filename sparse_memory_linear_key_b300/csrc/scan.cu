@@ -92,6 +92,8 @@ struct ScanArgs {
                                     // first write of a slot in a sequence, and every
                                     // read before it, loads the slot from M0
     const int* first_write;         // [B][N] first token writing each slot (>= T: none)
+    unsigned char* tape;            // non-null: [B*T][W][d] pre-write values of the write
+                                    // slots, for the backward pass
     long long items;                // B * T * nrb
     int B, T, d, N, nrb, rb_rows, win, ring_entries, chunk_bytes;
 };
@@ -757,6 +759,14 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
                                                           rg * 16)
                         : make_uint4(0, 0, 0, 0);
         consumer_arrive();   // this warp has taken its write chunks
+        if (a.tape != nullptr && act) {
+            // the pre-write values of this token's write slots, for the backward pass
+            unsigned char* tp = a.tape + ((size_t)m.tok * W * a.d + (size_t)m.rb * a.rb_rows) * sizeof(S) +
+                                rg * 16;
+#pragma unroll
+            for (int i = 0; i < SPL; ++i)
+                __stcs(reinterpret_cast<uint4*>(tp + (size_t)(i * kSG + sg) * a.d * sizeof(S)), Mv[i]);
+        }
 
         // u = M_S k (pre-write), reduced over the slot groups; fp32 pairs throughout
         float2 u[HPL];
@@ -1014,7 +1024,7 @@ ScanWs scan_ws_layout(const sdm_cfg& c, int B, int T)
 cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel, const void* v,
                         const float* alpha, const float* beta, void* banks, float* y, int B,
                         int T, void* ws, size_t ws_bytes, int* status, cudaStream_t s,
-                        const void* m0, const int32_t* first_write)
+                        const void* m0, const int32_t* first_write, void* tape)
 {
     if (B <= 0 || T <= 0)
         return cudaSuccess;
@@ -1040,6 +1050,7 @@ cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel,
     a.ring = ws_bytes >= L.total ? (unsigned char*)(base + L.ring) : nullptr;
     a.m0 = (const unsigned char*)m0;
     a.first_write = first_write;
+    a.tape = (unsigned char*)tape;
     a.B = B;
     a.T = T;
     a.d = c.d;

@@ -1,0 +1,242 @@
+// scan_bwd.cu -- backward of the recurrence: the gradients of the gated-delta write and
+// the weighted read ("Sparse Delta Memory" blog, "Write & Read"; the method is trained
+// end to end, paper Abstract) with respect to v, alpha, beta, the write and read
+// weights and the bank before the tokens.
+//
+// Forward, per token t: old_j = M[S_j], u = sum_j k_j old_j,
+//   M[S_j] <- alpha old_j + beta k_j (v - alpha u),   y = sum_j r_j M[R_j].
+// Backward, for t = T-1 .. 0, with G the gradient of the loss with respect to the bank
+// state after token t (G starts as the gradient with respect to the final bank):
+//   read:   dr_j = <M[R_j], dy>,  G[R_j] += r_j dy              (M: the post-write state)
+//   write:  g = sum_j k_j G[S_j],  c = v - alpha u,
+//           dv = beta g,  dbeta = <g, c>,  dalpha = sum_j <G[S_j], old_j - beta k_j u>,
+//           dk_j = beta <G[S_j], c> - alpha beta <g, old_j>,
+//           G[S_j] <- alpha (G[S_j] - beta k_j g),  M[S_j] <- old_j   (from the tape)
+// At the end G is the gradient with respect to the bank before the first token, and M
+// is that bank again. The stored state is rounded on each write in the forward; the
+// backward takes the rounding's derivative as 1 and uses the stored values.
+//
+// Rows are independent, so a block owns 64 rows of one sequence and walks its tokens in
+// reverse; 4 groups of 64 threads share the W slots of a token (slot j in group j % 4).
+// Sums over rows (dk, dr, dalpha, dbeta) are per-block partials, summed over the blocks
+// of a sequence by a second kernel.
+#include "sdm_common.cuh"
+#include "sdm_internal.h"
+
+namespace sdm {
+
+namespace {
+
+constexpr int kBRows = 64;
+constexpr int kBThreads = 256;
+constexpr int kBGroups = kBThreads / kBRows;
+
+__device__ __forceinline__ float ld_state(const bf16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ float ld_state(const float* p) { return *p; }
+__device__ __forceinline__ float ld_io(const bf16* p) { return __bfloat162float(__ldg(p)); }
+__device__ __forceinline__ float ld_io(const float* p) { return __ldg(p); }
+
+__device__ __forceinline__ float warp_sum(float x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+    return x;
+}
+
+// partials: [nblk][B*T][2W + 2] = dk[W], dr[W], dalpha, dbeta of this block's rows
+template <typename S, int W>
+__global__ void __launch_bounds__(kBThreads) scan_bwd_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ wsel, const S* __restrict__ v,
+    const float* __restrict__ alpha, const float* __restrict__ beta, const S* __restrict__ tape,
+    S* __restrict__ banks, const float* __restrict__ dy, float* __restrict__ dbank,
+    float* __restrict__ dv, float* __restrict__ part, int B, int T, int d, int N)
+{
+    constexpr int SPG = W / kBGroups;         // slots a thread: j = grp + 4 i
+    constexpr int P = 2 * W + 2;
+    __shared__ int sid[2][W];
+    __shared__ float sw[2][W];
+    __shared__ float gate[2];
+    __shared__ float red[2][kBGroups][kBRows];
+    __shared__ float acc[P];
+    const int b = blockIdx.y;
+    const int r = threadIdx.x % kBRows, grp = threadIdx.x / kBRows;
+    const int row = blockIdx.x * kBRows + r;
+    const bool act = row < d;
+    const int lane = threadIdx.x & 31;
+    S* bank = banks + (size_t)b * N * d;
+    float* G = dbank + (size_t)b * N * d;
+    for (int t = T - 1; t >= 0; --t) {
+        const int64_t tok = (int64_t)b * T + t;
+        for (int e = threadIdx.x; e < 2 * W; e += kBThreads) {
+            sid[e / W][e % W] = __ldg(idx + tok * 2 * W + e);
+            sw[e / W][e % W] = __ldg(wsel + tok * 2 * W + e);
+        }
+        for (int e = threadIdx.x; e < P; e += kBThreads)
+            acc[e] = 0.f;
+        if (threadIdx.x == 0) {
+            gate[0] = __ldg(alpha + tok);
+            gate[1] = __ldg(beta + tok);
+        }
+        __syncthreads();
+        const float dyr = act ? __ldg(dy + tok * d + row) : 0.f;
+        // ---- read: G[R_j] += r_j dy, dr_j = <M[R_j], dy> (M after this token's write)
+#pragma unroll
+        for (int i = 0; i < SPG; ++i) {
+            const int j = grp + kBGroups * i;
+            const int s = sid[1][j];
+            float pr = 0.f;
+            if (act && s >= 0 && s < N) {
+                pr = ld_state(bank + (size_t)s * d + row) * dyr;
+                G[(size_t)s * d + row] += sw[1][j] * dyr;
+            }
+            pr = warp_sum(pr);
+            if (lane == 0)
+                atomicAdd(&acc[W + j], pr);
+        }
+        __syncthreads();   // a slot both read and written: its G update is visible below
+        // ---- write
+        float old[SPG], gj[SPG];
+        float gp = 0.f, up = 0.f;
+#pragma unroll
+        for (int i = 0; i < SPG; ++i) {
+            const int j = grp + kBGroups * i;
+            const int s = sid[0][j];
+            old[i] = 0.f;
+            gj[i] = 0.f;
+            if (act && s >= 0 && s < N) {
+                old[i] = ld_state(tape + ((size_t)tok * W + j) * d + row);
+                gj[i] = G[(size_t)s * d + row];
+            }
+            gp = fmaf(sw[0][j], gj[i], gp);
+            up = fmaf(sw[0][j], old[i], up);
+        }
+        red[0][grp][r] = gp;
+        red[1][grp][r] = up;
+        __syncthreads();
+        float g = 0.f, u = 0.f;
+#pragma unroll
+        for (int q = 0; q < kBGroups; ++q) {
+            g += red[0][q][r];
+            u += red[1][q][r];
+        }
+        const float al = gate[0], be = gate[1];
+        const float vr = act ? ld_io(v + tok * d + row) : 0.f;
+        const float c = vr - al * u;
+        float pa = 0.f;
+#pragma unroll
+        for (int i = 0; i < SPG; ++i) {
+            const int j = grp + kBGroups * i;
+            const int s = sid[0][j];
+            const float kj = sw[0][j];
+            pa = fmaf(gj[i], old[i] - be * kj * u, pa);
+            float pk = be * gj[i] * c - al * be * g * old[i];
+            pk = warp_sum(pk);
+            if (lane == 0)
+                atomicAdd(&acc[j], pk);
+            if (act && s >= 0 && s < N) {
+                G[(size_t)s * d + row] = al * (gj[i] - be * kj * g);
+                bank[(size_t)s * d + row] = tape[((size_t)tok * W + j) * d + row];
+            }
+        }
+        pa = warp_sum(pa);
+        float pb = warp_sum(grp == 0 ? g * c : 0.f);
+        if (lane == 0) {
+            atomicAdd(&acc[2 * W], pa);
+            atomicAdd(&acc[2 * W + 1], pb);
+        }
+        if (grp == 0 && act)
+            dv[tok * d + row] = be * g;
+        __syncthreads();
+        for (int e = threadIdx.x; e < P; e += kBThreads)
+            part[((size_t)blockIdx.x * B * T + tok) * P + e] = acc[e];
+        __syncthreads();   // acc, sid, sw and gate are reset for the next token
+    }
+}
+
+// sums of the per-block partials: dwsel [B*T][2][W] (write weights, then read weights),
+// dalpha, dbeta [B*T]
+__global__ void __launch_bounds__(256) scan_bwd_reduce(const float* __restrict__ part, int nblk,
+                                                      int64_t ntok, int W, float* __restrict__ dwsel,
+                                                      float* __restrict__ dalpha,
+                                                      float* __restrict__ dbeta)
+{
+    const int P = 2 * W + 2;
+    const int64_t total = ntok * P;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        float sum = 0.f;
+        for (int k = 0; k < nblk; ++k)
+            sum += part[(size_t)k * total + e];
+        const int64_t tok = e / P;
+        const int q = (int)(e % P);
+        if (q < 2 * W)
+            dwsel[tok * 2 * W + q] = sum;
+        else if (q == 2 * W)
+            dalpha[tok] = sum;
+        else
+            dbeta[tok] = sum;
+    }
+}
+
+template <typename S, int W>
+cudaError_t launch_bwd_t(const int32_t* idx, const float* wsel, const void* v, const float* alpha,
+                         const float* beta, const void* tape, void* banks, const float* dy,
+                         float* dbank, float* dv, float* part, int B, int T, int d, int N,
+                         cudaStream_t s)
+{
+    const dim3 grid((unsigned)((d + kBRows - 1) / kBRows), (unsigned)B);
+    scan_bwd_kernel<S, W><<<grid, kBThreads, 0, s>>>(idx, wsel, (const S*)v, alpha, beta,
+                                                     (const S*)tape, (S*)banks, dy, dbank, dv,
+                                                     part, B, T, d, N);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t scan_backward_ws_bytes(const sdm_cfg& c, int B, int T)
+{
+    const size_t nblk = (size_t)(c.d + kBRows - 1) / kBRows;
+    return nblk * (size_t)B * T * (2 * c.w + 2) * sizeof(float);
+}
+
+cudaError_t launch_scan_backward(const sdm_cfg& c, const int32_t* idx, const float* wsel,
+                                 const void* v, const float* alpha, const float* beta,
+                                 const void* tape, void* banks, const float* dy, float* dbank,
+                                 float* dv, float* dalpha, float* dbeta, float* dwsel, int B,
+                                 int T, void* ws, cudaStream_t s)
+{
+    if (B <= 0 || T <= 0)
+        return cudaSuccess;
+    const int N = c.n_sub * c.n_sub;
+    float* part = (float*)ws;
+    const bool bf = c.dtype == SDM_BF16;
+    cudaError_t e;
+    switch (c.w) {
+    case 8: e = bf ? launch_bwd_t<bf16, 8>(idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, part, B, T, c.d, N, s)
+                   : launch_bwd_t<float, 8>(idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, part, B, T, c.d, N, s);
+        break;
+    case 16: e = bf ? launch_bwd_t<bf16, 16>(idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, part, B, T, c.d, N, s)
+                    : launch_bwd_t<float, 16>(idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, part, B, T, c.d, N, s);
+        break;
+    case 32: e = bf ? launch_bwd_t<bf16, 32>(idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, part, B, T, c.d, N, s)
+                    : launch_bwd_t<float, 32>(idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, part, B, T, c.d, N, s);
+        break;
+    case 64: e = bf ? launch_bwd_t<bf16, 64>(idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, part, B, T, c.d, N, s)
+                    : launch_bwd_t<float, 64>(idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, part, B, T, c.d, N, s);
+        break;
+    default: return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess)
+        return e;
+    const int nblk = (c.d + kBRows - 1) / kBRows;
+    const int64_t work = (int64_t)B * T * (2 * c.w + 2);
+    int64_t blocks = (work + 255) / 256;
+    if (blocks > (int64_t)num_sms_current_device() * 8)
+        blocks = (int64_t)num_sms_current_device() * 8;
+    scan_bwd_reduce<<<(unsigned)blocks, 256, 0, s>>>(part, nblk, (int64_t)B * T, c.w, dwsel, dalpha,
+                                                     dbeta);
+    return cudaGetLastError();
+}
+
+}  // namespace sdm

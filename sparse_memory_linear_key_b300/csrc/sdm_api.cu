@@ -459,6 +459,64 @@ int sdm_prefill_m0(const sdm_cfg* cfg, const sdm_weights* w, const void* M0, con
                         dev_status, stream);
 }
 
+// ------------------------------------------------------------ backward (a5 + a6)
+
+size_t sdm_tape_bytes(const sdm_cfg* cfg, int B, int T)
+{
+    if (check_scan_cfg(cfg) != SDM_OK || B < 0 || T < 0)
+        return 0;
+    return (size_t)B * T * cfg->w * cfg->d * esize(*cfg);
+}
+
+int sdm_scan_run_train(const sdm_cfg* cfg, const int32_t* idx, const float* wsel, const void* v,
+                       const float* alpha, const float* beta, const void* M0,
+                       const int32_t* first_write, void* banks, float* y, int B, int T,
+                       const void* ws, size_t ws_bytes, void* tape, int* dev_status, void* stream)
+{
+    const int rc = check_scan_args(cfg, idx, wsel, v, alpha, beta, banks, y, B, T, ws, ws_bytes,
+                                   dev_status);
+    if (rc != SDM_OK || B == 0 || T == 0)
+        return rc;
+    const size_t bank = (size_t)cfg->n_sub * cfg->n_sub * cfg->d * esize(*cfg);
+    if (tape == nullptr || !aligned16(tape) || (M0 != nullptr) != (first_write != nullptr) ||
+        (M0 != nullptr && (!aligned16(M0) || overlaps(M0, bank, banks, bank * B))))
+        return SDM_EINVAL;
+    return cuda_status(launch_scan(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T,
+                                   const_cast<void*>(ws), ws_bytes, dev_status,
+                                   (cudaStream_t)stream, M0, first_write, tape));
+}
+
+size_t sdm_scan_backward_workspace_bytes(const sdm_cfg* cfg, int B, int T)
+{
+    if (check_scan_cfg(cfg) != SDM_OK || B < 0 || T < 0)
+        return 0;
+    return scan_backward_ws_bytes(*cfg, B, T);
+}
+
+int sdm_scan_backward(const sdm_cfg* cfg, const int32_t* idx, const float* wsel, const void* v,
+                      const float* alpha, const float* beta, const void* tape, void* banks,
+                      const float* dy, float* dbank, float* dv, float* dalpha, float* dbeta,
+                      float* dwsel, int B, int T, void* ws, size_t ws_bytes, void* stream)
+{
+    int rc = check_scan_cfg(cfg);
+    if (rc != SDM_OK)
+        return rc;
+    if (B < 0 || T < 0)
+        return SDM_EINVAL;
+    if (B == 0 || T == 0)
+        return SDM_OK;
+    const void* ptrs[] = {idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, dalpha, dbeta,
+                          dwsel, ws};
+    for (const void* p : ptrs)
+        if (p == nullptr)
+            return SDM_EINVAL;
+    if (ws_bytes < scan_backward_ws_bytes(*cfg, B, T))
+        return SDM_EWORKSPACE;
+    return cuda_status(launch_scan_backward(*cfg, idx, wsel, v, alpha, beta, tape, banks, dy, dbank,
+                                            dv, dalpha, dbeta, dwsel, B, T, ws,
+                                            (cudaStream_t)stream));
+}
+
 // ------------------------------------------------------ dense-state comparator
 
 int sdm_gdn_dense_scan(const sdm_cfg* cfg, const float* S0, const float* kw, const float* kr,

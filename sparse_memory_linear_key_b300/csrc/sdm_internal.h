@@ -69,7 +69,17 @@ cudaError_t launch_scan_codes(const sdm_cfg& c, const int32_t* idx, int B, int T
 cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel, const void* v,
                         const float* alpha, const float* beta, void* banks, float* y, int B,
                         int T, void* ws, size_t ws_bytes, int* status, cudaStream_t s,
-                        const void* m0 = nullptr, const int32_t* first_write = nullptr);
+                        const void* m0 = nullptr, const int32_t* first_write = nullptr,
+                        void* tape = nullptr);
+
+// Backward of the recurrence (scan_bwd.cu): reverse token order over a gradient bank;
+// ws holds per-block partial sums (scan_backward_ws_bytes).
+size_t scan_backward_ws_bytes(const sdm_cfg& c, int B, int T);
+cudaError_t launch_scan_backward(const sdm_cfg& c, const int32_t* idx, const float* wsel,
+                                 const void* v, const float* alpha, const float* beta,
+                                 const void* tape, void* banks, const float* dy, float* dbank,
+                                 float* dv, float* dalpha, float* dbeta, float* dwsel, int B,
+                                 int T, void* ws, cudaStream_t s);
 
 // first_write [B][N] <- the first token of each sequence that writes each slot, or a
 // value >= T if none (bank_init.cu)

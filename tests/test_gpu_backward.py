@@ -1,0 +1,117 @@
+"""Backward of the recurrence (the gated-delta write and the weighted read) against the
+oracle's autograd of the per-token definition, teacher-forced with the CUDA path's own
+addressing. Also exact: after the backward walk the banks are the initial banks again,
+bit for bit (the tape restores every write)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_memory_linear_key_b300 as sdm
+import synth
+from tests import sdm_testlib as tl
+from tests.test_gpu_parity import SMALL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    from sparse_memory_linear_key_b300 import build
+    build.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def rel_err(got, want):
+    return float(np.abs(np.asarray(got, np.float64) - want).max() / max(np.abs(want).max(), 1e-30))
+
+
+@pytest.mark.parametrize("name,tol", [("tiny-f32", 1e-4), ("ragged-f32", 1e-4),
+                                      ("ragged-bf16", 2e-2), ("w64-small", 2e-2)])
+def test_scan_backward_matches_autograd(name, tol):
+    wl = SMALL[name]
+    cfg = tl.cfg_of(wl)
+    p = synth.make_params(wl)
+    tok = synth.make_tokens(wl)
+    out = tl.run_staged(wl, p, tok)       # the CUDA path's addressing and v
+    B, T, d, N, W = wl.B, wl.T, wl.d, wl.N, wl.W
+    idx, wsel, v = out["idx"], out["wsel"], out["v"]
+    al, be = out["alpha"].reshape(-1), out["beta"].reshape(-1)
+    dt = wl.torch_dtype
+    M0 = p["M0"].cuda()
+    banks = torch.empty(B, N, d, dtype=dt, device="cuda")
+    sdm.sdm_init_bank(cfg, M0, banks)
+    banks0 = banks.clone()
+    y = torch.empty(B * T, d, device="cuda")
+    tape = torch.empty(B * T, W, d, dtype=dt, device="cuda")
+    ws = sdm.alloc_workspace(sdm.scan_workspace_bytes(cfg, B, T))
+    st = sdm.new_status()
+    sdm.sdm_scan_prepare(cfg, idx, B, T, ws, st)
+    sdm.sdm_scan_run_train(cfg, idx, wsel, v, al, be, banks, y, B, T, ws, tape, st)
+    g = torch.Generator().manual_seed(7)
+    dy = torch.randn(B * T, d, generator=g)
+    dMf = torch.randn(B, N, d, generator=g) * 0.1
+    dbank = dMf.cuda()
+    dv = torch.empty(B * T, d, device="cuda")
+    dal = torch.empty(B * T, device="cuda")
+    dbe = torch.empty(B * T, device="cuda")
+    dw = torch.empty(B * T, 2, W, device="cuda")
+    wsb = sdm.alloc_workspace(sdm.scan_backward_workspace_bytes(cfg, B, T))
+    sdm.sdm_scan_backward(cfg, idx, wsel, v, al, be, tape, banks, dy.cuda(), dbank, dv, dal, dbe,
+                          dw, B, T, wsb)
+    torch.cuda.synchronize()
+    assert sdm.read_status(st) == 0
+    assert torch.equal(banks, banks0)     # walked back to the initial state, exactly
+    idx_h, w_h = idx.cpu().numpy(), wsel.cpu().numpy().astype(np.float64)
+    type_ = oracle.BF16 if wl.dtype == "bf16" else oracle.F32
+    for b in range(B):
+        sl = slice(b * T, (b + 1) * T)
+        ref = oracle.scan_backward(oracle.to_f64(p["M0"]), v[sl].cpu(), al[sl].cpu().numpy(),
+                                   be[sl].cpu().numpy(), idx_h[sl, 0], w_h[sl, 0], idx_h[sl, 1],
+                                   w_h[sl, 1], dy[sl].numpy(), dMf[b].numpy(), type_=type_)
+        checks = [("dM_init", dbank[b].cpu().numpy(), ref["dM_init"]),
+                  ("dv", dv[sl].cpu().numpy(), ref["dv"]),
+                  ("dalpha", dal[sl].cpu().numpy(), ref["dalpha"]),
+                  ("dbeta", dbe[sl].cpu().numpy(), ref["dbeta"]),
+                  ("dk", dw[sl, 0].cpu().numpy(), ref["dk"]),
+                  ("dr", dw[sl, 1].cpu().numpy(), ref["dr"])]
+        for what, got, want in checks:
+            e = rel_err(got, want)
+            assert e <= tol, (name, b, what, e)
+
+
+def test_scan_backward_from_m0_restores_m0():
+    """The forward from M0 without a copy (first touch) also records its tape; walking
+    back leaves every bank equal to M0."""
+    wl = SMALL["n480-small-d"]
+    cfg = tl.cfg_of(wl)
+    p = synth.make_params(wl)
+    tok = synth.make_tokens(wl)
+    out = tl.run_staged(wl, p, tok)
+    B, T, d, N, W = wl.B, wl.T, wl.d, wl.N, wl.W
+    idx, wsel, v = out["idx"], out["wsel"], out["v"]
+    al, be = out["alpha"].reshape(-1), out["beta"].reshape(-1)
+    M0 = p["M0"].cuda()
+    banks = torch.full((B, N, d), float("nan"), dtype=wl.torch_dtype, device="cuda")
+    fw = torch.empty(B, N, dtype=torch.int32, device="cuda")
+    ws = sdm.alloc_workspace(sdm.scan_workspace_bytes(cfg, B, T))
+    st = sdm.new_status()
+    tape = torch.empty(B * T, W, d, dtype=wl.torch_dtype, device="cuda")
+    y = torch.empty(B * T, d, device="cuda")
+    sdm.sdm_first_touch(cfg, idx, B, T, fw)
+    sdm.sdm_scan_prepare(cfg, idx, B, T, ws, st)
+    sdm.sdm_scan_run_train(cfg, idx, wsel, v, al, be, banks, y, B, T, ws, tape, st, M0=M0,
+                           first_write=fw)
+    sdm.sdm_fill_untouched(cfg, M0, fw, banks, B, T)
+    assert torch.equal(y, out["y"])        # the same forward as the copy path
+    dbank = torch.zeros(B, N, d, device="cuda")
+    z = torch.empty(B * T, device="cuda")
+    sdm.sdm_scan_backward(cfg, idx, wsel, v, al, be, tape, banks, torch.ones(B * T, d, device="cuda"),
+                          dbank, torch.empty(B * T, d, device="cuda"), z, torch.empty_like(z),
+                          torch.empty(B * T, 2, W, device="cuda"), B, T,
+                          sdm.alloc_workspace(sdm.scan_backward_workspace_bytes(cfg, B, T)))
+    torch.cuda.synchronize()
+    assert sdm.read_status(st) == 0
+    for b in range(B):
+        assert torch.equal(banks[b], M0)
