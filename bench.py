@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--tokens", type=int, default=None,
                     help="tokens per sequence instead of the workload's (for profiling a "
                          "small case of the same kernels)")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences instead of the workload's (for profiling a small case)")
     return ap.parse_args()
@@ -335,6 +336,56 @@ def gpu_arm(args, world, rank):
         "kernel": "gdn_dense_kernel: sequential in t per row, state in registers",
         "gpu_launches_per_call": 1}
     del y_g
+
+    # ---- training: the forward that records the tape, and the backward of the
+    # recurrence (dv, dalpha, dbeta, weight gradients, initial-bank gradient) on the same
+    # tokens. Timed once each after a warm-up pair; the banks walk back to M0 and are
+    # re-filled from M0 by the next forward.
+    if not args.no_backward:
+        tape = torch.empty(ntok, wl.W, d, dtype=torch.bfloat16, device=dev)
+        dy = torch.randn(ntok, d, device=dev)
+        dbank = torch.zeros(B, wl.N, d, device=dev)
+        dv = torch.empty(ntok, d, device=dev)
+        dal = torch.empty(ntok, device=dev)
+        dbe = torch.empty(ntok, device=dev)
+        dws = torch.empty(ntok, 2, wl.W, device=dev)
+        wsb = sdm.alloc_workspace(sdm.scan_backward_workspace_bytes(cfg, B, T))
+
+        def train_pair(e=None):
+            sdm.sdm_first_touch(cfg, idx, B, T, first_write)
+            sdm.sdm_scan_prepare(cfg, idx, B, T, ws_s, st)
+            if e is not None:
+                e[0].record(stream)
+            sdm.sdm_scan_run_train(cfg, idx, wsel, v, alpha, beta, banks, y, B, T, ws_s, tape, st,
+                                   M0=p["M0"], first_write=first_write)
+            if e is not None:
+                e[1].record(stream)
+            sdm.sdm_fill_untouched(cfg, p["M0"], first_write, banks, B, T)
+            dbank.zero_()
+            if e is not None:
+                e[2].record(stream)
+            sdm.sdm_scan_backward(cfg, idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, dal,
+                                  dbe, dws, B, T, wsb)
+            if e is not None:
+                e[3].record(stream)
+
+        train_pair()
+        torch.cuda.synchronize()
+        te = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        train_pair(te)
+        torch.cuda.synchronize()
+        if sdm.read_status(st) != 0:
+            raise RuntimeError("device status during the training pair")
+        fwd_ms, bwd_ms = te[0].elapsed_time(te[1]), te[2].elapsed_time(te[3])
+        res["training"] = {
+            "what": "scan forward recording the tape (pre-write slot values), then the backward "
+                    "of the recurrence; bf16 tape and banks, fp32 gradients",
+            "forward_with_tape_ms": round(fwd_ms, 3), "backward_ms": round(bwd_ms, 3),
+            "backward_tokens_per_s": round(ntok / (bwd_ms / 1e3), 1),
+            "tape_bytes": tape.numel() * 2,
+            "kernel": "scan_bwd_kernel: one block per (sequence, 64 rows), reverse token order"}
+        del tape, dy, dbank, dv, dal, dbe, dws, wsb
+        torch.cuda.empty_cache()
 
     # ---- e2e: the one-call public API with host buffers
     x_h = tok_cpu["x"].pin_memory()

@@ -80,19 +80,28 @@ __global__ void __launch_bounds__(kBThreads) scan_bwd_kernel(
         }
         __syncthreads();
         const float dyr = act ? __ldg(dy + tok * d + row) : 0.f;
-        // ---- read: G[R_j] += r_j dy, dr_j = <M[R_j], dy> (M after this token's write)
+        // ---- read: G[R_j] += r_j dy, dr_j = <M[R_j], dy> (M after this token's write).
+        // All loads first, then the updates, then the sums over rows.
+        float mv[SPG], gr[SPG];
+#pragma unroll
+        for (int i = 0; i < SPG; ++i) {
+            const int s = sid[1][grp + kBGroups * i];
+            const bool ok = act && s >= 0 && s < N;
+            mv[i] = ok ? ld_state(bank + (size_t)s * d + row) : 0.f;
+            gr[i] = ok ? G[(size_t)s * d + row] : 0.f;
+        }
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
             const int j = grp + kBGroups * i;
             const int s = sid[1][j];
-            float pr = 0.f;
-            if (act && s >= 0 && s < N) {
-                pr = ld_state(bank + (size_t)s * d + row) * dyr;
-                G[(size_t)s * d + row] += sw[1][j] * dyr;
-            }
-            pr = warp_sum(pr);
+            if (act && s >= 0 && s < N)
+                G[(size_t)s * d + row] = fmaf(sw[1][j], dyr, gr[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < SPG; ++i) {
+            const float pr = warp_sum(mv[i] * dyr);
             if (lane == 0)
-                atomicAdd(&acc[W + j], pr);
+                atomicAdd(&acc[W + grp + kBGroups * i], pr);
         }
         __syncthreads();   // a slot both read and written: its G update is visible below
         // ---- write
@@ -124,20 +133,26 @@ __global__ void __launch_bounds__(kBThreads) scan_bwd_kernel(
         const float vr = act ? ld_io(v + tok * d + row) : 0.f;
         const float c = vr - al * u;
         float pa = 0.f;
+        float pk[SPG];
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
             const int j = grp + kBGroups * i;
             const int s = sid[0][j];
             const float kj = sw[0][j];
             pa = fmaf(gj[i], old[i] - be * kj * u, pa);
-            float pk = be * gj[i] * c - al * be * g * old[i];
-            pk = warp_sum(pk);
-            if (lane == 0)
-                atomicAdd(&acc[j], pk);
+            pk[i] = be * gj[i] * c - al * be * g * old[i];
             if (act && s >= 0 && s < N) {
                 G[(size_t)s * d + row] = al * (gj[i] - be * kj * g);
-                bank[(size_t)s * d + row] = tape[((size_t)tok * W + j) * d + row];
+                // the tape value read above, stored back exactly (a stored value converts
+                // to fp32 and back unchanged)
+                bank[(size_t)s * d + row] = S(old[i]);
             }
+        }
+#pragma unroll
+        for (int i = 0; i < SPG; ++i) {
+            const float q = warp_sum(pk[i]);
+            if (lane == 0)
+                atomicAdd(&acc[grp + kBGroups * i], q);
         }
         pa = warp_sum(pa);
         float pb = warp_sum(grp == 0 ? g * c : 0.f);
