@@ -54,38 +54,77 @@ __global__ void __launch_bounds__(kBThreads) scan_bwd_kernel(
 {
     constexpr int SPG = W / kBGroups;         // slots a thread: j = grp + 4 i
     constexpr int P = 2 * W + 2;
-    __shared__ int sid[2][W];
-    __shared__ float sw[2][W];
-    __shared__ float gate[2];
+    // Token t's slot ids, weights and gates sit in buffer t & 1 (written during token
+    // t + 1), and so do its partial sums (cleared during token t + 1, after every thread
+    // has written out token t + 2's).
+    static_assert(2 * W <= kBThreads && P <= kBThreads, "one metadata entry a thread");
+    __shared__ int sid[2][2][W];
+    __shared__ float sw[2][2][W];
+    __shared__ float gate[2][2];
     __shared__ float red[2][kBGroups][kBRows];
-    __shared__ float acc[P];
+    __shared__ float acc[2][P];
     const int b = blockIdx.y;
     const int r = threadIdx.x % kBRows, grp = threadIdx.x / kBRows;
     const int row = blockIdx.x * kBRows + r;
     const bool act = row < d;
     const int lane = threadIdx.x & 31;
+    const int e = threadIdx.x;                       // metadata entry of this thread
     S* bank = banks + (size_t)b * N * d;
     float* G = dbank + (size_t)b * N * d;
+    if (T <= 0)
+        return;
+    // what a token needs besides the gradient bank, loaded one token ahead
+    int nid = -1;
+    float nw = 0.f, nal = 0.f, nbe = 0.f, ndy = 0.f, nv = 0.f;
+    float nold[SPG];
+    auto prefetch = [&](int64_t tk) {
+        if (e < 2 * W) {
+            nid = __ldg(idx + tk * 2 * W + e);
+            nw = __ldg(wsel + tk * 2 * W + e);
+        }
+        if (e == 0) {
+            nal = __ldg(alpha + tk);
+            nbe = __ldg(beta + tk);
+        }
+        ndy = act ? __ldg(dy + tk * d + row) : 0.f;
+        nv = act ? ld_io(v + tk * d + row) : 0.f;
+#pragma unroll
+        for (int i = 0; i < SPG; ++i)   // tape rows exist for every position, ids aside
+            nold[i] = act ? ld_state(tape + ((size_t)tk * W + grp + kBGroups * i) * d + row) : 0.f;
+    };
+    auto publish = [&](int buf) {
+        if (e < 2 * W) {
+            sid[buf][e / W][e % W] = nid;
+            sw[buf][e / W][e % W] = nw;
+        }
+        if (e == 0) {
+            gate[buf][0] = nal;
+            gate[buf][1] = nbe;
+        }
+    };
+    prefetch((int64_t)b * T + T - 1);
+    publish((T - 1) & 1);
+    if (e < P) {
+        acc[0][e] = 0.f;
+        acc[1][e] = 0.f;
+    }
+    __syncthreads();
     for (int t = T - 1; t >= 0; --t) {
         const int64_t tok = (int64_t)b * T + t;
-        for (int e = threadIdx.x; e < 2 * W; e += kBThreads) {
-            sid[e / W][e % W] = __ldg(idx + tok * 2 * W + e);
-            sw[e / W][e % W] = __ldg(wsel + tok * 2 * W + e);
-        }
-        for (int e = threadIdx.x; e < P; e += kBThreads)
-            acc[e] = 0.f;
-        if (threadIdx.x == 0) {
-            gate[0] = __ldg(alpha + tok);
-            gate[1] = __ldg(beta + tok);
-        }
-        __syncthreads();
-        const float dyr = act ? __ldg(dy + tok * d + row) : 0.f;
+        const int cb = t & 1;
+        const float dyr = ndy, vr = nv;
+        float old[SPG];
+#pragma unroll
+        for (int i = 0; i < SPG; ++i)
+            old[i] = nold[i];
+        if (t > 0)
+            prefetch(tok - 1);
         // ---- read: G[R_j] += r_j dy, dr_j = <M[R_j], dy> (M after this token's write).
         // All loads first, then the updates, then the sums over rows.
         float mv[SPG], gr[SPG];
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
-            const int s = sid[1][grp + kBGroups * i];
+            const int s = sid[cb][1][grp + kBGroups * i];
             const bool ok = act && s >= 0 && s < N;
             mv[i] = ok ? ld_state(bank + (size_t)s * d + row) : 0.f;
             gr[i] = ok ? G[(size_t)s * d + row] : 0.f;
@@ -93,58 +132,59 @@ __global__ void __launch_bounds__(kBThreads) scan_bwd_kernel(
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
             const int j = grp + kBGroups * i;
-            const int s = sid[1][j];
+            const int s = sid[cb][1][j];
             if (act && s >= 0 && s < N)
-                G[(size_t)s * d + row] = fmaf(sw[1][j], dyr, gr[i]);
+                G[(size_t)s * d + row] = fmaf(sw[cb][1][j], dyr, gr[i]);
         }
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
             const float pr = warp_sum(mv[i] * dyr);
             if (lane == 0)
-                atomicAdd(&acc[W + grp + kBGroups * i], pr);
+                atomicAdd(&acc[cb][W + grp + kBGroups * i], pr);
         }
-        __syncthreads();   // a slot both read and written: its G update is visible below
+        __syncthreads();   // (A) a slot both read and written: its G update is visible below
+        // every thread has written out token t + 1's partials (before A): clear them for
+        // token t - 1, which starts after barrier C
+        if (e < P)
+            acc[cb ^ 1][e] = 0.f;
         // ---- write
-        float old[SPG], gj[SPG];
+        float gj[SPG];
         float gp = 0.f, up = 0.f;
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
             const int j = grp + kBGroups * i;
-            const int s = sid[0][j];
-            old[i] = 0.f;
-            gj[i] = 0.f;
-            if (act && s >= 0 && s < N) {
-                old[i] = ld_state(tape + ((size_t)tok * W + j) * d + row);
-                gj[i] = G[(size_t)s * d + row];
-            }
-            gp = fmaf(sw[0][j], gj[i], gp);
-            up = fmaf(sw[0][j], old[i], up);
+            const int s = sid[cb][0][j];
+            const bool ok = act && s >= 0 && s < N;
+            if (!ok)
+                old[i] = 0.f;
+            gj[i] = ok ? G[(size_t)s * d + row] : 0.f;
+            gp = fmaf(sw[cb][0][j], gj[i], gp);
+            up = fmaf(sw[cb][0][j], old[i], up);
         }
         red[0][grp][r] = gp;
         red[1][grp][r] = up;
-        __syncthreads();
+        __syncthreads();   // (B)
         float g = 0.f, u = 0.f;
 #pragma unroll
         for (int q = 0; q < kBGroups; ++q) {
             g += red[0][q][r];
             u += red[1][q][r];
         }
-        const float al = gate[0], be = gate[1];
-        const float vr = act ? ld_io(v + tok * d + row) : 0.f;
+        const float al = gate[cb][0], be = gate[cb][1];
         const float c = vr - al * u;
         float pa = 0.f;
         float pk[SPG];
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
             const int j = grp + kBGroups * i;
-            const int s = sid[0][j];
-            const float kj = sw[0][j];
+            const int s = sid[cb][0][j];
+            const float kj = sw[cb][0][j];
             pa = fmaf(gj[i], old[i] - be * kj * u, pa);
             pk[i] = be * gj[i] * c - al * be * g * old[i];
             if (act && s >= 0 && s < N) {
                 G[(size_t)s * d + row] = al * (gj[i] - be * kj * g);
-                // the tape value read above, stored back exactly (a stored value converts
-                // to fp32 and back unchanged)
+                // the tape value, stored back exactly (a stored value converts to fp32
+                // and back unchanged)
                 bank[(size_t)s * d + row] = S(old[i]);
             }
         }
@@ -152,20 +192,25 @@ __global__ void __launch_bounds__(kBThreads) scan_bwd_kernel(
         for (int i = 0; i < SPG; ++i) {
             const float q = warp_sum(pk[i]);
             if (lane == 0)
-                atomicAdd(&acc[grp + kBGroups * i], q);
+                atomicAdd(&acc[cb][grp + kBGroups * i], q);
         }
         pa = warp_sum(pa);
-        float pb = warp_sum(grp == 0 ? g * c : 0.f);
+        const float pb = warp_sum(grp == 0 ? g * c : 0.f);
         if (lane == 0) {
-            atomicAdd(&acc[2 * W], pa);
-            atomicAdd(&acc[2 * W + 1], pb);
+            atomicAdd(&acc[cb][2 * W], pa);
+            atomicAdd(&acc[cb][2 * W + 1], pb);
         }
         if (grp == 0 && act)
             dv[tok * d + row] = be * g;
-        __syncthreads();
-        for (int e = threadIdx.x; e < P; e += kBThreads)
-            part[((size_t)blockIdx.x * B * T + tok) * P + e] = acc[e];
-        __syncthreads();   // acc, sid, sw and gate are reset for the next token
+        // token t - 1's slot ids, weights and gates into the other buffer (token t + 1
+        // finished with it before barrier A)
+        if (t > 0)
+            publish(cb ^ 1);
+        __syncthreads();   // (C) partial sums complete; token t - 1's metadata visible
+        if (e < P)
+            part[((size_t)blockIdx.x * B * T + tok) * P + e] = acc[cb][e];
+        // red is rewritten after token t - 1's barrier A, which every thread reaches only
+        // after these reads; acc[cb] is cleared only after that barrier too
     }
 }
 
