@@ -343,3 +343,26 @@ def scan_backward(M_init, v, alpha, beta, S, k, Rd, r, dy, dM_final=None, type_=
     return {"dM_init": M0.grad.numpy(), "dv": vv.grad.numpy(), "dalpha": al.grad.numpy(),
             "dbeta": be.grad.numpy(), "dk": kk.grad.numpy(), "dr": rr.grad.numpy(),
             "y": y.detach().numpy(), "M_final": M.detach().numpy()}
+
+
+def address_backward(q, K1, K2, slots, dw):
+    """Gradients of the selection weights with respect to the queries and sub-keys,
+    the kept slots held fixed (the top-W selection is piecewise constant; the weights
+    are a softmax of the kept combined scores c_j = <K1[i_j], q1> + <K2[l_j], q2>, slot
+    i_j * n + l_j). q [ntok, dk], K1/K2 [n, dk/2], slots [ntok, W], dw [ntok, W].
+    Autograd in fp64 with plain PyTorch CPU ops. Returns (w, dq, dK1, dK2) as numpy."""
+    import torch
+    f = torch.float64
+    qq = torch.tensor(to_f64(q), dtype=f, requires_grad=True)
+    k1 = torch.tensor(to_f64(K1), dtype=f, requires_grad=True)
+    k2 = torch.tensor(to_f64(K2), dtype=f, requires_grad=True)
+    n = k1.shape[0]
+    h = k1.shape[1]
+    sl = torch.as_tensor(np.asarray(slots), dtype=torch.long)
+    i_idx, l_idx = sl // n, sl % n
+    s1 = qq[:, :h] @ k1.T                          # [ntok, n]
+    s2 = qq[:, h:] @ k2.T
+    c = torch.gather(s1, 1, i_idx) + torch.gather(s2, 1, l_idx)
+    w = torch.softmax(c, dim=1)
+    (w * torch.tensor(np.asarray(dw, np.float64), dtype=f)).sum().backward()
+    return w.detach().numpy(), qq.grad.numpy(), k1.grad.numpy(), k2.grad.numpy()

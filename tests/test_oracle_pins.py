@@ -541,3 +541,36 @@ def test_scan_backward_closed_form_single_token():
     assert abs(g["dM_init"][0, 0] - a * (1 - b)) < 1e-14
     assert abs(g["dalpha"][0] - (1 - b) * m) < 1e-14
     assert abs(g["dbeta"][0] - (vv - a * m)) < 1e-14
+
+
+def test_address_backward_matches_finite_differences():
+    """The selection weights as a function of q and the sub-keys with the kept slots
+    fixed, differentiated by central differences of the plain formula."""
+    rng = np.random.default_rng(41)
+    ntok, n, h, W = 3, 5, 4, 4
+    q = rng.normal(size=(ntok, 2 * h))
+    K1 = rng.normal(size=(n, h))
+    K2 = rng.normal(size=(n, h))
+    slots = np.stack([rng.choice(n * n, W, replace=False) for _ in range(ntok)])
+    dw = rng.normal(size=(ntok, W))
+
+    def loss(q_, K1_, K2_):
+        i, l = slots // n, slots % n
+        c = np.einsum("th,tjh->tj", q_[:, :h], K1_[i]) + np.einsum("th,tjh->tj", q_[:, h:], K2_[l])
+        e = np.exp(c - c.max(1, keepdims=True))
+        return float(((e / e.sum(1, keepdims=True)) * dw).sum())
+
+    w, dq, dK1, dK2 = oracle.address_backward(q, K1, K2, slots, dw)
+    i, l = slots // n, slots % n
+    c = np.einsum("th,tjh->tj", q[:, :h], K1[i]) + np.einsum("th,tjh->tj", q[:, h:], K2[l])
+    np.testing.assert_allclose(w.sum(1), 1.0, atol=1e-12)
+    np.testing.assert_allclose(w, np.stack([oracle.softmax(row) for row in c]), atol=1e-12)
+    hh = 1e-6
+    for arr, grad, which in ((q, dq, 0), (K1, dK1, 1), (K2, dK2, 2)):
+        for e_ in range(arr.size):
+            args = [q.copy(), K1.copy(), K2.copy()]
+            args[which].reshape(-1)[e_] += hh
+            up = loss(*args)
+            args[which].reshape(-1)[e_] -= 2 * hh
+            fd = (up - loss(*args)) / (2 * hh)
+            assert abs(fd - grad.reshape(-1)[e_]) < 1e-7, (which, e_)
