@@ -248,6 +248,20 @@ SDM_API int sdm_scan_backward(const sdm_cfg* cfg, const int32_t* idx, const floa
                               float* dv, float* dalpha, float* dbeta, float* dwsel, int B, int T,
                               void* ws, size_t ws_bytes, void* stream);
 
+/* Backward of the addressing: given dwsel [ntok, 2, w] fp32 (the gradient of the loss
+ * with respect to the selection weights wsel of sdm_address, e.g. from
+ * sdm_scan_backward), with the kept slots idx held fixed (the top-w selection is
+ * piecewise constant), writes dq_w, dq_r [ntok, dk] and dK1, dK2 [n_sub, dk/2], fp32,
+ * overwritten. q_w, q_r, K1, K2, idx, wsel as in sdm_address. Softmax backward per
+ * token, then strict-fp32 GEMMs on the dense score gradients. ws:
+ * sdm_address_backward_workspace_bytes(cfg, ntok), 256-byte aligned. */
+SDM_API size_t sdm_address_backward_workspace_bytes(const sdm_cfg* cfg, int64_t ntok);
+SDM_API int sdm_address_backward(const sdm_cfg* cfg, const void* K1, const void* K2,
+                                 const void* q_w, const void* q_r, int64_t ntok,
+                                 const int32_t* idx, const float* wsel, const float* dwsel,
+                                 float* dq_w, float* dq_r, float* dK1, float* dK2, void* ws,
+                                 size_t ws_bytes, void* stream);
+
 /* Dense-state comparator (NOT the method: a measured reference point). The pages set
  * SDM against gated-delta-net: SDM's W = 64 active slot vectors per token are exactly the
  * size of GDN's whole dense state, at identical FLOPs per token ("Sparse Delta Memory"

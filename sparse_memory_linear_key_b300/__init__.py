@@ -97,6 +97,8 @@ def lib():
             "sdm_prefill_m0": ([CP, WP, P, P, P, P, P, P, I, I, P, P, P, S, P, P], I),
             "sdm_gdn_dense_scan": ([CP, P, P, P, L64, P, P, P, P, P, I, I, P], I),
             "sdm_tape_bytes": ([CP, I, I], S),
+            "sdm_address_backward_workspace_bytes": ([CP, L64], S),
+            "sdm_address_backward": ([CP, P, P, P, P, L64, P, P, P, P, P, P, P, P, S, P], I),
             "sdm_scan_run_train": ([CP, P, P, P, P, P, P, P, P, P, I, I, P, S, P, P, P], I),
             "sdm_scan_backward_workspace_bytes": ([CP, I, I], S),
             "sdm_scan_backward": ([CP, P, P, P, P, P, P, P, P, P, P, P, P, P, I, I, P, S, P], I),
@@ -385,6 +387,27 @@ def sdm_scan_backward(cfg: Cfg, idx, wsel, v, alpha, beta, tape, banks, dy, dban
                                    _ptr(dwsel, f, "dwsel"), B, T, _ptr(ws, None, "ws"),
                                    ws.numel() * ws.element_size(), _stream(stream)),
            "sdm_scan_backward")
+
+
+def address_backward_workspace_bytes(cfg: Cfg, ntok: int) -> int:
+    return int(lib().sdm_address_backward_workspace_bytes(ctypes.byref(cfg), ntok))
+
+
+def sdm_address_backward(cfg: Cfg, K1, K2, q_w, q_r, idx, wsel, dwsel, dq_w, dq_r, dK1, dK2, ws,
+                         stream=None) -> None:
+    """dq_w, dq_r [ntok, dk] and dK1, dK2 [n, dk/2] (fp32) from the selection-weight
+    gradients dwsel [ntok, 2, w], the kept slots idx held fixed."""
+    dt = cfg.torch_dtype
+    f = torch.float32
+    ntok = q_w.shape[0]
+    _check(lib().sdm_address_backward(ctypes.byref(cfg), _ptr(K1, dt, "K1"), _ptr(K2, dt, "K2"),
+                                      _ptr(q_w, dt, "q_w"), _ptr(q_r, dt, "q_r"), ntok,
+                                      _ptr(idx, torch.int32, "idx"), _ptr(wsel, f, "wsel"),
+                                      _ptr(dwsel, f, "dwsel"), _ptr(dq_w, f, "dq_w"),
+                                      _ptr(dq_r, f, "dq_r"), _ptr(dK1, f, "dK1"), _ptr(dK2, f, "dK2"),
+                                      _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+                                      _stream(stream)),
+           "sdm_address_backward")
 
 
 def sdm_gdn_dense_scan(cfg: Cfg, kw, kr, k_stride: int, v, alpha, beta, y, B: int, T: int,

@@ -14,7 +14,7 @@ OUT_DIR = os.path.join(HERE, "lib")
 LIB = os.path.join(OUT_DIR, "libsdm.so")
 SOURCES = ["sdm_api.cu", "bank_init.cu", "project.cu", "address.cu", "score_tc.cu",
            "scan_codes.cu", "scan.cu", "scan_static.cu", "slot_stats.cu",
-           "gdn_dense.cu", "scan_bwd.cu"]
+           "gdn_dense.cu", "scan_bwd.cu", "addr_bwd.cu"]
 HEADERS = ["sdm_common.cuh", "sdm_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

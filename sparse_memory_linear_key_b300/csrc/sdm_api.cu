@@ -517,6 +517,37 @@ int sdm_scan_backward(const sdm_cfg* cfg, const int32_t* idx, const float* wsel,
                                             (cudaStream_t)stream));
 }
 
+size_t sdm_address_backward_workspace_bytes(const sdm_cfg* cfg, int64_t ntok)
+{
+    if (sdm_check_cfg(cfg) != SDM_OK || ntok < 0)
+        return 0;
+    return address_backward_ws_bytes(*cfg, ntok);
+}
+
+int sdm_address_backward(const sdm_cfg* cfg, const void* K1, const void* K2, const void* q_w,
+                         const void* q_r, int64_t ntok, const int32_t* idx, const float* wsel,
+                         const float* dwsel, float* dq_w, float* dq_r, float* dK1, float* dK2,
+                         void* ws, size_t ws_bytes, void* stream)
+{
+    int rc = sdm_check_cfg(cfg);
+    if (rc != SDM_OK)
+        return rc;
+    if (ntok < 0)
+        return SDM_EINVAL;
+    if (ntok == 0)
+        return SDM_OK;
+    const void* ptrs[] = {K1, K2, q_w, q_r, idx, wsel, dwsel, dq_w, dq_r, dK1, dK2, ws};
+    for (const void* p : ptrs)
+        if (p == nullptr)
+            return SDM_EINVAL;
+    if (((uintptr_t)ws & 255u) != 0)
+        return SDM_EINVAL;
+    if (ws_bytes < address_backward_ws_bytes(*cfg, ntok))
+        return SDM_EWORKSPACE;
+    return launch_address_backward(*cfg, K1, K2, q_w, q_r, ntok, idx, wsel, dwsel, dq_w, dq_r, dK1,
+                                   dK2, ws, (cudaStream_t)stream);
+}
+
 // ------------------------------------------------------ dense-state comparator
 
 int sdm_gdn_dense_scan(const sdm_cfg* cfg, const float* S0, const float* kw, const float* kr,

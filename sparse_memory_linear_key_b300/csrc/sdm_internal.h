@@ -85,6 +85,17 @@ cudaError_t launch_scan_backward(const sdm_cfg& c, const int32_t* idx, const flo
 // value >= T if none (bank_init.cu)
 cudaError_t launch_first_touch(const sdm_cfg& c, const int32_t* idx, int B, int T,
                                int32_t* first_write, cudaStream_t s);
+// row-major fp32 GEMM, C = op(A) op(B) + beta C, strict fp32 (project.cu)
+int gemm_f32_rm(cudaStream_t s, bool ta, bool tb, int M, int N, int K, const float* A, int lda,
+                const float* B, int ldb, float* C, int ldc, float beta);
+
+// Backward of the addressing (addr_bwd.cu): selection-weight gradients -> dq, dK
+size_t address_backward_ws_bytes(const sdm_cfg& c, int64_t ntok);
+int launch_address_backward(const sdm_cfg& c, const void* K1, const void* K2, const void* q_w,
+                            const void* q_r, int64_t ntok, const int32_t* idx, const float* wsel,
+                            const float* dwsel, float* dq_w, float* dq_r, float* dK1, float* dK2,
+                            void* ws, cudaStream_t s);
+
 // dense-state comparator (gdn_dense.cu): W = 64 columns, d % 16 == 0
 cudaError_t launch_gdn_dense(bool bf_io, const float* S0, const float* kw, const float* kr,
                              int64_t ks, const void* v, const float* alpha, const float* beta,

@@ -115,3 +115,39 @@ def test_scan_backward_from_m0_restores_m0():
     assert sdm.read_status(st) == 0
     for b in range(B):
         assert torch.equal(banks[b], M0)
+
+
+@pytest.mark.parametrize("name", ["tiny-f32", "w64-small", "n480-small-d", "n480-full-tiles"])
+def test_address_backward_matches_autograd(name):
+    """dq and dK from the selection-weight gradients, the kept slots fixed, against the
+    oracle's autograd of the softmax of the kept combined scores (the oracle scores the
+    CUDA path's own query bits)."""
+    wl = SMALL[name]
+    cfg = tl.cfg_of(wl)
+    p = synth.make_params(wl)
+    out = tl.run_staged(wl, p, synth.make_tokens(wl))
+    ntok, W, n, dk = wl.B * wl.T, wl.W, wl.n, wl.dk
+    g = torch.Generator().manual_seed(11)
+    dw = torch.randn(ntok, 2, W, generator=g)
+    dq_w = torch.empty(ntok, dk, device="cuda")
+    dq_r = torch.empty_like(dq_w)
+    dK1 = torch.empty(n, dk // 2, device="cuda")
+    dK2 = torch.empty_like(dK1)
+    ws = sdm.alloc_workspace(sdm.address_backward_workspace_bytes(cfg, ntok))
+    pd = tl.to_dev(p)
+    sdm.sdm_address_backward(cfg, pd["K1"], pd["K2"], out["q_w"], out["q_r"], out["idx"], out["wsel"],
+                             dw.cuda(), dq_w, dq_r, dK1, dK2, ws)
+    torch.cuda.synchronize()
+    idx = out["idx"].cpu().numpy()
+    wsel = out["wsel"].cpu().numpy()
+    dK1r = np.zeros((n, dk // 2))
+    dK2r = np.zeros((n, dk // 2))
+    for kind, q, got in ((0, out["q_w"], dq_w), (1, out["q_r"], dq_r)):
+        w, dq, k1, k2 = oracle.address_backward(q.cpu(), p["K1"], p["K2"], idx[:, kind],
+                                                dw[:, kind].numpy())
+        assert np.abs(w - wsel[:, kind]).max() <= 1e-5
+        assert rel_err(got.cpu().numpy(), dq) <= 1e-4, (name, kind)
+        dK1r += k1
+        dK2r += k2
+    assert rel_err(dK1.cpu().numpy(), dK1r) <= 1e-4, name
+    assert rel_err(dK2.cpu().numpy(), dK2r) <= 1e-4, name
