@@ -262,6 +262,19 @@ SDM_API int sdm_address_backward(const sdm_cfg* cfg, const void* K1, const void*
                                  float* dq_w, float* dq_r, float* dK1, float* dK2, void* ws,
                                  size_t ws_bytes, void* stream);
 
+/* Backward of the projections: with dq_w, dq_r [ntok, dk] and dv [ntok, d] fp32 (the
+ * gradients with respect to sdm_project's outputs; their rounding is passed through),
+ * writes dx [ntok, d] = dq_w W_qw^T + dq_r W_qr^T + dv W_v^T and dW_qw, dW_qr [d, dk],
+ * dW_v [d, d] = x^T d(out), fp32, overwritten. Strict-fp32 GEMMs on fp32 copies of x
+ * and the weights: ws sdm_project_backward_workspace_bytes(cfg, ntok), 256-byte
+ * aligned. With sdm_scan_backward and sdm_address_backward this completes the
+ * gradients of one layer (dq_w, dq_r from the addressing, dv from the scan). */
+SDM_API size_t sdm_project_backward_workspace_bytes(const sdm_cfg* cfg, int64_t ntok);
+SDM_API int sdm_project_backward(const sdm_cfg* cfg, const sdm_weights* wts, const void* x,
+                                 int64_t ntok, const float* dq_w, const float* dq_r,
+                                 const float* dv, float* dx, float* dW_qw, float* dW_qr,
+                                 float* dW_v, void* ws, size_t ws_bytes, void* stream);
+
 /* Dense-state comparator (NOT the method: a measured reference point). The pages set
  * SDM against gated-delta-net: SDM's W = 64 active slot vectors per token are exactly the
  * size of GDN's whole dense state, at identical FLOPs per token ("Sparse Delta Memory"

@@ -366,3 +366,12 @@ def address_backward(q, K1, K2, slots, dw):
     w = torch.softmax(c, dim=1)
     (w * torch.tensor(np.asarray(dw, np.float64), dtype=f)).sum().backward()
     return w.detach().numpy(), qq.grad.numpy(), k1.grad.numpy(), k2.grad.numpy()
+
+
+def project_backward(x, W_qw, W_qr, W_v, dq_w, dq_r, dv):
+    """Gradients of q_w = x W_qw, q_r = x W_qr, v = x W_v (the rounding of the outputs
+    passed through): dx = dq_w W_qw^T + dq_r W_qr^T + dv W_v^T, dW = x^T dout. fp64."""
+    xx = to_f64(x)
+    dqw, dqr, dvv = to_f64(dq_w), to_f64(dq_r), to_f64(dv)
+    dx = dqw @ to_f64(W_qw).T + dqr @ to_f64(W_qr).T + dvv @ to_f64(W_v).T
+    return dx, xx.T @ dqw, xx.T @ dqr, xx.T @ dvv

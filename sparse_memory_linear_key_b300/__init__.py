@@ -98,6 +98,8 @@ def lib():
             "sdm_gdn_dense_scan": ([CP, P, P, P, L64, P, P, P, P, P, I, I, P], I),
             "sdm_tape_bytes": ([CP, I, I], S),
             "sdm_address_backward_workspace_bytes": ([CP, L64], S),
+            "sdm_project_backward_workspace_bytes": ([CP, L64], S),
+            "sdm_project_backward": ([CP, WP, P, L64, P, P, P, P, P, P, P, P, S, P], I),
             "sdm_address_backward": ([CP, P, P, P, P, L64, P, P, P, P, P, P, P, P, S, P], I),
             "sdm_scan_run_train": ([CP, P, P, P, P, P, P, P, P, P, I, I, P, S, P, P, P], I),
             "sdm_scan_backward_workspace_bytes": ([CP, I, I], S),
@@ -408,6 +410,27 @@ def sdm_address_backward(cfg: Cfg, K1, K2, q_w, q_r, idx, wsel, dwsel, dq_w, dq_
                                       _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
                                       _stream(stream)),
            "sdm_address_backward")
+
+
+def project_backward_workspace_bytes(cfg: Cfg, ntok: int) -> int:
+    return int(lib().sdm_project_backward_workspace_bytes(ctypes.byref(cfg), ntok))
+
+
+def sdm_project_backward(cfg: Cfg, params, x, dq_w, dq_r, dv, dx, dW_qw, dW_qr, dW_v, ws,
+                         stream=None) -> None:
+    """dx [ntok, d], dW_qw, dW_qr [d, dk], dW_v [d, d] (fp32) from the gradients of the
+    projection outputs."""
+    dt = cfg.torch_dtype
+    f = torch.float32
+    w = _weights(cfg, params)
+    ntok = x.numel() // cfg.d
+    _check(lib().sdm_project_backward(ctypes.byref(cfg), ctypes.byref(w), _ptr(x, dt, "x"), ntok,
+                                      _ptr(dq_w, f, "dq_w"), _ptr(dq_r, f, "dq_r"), _ptr(dv, f, "dv"),
+                                      _ptr(dx, f, "dx"), _ptr(dW_qw, f, "dW_qw"),
+                                      _ptr(dW_qr, f, "dW_qr"), _ptr(dW_v, f, "dW_v"),
+                                      _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+                                      _stream(stream)),
+           "sdm_project_backward")
 
 
 def sdm_gdn_dense_scan(cfg: Cfg, kw, kr, k_stride: int, v, alpha, beta, y, B: int, T: int,

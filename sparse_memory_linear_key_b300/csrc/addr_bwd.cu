@@ -1,6 +1,6 @@
-// addr_bwd.cu -- backward of the product-key addressing ("Sparse Delta Memory" blog,
-// "Write & Read": two sub-keys -> outer sum -> top-k, softmax weights; the addressing
-// is learned end to end, paper Abstract).
+// addr_bwd.cu -- backward of the product-key addressing and of the projections
+// ("Sparse Delta Memory" blog, "Write & Read": two sub-keys -> outer sum -> top-k,
+// softmax weights; the addressing is learned end to end, paper Abstract).
 //
 // The top-W selection is piecewise constant, so the gradient flows through the kept
 // pairs only. Per token and kind (write / read) with kept weights w_j = softmax(c)_j,
@@ -158,6 +158,59 @@ int launch_address_backward(const sdm_cfg& c, const void* K1, const void* K2, co
             return rc;
     }
     return SDM_OK;
+}
+
+}  // namespace sdm
+
+// ---------------------------------------------------------- projection backward
+// q_w = x W_qw, q_r = x W_qr, v = x W_v (the rounding of the outputs passed through):
+//   dx = dq_w W_qw^T + dq_r W_qr^T + dv W_v^T,   dW_* = x^T d(out)_*
+// strict-fp32 GEMMs on fp32 copies of x and the weights.
+
+namespace sdm {
+
+size_t project_backward_ws_bytes(const sdm_cfg& c, int64_t ntok)
+{
+    const size_t xb = ((size_t)ntok * c.d * 4 + 255) / 256 * 256;
+    const size_t wb = ((size_t)c.d * (2 * c.dk + c.d) * 4 + 255) / 256 * 256;
+    return xb + wb;
+}
+
+int launch_project_backward(const sdm_cfg& c, const sdm_weights& w, const void* x, int64_t ntok,
+                            const float* dq_w, const float* dq_r, const float* dv, float* dx,
+                            float* dW_qw, float* dW_qr, float* dW_v, void* ws, cudaStream_t s)
+{
+    if (ntok <= 0)
+        return SDM_OK;
+    if (ntok > 0x7FFFFFFF)
+        return SDM_EUNSUPPORTED;
+    const int d = c.d, dk = c.dk, nt = (int)ntok;
+    float* xf = (float*)ws;
+    float* wqw = (float*)((char*)ws + ((size_t)ntok * d * 4 + 255) / 256 * 256);
+    float* wqr = wqw + (size_t)d * dk;
+    float* wv = wqr + (size_t)d * dk;
+    const bool bf = c.dtype == SDM_BF16;
+    cudaError_t e = bf ? widen<bf16>(x, ntok, d, xf, d, s) : widen<float>(x, ntok, d, xf, d, s);
+    if (e == cudaSuccess)
+        e = bf ? widen<bf16>(w.W_qw, d, dk, wqw, dk, s) : widen<float>(w.W_qw, d, dk, wqw, dk, s);
+    if (e == cudaSuccess)
+        e = bf ? widen<bf16>(w.W_qr, d, dk, wqr, dk, s) : widen<float>(w.W_qr, d, dk, wqr, dk, s);
+    if (e == cudaSuccess)
+        e = bf ? widen<bf16>(w.W_v, d, d, wv, d, s) : widen<float>(w.W_v, d, d, wv, d, s);
+    if (e != cudaSuccess)
+        return SDM_ECUDA;
+    int rc = gemm_f32_rm(s, false, true, nt, d, dk, dq_w, dk, wqw, dk, dx, d, 0.f);
+    if (rc == SDM_OK)
+        rc = gemm_f32_rm(s, false, true, nt, d, dk, dq_r, dk, wqr, dk, dx, d, 1.f);
+    if (rc == SDM_OK)
+        rc = gemm_f32_rm(s, false, true, nt, d, d, dv, d, wv, d, dx, d, 1.f);
+    if (rc == SDM_OK)
+        rc = gemm_f32_rm(s, true, false, d, dk, nt, xf, d, dq_w, dk, dW_qw, dk, 0.f);
+    if (rc == SDM_OK)
+        rc = gemm_f32_rm(s, true, false, d, dk, nt, xf, d, dq_r, dk, dW_qr, dk, 0.f);
+    if (rc == SDM_OK)
+        rc = gemm_f32_rm(s, true, false, d, d, nt, xf, d, dv, d, dW_v, d, 0.f);
+    return rc;
 }
 
 }  // namespace sdm

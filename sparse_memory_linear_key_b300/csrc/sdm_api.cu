@@ -548,6 +548,37 @@ int sdm_address_backward(const sdm_cfg* cfg, const void* K1, const void* K2, con
                                    dK2, ws, (cudaStream_t)stream);
 }
 
+size_t sdm_project_backward_workspace_bytes(const sdm_cfg* cfg, int64_t ntok)
+{
+    if (sdm_check_cfg(cfg) != SDM_OK || ntok < 0)
+        return 0;
+    return project_backward_ws_bytes(*cfg, ntok);
+}
+
+int sdm_project_backward(const sdm_cfg* cfg, const sdm_weights* w, const void* x, int64_t ntok,
+                         const float* dq_w, const float* dq_r, const float* dv, float* dx,
+                         float* dW_qw, float* dW_qr, float* dW_v, void* ws, size_t ws_bytes,
+                         void* stream)
+{
+    int rc = sdm_check_cfg(cfg);
+    if (rc != SDM_OK)
+        return rc;
+    if (w == nullptr || ntok < 0)
+        return SDM_EINVAL;
+    if (ntok == 0)
+        return SDM_OK;
+    const void* ptrs[] = {w->W_qw, w->W_qr, w->W_v, x, dq_w, dq_r, dv, dx, dW_qw, dW_qr, dW_v, ws};
+    for (const void* p : ptrs)
+        if (p == nullptr)
+            return SDM_EINVAL;
+    if (((uintptr_t)ws & 255u) != 0)
+        return SDM_EINVAL;
+    if (ws_bytes < project_backward_ws_bytes(*cfg, ntok))
+        return SDM_EWORKSPACE;
+    return launch_project_backward(*cfg, *w, x, ntok, dq_w, dq_r, dv, dx, dW_qw, dW_qr, dW_v, ws,
+                                   (cudaStream_t)stream);
+}
+
 // ------------------------------------------------------ dense-state comparator
 
 int sdm_gdn_dense_scan(const sdm_cfg* cfg, const float* S0, const float* kw, const float* kr,

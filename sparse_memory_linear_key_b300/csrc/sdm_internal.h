@@ -96,6 +96,12 @@ int launch_address_backward(const sdm_cfg& c, const void* K1, const void* K2, co
                             const float* dwsel, float* dq_w, float* dq_r, float* dK1, float* dK2,
                             void* ws, cudaStream_t s);
 
+// Backward of the projections (addr_bwd.cu): dx, dW from dq_w, dq_r, dv
+size_t project_backward_ws_bytes(const sdm_cfg& c, int64_t ntok);
+int launch_project_backward(const sdm_cfg& c, const sdm_weights& w, const void* x, int64_t ntok,
+                            const float* dq_w, const float* dq_r, const float* dv, float* dx,
+                            float* dW_qw, float* dW_qr, float* dW_v, void* ws, cudaStream_t s);
+
 // dense-state comparator (gdn_dense.cu): W = 64 columns, d % 16 == 0
 cudaError_t launch_gdn_dense(bool bf_io, const float* S0, const float* kw, const float* kr,
                              int64_t ks, const void* v, const float* alpha, const float* beta,

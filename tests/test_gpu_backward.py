@@ -151,3 +151,102 @@ def test_address_backward_matches_autograd(name):
         dK2r += k2
     assert rel_err(dK1.cpu().numpy(), dK1r) <= 1e-4, name
     assert rel_err(dK2.cpu().numpy(), dK2r) <= 1e-4, name
+
+
+@pytest.mark.parametrize("name", ["tiny-f32", "w64-small"])
+def test_project_backward_matches_oracle(name):
+    wl = SMALL[name]
+    cfg = tl.cfg_of(wl)
+    p = synth.make_params(wl)
+    x = synth.make_tokens(wl)["x"].reshape(-1, wl.d)
+    ntok, d, dk = x.shape[0], wl.d, wl.dk
+    g = torch.Generator().manual_seed(13)
+    dqw, dqr, dvv = torch.randn(ntok, dk, generator=g), torch.randn(ntok, dk, generator=g), \
+        torch.randn(ntok, d, generator=g)
+    dx = torch.empty(ntok, d, device="cuda")
+    dWqw = torch.empty(d, dk, device="cuda")
+    dWqr = torch.empty_like(dWqw)
+    dWv = torch.empty(d, d, device="cuda")
+    ws = sdm.alloc_workspace(sdm.project_backward_workspace_bytes(cfg, ntok))
+    sdm.sdm_project_backward(cfg, tl.to_dev(p), x.cuda(), dqw.cuda(), dqr.cuda(), dvv.cuda(), dx,
+                             dWqw, dWqr, dWv, ws)
+    torch.cuda.synchronize()
+    ref = oracle.project_backward(x, p["W_qw"], p["W_qr"], p["W_v"], dqw.numpy(), dqr.numpy(),
+                                  dvv.numpy())
+    for got, want in zip((dx, dWqw, dWqr, dWv), ref):
+        assert rel_err(got.cpu().numpy(), want) <= 1e-5, name
+
+
+@pytest.mark.parametrize("name,tol", [("tiny-f32", 1e-4), ("w64-small", 2e-2)])
+def test_layer_backward_chain_matches_oracle(name, tol):
+    """The whole layer's gradients: scan backward -> addressing backward -> projection
+    backward on the GPU, against the same chain of oracle gradients (each oracle step
+    fed the oracle's own upstream gradients)."""
+    wl = SMALL[name]
+    cfg = tl.cfg_of(wl)
+    p = synth.make_params(wl)
+    tok = synth.make_tokens(wl)
+    out = tl.run_staged(wl, p, tok)
+    B, T, d, N, W, dk, n = wl.B, wl.T, wl.d, wl.N, wl.W, wl.dk, wl.n
+    ntok = B * T
+    idx, wsel, v = out["idx"], out["wsel"], out["v"]
+    al, be = out["alpha"].reshape(-1), out["beta"].reshape(-1)
+    dt = wl.torch_dtype
+    pd = tl.to_dev(p)
+    banks = torch.empty(B, N, d, dtype=dt, device="cuda")
+    sdm.sdm_init_bank(cfg, pd["M0"], banks)
+    y = torch.empty(ntok, d, device="cuda")
+    tape = torch.empty(ntok, W, d, dtype=dt, device="cuda")
+    ws = sdm.alloc_workspace(sdm.scan_workspace_bytes(cfg, B, T))
+    st = sdm.new_status()
+    sdm.sdm_scan_prepare(cfg, idx, B, T, ws, st)
+    sdm.sdm_scan_run_train(cfg, idx, wsel, v, al, be, banks, y, B, T, ws, tape, st)
+    dy = torch.randn(ntok, d, generator=torch.Generator().manual_seed(17))
+    dbank = torch.zeros(B, N, d, device="cuda")
+    dv = torch.empty(ntok, d, device="cuda")
+    dal = torch.empty(ntok, device="cuda")
+    dbe = torch.empty(ntok, device="cuda")
+    dws = torch.empty(ntok, 2, W, device="cuda")
+    sdm.sdm_scan_backward(cfg, idx, wsel, v, al, be, tape, banks, dy.cuda(), dbank, dv, dal, dbe,
+                          dws, B, T, sdm.alloc_workspace(sdm.scan_backward_workspace_bytes(cfg, B, T)))
+    dq_w = torch.empty(ntok, dk, device="cuda")
+    dq_r = torch.empty_like(dq_w)
+    dK1 = torch.empty(n, dk // 2, device="cuda")
+    dK2 = torch.empty_like(dK1)
+    sdm.sdm_address_backward(cfg, pd["K1"], pd["K2"], out["q_w"], out["q_r"], idx, wsel, dws, dq_w,
+                             dq_r, dK1, dK2,
+                             sdm.alloc_workspace(sdm.address_backward_workspace_bytes(cfg, ntok)))
+    dx = torch.empty(ntok, d, device="cuda")
+    dW = [torch.empty(d, dk, device="cuda"), torch.empty(d, dk, device="cuda"),
+          torch.empty(d, d, device="cuda")]
+    x = tok["x"].reshape(ntok, d)
+    sdm.sdm_project_backward(cfg, pd, x.cuda(), dq_w, dq_r, dv, dx, *dW,
+                             sdm.alloc_workspace(sdm.project_backward_workspace_bytes(cfg, ntok)))
+    torch.cuda.synchronize()
+    assert sdm.read_status(st) == 0
+    # the oracle chain
+    idx_h, w_h = idx.cpu().numpy(), wsel.cpu().numpy().astype(np.float64)
+    type_ = oracle.BF16 if wl.dtype == "bf16" else oracle.F32
+    dvr = np.zeros((ntok, d))
+    dwr = np.zeros((ntok, 2, W))
+    for b in range(B):
+        sl = slice(b * T, (b + 1) * T)
+        ref = oracle.scan_backward(oracle.to_f64(p["M0"]), v[sl].cpu(), al[sl].cpu().numpy(),
+                                   be[sl].cpu().numpy(), idx_h[sl, 0], w_h[sl, 0], idx_h[sl, 1],
+                                   w_h[sl, 1], dy[sl].numpy(), None, type_=type_)
+        dvr[sl], dwr[sl, 0], dwr[sl, 1] = ref["dv"], ref["dk"], ref["dr"]
+    dqr_ = []
+    dK1r = np.zeros((n, dk // 2))
+    dK2r = np.zeros((n, dk // 2))
+    for kind, q in ((0, out["q_w"]), (1, out["q_r"])):
+        _, dq, k1, k2 = oracle.address_backward(q.cpu(), p["K1"], p["K2"], idx_h[:, kind],
+                                                dwr[:, kind])
+        dqr_.append(dq)
+        dK1r += k1
+        dK2r += k2
+    dxr, *dWr = oracle.project_backward(x, p["W_qw"], p["W_qr"], p["W_v"], dqr_[0], dqr_[1], dvr)
+    checks = [("dK1", dK1, dK1r), ("dK2", dK2, dK2r), ("dx", dx, dxr)] + \
+        [("dW%d" % i, got, want) for i, (got, want) in enumerate(zip(dW, dWr))]
+    for what, got, want in checks:
+        e = rel_err(got.cpu().numpy(), want)
+        assert e <= tol, (name, what, e)

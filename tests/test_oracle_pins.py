@@ -574,3 +574,20 @@ def test_address_backward_matches_finite_differences():
             args[which].reshape(-1)[e_] -= 2 * hh
             fd = (up - loss(*args)) / (2 * hh)
             assert abs(fd - grad.reshape(-1)[e_]) < 1e-7, (which, e_)
+
+
+def test_project_backward_is_autograd_of_the_projections():
+    import torch
+    rng = np.random.default_rng(51)
+    ntok, d, dk = 5, 6, 4
+    x = rng.normal(size=(ntok, d))
+    Ws = [rng.normal(size=(d, dk)), rng.normal(size=(d, dk)), rng.normal(size=(d, d))]
+    douts = [rng.normal(size=(ntok, dk)), rng.normal(size=(ntok, dk)), rng.normal(size=(ntok, d))]
+    xt = torch.tensor(x, requires_grad=True)
+    Wt = [torch.tensor(w, requires_grad=True) for w in Ws]
+    loss = sum(((xt @ w) * torch.tensor(g)).sum() for w, g in zip(Wt, douts))
+    loss.backward()
+    dx, dW1, dW2, dW3 = oracle.project_backward(x, *Ws, *douts)
+    np.testing.assert_allclose(dx, xt.grad.numpy(), atol=1e-12)
+    for got, w in zip((dW1, dW2, dW3), Wt):
+        np.testing.assert_allclose(got, w.grad.numpy(), atol=1e-12)
