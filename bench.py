@@ -377,11 +377,45 @@ def gpu_arm(args, world, rank):
         if sdm.read_status(st) != 0:
             raise RuntimeError("device status during the training pair")
         fwd_ms, bwd_ms = te[0].elapsed_time(te[1]), te[2].elapsed_time(te[3])
+        # the rest of the layer's gradients: addressing (dq, dK) and projections (dx, dW)
+        dq_w = torch.empty(ntok, wl.dk, device=dev)
+        dq_r = torch.empty_like(dq_w)
+        dK1 = torch.empty(wl.n, wl.dk // 2, device=dev)
+        dK2 = torch.empty_like(dK1)
+        dx = torch.empty(ntok, d, device=dev)
+        dW = [torch.empty(d, wl.dk, device=dev), torch.empty(d, wl.dk, device=dev),
+              torch.empty(d, d, device=dev)]
+        wsa_b = sdm.alloc_workspace(sdm.address_backward_workspace_bytes(cfg, ntok))
+        wsp_b = sdm.alloc_workspace(sdm.project_backward_workspace_bytes(cfg, ntok))
+        xb = x.reshape(ntok, d)
+
+        def front_bwd(e=None):
+            if e is not None:
+                e[0].record(stream)
+            sdm.sdm_address_backward(cfg, p["K1"], p["K2"], q_w, q_r, idx, wsel, dws, dq_w, dq_r,
+                                     dK1, dK2, wsa_b)
+            if e is not None:
+                e[1].record(stream)
+            sdm.sdm_project_backward(cfg, p, xb, dq_w, dq_r, dv, dx, *dW, wsp_b)
+            if e is not None:
+                e[2].record(stream)
+
+        front_bwd()
+        fe = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        front_bwd(fe)
+        torch.cuda.synchronize()
+        addr_bwd_ms, proj_bwd_ms = fe[0].elapsed_time(fe[1]), fe[1].elapsed_time(fe[2])
+        del dq_w, dq_r, dK1, dK2, dx, dW, wsa_b, wsp_b
         res["training"] = {
             "what": "scan forward recording the tape (pre-write slot values), then the backward "
-                    "of the recurrence; bf16 tape and banks, fp32 gradients",
+                    "of the recurrence, the addressing and the projections; bf16 tape and banks, "
+                    "fp32 gradients",
             "forward_with_tape_ms": round(fwd_ms, 3), "backward_ms": round(bwd_ms, 3),
             "backward_tokens_per_s": round(ntok / (bwd_ms / 1e3), 1),
+            "address_backward_ms": round(addr_bwd_ms, 3),
+            "project_backward_ms": round(proj_bwd_ms, 3),
+            "layer_backward_tokens_per_s": round(
+                ntok / ((bwd_ms + addr_bwd_ms + proj_bwd_ms) / 1e3), 1),
             "tape_bytes": tape.numel() * 2,
             "kernel": "scan_bwd_kernel: one block per (sequence, 64 rows), reverse token order"}
         del tape, dy, dbank, dv, dal, dbe, dws, wsb
