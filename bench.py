@@ -421,35 +421,59 @@ def gpu_arm(args, world, rank):
         del tape, dy, dbank, dv, dal, dbe, dws, wsb
         torch.cuda.empty_cache()
 
-    # ---- e2e: the one-call public API with host buffers
+    # ---- e2e: the one-call public API with host buffers. Every step copies its inputs
+    # in from pinned host memory, runs sdm_prefill_m0 and copies y back out; the copies
+    # run on their own streams (the copy engines), double-buffered, so that step i+1's
+    # inputs come in and step i-1's y goes out while step i computes.
     x_h = tok_cpu["x"].pin_memory()
     a_h = tok_cpu["alpha"].pin_memory()
     b_h = tok_cpu["beta"].pin_memory()
     y_h = torch.empty(B, T, d, dtype=torch.float32).pin_memory()
     ws_p = sdm.alloc_workspace(sdm.prefill_m0_workspace_bytes(cfg, B, T))
-    x_d = torch.empty_like(x)
-    a_d = torch.empty_like(alpha)
-    b_d = torch.empty_like(beta)
-    y_d = torch.empty(B, T, d, dtype=torch.float32, device=dev)
+    x_d = [torch.empty_like(x) for _ in range(2)]
+    a_d = [torch.empty_like(alpha) for _ in range(2)]
+    b_d = [torch.empty_like(beta) for _ in range(2)]
+    y_d = [torch.empty(B, T, d, dtype=torch.float32, device=dev) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]      # step's inputs on the device
+    ev_done = [torch.cuda.Event() for _ in range(2)]    # step computed (inputs free, y ready)
+    ev_out = [torch.cuda.Event() for _ in range(2)]     # step's y copied out (y buffer free)
+    used = [False, False]
 
-    def e2e_step():
-        x_d.copy_(x_h, non_blocking=True)
-        a_d.copy_(a_h, non_blocking=True)
-        b_d.copy_(b_h, non_blocking=True)
-        sdm.sdm_prefill_m0(cfg, p, p["M0"], x_d, a_d, b_d, banks, y_d, ws_p, st)
-        y_h.copy_(y_d, non_blocking=True)
+    def e2e_step(i):
+        j = i & 1
+        with torch.cuda.stream(s_in):
+            if used[j]:
+                s_in.wait_event(ev_done[j])                  # step i-2 has read these inputs
+            x_d[j].copy_(x_h, non_blocking=True)
+            a_d[j].copy_(a_h, non_blocking=True)
+            b_d[j].copy_(b_h, non_blocking=True)
+            ev_in[j].record(s_in)
+        stream.wait_event(ev_in[j])
+        if used[j]:
+            stream.wait_event(ev_out[j])                     # step i-2's y has been copied out
+        sdm.sdm_prefill_m0(cfg, p, p["M0"], x_d[j], a_d[j], b_d[j], banks, y_d[j], ws_p, st)
+        ev_done[j].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[j])
+            y_h.copy_(y_d[j], non_blocking=True)
+            ev_out[j].record(s_out)
+        used[j] = True
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+    for i in range(max(2, args.warmup)):
+        e2e_step(i)
     torch.cuda.synchronize()
-    n_e2e = max(3, args.steps // 5)
+    # the pipeline's fill (first copy in) and drain (last copy out) are timed too
+    n_e2e = max(10, args.steps // 2)
     barrier(world)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(n_e2e):
-        e2e_step()
+    s_in.wait_event(e0)
+    for i in range(n_e2e):
+        e2e_step(i)
+    stream.wait_stream(s_out)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(world, e0.elapsed_time(e1))
@@ -459,7 +483,9 @@ def gpu_arm(args, world, rank):
     d2h = y_h.numel() * 4
     res["e2e"] = {"value": round(ntok * world * n_e2e / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
-                  "ms_per_step": round(e2e_ms / n_e2e, 4)}
+                  "ms_per_step": round(e2e_ms / n_e2e, 4),
+                  "api": "sdm_prefill_m0 per step; copies on two side streams, double-buffered, "
+                         "overlapping the neighbouring steps' compute"}
     del ws_p, x_d, y_d
 
     if not args.no_decode:
