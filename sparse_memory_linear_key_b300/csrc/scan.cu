@@ -269,12 +269,36 @@ __device__ __forceinline__ void fetch_ahead(const ScanArgs& a, unsigned long lon
         if (j < W) {
             n.wid[jj] = __ldg(a.idx + tok * 2 * W + j);
             n.rid[jj] = __ldg(a.idx + tok * 2 * W + W + j);
-            n.wc[jj] = __ldg(a.codes + tok * 2 * W + j);
-            n.rc[jj] = __ldg(a.codes + tok * 2 * W + W + j);
+            n.wc[jj] = a.T > 1 ? __ldg(a.codes + tok * 2 * W + j) : kNoFwd;
+            n.rc[jj] = a.T > 1 ? __ldg(a.codes + tok * 2 * W + W + j) : kNoFwd;
         } else {
             n.wid[jj] = n.rid[jj] = -1;
             n.wc[jj] = n.rc[jj] = kNoFwd;
         }
+    }
+    if (a.T == 1) {
+        // one token a sequence (a decode step): no earlier writer exists, and a read's only
+        // possible writer is its own token -- matched here instead of by the codes kernel
+        int pos[JW];
+#pragma unroll
+        for (int jj = 0; jj < JW; ++jj)
+            pos[jj] = -1;
+        for (int i = 0; i < W; ++i) {
+            int src = n.wid[0];
+#pragma unroll
+            for (int jj = 1; jj < JW; ++jj)
+                if ((i >> 5) == jj)
+                    src = n.wid[jj];
+            const int wv = __shfl_sync(0xFFFFFFFFu, src, i & 31);
+#pragma unroll
+            for (int jj = 0; jj < JW; ++jj)
+                if (pos[jj] < 0 && wv >= 0 && wv == n.rid[jj])
+                    pos[jj] = i;
+        }
+#pragma unroll
+        for (int jj = 0; jj < JW; ++jj)
+            if (pos[jj] >= 0 && n.rid[jj] < a.N)
+                n.rc[jj] = (uint16_t)pos[jj];   // dt = 0, position pos
     }
     // M0 mode: the first writer of each referenced slot in this sequence
 #pragma unroll
@@ -292,11 +316,13 @@ __device__ __forceinline__ void fetch_ahead(const ScanArgs& a, unsigned long lon
         n.alpha = __ldg(a.alpha + tok);
         n.beta = __ldg(a.beta + tok);
         const size_t BT = (size_t)a.B * a.T;
-        // without the ring, nothing is handed over and every store is needed
-        n.fwdmask = a.ring != nullptr ? __ldg(a.masks + tok) : 0ull;
-        n.deadmask = a.ring != nullptr ? __ldg(a.masks + BT + tok) : 0ull;
-        n.war0 = __ldg(a.masks + 2 * BT + 2 * tok);
-        n.war1 = __ldg(a.masks + 2 * BT + 2 * tok + 1);
+        // without the ring, nothing is handed over and every store is needed; with one
+        // token a sequence nothing else references this token's slots
+        const bool many = a.T > 1;
+        n.fwdmask = many && a.ring != nullptr ? __ldg(a.masks + tok) : 0ull;
+        n.deadmask = many && a.ring != nullptr ? __ldg(a.masks + BT + tok) : 0ull;
+        n.war0 = many ? __ldg(a.masks + 2 * BT + 2 * tok) : 0ull;
+        n.war1 = many ? __ldg(a.masks + 2 * BT + 2 * tok + 1) : 0ull;
     }
 }
 

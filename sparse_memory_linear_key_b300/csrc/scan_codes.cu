@@ -162,49 +162,6 @@ __global__ void __launch_bounds__(kCodeThreads) codes_kernel(const int32_t* __re
     }
 }
 
-// One token per sequence (a decode step): no earlier token exists, so every write code
-// is "no writer" and a read's only possible writer is its own token (dt = 0). One warp
-// per token matches the read set against the write set; the masks are all zero.
-__global__ void __launch_bounds__(256) codes_single_kernel(const int32_t* __restrict__ idx, int B,
-                                                           int W, int N, uint16_t* __restrict__ codes,
-                                                           unsigned long long* __restrict__ masks,
-                                                           int* status)
-{
-    const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (b >= B)
-        return;
-    const int32_t* wr = idx + (size_t)b * 2 * W;
-    const int32_t* rd = wr + W;
-    uint16_t* cw = codes + (size_t)b * 2 * W;
-    uint16_t* cr = cw + W;
-    // the write set in registers (lane l holds positions l and l + 32), read set likewise
-    const int32_t w0 = lane < W ? __ldg(wr + lane) : -1;
-    const int32_t w1 = lane + 32 < W ? __ldg(wr + lane + 32) : -1;
-    const int32_t r0 = lane < W ? __ldg(rd + lane) : -1;
-    const int32_t r1 = lane + 32 < W ? __ldg(rd + lane + 32) : -1;
-    int p0 = -1, p1 = -1;
-    for (int i = 0; i < W; ++i) {
-        const int32_t wv = __shfl_sync(0xFFFFFFFFu, i < 32 ? w0 : w1, i & 31);
-        if (wv == r0 && p0 < 0)
-            p0 = i;
-        if (wv == r1 && p1 < 0)
-            p1 = i;
-    }
-    if ((lane < W && (w0 < 0 || w0 >= N)) || (lane + 32 < W && (w1 < 0 || w1 >= N)))
-        report(status, SDM_ERANGE);
-    if (lane < W) {
-        cw[lane] = kNoFwd;
-        cr[lane] = (r0 >= 0 && r0 < N && p0 >= 0) ? (uint16_t)p0 : kNoFwd;
-    }
-    if (lane + 32 < W) {
-        cw[lane + 32] = kNoFwd;
-        cr[lane + 32] = (r1 >= 0 && r1 < N && p1 >= 0) ? (uint16_t)p1 : kNoFwd;
-    }
-    if (lane < 4)
-        masks[(size_t)lane * B + b] = 0ull;   // the 4*B mask words (B*T = B), all zero
-}
-
 }  // namespace
 
 cudaError_t launch_scan_codes(const sdm_cfg& c, const int32_t* idx, int B, int T, int win,
@@ -213,11 +170,8 @@ cudaError_t launch_scan_codes(const sdm_cfg& c, const int32_t* idx, int B, int T
 {
     if (B <= 0 || T <= 0)
         return cudaSuccess;
-    if (T == 1) {
-        codes_single_kernel<<<(B + 7) / 8, 256, 0, s>>>(idx, B, c.w, c.n_sub * c.n_sub, codes, masks,
-                                                         status);
-        return cudaGetLastError();
-    }
+    if (T == 1)   // one token a sequence: the scan matches reads to own writes itself
+        return cudaSuccess;
     // masks: fwdmask [B*T], deadmask [B*T], warmask [B*T][2], all cleared first
     cudaError_t e = cudaMemsetAsync(masks, 0, (size_t)B * T * 4 * sizeof(unsigned long long), s);
     if (e != cudaSuccess)

@@ -214,8 +214,10 @@ static int scan_impl(const sdm_cfg& c, const int32_t* idx, const float* wsel, co
 {
     const ScanWs L = scan_ws_layout(c, B, T);
     char* base = (char*)ws;
-    cudaError_t e = launch_scan_codes(c, idx, B, T, L.win, (uint16_t*)(base + L.codes),
-                                      (unsigned long long*)(base + L.masks), dev_status, s);
+    // one token a sequence: the scan matches a token's reads with its writes itself
+    cudaError_t e = T > 1 ? launch_scan_codes(c, idx, B, T, L.win, (uint16_t*)(base + L.codes),
+                                              (unsigned long long*)(base + L.masks), dev_status, s)
+                          : cudaSuccess;
     // v comes from a projection forked off the stream: the scan is its first reader
     if (v_ready != nullptr && cudaStreamWaitEvent(s, v_ready, 0) != cudaSuccess)
         return SDM_ECUDA;
