@@ -559,7 +559,7 @@ def decode_arm(sdm, args, world):
            "unit": "tokens/s", "steps": S, "us_per_step": round(ms * 1e3 / S, 2),
            "state_hbm_gbs": round(per_step_bytes * S / (ms / 1e3) / 1e9, 1),
            "eager_us_per_step": round(eager_ms * 1e3 / S, 2),
-           "note": "512 sdm_decode_step calls (projections, addressing, codes, scan) "
+           "note": "512 sdm_decode_step calls (projections, addressing, scan) "
                    "captured in one CUDA graph; eager = one host call per step"}
     del g
     del banks, p, xd, y
