@@ -53,6 +53,10 @@ def parse():
                     help="tokens per sequence instead of the workload's (for profiling a "
                          "small case of the same kernels)")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--only-decode", action="store_true",
+                    help="run the decode arm alone (for profiling it)")
+    ap.add_argument("--decode-steps", type=int, default=None,
+                    help="decode steps instead of the workload's 512 (for profiling)")
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences instead of the workload's (for profiling a small case)")
     return ap.parse_args()
@@ -518,8 +522,8 @@ def decode_arm(sdm, args, world):
     xd = dec["x"].to(dev)
     ad = dec["alpha"].to(dev)
     bd = dec["beta"].to(dev)
-    y = torch.empty(wl.decode_steps, B, wl.d, device=dev)
-    S = wl.decode_steps
+    S = args.decode_steps if args.decode_steps else wl.decode_steps
+    y = torch.empty(S, B, wl.d, device=dev)
 
     def steps():
         for s_ in range(S):
@@ -559,8 +563,8 @@ def decode_arm(sdm, args, world):
            "unit": "tokens/s", "steps": S, "us_per_step": round(ms * 1e3 / S, 2),
            "state_hbm_gbs": round(per_step_bytes * S / (ms / 1e3) / 1e9, 1),
            "eager_us_per_step": round(eager_ms * 1e3 / S, 2),
-           "note": "512 sdm_decode_step calls (projections, addressing, scan) "
-                   "captured in one CUDA graph; eager = one host call per step"}
+           "note": "%d sdm_decode_step calls (projections, addressing, scan) "
+                   "captured in one CUDA graph; eager = one host call per step" % S}
     del g
     del banks, p, xd, y
     torch.cuda.empty_cache()
@@ -632,6 +636,15 @@ def main():
         res = reference_arm(args, world, rank)
         if res is not None:
             print(json.dumps(res), flush=True)
+        return
+    if args.only_decode:
+        import sparse_memory_linear_key_b300 as sdm
+        from sparse_memory_linear_key_b300 import build
+        build.build()
+        res = {"metric": METRIC, "decode": decode_arm(sdm, args, world)}
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        barrier(world)
         return
     res, p_cpu, tok_cpu = gpu_arm(args, world, rank)
     if rank == 0:
