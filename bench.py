@@ -410,6 +410,13 @@ def gpu_arm(args, world, rank):
         torch.cuda.synchronize()
         addr_bwd_ms, proj_bwd_ms = fe[0].elapsed_time(fe[1]), fe[1].elapsed_time(fe[2])
         del dq_w, dq_r, dK1, dK2, dx, dW, wsa_b, wsp_b
+        # the backward walk's algorithmic bytes per token: at each read slot the bank row
+        # (bf16) and the gradient row read and written (fp32); at each write slot the
+        # gradient row read and written, the tape row read and the bank row restored;
+        # dy and dv (fp32) and v (bf16)
+        bwd_tok = wl.W * d * (2 + 4 + 4) + wl.W * d * (4 + 4 + 2 + 2) + d * (4 + 4 + 2)
+        peak_b, _ = measured_peaks()
+        bwd_gbs = bwd_tok * ntok / (bwd_ms / 1e3) / 1e9
         res["training"] = {
             "what": "scan forward recording the tape (pre-write slot values), then the backward "
                     "of the recurrence, the addressing and the projections; bf16 tape and banks, "
@@ -421,7 +428,13 @@ def gpu_arm(args, world, rank):
             "layer_backward_tokens_per_s": round(
                 ntok / ((bwd_ms + addr_bwd_ms + proj_bwd_ms) / 1e3), 1),
             "tape_bytes": tape.numel() * 2,
-            "kernel": "scan_bwd_kernel: one block per (sequence, 64 rows), reverse token order"}
+            "backward_roofline": {"bound": "hbm", "bytes_per_token": bwd_tok,
+                                  "achieved": round(bwd_gbs, 1), "peak": peak_b, "unit": "GB/s",
+                                  "frac": round(bwd_gbs / peak_b, 4),
+                                  "timed": "the whole sdm_scan_backward call (match table, "
+                                           "walk, partial-sum reduction)"},
+            "kernel": "scan_bwd_kernel: one block per (sequence, 64 rows), reverse token order, "
+                      "each token's gathers issued one token ahead"}
         del tape, dy, dbank, dv, dal, dbe, dws, wsb
         torch.cuda.empty_cache()
 

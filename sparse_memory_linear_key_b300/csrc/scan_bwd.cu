@@ -20,6 +20,18 @@
 // reverse; 4 groups of 64 threads share the W slots of a token (slot j in group j % 4).
 // Sums over rows (dk, dr, dalpha, dbeta) are per-block partials, summed over the blocks
 // of a sequence by a second kernel.
+//
+// Latency: a token's gathers (G and M at its read slots, G at its write slots, its tape
+// rows, dy and v) are 16-byte cp.async copies into a shared-memory stage, issued one
+// token ahead while the token before it in the walk is processed; barriers do not wait
+// for them, so the gathers of one token overlap the arithmetic of the other. A slot that
+// token then writes is gathered stale. A per-token match table, built by a small kernel
+// beforehand, names for each slot of token t the position in token t+1 that touched it
+// last; token t takes that position's final G value from shared memory instead (token
+// t+1 leaves all of its final values there), and gathers M from token t+1's tape row,
+// which is the value the restore puts back. The same table names, for a write slot that
+// is also read by its own token, the read position, so the read's addition r_j dy is
+// applied in registers and no barrier separates the read from the write.
 #include "sdm_common.cuh"
 #include "sdm_internal.h"
 
@@ -30,11 +42,8 @@ namespace {
 constexpr int kBRows = 64;
 constexpr int kBThreads = 256;
 constexpr int kBGroups = kBThreads / kBRows;
+constexpr int kMetaRing = 4;   // token t, t-1 (gathers) and t-2 (being published)
 
-__device__ __forceinline__ float ld_state(const bf16* p) { return __bfloat162float(*p); }
-__device__ __forceinline__ float ld_state(const float* p) { return *p; }
-__device__ __forceinline__ float ld_io(const bf16* p) { return __bfloat162float(__ldg(p)); }
-__device__ __forceinline__ float ld_io(const float* p) { return __ldg(p); }
 
 __device__ __forceinline__ float warp_sum(float x)
 {
@@ -44,174 +53,312 @@ __device__ __forceinline__ float warp_sum(float x)
     return x;
 }
 
+// Sums each of the V values of every lane over the warp with V - 1 + log2(32 / V)
+// exchanges: each step halves the values a lane keeps, trading the other half with the
+// lane `o` away. Lane L ends with the sum of value L / (32 / V).
+template <int V>
+__device__ __forceinline__ float warp_sum_many(float (&x)[V], int lane)
+{
+    static_assert(V >= 1 && V <= 32 && (V & (V - 1)) == 0, "a power of two up to 32");
+#pragma unroll
+    for (int h = V / 2; h >= 1; h >>= 1) {
+        const int o = 32 * h / V;
+        const bool hi = (lane & o) != 0;
+#pragma unroll
+        for (int k = 0; k < h; ++k) {
+            const float send = hi ? x[k] : x[k + h];
+            const float keep = hi ? x[k + h] : x[k];
+            x[k] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+        }
+    }
+    float s = x[0];
+#pragma unroll
+    for (int o = 16 / V; o >= 1; o >>= 1)
+        s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    return s;
+}
+
+// match [B*T][4W] bytes, per token t (positions: write j = j, read j = W + j):
+//   [0, 2W)  the position in token t+1 of the same slot (its write position if it has
+//            both), or -1 (no such slot, an invalid slot, or t the last token);
+//   [2W, 3W) for write position j, the read position of the same slot in token t, or -1;
+//   [3W, 4W) for read position j, 1 if token t also writes that slot, else 0.
+// Slots within one kind of one token are distinct (a top-W selection).
+template <int W>
+__global__ void __launch_bounds__(2 * W) bwd_match_kernel(const int32_t* __restrict__ idx, int T,
+                                                          int N, int8_t* __restrict__ match)
+{
+    __shared__ int cs[2 * W], ns[2 * W];
+    const int64_t tok = blockIdx.x;
+    const int t = (int)(tok % T);
+    const int p = threadIdx.x;
+    int s = __ldg(idx + tok * 2 * W + p);
+    if (s < 0 || s >= N)
+        s = -1;
+    cs[p] = s;
+    int q = -2;
+    if (t + 1 < T) {
+        q = __ldg(idx + (tok + 1) * 2 * W + p);
+        if (q < 0 || q >= N)
+            q = -2;
+    }
+    ns[p] = q;
+    __syncthreads();
+    int src = -1;
+    if (s >= 0)
+        for (int k = 0; k < 2 * W; ++k)
+            if (ns[k] == s) {
+                src = k;
+                break;
+            }
+    int8_t* m = match + tok * 4 * W;
+    m[p] = (int8_t)src;
+    int other = -1;
+    const int base = p < W ? W : 0;   // a write position looks among the reads, and back
+    if (s >= 0)
+        for (int k = 0; k < W; ++k)
+            if (cs[base + k] == s) {
+                other = k;
+                break;
+            }
+    if (p < W)
+        m[2 * W + p] = (int8_t)other;
+    else
+        m[3 * W + p - W] = (int8_t)(other >= 0 ? 1 : 0);
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+__device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f(float x) { return x; }
+
+// Shared memory of the walk. A token's gathers land in stage t & 1; its metadata in
+// ring entry t % 4 (in flight two tokens ahead, read by the gathers issued one token
+// ahead and by the token itself).
+template <typename S, int W>
+struct BwdStage {
+    float g[2 * W][kBRows];     // G at the write positions, then at the read positions
+    S st[2 * W][kBRows];        // tape rows (write positions), then bank rows (read positions)
+    float dy[kBRows];
+    S v[kBRows];
+};
+template <int W>
+struct BwdMeta {
+    int sid[2 * W];             // slot ids: write positions, then read positions
+    float sw[2 * W];            // their weights
+    int8_t mt[4 * W];           // the match bytes of the token
+    float gate[4];              // alpha, beta
+};
+template <typename S, int W>
+struct BwdSmem {
+    BwdStage<S, W> stage[2];
+    BwdMeta<W> meta[kMetaRing];
+    float xg[2 * W][kBRows];    // the final G values of the previous token, by its position
+    float red[2][kBGroups][kBRows];
+    float acc[2][2 * W + 2];    // partial sums of token t in entry t & 1
+};
+
 // partials: [nblk][B*T][2W + 2] = dk[W], dr[W], dalpha, dbeta of this block's rows
 template <typename S, int W>
-__global__ void __launch_bounds__(kBThreads) scan_bwd_kernel(
-    const int32_t* __restrict__ idx, const float* __restrict__ wsel, const S* __restrict__ v,
-    const float* __restrict__ alpha, const float* __restrict__ beta, const S* __restrict__ tape,
-    S* __restrict__ banks, const float* __restrict__ dy, float* __restrict__ dbank,
-    float* __restrict__ dv, float* __restrict__ part, int B, int T, int d, int N)
+__global__ void __launch_bounds__(kBThreads, 1) scan_bwd_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ wsel,
+    const int8_t* __restrict__ match, const S* __restrict__ v, const float* __restrict__ alpha,
+    const float* __restrict__ beta, const S* __restrict__ tape, S* __restrict__ banks,
+    const float* __restrict__ dy, float* __restrict__ dbank, float* __restrict__ dv,
+    float* __restrict__ part, int B, int T, int d, int N)
 {
     constexpr int SPG = W / kBGroups;         // slots a thread: j = grp + 4 i
     constexpr int P = 2 * W + 2;
-    // Token t's slot ids, weights and gates sit in buffer t & 1 (written during token
-    // t + 1), and so do its partial sums (cleared during token t + 1, after every thread
-    // has written out token t + 2's).
-    static_assert(2 * W <= kBThreads && P <= kBThreads, "one metadata entry a thread");
-    __shared__ int sid[2][2][W];
-    __shared__ float sw[2][2][W];
-    __shared__ float gate[2][2];
-    __shared__ float red[2][kBGroups][kBRows];
-    __shared__ float acc[2][P];
+    constexpr int GCH = kBRows * 4 / 16;      // 16-byte chunks of a G row segment
+    constexpr int SCH = kBRows * (int)sizeof(S) / 16;
+    static_assert(P <= kBThreads, "one partial sum a thread");
+    static_assert(SPG >= 1 && 32 % SPG == 0, "whole lanes per reduced value");
+    static_assert(W / 2 <= 64 && W / 4 <= 64, "metadata copies fit their thread ranges");
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    BwdSmem<S, W>& sm = *reinterpret_cast<BwdSmem<S, W>*>(smem_raw);
     const int b = blockIdx.y;
-    const int r = threadIdx.x % kBRows, grp = threadIdx.x / kBRows;
-    const int row = blockIdx.x * kBRows + r;
-    const bool act = row < d;
-    const int lane = threadIdx.x & 31;
-    const int e = threadIdx.x;                       // metadata entry of this thread
+    const int tid = threadIdx.x;
+    const int r = tid % kBRows, grp = tid / kBRows;
+    const int row0 = blockIdx.x * kBRows;
+    const int row = row0 + r;
+    const int nrows = min(kBRows, d - row0);  // a multiple of 16: d is
+    const bool act = r < nrows;
+    const int lane = tid & 31;
     S* bank = banks + (size_t)b * N * d;
     float* G = dbank + (size_t)b * N * d;
     if (T <= 0)
         return;
-    // what a token needs besides the gradient bank, loaded one token ahead
-    int nid = -1;
-    float nw = 0.f, nal = 0.f, nbe = 0.f, ndy = 0.f, nv = 0.f;
-    float nold[SPG];
-    auto prefetch = [&](int64_t tk) {
-        if (e < 2 * W) {
-            nid = __ldg(idx + tk * 2 * W + e);
-            nw = __ldg(wsel + tk * 2 * W + e);
-        }
-        if (e == 0) {
-            nal = __ldg(alpha + tk);
-            nbe = __ldg(beta + tk);
-        }
-        ndy = act ? __ldg(dy + tk * d + row) : 0.f;
-        nv = act ? ld_io(v + tk * d + row) : 0.f;
-#pragma unroll
-        for (int i = 0; i < SPG; ++i)   // tape rows exist for every position, ids aside
-            nold[i] = act ? ld_state(tape + ((size_t)tk * W + grp + kBGroups * i) * d + row) : 0.f;
+    const int64_t tok0 = (int64_t)b * T;
+
+    // token tk's slot ids, weights, match bytes and gates into ring entry mb
+    auto issue_meta = [&](int64_t tk, int mb) {
+        BwdMeta<W>& m = sm.meta[mb];
+        if (tid < W / 2)
+            cp_async16(smem_u32(&m.sid[tid * 4]), idx + tk * 2 * W + tid * 4);
+        else if (tid >= 64 && tid < 64 + W / 2)
+            cp_async16(smem_u32(&m.sw[(tid - 64) * 4]), wsel + tk * 2 * W + (tid - 64) * 4);
+        else if (tid >= 128 && tid < 128 + W / 4)
+            cp_async16(smem_u32(&m.mt[(tid - 128) * 16]), match + tk * 4 * W + (tid - 128) * 16);
+        else if (tid == 192)
+            cp_async4(smem_u32(&m.gate[0]), alpha + tk);
+        else if (tid == 193)
+            cp_async4(smem_u32(&m.gate[1]), beta + tk);
     };
-    auto publish = [&](int buf) {
-        if (e < 2 * W) {
-            sid[buf][e / W][e % W] = nid;
-            sw[buf][e / W][e % W] = nw;
+    // token tk's gathers into stage gb, its metadata in ring entry mb (landed). Issued
+    // before the token after it (tk + 1) stores anything: the slots that token writes
+    // are loaded stale here and replaced from xg when token tk runs.
+    auto issue_gathers = [&](int64_t tk, int mb, int gb) {
+        const BwdMeta<W>& m = sm.meta[mb];
+        BwdStage<S, W>& g = sm.stage[gb];
+        const int gch = nrows * 4 / 16, sch = nrows * (int)sizeof(S) / 16;
+        for (int k = tid; k < 2 * W * GCH; k += kBThreads) {
+            const int p = k / GCH, c = k % GCH;
+            const int s = m.sid[p];
+            if (c < gch && s >= 0 && s < N)
+                cp_async16(smem_u32(&g.g[p][c * 4]), G + (size_t)s * d + row0 + c * 4);
         }
-        if (e == 0) {
-            gate[buf][0] = nal;
-            gate[buf][1] = nbe;
+        for (int k = tid; k < 2 * W * SCH; k += kBThreads) {
+            const int p = k / SCH, c = k % SCH;
+            const int s = m.sid[p];
+            if (c >= sch || s < 0 || s >= N)
+                continue;
+            const int e16 = c * (16 / (int)sizeof(S));
+            const S* src;
+            if (p < W) {
+                src = tape + ((size_t)tk * W + p) * d;   // the pre-write row of the write
+            } else {
+                // the bank after token tk's write: token tk + 1's pre-write row if it
+                // wrote the slot (the value its restore puts back), else the bank row
+                const int q = m.mt[p];
+                src = (q >= 0 && q < W) ? tape + ((size_t)(tk + 1) * W + q) * d : bank + (size_t)s * d;
+            }
+            cp_async16(smem_u32(&g.st[p][e16]), src + row0 + e16);
         }
+        if (tid < nrows / 4)
+            cp_async16(smem_u32(&g.dy[tid * 4]), dy + tk * d + row0 + tid * 4);
+        else if (tid >= 32 && tid - 32 < sch)
+            cp_async16(smem_u32(&g.v[(tid - 32) * (16 / (int)sizeof(S))]),
+                       v + tk * d + row0 + (tid - 32) * (16 / (int)sizeof(S)));
     };
-    prefetch((int64_t)b * T + T - 1);
-    publish((T - 1) & 1);
-    if (e < P) {
-        acc[0][e] = 0.f;
-        acc[1][e] = 0.f;
+
+    issue_meta(tok0 + T - 1, (T - 1) % kMetaRing);
+    if (T >= 2)
+        issue_meta(tok0 + T - 2, (T - 2) % kMetaRing);
+    cp_async_commit();
+    if (tid < P) {
+        sm.acc[0][tid] = 0.f;
+        sm.acc[1][tid] = 0.f;
     }
+    cp_async_wait_all();
     __syncthreads();
+    issue_gathers(tok0 + T - 1, (T - 1) % kMetaRing, (T - 1) & 1);
+    cp_async_commit();
     for (int t = T - 1; t >= 0; --t) {
-        const int64_t tok = (int64_t)b * T + t;
-        const int cb = t & 1;
-        const float dyr = ndy, vr = nv;
-        float old[SPG];
-#pragma unroll
-        for (int i = 0; i < SPG; ++i)
-            old[i] = nold[i];
-        if (t > 0)
-            prefetch(tok - 1);
-        // ---- read: G[R_j] += r_j dy, dr_j = <M[R_j], dy> (M after this token's write).
-        // All loads first, then the updates, then the sums over rows.
-        float mv[SPG], gr[SPG];
-#pragma unroll
-        for (int i = 0; i < SPG; ++i) {
-            const int s = sid[cb][1][grp + kBGroups * i];
-            const bool ok = act && s >= 0 && s < N;
-            mv[i] = ok ? ld_state(bank + (size_t)s * d + row) : 0.f;
-            gr[i] = ok ? G[(size_t)s * d + row] : 0.f;
+        const int64_t tok = tok0 + t;
+        const int mb = t % kMetaRing, cb = t & 1;
+        // token t's gathers and token t - 1's metadata have landed (issued during token
+        // t + 1); token t + 1's xg, partial sums and stores are complete
+        cp_async_wait_all();
+        __syncthreads();
+        if (t + 1 < T && tid < P) {
+            part[((size_t)blockIdx.x * B * T + tok + 1) * P + tid] = sm.acc[cb ^ 1][tid];
+            sm.acc[cb ^ 1][tid] = 0.f;   // token t - 1 adds into it after the next barrier
         }
+        if (t >= 1)
+            issue_gathers(tok - 1, (t - 1) % kMetaRing, cb ^ 1);
+        if (t >= 2)
+            issue_meta(tok - 2, (t - 2) % kMetaRing);
+        cp_async_commit();
+
+        const BwdMeta<W>& m = sm.meta[mb];
+        const BwdStage<S, W>& g = sm.stage[cb];
+        const float dyr = act ? g.dy[r] : 0.f;
+        // ---- this token's values: G from the previous token's final values where it
+        // touched the slot, else as gathered
+        float gw[SPG], gr[SPG], ow[SPG], pr[SPG];
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
             const int j = grp + kBGroups * i;
-            const int s = sid[cb][1][j];
-            if (act && s >= 0 && s < N)
-                G[(size_t)s * d + row] = fmaf(sw[cb][1][j], dyr, gr[i]);
+            const int sw_ = m.sid[j], sr = m.sid[W + j];
+            const bool okw = act && sw_ >= 0 && sw_ < N;
+            const bool okr = act && sr >= 0 && sr < N;
+            const int qw = m.mt[j], qr = m.mt[W + j];
+            gw[i] = okw ? (qw >= 0 ? sm.xg[qw][r] : g.g[j][r]) : 0.f;
+            gr[i] = okr ? (qr >= 0 ? sm.xg[qr][r] : g.g[W + j][r]) : 0.f;
+            ow[i] = okw ? to_f(g.st[j][r]) : 0.f;
+            // ---- read: dr_j = <M[R_j], dy> (M after this token's write), G[R_j] += r_j dy
+            pr[i] = okr ? to_f(g.st[W + j][r]) * dyr : 0.f;
+            if (okr && m.mt[3 * W + j] == 0)   // else the write stores the slot
+                G[(size_t)sr * d + row] = fmaf(m.sw[W + j], dyr, gr[i]);
         }
-#pragma unroll
-        for (int i = 0; i < SPG; ++i) {
-            const float pr = warp_sum(mv[i] * dyr);
-            if (lane == 0)
-                atomicAdd(&acc[cb][W + grp + kBGroups * i], pr);
-        }
-        __syncthreads();   // (A) a slot both read and written: its G update is visible below
-        // every thread has written out token t + 1's partials (before A): clear them for
-        // token t - 1, which starts after barrier C
-        if (e < P)
-            acc[cb ^ 1][e] = 0.f;
-        // ---- write
-        float gj[SPG];
+        // ---- write: G at the write slots after the read's additions
         float gp = 0.f, up = 0.f;
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
             const int j = grp + kBGroups * i;
-            const int s = sid[cb][0][j];
-            const bool ok = act && s >= 0 && s < N;
-            if (!ok)
-                old[i] = 0.f;
-            gj[i] = ok ? G[(size_t)s * d + row] : 0.f;
-            gp = fmaf(sw[cb][0][j], gj[i], gp);
-            up = fmaf(sw[cb][0][j], old[i], up);
+            const int q = m.mt[2 * W + j];
+            if (q >= 0)
+                gw[i] = fmaf(m.sw[W + q], dyr, gw[i]);
+            gp = fmaf(m.sw[j], gw[i], gp);
+            up = fmaf(m.sw[j], ow[i], up);
         }
-        red[0][grp][r] = gp;
-        red[1][grp][r] = up;
-        __syncthreads();   // (B)
-        float g = 0.f, u = 0.f;
+        sm.red[0][grp][r] = gp;
+        sm.red[1][grp][r] = up;
+        {
+            const float sum = warp_sum_many<SPG>(pr, lane);
+            if (lane % (32 / SPG) == 0)
+                atomicAdd(&sm.acc[cb][W + grp + kBGroups * (lane / (32 / SPG))], sum);
+        }
+        __syncthreads();   // red complete; every thread has read xg
+        float gs = 0.f, u = 0.f;
 #pragma unroll
         for (int q = 0; q < kBGroups; ++q) {
-            g += red[0][q][r];
-            u += red[1][q][r];
+            gs += sm.red[0][q][r];
+            u += sm.red[1][q][r];
         }
-        const float al = gate[cb][0], be = gate[cb][1];
-        const float c = vr - al * u;
+        const float al = m.gate[0], be = m.gate[1];
+        const float c = (act ? to_f(g.v[r]) : 0.f) - al * u;
         float pa = 0.f;
         float pk[SPG];
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
             const int j = grp + kBGroups * i;
-            const int s = sid[cb][0][j];
-            const float kj = sw[cb][0][j];
-            pa = fmaf(gj[i], old[i] - be * kj * u, pa);
-            pk[i] = be * gj[i] * c - al * be * g * old[i];
+            const int s = m.sid[j];
+            const float kj = m.sw[j];
+            pa = fmaf(gw[i], ow[i] - be * kj * u, pa);
+            pk[i] = be * gw[i] * c - al * be * gs * ow[i];
+            const float gn = al * (gw[i] - be * kj * gs);
             if (act && s >= 0 && s < N) {
-                G[(size_t)s * d + row] = al * (gj[i] - be * kj * g);
+                G[(size_t)s * d + row] = gn;
                 // the tape value, stored back exactly (a stored value converts to fp32
                 // and back unchanged)
-                bank[(size_t)s * d + row] = S(old[i]);
+                bank[(size_t)s * d + row] = S(ow[i]);
             }
+            sm.xg[j][r] = gn;
+            sm.xg[W + j][r] = fmaf(m.sw[W + j], dyr, gr[i]);
         }
-#pragma unroll
-        for (int i = 0; i < SPG; ++i) {
-            const float q = warp_sum(pk[i]);
-            if (lane == 0)
-                atomicAdd(&acc[cb][grp + kBGroups * i], q);
+        {
+            const float sum = warp_sum_many<SPG>(pk, lane);
+            if (lane % (32 / SPG) == 0)
+                atomicAdd(&sm.acc[cb][grp + kBGroups * (lane / (32 / SPG))], sum);
         }
         pa = warp_sum(pa);
-        const float pb = warp_sum(grp == 0 ? g * c : 0.f);
+        const float pb = warp_sum(grp == 0 ? gs * c : 0.f);
         if (lane == 0) {
-            atomicAdd(&acc[cb][2 * W], pa);
-            atomicAdd(&acc[cb][2 * W + 1], pb);
+            atomicAdd(&sm.acc[cb][2 * W], pa);
+            atomicAdd(&sm.acc[cb][2 * W + 1], pb);
         }
         if (grp == 0 && act)
-            dv[tok * d + row] = be * g;
-        // token t - 1's slot ids, weights and gates into the other buffer (token t + 1
-        // finished with it before barrier A)
-        if (t > 0)
-            publish(cb ^ 1);
-        __syncthreads();   // (C) partial sums complete; token t - 1's metadata visible
-        if (e < P)
-            part[((size_t)blockIdx.x * B * T + tok) * P + e] = acc[cb][e];
-        // red is rewritten after token t - 1's barrier A, which every thread reaches only
-        // after these reads; acc[cb] is cleared only after that barrier too
+            dv[tok * d + row] = be * gs;
+        // red, xg and the stage are rewritten only after the next token's first barrier
     }
+    __syncthreads();
+    if (tid < P)
+        part[((size_t)blockIdx.x * B * T + tok0) * P + tid] = sm.acc[0][tid];
 }
 
 // sums of the per-block partials: dwsel [B*T][2][W] (write weights, then read weights),
@@ -240,24 +387,39 @@ __global__ void __launch_bounds__(256) scan_bwd_reduce(const float* __restrict__
 }
 
 template <typename S, int W>
-cudaError_t launch_bwd_t(const int32_t* idx, const float* wsel, const void* v, const float* alpha,
-                         const float* beta, const void* tape, void* banks, const float* dy,
-                         float* dbank, float* dv, float* part, int B, int T, int d, int N,
-                         cudaStream_t s)
+cudaError_t launch_bwd_t(const int32_t* idx, const float* wsel, int8_t* match, const void* v,
+                         const float* alpha, const float* beta, const void* tape, void* banks,
+                         const float* dy, float* dbank, float* dv, float* part, int B, int T, int d,
+                         int N, cudaStream_t s)
 {
+    bwd_match_kernel<W><<<(unsigned)((int64_t)B * T), 2 * W, 0, s>>>(idx, T, N, match);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
     const dim3 grid((unsigned)((d + kBRows - 1) / kBRows), (unsigned)B);
-    scan_bwd_kernel<S, W><<<grid, kBThreads, 0, s>>>(idx, wsel, (const S*)v, alpha, beta,
+    const size_t smem = sizeof(BwdSmem<S, W>);
+    e = cudaFuncSetAttribute(scan_bwd_kernel<S, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    scan_bwd_kernel<S, W><<<grid, kBThreads, smem, s>>>(idx, wsel, match, (const S*)v, alpha, beta,
                                                      (const S*)tape, (S*)banks, dy, dbank, dv,
                                                      part, B, T, d, N);
     return cudaGetLastError();
+}
+
+// workspace: the per-block partials, then the match table
+size_t part_bytes(const sdm_cfg& c, int B, int T)
+{
+    const size_t nblk = (size_t)(c.d + kBRows - 1) / kBRows;
+    return (nblk * (size_t)B * T * (2 * c.w + 2) * sizeof(float) + 255) / 256 * 256;
 }
 
 }  // namespace
 
 size_t scan_backward_ws_bytes(const sdm_cfg& c, int B, int T)
 {
-    const size_t nblk = (size_t)(c.d + kBRows - 1) / kBRows;
-    return nblk * (size_t)B * T * (2 * c.w + 2) * sizeof(float);
+    return part_bytes(c, B, T) + (size_t)B * T * 4 * c.w;
 }
 
 cudaError_t launch_scan_backward(const sdm_cfg& c, const int32_t* idx, const float* wsel,
@@ -268,25 +430,26 @@ cudaError_t launch_scan_backward(const sdm_cfg& c, const int32_t* idx, const flo
 {
     if (B <= 0 || T <= 0)
         return cudaSuccess;
+    if ((int64_t)B * T > 0x7FFFFFFF)
+        return cudaErrorInvalidValue;
     const int N = c.n_sub * c.n_sub;
     float* part = (float*)ws;
+    int8_t* match = (int8_t*)ws + part_bytes(c, B, T);
     const bool bf = c.dtype == SDM_BF16;
     cudaError_t e;
+#define SDM_BWD(WW)                                                                                \
+    (bf ? launch_bwd_t<bf16, WW>(idx, wsel, match, v, alpha, beta, tape, banks, dy, dbank, dv,     \
+                                 part, B, T, c.d, N, s)                                            \
+        : launch_bwd_t<float, WW>(idx, wsel, match, v, alpha, beta, tape, banks, dy, dbank, dv,    \
+                                  part, B, T, c.d, N, s))
     switch (c.w) {
-    case 8: e = bf ? launch_bwd_t<bf16, 8>(idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, part, B, T, c.d, N, s)
-                   : launch_bwd_t<float, 8>(idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, part, B, T, c.d, N, s);
-        break;
-    case 16: e = bf ? launch_bwd_t<bf16, 16>(idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, part, B, T, c.d, N, s)
-                    : launch_bwd_t<float, 16>(idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, part, B, T, c.d, N, s);
-        break;
-    case 32: e = bf ? launch_bwd_t<bf16, 32>(idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, part, B, T, c.d, N, s)
-                    : launch_bwd_t<float, 32>(idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, part, B, T, c.d, N, s);
-        break;
-    case 64: e = bf ? launch_bwd_t<bf16, 64>(idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, part, B, T, c.d, N, s)
-                    : launch_bwd_t<float, 64>(idx, wsel, v, alpha, beta, tape, banks, dy, dbank, dv, part, B, T, c.d, N, s);
-        break;
+    case 8: e = SDM_BWD(8); break;
+    case 16: e = SDM_BWD(16); break;
+    case 32: e = SDM_BWD(32); break;
+    case 64: e = SDM_BWD(64); break;
     default: return cudaErrorInvalidValue;
     }
+#undef SDM_BWD
     if (e != cudaSuccess)
         return e;
     const int nblk = (c.d + kBRows - 1) / kBRows;

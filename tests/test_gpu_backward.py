@@ -27,21 +27,13 @@ def rel_err(got, want):
     return float(np.abs(np.asarray(got, np.float64) - want).max() / max(np.abs(want).max(), 1e-30))
 
 
-@pytest.mark.parametrize("name,tol", [("tiny-f32", 1e-4), ("ragged-f32", 1e-4),
-                                      ("ragged-bf16", 2e-2), ("w64-small", 2e-2)])
-def test_scan_backward_matches_autograd(name, tol):
-    wl = SMALL[name]
-    cfg = tl.cfg_of(wl)
-    p = synth.make_params(wl)
-    tok = synth.make_tokens(wl)
-    out = tl.run_staged(wl, p, tok)       # the CUDA path's addressing and v
+def _walk_back_and_check(wl, cfg, M0, idx, wsel, v, al, be, tol, name):
+    """Forward with a tape from banks = M0, the backward walk, then every gradient against
+    the oracle's autograd, sequence by sequence."""
     B, T, d, N, W = wl.B, wl.T, wl.d, wl.N, wl.W
-    idx, wsel, v = out["idx"], out["wsel"], out["v"]
-    al, be = out["alpha"].reshape(-1), out["beta"].reshape(-1)
     dt = wl.torch_dtype
-    M0 = p["M0"].cuda()
     banks = torch.empty(B, N, d, dtype=dt, device="cuda")
-    sdm.sdm_init_bank(cfg, M0, banks)
+    sdm.sdm_init_bank(cfg, M0.cuda(), banks)
     banks0 = banks.clone()
     y = torch.empty(B * T, d, device="cuda")
     tape = torch.empty(B * T, W, d, dtype=dt, device="cuda")
@@ -67,7 +59,7 @@ def test_scan_backward_matches_autograd(name, tol):
     type_ = oracle.BF16 if wl.dtype == "bf16" else oracle.F32
     for b in range(B):
         sl = slice(b * T, (b + 1) * T)
-        ref = oracle.scan_backward(oracle.to_f64(p["M0"]), v[sl].cpu(), al[sl].cpu().numpy(),
+        ref = oracle.scan_backward(oracle.to_f64(M0), v[sl].cpu(), al[sl].cpu().numpy(),
                                    be[sl].cpu().numpy(), idx_h[sl, 0], w_h[sl, 0], idx_h[sl, 1],
                                    w_h[sl, 1], dy[sl].numpy(), dMf[b].numpy(), type_=type_)
         checks = [("dM_init", dbank[b].cpu().numpy(), ref["dM_init"]),
@@ -79,6 +71,42 @@ def test_scan_backward_matches_autograd(name, tol):
         for what, got, want in checks:
             e = rel_err(got, want)
             assert e <= tol, (name, b, what, e)
+
+
+@pytest.mark.parametrize("name,tol", [("tiny-f32", 1e-4), ("ragged-f32", 1e-4),
+                                      ("ragged-bf16", 2e-2), ("w64-small", 2e-2)])
+def test_scan_backward_matches_autograd(name, tol):
+    wl = SMALL[name]
+    cfg = tl.cfg_of(wl)
+    p = synth.make_params(wl)
+    tok = synth.make_tokens(wl)
+    out = tl.run_staged(wl, p, tok)       # the CUDA path's addressing and v
+    _walk_back_and_check(wl, cfg, p["M0"], out["idx"], out["wsel"], out["v"],
+                         out["alpha"].reshape(-1), out["beta"].reshape(-1), tol, name)
+
+
+@pytest.mark.parametrize("dtype,W,d,tol", [("f32", 8, 80, 1e-4), ("bf16", 16, 144, 2e-2),
+                                           ("bf16", 64, 64, 2e-2)])
+def test_scan_backward_crowded_slots(dtype, W, d, tol):
+    """Every slot drawn from a pool of 2W (offset into the bank), so consecutive tokens
+    share most of their slots and most write slots are read by their own token too: the
+    values the walk takes over from the token after it, and the reads folded into the
+    write, are exercised on nearly every token. d = 80 and 144 leave a partial row block."""
+    wl = synth.Workload("crowded", B=2, T=64, d=d, n=W, dk=16, W=W, dtype=dtype, seed=5)
+    cfg = tl.cfg_of(wl)
+    B, T, N = wl.B, wl.T, wl.N
+    g = torch.Generator().manual_seed(11)
+    pool, base = 2 * W, N - 2 * W - 3
+    idx = torch.stack([torch.randperm(pool, generator=g)[:W] + base for _ in range(B * T * 2)])
+    idx = idx.view(B * T, 2, W).to(torch.int32)
+    w = torch.rand(B * T, 2, W, generator=g) + 0.05
+    w = w / w.sum(-1, keepdim=True)
+    v = torch.randn(B * T, d, generator=g).to(wl.torch_dtype)
+    al = torch.rand(B * T, generator=g) * 0.5 + 0.5
+    be = torch.rand(B * T, generator=g)
+    M0 = synth.make_params(wl)["M0"]
+    _walk_back_and_check(wl, cfg, M0, idx.cuda(), w.cuda(), v.cuda(), al.cuda(), be.cuda(), tol,
+                         f"crowded-{dtype}-w{W}")
 
 
 def test_scan_backward_from_m0_restores_m0():
