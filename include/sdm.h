@@ -235,8 +235,9 @@ SDM_API int sdm_prefill_m0(const sdm_cfg* cfg, const sdm_weights* wts, const voi
  *   state before them) are walked back with the tape. idx, wsel, v, alpha, beta as in
  *   the forward. ws: sdm_scan_backward_workspace_bytes(cfg, B, T) (per-block partial
  *   sums and a per-token table of the slots shared with the next token). Every pointer
- *   is 16-byte aligned (SDM_EINVAL otherwise). The stored state's rounding is
- *   differentiated as the identity. */
+ *   is 16-byte aligned (SDM_EINVAL otherwise); N * d must be below 2^32
+ *   (SDM_EUNSUPPORTED otherwise). The stored state's rounding is differentiated as
+ *   the identity. */
 SDM_API size_t sdm_tape_bytes(const sdm_cfg* cfg, int B, int T);
 SDM_API int sdm_scan_run_train(const sdm_cfg* cfg, const int32_t* idx, const float* wsel,
                                const void* v, const float* alpha, const float* beta,

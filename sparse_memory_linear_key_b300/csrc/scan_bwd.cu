@@ -17,7 +17,7 @@
 // backward takes the rounding's derivative as 1 and uses the stored values.
 //
 // Rows are independent, so a block owns 64 rows of one sequence and walks its tokens in
-// reverse; 4 groups of 64 threads share the W slots of a token (slot j in group j % 4).
+// reverse; 8 groups of 64 threads share the W slots of a token (slot j in group j % 8).
 // Sums over rows (dk, dr, dalpha, dbeta) are per-block partials, summed over the blocks
 // of a sequence by a second kernel.
 //
@@ -40,7 +40,7 @@ namespace sdm {
 namespace {
 
 constexpr int kBRows = 64;
-constexpr int kBThreads = 256;
+constexpr int kBThreads = 512;
 constexpr int kBGroups = kBThreads / kBRows;
 constexpr int kMetaRing = 4;   // token t, t-1 (gathers) and t-2 (being published)
 
@@ -78,11 +78,12 @@ __device__ __forceinline__ float warp_sum_many(float (&x)[V], int lane)
     return s;
 }
 
-// match [B*T][4W] bytes, per token t (positions: write j = j, read j = W + j):
-//   [0, 2W)  the position in token t+1 of the same slot (its write position if it has
-//            both), or -1 (no such slot, an invalid slot, or t the last token);
-//   [2W, 3W) for write position j, the read position of the same slot in token t, or -1;
-//   [3W, 4W) for read position j, 1 if token t also writes that slot, else 0.
+// match [B*T][W] words of 4 bytes, word j of token t (positions: write j = j, read
+// j = W + j; "next" below is the position of the same slot in token t+1, its write
+// position if it has both, or -1: no such slot, an invalid slot, or t the last token):
+//   byte 0: next of write position j;   byte 1: next of read position j;
+//   byte 2: the read position of token t with write j's slot, or -1;
+//   byte 3: 1 if token t also writes read j's slot, else 0.
 // Slots within one kind of one token are distinct (a top-W selection).
 template <int W>
 __global__ void __launch_bounds__(2 * W) bwd_match_kernel(const int32_t* __restrict__ idx, int T,
@@ -112,7 +113,7 @@ __global__ void __launch_bounds__(2 * W) bwd_match_kernel(const int32_t* __restr
                 break;
             }
     int8_t* m = match + tok * 4 * W;
-    m[p] = (int8_t)src;
+    m[4 * (p % W) + (p < W ? 0 : 1)] = (int8_t)src;
     int other = -1;
     const int base = p < W ? W : 0;   // a write position looks among the reads, and back
     if (s >= 0)
@@ -122,9 +123,9 @@ __global__ void __launch_bounds__(2 * W) bwd_match_kernel(const int32_t* __restr
                 break;
             }
     if (p < W)
-        m[2 * W + p] = (int8_t)other;
+        m[4 * p + 2] = (int8_t)other;
     else
-        m[3 * W + p - W] = (int8_t)(other >= 0 ? 1 : 0);
+        m[4 * (p - W) + 3] = (int8_t)(other >= 0 ? 1 : 0);
 }
 
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src)
@@ -150,7 +151,7 @@ template <int W>
 struct BwdMeta {
     int sid[2 * W];             // slot ids: write positions, then read positions
     float sw[2 * W];            // their weights
-    int8_t mt[4 * W];           // the match bytes of the token
+    int mt[W];                  // the match words of the token
     float gate[4];              // alpha, beta
 };
 template <typename S, int W>
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(kBThreads, 1) scan_bwd_kernel(
     const float* __restrict__ dy, float* __restrict__ dbank, float* __restrict__ dv,
     float* __restrict__ part, int B, int T, int d, int N)
 {
-    constexpr int SPG = W / kBGroups;         // slots a thread: j = grp + 4 i
+    constexpr int SPG = W / kBGroups;         // slots a thread: j = grp + 8 i
     constexpr int P = 2 * W + 2;
     constexpr int GCH = kBRows * 4 / 16;      // 16-byte chunks of a G row segment
     constexpr int SCH = kBRows * (int)sizeof(S) / 16;
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(kBThreads, 1) scan_bwd_kernel(
         else if (tid >= 64 && tid < 64 + W / 2)
             cp_async16(smem_u32(&m.sw[(tid - 64) * 4]), wsel + tk * 2 * W + (tid - 64) * 4);
         else if (tid >= 128 && tid < 128 + W / 4)
-            cp_async16(smem_u32(&m.mt[(tid - 128) * 16]), match + tk * 4 * W + (tid - 128) * 16);
+            cp_async16(smem_u32(&m.mt[(tid - 128) * 4]), match + tk * 4 * W + (tid - 128) * 16);
         else if (tid == 192)
             cp_async4(smem_u32(&m.gate[0]), alpha + tk);
         else if (tid == 193)
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kBThreads, 1) scan_bwd_kernel(
             const int p = k / GCH, c = k % GCH;
             const int s = m.sid[p];
             if (c < gch && s >= 0 && s < N)
-                cp_async16(smem_u32(&g.g[p][c * 4]), G + (size_t)s * d + row0 + c * 4);
+                cp_async16(smem_u32(&g.g[p][c * 4]), G + ((uint32_t)s * (uint32_t)d + row0 + c * 4));
         }
         for (int k = tid; k < 2 * W * SCH; k += kBThreads) {
             const int p = k / SCH, c = k % SCH;
@@ -233,8 +234,9 @@ __global__ void __launch_bounds__(kBThreads, 1) scan_bwd_kernel(
             } else {
                 // the bank after token tk's write: token tk + 1's pre-write row if it
                 // wrote the slot (the value its restore puts back), else the bank row
-                const int q = m.mt[p];
-                src = (q >= 0 && q < W) ? tape + ((size_t)(tk + 1) * W + q) * d : bank + (size_t)s * d;
+                const int q = (int8_t)(m.mt[p - W] >> 8);
+                src = (q >= 0 && q < W) ? tape + ((size_t)(tk + 1) * W + q) * d
+                                        : bank + (uint32_t)s * (uint32_t)d;
             }
             cp_async16(smem_u32(&g.st[p][e16]), src + row0 + e16);
         }
@@ -278,31 +280,35 @@ __global__ void __launch_bounds__(kBThreads, 1) scan_bwd_kernel(
         const BwdStage<S, W>& g = sm.stage[cb];
         const float dyr = act ? g.dy[r] : 0.f;
         // ---- this token's values: G from the previous token's final values where it
-        // touched the slot, else as gathered
+        // touched the slot, else as gathered. Offsets within a sequence's bank fit 32 bits.
         float gw[SPG], gr[SPG], ow[SPG], pr[SPG];
+        int rmj[SPG];
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
             const int j = grp + kBGroups * i;
             const int sw_ = m.sid[j], sr = m.sid[W + j];
+            const int mw = m.mt[j];
+            const int qw = (int8_t)mw, qr = (int8_t)(mw >> 8);
+            rmj[i] = (int8_t)(mw >> 16);
             const bool okw = act && sw_ >= 0 && sw_ < N;
             const bool okr = act && sr >= 0 && sr < N;
-            const int qw = m.mt[j], qr = m.mt[W + j];
-            gw[i] = okw ? (qw >= 0 ? sm.xg[qw][r] : g.g[j][r]) : 0.f;
-            gr[i] = okr ? (qr >= 0 ? sm.xg[qr][r] : g.g[W + j][r]) : 0.f;
+            const float* pw = qw >= 0 ? sm.xg[qw] : g.g[j];
+            const float* pq = qr >= 0 ? sm.xg[qr] : g.g[W + j];
+            gw[i] = okw ? pw[r] : 0.f;
+            gr[i] = okr ? pq[r] : 0.f;
             ow[i] = okw ? to_f(g.st[j][r]) : 0.f;
             // ---- read: dr_j = <M[R_j], dy> (M after this token's write), G[R_j] += r_j dy
             pr[i] = okr ? to_f(g.st[W + j][r]) * dyr : 0.f;
-            if (okr && m.mt[3 * W + j] == 0)   // else the write stores the slot
-                G[(size_t)sr * d + row] = fmaf(m.sw[W + j], dyr, gr[i]);
+            if (okr && (mw >> 24) == 0)   // else the write stores the slot
+                G[(uint32_t)sr * (uint32_t)d + (uint32_t)row] = fmaf(m.sw[W + j], dyr, gr[i]);
         }
         // ---- write: G at the write slots after the read's additions
         float gp = 0.f, up = 0.f;
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
             const int j = grp + kBGroups * i;
-            const int q = m.mt[2 * W + j];
-            if (q >= 0)
-                gw[i] = fmaf(m.sw[W + q], dyr, gw[i]);
+            if (rmj[i] >= 0)
+                gw[i] = fmaf(m.sw[W + rmj[i]], dyr, gw[i]);
             gp = fmaf(m.sw[j], gw[i], gp);
             up = fmaf(m.sw[j], ow[i], up);
         }
@@ -333,10 +339,11 @@ __global__ void __launch_bounds__(kBThreads, 1) scan_bwd_kernel(
             pk[i] = be * gw[i] * c - al * be * gs * ow[i];
             const float gn = al * (gw[i] - be * kj * gs);
             if (act && s >= 0 && s < N) {
-                G[(size_t)s * d + row] = gn;
+                const uint32_t off = (uint32_t)s * (uint32_t)d + (uint32_t)row;
+                G[off] = gn;
                 // the tape value, stored back exactly (a stored value converts to fp32
                 // and back unchanged)
-                bank[(size_t)s * d + row] = S(ow[i]);
+                bank[off] = S(ow[i]);
             }
             sm.xg[j][r] = gn;
             sm.xg[W + j][r] = fmaf(m.sw[W + j], dyr, gr[i]);
@@ -433,6 +440,8 @@ cudaError_t launch_scan_backward(const sdm_cfg& c, const int32_t* idx, const flo
     if ((int64_t)B * T > 0x7FFFFFFF)
         return cudaErrorInvalidValue;
     const int N = c.n_sub * c.n_sub;
+    if ((uint64_t)N * (uint64_t)c.d > 0xFFFFFFFFull)   // offsets within a bank are 32-bit
+        return cudaErrorInvalidValue;
     float* part = (float*)ws;
     int8_t* match = (int8_t*)ws + part_bytes(c, B, T);
     const bool bf = c.dtype == SDM_BF16;

@@ -515,6 +515,8 @@ int sdm_scan_backward(const sdm_cfg* cfg, const int32_t* idx, const float* wsel,
     for (const void* p : ptrs)   // rows are staged by 16-byte copies
         if (!aligned16(p))
             return SDM_EINVAL;
+    if ((uint64_t)cfg->n_sub * cfg->n_sub * (uint64_t)cfg->d > 0xFFFFFFFFull)
+        return SDM_EUNSUPPORTED;   // offsets within one bank are 32-bit
     if (ws_bytes < scan_backward_ws_bytes(*cfg, B, T))
         return SDM_EWORKSPACE;
     return cuda_status(launch_scan_backward(*cfg, idx, wsel, v, alpha, beta, tape, banks, dy, dbank,
