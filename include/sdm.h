@@ -268,8 +268,10 @@ SDM_API int sdm_address_backward(const sdm_cfg* cfg, const void* K1, const void*
 /* Backward of the projections: with dq_w, dq_r [ntok, dk] and dv [ntok, d] fp32 (the
  * gradients with respect to sdm_project's outputs; their rounding is passed through),
  * writes dx [ntok, d] = dq_w W_qw^T + dq_r W_qr^T + dv W_v^T and dW_qw, dW_qr [d, dk],
- * dW_v [d, d] = x^T d(out), fp32, overwritten. Strict-fp32 GEMMs on fp32 copies of x
- * and the weights: ws sdm_project_backward_workspace_bytes(cfg, ntok), 256-byte
+ * dW_v [d, d] = x^T d(out), fp32, overwritten. GEMMs on fp32 copies of x and the
+ * weights: strict fp32 for an fp32 layer; TF32 tensor cores for a bf16 layer (x and
+ * the weights are exact in TF32, the incoming gradients are rounded to a relative
+ * 2^-11, products summed in fp32). ws sdm_project_backward_workspace_bytes(cfg, ntok), 256-byte
  * aligned. With sdm_scan_backward and sdm_address_backward this completes the
  * gradients of one layer (dq_w, dq_r from the addressing, dv from the scan). */
 SDM_API size_t sdm_project_backward_workspace_bytes(const sdm_cfg* cfg, int64_t ntok);

@@ -165,7 +165,10 @@ int launch_address_backward(const sdm_cfg& c, const void* K1, const void* K2, co
 // ---------------------------------------------------------- projection backward
 // q_w = x W_qw, q_r = x W_qr, v = x W_v (the rounding of the outputs passed through):
 //   dx = dq_w W_qw^T + dq_r W_qr^T + dv W_v^T,   dW_* = x^T d(out)_*
-// strict-fp32 GEMMs on fp32 copies of x and the weights.
+// GEMMs on fp32 copies of x and the weights: strict fp32 for an fp32 layer; for a bf16
+// layer on the tensor cores in TF32, where x and the weights are exact (a bf16 value has
+// fewer mantissa bits than TF32) and only the incoming fp32 gradients are rounded, to a
+// relative 2^-11, finer than the layer's own bf16 rounding of its outputs (2^-9).
 
 namespace sdm {
 
@@ -190,6 +193,7 @@ int launch_project_backward(const sdm_cfg& c, const sdm_weights& w, const void* 
     float* wqr = wqw + (size_t)d * dk;
     float* wv = wqr + (size_t)d * dk;
     const bool bf = c.dtype == SDM_BF16;
+    const bool tc = bf;   // TF32 tensor cores for a bf16 layer
     cudaError_t e = bf ? widen<bf16>(x, ntok, d, xf, d, s) : widen<float>(x, ntok, d, xf, d, s);
     if (e == cudaSuccess)
         e = bf ? widen<bf16>(w.W_qw, d, dk, wqw, dk, s) : widen<float>(w.W_qw, d, dk, wqw, dk, s);
@@ -199,17 +203,17 @@ int launch_project_backward(const sdm_cfg& c, const sdm_weights& w, const void* 
         e = bf ? widen<bf16>(w.W_v, d, d, wv, d, s) : widen<float>(w.W_v, d, d, wv, d, s);
     if (e != cudaSuccess)
         return SDM_ECUDA;
-    int rc = gemm_f32_rm(s, false, true, nt, d, dk, dq_w, dk, wqw, dk, dx, d, 0.f);
+    int rc = gemm_f32_rm(s, false, true, nt, d, dk, dq_w, dk, wqw, dk, dx, d, 0.f, tc);
     if (rc == SDM_OK)
-        rc = gemm_f32_rm(s, false, true, nt, d, dk, dq_r, dk, wqr, dk, dx, d, 1.f);
+        rc = gemm_f32_rm(s, false, true, nt, d, dk, dq_r, dk, wqr, dk, dx, d, 1.f, tc);
     if (rc == SDM_OK)
-        rc = gemm_f32_rm(s, false, true, nt, d, d, dv, d, wv, d, dx, d, 1.f);
+        rc = gemm_f32_rm(s, false, true, nt, d, d, dv, d, wv, d, dx, d, 1.f, tc);
     if (rc == SDM_OK)
-        rc = gemm_f32_rm(s, true, false, d, dk, nt, xf, d, dq_w, dk, dW_qw, dk, 0.f);
+        rc = gemm_f32_rm(s, true, false, d, dk, nt, xf, d, dq_w, dk, dW_qw, dk, 0.f, tc);
     if (rc == SDM_OK)
-        rc = gemm_f32_rm(s, true, false, d, dk, nt, xf, d, dq_r, dk, dW_qr, dk, 0.f);
+        rc = gemm_f32_rm(s, true, false, d, dk, nt, xf, d, dq_r, dk, dW_qr, dk, 0.f, tc);
     if (rc == SDM_OK)
-        rc = gemm_f32_rm(s, true, false, d, d, nt, xf, d, dv, d, dW_v, d, 0.f);
+        rc = gemm_f32_rm(s, true, false, d, d, nt, xf, d, dv, d, dW_v, d, 0.f, tc);
     return rc;
 }
 

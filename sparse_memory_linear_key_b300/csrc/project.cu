@@ -155,11 +155,12 @@ int launch_project_forked(const sdm_cfg& c, const sdm_weights& w, const void* x,
 
 namespace sdm {
 
-// Row-major fp32 GEMM on the library's own handle (strict fp32, no TF32):
+// Row-major fp32 GEMM on the library's own handle (strict fp32; with tf32 the inputs are
+// rounded to TF32 and the products summed in fp32 on the tensor cores):
 //   C [M, N] = op(A) [M, K] op(B) [K, N] (+ beta C), op = transpose when ta / tb.
 // In column-major terms C^T = op(B)^T op(A)^T, which is the call below.
 int gemm_f32_rm(cudaStream_t s, bool ta, bool tb, int M, int N, int K, const float* A, int lda,
-                const float* B, int ldb, float* C, int ldc, float beta)
+                const float* B, int ldb, float* C, int ldc, float beta, bool tf32)
 {
     std::lock_guard<std::mutex> lock(g_blas_mu);
     cublasHandle_t h = blas_handle(0);
@@ -168,7 +169,8 @@ int gemm_f32_rm(cudaStream_t s, bool ta, bool tb, int M, int N, int K, const flo
     const float one = 1.0f;
     return cublasGemmEx(h, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N, N, M, K,
                         &one, B, CUDA_R_32F, ldb, A, CUDA_R_32F, lda, &beta, C, CUDA_R_32F, ldc,
-                        CUBLAS_COMPUTE_32F_PEDANTIC, CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS
+                        tf32 ? CUBLAS_COMPUTE_32F_FAST_TF32 : CUBLAS_COMPUTE_32F_PEDANTIC,
+                        CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS
                ? SDM_OK
                : SDM_ECUDA;
 }

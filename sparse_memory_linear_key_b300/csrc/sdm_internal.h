@@ -85,9 +85,10 @@ cudaError_t launch_scan_backward(const sdm_cfg& c, const int32_t* idx, const flo
 // value >= T if none (bank_init.cu)
 cudaError_t launch_first_touch(const sdm_cfg& c, const int32_t* idx, int B, int T,
                                int32_t* first_write, cudaStream_t s);
-// row-major fp32 GEMM, C = op(A) op(B) + beta C, strict fp32 (project.cu)
+// row-major fp32 GEMM, C = op(A) op(B) + beta C, strict fp32, or on the tensor cores
+// with the inputs rounded to TF32 (project.cu)
 int gemm_f32_rm(cudaStream_t s, bool ta, bool tb, int M, int N, int K, const float* A, int lda,
-                const float* B, int ldb, float* C, int ldc, float beta);
+                const float* B, int ldb, float* C, int ldc, float beta, bool tf32 = false);
 
 // Backward of the addressing (addr_bwd.cu): selection-weight gradients -> dq, dK
 size_t address_backward_ws_bytes(const sdm_cfg& c, int64_t ntok);

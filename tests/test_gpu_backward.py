@@ -201,8 +201,14 @@ def test_project_backward_matches_oracle(name):
     torch.cuda.synchronize()
     ref = oracle.project_backward(x, p["W_qw"], p["W_qr"], p["W_v"], dqw.numpy(), dqr.numpy(),
                                   dvv.numpy())
+    # fp32 layer: strict fp32 GEMMs. bf16 layer: TF32 tensor-core GEMMs, where x and the
+    # weights are exact and each incoming gradient is rounded by at most u = 2^-11 of
+    # itself, so an output's error is at most u * sum_k |a_k b_k|; with K <= 640 terms of
+    # N(0,1)-like products that is u * 0.64 K against outputs of size ~4 sqrt(K) at the
+    # largest, a relative 0.16 u sqrt(K) <= 2e-3 (the typical error is ~u / 4)
+    tol = 1e-5 if wl.dtype == "f32" else 2e-3
     for got, want in zip((dx, dWqw, dWqr, dWv), ref):
-        assert rel_err(got.cpu().numpy(), want) <= 1e-5, name
+        assert rel_err(got.cpu().numpy(), want) <= tol, name
 
 
 @pytest.mark.parametrize("name,tol", [("tiny-f32", 1e-4), ("w64-small", 2e-2)])
