@@ -17,7 +17,8 @@
 // backward takes the rounding's derivative as 1 and uses the stored values.
 //
 // Rows are independent, so a block owns 64 rows of one sequence and walks its tokens in
-// reverse; 8 groups of 64 threads share the W slots of a token (slot j in group j % 8).
+// reverse; its warps share the W slots of a token (slot j in warp j % 16, or one slot a
+// warp for W < 16), each lane two adjacent rows.
 // Sums over rows (dk, dr, dalpha, dbeta) are per-block partials, summed over the blocks
 // of a sequence by a second kernel.
 //
@@ -40,8 +41,6 @@ namespace sdm {
 namespace {
 
 constexpr int kBRows = 64;
-constexpr int kBThreads = 512;
-constexpr int kBGroups = kBThreads / kBRows;
 constexpr int kMetaRing = 4;   // token t, t-1 (gathers) and t-2 (being published)
 
 
@@ -134,8 +133,16 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src)
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
-__device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
-__device__ __forceinline__ float to_f(float x) { return x; }
+
+// Shape of the walk: a block owns 64 rows of one sequence; each warp is a group that
+// owns slots j = group + NG i of every token, each lane rows 2 lane and 2 lane + 1 of
+// them (so the per-slot index work is shared by two rows and rows move as pairs).
+template <int W>
+struct BwdShape {
+    static constexpr int NG = W < 16 ? W : 16;   // groups (warps)
+    static constexpr int threads = NG * 32;
+    static constexpr int SPG = W / NG;           // slots a thread
+};
 
 // Shared memory of the walk. A token's gathers land in stage t & 1; its metadata in
 // ring entry t % 4 (in flight two tokens ahead, read by the gathers issued one token
@@ -158,44 +165,58 @@ template <typename S, int W>
 struct BwdSmem {
     BwdStage<S, W> stage[2];
     BwdMeta<W> meta[kMetaRing];
-    float xg[2 * W][kBRows];    // the final G values of the previous token, by its position
-    float red[2][kBGroups][kBRows];
-    float acc[2][2 * W + 2];    // partial sums of token t in entry t & 1
+    float2 xg[2 * W][kBRows / 2];   // the final G values of the previous token, by its position
+    float2 red[2][BwdShape<W>::NG][kBRows / 2];
+    float acc[2][2 * W + 2];        // partial sums of token t in entry t & 1
 };
+
+__device__ __forceinline__ float2 ld_pair(const bf16* p)
+{
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+__device__ __forceinline__ float2 ld_pair(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ void st_pair(bf16* p, float2 x)
+{
+    *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(x.x, x.y);
+}
+__device__ __forceinline__ void st_pair(float* p, float2 x) { *reinterpret_cast<float2*>(p) = x; }
+__device__ __forceinline__ float2 dup(float x) { return make_float2(x, x); }
+__device__ __forceinline__ float dot2(float2 a, float2 b) { return fmaf(a.x, b.x, a.y * b.y); }
 
 // partials: [nblk][B*T][2W + 2] = dk[W], dr[W], dalpha, dbeta of this block's rows
 template <typename S, int W>
-__global__ void __launch_bounds__(kBThreads, 1) scan_bwd_kernel(
+__global__ void __launch_bounds__(BwdShape<W>::threads, 1) scan_bwd_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ wsel,
     const int8_t* __restrict__ match, const S* __restrict__ v, const float* __restrict__ alpha,
     const float* __restrict__ beta, const S* __restrict__ tape, S* __restrict__ banks,
     const float* __restrict__ dy, float* __restrict__ dbank, float* __restrict__ dv,
     float* __restrict__ part, int B, int T, int d, int N)
 {
-    constexpr int SPG = W / kBGroups;         // slots a thread: j = grp + 8 i
+    constexpr int NG = BwdShape<W>::NG, NT = BwdShape<W>::threads, SPG = BwdShape<W>::SPG;
     constexpr int P = 2 * W + 2;
     constexpr int GCH = kBRows * 4 / 16;      // 16-byte chunks of a G row segment
     constexpr int SCH = kBRows * (int)sizeof(S) / 16;
-    static_assert(P <= kBThreads, "one partial sum a thread");
+    static_assert(P <= NT, "one partial sum a thread");
+    static_assert(NT >= 194, "the metadata copies' thread ranges");
     static_assert(SPG >= 1 && 32 % SPG == 0, "whole lanes per reduced value");
     static_assert(W / 2 <= 64 && W / 4 <= 64, "metadata copies fit their thread ranges");
     extern __shared__ __align__(16) unsigned char smem_raw[];
     BwdSmem<S, W>& sm = *reinterpret_cast<BwdSmem<S, W>*>(smem_raw);
     const int b = blockIdx.y;
     const int tid = threadIdx.x;
-    const int r = tid % kBRows, grp = tid / kBRows;
+    const int grp = tid >> 5, lane = tid & 31;
+    const int rr = 2 * lane;                  // the lane's first row within the block
     const int row0 = blockIdx.x * kBRows;
-    const int row = row0 + r;
+    const int row = row0 + rr;
     const int nrows = min(kBRows, d - row0);  // a multiple of 16: d is
-    const bool act = r < nrows;
-    const int lane = tid & 31;
+    const bool act = rr < nrows;              // both rows, nrows being even
     S* bank = banks + (size_t)b * N * d;
     float* G = dbank + (size_t)b * N * d;
     if (T <= 0)
         return;
     const int64_t tok0 = (int64_t)b * T;
 
-    // token tk's slot ids, weights, match bytes and gates into ring entry mb
+    // token tk's slot ids, weights, match words and gates into ring entry mb
     auto issue_meta = [&](int64_t tk, int mb) {
         BwdMeta<W>& m = sm.meta[mb];
         if (tid < W / 2)
@@ -216,13 +237,13 @@ __global__ void __launch_bounds__(kBThreads, 1) scan_bwd_kernel(
         const BwdMeta<W>& m = sm.meta[mb];
         BwdStage<S, W>& g = sm.stage[gb];
         const int gch = nrows * 4 / 16, sch = nrows * (int)sizeof(S) / 16;
-        for (int k = tid; k < 2 * W * GCH; k += kBThreads) {
+        for (int k = tid; k < 2 * W * GCH; k += NT) {
             const int p = k / GCH, c = k % GCH;
             const int s = m.sid[p];
             if (c < gch && s >= 0 && s < N)
                 cp_async16(smem_u32(&g.g[p][c * 4]), G + ((uint32_t)s * (uint32_t)d + row0 + c * 4));
         }
-        for (int k = tid; k < 2 * W * SCH; k += kBThreads) {
+        for (int k = tid; k < 2 * W * SCH; k += NT) {
             const int p = k / SCH, c = k % SCH;
             const int s = m.sid[p];
             if (c >= sch || s < 0 || s >= N)
@@ -259,6 +280,7 @@ __global__ void __launch_bounds__(kBThreads, 1) scan_bwd_kernel(
     __syncthreads();
     issue_gathers(tok0 + T - 1, (T - 1) % kMetaRing, (T - 1) & 1);
     cp_async_commit();
+    const float2 zero2 = make_float2(0.f, 0.f);
     for (int t = T - 1; t >= 0; --t) {
         const int64_t tok = tok0 + t;
         const int mb = t % kMetaRing, cb = t & 1;
@@ -278,89 +300,94 @@ __global__ void __launch_bounds__(kBThreads, 1) scan_bwd_kernel(
 
         const BwdMeta<W>& m = sm.meta[mb];
         const BwdStage<S, W>& g = sm.stage[cb];
-        const float dyr = act ? g.dy[r] : 0.f;
+        const float2 dy2 = act ? *reinterpret_cast<const float2*>(&g.dy[rr]) : zero2;
         // ---- this token's values: G from the previous token's final values where it
         // touched the slot, else as gathered. Offsets within a sequence's bank fit 32 bits.
-        float gw[SPG], gr[SPG], ow[SPG], pr[SPG];
+        float2 gw[SPG], gr[SPG], ow[SPG];
+        float pr[SPG];
+        uint32_t offw[SPG];                    // G / bank offset of the write slot, or ~0
         int rmj[SPG];
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
-            const int j = grp + kBGroups * i;
+            const int j = grp + NG * i;
             const int sw_ = m.sid[j], sr = m.sid[W + j];
             const int mw = m.mt[j];
             const int qw = (int8_t)mw, qr = (int8_t)(mw >> 8);
             rmj[i] = (int8_t)(mw >> 16);
             const bool okw = act && sw_ >= 0 && sw_ < N;
             const bool okr = act && sr >= 0 && sr < N;
-            const float* pw = qw >= 0 ? sm.xg[qw] : g.g[j];
-            const float* pq = qr >= 0 ? sm.xg[qr] : g.g[W + j];
-            gw[i] = okw ? pw[r] : 0.f;
-            gr[i] = okr ? pq[r] : 0.f;
-            ow[i] = okw ? to_f(g.st[j][r]) : 0.f;
+            offw[i] = okw ? (uint32_t)sw_ * (uint32_t)d + (uint32_t)row : 0xFFFFFFFFu;
+            const float2* pw = qw >= 0 ? sm.xg[qw] : reinterpret_cast<const float2*>(g.g[j]);
+            const float2* pq = qr >= 0 ? sm.xg[qr] : reinterpret_cast<const float2*>(g.g[W + j]);
+            gw[i] = okw ? pw[lane] : zero2;
+            gr[i] = okr ? pq[lane] : zero2;
+            ow[i] = okw ? ld_pair(&g.st[j][rr]) : zero2;
             // ---- read: dr_j = <M[R_j], dy> (M after this token's write), G[R_j] += r_j dy
-            pr[i] = okr ? to_f(g.st[W + j][r]) * dyr : 0.f;
+            pr[i] = okr ? dot2(ld_pair(&g.st[W + j][rr]), dy2) : 0.f;
             if (okr && (mw >> 24) == 0)   // else the write stores the slot
-                G[(uint32_t)sr * (uint32_t)d + (uint32_t)row] = fmaf(m.sw[W + j], dyr, gr[i]);
+                st_pair(G + ((uint32_t)sr * (uint32_t)d + (uint32_t)row),
+                        __ffma2_rn(dup(m.sw[W + j]), dy2, gr[i]));
         }
         // ---- write: G at the write slots after the read's additions
-        float gp = 0.f, up = 0.f;
+        float2 gp = zero2, up = zero2;
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
-            const int j = grp + kBGroups * i;
+            const int j = grp + NG * i;
             if (rmj[i] >= 0)
-                gw[i] = fmaf(m.sw[W + rmj[i]], dyr, gw[i]);
-            gp = fmaf(m.sw[j], gw[i], gp);
-            up = fmaf(m.sw[j], ow[i], up);
+                gw[i] = __ffma2_rn(dup(m.sw[W + rmj[i]]), dy2, gw[i]);
+            const float2 k2 = dup(m.sw[j]);
+            gp = __ffma2_rn(k2, gw[i], gp);
+            up = __ffma2_rn(k2, ow[i], up);
         }
-        sm.red[0][grp][r] = gp;
-        sm.red[1][grp][r] = up;
+        sm.red[0][grp][lane] = gp;
+        sm.red[1][grp][lane] = up;
         {
             const float sum = warp_sum_many<SPG>(pr, lane);
             if (lane % (32 / SPG) == 0)
-                atomicAdd(&sm.acc[cb][W + grp + kBGroups * (lane / (32 / SPG))], sum);
+                atomicAdd(&sm.acc[cb][W + grp + NG * (lane / (32 / SPG))], sum);
         }
         __syncthreads();   // red complete; every thread has read xg
-        float gs = 0.f, u = 0.f;
+        float2 gs = zero2, u = zero2;
 #pragma unroll
-        for (int q = 0; q < kBGroups; ++q) {
-            gs += sm.red[0][q][r];
-            u += sm.red[1][q][r];
+        for (int q = 0; q < NG; ++q) {
+            gs = __fadd2_rn(gs, sm.red[0][q][lane]);
+            u = __fadd2_rn(u, sm.red[1][q][lane]);
         }
         const float al = m.gate[0], be = m.gate[1];
-        const float c = (act ? to_f(g.v[r]) : 0.f) - al * u;
+        const float2 c = __ffma2_rn(dup(-al), u, act ? ld_pair(&g.v[rr]) : zero2);
         float pa = 0.f;
         float pk[SPG];
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
-            const int j = grp + kBGroups * i;
-            const int s = m.sid[j];
+            const int j = grp + NG * i;
             const float kj = m.sw[j];
-            pa = fmaf(gw[i], ow[i] - be * kj * u, pa);
-            pk[i] = be * gw[i] * c - al * be * gs * ow[i];
-            const float gn = al * (gw[i] - be * kj * gs);
-            if (act && s >= 0 && s < N) {
-                const uint32_t off = (uint32_t)s * (uint32_t)d + (uint32_t)row;
-                G[off] = gn;
+            const float bk = be * kj;
+            // dalpha: <G_j, old_j - beta k_j u>;  dk_j: beta <G_j, c> - alpha beta <g, old_j>
+            pa += dot2(gw[i], __ffma2_rn(dup(-bk), u, ow[i]));
+            pk[i] = be * dot2(gw[i], c) - al * be * dot2(gs, ow[i]);
+            const float2 gn = __fmul2_rn(dup(al), __ffma2_rn(dup(-bk), gs, gw[i]));
+            if (offw[i] != 0xFFFFFFFFu) {
+                st_pair(G + offw[i], gn);
                 // the tape value, stored back exactly (a stored value converts to fp32
                 // and back unchanged)
-                bank[off] = S(ow[i]);
+                st_pair(bank + offw[i], ow[i]);
             }
-            sm.xg[j][r] = gn;
-            sm.xg[W + j][r] = fmaf(m.sw[W + j], dyr, gr[i]);
+            sm.xg[j][lane] = gn;
+            sm.xg[W + j][lane] = __ffma2_rn(dup(m.sw[W + j]), dy2, gr[i]);
         }
         {
             const float sum = warp_sum_many<SPG>(pk, lane);
             if (lane % (32 / SPG) == 0)
-                atomicAdd(&sm.acc[cb][grp + kBGroups * (lane / (32 / SPG))], sum);
+                atomicAdd(&sm.acc[cb][grp + NG * (lane / (32 / SPG))], sum);
         }
         pa = warp_sum(pa);
-        const float pb = warp_sum(grp == 0 ? gs * c : 0.f);
+        const float pb = warp_sum(grp == 0 ? dot2(gs, c) : 0.f);
         if (lane == 0) {
             atomicAdd(&sm.acc[cb][2 * W], pa);
             atomicAdd(&sm.acc[cb][2 * W + 1], pb);
         }
         if (grp == 0 && act)
-            dv[tok * d + row] = be * gs;
+            *reinterpret_cast<float2*>(dv + tok * d + row) = __fmul2_rn(dup(be), gs);
         // red, xg and the stage are rewritten only after the next token's first barrier
     }
     __syncthreads();
@@ -409,7 +436,7 @@ cudaError_t launch_bwd_t(const int32_t* idx, const float* wsel, int8_t* match, c
                              (int)smem);
     if (e != cudaSuccess)
         return e;
-    scan_bwd_kernel<S, W><<<grid, kBThreads, smem, s>>>(idx, wsel, match, (const S*)v, alpha, beta,
+    scan_bwd_kernel<S, W><<<grid, BwdShape<W>::threads, smem, s>>>(idx, wsel, match, (const S*)v, alpha, beta,
                                                      (const S*)tape, (S*)banks, dy, dbank, dv,
                                                      part, B, T, d, N);
     return cudaGetLastError();
