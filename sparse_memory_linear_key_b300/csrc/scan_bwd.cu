@@ -26,11 +26,11 @@
 // rows, dy and v) are 16-byte cp.async copies into a shared-memory stage, issued one
 // token ahead while the token before it in the walk is processed; barriers do not wait
 // for them, so the gathers of one token overlap the arithmetic of the other. A slot that
-// token then writes is gathered stale. A per-token match table, built by a small kernel
-// beforehand, names for each slot of token t the position in token t+1 that touched it
-// last; token t takes that position's final G value from shared memory instead (token
-// t+1 leaves all of its final values there), and gathers M from token t+1's tape row,
-// which is the value the restore puts back. The same table names, for a write slot that
+// token then writes is gathered stale. A pre-pass kernel builds per-token slot
+// descriptors: for each slot of token t, the position in token t+1 that touched it last;
+// token t takes that position's final G value from shared memory instead (token t+1
+// leaves there the values token t takes), and gathers M from token t+1's tape row, which
+// is the value the restore puts back. The same descriptors name, for a write slot that
 // is also read by its own token, the read position, so the read's addition r_j dy is
 // applied in registers and no barrier separates the read from the write.
 #include "sdm_common.cuh"
@@ -77,54 +77,79 @@ __device__ __forceinline__ float warp_sum_many(float (&x)[V], int lane)
     return s;
 }
 
-// match [B*T][W] words of 4 bytes, word j of token t (positions: write j = j, read
-// j = W + j; "next" below is the position of the same slot in token t+1, its write
-// position if it has both, or -1: no such slot, an invalid slot, or t the last token):
-//   byte 0: next of write position j;   byte 1: next of read position j;
-//   byte 2: the read position of token t with write j's slot, or -1;
-//   byte 3: 1 if token t also writes read j's slot, else 0.
+// The pre-pass: one 16-byte descriptor per token t and slot index j < W (positions: write
+// j = j, read j = W + j; "next" below is the position of the same slot in token t+1, its
+// write position if it has both, or -1: no such slot, an invalid slot, or t the last
+// token):
+//   offw, offr: the write / read slot's row offset s d within its sequence's bank, or
+//               ~0 for an invalid slot;
+//   mw byte 0:  next of write position j;   byte 1: next of read position j;
+//      byte 2:  the read position of token t with write j's slot, or -1;
+//      byte 3:  1 if token t also writes read j's slot, else 0;
+//   need byte 0 (1): 1 if token t-1 takes write (read) position j's final G value from
+//               token t, else 0 -- the positions that token t must leave in shared memory.
 // Slots within one kind of one token are distinct (a top-W selection).
+struct BwdDesc {
+    uint32_t offw, offr;
+    int mw, need;
+};
+
 template <int W>
-__global__ void __launch_bounds__(2 * W) bwd_match_kernel(const int32_t* __restrict__ idx, int T,
-                                                          int N, int8_t* __restrict__ match)
+__global__ void __launch_bounds__(2 * W) bwd_prep_kernel(const int32_t* __restrict__ idx, int T,
+                                                         int N, int d, BwdDesc* __restrict__ desc)
 {
-    __shared__ int cs[2 * W], ns[2 * W];
+    __shared__ int ps[2 * W], cs[2 * W], ns[2 * W];   // tokens t-1, t, t+1
     const int64_t tok = blockIdx.x;
     const int t = (int)(tok % T);
     const int p = threadIdx.x;
-    int s = __ldg(idx + tok * 2 * W + p);
-    if (s < 0 || s >= N)
-        s = -1;
+    auto slot = [&](int64_t tk) {
+        const int s = __ldg(idx + tk * 2 * W + p);
+        return (s < 0 || s >= N) ? -1 : s;
+    };
+    const int s = slot(tok);
     cs[p] = s;
-    int q = -2;
-    if (t + 1 < T) {
-        q = __ldg(idx + (tok + 1) * 2 * W + p);
-        if (q < 0 || q >= N)
-            q = -2;
-    }
-    ns[p] = q;
+    ns[p] = t + 1 < T ? slot(tok + 1) : -1;
+    ps[p] = t >= 1 ? slot(tok - 1) : -1;
     __syncthreads();
-    int src = -1;
-    if (s >= 0)
+    int src = -1, other = -1, need = 0;
+    if (s >= 0) {
         for (int k = 0; k < 2 * W; ++k)
             if (ns[k] == s) {
                 src = k;
                 break;
             }
-    int8_t* m = match + tok * 4 * W;
-    m[4 * (p % W) + (p < W ? 0 : 1)] = (int8_t)src;
-    int other = -1;
-    const int base = p < W ? W : 0;   // a write position looks among the reads, and back
-    if (s >= 0)
+        const int base = p < W ? W : 0;   // a write position looks among the reads, and back
         for (int k = 0; k < W; ++k)
             if (cs[base + k] == s) {
                 other = k;
                 break;
             }
-    if (p < W)
-        m[4 * p + 2] = (int8_t)other;
-    else
-        m[4 * (p - W) + 3] = (int8_t)(other >= 0 ? 1 : 0);
+        // token t-1 takes this position's value when it holds the slot, unless this is a
+        // read position whose slot token t also writes (the write position serves it)
+        if (p < W || other < 0)
+            for (int k = 0; k < 2 * W; ++k)
+                if (ps[k] == s) {
+                    need = 1;
+                    break;
+                }
+    }
+    BwdDesc& o = desc[tok * W + p % W];
+    int8_t* mw = reinterpret_cast<int8_t*>(&o.mw);
+    int8_t* nd = reinterpret_cast<int8_t*>(&o.need);
+    const uint32_t off = s >= 0 ? (uint32_t)s * (uint32_t)d : 0xFFFFFFFFu;
+    if (p < W) {
+        o.offw = off;
+        mw[0] = (int8_t)src;
+        mw[2] = (int8_t)other;
+        nd[0] = (int8_t)need;
+        nd[2] = 0;
+    } else {
+        o.offr = off;
+        mw[1] = (int8_t)src;
+        mw[3] = (int8_t)(other >= 0 ? 1 : 0);
+        nd[1] = (int8_t)need;
+        nd[3] = 0;
+    }
 }
 
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src)
@@ -156,9 +181,8 @@ struct BwdStage {
 };
 template <int W>
 struct BwdMeta {
-    int sid[2 * W];             // slot ids: write positions, then read positions
-    float sw[2 * W];            // their weights
-    int mt[W];                  // the match words of the token
+    BwdDesc desc[W];            // the token's slot descriptors
+    float sw[2 * W];            // the weights: write positions, then read positions
     float gate[4];              // alpha, beta
 };
 template <typename S, int W>
@@ -166,7 +190,8 @@ struct BwdSmem {
     BwdStage<S, W> stage[2];
     BwdMeta<W> meta[kMetaRing];
     float2 xg[2 * W][kBRows / 2];   // the final G values of the previous token, by its position
-    float2 red[2][BwdShape<W>::NG][kBRows / 2];
+    float2 red[2][BwdShape<W>::NG][kBRows / 2 + 1];   // per-warp sums g, u (padded rows)
+    float2 red2[2][kBRows / 2];                       // their sums over the warps
     float acc[2][2 * W + 2];        // partial sums of token t in entry t & 1
 };
 
@@ -186,8 +211,8 @@ __device__ __forceinline__ float dot2(float2 a, float2 b) { return fmaf(a.x, b.x
 // partials: [nblk][B*T][2W + 2] = dk[W], dr[W], dalpha, dbeta of this block's rows
 template <typename S, int W>
 __global__ void __launch_bounds__(BwdShape<W>::threads, 1) scan_bwd_kernel(
-    const int32_t* __restrict__ idx, const float* __restrict__ wsel,
-    const int8_t* __restrict__ match, const S* __restrict__ v, const float* __restrict__ alpha,
+    const BwdDesc* __restrict__ desc, const float* __restrict__ wsel,
+    const S* __restrict__ v, const float* __restrict__ alpha,
     const float* __restrict__ beta, const S* __restrict__ tape, S* __restrict__ banks,
     const float* __restrict__ dy, float* __restrict__ dbank, float* __restrict__ dv,
     float* __restrict__ part, int B, int T, int d, int N)
@@ -199,7 +224,8 @@ __global__ void __launch_bounds__(BwdShape<W>::threads, 1) scan_bwd_kernel(
     static_assert(P <= NT, "one partial sum a thread");
     static_assert(NT >= 194, "the metadata copies' thread ranges");
     static_assert(SPG >= 1 && 32 % SPG == 0, "whole lanes per reduced value");
-    static_assert(W / 2 <= 64 && W / 4 <= 64, "metadata copies fit their thread ranges");
+    static_assert(W <= 64, "metadata copies fit their thread ranges");
+    static_assert(NT % 64 == 0 && 2 * (NT / 64) == NG, "two warps' partials a lane in the sum of g, u");
     extern __shared__ __align__(16) unsigned char smem_raw[];
     BwdSmem<S, W>& sm = *reinterpret_cast<BwdSmem<S, W>*>(smem_raw);
     const int b = blockIdx.y;
@@ -216,15 +242,13 @@ __global__ void __launch_bounds__(BwdShape<W>::threads, 1) scan_bwd_kernel(
         return;
     const int64_t tok0 = (int64_t)b * T;
 
-    // token tk's slot ids, weights, match words and gates into ring entry mb
+    // token tk's slot descriptors, weights and gates into ring entry mb
     auto issue_meta = [&](int64_t tk, int mb) {
         BwdMeta<W>& m = sm.meta[mb];
-        if (tid < W / 2)
-            cp_async16(smem_u32(&m.sid[tid * 4]), idx + tk * 2 * W + tid * 4);
+        if (tid < W)
+            cp_async16(smem_u32(&m.desc[tid]), desc + tk * W + tid);
         else if (tid >= 64 && tid < 64 + W / 2)
             cp_async16(smem_u32(&m.sw[(tid - 64) * 4]), wsel + tk * 2 * W + (tid - 64) * 4);
-        else if (tid >= 128 && tid < 128 + W / 4)
-            cp_async16(smem_u32(&m.mt[(tid - 128) * 4]), match + tk * 4 * W + (tid - 128) * 16);
         else if (tid == 192)
             cp_async4(smem_u32(&m.gate[0]), alpha + tk);
         else if (tid == 193)
@@ -239,14 +263,14 @@ __global__ void __launch_bounds__(BwdShape<W>::threads, 1) scan_bwd_kernel(
         const int gch = nrows * 4 / 16, sch = nrows * (int)sizeof(S) / 16;
         for (int k = tid; k < 2 * W * GCH; k += NT) {
             const int p = k / GCH, c = k % GCH;
-            const int s = m.sid[p];
-            if (c < gch && s >= 0 && s < N)
-                cp_async16(smem_u32(&g.g[p][c * 4]), G + ((uint32_t)s * (uint32_t)d + row0 + c * 4));
+            const uint32_t off = (&m.desc[p % W].offw)[p / W];   // offw, then offr
+            if (c < gch && off != 0xFFFFFFFFu)
+                cp_async16(smem_u32(&g.g[p][c * 4]), G + (off + row0 + c * 4));
         }
         for (int k = tid; k < 2 * W * SCH; k += NT) {
             const int p = k / SCH, c = k % SCH;
-            const int s = m.sid[p];
-            if (c >= sch || s < 0 || s >= N)
+            const uint32_t off = (&m.desc[p % W].offw)[p / W];
+            if (c >= sch || off == 0xFFFFFFFFu)
                 continue;
             const int e16 = c * (16 / (int)sizeof(S));
             const S* src;
@@ -255,9 +279,8 @@ __global__ void __launch_bounds__(BwdShape<W>::threads, 1) scan_bwd_kernel(
             } else {
                 // the bank after token tk's write: token tk + 1's pre-write row if it
                 // wrote the slot (the value its restore puts back), else the bank row
-                const int q = (int8_t)(m.mt[p - W] >> 8);
-                src = (q >= 0 && q < W) ? tape + ((size_t)(tk + 1) * W + q) * d
-                                        : bank + (uint32_t)s * (uint32_t)d;
+                const int q = (int8_t)(m.desc[p - W].mw >> 8);
+                src = (q >= 0 && q < W) ? tape + ((size_t)(tk + 1) * W + q) * d : bank + off;
             }
             cp_async16(smem_u32(&g.st[p][e16]), src + row0 + e16);
         }
@@ -305,18 +328,19 @@ __global__ void __launch_bounds__(BwdShape<W>::threads, 1) scan_bwd_kernel(
         // touched the slot, else as gathered. Offsets within a sequence's bank fit 32 bits.
         float2 gw[SPG], gr[SPG], ow[SPG];
         float pr[SPG];
-        uint32_t offw[SPG];                    // G / bank offset of the write slot, or ~0
-        int rmj[SPG];
+        uint32_t offw[SPG];                    // G / bank offset of the write slot's rows, or ~0
+        int rmj[SPG], need[SPG];
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
             const int j = grp + NG * i;
-            const int sw_ = m.sid[j], sr = m.sid[W + j];
-            const int mw = m.mt[j];
+            const int4 dd = *reinterpret_cast<const int4*>(&m.desc[j]);
+            const int mw = dd.z;
             const int qw = (int8_t)mw, qr = (int8_t)(mw >> 8);
             rmj[i] = (int8_t)(mw >> 16);
-            const bool okw = act && sw_ >= 0 && sw_ < N;
-            const bool okr = act && sr >= 0 && sr < N;
-            offw[i] = okw ? (uint32_t)sw_ * (uint32_t)d + (uint32_t)row : 0xFFFFFFFFu;
+            need[i] = dd.w;
+            const bool okw = act && (uint32_t)dd.x != 0xFFFFFFFFu;
+            const bool okr = act && (uint32_t)dd.y != 0xFFFFFFFFu;
+            offw[i] = okw ? (uint32_t)dd.x + (uint32_t)row : 0xFFFFFFFFu;
             const float2* pw = qw >= 0 ? sm.xg[qw] : reinterpret_cast<const float2*>(g.g[j]);
             const float2* pq = qr >= 0 ? sm.xg[qr] : reinterpret_cast<const float2*>(g.g[W + j]);
             gw[i] = okw ? pw[lane] : zero2;
@@ -325,8 +349,7 @@ __global__ void __launch_bounds__(BwdShape<W>::threads, 1) scan_bwd_kernel(
             // ---- read: dr_j = <M[R_j], dy> (M after this token's write), G[R_j] += r_j dy
             pr[i] = okr ? dot2(ld_pair(&g.st[W + j][rr]), dy2) : 0.f;
             if (okr && (mw >> 24) == 0)   // else the write stores the slot
-                st_pair(G + ((uint32_t)sr * (uint32_t)d + (uint32_t)row),
-                        __ffma2_rn(dup(m.sw[W + j]), dy2, gr[i]));
+                st_pair(G + ((uint32_t)dd.y + (uint32_t)row), __ffma2_rn(dup(m.sw[W + j]), dy2, gr[i]));
         }
         // ---- write: G at the write slots after the read's additions
         float2 gp = zero2, up = zero2;
@@ -347,12 +370,22 @@ __global__ void __launch_bounds__(BwdShape<W>::threads, 1) scan_bwd_kernel(
                 atomicAdd(&sm.acc[cb][W + grp + NG * (lane / (32 / SPG))], sum);
         }
         __syncthreads();   // red complete; every thread has read xg
-        float2 gs = zero2, u = zero2;
+        {
+            // g, u summed over the warps: TPO adjacent lanes share one (quantity, row
+            // pair), each adding two warps' partials, then exchange
+            constexpr int TPO = NT / 64;
+            const int o = tid / TPO, part = tid % TPO;
+            float2 sum = __fadd2_rn(sm.red[o >> 5][2 * part][o & 31], sm.red[o >> 5][2 * part + 1][o & 31]);
 #pragma unroll
-        for (int q = 0; q < NG; ++q) {
-            gs = __fadd2_rn(gs, sm.red[0][q][lane]);
-            u = __fadd2_rn(u, sm.red[1][q][lane]);
+            for (int x = 1; x < TPO; x <<= 1) {
+                sum.x += __shfl_xor_sync(0xFFFFFFFFu, sum.x, x);
+                sum.y += __shfl_xor_sync(0xFFFFFFFFu, sum.y, x);
+            }
+            if (part == 0)
+                sm.red2[o >> 5][o & 31] = sum;
         }
+        __syncthreads();   // red2 complete
+        const float2 gs = sm.red2[0][lane], u = sm.red2[1][lane];
         const float al = m.gate[0], be = m.gate[1];
         const float2 c = __ffma2_rn(dup(-al), u, act ? ld_pair(&g.v[rr]) : zero2);
         float pa = 0.f;
@@ -372,8 +405,10 @@ __global__ void __launch_bounds__(BwdShape<W>::threads, 1) scan_bwd_kernel(
                 // and back unchanged)
                 st_pair(bank + offw[i], ow[i]);
             }
-            sm.xg[j][lane] = gn;
-            sm.xg[W + j][lane] = __ffma2_rn(dup(m.sw[W + j]), dy2, gr[i]);
+            if (need[i] & 0xFF)   // only what token t - 1 takes from this token
+                sm.xg[j][lane] = gn;
+            if (need[i] & 0xFF00)
+                sm.xg[W + j][lane] = __ffma2_rn(dup(m.sw[W + j]), dy2, gr[i]);
         }
         {
             const float sum = warp_sum_many<SPG>(pk, lane);
@@ -421,12 +456,12 @@ __global__ void __launch_bounds__(256) scan_bwd_reduce(const float* __restrict__
 }
 
 template <typename S, int W>
-cudaError_t launch_bwd_t(const int32_t* idx, const float* wsel, int8_t* match, const void* v,
+cudaError_t launch_bwd_t(const int32_t* idx, const float* wsel, BwdDesc* desc, const void* v,
                          const float* alpha, const float* beta, const void* tape, void* banks,
                          const float* dy, float* dbank, float* dv, float* part, int B, int T, int d,
                          int N, cudaStream_t s)
 {
-    bwd_match_kernel<W><<<(unsigned)((int64_t)B * T), 2 * W, 0, s>>>(idx, T, N, match);
+    bwd_prep_kernel<W><<<(unsigned)((int64_t)B * T), 2 * W, 0, s>>>(idx, T, N, d, desc);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
@@ -436,13 +471,13 @@ cudaError_t launch_bwd_t(const int32_t* idx, const float* wsel, int8_t* match, c
                              (int)smem);
     if (e != cudaSuccess)
         return e;
-    scan_bwd_kernel<S, W><<<grid, BwdShape<W>::threads, smem, s>>>(idx, wsel, match, (const S*)v, alpha, beta,
-                                                     (const S*)tape, (S*)banks, dy, dbank, dv,
-                                                     part, B, T, d, N);
+    scan_bwd_kernel<S, W><<<grid, BwdShape<W>::threads, smem, s>>>(
+        desc, wsel, (const S*)v, alpha, beta, (const S*)tape, (S*)banks, dy, dbank, dv, part, B, T,
+        d, N);
     return cudaGetLastError();
 }
 
-// workspace: the per-block partials, then the match table
+// workspace: the per-block partials, then the slot descriptors
 size_t part_bytes(const sdm_cfg& c, int B, int T)
 {
     const size_t nblk = (size_t)(c.d + kBRows - 1) / kBRows;
@@ -453,7 +488,7 @@ size_t part_bytes(const sdm_cfg& c, int B, int T)
 
 size_t scan_backward_ws_bytes(const sdm_cfg& c, int B, int T)
 {
-    return part_bytes(c, B, T) + (size_t)B * T * 4 * c.w;
+    return part_bytes(c, B, T) + (size_t)B * T * c.w * sizeof(BwdDesc);
 }
 
 cudaError_t launch_scan_backward(const sdm_cfg& c, const int32_t* idx, const float* wsel,
@@ -470,13 +505,13 @@ cudaError_t launch_scan_backward(const sdm_cfg& c, const int32_t* idx, const flo
     if ((uint64_t)N * (uint64_t)c.d > 0xFFFFFFFFull)   // offsets within a bank are 32-bit
         return cudaErrorInvalidValue;
     float* part = (float*)ws;
-    int8_t* match = (int8_t*)ws + part_bytes(c, B, T);
+    BwdDesc* desc = (BwdDesc*)((char*)ws + part_bytes(c, B, T));
     const bool bf = c.dtype == SDM_BF16;
     cudaError_t e;
 #define SDM_BWD(WW)                                                                                \
-    (bf ? launch_bwd_t<bf16, WW>(idx, wsel, match, v, alpha, beta, tape, banks, dy, dbank, dv,     \
+    (bf ? launch_bwd_t<bf16, WW>(idx, wsel, desc, v, alpha, beta, tape, banks, dy, dbank, dv,      \
                                  part, B, T, c.d, N, s)                                            \
-        : launch_bwd_t<float, WW>(idx, wsel, match, v, alpha, beta, tape, banks, dy, dbank, dv,    \
+        : launch_bwd_t<float, WW>(idx, wsel, desc, v, alpha, beta, tape, banks, dy, dbank, dv,     \
                                   part, B, T, c.d, N, s))
     switch (c.w) {
     case 8: e = SDM_BWD(8); break;

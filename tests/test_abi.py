@@ -102,11 +102,11 @@ def test_host_validation_before_cuda(L):
     assert L.sdm_scan(ctypes.byref(c), None, None, None, None, None, None, None, 0, 5, None, 0,
                       None, None) == sdm.SDM_OK
     # the backward walk: every row is staged by 16-byte copies; offsets within a bank are
-    # 32-bit; the workspace holds per-block partial sums and the match table
+    # 32-bit; the workspace holds per-block partial sums and 16-byte slot descriptors
     bw = lambda cc, ptr, ws, nbytes: L.sdm_scan_backward(
         ctypes.byref(cc), *([P(ptr)] * 13), 1, 4, P(ws), nbytes, None)
     need = sdm.scan_backward_workspace_bytes(c, 1, 4)
-    assert need == (((64 + 63) // 64) * 4 * (2 * 8 + 2) * 4 + 255) // 256 * 256 + 4 * 4 * 8
+    assert need == (((64 + 63) // 64) * 4 * (2 * 8 + 2) * 4 + 255) // 256 * 256 + 4 * 8 * 16
     assert bw(c, 24, 256, need) == sdm.SDM_EINVAL                    # misaligned
     assert bw(c, 16, 256, need - 1) == sdm.SDM_EWORKSPACE
     big = sdm.make_cfg(16400, 512, 256, 64, "bf16")                  # N d > 2^32
