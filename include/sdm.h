@@ -234,7 +234,8 @@ SDM_API int sdm_prefill_m0(const sdm_cfg* cfg, const sdm_weights* wts, const voi
  *   all fp32. banks (in: the state after the tokens, as the forward left it; out: the
  *   state before them) are walked back with the tape. idx, wsel, v, alpha, beta as in
  *   the forward. ws: sdm_scan_backward_workspace_bytes(cfg, B, T) (per-block partial
- *   sums and a per-token table of the slots shared with the next token). Every pointer
+ *   sums and per-token slot descriptors: row offsets and the slots shared with the
+ *   neighbouring tokens). Every pointer
  *   is 16-byte aligned (SDM_EINVAL otherwise); N * d must be below 2^32
  *   (SDM_EUNSUPPORTED otherwise). The stored state's rounding is differentiated as
  *   the identity. */
