@@ -922,7 +922,6 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
             return;
         S* bank = reinterpret_cast<S*>(a.banks) + (size_t)m.b * a.N * a.d +
                   (size_t)m.rb * a.rb_rows + rg * RPL;
-#pragma unroll
         const unsigned long long dead = m.deadmask;
 #pragma unroll
         for (int i = 0; i < SPL; ++i) {
