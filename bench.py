@@ -302,6 +302,13 @@ def gpu_arm(args, world, rank):
                            "filled from M0) + scan"},
         "stages_ms": {k: round(v_, 4) for k, v_ in stage_ms.items()},
         "scan_tokens_per_s": round(ntok / scan_s, 1),
+        # the same step without bank initialisation (as on banks already holding a
+        # state): the step less the first-touch table and the fill, from the stages'
+        # event times; the scan reads the same bytes from M0 as from a copied bank
+        "prefill_without_bank_init": {
+            "value": round(ntok * world / ((ms_per_step - stage_ms["first_touch"] - stage_ms["fill"]) / 1e3), 1),
+            "unit": "tokens/s",
+            "ms_per_step": round(ms_per_step - stage_ms["first_touch"] - stage_ms["fill"], 4)},
         "roofline": roofline,
         "clocks": clocks.summary(),
         "gpu_launches": 6 * args.steps,
