@@ -326,39 +326,54 @@ __global__ void __launch_bounds__(BwdShape<W>::threads, 1) scan_bwd_kernel(
         const float2 dy2 = act ? *reinterpret_cast<const float2*>(&g.dy[rr]) : zero2;
         // ---- this token's values: G from the previous token's final values where it
         // touched the slot, else as gathered. Offsets within a sequence's bank fit 32 bits.
-        float2 gw[SPG], gr[SPG], ow[SPG];
-        float pr[SPG];
-        uint32_t offw[SPG];                    // G / bank offset of the write slot's rows, or ~0
-        int rmj[SPG], need[SPG];
+        // All shared-memory loads of the token first (descriptors, weights, then the
+        // values they select), so that no load waits behind a store and the slots'
+        // dependency chains interleave; then the arithmetic and the stores.
+        int4 dd[SPG];
+        float kw[SPG], rwt[SPG], rmw[SPG];
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
             const int j = grp + NG * i;
-            const int4 dd = *reinterpret_cast<const int4*>(&m.desc[j]);
-            const int mw = dd.z;
-            const int qw = (int8_t)mw, qr = (int8_t)(mw >> 8);
-            rmj[i] = (int8_t)(mw >> 16);
-            need[i] = dd.w;
-            const bool okw = act && (uint32_t)dd.x != 0xFFFFFFFFu;
-            const bool okr = act && (uint32_t)dd.y != 0xFFFFFFFFu;
-            offw[i] = okw ? (uint32_t)dd.x + (uint32_t)row : 0xFFFFFFFFu;
+            dd[i] = *reinterpret_cast<const int4*>(&m.desc[j]);
+            kw[i] = m.sw[j];
+            rwt[i] = m.sw[W + j];
+        }
+        float2 gw[SPG], gr[SPG], ow[SPG], mr[SPG];
+        uint32_t offw[SPG], offr[SPG];   // G / bank offsets of the slots' rows, or ~0
+#pragma unroll
+        for (int i = 0; i < SPG; ++i) {
+            const int j = grp + NG * i;
+            const int mw = dd[i].z;
+            const int qw = (int8_t)mw, qr = (int8_t)(mw >> 8), rm = (int8_t)(mw >> 16);
+            const bool okw = act && (uint32_t)dd[i].x != 0xFFFFFFFFu;
+            const bool okr = act && (uint32_t)dd[i].y != 0xFFFFFFFFu;
+            offw[i] = okw ? (uint32_t)dd[i].x + (uint32_t)row : 0xFFFFFFFFu;
+            offr[i] = okr ? (uint32_t)dd[i].y + (uint32_t)row : 0xFFFFFFFFu;
+            // G: the previous token's final value where it touched the slot, else as
+            // gathered
             const float2* pw = qw >= 0 ? sm.xg[qw] : reinterpret_cast<const float2*>(g.g[j]);
             const float2* pq = qr >= 0 ? sm.xg[qr] : reinterpret_cast<const float2*>(g.g[W + j]);
             gw[i] = okw ? pw[lane] : zero2;
             gr[i] = okr ? pq[lane] : zero2;
             ow[i] = okw ? ld_pair(&g.st[j][rr]) : zero2;
-            // ---- read: dr_j = <M[R_j], dy> (M after this token's write), G[R_j] += r_j dy
-            pr[i] = okr ? dot2(ld_pair(&g.st[W + j][rr]), dy2) : 0.f;
-            if (okr && (mw >> 24) == 0)   // else the write stores the slot
-                st_pair(G + ((uint32_t)dd.y + (uint32_t)row), __ffma2_rn(dup(m.sw[W + j]), dy2, gr[i]));
+            mr[i] = okr ? ld_pair(&g.st[W + j][rr]) : zero2;
+            rmw[i] = rm >= 0 ? m.sw[W + rm] : 0.f;
+        }
+        // ---- read: dr_j = <M[R_j], dy> (M after this token's write), G[R_j] += r_j dy
+        float pr[SPG];
+#pragma unroll
+        for (int i = 0; i < SPG; ++i) {
+            pr[i] = dot2(mr[i], dy2);
+            if (offr[i] != 0xFFFFFFFFu && (dd[i].z >> 24) == 0)   // else the write stores it
+                st_pair(G + offr[i], __ffma2_rn(dup(rwt[i]), dy2, gr[i]));
         }
         // ---- write: G at the write slots after the read's additions
         float2 gp = zero2, up = zero2;
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
-            const int j = grp + NG * i;
-            if (rmj[i] >= 0)
-                gw[i] = __ffma2_rn(dup(m.sw[W + rmj[i]]), dy2, gw[i]);
-            const float2 k2 = dup(m.sw[j]);
+            if ((int8_t)(dd[i].z >> 16) >= 0)
+                gw[i] = __ffma2_rn(dup(rmw[i]), dy2, gw[i]);
+            const float2 k2 = dup(kw[i]);
             gp = __ffma2_rn(k2, gw[i], gp);
             up = __ffma2_rn(k2, ow[i], up);
         }
@@ -393,8 +408,7 @@ __global__ void __launch_bounds__(BwdShape<W>::threads, 1) scan_bwd_kernel(
 #pragma unroll
         for (int i = 0; i < SPG; ++i) {
             const int j = grp + NG * i;
-            const float kj = m.sw[j];
-            const float bk = be * kj;
+            const float bk = be * kw[i];
             // dalpha: <G_j, old_j - beta k_j u>;  dk_j: beta <G_j, c> - alpha beta <g, old_j>
             pa += dot2(gw[i], __ffma2_rn(dup(-bk), u, ow[i]));
             pk[i] = be * dot2(gw[i], c) - al * be * dot2(gs, ow[i]);
@@ -405,10 +419,10 @@ __global__ void __launch_bounds__(BwdShape<W>::threads, 1) scan_bwd_kernel(
                 // and back unchanged)
                 st_pair(bank + offw[i], ow[i]);
             }
-            if (need[i] & 0xFF)   // only what token t - 1 takes from this token
+            if (dd[i].w & 0xFF)   // only what token t - 1 takes from this token
                 sm.xg[j][lane] = gn;
-            if (need[i] & 0xFF00)
-                sm.xg[W + j][lane] = __ffma2_rn(dup(m.sw[W + j]), dy2, gr[i]);
+            if (dd[i].w & 0xFF00)
+                sm.xg[W + j][lane] = __ffma2_rn(dup(rwt[i]), dy2, gr[i]);
         }
         {
             const float sum = warp_sum_many<SPG>(pk, lane);
