@@ -438,7 +438,7 @@ def gpu_arm(args, world, rank):
             "backward_roofline": {"bound": "hbm", "bytes_per_token": bwd_tok,
                                   "achieved": round(bwd_gbs, 1), "peak": peak_b, "unit": "GB/s",
                                   "frac": round(bwd_gbs / peak_b, 4),
-                                  "timed": "the whole sdm_scan_backward call (match table, "
+                                  "timed": "the whole sdm_scan_backward call (descriptor pre-pass, "
                                            "walk, partial-sum reduction)"},
             "kernel": "scan_bwd_kernel: one block per (sequence, 64 rows), reverse token order, "
                       "each token's gathers issued one token ahead"}
