@@ -261,16 +261,26 @@ __global__ void __launch_bounds__(BwdShape<W>::threads, 1) scan_bwd_kernel(
         const BwdMeta<W>& m = sm.meta[mb];
         BwdStage<S, W>& g = sm.stage[gb];
         const int gch = nrows * 4 / 16, sch = nrows * (int)sizeof(S) / 16;
-        for (int k = tid; k < 2 * W * GCH; k += NT) {
+        // a thread's chunks are the same every token: fixed trip counts
+        constexpr int GIT = (2 * W * GCH + NT - 1) / NT, SIT = (2 * W * SCH + NT - 1) / NT;
+#pragma unroll
+        for (int it = 0; it < GIT; ++it) {
+            const int k = tid + it * NT;
             const int p = k / GCH, c = k % GCH;
+            if (k >= 2 * W * GCH || c >= gch)
+                continue;
             const uint32_t off = (&m.desc[p % W].offw)[p / W];   // offw, then offr
-            if (c < gch && off != 0xFFFFFFFFu)
+            if (off != 0xFFFFFFFFu)
                 cp_async16(smem_u32(&g.g[p][c * 4]), G + (off + row0 + c * 4));
         }
-        for (int k = tid; k < 2 * W * SCH; k += NT) {
+#pragma unroll
+        for (int it = 0; it < SIT; ++it) {
+            const int k = tid + it * NT;
             const int p = k / SCH, c = k % SCH;
+            if (k >= 2 * W * SCH || c >= sch)
+                continue;
             const uint32_t off = (&m.desc[p % W].offw)[p / W];
-            if (c >= sch || off == 0xFFFFFFFFu)
+            if (off == 0xFFFFFFFFu)
                 continue;
             const int e16 = c * (16 / (int)sizeof(S));
             const S* src;
