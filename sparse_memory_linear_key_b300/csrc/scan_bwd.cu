@@ -43,7 +43,6 @@ namespace {
 constexpr int kBRows = 64;
 constexpr int kMetaRing = 4;   // token t, t-1 (gathers) and t-2 (being published)
 
-
 __device__ __forceinline__ float warp_sum(float x)
 {
 #pragma unroll
