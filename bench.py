@@ -59,6 +59,8 @@ def parse():
                     help="decode steps instead of the workload's 512 (for profiling)")
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences instead of the workload's (for profiling a small case)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the lines of the other prefill workloads (d = 3840 pool, 131k)")
     return ap.parse_args()
 
 
@@ -264,6 +266,10 @@ def gpu_arm(args, world, rank):
     status = sdm.read_status(st)
     if status != 0:
         raise RuntimeError("device status %d during the timed steps" % status)
+    # for the slot-set check of the CPU-baseline leg: 128 sampled tokens' q bits and sets
+    import numpy as np
+    toks = np.sort(np.random.default_rng(7).choice(ntok, 128, replace=False))
+    samples = [(WORKLOAD, address_sample(q_w, q_r, idx, toks, x=x.reshape(ntok, d)))]
     elapsed_ms = t0.elapsed_time(t1)
     elapsed_ms = max_over_ranks(world, elapsed_ms)
     stage_ms = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev)
@@ -514,10 +520,20 @@ def gpu_arm(args, world, rank):
 
     if not args.no_decode:
         res["decode"] = decode_arm(sdm, args, world)
+        samples.append(res["decode"].pop("_sample"))
 
     del banks, q_w, q_r, v, idx, wsel, y, ws_a, ws_s
     torch.cuda.empty_cache()
-    return res, p_cpu, tok_cpu
+    # the pages' other prefill shapes: the 8B-width layer with repeated pool queries, and
+    # one 131,072-token sequence with the inserted key/value pattern
+    if not args.no_workloads and args.tokens is None and args.batch is None:
+        res["workloads"] = {}
+        for name in ("prefill-d3840-pool", "long-131k"):
+            line = prefill_line(sdm, name, steps=max(3, min(10, args.steps // 5)), warmup=2)
+            samples.append(line.pop("_sample"))
+            res["workloads"][name] = line
+            res["gpu_launches"] += line["gpu_launches_per_step"] * line["steps"]
+    return res, p_cpu, tok_cpu, samples
 
 
 def decode_arm(sdm, args, world):
@@ -585,22 +601,226 @@ def decode_arm(sdm, args, world):
            "eager_us_per_step": round(eager_ms * 1e3 / S, 2),
            "note": "%d sdm_decode_step calls (projections, addressing, scan) "
                    "captured in one CUDA graph; eager = one host call per step" % S}
+    peak, _ = measured_peaks()
+    out["state_roofline_frac"] = round(out["state_hbm_gbs"] / peak, 4)
+    # one more step, after the timed ones, returning the slot sets it used; the same
+    # projection kernel on the same x gives the q bits it scored (slot-set check)
+    idx1 = torch.empty(B, 2, wl.W, dtype=torch.int32, device=dev)
+    y1 = torch.empty(B, wl.d, device=dev)
+    sdm.sdm_decode_step(cfg, p, xd[0], ad[0], bd[0], banks, y1, wsd, st, idx_out=idx1)
+    qw1 = torch.empty(B, wl.dk, dtype=torch.bfloat16, device=dev)
+    qr1 = torch.empty_like(qw1)
+    sdm.sdm_project(cfg, p, xd[0], qw1, qr1, torch.empty(B, wl.d, dtype=torch.bfloat16, device=dev))
+    torch.cuda.synchronize()
+    out["_sample"] = (DECODE_WORKLOAD, address_sample(qw1, qr1, idx1, list(range(B))))
     del g
     del banks, p, xd, y
     torch.cuda.empty_cache()
     return out
 
 
+# ------------------------------------------------- the other prefill workloads
+
+def scan_bytes_per_token(wl):
+    """Algorithmic HBM bytes of the scan per token: the write set read and written, the
+    read set read (disjoint sets on random inputs), v in, y out (fp32), slot ids, weights
+    and collision codes of both sets, the two gates."""
+    s = wl.elem_bytes
+    return (3 * wl.W * wl.d * s + wl.d * s + wl.d * 4 + 2 * wl.W * (4 + 4 + 2) + 8)
+
+
+def address_sample(q_w, q_r, idx, toks, x=None):
+    """What the slot-set check needs of the GPU side, on sampled tokens, copied to the
+    host after the timed region: the q bits the addressing scored, the slot sets it
+    chose and (optionally) the tokens' x."""
+    tt = torch.as_tensor(toks, device=idx.device)
+    return {"q_w": q_w[tt].cpu(), "q_r": q_r[tt].cpu(), "idx": idx[tt].cpu().numpy(),
+            "x": None if x is None else x[tt].cpu()}
+
+
+def address_check(wl, p_cpu, smp):
+    """Slot sets of the sampled tokens against the oracle scoring the same q bits (the
+    CPU-baseline leg; nothing here is timed): mismatches a near-tie does not excuse, and
+    mismatches excused because the oracle's gap between the W-th and (W+1)-th combined
+    score is below 1e-5. With the tokens' x, also the oracle's own projections and
+    addressing (free-running: a one-ulp bf16 difference in q can flip a boundary slot)."""
+    import numpy as np
+    import oracle
+    gi = smp["idx"]
+    free_x = smp["x"]
+    out = {"sampled_tokens": int(gi.shape[0])}
+    for kind, q in ((0, smp["q_w"]), (1, smp["q_r"])):
+        S, _, _, gaps = oracle.address(q, p_cpu["K1"], p_cpu["K2"], wl.W)
+        bad = np.any(np.sort(gi[:, kind], -1) != np.sort(S, -1), axis=1)
+        tie = bad & (gaps < 1e-5)
+        key = ("write", "read")[kind]
+        out[key] = {"unexcused_mismatches": int((bad & ~tie).sum()),
+                    "near_tie_mismatches": int(tie.sum())}
+        if free_x is not None:
+            wm = p_cpu["W_qw" if kind == 0 else "W_qr"]
+            S2, _, _, g2 = oracle.address(oracle.project(free_x, wm), p_cpu["K1"], p_cpu["K2"],
+                                          wl.W)
+            bad2 = np.any(np.sort(gi[:, kind], -1) != np.sort(S2, -1), axis=1)
+            out[key]["free_running_mismatches"] = int(bad2.sum())
+            out[key]["free_running_near_ties"] = int((bad2 & (g2 < 1e-5)).sum())
+    return out
+
+
+def prefill_line(sdm, name, steps, warmup):
+    """One of the pages' other prefill shapes, timed like the main step: projections,
+    addressing, codes, first-touch table, the scan from M0 and the fill. The workload's
+    query substitution (a pool of repeated queries, or the inserted key/value pattern) is
+    a property of its inputs: it is applied once to projected queries before the timed
+    steps, and each step's addressing and scan take those; each step's projection still
+    runs in full (into buffers of its own)."""
+    import numpy as np
+    wl = synth.WORKLOADS[name]
+    dev = "cuda"
+    cfg = sdm.make_cfg(wl.d, wl.n, wl.dk, wl.W, wl.dtype)
+    p_cpu = synth.make_params(wl)
+    tok = synth.make_tokens(wl)
+    p = {k: v_.to(dev) for k, v_ in p_cpu.items()}
+    B, T, d = wl.B, wl.T, wl.d
+    ntok = B * T
+    x = tok["x"].to(dev)
+    alpha = tok["alpha"].to(dev)
+    beta = tok["beta"].to(dev)
+    q_w = torch.empty(ntok, wl.dk, dtype=torch.bfloat16, device=dev)
+    q_r = torch.empty_like(q_w)
+    v = torch.empty(ntok, d, dtype=torch.bfloat16, device=dev)
+    sdm.sdm_project(cfg, p, x, q_w, q_r, v)
+    pool, pattern = synth.make_pool(wl), synth.make_pattern(wl)
+    synth.inject_queries(wl, q_w.view(B, T, -1), q_r.view(B, T, -1), v.view(B, T, -1),
+                         pool=pool, pattern=pattern)
+    qs_w, qs_r, vs = torch.empty_like(q_w), torch.empty_like(q_r), torch.empty_like(v)
+    banks = torch.empty(B, wl.N, d, dtype=torch.bfloat16, device=dev)
+    idx = torch.empty(ntok, 2, wl.W, dtype=torch.int32, device=dev)
+    wsel = torch.empty(ntok, 2, wl.W, dtype=torch.float32, device=dev)
+    y = torch.empty(ntok, d, dtype=torch.float32, device=dev)
+    ws_a = sdm.alloc_workspace(sdm.address_workspace_bytes(cfg, ntok))
+    ws_s = sdm.alloc_workspace(sdm.scan_workspace_bytes(cfg, B, T))
+    first_write = torch.empty(B, wl.N, dtype=torch.int32, device=dev)
+    st = sdm.new_status()
+    stream = torch.cuda.current_stream()
+    names = ["project", "address", "codes", "first_touch", "scan", "fill"]
+
+    def step(e=None):
+        rec = (lambda j: e[j].record(stream)) if e is not None else (lambda j: None)
+        rec(0)
+        sdm.sdm_project(cfg, p, x, qs_w, qs_r, vs)
+        rec(1)
+        sdm.sdm_address(cfg, p["K1"], p["K2"], q_w, q_r, idx, wsel, ws_a, st)
+        rec(2)
+        sdm.sdm_scan_prepare(cfg, idx, B, T, ws_s, st)
+        rec(3)
+        sdm.sdm_first_touch(cfg, idx, B, T, first_write)
+        rec(4)
+        sdm.sdm_scan_run_m0(cfg, idx, wsel, v, alpha, beta, p["M0"], first_write, banks, y, B, T,
+                            ws_s, st)
+        rec(5)
+        sdm.sdm_fill_untouched(cfg, p["M0"], first_write, banks, B, T)
+        rec(6)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+          for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        step(ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if sdm.read_status(st) != 0:
+        raise RuntimeError("device status %d in %s" % (sdm.read_status(st), name))
+    ms = t0.elapsed_time(t1) / steps
+    stage_ms = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev)
+                for j, n in enumerate(names)}
+    peak, _ = measured_peaks()
+    per_tok = scan_bytes_per_token(wl)
+    achieved = per_tok * ntok / (stage_ms["scan"] / 1e3) / 1e9
+    line = {"workload": name, "B": B, "T": T, "d": d, "value": round(ntok / (ms / 1e3), 1),
+            "unit": "tokens/s", "steps": steps, "ms_per_step": round(ms, 4),
+            "stages_ms": {k: round(v_, 4) for k, v_ in stage_ms.items()},
+            "scan_tokens_per_s": round(ntok / (stage_ms["scan"] / 1e3), 1),
+            "scan_roofline": {"bound": "hbm", "bytes_per_token": per_tok,
+                              "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                              "frac": round(achieved / peak, 4),
+                              "vs_8tbs": round(achieved / 8000.0, 4)},
+            "gpu_launches_per_step": 6}
+    gi = idx.cpu().numpy()
+    if pattern is not None:
+        L, wa, ra = wl.pattern_len, wl.pattern_write_at, wl.pattern_read_at
+        line["needle"] = {
+            "what": "slots read by the %d pattern queries at %d.. equal the slots written at "
+                    "%d.. (blog, needle-in-a-haystack access pattern)" % (L, ra, wa),
+            "slot_sets_equal": bool(all(np.array_equal(gi[ra + i, 1], gi[wa + i, 0])
+                                        for i in range(L)))}
+    if pool is not None:
+        m = pool["mask"].reshape(-1).numpy()
+        pw = pool["pick_w"].reshape(-1).numpy()
+        same = [np.all(gi[np.nonzero(m & (pw == vec))[0], 0] ==
+                       gi[np.nonzero(m & (pw == vec))[0][0], 0]) for vec in range(wl.pool_size)
+                if np.any(m & (pw == vec))]
+        line["pool"] = {"tokens_from_pool": int(m.sum()),
+                        "identical_sets_per_pool_vector": bool(all(same))}
+    toks = np.sort(np.random.default_rng(7).choice(ntok, 128, replace=False))
+    line["_sample"] = (name, address_sample(q_w, q_r, idx, toks))
+    del banks, q_w, q_r, v, qs_w, qs_r, vs, idx, wsel, y, ws_a, ws_s, first_write, p, x
+    torch.cuda.empty_cache()
+    return line
+
+
 # ------------------------------------------------------------- the CPU oracle
+
+def address_checks(samples):
+    """The slot-set check of every sampled workload, and the tiny fp32 workload run whole
+    (its 256 tokens) free-running against the oracle."""
+    import numpy as np
+    import oracle
+    import sparse_memory_linear_key_b300 as sdm
+    out = {}
+    for name, smp in samples:
+        wl = synth.WORKLOADS[name]
+        out[name] = address_check(wl, synth.make_params(wl, with_m0=False), smp)
+    wl = synth.WORKLOADS["tiny-f32"]
+    p = synth.make_params(wl)
+    tok = synth.make_tokens(wl)
+    cfg = sdm.make_cfg(wl.d, wl.n, wl.dk, wl.W, wl.dtype)
+    pd = {k: v.cuda() for k, v in p.items()}
+    banks = torch.empty(wl.B, wl.N, wl.d, device="cuda")
+    sdm.sdm_init_bank(cfg, pd["M0"], banks)
+    y = torch.empty(wl.B, wl.T, wl.d, device="cuda")
+    idx = torch.empty(wl.B * wl.T, 2, wl.W, dtype=torch.int32, device="cuda")
+    st = sdm.new_status()
+    ws = sdm.alloc_workspace(sdm.workspace_bytes(cfg, wl.B, wl.T))
+    sdm.sdm_prefill(cfg, pd, tok["x"].cuda(), tok["alpha"].cuda(), tok["beta"].cuda(), banks, y,
+                    ws, st, idx_out=idx)
+    gi = idx.cpu().numpy()
+    ref = oracle.prefill_sequence(tok["x"][0], p, tok["alpha"][0], tok["beta"][0], wl.W)
+    tiny = {"sampled_tokens": wl.T, "mode": "free-running (the oracle's own projections)"}
+    for kind, S, g in ((0, ref["S"], ref["gap_w"]), (1, ref["R"], ref["gap_r"])):
+        bad = np.any(np.sort(gi[:, kind], -1) != np.sort(S, -1), axis=1)
+        tiny[("write", "read")[kind]] = {"mismatches": int(bad.sum()),
+                                         "near_tie_mismatches": int((bad & (g < 1e-5)).sum())}
+    tiny["max_abs_y_err"] = float(np.abs(y[0].cpu().numpy() - ref["y"]).max())
+    out["tiny-f32"] = tiny
+    return out
+
 
 def oracle_sample(p_cpu, tok_cpu, n_tokens):
     """The oracle (as it stands) on sequence 0's first n_tokens of the workload, all
-    rows: projections, exhaustive addressing and the recurrence. Returns seconds."""
+    rows: projections, exhaustive addressing and the recurrence. The bank it updates is a
+    copy of M0 made before the clock starts (a 0.94 GB copy is set-up, not per-token
+    work). Returns seconds."""
     import oracle
     wl = synth.WORKLOADS[WORKLOAD]
+    M = oracle.storage(p_cpu["M0"])[0].copy()
     t = time.perf_counter()
     oracle.prefill_sequence(tok_cpu["x"][0, :n_tokens], p_cpu, tok_cpu["alpha"][0, :n_tokens],
-                            tok_cpu["beta"][0, :n_tokens], wl.W)
+                            tok_cpu["beta"][0, :n_tokens], wl.W, M=M)
     return time.perf_counter() - t
 
 
@@ -610,24 +830,60 @@ def oracle_threads():
                              else os.cpu_count())
 
 
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def _omp_threads(n):
+    """Set the OpenMP thread count of the oracle's runtime (libgomp); returns the old one."""
+    import ctypes
+    import oracle
+    oracle.lib()
+    gomp = ctypes.CDLL("libgomp.so.1")
+    old = gomp.omp_get_max_threads()
+    gomp.omp_set_num_threads(int(n))
+    return old
+
+
 def cpu_baseline(p_cpu, tok_cpu):
     n = ORACLE_SAMPLE_TOKENS
     secs = oracle_sample(p_cpu, tok_cpu, n)
+    n1 = 256
+    old = _omp_threads(1)
+    try:
+        secs1 = oracle_sample(p_cpu, tok_cpu, n1)
+    finally:
+        _omp_threads(old)
     return {"value": round(n / secs, 2), "unit": "tokens/s", "cores": oracle_threads(),
-            "kind": "oracle",
+            "kind": "oracle", "cpu_model": cpu_model(),
             "sample": "sequence 0, first %d tokens of %s, all 2048 rows (fp64 C oracle: "
-                      "projections, exhaustive top-W over 230,400 slots, recurrence); %.1f s"
-                      % (n, WORKLOAD, secs)}
+                      "projections, exhaustive top-W over 230,400 slots, recurrence; the bank "
+                      "copy of M0 made before the clock starts); %.1f s" % (n, WORKLOAD, secs),
+            "single_thread": {"value": round(n1 / secs1, 2), "unit": "tokens/s", "cores": 1,
+                              "sample": "the first %d tokens of the same sequence; %.1f s"
+                                        % (n1, secs1)}}
+
+
+REFERENCE_SAMPLE_TOKENS = 2048
 
 
 def reference_arm(args, world, rank):
-    """The oracle as the reference arm: each step one bounded sample of the workload."""
+    """The oracle as the reference arm: each step one bounded sample of the workload
+    (sequence 0's first 2,048 tokens, all rows, the bank copied from M0 before the clock
+    starts), at most three timed steps."""
     if rank != 0:
         return None
     wl = synth.WORKLOADS[WORKLOAD]
     p_cpu = synth.make_params(wl)
     tok_cpu = synth.make_tokens(wl)
-    n = 128
+    n = REFERENCE_SAMPLE_TOKENS
     for _ in range(min(args.warmup, 1)):
         oracle_sample(p_cpu, tok_cpu, 16)
     times = [oracle_sample(p_cpu, tok_cpu, n) for _ in range(args.steps if args.steps <= 3 else 3)]
@@ -642,8 +898,9 @@ def reference_arm(args, world, rank):
         "config": {"workload": WORKLOAD, "B": wl.B, "T": wl.T, "d": wl.d, "N": wl.N, "W": wl.W,
                    "dk": wl.dk, "state": "bf16"},
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": oracle_threads(),
-                         "kind": "oracle",
-                         "sample": "per step: sequence 0, first %d tokens, all rows" % n},
+                         "kind": "oracle", "cpu_model": cpu_model(),
+                         "sample": "per step: sequence 0, first %d tokens, all rows; the bank "
+                                   "copy of M0 made before the clock starts" % n},
         "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -666,10 +923,11 @@ def main():
             print(json.dumps(res), flush=True)
         barrier(world)
         return
-    res, p_cpu, tok_cpu = gpu_arm(args, world, rank)
+    res, p_cpu, tok_cpu, samples = gpu_arm(args, world, rank)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline(p_cpu, tok_cpu)
+            res["address_check"] = address_checks(samples)
         print(json.dumps(res), flush=True)
     barrier(world)
 

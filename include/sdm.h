@@ -147,6 +147,21 @@ SDM_API int sdm_scan_run(const sdm_cfg* cfg, const int32_t* idx, const float* ws
                          float* y, int B, int T, const void* ws, size_t ws_bytes,
                          int* dev_status, void* stream);
 
+/* Failure detection of the recurrence, for tests: sdm_scan_run with two diagnostic
+ * controls. spin_limit_cycles bounds every wait inside the kernel, in SM clock cycles
+ * (<= 0: the default of about one second). skip_item >= 0 names one work item that the
+ * kernel claims and drops -- token t of sequence b on row block rb, numbered
+ * (t * B + b) * nrb + rb with nrb = ceil(d * element bytes / 1024) -- so that the tokens
+ * depending on it wait for it until their bound runs out. Such a run records
+ * SDM_ETIMEOUT in *dev_status, every warp leaves once the copies it started have landed,
+ * and the call returns normally (banks and y are then undefined; the device stays
+ * usable). skip_item < 0 withholds nothing. Other arguments as sdm_scan_run. */
+SDM_API int sdm_scan_run_diag(const sdm_cfg* cfg, const int32_t* idx, const float* wsel,
+                              const void* v, const float* alpha, const float* beta, void* banks,
+                              float* y, int B, int T, const void* ws, size_t ws_bytes,
+                              long long spin_limit_cycles, long long skip_item, int* dev_status,
+                              void* stream);
+
 /* Size of the device array that sdm_scan_noalloc uses as its scratch: 8 MiB. A call
  * needs sdm_scan_min_workspace_bytes(cfg, B, T) of it: the collision codes (B * T * w * 4
  * bytes), four ordering masks per token (B * T * 32 bytes) and one progress flag per
@@ -168,7 +183,9 @@ SDM_API int sdm_scan_run(const sdm_cfg* cfg, const int32_t* idx, const float* ws
  *  - Allocates nothing (no cudaMalloc, cudaFree or allocating library call); it clears
  *    the flags it uses with cudaMemsetAsync on `stream`.
  *  - The first call on a device looks up the array's device address (once per device,
- *    with that device current); make that first call before any stream capture.
+ *    with that device current); make that first call before any stream capture. The
+ *    address is kept for the life of the process: after a cudaDeviceReset of that device
+ *    it is stale, so do not call this entry point on a device that has been reset.
  *  - Every call shares the one array: calls whose work overlaps on the GPU (other
  *    streams, other host threads) race on it and must be serialised by the caller. */
 SDM_API int sdm_scan_noalloc(const sdm_cfg* cfg, const int32_t* idx, const float* wsel,
@@ -317,12 +334,16 @@ SDM_API int sdm_slot_overlap(const sdm_cfg* cfg, const int32_t* idx, int B, int 
                              int r0, int r1, uint32_t* out, void* ws, size_t ws_bytes,
                              void* stream);
 
-/* One decode step: advance B independent sequences by one token each.
+/* One decode step: advance B independent sequences by one token each ("Sparse Delta
+ * Memory" blog, "How does SDM work?": per token, select, write, then read).
  * x [B, d], alpha/beta [B], banks [B, N, d] (in place), y [B, d] fp32.
+ * idx_out [B, 2, w] int32 / w_out [B, 2, w] fp32 optional (NULL = not returned): the
+ * slot sets and selection weights this step used, as sdm_address reports them.
  * ws: sdm_workspace_bytes(cfg, B, 1) bytes. */
 SDM_API int sdm_decode_step(const sdm_cfg* cfg, const sdm_weights* wts, const void* x,
                     const float* alpha, const float* beta, void* banks, float* y, int B,
-                    void* ws, size_t ws_bytes, int* dev_status, void* stream);
+                    int32_t* idx_out, float* w_out, void* ws, size_t ws_bytes,
+                    int* dev_status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -87,8 +87,10 @@ def lib():
             "sdm_scan_prepare": ([CP, P, I, I, P, S, P, P], I),
             "sdm_scan_run": ([CP, P, P, P, P, P, P, P, I, I, P, S, P, P], I),
             "sdm_scan_noalloc": ([CP, P, P, P, P, P, P, P, I, I, P, P], I),
+            "sdm_scan_run_diag": ([CP, P, P, P, P, P, P, P, I, I, P, S, ctypes.c_longlong,
+                                   ctypes.c_longlong, P, P], I),
             "sdm_prefill": ([CP, WP, P, P, P, P, P, I, I, P, P, P, S, P, P], I),
-            "sdm_decode_step": ([CP, WP, P, P, P, P, P, I, P, S, P, P], I),
+            "sdm_decode_step": ([CP, WP, P, P, P, P, P, I, P, P, P, S, P, P], I),
             "sdm_first_touch_bytes": ([CP, I], S),
             "sdm_first_touch": ([CP, P, I, I, P, P], I),
             "sdm_scan_run_m0": ([CP, P, P, P, P, P, P, P, P, P, I, I, P, S, P, P], I),
@@ -260,6 +262,22 @@ def sdm_scan_run(cfg: Cfg, idx, wsel, v, alpha, beta, banks, y, B: int, T: int, 
                               ws.numel() * ws.element_size(),
                               _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)),
            "sdm_scan_run")
+
+
+def sdm_scan_run_diag(cfg: Cfg, idx, wsel, v, alpha, beta, banks, y, B: int, T: int, ws,
+                      spin_limit_cycles: int, skip_item: int, dev_status, stream=None) -> None:
+    """sdm_scan_run with the bound of every wait given in SM clock cycles and, for
+    skip_item >= 0, one work item withheld (tests of the failure detection)."""
+    dt = cfg.torch_dtype
+    _check(lib().sdm_scan_run_diag(ctypes.byref(cfg), _ptr(idx, torch.int32, "idx"),
+                                   _ptr(wsel, torch.float32, "wsel"), _ptr(v, dt, "v"),
+                                   _ptr(alpha, torch.float32, "alpha"),
+                                   _ptr(beta, torch.float32, "beta"), _ptr(banks, dt, "banks"),
+                                   _ptr(y, torch.float32, "y"), B, T, _ptr(ws, None, "ws"),
+                                   ws.numel() * ws.element_size(), int(spin_limit_cycles),
+                                   int(skip_item), _ptr(dev_status, torch.int32, "dev_status"),
+                                   _stream(stream)),
+           "sdm_scan_run_diag")
 
 
 def sdm_scan_noalloc(cfg: Cfg, idx, wsel, v, alpha, beta, banks, y, B: int, T: int, dev_status,
@@ -473,14 +491,18 @@ def sdm_slot_overlap(cfg: Cfg, idx, B: int, T: int, w0: int, w1: int, r0: int, r
 
 
 def sdm_decode_step(cfg: Cfg, params, x, alpha, beta, banks, y, ws, dev_status,
-                    stream=None) -> None:
+                    idx_out=None, w_out=None, stream=None) -> None:
+    """One token for each of B sequences; idx_out / w_out [B, 2, w] optionally receive
+    the slot sets and weights the step used."""
     dt = cfg.torch_dtype
     B = x.shape[0]
     w = _weights(cfg, params)
     _check(lib().sdm_decode_step(ctypes.byref(cfg), ctypes.byref(w), _ptr(x, dt, "x"),
                                  _ptr(alpha, torch.float32, "alpha"),
                                  _ptr(beta, torch.float32, "beta"), _ptr(banks, dt, "banks"),
-                                 _ptr(y, torch.float32, "y"), B, _ptr(ws, None, "ws"),
+                                 _ptr(y, torch.float32, "y"), B,
+                                 _ptr(idx_out, torch.int32, "idx_out"),
+                                 _ptr(w_out, torch.float32, "w_out"), _ptr(ws, None, "ws"),
                                  ws.numel() * ws.element_size(),
                                  _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)),
            "sdm_decode_step")

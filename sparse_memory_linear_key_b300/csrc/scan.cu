@@ -95,8 +95,14 @@ struct ScanArgs {
     unsigned char* tape;            // non-null: [B*T][W][d] pre-write values of the write
                                     // slots, for the backward pass
     long long items;                // B * T * nrb
+    long long spin_limit;           // bound of every wait, SM clock cycles
+    long long skip_item;            // diagnostics: an item never processed (-1: none)
     int B, T, d, N, nrb, rb_rows, win, ring_entries, chunk_bytes;
 };
+
+// How long a warp leaving an aborted kernel waits for the copies it started (cycles, about
+// two milliseconds): far longer than any copy takes to land.
+constexpr long long kDrainCycles = 4000000LL;
 
 // Everything about one item besides the chunks.
 struct __align__(16) Meta {
@@ -190,7 +196,7 @@ __device__ __forceinline__ float2 slot_group_sum(float2 v)
 
 __device__ __forceinline__ bool uniform_wait(uint32_t bar, uint32_t parity, const ScanArgs& a)
 {
-    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, a.abort_flag, a.status));
+    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, a.abort_flag, a.status, a.spin_limit));
 }
 
 // warp-uniform non-blocking test of an mbarrier phase
@@ -230,7 +236,8 @@ __device__ __forceinline__ bool window_geq(const ScanArgs& a, const int* fl, int
 #pragma unroll
     for (int q = 0; q < kMaxWindow / 32; ++q) {
         const int tt = lo + lane + 32 * q;
-        if (ok && got[q] < target && !spin_geq_gpu(fl + tt, target, a.abort_flag, a.status))
+        if (ok && got[q] < target &&
+            !spin_geq_gpu(fl + tt, target, a.abort_flag, a.status, a.spin_limit))
             ok = false;
     }
     return __all_sync(0xFFFFFFFFu, ok);
@@ -331,13 +338,19 @@ __device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
 {
     constexpr int JW = (W + 31) / 32;
     const int lane = threadIdx.x & 31;
-    Ahead<JW> nx;
-    {
+    // the next item in claim order (a withheld item, for diagnostics, is claimed and
+    // dropped: the tokens that depend on it then wait for it until their bound runs out)
+    auto claim = [&]() -> unsigned long long {
         unsigned long long item = 0;
-        if (lane == 0)
+        if (lane == 0) {
             item = atomicAdd(a.counter, 1ull);
-        fetch_ahead<W, JW>(a, __shfl_sync(0xFFFFFFFFu, item, 0), nx);
-    }
+            if (item == (unsigned long long)a.skip_item)
+                item = atomicAdd(a.counter, 1ull);
+        }
+        return __shfl_sync(0xFFFFFFFFu, item, 0);
+    };
+    Ahead<JW> nx;
+    fetch_ahead<W, JW>(a, claim(), nx);
     for (int k = 0;; ++k) {
         const int p = k & 1;
         Meta& m = meta[p];
@@ -421,10 +434,7 @@ __device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
             mbar_arrive(smem_u32(bars + kPosted + p));  // consumers and D may start on it
 
         // ---- the next item
-        unsigned long long next = 0;
-        if (lane == 0)
-            next = atomicAdd(a.counter, 1ull);
-        fetch_ahead<W, JW>(a, __shfl_sync(0xFFFFFFFFu, next, 0), nx);
+        fetch_ahead<W, JW>(a, claim(), nx);
     }
 }
 
@@ -439,8 +449,15 @@ __device__ void role_deps(const ScanArgs& a, unsigned char* wbuf, unsigned char*
     const int need = a.ring != nullptr ? 2 : 3;
     for (int k = 0;; ++k) {
         const int p = k & 1;
-        if (!uniform_wait(smem_u32(bars + kPosted + p), (k >> 1) & 1, a))
+        if (!uniform_wait(smem_u32(bars + kPosted + p), (k >> 1) & 1, a)) {
+            // aborted: the previous item's copies land before the CTA may end
+            if (k > 0 && lane == 0) {
+                mbar_drain(smem_u32(bars + kDepB + (p ^ 1)), ((k - 1) >> 1) & 1, kDrainCycles);
+                mbar_drain(smem_u32(bars + kDepR + (p ^ 1)), ((k - 1) >> 1) & 1, kDrainCycles);
+            }
+            __syncwarp();
             return;
+        }
         const Meta& m = meta[p];
         if (!m.valid)
             return;
@@ -485,7 +502,7 @@ __device__ void role_deps(const ScanArgs& a, unsigned char* wbuf, unsigned char*
             const int r = lane + 32 * q;
             const uint16_t c = m.code[r];
             const int tw = t - (c >> 8);
-            if (got[q] < need && !spin_geq_gpu(fl + tw, need, a.abort_flag, a.status)) {
+            if (got[q] < need && !spin_geq_gpu(fl + tw, need, a.abort_flag, a.status, a.spin_limit)) {
                 ok = false;
                 continue;
             }
@@ -515,8 +532,12 @@ __device__ void role_deps(const ScanArgs& a, unsigned char* wbuf, unsigned char*
                     mbar_complete_tx(depB, (uint32_t)mw);
                 if (mr > 0)
                     mbar_complete_tx(depR, (uint32_t)mr);
-                mbar_wait(depB, (k >> 1) & 1, nullptr, a.status);
-                mbar_wait(depR, (k >> 1) & 1, nullptr, a.status);
+                mbar_drain(depB, (k >> 1) & 1, kDrainCycles);
+                mbar_drain(depR, (k >> 1) & 1, kDrainCycles);
+                if (k > 0) {   // and the previous item's, if the consumers never took them
+                    mbar_drain(smem_u32(bars + kDepB + (p ^ 1)), ((k - 1) >> 1) & 1, kDrainCycles);
+                    mbar_drain(smem_u32(bars + kDepR + (p ^ 1)), ((k - 1) >> 1) & 1, kDrainCycles);
+                }
             }
             __syncwarp();
             return;
@@ -552,7 +573,7 @@ __device__ void role_clear(const ScanArgs& a, const Meta* meta, uint64_t* bars)
         for (int q = 0; q < 4; ++q) {
             const int dt = lane + 32 * q + 1;
             const bool need = (war[q >> 1] >> ((dt - 1) & 63)) & 1;
-            if (ok && need && !spin_geq_gpu(fl + t - dt, 1, a.abort_flag, a.status))
+            if (ok && need && !spin_geq_gpu(fl + t - dt, 1, a.abort_flag, a.status, a.spin_limit))
                 ok = false;
         }
         if (!__all_sync(0xFFFFFFFFu, ok))
@@ -629,7 +650,7 @@ __device__ void role_marks(const ScanArgs& a, const Meta* meta, uint64_t* bars)
         if (lane == 0) {
             if (ld_relaxed_gpu(a.abort_flag) != 0) {
                 stop = 1;
-            } else if (clock64() - idle > kSpinLimitCycles) {
+            } else if (clock64() - idle > a.spin_limit) {
                 report(a.status, SDM_ETIMEOUT);
                 st_relaxed_gpu(a.abort_flag, 1);
                 stop = 1;
@@ -663,7 +684,27 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
             mbar_arrive(cbar);
     };
     auto consumer_wait = [&](int k) -> bool {
-        return __all_sync(0xFFFFFFFFu, mbar_wait(cbar, k & 1, a.abort_flag, a.status));
+        return __all_sync(0xFFFFFFFFu,
+                          mbar_wait(cbar, k & 1, a.abort_flag, a.status, a.spin_limit));
+    };
+    int armed = -1;   // the last item whose bank gathers this warp has issued
+    // Leaving an aborted kernel at item k: the gathers this warp issued land first (item
+    // k's if its arrival was not yet seen, and item k+1's if already issued), each wait
+    // bounded: a phase that another warp never armed does not complete, and its wait
+    // runs to the bound, by which time every copy issued has long landed.
+    auto leave = [&](int k, bool seen) {
+        if (lane == 0) {
+            if (!seen && armed >= k) {
+                mbar_drain(smem_u32(bars + kFullW), k & 1, kDrainCycles);
+                mbar_drain(smem_u32(bars + kFullR + (k & 1)), (k >> 1) & 1, kDrainCycles);
+            }
+            if (armed == k + 1) {
+                mbar_drain(smem_u32(bars + kFullW), (k + 1) & 1, kDrainCycles);
+                mbar_drain(smem_u32(bars + kFullR + ((k + 1) & 1)), ((k + 1) >> 1) & 1,
+                           kDrainCycles);
+            }
+        }
+        __syncwarp();
     };
     // Bank gathers of item kn, split over the consumer warps (8 bulk copies a warp at
     // W = 64). The full barriers count one arrival per consumer warp: each warp declares
@@ -671,6 +712,7 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
     // land on a phase that does not expect it yet. For the empty end item each warp just
     // arrives.
     auto issue = [&](int kn) {
+        armed = kn;
         const int pn = kn & 1;
         const Meta& mn = meta[pn];
         const uint32_t fw = smem_u32(bars + kFullW), fr = smem_u32(bars + kFullR + pn);
@@ -720,8 +762,10 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
     for (int k = 0;; ++k) {
         const int p = k & 1;
         if (!uniform_wait(smem_u32(bars + kFullW), k & 1, a) ||
-            !uniform_wait(smem_u32(bars + kFullR + p), (k >> 1) & 1, a))
+            !uniform_wait(smem_u32(bars + kFullR + p), (k >> 1) & 1, a)) {
+            leave(k, false);
             return;
+        }
         const Meta& m = meta[p];
         if (!m.valid)
             return;
@@ -776,8 +820,10 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
         const bool bank_first = !uniform_test(smem_u32(bars + kDepB + p), (k >> 1) & 1);
         if (bank_first)
             y_bank();
-        if (!uniform_wait(smem_u32(bars + kDepB + p), (k >> 1) & 1, a))
+        if (!uniform_wait(smem_u32(bars + kDepB + p), (k >> 1) & 1, a)) {
+            leave(k, true);
             return;
+        }
         uint4 Mv[SPL];
 #pragma unroll
         for (int i = 0; i < SPL; ++i)
@@ -809,8 +855,10 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
                 u[h] = __ffma2_rn(make_float2(kw, kw), f[h], u[h]);
         }
         // every consumer has taken the write chunks: the buffer is free for item k+1
-        if (!consumer_wait(k))
+        if (!consumer_wait(k)) {
+            leave(k, true);
             return;
+        }
         if (ct == 0)
             mbar_arrive(smem_u32(bars + kWfree));
         const uint32_t posted_next = smem_u32(bars + kPosted + ((k + 1) & 1));
@@ -854,8 +902,10 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
             y_bank();
         if (y_rest) {
             // the read chunks D copies (writer still in flight when this item was described)
-            if (!uniform_wait(smem_u32(bars + kDepR + p), (k >> 1) & 1, a))
+            if (!uniform_wait(smem_u32(bars + kDepR + p), (k >> 1) & 1, a)) {
+                leave(k, true);
                 return;
+            }
             // own writes: the new value of write position pos is in the registers of slot
             // group pos % 8; that lane adds it, and a slot-group sum collects the terms
             float2 ye[HPL];
@@ -918,8 +968,10 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
         }
 
         // bank stores, once cleared
-        if (!uniform_wait(smem_u32(bars + kWar + p), (k >> 1) & 1, a))
+        if (!uniform_wait(smem_u32(bars + kWar + p), (k >> 1) & 1, a)) {
+            leave(k, true);
             return;
+        }
         S* bank = reinterpret_cast<S*>(a.banks) + (size_t)m.b * a.N * a.d +
                   (size_t)m.rb * a.rb_rows + rg * RPL;
         const unsigned long long dead = m.deadmask;
@@ -933,8 +985,10 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
         if (lane == 0)
             mbar_arrive(smem_u32(bars + kStored + p));
         if (!issued) {
-            if (!uniform_wait(lmark, k & 1, a) || !uniform_wait(posted_next, ((k + 1) >> 1) & 1, a))
+            if (!uniform_wait(lmark, k & 1, a) || !uniform_wait(posted_next, ((k + 1) >> 1) & 1, a)) {
+                leave(k, true);
                 return;
+            }
             issue(k + 1);
         }
     }
@@ -1049,7 +1103,8 @@ ScanWs scan_ws_layout(const sdm_cfg& c, int B, int T)
 cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel, const void* v,
                         const float* alpha, const float* beta, void* banks, float* y, int B,
                         int T, void* ws, size_t ws_bytes, int* status, cudaStream_t s,
-                        const void* m0, const int32_t* first_write, void* tape)
+                        const void* m0, const int32_t* first_write, void* tape,
+                        long long spin_limit, long long skip_item)
 {
     if (B <= 0 || T <= 0)
         return cudaSuccess;
@@ -1086,6 +1141,8 @@ cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel,
     a.ring_entries = L.ring_entries;
     a.chunk_bytes = L.chunk_bytes;
     a.items = (long long)B * T * a.nrb;
+    a.spin_limit = spin_limit > 0 ? spin_limit : kSpinLimitCycles;
+    a.skip_item = skip_item;
     const bool bf = c.dtype == SDM_BF16;
     switch (c.w) {
     case 8: return bf ? launch_scan_t<bf16, 8>(a, s) : launch_scan_t<float, 8>(a, s);

@@ -12,7 +12,8 @@
 //
 // The first call on each device looks up the array's device address with
 // cudaGetSymbolAddress (with that device current) and caches it; that first call
-// should come before any stream capture. The array is shared by every call: each call
+// should come before any stream capture. The cached address is not looked up again,
+// so it is stale after a cudaDeviceReset of that device (documented in the header). The array is shared by every call: each call
 // rewrites the codes it uses and clears the flags it uses (cudaMemsetAsync on the
 // caller's stream) before reading them, and calls whose work overlaps on the GPU race
 // on it.

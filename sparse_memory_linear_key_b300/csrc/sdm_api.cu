@@ -289,6 +289,21 @@ int sdm_scan_run(const sdm_cfg* cfg, const int32_t* idx, const float* wsel, cons
                                    (cudaStream_t)stream));
 }
 
+int sdm_scan_run_diag(const sdm_cfg* cfg, const int32_t* idx, const float* wsel, const void* v,
+                      const float* alpha, const float* beta, void* banks, float* y, int B, int T,
+                      const void* ws, size_t ws_bytes, long long spin_limit_cycles,
+                      long long skip_item, int* dev_status, void* stream)
+{
+    const int rc = check_scan_args(cfg, idx, wsel, v, alpha, beta, banks, y, B, T, ws, ws_bytes,
+                                   dev_status);
+    if (rc != SDM_OK || B == 0 || T == 0)
+        return rc;
+    return cuda_status(launch_scan(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T,
+                                   const_cast<void*>(ws), ws_bytes, dev_status,
+                                   (cudaStream_t)stream, nullptr, nullptr, nullptr,
+                                   spin_limit_cycles, skip_item < 0 ? -1 : skip_item));
+}
+
 int sdm_scan(const sdm_cfg* cfg, const int32_t* idx, const float* wsel, const void* v,
              const float* alpha, const float* beta, void* banks, float* y, int B, int T,
              void* ws, size_t ws_bytes, int* dev_status, void* stream)
@@ -658,10 +673,10 @@ int sdm_slot_overlap(const sdm_cfg* cfg, const int32_t* idx, int B, int T, int w
 }
 
 int sdm_decode_step(const sdm_cfg* cfg, const sdm_weights* w, const void* x, const float* alpha,
-                    const float* beta, void* banks, float* y, int B, void* ws, size_t ws_bytes,
-                    int* dev_status, void* stream)
+                    const float* beta, void* banks, float* y, int B, int32_t* idx_out,
+                    float* w_out, void* ws, size_t ws_bytes, int* dev_status, void* stream)
 {
-    return sdm_prefill(cfg, w, x, alpha, beta, banks, y, B, 1, nullptr, nullptr, ws, ws_bytes,
+    return sdm_prefill(cfg, w, x, alpha, beta, banks, y, B, 1, idx_out, w_out, ws, ws_bytes,
                        dev_status, stream);
 }
 

@@ -290,7 +290,8 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
 // Bounded wait for the phase of parity `parity` of an mbarrier. Returns false if the
 // global abort flag is raised (abort may be null: not watched) or the wait ran out;
 // a wait that ran out records SDM_ETIMEOUT and raises the abort flag.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* abort, int* status)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* abort, int* status,
+                                          long long limit = kSpinLimitCycles)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -300,7 +301,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* ab
             return true;
         if (abort != nullptr && ld_relaxed_gpu(abort) != 0)
             return false;
-        if (clock64() - t0 > kSpinLimitCycles) {
+        if (clock64() - t0 > limit) {
             report(status, SDM_ETIMEOUT);
             if (abort != nullptr)
                 st_relaxed_gpu(abort, 1);
@@ -311,7 +312,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* ab
 
 // Bounded wait until *f >= target (relaxed reads; the caller follows a successful wait
 // with fence_acq_rel_gpu() to make it an acquire).
-__device__ __forceinline__ bool spin_geq_gpu(const int* f, int target, int* abort, int* status)
+__device__ __forceinline__ bool spin_geq_gpu(const int* f, int target, int* abort, int* status,
+                                             long long limit = kSpinLimitCycles)
 {
     if (ld_relaxed_gpu(f) >= target)
         return true;
@@ -322,11 +324,21 @@ __device__ __forceinline__ bool spin_geq_gpu(const int* f, int target, int* abor
             return true;
         if (ld_relaxed_gpu(abort) != 0)
             return false;
-        if (clock64() - t0 > kSpinLimitCycles) {
+        if (clock64() - t0 > limit) {
             report(status, SDM_ETIMEOUT);
             st_relaxed_gpu(abort, 1);
             return false;
         }
+    }
+}
+
+// Wait for an mbarrier phase for at most `limit` cycles, ignoring the abort flag and
+// reporting nothing: used on the way out of an aborted kernel, to let copies this warp
+// started land before the CTA's shared memory is released.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, long long limit)
+{
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity) && clock64() - t0 <= limit) {
     }
 }
 

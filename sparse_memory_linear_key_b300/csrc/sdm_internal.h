@@ -70,7 +70,8 @@ cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel,
                         const float* alpha, const float* beta, void* banks, float* y, int B,
                         int T, void* ws, size_t ws_bytes, int* status, cudaStream_t s,
                         const void* m0 = nullptr, const int32_t* first_write = nullptr,
-                        void* tape = nullptr);
+                        void* tape = nullptr, long long spin_limit = 0,
+                        long long skip_item = -1);
 
 // Backward of the recurrence (scan_bwd.cu): reverse token order over a gradient bank;
 // ws holds per-block partial sums (scan_backward_ws_bytes).

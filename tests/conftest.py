@@ -1,3 +1,4 @@
+import json
 import os
 import sys
 
@@ -19,3 +20,17 @@ def cuda_ok():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     return True
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Slot-set parity counts of every workload the GPU tests checked against the
+    oracle: sampled tokens, mismatches a near-tie does not excuse (the tests fail on
+    any), and mismatches excused because the oracle's gap between the W-th and
+    (W+1)-th combined score is below 1e-5. One JSON line per workload and query kind."""
+    mod = sys.modules.get("tests.sdm_testlib")
+    recs = getattr(mod, "ADDRESS_REPORT", None) if mod is not None else None
+    if not recs:
+        return
+    terminalreporter.section("slot-set parity (near-ties counted)")
+    for r in recs:
+        terminalreporter.write_line(json.dumps(r))

@@ -164,13 +164,36 @@ def oracle_scan_rows(wl: synth.Workload, M0: torch.Tensor, out: Dict[str, torch.
     return y, M
 
 
-def sample_rows(d: int, k: int, seed: int = 0) -> np.ndarray:
-    """k rows spread over the machines (16-row slices) and lanes, plus both ends."""
+def sample_rows(d: int, k: int, seed: int = 0, elem_bytes: int = 2) -> np.ndarray:
+    """Bank rows to compare at full size. The scan splits every slot vector into 1 KB
+    row blocks (512 rows in bf16, 256 in fp32), and each block is an independent token
+    stream with its own flags, ring entries and M0 offsets. So every block contributes
+    its first row, its last row and one random interior row (the last block may be
+    partial), plus random rows over the whole width up to k, plus both ends."""
     rng = np.random.default_rng(seed)
+    rb = 1024 // elem_bytes
     r = set([0, d - 1])
-    while len(r) < min(k, d):
+    for b0 in range(0, d, rb):
+        b1 = min(d, b0 + rb)
+        r.update((b0, b1 - 1, int(rng.integers(b0, b1))))
+    while len(r) < min(max(k, len(r)), d):
         r.add(int(rng.integers(0, d)))
     return np.array(sorted(r))
+
+
+# ------------------------------------------------------------- near-tie report
+# The specification wants the slot-set mismatches that near-ties excuse counted and
+# reported. Tests add one record per checked workload; tests/conftest.py prints them all
+# at the end of the session (pytest's terminal summary, shown even with -q).
+
+ADDRESS_REPORT: list = []
+
+
+def report_address(name: str, kind: str, sampled: int, unexcused: int, excused: int,
+                   mode: str = "teacher-forced q") -> None:
+    ADDRESS_REPORT.append({"workload": name, "queries": kind, "mode": mode,
+                           "sampled_tokens": int(sampled), "unexcused_mismatches": int(unexcused),
+                           "near_tie_mismatches": int(excused)})
 
 
 def cos(a, b) -> float:

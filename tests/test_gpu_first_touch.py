@@ -28,7 +28,8 @@ def _garbage_like(t):
     return torch.randn(t.shape, generator=g, device="cuda").to(t.dtype) * 1e3
 
 
-@pytest.mark.parametrize("name", ["tiny-f32", "ragged-bf16", "w64-small", "n480-full-tiles"])
+@pytest.mark.parametrize("name", ["tiny-f32", "ragged-bf16", "w64-small", "n480-full-tiles",
+                                  "multiblock-bf16", "multiblock-f32"])
 def test_prefill_m0_matches_init_then_prefill(name):
     wl = SMALL[name]
     cfg = tl.cfg_of(wl)
@@ -84,7 +85,7 @@ def test_first_touch_table_is_the_first_writer():
     assert np.all(got[never] >= T)
 
 
-@pytest.mark.parametrize("name", ["ragged-f32", "n480-small-d"])
+@pytest.mark.parametrize("name", ["ragged-f32", "n480-small-d", "multiblock-bf16"])
 def test_staged_first_touch_matches_copy(name):
     """first_touch + scan_run_m0 + fill_untouched against init_bank + scan_run, on the
     minimum workspace (no forwarding ring) and on the full one."""
@@ -131,3 +132,55 @@ def test_prefill_m0_with_no_tokens_is_the_copy():
     torch.cuda.synchronize()
     for b in range(wl.B):
         assert torch.equal(banks[b], p["M0"])
+
+
+@pytest.mark.parametrize("name", ["multiblock-bf16", "multiblock-f32", "w64-small"])
+@pytest.mark.parametrize("staged", [False, True])
+def test_first_touch_against_oracle(name, staged):
+    """The fused path alone against the oracle, every row of every sequence: banks full
+    of garbage on entry, the scan reading M0 for slots not yet written in the sequence
+    (per row block: these workloads have two or three 1 KB blocks, the last partial),
+    never-written slots filled from M0 afterwards. The oracle starts each sequence from
+    M0 itself and is teacher-forced with the CUDA path's addressing and v bits."""
+    import oracle
+    wl = SMALL[name]
+    cfg = tl.cfg_of(wl)
+    p_cpu = synth.make_params(wl)
+    p = tl.to_dev(p_cpu)
+    tok = synth.make_tokens(wl)
+    B, T, ntok = wl.B, wl.T, wl.B * wl.T
+    x, al, be = tok["x"].cuda(), tok["alpha"].cuda(), tok["beta"].cuda()
+    dt = wl.torch_dtype
+    q_w = torch.empty(ntok, wl.dk, dtype=dt, device="cuda")
+    q_r = torch.empty_like(q_w)
+    v = torch.empty(ntok, wl.d, dtype=dt, device="cuda")
+    sdm.sdm_project(cfg, p, x.reshape(ntok, wl.d), q_w, q_r, v)
+    idx = torch.empty(ntok, 2, wl.W, dtype=torch.int32, device="cuda")
+    wsel = torch.empty(ntok, 2, wl.W, device="cuda")
+    st = sdm.new_status()
+    banks = _garbage_like(torch.empty(B, wl.N, wl.d, dtype=dt, device="cuda"))
+    y = torch.empty(ntok, wl.d, device="cuda")
+    if staged:
+        ws_a = sdm.alloc_workspace(sdm.address_workspace_bytes(cfg, ntok))
+        sdm.sdm_address(cfg, p["K1"], p["K2"], q_w, q_r, idx, wsel, ws_a, st)
+        fw = torch.empty(B, wl.N, dtype=torch.int32, device="cuda")
+        ws = sdm.alloc_workspace(sdm.scan_workspace_bytes(cfg, B, T))
+        sdm.sdm_first_touch(cfg, idx, B, T, fw)
+        sdm.sdm_scan_prepare(cfg, idx, B, T, ws, st)
+        sdm.sdm_scan_run_m0(cfg, idx, wsel, v, al, be, p["M0"], fw, banks, y, B, T, ws, st)
+        sdm.sdm_fill_untouched(cfg, p["M0"], fw, banks, B, T)
+    else:
+        ws = sdm.alloc_workspace(sdm.prefill_m0_workspace_bytes(cfg, B, T))
+        sdm.sdm_prefill_m0(cfg, p, p["M0"], x, al, be, banks, y.view(B, T, wl.d), ws, st,
+                           idx_out=idx, w_out=wsel)
+    torch.cuda.synchronize()
+    assert sdm.read_status(st) == 0
+    out = {"idx": idx, "wsel": wsel, "v": v, "alpha": al, "beta": be}
+    rows = np.arange(wl.d)
+    yg = y.cpu().numpy().reshape(B, T, wl.d)
+    for b in range(B):
+        yr, M = tl.oracle_scan_rows(wl, p_cpu["M0"], out, b, rows)
+        ok, m = tl.state_ok(wl.dtype, yg[b], yr)
+        assert ok, (name, staged, b, "y", m)
+        ok, m = tl.state_ok(wl.dtype, tl.bank_rows_cpu(banks, b, rows), oracle.to_f64(M))
+        assert ok, (name, staged, b, "bank", m)

@@ -41,7 +41,9 @@ def _check_projection(wl, p, tok, out, toks):
         assert tl.projection_ok(got, ref, oracle.to_f64(x), oracle.to_f64(p[w])), key
 
 
-def _check_address(wl, p, out, toks):
+def _check_address(wl, p, out, toks, name=None):
+    """Slot sets of the sampled tokens against the oracle scoring the CUDA path's own q
+    bits: exact except near-ties, which are counted and reported."""
     idx = out["idx"][torch.as_tensor(toks, device="cuda")].cpu().numpy()
     wsel = out["wsel"][torch.as_tensor(toks, device="cuda")].cpu().numpy()
     excused = 0
@@ -49,10 +51,27 @@ def _check_address(wl, p, out, toks):
         q = out[key][torch.as_tensor(toks, device="cuda")].cpu()
         S, k, _, gaps = oracle.address(q, p["K1"], p["K2"], wl.W)
         n_bad, n_exc, unexc = tl.set_parity(idx[:, kind], S, gaps)
+        tl.report_address(name or wl.name, ("write", "read")[kind], len(toks), len(unexc), n_exc)
         assert len(unexc) == 0, (kind, n_bad, n_exc)
         excused += n_exc
         assert tl.max_weight_err(idx[:, kind], wsel[:, kind], S, k, range(len(S))) <= tl.WEIGHT_ATOL
     return excused
+
+
+def _free_running_address(wl, p, tok, out, toks, name):
+    """The oracle's own projections and addressing (not teacher-forced with the CUDA
+    path's q bits) on the sampled tokens: the slot-set mismatches it finds are reported.
+    A bf16 query may differ by one ulp between the fp32-accumulated GEMM and the fp64 sum,
+    which moves scores by ~1e-3 and flips boundary slots for reasons unrelated to the
+    method, so only a gross count fails."""
+    x = tok["x"].reshape(-1, wl.d)[toks]
+    idx = out["idx"][torch.as_tensor(toks, device="cuda")].cpu().numpy()
+    for kind, w in ((0, "W_qw"), (1, "W_qr")):
+        S, _, _, gaps = oracle.address(oracle.project(x, p[w]), p["K1"], p["K2"], wl.W)
+        n_bad, n_exc, _ = tl.set_parity(idx[:, kind], S, gaps)
+        tl.report_address(name, ("write", "read")[kind], len(toks), n_bad - n_exc, n_exc,
+                          mode="free-running (oracle's own q)")
+        assert n_bad <= max(2, len(toks) // 10), (kind, n_bad)
 
 
 def _check_scan(wl, p, out, b, rows, T=None):
@@ -96,7 +115,9 @@ def test_full_prefill_workload(name):
         plain = plain[(plain < wl.pattern_read_at) | (plain >= wl.pattern_read_at + wl.pattern_len)]
     _check_projection(wl, p, tok, out, plain[:64])
     _check_address(wl, p, out, toks)
-    rows = tl.sample_rows(wl.d, N_ROWS, seed=2)
+    if name == "prefill-d2048-b4":
+        _free_running_address(wl, p, tok, out, plain[:128], name)
+    rows = tl.sample_rows(wl.d, N_ROWS, seed=2, elem_bytes=wl.elem_bytes)
     for b in range(wl.B):
         _check_scan(wl, p, out, b, rows)
     idx = out["idx"].cpu().numpy()
@@ -130,8 +151,10 @@ def test_full_prefill_workload(name):
 
 def test_full_decode_workload():
     """64 sequences: 1024 prior writes by a prefill, then 512 sdm_decode_step calls.
-    Oracle on sequences {0, 17, 42, 63} and sampled rows, teacher-forced with the
-    addressing that the same kernels give for the same inputs."""
+    Each step returns the slot sets and weights it used; on sampled steps they are
+    checked against the oracle scoring the step's own q bits (sdm_project of the same x
+    runs the same kernel), and the oracle's recurrence on sequences {0, 17, 42, 63} and
+    the block-complete sampled rows is teacher-forced with exactly those sets."""
     wl = synth.WORKLOADS["decode-d2048-b64"]
     cfg = tl.cfg_of(wl)
     p = synth.make_params(wl)
@@ -155,24 +178,32 @@ def test_full_decode_workload():
     sdm.sdm_project(cfg, pd, x0, qtmp, torch.empty_like(qtmp), v0)
     del qtmp, ws
     wsd = sdm.alloc_workspace(sdm.workspace_bytes(cfg, B, 1))
-    wsa = sdm.alloc_workspace(sdm.address_workspace_bytes(cfg, B))
     ydec = torch.empty(S, B, wl.d, device=dev)
     idxd = torch.empty(S, B, 2, wl.W, dtype=torch.int32, device=dev)
     wd = torch.empty(S, B, 2, wl.W, device=dev)
-    vd = torch.empty(S, B, wl.d, dtype=torch.bfloat16, device=dev)
-    qw = torch.empty(B, wl.dk, dtype=torch.bfloat16, device=dev)
-    qr = torch.empty_like(qw)
     xd = dec["x"].to(dev)
     ad = dec["alpha"].to(dev)
     bd = dec["beta"].to(dev)
     for s in range(S):
-        sdm.sdm_decode_step(cfg, pd, xd[s], ad[s], bd[s], banks, ydec[s], wsd, st)
-        # the addressing of this step, recomputed with the same kernels for the oracle
-        sdm.sdm_project(cfg, pd, xd[s], qw, qr, vd[s])
-        sdm.sdm_address(cfg, pd["K1"], pd["K2"], qw, qr, idxd[s], wd[s], wsa, st)
+        sdm.sdm_decode_step(cfg, pd, xd[s], ad[s], bd[s], banks, ydec[s], wsd, st,
+                            idx_out=idxd[s], w_out=wd[s])
+    # the step's v and q, by the same projection kernel on the same x
+    vd = torch.empty(S * B, wl.d, dtype=torch.bfloat16, device=dev)
+    qw = torch.empty(S * B, wl.dk, dtype=torch.bfloat16, device=dev)
+    qr = torch.empty_like(qw)
+    sdm.sdm_project(cfg, pd, xd.reshape(S * B, wl.d), qw, qr, vd)
     torch.cuda.synchronize()
     assert st.item() == 0
-    rows = tl.sample_rows(wl.d, N_ROWS, seed=3)
+    vd = vd.view(S, B, wl.d)
+    # the steps' own addressing against the oracle on 16 sampled steps (1,024 tokens)
+    steps = np.sort(np.random.default_rng(4).choice(S, 16, replace=False))
+    toks = (steps[:, None] * B + np.arange(B)[None, :]).ravel()
+    tt = torch.as_tensor(toks, device=dev)
+    out = {"idx": idxd.view(S * B, 2, wl.W), "wsel": wd.view(S * B, 2, wl.W), "q_w": qw,
+           "q_r": qr}
+    _check_address(wl, p, out, toks, name="decode-d2048-b64 (steps' own sets)")
+    del tt
+    rows = tl.sample_rows(wl.d, N_ROWS, seed=3, elem_bytes=wl.elem_bytes)
     rt = torch.as_tensor(rows, device=dev)
     for b in (0, 17, 42, 63):
         idx_b = np.concatenate([idx0[b * T:(b + 1) * T].cpu().numpy(), idxd[:, b].cpu().numpy()])
@@ -189,3 +220,59 @@ def test_full_decode_workload():
         assert ok, ("y", b, m)
         ok, m = tl.state_ok("bf16", tl.bank_rows_cpu(banks, b, rows), oracle.to_f64(M))
         assert ok, ("bank", b, m)
+
+
+def test_full_prefill_from_m0():
+    """The benchmarked path -- bank initialisation fused into the scan as first touch --
+    against the oracle at the full size of the benchmarked workload (4 x 4096 tokens,
+    d = 2048: four 1 KB row blocks per slot vector), through both the one-call
+    sdm_prefill_m0 and the staged sdm_first_touch + sdm_scan_run_m0 + sdm_fill_untouched,
+    with banks full of garbage on entry. Addressing on sampled tokens, y and the final
+    banks on the block-complete sampled rows of every sequence."""
+    name = "prefill-d2048-b4"
+    wl = synth.WORKLOADS[name]
+    cfg = tl.cfg_of(wl)
+    p = synth.make_params(wl)
+    tok = synth.make_tokens(wl)
+    pd = tl.to_dev(p)
+    dev = "cuda"
+    B, T, ntok = wl.B, wl.T, wl.B * wl.T
+    x = tok["x"].to(dev)
+    al = tok["alpha"].to(dev)
+    be = tok["beta"].to(dev)
+    q_w = torch.empty(ntok, wl.dk, dtype=torch.bfloat16, device=dev)
+    q_r = torch.empty_like(q_w)
+    v = torch.empty(ntok, wl.d, dtype=torch.bfloat16, device=dev)
+    sdm.sdm_project(cfg, pd, x.reshape(ntok, wl.d), q_w, q_r, v)
+    rows = tl.sample_rows(wl.d, N_ROWS, seed=5, elem_bytes=wl.elem_bytes)
+    toks = np.sort(np.random.default_rng(6).choice(ntok, 128, replace=False))
+    st = sdm.new_status()
+    banks = torch.empty(B, wl.N, wl.d, dtype=torch.bfloat16, device=dev)
+    for staged in (False, True):
+        banks.fill_(float("nan"))          # content on entry is ignored
+        y = torch.empty(ntok, wl.d, device=dev)
+        idx = torch.empty(ntok, 2, wl.W, dtype=torch.int32, device=dev)
+        wsel = torch.empty(ntok, 2, wl.W, device=dev)
+        if staged:
+            ws_a = sdm.alloc_workspace(sdm.address_workspace_bytes(cfg, ntok))
+            sdm.sdm_address(cfg, pd["K1"], pd["K2"], q_w, q_r, idx, wsel, ws_a, st)
+            del ws_a
+            fw = torch.empty(B, wl.N, dtype=torch.int32, device=dev)
+            ws = sdm.alloc_workspace(sdm.scan_workspace_bytes(cfg, B, T))
+            sdm.sdm_first_touch(cfg, idx, B, T, fw)
+            sdm.sdm_scan_prepare(cfg, idx, B, T, ws, st)
+            sdm.sdm_scan_run_m0(cfg, idx, wsel, v, al, be, pd["M0"], fw, banks, y, B, T, ws, st)
+            sdm.sdm_fill_untouched(cfg, pd["M0"], fw, banks, B, T)
+        else:
+            ws = sdm.alloc_workspace(sdm.prefill_m0_workspace_bytes(cfg, B, T))
+            sdm.sdm_prefill_m0(cfg, pd, pd["M0"], x, al, be, banks, y, ws, st, idx_out=idx,
+                               w_out=wsel)
+        torch.cuda.synchronize()
+        assert sdm.read_status(st) == 0
+        del ws
+        out = {"idx": idx, "wsel": wsel, "q_w": q_w, "q_r": q_r, "v": v, "alpha": al,
+               "beta": be, "y": y, "banks": banks}
+        if not staged:
+            _check_address(wl, p, out, toks, name=name + " (sdm_prefill_m0)")
+        for b in range(B):
+            _check_scan(wl, p, out, b, rows)

@@ -34,6 +34,12 @@ SMALL = {
     # of 32), with a ragged last tile
     "n480-full-tiles": synth.Workload("n480-full-tiles", B=4, T=700, d=32, n=480, dk=256,
                                       W=64, dtype="bf16", seed=82),
+    # slot vectors wider than one 1 KB row block of the scan, the last block partial:
+    # bf16 d = 1280 is blocks of 512, 512 and 256 rows; fp32 d = 640 is 256, 256 and 128
+    "multiblock-bf16": synth.Workload("multiblock-bf16", B=2, T=150, d=1280, n=24, dk=32,
+                                      W=16, dtype="bf16", seed=83),
+    "multiblock-f32": synth.Workload("multiblock-f32", B=2, T=130, d=640, n=16, dk=32, W=8,
+                                     dtype="f32", seed=84),
 }
 
 
@@ -93,6 +99,7 @@ def test_address_parity(name):
     for kind, key in ((0, "q_w"), (1, "q_r")):
         S, k, _, gaps = oracle.address(out[key].cpu(), p["K1"], p["K2"], wl.W)
         n_bad, n_exc, unexc = tl.set_parity(idx[:, kind], S, gaps)
+        tl.report_address(name, ("write", "read")[kind], wl.B * wl.T, len(unexc), n_exc)
         assert len(unexc) == 0, (name, kind, unexc[:5], n_bad, n_exc)
         err = tl.max_weight_err(idx[:, kind], wsel[:, kind], S, k, range(len(S)))
         assert err <= tl.WEIGHT_ATOL, (name, kind, err)
@@ -181,6 +188,8 @@ def test_tiny_f32_free_running():
     idx = out["idx"].cpu().numpy()
     for kind, S, g in ((0, ref["S"], ref["gap_w"]), (1, ref["R"], ref["gap_r"])):
         n_bad, n_exc, unexc = tl.set_parity(idx[:, kind], S, g)
+        tl.report_address(wl.name, ("write", "read")[kind], wl.B * wl.T, n_bad - n_exc, n_exc,
+                          mode="free-running (oracle's own q)")
         assert n_bad == 0, (kind, n_bad, n_exc)
     y = out["y"].cpu().numpy()
     assert np.abs(y - ref["y"]).max() <= tl.F32_ATOL

@@ -25,7 +25,8 @@ def _load(name):
 # ---------------------------------------------------------------- bf16 storage
 
 def test_bf16_rounding_matches_fp32_cast_on_floats():
-    """Storage rounding (SPEC 'Storage'): for values that are already fp32, rounding
+    """Storage rounding (the state is stored in bf16, each written value rounded once to
+nearest, ties to even): for values that are already fp32, rounding
     to bf16 must equal the standard fp32 -> bf16 round-to-nearest-even cast."""
     rng = np.random.default_rng(0)
     bits = rng.integers(0, 2**32, size=200000, dtype=np.uint64).astype(np.uint32)
@@ -135,7 +136,8 @@ def _pruned_topw(s1, s2, W):
 
 @pytest.mark.parametrize("seed", range(12))
 def test_product_key_route_is_exact(seed):
-    """SPEC property 7: with W <= n, pruning to per-half top-W and rank products
+    """The product-key route ("Write & Read": two sub-keys -> outer sum -> top-k): with
+    W <= n, pruning to per-half top-W and rank products
     a*b <= W keeps the exact top-W of all n^2 sums (continuous scores, no ties)."""
     rng = np.random.default_rng(100 + seed)
     n = int(rng.integers(8, 65))
@@ -231,7 +233,8 @@ def test_idempotence_invariant():
 
 def test_read_after_write_closed_form():
     """R = S, r = k: y = alpha (1 - beta |k|^2) u + beta |k|^2 v, u = M_S k before
-    the write (SPEC property 3; softmax weights, so |k| < 1)."""
+    the write (the read follows this token's write, "How does SDM work?"; softmax weights,
+    so |k| < 1)."""
     rng = np.random.default_rng(13)
     N, R, W = 200, 10, 16
     for _ in range(5):
@@ -287,7 +290,8 @@ def test_disjoint_tokens_commute():
 
 
 def test_row_subset_is_independent():
-    """SPEC property 6: rows of M and y evolve independently (bits, bf16 storage)."""
+    """Rows of M and y evolve independently: the delta rule and the read act on each row
+    of the selected slot vectors separately (bits, bf16 storage)."""
     rng = np.random.default_rng(16)
     N, d, W, T = 64, 24, 8, 20
     M0 = torch.randn(N, d, generator=torch.Generator().manual_seed(1)).mul(0.1).to(torch.bfloat16)
