@@ -105,7 +105,8 @@ SDM_API int sdm_init_bank(const sdm_cfg* cfg, const void* M0, void* banks, int B
 /* Projections ("Write & Read": the token embedding is projected to write keys; a
  * separate query projection selects the read slots): for ntok tokens
  *   q_w = x W_qw [ntok, dk], q_r = x W_qr [ntok, dk], v = x W_v [ntok, d],
- * fp32 accumulation, rounded once (bf16 RNE in SDM_BF16). x [ntok, d]. */
+ * fp32 accumulation, rounded once (bf16 RNE in SDM_BF16). x [ntok, d]. The order of the
+ * fp32 sums depends only on (cfg, ntok): the same shape always gives the same bits. */
 SDM_API int sdm_project(const sdm_cfg* cfg, const sdm_weights* wts, const void* x, int64_t ntok,
                 void* q_w, void* q_r, void* v, void* stream);
 
@@ -194,9 +195,8 @@ SDM_API int sdm_scan_noalloc(const sdm_cfg* cfg, const int32_t* idx, const float
                              void* stream);
 
 /* Whole layer over a prefill of B sequences of T tokens: sdm_project, sdm_address and
- * sdm_scan in one call. Everything, cuBLAS's scratch included, lives in ws, so once a
- * first call on a device has set up its cuBLAS handle, later calls (and
- * sdm_decode_step) can be captured in a CUDA graph. x [B, T, d], alpha/beta [B, T], banks [B, N, d] (in place),
+ * sdm_scan in one call. All scratch lives in ws: the call (like sdm_decode_step)
+ * allocates nothing and synchronises nothing, so it can be captured in a CUDA graph. x [B, T, d], alpha/beta [B, T], banks [B, N, d] (in place),
  * y [B, T, d] fp32. idx_out [B, T, 2, w] / w_out [B, T, 2, w] optional (NULL = not
  * returned). ws: sdm_workspace_bytes(cfg, B, T) bytes. */
 SDM_API int sdm_prefill(const sdm_cfg* cfg, const sdm_weights* wts, const void* x, const float* alpha,

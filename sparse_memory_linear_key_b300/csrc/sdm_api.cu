@@ -52,7 +52,7 @@ static int cuda_status(cudaError_t e) { return e == cudaSuccess ? SDM_OK : SDM_E
 
 // Workspace layout of a prefill / decode call over B sequences of T tokens.
 struct PrefillWs {
-    size_t q_w, q_r, v, idx, wsel, scan, addr, blas, total;
+    size_t q_w, q_r, v, idx, wsel, scan, addr, total;
 };
 
 static PrefillWs prefill_layout(const sdm_cfg& c, int B, int T)
@@ -68,7 +68,6 @@ static PrefillWs prefill_layout(const sdm_cfg& c, int B, int T)
     L.wsel = o; o += align256((size_t)ntok * W2 * 4);
     L.scan = o; o += scan_ws_layout(c, B, T).total;
     L.addr = o; o += align256(address_ws_bytes(c, ntok));
-    L.blas = o; o += kBlasWsBytes;
     L.total = o;
     return L;
 }
@@ -180,7 +179,9 @@ int sdm_project(const sdm_cfg* cfg, const sdm_weights* w, const void* x, int64_t
     for (const void* p : ptrs)
         if (p == nullptr || !aligned16(p))
             return SDM_EINVAL;
-    return launch_project(*cfg, *w, x, ntok, q_w, q_r, v, (cudaStream_t)stream);
+    if (ntok > 0x7FFFFFFF)
+        return SDM_EUNSUPPORTED;
+    return cuda_status(launch_project_tc(*cfg, *w, x, ntok, q_w, q_r, v, (cudaStream_t)stream));
 }
 
 int sdm_address(const sdm_cfg* cfg, const void* K1, const void* K2, const void* q_w,
@@ -209,8 +210,7 @@ int sdm_address(const sdm_cfg* cfg, const void* K1, const void* K2, const void* 
 static int scan_impl(const sdm_cfg& c, const int32_t* idx, const float* wsel, const void* v,
                      const float* alpha, const float* beta, void* banks, float* y, int B, int T,
                      void* ws, size_t ws_bytes, int* dev_status, cudaStream_t s,
-                     cudaEvent_t v_ready = nullptr, const void* m0 = nullptr,
-                     const int32_t* first_write = nullptr)
+                     const void* m0 = nullptr, const int32_t* first_write = nullptr)
 {
     const ScanWs L = scan_ws_layout(c, B, T);
     char* base = (char*)ws;
@@ -218,9 +218,6 @@ static int scan_impl(const sdm_cfg& c, const int32_t* idx, const float* wsel, co
     cudaError_t e = T > 1 ? launch_scan_codes(c, idx, B, T, L.win, (uint16_t*)(base + L.codes),
                                               (unsigned long long*)(base + L.masks), dev_status, s)
                           : cudaSuccess;
-    // v comes from a projection forked off the stream: the scan is its first reader
-    if (v_ready != nullptr && cudaStreamWaitEvent(s, v_ready, 0) != cudaSuccess)
-        return SDM_ECUDA;
     if (e != cudaSuccess)
         return SDM_ECUDA;
     e = launch_scan(c, idx, wsel, v, alpha, beta, banks, y, B, T, ws, ws_bytes, dev_status, s, m0,
@@ -425,25 +422,15 @@ static int prefill_impl(const sdm_cfg* cfg, const sdm_weights* w, const void* M0
     float* wsel = w_out ? w_out : (float*)(base + L.wsel);
 
     cudaStream_t s = (cudaStream_t)stream;
-    // the projections fork off the stream and join it again (v before the scan); the
-    // lock keeps another thread's call off the fork's events until the join is enqueued
-    std::unique_lock<std::mutex> lock;
-    cudaEvent_t v_ready = nullptr;
-    rc = launch_project_forked(*cfg, *w, x, ntok, q_w, q_r, v, s, base + L.blas, kBlasWsBytes, lock,
-                               &v_ready);
-    if (rc != SDM_OK) {
-        if (v_ready != nullptr)
-            cudaStreamWaitEvent(s, v_ready, 0);
-        return rc;
-    }
-    if (launch_address(*cfg, w->K1, w->K2, q_w, q_r, ntok, idx, wsel, base + L.addr, dev_status,
+    if (ntok > 0x7FFFFFFF)
+        return SDM_EUNSUPPORTED;
+    if (launch_project_tc(*cfg, *w, x, ntok, q_w, q_r, v, s) != cudaSuccess ||
+        launch_address(*cfg, w->K1, w->K2, q_w, q_r, ntok, idx, wsel, base + L.addr, dev_status,
                        s) != cudaSuccess ||
-        (M0 != nullptr && launch_first_touch(*cfg, idx, B, T, first_write, s) != cudaSuccess)) {
-        cudaStreamWaitEvent(s, v_ready, 0);
+        (M0 != nullptr && launch_first_touch(*cfg, idx, B, T, first_write, s) != cudaSuccess))
         return SDM_ECUDA;
-    }
     rc = scan_impl(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, base + L.scan,
-                   scan_ws_layout(*cfg, B, T).total, dev_status, s, v_ready, M0, first_write);
+                   scan_ws_layout(*cfg, B, T).total, dev_status, s, M0, first_write);
     if (rc != SDM_OK || M0 == nullptr)
         return rc;
     return cuda_status(launch_fill_untouched(*cfg, M0, first_write, banks, B, T, s));

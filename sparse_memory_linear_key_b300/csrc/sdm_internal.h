@@ -22,19 +22,10 @@ constexpr uint16_t kNoFwd = 0xFFFF;
 cudaError_t launch_bank_init(const void* M0, void* banks, size_t bank_bytes, int B,
                              cudaStream_t s);
 
-// ---- projections (project.cu)
-// blas_ws (may be null: cuBLAS's own workspace) is a region of the caller's workspace
-constexpr size_t kBlasWsBytes = (size_t)32 << 20;
-int launch_project(const sdm_cfg& c, const sdm_weights& w, const void* x, int64_t ntok,
-                   void* q_w, void* q_r, void* v, cudaStream_t s, void* blas_ws = nullptr,
-                   size_t blas_ws_bytes = 0);
-// The same three GEMMs forked over two side streams (sdm_prefill / sdm_decode_step):
-// returns with `lock` held and *v_ready the event that v is done on; the caller makes its
-// stream wait for it before the scan, then releases the lock (the events are per device).
-int launch_project_forked(const sdm_cfg& c, const sdm_weights& w, const void* x, int64_t ntok,
-                          void* q_w, void* q_r, void* v, cudaStream_t s, void* blas_ws,
-                          size_t blas_ws_bytes, std::unique_lock<std::mutex>& lock,
-                          cudaEvent_t* v_ready);
+// ---- projections (proj_tc.cu): q_w, q_r, v of ntok tokens in one launch (bf16: tcgen05
+// tensor cores; fp32: SIMT fp32)
+cudaError_t launch_project_tc(const sdm_cfg& c, const sdm_weights& w, const void* x, int64_t ntok,
+                              void* q_w, void* q_r, void* v, cudaStream_t s);
 
 // ---- addressing (address.cu, score_tc.cu)
 bool score_tc_supported(const sdm_cfg& c);

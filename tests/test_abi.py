@@ -58,8 +58,7 @@ def test_workspace_sizes(L):
     # q_w, q_r, v (bf16), idx + wsel (int32/fp32), the scan's workspace, half lists
     front = ntok * (2 * 256 * 2 + 2048 * 2 + 128 * 4 * 2) + 2 * ntok * 2 * 64 * 8
     scan = sdm.scan_workspace_bytes(c, 4, 4096)
-    blas = 32 << 20                      # cuBLAS scratch of the projections
-    assert front + scan + blas <= ws <= front + scan + blas + 8 * 256
+    assert front + scan <= ws <= front + scan + 8 * 256
     # scan: codes (uint16), four ordering masks (uint64), one progress flag per token
     # and 1 KB row block (4 blocks at d = 2048 bf16), then the forwarding ring (whole
     # 1 KB chunks of up to 64 slots per ring entry, 4 sequences x 4 blocks, 16..256

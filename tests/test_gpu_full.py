@@ -187,14 +187,19 @@ def test_full_decode_workload():
     for s in range(S):
         sdm.sdm_decode_step(cfg, pd, xd[s], ad[s], bd[s], banks, ydec[s], wsd, st,
                             idx_out=idxd[s], w_out=wd[s])
-    # the step's v and q, by the same projection kernel on the same x
-    vd = torch.empty(S * B, wl.d, dtype=torch.bfloat16, device=dev)
-    qw = torch.empty(S * B, wl.dk, dtype=torch.bfloat16, device=dev)
+    # each step's v and q, by the same projection kernel on the same x and the same shape
+    # (B tokens a call: the projection's summation order depends on the shape only)
+    vd = torch.empty(S, B, wl.d, dtype=torch.bfloat16, device=dev)
+    qw = torch.empty(S, B, wl.dk, dtype=torch.bfloat16, device=dev)
     qr = torch.empty_like(qw)
-    sdm.sdm_project(cfg, pd, xd.reshape(S * B, wl.d), qw, qr, vd)
+    for s in range(S):
+        sdm.sdm_project(cfg, pd, xd[s], qw[s], qr[s], vd[s])
     torch.cuda.synchronize()
     assert st.item() == 0
-    vd = vd.view(S, B, wl.d)
+    qw, qr = qw.view(S * B, wl.dk), qr.view(S * B, wl.dk)
+    # the projections of the decode shape against the oracle on one step
+    _check_projection(wl, p, {"x": dec["x"][5]},
+                      {"q_w": qw[5 * B:6 * B], "q_r": qr[5 * B:6 * B], "v": vd[5]}, np.arange(B))
     # the steps' own addressing against the oracle on 16 sampled steps (1,024 tokens)
     steps = np.sort(np.random.default_rng(4).choice(S, 16, replace=False))
     toks = (steps[:, None] * B + np.arange(B)[None, :]).ravel()

@@ -337,7 +337,7 @@ def test_out_of_range_slot_is_reported_not_faulted():
 
 
 def test_decode_steps_captured_in_a_graph_match_eager():
-    """sdm_decode_step allocates nothing (cuBLAS works in the caller's workspace), so a
+    """sdm_decode_step allocates nothing (all scratch is in the caller's workspace), so a
     sequence of decode steps can be captured in a CUDA graph after a first call; the
     replay gives the same bits as the eager calls."""
     wl = synth.Workload("g", B=8, T=6, d=64, n=32, dk=64, W=16, dtype="bf16", seed=77)
