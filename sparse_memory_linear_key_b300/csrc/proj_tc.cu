@@ -325,7 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1) proj_tc_kernel(
         const int row = q * 32 + lane;
         const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
         float* red = reinterpret_cast<float*>(sp);     // split: fp32 partial tile, reuses stages
-        if (split && nkb == 0) {
+        // split: rows past the batch are not needed in the partial tile
+        int rows_needed = kBM;
+        if (split) {
+            int j, n0, m0;
+            tile_coords(a, first_tile, j, n0, m0);
+            rows_needed = min(kBM, a.M - m0);
+        }
+        if (split && nkb == 0 && row < rows_needed) {
             // (a CTA without K blocks contributes zeros)
             for (int c0 = 0; c0 < kBN; c0 += 4)
                 *reinterpret_cast<float4*>(red + (size_t)row * kRedStride + c0) =
@@ -344,8 +351,12 @@ __global__ void __launch_bounds__(kThreads, 1) proj_tc_kernel(
             const int m = m0 + row;
             uint32_t v[32];
             for (int c0 = 0; c0 < kBN; c0 += 32) {
+                if (split && q * 32 >= rows_needed)
+                    break;                                   // (warp-uniform)
                 tmem_ld32(trow + acc * kBN + c0, v);
                 if (split) {
+                    if (row >= rows_needed)
+                        continue;
                     float4* dst = reinterpret_cast<float4*>(red + (size_t)row * kRedStride + c0);
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
@@ -390,13 +401,22 @@ __global__ void __launch_bounds__(kThreads, 1) proj_tc_kernel(
             for (int e = threadIdx.x; e < (r1 - r0) * groups; e += kThreads) {
                 const int r = r0 + e / groups, c = (e % groups) * 8;
                 const uint32_t la = red0 + (uint32_t)(r * kRedStride + c) * 4u;
+                // every source's partial in flight at once, then summed in rank order
+                float4 p[2 * kMaxSplit];
+#pragma unroll
+                for (int src = 0; src < kMaxSplit; ++src)
+                    if (src < a.split) {
+                        p[2 * src] = ld_dsmem_f4(la, (uint32_t)src);
+                        p[2 * src + 1] = ld_dsmem_f4(la + 16, (uint32_t)src);
+                    }
                 float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
-                for (int src = 0; src < a.split; ++src) {
-                    const float4 p0 = ld_dsmem_f4(la, (uint32_t)src);
-                    const float4 p1 = ld_dsmem_f4(la + 16, (uint32_t)src);
-                    s0.x += p0.x; s0.y += p0.y; s0.z += p0.z; s0.w += p0.w;
-                    s1.x += p1.x; s1.y += p1.y; s1.z += p1.z; s1.w += p1.w;
-                }
+#pragma unroll
+                for (int src = 0; src < kMaxSplit; ++src)
+                    if (src < a.split) {
+                        const float4 p0 = p[2 * src], p1 = p[2 * src + 1];
+                        s0.x += p0.x; s0.y += p0.y; s0.z += p0.z; s0.w += p0.w;
+                        s1.x += p1.x; s1.y += p1.y; s1.z += p1.z; s1.w += p1.w;
+                    }
                 uint4 o = make_uint4(pack_bf16x2(s0.x, s0.y), pack_bf16x2(s0.z, s0.w),
                                      pack_bf16x2(s1.x, s1.y), pack_bf16x2(s1.z, s1.w));
                 __stcs(reinterpret_cast<uint4*>(static_cast<bf16*>(mat.out) + (size_t)(m0 + r) * mat.n + n0 + c), o);
@@ -515,11 +535,15 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uin
 static size_t proj_smem_bytes() { return 1024 + (size_t)kStages * kStageBytes + (2 * kStages + 4) * 8 + 16; }
 
 // CTAs per tile: a cluster per tile along K once the tiles of the whole-K kernel would
-// leave most SMs idle (few tokens). A function of the shape only, so that the same
-// shape always takes the same path and gives the same bits.
-static int proj_split_for(int64_t tiles, int kblocks)
+// leave most SMs idle (few tokens). A function of the layer's shape and the token count
+// only (all three products counted, whichever a launch computes), so that the same shape
+// always takes the same path and gives the same bits.
+static int proj_split_for(const sdm_cfg& c, int64_t ntok)
 {
     const int sms = num_sms_current_device();
+    const int64_t mtiles = (ntok + kBM - 1) / kBM;
+    const int64_t tiles = mtiles * (2 * ((c.dk + kBN - 1) / kBN) + (c.d + kBN - 1) / kBN);
+    const int kblocks = (c.d + kBK - 1) / kBK;
     if (tiles * 2 >= sms)
         return 1;
     int s = kMaxSplit;
@@ -529,37 +553,47 @@ static int proj_split_for(int64_t tiles, int kblocks)
 }
 
 cudaError_t launch_project_tc(const sdm_cfg& c, const sdm_weights& w, const void* x, int64_t ntok,
-                              void* q_w, void* q_r, void* v, cudaStream_t s)
+                              void* q_w, void* q_r, void* v, cudaStream_t s, int which)
 {
-    if (ntok <= 0)
+    if (ntok <= 0 || (which & 7) == 0)
         return cudaSuccess;
+    const void* wts[3] = {w.W_qw, w.W_qr, w.W_v};
+    void* outs[3] = {q_w, q_r, v};
+    const int ns[3] = {c.dk, c.dk, c.d};
+    int sel[3], nsel = 0;                  // the products this launch computes, in order
+    for (int j = 0; j < 3; ++j)
+        if (which & (1 << j))
+            sel[nsel++] = j;
     if (c.dtype != SDM_BF16) {
         F32Mats fm;
-        fm.w[0] = (const float*)w.W_qw; fm.w[1] = (const float*)w.W_qr; fm.w[2] = (const float*)w.W_v;
-        fm.out[0] = (float*)q_w; fm.out[1] = (float*)q_r; fm.out[2] = (float*)v;
-        fm.n[0] = c.dk; fm.n[1] = c.dk; fm.n[2] = c.d;
-        const int nmax = c.d > c.dk ? c.d : c.dk;
-        dim3 grid((unsigned)((nmax + 63) / 64), (unsigned)((ntok + 63) / 64), 3);
+        int nmax = 0;
+        for (int q = 0; q < 3; ++q) {
+            const int j = sel[q < nsel ? q : 0];
+            fm.w[q] = (const float*)wts[j];
+            fm.out[q] = (float*)outs[j];
+            fm.n[q] = ns[j];
+            nmax = ns[j] > nmax ? ns[j] : nmax;
+        }
+        dim3 grid((unsigned)((nmax + 63) / 64), (unsigned)((ntok + 63) / 64), (unsigned)nsel);
         if (grid.y > 65535u)
             return cudaErrorInvalidValue;
         proj_f32_kernel<<<grid, 256, 0, s>>>((const float*)x, fm, (int)ntok, c.d);
         return cudaGetLastError();
     }
-    CUtensorMap mx, m0, m1, m2;
-    if (!make_map(&mx, x, (uint64_t)c.d, (uint64_t)ntok, kBM) ||
-        !make_map(&m0, w.W_qw, (uint64_t)c.dk, (uint64_t)c.d, kBK) ||
-        !make_map(&m1, w.W_qr, (uint64_t)c.dk, (uint64_t)c.d, kBK) ||
-        !make_map(&m2, w.W_v, (uint64_t)c.d, (uint64_t)c.d, kBK))
+    CUtensorMap mx, mw[3];
+    if (!make_map(&mx, x, (uint64_t)c.d, (uint64_t)ntok, kBM))
         return cudaErrorInvalidValue;
     ProjArgs a;
-    void* outs[3] = {q_w, q_r, v};
-    const int ns[3] = {c.dk, c.dk, c.d};
     int ntiles = 0;
-    for (int j = 0; j < 3; ++j) {
-        a.mat[j].out = outs[j];
-        a.mat[j].n = ns[j];
-        a.mat[j].ntiles = (ns[j] + kBN - 1) / kBN;
-        ntiles += a.mat[j].ntiles;
+    for (int q = 0; q < 3; ++q) {
+        const bool used = q < nsel;
+        const int j = sel[used ? q : 0];
+        if (!make_map(&mw[q], wts[j], (uint64_t)ns[j], (uint64_t)c.d, kBK))
+            return cudaErrorInvalidValue;
+        a.mat[q].out = outs[j];
+        a.mat[q].n = ns[j];
+        a.mat[q].ntiles = used ? (ns[j] + kBN - 1) / kBN : 0;
+        ntiles += a.mat[q].ntiles;
     }
     a.M = (int)ntok;
     a.K = c.d;
@@ -567,7 +601,7 @@ cudaError_t launch_project_tc(const sdm_cfg& c, const sdm_weights& w, const void
     a.mtiles = (int)((ntok + kBM - 1) / kBM);
     a.tiles = a.mtiles * ntiles;
     a.status = nullptr;
-    a.split = proj_split_for(a.tiles, a.kblocks);
+    a.split = proj_split_for(c, ntok);
     const size_t smem = proj_smem_bytes();
     cudaError_t e = cudaFuncSetAttribute(proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
@@ -577,7 +611,7 @@ cudaError_t launch_project_tc(const sdm_cfg& c, const sdm_weights& w, const void
         int grid = num_sms_current_device();
         if (grid > a.tiles)
             grid = a.tiles;
-        proj_tc_kernel<<<grid, kThreads, smem, s>>>(mx, m0, m1, m2, a);
+        proj_tc_kernel<<<grid, kThreads, smem, s>>>(mx, mw[0], mw[1], mw[2], a);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -592,7 +626,7 @@ cudaError_t launch_project_tc(const sdm_cfg& c, const sdm_weights& w, const void
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, proj_tc_kernel, mx, m0, m1, m2, a);
+    return cudaLaunchKernelEx(&cfg, proj_tc_kernel, mx, mw[0], mw[1], mw[2], a);
 }
 
 }  // namespace sdm

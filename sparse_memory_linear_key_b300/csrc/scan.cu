@@ -1060,14 +1060,6 @@ cudaError_t launch_scan_t(const ScanArgs& a, cudaStream_t s)
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-long long pow2_ceil(long long x)
-{
-    long long p = 1;
-    while (p < x)
-        p *= 2;
-    return p;
-}
-
 }  // namespace
 
 ScanWs scan_ws_layout(const sdm_cfg& c, int B, int T)
@@ -1077,11 +1069,16 @@ ScanWs scan_ws_layout(const sdm_cfg& c, int B, int T)
     L.rb_rows = kChunk / es;
     L.nrb = (c.d + L.rb_rows - 1) / L.rb_rows;
     L.chunk_bytes = (c.d < L.rb_rows ? c.d : L.rb_rows) * es;
-    // Window: room for about twice the tokens of one stream the grid keeps in flight
-    // (one CTA per SM, about two items each), between 16 and kMaxWindow tokens.
+    // Window: the tokens of one stream the grid keeps in flight (one CTA per SM, about
+    // two items each) plus 16, between 16 and kMaxWindow tokens. A wider window hands more
+    // references over through the ring (a reference whose writer lies within the window
+    // is copied from the writer's ring entry even when the writer is long done); a
+    // narrower one holds tokens back until the window behind them has committed. Swept on
+    // this GPU (d = 2048: one, two and four sequences, 74, 37 and 18.5 tokens in flight a
+    // stream; d = 3840, two sequences), in flight + 16 sits at the optimum of every case.
     const long long streams = (long long)(B > 0 ? B : 1) * L.nrb;
-    const long long inflight = (2LL * num_sms_current_device() + streams - 1) / streams;
-    long long win = pow2_ceil(2 * inflight);
+    const double inflight = 2.0 * num_sms_current_device() / (double)streams;
+    long long win = (long long)(inflight + 0.5) + 16;
     if (win < 16)
         win = 16;
     if (win > kMaxWindow)

@@ -19,10 +19,11 @@
 //
 // Block: one sequence, a run of `tb` tokens [t0, t1). The references of the window
 // [t0 - win, t1) (slot ids are one contiguous run of idx) are indexed by slot: a counting
-// sort places them in kBuckets hash buckets of (slot, token, kind, position) entries.
-// Each reference of the block then scans only its slot's bucket -- a handful of entries,
-// more for popular slots -- for the latest earlier writer and the earlier referencing
-// tokens.
+// sort places them in kBuckets hash buckets of (slot, token, kind, position) entries,
+// 6 bytes each. Each reference of the block then scans only its slot's bucket -- a handful
+// of entries, more for popular slots -- for the latest earlier writer and the earlier
+// referencing tokens. The window is indexed again by every block, so blocks take as many
+// tokens as shared memory allows while the grid still fills the GPU twice over.
 #include "sdm_common.cuh"
 #include "sdm_internal.h"
 
@@ -31,7 +32,8 @@ namespace sdm {
 namespace {
 
 constexpr int kBuckets = 4096;
-constexpr int kCodeThreads = 256;
+constexpr int kCodeThreads = 512;
+constexpr size_t kCodeSmemMax = 225 * 1024;
 
 __device__ __forceinline__ uint32_t bucket_of(int32_t s)
 {
@@ -50,7 +52,7 @@ __global__ void __launch_bounds__(kCodeThreads) codes_kernel(const int32_t* __re
     uint32_t* off = reinterpret_cast<uint32_t*>(smem_raw);           // [kBuckets + 1]
     uint32_t* cur = off + kBuckets + 4;                               // [kBuckets] counts, cursors
     int32_t* slot = reinterpret_cast<int32_t*>(cur + kBuckets);       // [nref window]
-    uint32_t* info = reinterpret_cast<uint32_t*>(slot + (tb + win) * 2 * W);  // tloc<<8|kind<<7|pos
+    uint16_t* info = reinterpret_cast<uint16_t*>(slot + (tb + win) * 2 * W);  // tloc<<7|kind<<6|pos
     __shared__ uint32_t wsum[kCodeThreads / 32];
     const int b = blockIdx.y;
     const int t0 = blockIdx.x * tb;
@@ -69,7 +71,7 @@ __global__ void __launch_bounds__(kCodeThreads) codes_kernel(const int32_t* __re
             report(status, SDM_ERANGE);
     }
     __syncthreads();
-    // exclusive prefix sum of the bucket sizes (16 buckets a thread)
+    // exclusive prefix sum of the bucket sizes (8 buckets a thread)
     {
         constexpr int PER = kBuckets / kCodeThreads;
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -108,7 +110,7 @@ __global__ void __launch_bounds__(kCodeThreads) codes_kernel(const int32_t* __re
         if (s >= 0 && s < N) {
             const uint32_t at = atomicAdd(&cur[bucket_of(s)], 1u);
             slot[at] = s;
-            info[at] = ((uint32_t)(e / (2 * W)) << 8) | ((uint32_t)((e / W) & 1) << 7) | (uint32_t)(e % W);
+            info[at] = (uint16_t)(((e / (2 * W)) << 7) | (((e / W) & 1) << 6) | (e % W));
         }
     }
     __syncthreads();
@@ -127,15 +129,15 @@ __global__ void __launch_bounds__(kCodeThreads) codes_kernel(const int32_t* __re
                 if (slot[q] != s)
                     continue;
                 const uint32_t in = info[q];
-                const int dt = t - (base + (int)(in >> 8));
+                const int dt = t - (base + (int)(in >> 7));
                 if (dt < 0 || dt > win)
                     continue;
-                const bool is_w = ((in >> 7) & 1) == 0;
+                const bool is_w = ((in >> 6) & 1) == 0;
                 // writers: the latest one at or before t (a read sees its own token's
                 // write), strictly before t for a write
                 if (is_w && dt < best_dt && (kind ? dt >= 0 : dt >= 1)) {
                     best_dt = dt;
-                    best_pos = (int)(in & 0x7F);
+                    best_pos = (int)(in & 0x3F);
                 }
                 // a write waits for the bank loads of every earlier referencing token
                 if (!kind && dt >= 1) {
@@ -180,12 +182,24 @@ cudaError_t launch_scan_codes(const sdm_cfg& c, const int32_t* idx, int B, int T
     unsigned long long* deadmask = masks + (size_t)B * T;
     unsigned long long* warmask = masks + (size_t)B * T * 2;
     const int N = c.n_sub * c.n_sub;
-    // tokens a block: keep the indexed window (tb + win tokens, 8 bytes a reference) near
-    // 80 KB, so that two blocks share an SM where the window allows
-    int tb = 32;
-    while (tb > 8 && (size_t)(tb + win) * 2 * c.w * 8 > 80 * 1024)
-        tb /= 2;
-    const size_t smem = (size_t)(2 * kBuckets + 4) * 4 + (size_t)(tb + win) * 2 * c.w * 8;
+    // Tokens a block: every block indexes its run and the window before it, so the
+    // largest run whose index fits in shared memory (6 bytes a reference; at most 512
+    // tokens indexed, the reach of the 9-bit token field), as long as the grid keeps two
+    // blocks a SM busy; runs of at most 32 tokens always qualify.
+    const int sms = num_sms_current_device();
+    auto smem_for = [&](int tb_) {
+        return (size_t)(2 * kBuckets + 4) * 4 + (size_t)(tb_ + win) * 2 * c.w * 6;
+    };
+    int tb = 8;
+    const int cand[] = {256, 192, 128, 96, 64, 48, 32, 16, 8};
+    for (int tb_ : cand) {
+        const long long blocks = (long long)B * ((T + tb_ - 1) / tb_);
+        if (smem_for(tb_) <= kCodeSmemMax && tb_ + win <= 512 && (blocks >= 2LL * sms || tb_ <= 32)) {
+            tb = tb_;
+            break;
+        }
+    }
+    const size_t smem = smem_for(tb);
     e = cudaFuncSetAttribute(codes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;

@@ -536,6 +536,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 // 2D bf16 row-major tensor [rows, cols], box {64 columns, box_rows}, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_rows)
+{
+    auto enc = encode_fn();
+    if (enc == nullptr)
+        return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kKAtom, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 // z with P(Z > z) = p for a standard normal Z: bisection on the upper tail
 // 0.5 erfc(z / sqrt 2), which falls as z grows. Only a starting bracket for an exact
 // search, so a float is plenty.
@@ -554,21 +570,6 @@ float normal_upper_quantile(double p)
     return (float)(0.5 * (lo + hi));
 }
 
-bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_rows)
-{
-    auto enc = encode_fn();
-    if (enc == nullptr)
-        return false;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kKAtom, box_rows};
-    cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-}  // namespace
 
 bool score_tc_supported(const sdm_cfg& c)
 {

@@ -28,6 +28,40 @@ int num_sms_current_device()
 
 static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
+// Few tokens (a decode step): only q_w and q_r are on the way to the addressing, so v is
+// projected on a side stream forked off the caller's stream and joined back before the
+// scan (event record / wait, so that a captured graph gets a parallel branch). One side
+// stream and two events per device; the lock keeps another thread's call off them from
+// the fork until the join is enqueued.
+constexpr int64_t kForkTokens = 256;
+
+struct ProjFork {
+    bool ready = false;
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_v = nullptr;
+};
+static ProjFork g_fork[64];
+static std::mutex g_fork_mu;
+
+static ProjFork* fork_state()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return nullptr;
+    ProjFork& f = g_fork[dev];
+    if (f.ready)
+        return &f;
+    if (f.side == nullptr && cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking) != cudaSuccess)
+        return nullptr;
+    if (f.ev_fork == nullptr &&
+        cudaEventCreateWithFlags(&f.ev_fork, cudaEventDisableTiming) != cudaSuccess)
+        return nullptr;
+    if (f.ev_v == nullptr && cudaEventCreateWithFlags(&f.ev_v, cudaEventDisableTiming) != cudaSuccess)
+        return nullptr;
+    f.ready = true;
+    return &f;
+}
+
 // Shapes the scan alone needs (the recurrence does not care how the slots were
 // chosen, so w <= n_sub is not required here): d % 16, w in {8,16,32,64}, w <= N.
 static int check_scan_cfg(const sdm_cfg* cfg)
@@ -424,10 +458,36 @@ static int prefill_impl(const sdm_cfg* cfg, const sdm_weights* w, const void* M0
     cudaStream_t s = (cudaStream_t)stream;
     if (ntok > 0x7FFFFFFF)
         return SDM_EUNSUPPORTED;
-    if (launch_project_tc(*cfg, *w, x, ntok, q_w, q_r, v, s) != cudaSuccess ||
-        launch_address(*cfg, w->K1, w->K2, q_w, q_r, ntok, idx, wsel, base + L.addr, dev_status,
-                       s) != cudaSuccess ||
-        (M0 != nullptr && launch_first_touch(*cfg, idx, B, T, first_write, s) != cudaSuccess))
+    std::unique_lock<std::mutex> lock;
+    ProjFork* f = nullptr;
+    bool ok = true;
+    if (ntok <= kForkTokens) {
+        lock = std::unique_lock<std::mutex>(g_fork_mu);
+        f = fork_state();
+        if (f == nullptr)
+            return SDM_ECUDA;
+        if (cudaEventRecord(f->ev_fork, s) != cudaSuccess ||
+            cudaStreamWaitEvent(f->side, f->ev_fork, 0) != cudaSuccess)
+            return SDM_ECUDA;
+        ok = launch_project_tc(*cfg, *w, x, ntok, q_w, q_r, v, f->side, 4) == cudaSuccess;
+        // the side stream is joined back whatever happened (a forked capture must rejoin)
+        if (cudaEventRecord(f->ev_v, f->side) != cudaSuccess)
+            return SDM_ECUDA;
+        ok = ok && launch_project_tc(*cfg, *w, x, ntok, q_w, q_r, v, s, 3) == cudaSuccess;
+    } else {
+        ok = launch_project_tc(*cfg, *w, x, ntok, q_w, q_r, v, s) == cudaSuccess;
+    }
+    ok = ok &&
+         launch_address(*cfg, w->K1, w->K2, q_w, q_r, ntok, idx, wsel, base + L.addr, dev_status,
+                        s) == cudaSuccess &&
+         (M0 == nullptr || launch_first_touch(*cfg, idx, B, T, first_write, s) == cudaSuccess);
+    if (f != nullptr) {
+        // v is ready for the scan
+        const bool joined = cudaStreamWaitEvent(s, f->ev_v, 0) == cudaSuccess;
+        lock.unlock();
+        ok = ok && joined;
+    }
+    if (!ok)
         return SDM_ECUDA;
     rc = scan_impl(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, base + L.scan,
                    scan_ws_layout(*cfg, B, T).total, dev_status, s, M0, first_write);

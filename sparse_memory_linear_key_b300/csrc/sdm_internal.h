@@ -24,10 +24,13 @@ cudaError_t launch_bank_init(const void* M0, void* banks, size_t bank_bytes, int
 
 // ---- projections (proj_tc.cu): q_w, q_r, v of ntok tokens in one launch (bf16: tcgen05
 // tensor cores; fp32: SIMT fp32)
+// which: bit 0 q_w, bit 1 q_r, bit 2 v (the products to compute)
 cudaError_t launch_project_tc(const sdm_cfg& c, const sdm_weights& w, const void* x, int64_t ntok,
-                              void* q_w, void* q_r, void* v, cudaStream_t s);
+                              void* q_w, void* q_r, void* v, cudaStream_t s, int which = 7);
 
 // ---- addressing (address.cu, score_tc.cu)
+// z with P(Z > z) = p for a standard normal Z (a starting bracket for exact top-W searches)
+float normal_upper_quantile(double p);
 bool score_tc_supported(const sdm_cfg& c);
 cudaError_t launch_score_tc(const sdm_cfg& c, const void* K1, const void* K2, const void* q_w,
                             const void* q_r, int64_t ntok, float* hv, int32_t* hi, int* status,

@@ -130,11 +130,50 @@ def test_address_tile_modes_agree():
         return idx.cpu(), w.cpu()
 
     idx_all, w_all = address(0, ntok)
-    for lo, hi in ((0, 64), (1000, 1257), (ntok - 33, ntok)):
+    # 2800 tokens take tiles of 128 queries, 300 to 1000 tokens replicated tiles of 32
+    for lo, hi in ((0, 300), (1000, 1557), (ntok - 999, ntok)):
         idx, w = address(lo, hi)
         assert torch.equal(idx, idx_all[lo:hi]), (lo, hi)
         assert torch.equal(w, w_all[lo:hi]), (lo, hi)
     assert sdm.read_status(st) == 0
+
+
+@pytest.mark.parametrize("ntok", [1, 7, 64, 256])
+@pytest.mark.parametrize("shape", ["n480-w64", "w-eq-n", "ragged-f32-w8", "n96-w16"])
+def test_address_few_tokens(ntok, shape):
+    """Batches of at most 256 tokens (a decode step) take one block per query on the SIMT
+    cores: slot sets exact against the oracle except counted near-ties, weights within
+    1e-5, ascending and distinct."""
+    d, n, dk, W, dt = {"n480-w64": (64, 480, 256, 64, "bf16"), "w-eq-n": (64, 32, 64, 32, "bf16"),
+                       "ragged-f32-w8": (48, 24, 32, 8, "f32"),
+                       "n96-w16": (64, 96, 128, 16, "bf16")}[shape]
+    cfg = sdm.make_cfg(d, n, dk, W, dt)
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    g = torch.Generator().manual_seed(ntok + n)
+    K1 = (torch.randn(n, dk // 2, generator=g) / (dk // 2) ** 0.5).to(tdt)
+    K2 = (torch.randn(n, dk // 2, generator=g) / (dk // 2) ** 0.5).to(tdt)
+    q_w = torch.randn(ntok, dk, generator=g).to(tdt)
+    q_r = torch.randn(ntok, dk, generator=g).to(tdt)
+    if ntok >= 7:
+        q_r[3] = q_w[3]                           # a read query equal to a write query
+    idx = torch.empty(ntok, 2, W, dtype=torch.int32, device="cuda")
+    w = torch.empty(ntok, 2, W, device="cuda")
+    st = sdm.new_status()
+    ws = sdm.alloc_workspace(sdm.address_workspace_bytes(cfg, ntok))
+    sdm.sdm_address(cfg, K1.cuda(), K2.cuda(), q_w.cuda(), q_r.cuda(), idx, w, ws, st)
+    torch.cuda.synchronize()
+    assert sdm.read_status(st) == 0
+    gi, gw = idx.cpu().numpy(), w.cpu().numpy()
+    assert np.all(np.diff(gi, axis=-1) > 0) and gi.min() >= 0 and gi.max() < n * n
+    for kind, q in ((0, q_w), (1, q_r)):
+        S, k, _, gaps = oracle.address(q, K1, K2, W)
+        n_bad, n_exc, unexc = tl.set_parity(gi[:, kind], S, gaps)
+        tl.report_address("few-tokens %s x%d" % (shape, ntok), ("write", "read")[kind], ntok,
+                          len(unexc), n_exc)
+        assert len(unexc) == 0, (shape, ntok, kind, n_bad, n_exc)
+        assert tl.max_weight_err(gi[:, kind], gw[:, kind], S, k, range(ntok)) <= tl.WEIGHT_ATOL
+    if ntok >= 7:
+        assert np.array_equal(gi[3, 0], gi[3, 1]) and np.array_equal(gw[3, 0], gw[3, 1])
 
 
 @pytest.mark.parametrize("name", list(SMALL))
