@@ -14,10 +14,11 @@
 //  * many tokens (prefill): a persistent kernel, one CTA per SM walking the tiles, two
 //    TMEM accumulators so that a tile's epilogue overlaps the next tile's MMAs;
 //  * few tokens (decode): too few tiles to fill the SMs, so each tile is split along K
-//    over a cluster of up to 8 CTAs; every CTA leaves its fp32 partial tile in its own
-//    shared memory and, after a cluster barrier, sums one slice of the rows over all the
-//    cluster's partials through distributed shared memory, in a fixed order (the same
-//    shape always gives the same bits).
+//    over a cluster of up to 8 CTAs; after a cluster barrier every CTA pushes each row
+//    of its fp32 partial tile into the shared memory of the CTA that owns the row
+//    (distributed shared memory stores), and after a second one each CTA sums its rows
+//    over the cluster's partials in rank order (the same shape always gives the same
+//    bits).
 // fp32 layers (exact fp32 products are wanted there, which the tensor cores' tf32 path
 // does not give) use a tiled SIMT fp32 GEMM.
 // Every wait is bounded (status SDM_ETIMEOUT); on time-out a role stops, the CTA waits
@@ -141,18 +142,6 @@ __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t local, uint32_t rank)
-{
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(remote)
-                 : "memory");
-    return v;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
@@ -324,20 +313,6 @@ __global__ void __launch_bounds__(kThreads, 1) proj_tc_kernel(
         const int q = warp & 3;
         const int row = q * 32 + lane;
         const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-        float* red = reinterpret_cast<float*>(sp);     // split: fp32 partial tile, reuses stages
-        // split: rows past the batch are not needed in the partial tile
-        int rows_needed = kBM;
-        if (split) {
-            int j, n0, m0;
-            tile_coords(a, first_tile, j, n0, m0);
-            rows_needed = min(kBM, a.M - m0);
-        }
-        if (split && nkb == 0 && row < rows_needed) {
-            // (a CTA without K blocks contributes zeros)
-            for (int c0 = 0; c0 < kBN; c0 += 4)
-                *reinterpret_cast<float4*>(red + (size_t)row * kRedStride + c0) =
-                    make_float4(0.f, 0.f, 0.f, 0.f);
-        }
         int tl = 0;
         for (int t = first_tile; t < a.tiles && nkb > 0; t += tile_step, ++tl) {
             const int acc = tl % naccs;
@@ -345,25 +320,15 @@ __global__ void __launch_bounds__(kThreads, 1) proj_tc_kernel(
             if (!__all_sync(0xFFFFFFFFu, got))
                 break;
             tc_fence_after();
+            if (split)
+                break;                   // (the partial is read after the cluster barrier)
             int j, n0, m0;
             tile_coords(a, t, j, n0, m0);
             const ProjMat& mat = a.mat[j];
             const int m = m0 + row;
             uint32_t v[32];
             for (int c0 = 0; c0 < kBN; c0 += 32) {
-                if (split && q * 32 >= rows_needed)
-                    break;                                   // (warp-uniform)
                 tmem_ld32(trow + acc * kBN + c0, v);
-                if (split) {
-                    if (row >= rows_needed)
-                        continue;
-                    float4* dst = reinterpret_cast<float4*>(red + (size_t)row * kRedStride + c0);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                             __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-                    continue;
-                }
                 if (m >= a.M || n0 + c0 >= mat.n)
                     continue;
                 uint32_t w[16];
@@ -384,46 +349,68 @@ __global__ void __launch_bounds__(kThreads, 1) proj_tc_kernel(
         }
     }
     if (split) {
-        // every CTA of the cluster has its partial tile in shared memory; CTA r sums rows
-        // [r R, (r+1) R) over the cluster's partials (in rank order) and stores them
+        // Every CTA's MMAs are done once all have reached the barrier, so their stage
+        // memory is free. Rows [r R, (r+1) R) of the tile belong to rank r: each epilogue
+        // thread pushes its row of the fp32 partial, 32 columns at a time, into the owning
+        // rank's shared memory, slot [this rank][row - r R]; after a second barrier each rank
+        // sums its rows over the slots in rank order and stores them.
         __syncthreads();
         cluster_sync();
-        {
-            int j, n0, m0;
-            tile_coords(a, first_tile, j, n0, m0);
-            const ProjMat& mat = a.mat[j];
-            const int rows = min(kBM, a.M - m0);
-            const int R = (rows + a.split - 1) / a.split;
-            const int r0 = (int)rank * R, r1 = min(rows, r0 + R);
-            const int cols = min(kBN, mat.n - n0);        // a multiple of 8
-            const int groups = cols / 8;
-            const uint32_t red0 = base;
-            for (int e = threadIdx.x; e < (r1 - r0) * groups; e += kThreads) {
-                const int r = r0 + e / groups, c = (e % groups) * 8;
-                const uint32_t la = red0 + (uint32_t)(r * kRedStride + c) * 4u;
-                // every source's partial in flight at once, then summed in rank order
-                float4 p[2 * kMaxSplit];
+        tc_fence_after();
+        int j, n0, m0;
+        tile_coords(a, first_tile, j, n0, m0);
+        const ProjMat& mat = a.mat[j];
+        const int rows = min(kBM, a.M - m0);
+        const int R = (rows + a.split - 1) / a.split;
+        const uint32_t red0 = base;                     // [split][R][kRedStride] fp32
+        if (warp >= 2) {
+            const int q = warp & 3, row = q * 32 + lane;
+            const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+            if (q * 32 < rows) {                        // (warp-uniform)
+                const uint32_t owner = (uint32_t)(row / R);
+                const uint32_t slot =
+                    red0 + (uint32_t)((rank * R + (row - (int)owner * R)) * kRedStride) * 4u;
+                uint32_t remote = 0;
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(slot), "r"(owner));
+                for (int c0 = 0; c0 < kBN; c0 += 32) {
+                    uint32_t v[32];
+                    if (nkb > 0) {
+                        tmem_ld32(trow + c0, v);
+                    } else {
 #pragma unroll
-                for (int src = 0; src < kMaxSplit; ++src)
-                    if (src < a.split) {
-                        p[2 * src] = ld_dsmem_f4(la, (uint32_t)src);
-                        p[2 * src + 1] = ld_dsmem_f4(la + 16, (uint32_t)src);
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = 0u;                  // (a CTA without K blocks adds zeros)
                     }
-                float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+                    if (row < rows) {
 #pragma unroll
-                for (int src = 0; src < kMaxSplit; ++src)
-                    if (src < a.split) {
-                        const float4 p0 = p[2 * src], p1 = p[2 * src + 1];
-                        s0.x += p0.x; s0.y += p0.y; s0.z += p0.z; s0.w += p0.w;
-                        s1.x += p1.x; s1.y += p1.y; s1.z += p1.z; s1.w += p1.w;
+                        for (int i = 0; i < 8; ++i)
+                            asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                             remote + (uint32_t)(c0 + 4 * i) * 4u),
+                                         "r"(v[4 * i]), "r"(v[4 * i + 1]), "r"(v[4 * i + 2]),
+                                         "r"(v[4 * i + 3])
+                                         : "memory");
                     }
-                uint4 o = make_uint4(pack_bf16x2(s0.x, s0.y), pack_bf16x2(s0.z, s0.w),
-                                     pack_bf16x2(s1.x, s1.y), pack_bf16x2(s1.z, s1.w));
-                __stcs(reinterpret_cast<uint4*>(static_cast<bf16*>(mat.out) + (size_t)(m0 + r) * mat.n + n0 + c), o);
+                }
             }
         }
-        // no CTA leaves while another may still read its shared memory
         cluster_sync();
+        const float* red = reinterpret_cast<const float*>(sp);
+        const int r0 = (int)rank * R, r1 = min(rows, r0 + R);
+        const int cols = min(kBN, mat.n - n0);          // a multiple of 8
+        const int groups = cols / 8;
+        for (int e = threadIdx.x; e < (r1 - r0) * groups; e += kThreads) {
+            const int rl = e / groups, c = (e % groups) * 8;
+            float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int src = 0; src < a.split; ++src) {
+                const float4* pp = reinterpret_cast<const float4*>(red + (size_t)(src * R + rl) * kRedStride + c);
+                const float4 p0 = pp[0], p1 = pp[1];
+                sum[0] += p0.x; sum[1] += p0.y; sum[2] += p0.z; sum[3] += p0.w;
+                sum[4] += p1.x; sum[5] += p1.y; sum[6] += p1.z; sum[7] += p1.w;
+            }
+            uint4 o = make_uint4(pack_bf16x2(sum[0], sum[1]), pack_bf16x2(sum[2], sum[3]),
+                                 pack_bf16x2(sum[4], sum[5]), pack_bf16x2(sum[6], sum[7]));
+            __stcs(reinterpret_cast<uint4*>(static_cast<bf16*>(mat.out) + (size_t)(m0 + r0 + rl) * mat.n + n0 + c), o);
+        }
     }
     tc_fence_before();
     __syncthreads();

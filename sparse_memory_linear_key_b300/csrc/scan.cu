@@ -285,27 +285,34 @@ __device__ __forceinline__ void fetch_ahead(const ScanArgs& a, unsigned long lon
     }
     if (a.T == 1) {
         // one token a sequence (a decode step): no earlier writer exists, and a read's only
-        // possible writer is its own token -- matched here instead of by the codes kernel
-        int pos[JW];
+        // possible writer is its own token -- matched here instead of by the codes kernel:
+        // the write set is in ascending order, so each read id is looked up by a binary
+        // search over it (element i of the set is in lane i % 32, register i / 32)
+        auto wid_at = [&](int i) -> int {
+            int v = __shfl_sync(0xFFFFFFFFu, n.wid[0], i & 31);
 #pragma unroll
-        for (int jj = 0; jj < JW; ++jj)
-            pos[jj] = -1;
-        for (int i = 0; i < W; ++i) {
-            int src = n.wid[0];
-#pragma unroll
-            for (int jj = 1; jj < JW; ++jj)
+            for (int jj = 1; jj < JW; ++jj) {
+                const int u = __shfl_sync(0xFFFFFFFFu, n.wid[jj], i & 31);
                 if ((i >> 5) == jj)
-                    src = n.wid[jj];
-            const int wv = __shfl_sync(0xFFFFFFFFu, src, i & 31);
+                    v = u;
+            }
+            return v;
+        };
 #pragma unroll
-            for (int jj = 0; jj < JW; ++jj)
-                if (pos[jj] < 0 && wv >= 0 && wv == n.rid[jj])
-                    pos[jj] = i;
+        for (int jj = 0; jj < JW; ++jj) {
+            const int r = n.rid[jj];
+            int at = -1;                       // the last position holding an id below r
+#pragma unroll
+            for (int step = W / 2; step > 0; step >>= 1) {
+                const int cand = at + step;
+                if (wid_at(cand) < r)
+                    at = cand;
+            }
+            const int pos = at + 1;
+            const int found = wid_at(pos < W ? pos : W - 1);
+            if (pos < W && found == r && r >= 0 && r < a.N)
+                n.rc[jj] = (uint16_t)pos;       // dt = 0, position pos
         }
-#pragma unroll
-        for (int jj = 0; jj < JW; ++jj)
-            if (pos[jj] >= 0 && n.rid[jj] < a.N)
-                n.rc[jj] = (uint16_t)pos[jj];   // dt = 0, position pos
     }
     // M0 mode: the first writer of each referenced slot in this sequence
 #pragma unroll
@@ -340,8 +347,16 @@ __device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
     const int lane = threadIdx.x & 31;
     // the next item in claim order (a withheld item, for diagnostics, is claimed and
     // dropped: the tokens that depend on it then wait for it until their bound runs out)
+    // With one token a sequence the items are independent: block b takes items b, b +
+    // grid, ... without a shared counter.
+    unsigned long long next_static = blockIdx.x;
     auto claim = [&]() -> unsigned long long {
         unsigned long long item = 0;
+        if (a.T == 1 && a.skip_item < 0) {
+            item = next_static;
+            next_static += gridDim.x;
+            return item;
+        }
         if (lane == 0) {
             item = atomicAdd(a.counter, 1ull);
             if (item == (unsigned long long)a.skip_item)
