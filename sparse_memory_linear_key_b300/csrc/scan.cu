@@ -52,6 +52,8 @@
 // Every wait is bounded: on time-out the kernel records SDM_ETIMEOUT and raises a
 // global abort flag that every warp watches. Each warp leaves as a whole, and no warp
 // waits on another without a bound, so none can hang.
+#include <cstddef>
+
 #include "sdm_common.cuh"
 #include "sdm_internal.h"
 
@@ -72,6 +74,17 @@ static_assert(kCWarps * 32 * kConsumerRegs + 4 * 32 * kRoleRegs <= kScanThreads 
 static_assert(kCWarps % 4 == 0, "consumer warps must form whole warpgroups");
 constexpr int kMaxW = 64;
 constexpr int kSG = 8;             // slot groups (lanes sharing a row group)
+
+// With bf16 state and W >= 16 the read y = sum_j r_j M[R_j] runs on the tensor cores
+// (mma.sync m16n8k16 per 16 rows, the read chunks as A through ldmatrix.trans). The eight
+// slots that one ldmatrix phase reads at one row offset must then fall in different banks:
+// read chunks are 1040 bytes apart (260 words, 4 mod 32). Write chunks keep 1088 (16 mod
+// 32), right for the lanes of the consumers' SIMT pattern.
+template <typename S, int W>
+struct ScanShape {
+    static constexpr bool kMmaY = sizeof(S) == 2 && W >= 16;
+    static constexpr int kRStride = kMmaY ? 1040 : kStride;
+};
 
 struct ScanArgs {
     unsigned char* banks;
@@ -124,7 +137,14 @@ struct __align__(16) Meta {
     int b, t, rb, rows;
     float alpha, beta;
     int valid;                      // 0: no more work
+    // y on the tensor cores: bit j set when read slot j is in range (its weight counts),
+    // and for each write position the read position of the same slot (-1: not read by
+    // this token)
+    unsigned long long rvalid;
+    signed char rpos[kMaxW];
 };
+static_assert(offsetof(Meta, wsel) % 16 == 0 && offsetof(Meta, v) % 16 == 0,
+              "bulk copy targets must be 16-byte aligned");
 
 // mbarriers: full* = an item's chunks landed (armed by the consumer warps issuing them),
 // Wfree = the consumers took the write chunks, EmptyR = item description and read
@@ -340,10 +360,21 @@ __device__ __forceinline__ void fetch_ahead(const ScanArgs& a, unsigned long lon
     }
 }
 
-template <int W>
+// the part of a weight that column `part` of the B fragment holds: 0 the nearest bf16, 1
+// the nearest bf16 of what that leaves (together about 16 bits of the fp32 weight)
+__device__ __forceinline__ uint32_t weight_part_bits(float w, int part)
+{
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(w - __bfloat162float(hi));
+    const __nv_bfloat16 v = part == 0 ? hi : lo;
+    return part < 2 ? (uint32_t)*reinterpret_cast<const unsigned short*>(&v) : 0u;
+}
+
+template <typename S, int W>
 __device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
 {
     constexpr int JW = (W + 31) / 32;
+    constexpr bool kMmaY = ScanShape<S, W>::kMmaY;
     const int lane = threadIdx.x & 31;
     // the next item in claim order (a withheld item, for diagnostics, is claimed and
     // dropped: the tokens that depend on it then wait for it until their bound runs out)
@@ -390,6 +421,7 @@ __device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
         fence_acq_rel_gpu();
 
         unsigned long long wload = 0, rload = 0, fmask = 0, rdmask = 0, m0w = 0, m0r = 0;
+        unsigned long long rvalid = 0;
 #pragma unroll
         for (int jj = 0; jj < JW; ++jj) {
             const int j = lane + 32 * jj;
@@ -416,6 +448,7 @@ __device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
             m0r |= (unsigned long long)__ballot_sync(
                        0xFFFFFFFFu, a.m0 != nullptr && rval && !rown && !rdep && nx.ftr[jj] > t)
                    << (32 * jj);
+            rvalid |= (unsigned long long)__ballot_sync(0xFFFFFFFFu, rval) << (32 * jj);
             if (has) {
                 m.wid[j] = wval ? nx.wid[jj] : -1;
                 m.rid[j] = rval ? nx.rid[jj] : -1;
@@ -435,6 +468,7 @@ __device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
             m.rdmask = rdmask;
             m.m0w = m0w;
             m.m0r = m0r;
+            m.rvalid = rvalid;
             m.tok = (long long)b * a.T + t;
             m.b = b;
             m.t = t;
@@ -443,6 +477,20 @@ __device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
             m.alpha = nx.alpha;
             m.beta = nx.beta;
             m.valid = 1;
+        }
+        if (kMmaY) {
+            // for each write position, the read position of the same slot
+#pragma unroll
+            for (int jj = 0; jj < JW; ++jj)
+                if (lane + 32 * jj < kMaxW)
+                    m.rpos[lane + 32 * jj] = -1;
+            __syncwarp();
+#pragma unroll
+            for (int jj = 0; jj < JW; ++jj) {
+                const int j = lane + 32 * jj;
+                if (j < W && m.fpos[j] >= 0)
+                    m.rpos[m.fpos[j]] = (signed char)j;
+            }
         }
         __syncwarp();
         if (lane == 0)
@@ -532,7 +580,9 @@ __device__ void role_deps(const ScanArgs& a, unsigned char* wbuf, unsigned char*
                 const int id = is_w ? m.wid[j] : m.rid[j];
                 src = a.banks + (((size_t)b * a.N + id) * a.d + (size_t)rb * a.rb_rows) * sizeof(S);
             }
-            unsigned char* dst = (is_w ? wbuf : rbuf + (size_t)p * W * kStride) + (size_t)j * kStride;
+            constexpr int RS = ScanShape<S, W>::kRStride;
+            unsigned char* dst = is_w ? wbuf + (size_t)j * kStride
+                                      : rbuf + ((size_t)p * W + j) * RS;
             bulk_g2s(smem_u32(dst), src, cb, is_w ? depB : depR);
             (is_w ? missw : missr) -= cb;
         }
@@ -681,9 +731,11 @@ __device__ void role_marks(const ScanArgs& a, const Meta* meta, uint64_t* bars)
 
 template <typename S, int W>
 __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned char* rbuf,
-                              const Meta* meta, uint64_t* bars, float* ybuf)
+                              const Meta* meta, uint64_t* bars, float* ybuf, uint32_t* bfr)
 {
     constexpr int SPL = W / kSG;       // slots of each set per thread: i*8 + sg
+    constexpr bool kMmaY = ScanShape<S, W>::kMmaY;
+    constexpr int RS = ScanShape<S, W>::kRStride;
     using P = Pack16<S>;
     constexpr int RPL = P::R;          // rows per thread (16 bytes)
     constexpr int HPL = P::H;          // fp32 pairs per thread
@@ -758,7 +810,7 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
             a.banks + ((size_t)mn.b * a.N * a.d + (size_t)mn.rb * a.rb_rows) * sizeof(S);
         if (chunk) {
             const int id = is_r ? mn.rid[j] : mn.wid[j];
-            unsigned char* dst = (is_r ? rbuf + (size_t)pn * W * kStride : wbuf) + (size_t)j * kStride;
+            unsigned char* dst = is_r ? rbuf + ((size_t)pn * W + j) * RS : wbuf + (size_t)j * kStride;
             const bool from_m0 = (((is_r ? mn.m0r : mn.m0w) >> j) & 1) != 0;
             const unsigned char* src =
                 from_m0 ? a.m0 + ((size_t)id * a.d + (size_t)mn.rb * a.rb_rows) * sizeof(S)
@@ -784,8 +836,24 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
         const Meta& m = meta[p];
         if (!m.valid)
             return;
-        unsigned char* rb_buf = rbuf + (size_t)p * W * kStride;
+        unsigned char* rb_buf = rbuf + (size_t)p * W * RS;
         const bool act = rg * 16 < m.rows * (int)sizeof(S);
+        if constexpr (kMmaY) {
+            // The read's B fragments, [k-step][lane][2] flat: lane (g, q) of step ks holds
+            // the weights of read slots 16 ks + 2q, + 1 (register 0) and + 8, + 9 (register
+            // 1) in column g: the nearest bf16 in column 0, the nearest bf16 of what that
+            // leaves in column 1 (about 16 bits of the fp32 weight together), zero elsewhere
+            // and for slots out of range. The weights have landed with FullR; each warp
+            // fills 16 entries, published to every warp by the consumer barrier below.
+            uint32_t* bt = bfr + p * (W / 16) * 64;
+            for (int e = w * 16 + lane; lane < 16 && e < (W / 16) * 64; e += kCWarps * 16) {
+                const int reg = e & 1, ln = (e >> 1) & 31, ks = e >> 6;
+                const int g = ln >> 2, j = 16 * ks + 2 * (ln & 3) + 8 * reg;
+                const float w0 = ((m.rvalid >> j) & 1) ? m.wsel[W + j] : 0.f;
+                const float w1 = ((m.rvalid >> (j + 1)) & 1) ? m.wsel[W + j + 1] : 0.f;
+                bt[e] = weight_part_bits(w0, g) | (weight_part_bits(w1, g) << 16);
+            }
+        }
         // y = sum_j r_j M[R_j] (post-write). The chunks gathered from the bank need nothing
         // of the write: each thread reduces its read slots i*8 + sg, then the slot groups
         // are summed. Chunks D copies from the ring and this token's own writes are few;
@@ -805,7 +873,7 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
                     continue;
                 const float rw = m.wsel[W + i * kSG + sg];
                 float2 f[HPL];
-                P::unpack(*reinterpret_cast<const uint4*>(rb_buf + (size_t)(i * kSG + sg) * kStride +
+                P::unpack(*reinterpret_cast<const uint4*>(rb_buf + (size_t)(i * kSG + sg) * RS +
                                                           rg * 16),
                           f);
 #pragma unroll
@@ -832,7 +900,7 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
         };
         // while a write-side dependency is still in flight, the bank chunks of the read
         // go first; otherwise the write goes first (later tokens wait for its ring entries)
-        const bool bank_first = !uniform_test(smem_u32(bars + kDepB + p), (k >> 1) & 1);
+        const bool bank_first = !kMmaY && !uniform_test(smem_u32(bars + kDepB + p), (k >> 1) & 1);
         if (bank_first)
             y_bank();
         if (!uniform_wait(smem_u32(bars + kDepB + p), (k >> 1) & 1, a)) {
@@ -913,9 +981,61 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_u32(bars + kFwdw + p));
-        if (!bank_first)
+        if constexpr (kMmaY) {
+            // reads of slots this token writes: the new values go into the read buffer at
+            // their read positions (rows of this warp's row groups only)
+            if (m.fmask != 0 && act) {
+#pragma unroll
+                for (int i = 0; i < SPL; ++i) {
+                    const int j = m.rpos[i * kSG + sg];
+                    if (j >= 0)
+                        *reinterpret_cast<uint4*>(rb_buf + (size_t)j * RS + rg * 16) = Mv[i];
+                }
+            }
+            __syncwarp();
+            // the read chunks D copies from writers still in flight (only items that have
+            // some wait: the others stay clear of D's progress)
+            if (m.rdmask != 0 && !uniform_wait(smem_u32(bars + kDepR + p), (k >> 1) & 1, a)) {
+                leave(k, true);
+                return;
+            }
+            // y of this warp's 32 rows: two 16-row tiles, W / 16 steps of 16 slots each;
+            // A = the read chunks (ldmatrix.trans: slot rows of 8 consecutive state rows),
+            // B = the weights in two bf16 parts (columns 0 and 1), fp32 accumulation
+            const int gid = lane >> 2, tig = lane & 3;
+            const uint32_t rbase = smem_u32(rb_buf) +
+                                   (uint32_t)(((lane & 7) + 8 * (lane >> 4)) * RS) +
+                                   (uint32_t)(16 * ((lane >> 3) & 1));
+#pragma unroll
+            for (int t2 = 0; t2 < 2; ++t2) {
+                const int m0 = w * 32 + 16 * t2;
+                if (m0 >= m.rows)
+                    break;                                   // (warp-uniform)
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < W / 16; ++ks) {
+                    uint32_t a0, a1, a2, a3;
+                    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                                 : "r"(rbase + (uint32_t)(ks * 16 * RS) + (uint32_t)(m0 * 2)));
+                    const uint2 bb = reinterpret_cast<const uint2*>(bfr + p * (W / 16) * 64)[ks * 32 + lane];
+                    asm volatile(
+                        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+                        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(bb.x), "r"(bb.y));
+                }
+                // columns 0 and 1 (the two parts of the weights) are in lanes tig = 0
+                if (tig == 0) {
+                    float* yp = a.y + (size_t)m.tok * a.d + (size_t)m.rb * a.rb_rows + m0 + gid;
+                    __stcs(yp, c[0] + c[1]);
+                    __stcs(yp + 8, c[2] + c[3]);
+                }
+            }
+        }
+        if (!kMmaY && !bank_first)
             y_bank();
-        if (y_rest) {
+        if (!kMmaY && y_rest) {
             // the read chunks D copies (writer still in flight when this item was described)
             if (!uniform_wait(smem_u32(bars + kDepR + p), (k >> 1) & 1, a)) {
                 leave(k, true);
@@ -961,7 +1081,7 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
                     rd &= rd - 1;
                     const float rw = m.wsel[W + j];
                     float2 f[HPL];
-                    P::unpack(*reinterpret_cast<const uint4*>(rb_buf + (size_t)j * kStride + rg * 16), f);
+                    P::unpack(*reinterpret_cast<const uint4*>(rb_buf + (size_t)j * RS + rg * 16), f);
 #pragma unroll
                     for (int h = 0; h < HPL; ++h)
                         ye[h] = __ffma2_rn(make_float2(rw, rw), f[h], ye[h]);
@@ -1014,10 +1134,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a)
 {
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* wbuf = smem;
+    constexpr int RS = ScanShape<S, W>::kRStride;
     unsigned char* rbuf = smem + (size_t)W * kStride;
-    Meta* meta = reinterpret_cast<Meta*>(smem + (size_t)3 * W * kStride);
+    Meta* meta = reinterpret_cast<Meta*>(smem + (size_t)W * kStride + (size_t)2 * W * RS);
     uint64_t* bars = reinterpret_cast<uint64_t*>(meta + 2);
     float* ybuf = reinterpret_cast<float*>(bars + kNumBars);   // [64 row groups][8 rows]
+    uint32_t* bfr = reinterpret_cast<uint32_t*>(ybuf + (kChunk / 16) * 8);   // [2][W/16][32][2]
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(bars + kFullW), kCWarps);
         mbar_init(smem_u32(bars + kWfree), 1);
@@ -1035,6 +1157,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a)
         mbar_init(smem_u32(bars + kLmark), 1);
         fence_mbarrier_init();
     }
+    if (ScanShape<S, W>::kMmaY) {
+        // the tensor-core read takes every slot of a read buffer (weight 0 where a slot id is
+        // out of range): slots no copy ever reaches must hold finite values
+        for (int e = threadIdx.x; e < 2 * W * RS / 16; e += blockDim.x)
+            reinterpret_cast<uint4*>(rbuf)[e] = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_shared();   // (before bulk copies write the buffers)
+    }
     __syncthreads();
     const int warp = threadIdx.x >> 5;
     // Register split: the block is launched with 96 registers a thread (640 x 96 =
@@ -1042,12 +1171,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a)
     // warpgroup (warps 16..19) gives back down to 64 (128 x 64 = 8,192): 61,440 in all.
     if (warp < kCWarps) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kConsumerRegs) : "memory");
-        role_consumer<S, W>(a, wbuf, rbuf, meta, bars, ybuf);
+        role_consumer<S, W>(a, wbuf, rbuf, meta, bars, ybuf, bfr);
         return;
     }
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRoleRegs) : "memory");
     if (warp == kWarpP)
-        role_producer<W>(a, meta, bars);
+        role_producer<S, W>(a, meta, bars);
     else if (warp == kWarpD)
         role_deps<S, W>(a, wbuf, rbuf, meta, bars);
     else if (warp == kWarpF1)
@@ -1059,8 +1188,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a)
 template <typename S, int W>
 cudaError_t launch_scan_t(const ScanArgs& a, cudaStream_t s)
 {
-    const size_t smem = (size_t)3 * W * kStride + 2 * sizeof(Meta) + kNumBars * sizeof(uint64_t) +
-                        (size_t)(kChunk / 16) * 8 * sizeof(float);   // partial y: 64 row groups x 8 rows
+    const size_t smem = (size_t)W * kStride + (size_t)2 * W * ScanShape<S, W>::kRStride +
+                        2 * sizeof(Meta) + kNumBars * sizeof(uint64_t) +
+                        (size_t)(kChunk / 16) * 8 * sizeof(float) +  // partial y: 64 row groups x 8 rows
+                        (size_t)2 * (W / 16 > 0 ? W / 16 : 1) * 64 * sizeof(uint32_t);  // B fragments
     auto kern = scan_kernel<S, W>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
