@@ -9,13 +9,13 @@
 //                          (score desc, row asc)
 //   address_small_kernel   few tokens (a decode step): a cluster of two blocks per group
 //                          of queries, one per half, scores from the sub-key table staged
-//                          in shared memory on the SIMT cores, keeps each half's top-W, and
-//                          merges the halves through distributed shared memory
-//   candidate_select_kernel  sorts each half's list, then forms the outer sums of the
+//                          in shared memory, keeps each half's top-W, and merges the
+//                          halves through distributed shared memory
+//   candidate_select_kernel  orders each half's list, then forms the outer sums of the
 //                          pairs of half-ranks (a, b) with (a+1)(b+1) <= W -- the only
 //                          pairs that can reach the top-W of all n^2 sums -- keeps their
-//                          top-W (bisection over the sums), takes the softmax, and reports
-//                          the set in ascending slot order.
+//                          top-W (warp_kth), takes the softmax, and reports the set in
+//                          ascending slot order.
 #include <algorithm>
 
 #include "sdm_common.cuh"
@@ -115,13 +115,119 @@ __device__ __forceinline__ void build_pairs(unsigned short* pairs, int* npairs, 
     }
 }
 
+// ------------------------------------------------------- exact top-W of a warp
+
+// An element's composite key: ascending = larger order key first, then smaller id.
+__device__ __forceinline__ uint64_t comp_key(uint32_t key, uint32_t id)
+{
+    return ((uint64_t)(~key) << 32) | id;
+}
+
+// Which elements warp_kth keeps: exact ? key >= lo : comp_key(key, id) <= e.
+struct KthSel {
+    bool exact;
+    uint32_t lo;
+    uint64_t e;
+};
+
+// Narrow the bracket [lo, hi) with a probe p that c elements reach (key >= p).
+__device__ __forceinline__ void kth_narrow(uint32_t p, int c, int W, uint32_t& lo, uint32_t& hi,
+                                           int& cnt_lo, int& cnt_hi)
+{
+    if (c >= W) {
+        if (p > lo) {
+            lo = p;
+            cnt_lo = c;
+        }
+    } else if (p < hi) {
+        hi = p;
+        cnt_hi = c;
+    }
+}
+
+// One warp, NK elements a lane: order keys key[] (0: no element) with distinct ids id[].
+// Finds the W best elements by (key desc, id asc) from a bracket [lo, hi) that holds
+// cnt_lo = #{key >= lo} >= W > cnt_hi = #{key >= hi}. Each round counts three probes:
+// two where a count falling linearly in the score between the ends of the bracket
+// would reach W, 12 elements' worth either side, and the middle of the key range, which
+// at least halves it. It stops when exactly W keys lie at or above lo, or at most 32
+// in the bracket: those are ranked directly, one a lane, and the e above is the
+// (W - cnt_hi)-th of them. Should more than 32 share one key value, the same rank among
+// their ids comes from a bisection over the ids. scratch: 32 entries.
+template <int NK>
+__device__ __forceinline__ KthSel warp_kth(const uint32_t (&key)[NK], const uint32_t (&id)[NK],
+                                           int W, uint32_t lo, uint32_t hi, int cnt_lo,
+                                           int cnt_hi, uint64_t* scratch)
+{
+    const int lane = threadIdx.x & 31;
+    const unsigned below = (1u << lane) - 1u;
+    auto count_ge = [&](uint32_t p) {
+        int c = 0;
+#pragma unroll
+        for (int i = 0; i < NK; ++i)
+            c += key[i] >= p ? 1 : 0;
+        return __reduce_add_sync(0xFFFFFFFFu, c);
+    };
+    for (int round = 0; round < 40 && cnt_lo != W && cnt_lo - cnt_hi > 32 && hi - lo > 1; ++round) {
+        const uint32_t mid = lo + ((hi - lo) >> 1);
+        const float vlo = float_from_order_bits(lo), vhi = float_from_order_bits(hi);
+        const float span = (float)(cnt_lo - cnt_hi);
+        const float f = (float)(cnt_lo - W) / span, dl = 12.0f / span;
+        const uint32_t pa = min(max(float_order_bits(vlo + (vhi - vlo) * (f - dl)), lo + 1), hi - 1);
+        const uint32_t pb = min(max(float_order_bits(vlo + (vhi - vlo) * (f + dl)), lo + 1), hi - 1);
+        const int ca = count_ge(pa), cb = count_ge(pb), cm = count_ge(mid);
+        kth_narrow(pa, ca, W, lo, hi, cnt_lo, cnt_hi);
+        kth_narrow(pb, cb, W, lo, hi, cnt_lo, cnt_hi);
+        kth_narrow(mid, cm, W, lo, hi, cnt_lo, cnt_hi);
+    }
+    KthSel r{cnt_lo == W, lo, 0ull};
+    if (r.exact)
+        return r;
+    const int m = cnt_lo - cnt_hi, need = W - cnt_hi;
+    if (m <= 32) {
+        int at = 0;
+#pragma unroll
+        for (int i = 0; i < NK; ++i) {
+            const bool in = key[i] >= lo && key[i] < hi;
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, in);
+            if (in)
+                scratch[at + __popc(bal & below)] = comp_key(key[i], id[i]);
+            at += __popc(bal);
+        }
+        __syncwarp();
+        const uint64_t e = lane < m ? scratch[lane] : ~0ull;
+        int rank = 0;
+        for (int j = 0; j < m; ++j)
+            rank += scratch[j] < e ? 1 : 0;
+        const unsigned who = __ballot_sync(0xFFFFFFFFu, lane < m && rank == need - 1);
+        r.e = __shfl_sync(0xFFFFFFFFu, e, __ffs(who) - 1);
+        __syncwarp();
+        return r;
+    }
+    // more than 32 left, all with key lo: the need-th lowest id among them
+    uint32_t ia = 0u, ib = 0xFFFFFFFFu;
+    for (int round = 0; round < 33 && ia < ib; ++round) {
+        const uint32_t md = ia + ((ib - ia) >> 1);
+        int c = 0;
+#pragma unroll
+        for (int i = 0; i < NK; ++i)
+            c += (key[i] == lo && id[i] <= md) ? 1 : 0;
+        c = __reduce_add_sync(0xFFFFFFFFu, c);
+        if (c >= need)
+            ib = md;
+        else
+            ia = md + 1u;
+    }
+    r.e = comp_key(lo, ia);
+    return r;
+}
+
 // One warp: given each half's W best (score, row) sorted by (score desc, row asc) in
 // lv0/li0 and lv1/li1, the W largest outer sums over the candidate pairs by (sum desc,
-// slot asc) -- a bisection over the order-preserving keys of the sums, NC candidates a
-// lane, stopping once exactly W keys lie at or above the probe, equal sums at the
-// threshold to the lower slot -- then the softmax over them, and the set in ascending
-// slot order with its weights into idx[0..W) / wsel[0..W). sel: W entries of scratch.
-template <int NC, int EW>
+// slot asc) (warp_kth, NC candidates a lane), then the softmax over them, and the set in
+// ascending slot order with its weights into idx[0..W) / wsel[0..W). sel: W entries of
+// scratch.
+template <int NC>
 __device__ __forceinline__ void select_candidates(const float* lv0, const int* li0, const float* lv1,
                                                   const int* li1, const unsigned short* pairs, int C,
                                                   int n, int W, uint64_t* sel, int32_t* idx,
@@ -148,82 +254,51 @@ __device__ __forceinline__ void select_candidates(const float* lv0, const int* l
     }
     kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
     kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
-    uint32_t lo = kmin, hi = kmax + 1;
-    int cnt_hi = 0;
-    bool exact = false;
-    while (!exact && hi - lo > 1) {
-        const uint32_t mid = lo + ((hi - lo) >> 1);
-        int c = 0;
-#pragma unroll
-        for (int i = 0; i < NC; ++i)
-            c += ck[i] >= mid ? 1 : 0;
-        c = __reduce_add_sync(0xFFFFFFFFu, c);
-        if (c == W) {
-            lo = mid;
-            exact = true;
-        } else if (c > W) {
-            lo = mid;
-        } else {
-            hi = mid;
-            cnt_hi = c;
-        }
-    }
-    bool keep[NC];
-#pragma unroll
-    for (int i = 0; i < NC; ++i)
-        keep[i] = exact ? ck[i] >= lo : ck[i] >= hi;
-    for (int need = exact ? 0 : W - cnt_hi; need > 0; --need) {
-        // the lowest slot among the equal sums not yet kept
-        uint32_t best = 0xFFFFFFFFu;
-#pragma unroll
-        for (int i = 0; i < NC; ++i)
-            if (!keep[i] && ck[i] == lo)
-                best = min(best, cs[i]);
-        best = __reduce_min_sync(0xFFFFFFFFu, best);
-#pragma unroll
-        for (int i = 0; i < NC; ++i)
-            if (!keep[i] && ck[i] == lo && cs[i] == best)
-                keep[i] = true;
-    }
+    const KthSel ks = warp_kth<NC>(ck, cs, W, kmin, kmax + 1u, C, 0, sel);
     // softmax over the kept sums (the largest one is the largest of all)
     const float mx = float_from_order_bits(kmax);
+    bool keep[NC];
+    float ev[NC];
     float part = 0.0f;
 #pragma unroll
-    for (int i = 0; i < NC; ++i)
-        part += keep[i] ? expf(cv[i] - mx) : 0.0f;
+    for (int i = 0; i < NC; ++i) {
+        keep[i] = ck[i] != 0u && (ks.exact ? ck[i] >= ks.lo : comp_key(ck[i], cs[i]) <= ks.e);
+        ev[i] = keep[i] ? expf(cv[i] - mx) : 0.0f;
+        part += ev[i];
+    }
     part = __reduce_add_sync_f(part);
-    int base_pos = 0;
+    int at = 0;
 #pragma unroll
     for (int i = 0; i < NC; ++i) {
         const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep[i]);
-        if (keep[i]) {
-            const int pos = base_pos + __popc(bal & ((1u << lane) - 1u));
-            sel[pos] = ((uint64_t)cs[i] << 32) | __float_as_uint(expf(cv[i] - mx) / part);
-        }
-        base_pos += __popc(bal);
+        if (keep[i])
+            sel[at + __popc(bal & ((1u << lane) - 1u))] =
+                ((uint64_t)cs[i] << 32) | __float_as_uint(ev[i] / part);
+        at += __popc(bal);
     }
     __syncwarp();
-    // report the set in ascending slot order, weights alongside
-    uint64_t k2[EW];
+    // the set in ascending slot order, weights alongside
+    uint64_t k2[2];
 #pragma unroll
-    for (int i = 0; i < EW; ++i) {
-        const int e = lane * EW + i;
-        k2[i] = (e < W) ? sel[e] : ~0ull;
+    for (int i = 0; i < 2; ++i) {
+        const int e = lane * 2 + i;
+        k2[i] = e < W ? sel[e] : ~0ull;
     }
-    warp_bitonic_sort<EW>(k2);
+    warp_bitonic_sort<2>(k2);
 #pragma unroll
-    for (int i = 0; i < EW; ++i) {
-        const int e = lane * EW + i;
+    for (int i = 0; i < 2; ++i) {
+        const int e = lane * 2 + i;
         if (e < W) {
             idx[e] = (int32_t)(k2[i] >> 32);
             wsel[e] = __uint_as_float((uint32_t)k2[i]);
         }
     }
+    __syncwarp();
 }
 
 // One warp per (token, kind). Candidate pairs (a, b) of half-ranks come from a table
 // built in shared memory at block start.
-template <int NC, int EW, int EH>
+template <int NC>
 __global__ void __launch_bounds__(256) candidate_select_kernel(
     const float* __restrict__ hv, const int32_t* __restrict__ hi, int64_t ntok, int n, int W,
     int32_t* __restrict__ idx, float* __restrict__ wsel)
@@ -242,21 +317,20 @@ __global__ void __launch_bounds__(256) candidate_select_kernel(
         const int kind = (int)(qi / ntok);
         const int64_t tok = qi % ntok;
         const size_t base = ((size_t)kind * ntok + tok) * 2 * W;
-        // each half's W best rows, sorted (score desc, row asc): the tensor-core scoring
+        // each half's W best rows sorted by (score desc, row asc): the tensor-core scoring
         // writes them in row order
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            uint64_t hk[EH];
+            uint64_t hk[2];
 #pragma unroll
-            for (int i = 0; i < EH; ++i) {
-                const int e = lane * EH + i;
+            for (int i = 0; i < 2; ++i) {
+                const int e = lane * 2 + i;
                 hk[i] = e < W ? desc_key(hv[base + h * W + e], (uint32_t)hi[base + h * W + e]) : ~0ull;
             }
-            warp_bitonic_sort<EH>(hk);
-            __syncwarp();
+            warp_bitonic_sort<2>(hk);
 #pragma unroll
-            for (int i = 0; i < EH; ++i) {
-                const int e = lane * EH + i;
+            for (int i = 0; i < 2; ++i) {
+                const int e = lane * 2 + i;
                 if (e < W) {
                     lv[warp][h][e] = key_score(hk[i]);
                     li[warp][h][e] = (int)key_id(hk[i]);
@@ -265,8 +339,342 @@ __global__ void __launch_bounds__(256) candidate_select_kernel(
         }
         __syncwarp();
         const size_t ob = ((size_t)tok * 2 + kind) * W;
-        select_candidates<NC, EW>(lv[warp][0], li[warp][0], lv[warp][1], li[warp][1], pairs, C, n, W,
-                                  sel[warp], idx + ob, wsel + ob);
+        select_candidates<NC>(lv[warp][0], li[warp][0], lv[warp][1], li[warp][1], pairs, C, n,
+                                    W, sel[warp], idx + ob, wsel + ob);
+    }
+}
+
+// ------------------------------------- few tokens: a query's selection on a warp group
+
+constexpr int kGW = 4;                 // warps a query group
+constexpr int kGT = kGW * 32;          // threads a query group
+constexpr int kKList = 40;             // entries of a group's bracket list (32 + the pick)
+
+// A query group (kGW warps at named barrier `bar`) exchanging partial results through
+// shared memory: xs holds two halves of kGW x 4 words, used in turn, so that one barrier
+// per exchange suffices (a half is written again only after the barrier of the exchange
+// in between, which every reader of its last use has passed).
+struct Group {
+    int bar;          // named barrier (1 + the group's index)
+    int gw;           // warp within the group
+    int tid;          // thread within the group
+    uint32_t* xs;     // [2][kGW][4]
+    int ph;           // the half the next exchange uses
+};
+
+__device__ __forceinline__ void grp_sync(const Group& g)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(g.bar), "n"(kGT) : "memory");
+}
+
+// this warp's words w[0..NV) into the exchange, then every thread reads all warps'
+template <int NV>
+__device__ __forceinline__ const uint32_t* grp_post(Group& g, const uint32_t (&w)[NV])
+{
+    uint32_t* x = g.xs + g.ph * kGW * 4;
+    g.ph ^= 1;
+    if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+            x[g.gw * 4 + i] = w[i];
+    }
+    grp_sync(g);
+    return x;
+}
+
+// group sums of NV ints
+template <int NV>
+__device__ __forceinline__ void grp_sum(Group& g, int (&v)[NV])
+{
+    uint32_t w[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+        w[i] = (uint32_t)__reduce_add_sync(0xFFFFFFFFu, v[i]);
+    const uint32_t* x = grp_post<NV>(g, w);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        int s = 0;
+#pragma unroll
+        for (int q = 0; q < kGW; ++q)
+            s += (int)x[q * 4 + i];
+        v[i] = s;
+    }
+}
+
+// offset of this warp's c elements in the group's order (warps in turn) and the total
+__device__ __forceinline__ int grp_offset(Group& g, int c, int& total)
+{
+    const uint32_t w[1] = {(uint32_t)c};
+    const uint32_t* x = grp_post<1>(g, w);
+    int off = 0;
+    total = 0;
+#pragma unroll
+    for (int q = 0; q < kGW; ++q) {
+        off += q < g.gw ? (int)x[q * 4] : 0;
+        total += (int)x[q * 4];
+    }
+    return off;
+}
+
+// warp_kth for a group: NK elements a thread, counts summed over the group; the bracket's
+// last elements gathered in list (kKList entries) and ranked by the group's first warp.
+template <int NK>
+__device__ __forceinline__ KthSel group_kth(Group& g, const uint32_t (&key)[NK],
+                                            const uint32_t (&id)[NK], int W, uint32_t lo,
+                                            uint32_t hi, int cnt_lo, int cnt_hi, uint64_t* list)
+{
+    const int lane = threadIdx.x & 31;
+    const unsigned below = (1u << lane) - 1u;
+    auto count_ge = [&](uint32_t p) {
+        int c = 0;
+#pragma unroll
+        for (int i = 0; i < NK; ++i)
+            c += key[i] >= p ? 1 : 0;
+        return c;
+    };
+    for (int round = 0; round < 40 && cnt_lo != W && cnt_lo - cnt_hi > 32 && hi - lo > 1; ++round) {
+        const uint32_t mid = lo + ((hi - lo) >> 1);
+        const float vlo = float_from_order_bits(lo), vhi = float_from_order_bits(hi);
+        const float span = (float)(cnt_lo - cnt_hi);
+        const float f = (float)(cnt_lo - W) / span, dl = 12.0f / span;
+        const uint32_t pa = min(max(float_order_bits(vlo + (vhi - vlo) * (f - dl)), lo + 1), hi - 1);
+        const uint32_t pb = min(max(float_order_bits(vlo + (vhi - vlo) * (f + dl)), lo + 1), hi - 1);
+        int c[3] = {count_ge(pa), count_ge(pb), count_ge(mid)};
+        grp_sum<3>(g, c);
+        kth_narrow(pa, c[0], W, lo, hi, cnt_lo, cnt_hi);
+        kth_narrow(pb, c[1], W, lo, hi, cnt_lo, cnt_hi);
+        kth_narrow(mid, c[2], W, lo, hi, cnt_lo, cnt_hi);
+    }
+    KthSel r{cnt_lo == W, lo, 0ull};
+    if (r.exact)
+        return r;
+    const int m = cnt_lo - cnt_hi, need = W - cnt_hi;
+    if (m <= 32) {
+        // the bracket's elements into list[0..m), warps in turn
+        int at = 0;
+        uint64_t mine[NK];
+        int pos[NK];
+#pragma unroll
+        for (int i = 0; i < NK; ++i) {
+            const bool in = key[i] >= lo && key[i] < hi;
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, in);
+            pos[i] = in ? at + __popc(bal & below) : -1;
+            mine[i] = comp_key(key[i], id[i]);
+            at += __popc(bal);
+        }
+        int total = 0;
+        const int off = grp_offset(g, at, total);
+#pragma unroll
+        for (int i = 0; i < NK; ++i)
+            if (pos[i] >= 0)
+                list[off + pos[i]] = mine[i];
+        grp_sync(g);
+        if (g.gw == 0) {
+            const uint64_t e = lane < m ? list[lane] : ~0ull;
+            int rank = 0;
+            for (int j = 0; j < m; ++j)
+                rank += list[j] < e ? 1 : 0;
+            const unsigned who = __ballot_sync(0xFFFFFFFFu, lane < m && rank == need - 1);
+            const uint64_t pick = __shfl_sync(0xFFFFFFFFu, e, __ffs(who) - 1);
+            if (lane == 0)
+                list[32] = pick;
+        }
+        grp_sync(g);
+        r.e = list[32];
+        return r;
+    }
+    // more than 32 left, all with key lo: the need-th lowest id among them
+    uint32_t ia = 0u, ib = 0xFFFFFFFFu;
+    for (int round = 0; round < 33 && ia < ib; ++round) {
+        const uint32_t md = ia + ((ib - ia) >> 1);
+        int c[1] = {0};
+#pragma unroll
+        for (int i = 0; i < NK; ++i)
+            c[0] += (key[i] == lo && id[i] <= md) ? 1 : 0;
+        grp_sum<1>(g, c);
+        if (c[0] >= need)
+            ib = md;
+        else
+            ia = md + 1u;
+    }
+    r.e = comp_key(lo, ia);
+    return r;
+}
+
+// the group's kept elements (keep[i]) into dst[0..), warps in turn; returns how many
+template <int NK>
+__device__ __forceinline__ int grp_compact(Group& g, const bool (&keep)[NK], const uint64_t (&val)[NK],
+                                           uint64_t* dst)
+{
+    const int lane = threadIdx.x & 31;
+    const unsigned below = (1u << lane) - 1u;
+    int at = 0, pos[NK];
+#pragma unroll
+    for (int i = 0; i < NK; ++i) {
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep[i]);
+        pos[i] = keep[i] ? at + __popc(bal & below) : -1;
+        at += __popc(bal);
+    }
+    int total = 0;
+    const int off = grp_offset(g, at, total);
+#pragma unroll
+    for (int i = 0; i < NK; ++i)
+        if (pos[i] >= 0)
+            dst[off + pos[i]] = val[i];
+    grp_sync(g);
+    return total;
+}
+
+// One query group: the W best of the n scores s[0..n) by (score desc, row asc), sorted,
+// into lv[0..W) / li[0..W), NK scores a thread (rows tid + kGT i). The first bracket is
+// what holds of mean + (z -+ 1/2) sd around the W-th score (the scores of a row are near
+// normal; z is the standard normal quantile of 1 - W/n), checked by one counting pass;
+// group_kth's search is exact either way. out: 64 entries, list: kKList entries of
+// scratch.
+template <int NK>
+__device__ __forceinline__ void group_topw(Group& g, const float* s, int n, int W, float z,
+                                           uint64_t* out, uint64_t* list, float* lv, int* li)
+{
+    uint32_t key[NK], id[NK];
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+    float sum = 0.f, sum2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < NK; ++i) {
+        const int r = g.tid + kGT * i;
+        const float f = r < n ? s[r] : 0.f;
+        key[i] = r < n ? float_order_bits(f) : 0u;     // 0 is below every real key
+        id[i] = (uint32_t)r;
+        if (r < n) {
+            kmin = min(kmin, key[i]);
+            kmax = max(kmax, key[i]);
+            sum += f;
+            sum2 = fmaf(f, f, sum2);
+        }
+    }
+    {
+        const uint32_t w[4] = {__reduce_min_sync(0xFFFFFFFFu, kmin), __reduce_max_sync(0xFFFFFFFFu, kmax),
+                               __float_as_uint(__reduce_add_sync_f(sum)),
+                               __float_as_uint(__reduce_add_sync_f(sum2))};
+        const uint32_t* x = grp_post<4>(g, w);
+        sum = 0.f;
+        sum2 = 0.f;
+#pragma unroll
+        for (int q = 0; q < kGW; ++q) {
+            kmin = min(kmin, x[q * 4]);
+            kmax = max(kmax, x[q * 4 + 1]);
+            sum += __uint_as_float(x[q * 4 + 2]);
+            sum2 += __uint_as_float(x[q * 4 + 3]);
+        }
+    }
+    uint32_t lo = kmin, hi = kmax + 1u;
+    int cnt_lo = n, cnt_hi = 0;
+    {
+        const float mean = sum / n;
+        const float sd = sqrtf(fmaxf(sum2 / n - mean * mean, 0.f));
+        const uint32_t bl = float_order_bits(mean + (z - 0.5f) * sd);
+        const uint32_t bh = float_order_bits(mean + (z + 0.5f) * sd);
+        int c[2] = {0, 0};
+#pragma unroll
+        for (int i = 0; i < NK; ++i) {
+            c[0] += key[i] >= bl ? 1 : 0;
+            c[1] += key[i] >= bh ? 1 : 0;
+        }
+        grp_sum<2>(g, c);
+        kth_narrow(bl, c[0], W, lo, hi, cnt_lo, cnt_hi);
+        kth_narrow(bh, c[1], W, lo, hi, cnt_lo, cnt_hi);
+    }
+    const KthSel ks = group_kth<NK>(g, key, id, W, lo, hi, cnt_lo, cnt_hi, list);
+    bool keep[NK];
+    uint64_t ck[NK];
+#pragma unroll
+    for (int i = 0; i < NK; ++i) {
+        ck[i] = comp_key(key[i], id[i]);
+        keep[i] = key[i] != 0u && (ks.exact ? key[i] >= ks.lo : ck[i] <= ks.e);
+    }
+    grp_compact<NK>(g, keep, ck, out);
+    // in order of (score desc, row asc): each entry's place is the number before it
+    if (g.tid < W) {
+        const uint64_t e = out[g.tid];
+        int place = 0;
+#pragma unroll 8
+        for (int j = 0; j < W; ++j)
+            place += out[j] < e ? 1 : 0;
+        lv[place] = key_score(e);
+        li[place] = (int)key_id(e);
+    }
+    grp_sync(g);
+}
+
+// One query group: select_candidates' merge, NC candidates a thread (candidate tid + kGT i);
+// the softmax normaliser is summed in a fixed order (each warp's butterfly, then the warps
+// in turn). sel: 64 entries, list: kKList entries of scratch.
+template <int NC>
+__device__ __forceinline__ void group_merge(Group& g, const float* lv0, const int* li0, const float* lv1,
+                                            const int* li1, const unsigned short* pairs, int C, int n,
+                                            int W, uint64_t* sel, uint64_t* list, int32_t* idx,
+                                            float* wsel)
+{
+    uint32_t ck[NC], cs[NC];
+    float cv[NC];
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+        const int c = g.tid + kGT * i;
+        ck[i] = 0u;                                    // below every real key
+        cv[i] = 0.0f;
+        cs[i] = 0xFFFFFFFFu;
+        if (c < C) {
+            const int a = pairs[c] >> 8, b = pairs[c] & 0xFF;
+            cv[i] = lv0[a] + lv1[b];
+            cs[i] = (uint32_t)li0[a] * (uint32_t)n + (uint32_t)li1[b];
+            ck[i] = float_order_bits(cv[i]);
+            kmin = min(kmin, ck[i]);
+            kmax = max(kmax, ck[i]);
+        }
+    }
+    {
+        const uint32_t w[2] = {__reduce_min_sync(0xFFFFFFFFu, kmin), __reduce_max_sync(0xFFFFFFFFu, kmax)};
+        const uint32_t* x = grp_post<2>(g, w);
+#pragma unroll
+        for (int q = 0; q < kGW; ++q) {
+            kmin = min(kmin, x[q * 4]);
+            kmax = max(kmax, x[q * 4 + 1]);
+        }
+    }
+    const KthSel ks = group_kth<NC>(g, ck, cs, W, kmin, kmax + 1u, C, 0, list);
+    // softmax over the kept sums (the largest one is the largest of all)
+    const float mx = float_from_order_bits(kmax);
+    bool keep[NC];
+    float ev[NC];
+    float part = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+        keep[i] = ck[i] != 0u && (ks.exact ? ck[i] >= ks.lo : comp_key(ck[i], cs[i]) <= ks.e);
+        ev[i] = keep[i] ? expf(cv[i] - mx) : 0.0f;
+        part += ev[i];
+    }
+    {
+        const uint32_t w[1] = {__float_as_uint(__reduce_add_sync_f(part))};
+        const uint32_t* x = grp_post<1>(g, w);
+        part = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kGW; ++q)
+            part += __uint_as_float(x[q * 4]);
+    }
+    uint64_t val[NC];
+#pragma unroll
+    for (int i = 0; i < NC; ++i)
+        val[i] = ((uint64_t)cs[i] << 32) | __float_as_uint(keep[i] ? ev[i] / part : 0.0f);
+    grp_compact<NC>(g, keep, val, sel);
+    // the set in ascending slot order, weights alongside
+    if (g.tid < W) {
+        const uint64_t e = sel[g.tid];
+        int place = 0;
+#pragma unroll 8
+        for (int j = 0; j < W; ++j)
+            place += sel[j] < e ? 1 : 0;
+        idx[place] = (int32_t)(e >> 32);
+        wsel[place] = __uint_as_float((uint32_t)e);
     }
 }
 
@@ -313,132 +721,6 @@ __device__ __forceinline__ float dot16(const uint4& k, const uint4& q, float acc
     acc = fmaf(__uint_as_float(k.y), __uint_as_float(q.y), acc);
     acc = fmaf(__uint_as_float(k.z), __uint_as_float(q.z), acc);
     return fmaf(__uint_as_float(k.w), __uint_as_float(q.w), acc);
-}
-
-// One warp: the W best of the n scores s[0..n) by (score desc, row asc), sorted, into
-// lv[0..W) / li[0..W). A bisection over the order-preserving keys finds the W-th largest;
-// ties at the threshold go to the lower rows. It starts from whatever holds of a bracket
-// mean + (z -+ 1/2) sd around the W-th score (the scores of a row are near normal; z is
-// the standard normal quantile of 1 - W/n), checked by one counting pass; the search is
-// exact either way. out: 64 entries of scratch.
-template <int KPL>
-__device__ __forceinline__ void warp_topw(const float* s, int n, int W, float z, uint64_t* out,
-                                          float* lv, int* li)
-{
-    const int lane = threadIdx.x & 31;
-    uint32_t key[KPL];
-    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-    float sum = 0.f, sum2 = 0.f;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-        const int r = lane + 32 * i;
-        const float f = r < n ? s[r] : 0.f;
-        key[i] = r < n ? float_order_bits(f) : 0u;     // 0 is below every real key
-        if (r < n) {
-            kmin = min(kmin, key[i]);
-            kmax = max(kmax, key[i]);
-            sum += f;
-            sum2 = fmaf(f, f, sum2);
-        }
-    }
-    kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
-    kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
-    sum = __reduce_add_sync_f(sum);
-    sum2 = __reduce_add_sync_f(sum2);
-    uint32_t lo = kmin, hi = kmax + 1;
-    int cnt_hi = 0;
-    bool exact = false;
-    {
-        const float mean = sum / n;
-        const float sd = sqrtf(fmaxf(sum2 / n - mean * mean, 0.f));
-        const uint32_t bl = float_order_bits(mean + (z - 0.5f) * sd);
-        const uint32_t bh = float_order_bits(mean + (z + 0.5f) * sd);
-        int cl = 0, ch = 0;
-#pragma unroll
-        for (int i = 0; i < KPL; ++i) {
-            cl += key[i] >= bl ? 1 : 0;
-            ch += key[i] >= bh ? 1 : 0;
-        }
-        cl = __reduce_add_sync(0xFFFFFFFFu, cl);
-        ch = __reduce_add_sync(0xFFFFFFFFu, ch);
-        // at least W keys lie at or above lo, fewer than W at or above hi
-        if (bl > lo && bl < hi) {
-            if (cl == W) {
-                lo = bl;
-                exact = true;
-            } else if (cl > W) {
-                lo = bl;
-            } else {
-                hi = bl;
-                cnt_hi = cl;
-            }
-        }
-        if (!exact && bh > lo && bh < hi) {
-            if (ch == W) {
-                lo = bh;
-                exact = true;
-            } else if (ch > W) {
-                lo = bh;
-            } else {
-                hi = bh;
-                cnt_hi = ch;
-            }
-        }
-    }
-    while (!exact && hi - lo > 1) {
-        const uint32_t mid = lo + ((hi - lo) >> 1);
-        int c = 0;
-#pragma unroll
-        for (int i = 0; i < KPL; ++i)
-            c += key[i] >= mid ? 1 : 0;
-        c = __reduce_add_sync(0xFFFFFFFFu, c);
-        if (c == W) {
-            lo = mid;
-            exact = true;
-        } else if (c > W) {
-            lo = mid;
-        } else {
-            hi = mid;
-            cnt_hi = c;
-        }
-    }
-    // kept: keys >= lo when exactly W lie there, else keys >= hi and the lowest rows
-    // among those equal to lo (rows ascend with i, then with the lane)
-    const int need = exact ? 0 : W - cnt_hi;
-    int ties_before = 0, pos = 0;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-        const bool tie = !exact && key[i] == lo && key[i] != 0u;
-        const unsigned tb = __ballot_sync(0xFFFFFFFFu, tie);
-        const int trank = ties_before + __popc(tb & ((1u << lane) - 1u));
-        const bool keep = key[i] != 0u && ((exact ? key[i] >= lo : key[i] >= hi) ||
-                                           (tie && trank < need));
-        const unsigned kb = __ballot_sync(0xFFFFFFFFu, keep);
-        const int at = pos + __popc(kb & ((1u << lane) - 1u));
-        if (keep && at < 64) {
-            const int r = lane + 32 * i;
-            out[at] = desc_key(s[r], (uint32_t)r);
-        }
-        pos += __popc(kb);
-        ties_before += __popc(tb);
-    }
-    __syncwarp();
-    uint64_t k2[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int e = lane * 2 + i;
-        k2[i] = e < W ? out[e] : ~0ull;
-    }
-    warp_bitonic_sort<2>(k2);
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int e = lane * 2 + i;
-        if (e < W) {
-            lv[e] = key_score(k2[i]);
-            li[e] = (int)key_id(k2[i]);
-        }
-    }
-    __syncwarp();
 }
 
 // the scores of a bf16 half on the tensor cores when its width is a multiple of 16
@@ -495,7 +777,7 @@ struct SmallSmem {
     // offsets in the dynamic shared memory of address_small_kernel; rows of the sub-key
     // table and of the queries are rs bytes apart (one row plus 16 bytes, so that eight
     // rows read at one column fall in different banks)
-    uint32_t rs, ktab, qs, sc, lv, li, lv1, li1, hk, total;
+    uint32_t rs, ktab, qs, sc, lv, li, lv1, li1, hk, kl, xs, total;
 };
 
 __host__ __device__ inline SmallSmem small_layout(int n, int h, int es, int kpl)
@@ -511,36 +793,41 @@ __host__ __device__ inline SmallSmem small_layout(int n, int h, int es, int kpl)
     L.lv1 = o; o += kQG * 64 * 4;
     L.li1 = o; o += kQG * 64 * 4;
     L.hk = o; o += kQG * 64 * 8;
+    L.kl = o; o += kQG * kKList * 8;
+    L.xs = o; o += kQG * 2 * kGW * 4 * 4;
     L.total = o;
     return L;
 }
 
 // Few tokens (a decode step): a cluster of two blocks takes kQG queries (token, kind),
 // block 0 the first half of each query against K1, block 1 the second against K2:
-//  1. the block stages its sub-key table in shared memory with one bulk copy a row and
-//     its queries' halves with plain loads;
-//  2. the scores s[r] = <K[r], q_half>, fp32 sums of exact products: bf16 tables whose
+//  1. the block stages its sub-key table in shared memory with one bulk copy a row;
+//  2. it waits for the kernel before it (the projections, when launched early: the table
+//     copy then overlaps them) and loads its queries' halves with plain loads;
+//  3. the scores s[r] = <K[r], q_half>, fp32 sums of exact products: bf16 tables whose
 //     half-width is a multiple of 16 on the tensor cores (mma.sync m16n8k16, the table as
 //     A in 16-row tiles, the kQG queries padded to 8 as B), others on the SIMT cores
 //     (thread t takes row t, its 16-byte chunks in a rotated order, products in element
 //     order);
-//  3. warp j keeps query j's W best rows of this half (warp_topw);
-//  4. after a cluster barrier, block 0's warp j reads block 1's list of query j through
-//     distributed shared memory and merges the two exactly as the candidate kernel does
-//     (select_candidates): the set and its softmax weights.
+//  4. warp group j (warps 4j .. 4j+3) keeps query j's W best rows of this half
+//     (group_topw);
+//  5. after a cluster barrier, block 0's group j reads block 1's list of query j through
+//     distributed shared memory and merges the two as the candidate kernel does, on the
+//     group (group_merge): the set and its softmax weights.
 constexpr int kSmallThreads = 512;
 
-template <typename IO, int NC, int EW, int KPL>
+template <typename IO, int NC, int KPL>
 __global__ void __launch_bounds__(kSmallThreads) address_small_kernel(
     const IO* __restrict__ q_w, const IO* __restrict__ q_r, const IO* __restrict__ K1,
     const IO* __restrict__ K2, int64_t ntok, int dk, int n, int W, float z,
-    int32_t* __restrict__ idx, float* __restrict__ wsel, int* status)
+    int32_t* __restrict__ idx, float* __restrict__ wsel, int* status, uint32_t* clear,
+    long long clear_words)
 {
     extern __shared__ __align__(16) unsigned char sm[];
     __shared__ unsigned short pairs[32 * NC];
     __shared__ int npairs;
     __shared__ __align__(8) uint64_t kbar;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     const uint32_t half = cluster_rank_u();
     const int64_t q0 = (int64_t)(blockIdx.x >> 1) * kQG;      // first query of the group
     const int64_t nq = 2 * ntok;
@@ -559,8 +846,7 @@ __global__ void __launch_bounds__(kSmallThreads) address_small_kernel(
         fence_mbarrier_init();
     }
     __syncthreads();
-    // 1. the half's sub-key table (one bulk copy a row, issued by every thread) and the
-    //    queries' halves (rows kQG..7 zero)
+    // 1. the half's sub-key table (one bulk copy a row, issued by every thread)
     if (threadIdx.x == 0)
         mbar_arrive_expect_tx(smem_u32(&kbar), tbytes);
     __syncthreads();
@@ -569,14 +855,6 @@ __global__ void __launch_bounds__(kSmallThreads) address_small_kernel(
         for (int r = threadIdx.x; r < n; r += blockDim.x)
             bulk_g2s(base + L.ktab + (uint32_t)(r * rs), src + (size_t)r * rowb, (uint32_t)rowb,
                      smem_u32(&kbar));
-        for (int e = threadIdx.x; e < 8 * h; e += blockDim.x) {
-            const int j = e / h, k = e % h;
-            const int64_t qi = q0 + j;                          // token-major: tok * 2 + kind
-            IO val = IO(0.0f);
-            if (j < kQG && qi < nq)
-                val = ((qi & 1) ? q_r : q_w)[(qi >> 1) * dk + half * h + k];
-            reinterpret_cast<IO*>(sm + L.qs + j * rs)[k] = val;
-        }
         // rows of the last 16-row tile past the table: zero (read by the MMA, never kept)
         for (int e = threadIdx.x; e < ((n + 15) / 16 * 16 - n) * h; e += blockDim.x)
             reinterpret_cast<IO*>(sm + L.ktab + (n + e / h) * rs)[e % h] = IO(0.0f);
@@ -585,7 +863,23 @@ __global__ void __launch_bounds__(kSmallThreads) address_small_kernel(
     __syncthreads();
     bool ok = mbar_wait(smem_u32(&kbar), 0, nullptr, status);
     ok = __syncthreads_and(ok) != 0;
-    // 2. scores of this half
+    // 2. the queries' halves (rows kQG..7 zero), once the projections that write them
+    //    are done (a programmatic launch starts before)
+    griddep_wait();
+    griddep_launch();
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < clear_words;
+         e += (long long)gridDim.x * blockDim.x)
+        clear[e] = 0u;
+    for (int e = threadIdx.x; e < 8 * h; e += blockDim.x) {
+        const int j = e / h, k = e % h;
+        const int64_t qi = q0 + j;                          // token-major: tok * 2 + kind
+        IO val = IO(0.0f);
+        if (j < kQG && qi < nq)
+            val = ((qi & 1) ? q_r : q_w)[(qi >> 1) * dk + half * h + k];
+        reinterpret_cast<IO*>(sm + L.qs + j * rs)[k] = val;
+    }
+    ok = __syncthreads_and(ok) != 0;
+    // 3. scores of this half
     if (ok && score_mma<IO>(h)) {
         score_tiles_mma(base + L.ktab, base + L.qs, rs, n, h, sc, 32 * KPL);
     } else if (ok) {
@@ -610,27 +904,30 @@ __global__ void __launch_bounds__(kSmallThreads) address_small_kernel(
         }
     }
     __syncthreads();
-    // 3. query j's W best rows of this half
-    if (ok && warp < kQG && q0 + warp < nq)
-        warp_topw<KPL>(sc + warp * 32 * KPL, n, W, z,
-                       reinterpret_cast<uint64_t*>(sm + L.hk) + warp * 64, lv + warp * 64,
-                       li + warp * 64);
+    // 4. query j's W best rows of this half, on warp group j
+    const int grp = warp / kGW;
+    Group g{1 + grp, warp % kGW, (int)threadIdx.x - grp * kGT,
+            reinterpret_cast<uint32_t*>(sm + L.xs) + grp * 2 * kGW * 4, 0};
+    uint64_t* gout = reinterpret_cast<uint64_t*>(sm + L.hk) + grp * 64;
+    uint64_t* glist = reinterpret_cast<uint64_t*>(sm + L.kl) + grp * kKList;
+    constexpr int KPG = KPL >= 4 ? KPL / 4 : 1;      // scores a thread of the group
+    if (ok && grp < kQG && q0 + grp < nq)
+        group_topw<KPG>(g, sc + grp * 32 * KPL, n, W, z, gout, glist, lv + grp * 64, li + grp * 64);
     __syncthreads();
     cluster_sync_all();
-    // 4. block 0 merges each query's halves
-    if (ok && half == 0 && warp < kQG && q0 + warp < nq) {
-        float* lv1 = reinterpret_cast<float*>(sm + L.lv1) + warp * 64;
-        int* li1 = reinterpret_cast<int*>(sm + L.li1) + warp * 64;
-        for (int e = lane; e < W; e += 32) {
-            lv1[e] = __uint_as_float(ld_dsmem_u32(base + L.lv + (warp * 64 + e) * 4, 1));
-            li1[e] = (int)ld_dsmem_u32(base + L.li + (warp * 64 + e) * 4, 1);
+    // 5. block 0 merges each query's halves: group j reads block 1's list of query j
+    if (ok && half == 0 && grp < kQG && q0 + grp < nq) {
+        float* lv1 = reinterpret_cast<float*>(sm + L.lv1) + grp * 64;
+        int* li1 = reinterpret_cast<int*>(sm + L.li1) + grp * 64;
+        if (g.tid < W) {
+            lv1[g.tid] = __uint_as_float(ld_dsmem_u32(base + L.lv + (grp * 64 + g.tid) * 4, 1));
+            li1[g.tid] = (int)ld_dsmem_u32(base + L.li + (grp * 64 + g.tid) * 4, 1);
         }
-        __syncwarp();
-        const int64_t qi = q0 + warp;
+        grp_sync(g);
+        const int64_t qi = q0 + grp;
         const size_t ob = ((size_t)(qi >> 1) * 2 + (qi & 1)) * W;
-        select_candidates<NC, EW>(lv + warp * 64, li + warp * 64, lv1, li1, pairs, npairs, n, W,
-                                  reinterpret_cast<uint64_t*>(sm + L.hk) + warp * 64, idx + ob,
-                                  wsel + ob);
+        group_merge<(NC + 3) / 4>(g, lv + grp * 64, li + grp * 64, lv1, li1, pairs, npairs, n, W,
+                                  gout, glist, idx + ob, wsel + ob);
     }
     // block 1 stays until block 0 has read its lists
     cluster_sync_all();
@@ -686,7 +983,7 @@ static cudaError_t run_topw_e(const sdm_cfg& c, const void* K1, const void* K2, 
     return run_topw<IO, 16>(c, K1, K2, q_w, q_r, ntok, hv, hi, s);
 }
 
-template <int NC, int EW, int EH>
+template <int NC>
 static cudaError_t run_cand(const sdm_cfg& c, int64_t ntok, const float* hv, const int32_t* hi,
                             int32_t* idx, float* wsel, cudaStream_t s)
 {
@@ -694,7 +991,7 @@ static cudaError_t run_cand(const sdm_cfg& c, int64_t ntok, const float* hv, con
     int64_t blocks = (2 * ntok + 7) / 8;
     if (blocks > (int64_t)sms * 4)
         blocks = (int64_t)sms * 4;
-    candidate_select_kernel<NC, EW, EH><<<(unsigned)blocks, 256, 0, s>>>(hv, hi, ntok, c.n_sub, c.w,
+    candidate_select_kernel<NC><<<(unsigned)blocks, 256, 0, s>>>(hv, hi, ntok, c.n_sub, c.w,
                                                                     idx, wsel);
     return cudaGetLastError();
 }
@@ -714,12 +1011,13 @@ bool address_small_path(const sdm_cfg& c, int64_t ntok)
            small_layout(c.n_sub, h, es, small_kpl(c.n_sub)).total <= 200u * 1024u;
 }
 
-template <typename IO, int NC, int EW, int KPL>
+template <typename IO, int NC, int KPL>
 static cudaError_t run_small_kpl(const sdm_cfg& c, const void* K1, const void* K2, const void* q_w,
                                  const void* q_r, int64_t ntok, int32_t* idx, float* wsel,
-                                 int* status, cudaStream_t s)
+                                 int* status, cudaStream_t s, bool early, void* clear,
+                                 size_t clear_bytes)
 {
-    auto kern = address_small_kernel<IO, NC, EW, KPL>;
+    auto kern = address_small_kernel<IO, NC, KPL>;
     const SmallSmem L = small_layout(c.n_sub, c.dk / 2, (int)sizeof(IO), KPL);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)L.total);
@@ -731,56 +1029,78 @@ static cudaError_t run_small_kpl(const sdm_cfg& c, const void* K1, const void* K
     cfg.blockDim = dim3(kSmallThreads, 1, 1);
     cfg.dynamicSmemBytes = L.total;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = early ? 2 : 1;
     const float z = normal_upper_quantile((double)c.w / c.n_sub);
     return cudaLaunchKernelEx(&cfg, kern, (const IO*)q_w, (const IO*)q_r, (const IO*)K1,
-                              (const IO*)K2, ntok, c.dk, c.n_sub, c.w, z, idx, wsel, status);
+                              (const IO*)K2, ntok, c.dk, c.n_sub, c.w, z, idx, wsel, status,
+                              (uint32_t*)clear, (long long)(clear_bytes / 4));
 }
 
-template <typename IO, int NC, int EW>
+template <typename IO, int NC>
 static cudaError_t run_small_k(const sdm_cfg& c, const void* K1, const void* K2, const void* q_w,
                                const void* q_r, int64_t ntok, int32_t* idx, float* wsel,
-                               int* status, cudaStream_t s)
+                               int* status, cudaStream_t s, bool early, void* clear,
+                               size_t clear_bytes)
 {
     switch (small_kpl(c.n_sub)) {
-    case 1: return run_small_kpl<IO, NC, EW, 1>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s);
-    case 2: return run_small_kpl<IO, NC, EW, 2>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s);
-    case 4: return run_small_kpl<IO, NC, EW, 4>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s);
-    case 8: return run_small_kpl<IO, NC, EW, 8>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s);
-    default: return run_small_kpl<IO, NC, EW, 16>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s);
+    case 1: return run_small_kpl<IO, NC, 1>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s, early,
+                                             clear, clear_bytes);
+    case 2: return run_small_kpl<IO, NC, 2>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s, early,
+                                             clear, clear_bytes);
+    case 4: return run_small_kpl<IO, NC, 4>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s, early,
+                                             clear, clear_bytes);
+    case 8: return run_small_kpl<IO, NC, 8>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s, early,
+                                             clear, clear_bytes);
+    default: return run_small_kpl<IO, NC, 16>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s, early,
+                                              clear, clear_bytes);
     }
 }
 
 template <typename IO>
 static cudaError_t run_small(const sdm_cfg& c, const void* K1, const void* K2, const void* q_w,
                              const void* q_r, int64_t ntok, int32_t* idx, float* wsel,
-                             int* status, cudaStream_t s)
+                             int* status, cudaStream_t s, bool early, void* clear,
+                             size_t clear_bytes)
 {
     switch (c.w) {
-    case 8: return run_small_k<IO, 1, 1>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s);
-    case 16: return run_small_k<IO, 2, 1>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s);
-    case 32: return run_small_k<IO, 4, 1>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s);
-    case 64: return run_small_k<IO, 9, 2>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s);
+    case 8: return run_small_k<IO, 1>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s, early, clear,
+                                       clear_bytes);
+    case 16: return run_small_k<IO, 2>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s, early, clear,
+                                       clear_bytes);
+    case 32: return run_small_k<IO, 4>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s, early, clear,
+                                       clear_bytes);
+    case 64: return run_small_k<IO, 9>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s, early, clear,
+                                       clear_bytes);
     default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_address(const sdm_cfg& c, const void* K1, const void* K2, const void* q_w,
                            const void* q_r, int64_t ntok, int32_t* idx, float* wsel, void* ws,
-                           int* status, cudaStream_t s)
+                           int* status, cudaStream_t s, bool early, void* clear,
+                           size_t clear_bytes)
 {
     if (ntok <= 0)
-        return cudaSuccess;
+        return clear_bytes > 0 ? cudaMemsetAsync(clear, 0, clear_bytes, s) : cudaSuccess;
     if (address_small_path(c, ntok))
         return c.dtype == SDM_BF16
-                   ? run_small<bf16>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s)
-                   : run_small<float>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s);
+                   ? run_small<bf16>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s, early, clear,
+                                     clear_bytes)
+                   : run_small<float>(c, K1, K2, q_w, q_r, ntok, idx, wsel, status, s, early, clear,
+                                      clear_bytes);
+    if (clear_bytes > 0) {
+        const cudaError_t ec = cudaMemsetAsync(clear, 0, clear_bytes, s);
+        if (ec != cudaSuccess)
+            return ec;
+    }
     float* hv = (float*)ws;
     int32_t* hi = (int32_t*)((char*)ws + (size_t)2 * ntok * 2 * c.w * sizeof(float));
     // bf16 layers score on the tensor cores; fp32 layers (exact fp32 products) and other
@@ -794,10 +1114,10 @@ cudaError_t launch_address(const sdm_cfg& c, const void* K1, const void* K2, con
         return e;
     const int C = candidate_count(c.w);
     switch (c.w) {
-    case 8: return run_cand<1, 1, 1>(c, ntok, hv, hi, idx, wsel, s);      // 20 candidates
-    case 16: return run_cand<2, 1, 1>(c, ntok, hv, hi, idx, wsel, s);     // 50
-    case 32: return run_cand<4, 1, 1>(c, ntok, hv, hi, idx, wsel, s);     // 119
-    case 64: return run_cand<9, 2, 2>(c, ntok, hv, hi, idx, wsel, s);     // 280
+    case 8: return run_cand<1>(c, ntok, hv, hi, idx, wsel, s);      // 20 candidates
+    case 16: return run_cand<2>(c, ntok, hv, hi, idx, wsel, s);     // 50
+    case 32: return run_cand<4>(c, ntok, hv, hi, idx, wsel, s);     // 119
+    case 64: return run_cand<9>(c, ntok, hv, hi, idx, wsel, s);     // 280
     default: (void)C; return cudaErrorInvalidValue;
     }
 }

@@ -11,14 +11,18 @@
 //  * one thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M = 128, N = 256,
 //    B transposed) into a TMEM accumulator; four epilogue warps read it back with
 //    tcgen05.ld (one token row per thread), round to bf16 and store;
-//  * many tokens (prefill): a persistent kernel, one CTA per SM walking the tiles, two
-//    TMEM accumulators so that a tile's epilogue overlaps the next tile's MMAs;
-//  * few tokens (decode): too few tiles to fill the SMs, so each tile is split along K
-//    over a cluster of up to 8 CTAs; after a cluster barrier every CTA pushes each row
-//    of its fp32 partial tile into the shared memory of the CTA that owns the row
-//    (distributed shared memory stores), and after a second one each CTA sums its rows
-//    over the cluster's partials in rank order (the same shape always gives the same
-//    bits).
+//  * a persistent kernel, one CTA per SM walking the tiles, two TMEM accumulators so
+//    that a tile's epilogue overlaps the next tile's MMAs, every tile over the whole K
+//    (one accumulation order, so the same shape always gives the same bits);
+//  * many tokens (prefill): tiles of 256 output columns, four 48 KB stages;
+//  * few tokens (decode), where 256-column tiles would leave most SMs idle: tiles of 64
+//    columns, eight 24 KB stages, and each tile split along K over a cluster of two
+//    CTAs (64 tokens, d = 2048, dk = 256: 40 tiles, 80 CTAs). Rows [r R, (r+1) R)
+//    of a tile belong to rank r: once its MMAs are done, each CTA puts the rows of its
+//    fp32 partial that others own into its own shared memory and sends each owner its
+//    rows with one bulk copy into a receive buffer of the owner's (no partial ever
+//    lands on memory its owner still uses), and each owner sums its rows over the
+//    ranks in rank order (the same shape always gives the same bits).
 // fp32 layers (exact fp32 products are wanted there, which the tensor cores' tf32 path
 // does not give) use a tiled SIMT fp32 GEMM.
 // Every wait is bounded (status SDM_ETIMEOUT); on time-out a role stops, the CTA waits
@@ -36,27 +40,41 @@ namespace sdm {
 namespace {
 
 constexpr int kBM = 128;                 // tokens a tile (TMEM lanes)
-constexpr int kBN = 256;                 // output columns a tile (MMA N)
 constexpr int kBK = 64;                  // K columns a stage: one 128-byte swizzle row
-constexpr int kStages = 4;
 constexpr uint32_t kAStage = kBM * kBK * 2;            // 16 KB
 constexpr uint32_t kBChunk = kBK * 64 * 2;             // 64 K-rows x 64 columns: 8 KB
-constexpr uint32_t kBStage = kBChunk * (kBN / 64);     // 32 KB
-constexpr uint32_t kStageBytes = kAStage + kBStage;    // 48 KB
+constexpr uint32_t kStageBudget = 192 * 1024;          // shared memory for the stages
 constexpr int kThreads = 192;            // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kMaxSplit = 8;             // CTAs of a cluster sharing one tile along K
-constexpr int kRedStride = kBN + 4;      // fp32 per partial-tile row in shared memory
+// CTAs of a cluster sharing a 64-column tile: two, so that the projections of a decode
+// step (40 tiles, 80 CTAs) leave room for the addressing kernel's 64 CTAs, which launch
+// while the projections run and stage their sub-key tables
+constexpr int kMaxSplit = 2;
+constexpr int kXStride = 64 + 4;         // fp32 per partial row in an exchange buffer
+constexpr uint32_t kXRow = kXStride * 4; // bytes of that row (a multiple of 16)
+// receive buffers: (split - 1) sources x the rows one rank owns
+constexpr uint32_t kRecvBytes = (kMaxSplit - 1) * ((kBM + kMaxSplit - 1) / kMaxSplit) * kXRow;
+
+// A tile of BN output columns (the MMA's N): the stage holds the x tile and BN / 64
+// weight chunks; as many stages as the budget takes.
+template <int BN>
+struct Tile {
+    static constexpr uint32_t kBStage = kBChunk * (BN / 64);
+    static constexpr uint32_t kStageBytes = kAStage + kBStage;
+    static constexpr int kStages = (int)(kStageBudget / kStageBytes);
+    static constexpr uint32_t kTmemCols = 2 * BN;      // two accumulators
+};
 
 struct ProjMat {
     void* out;      // [M, n] bf16
     int n;          // output columns
-    int ntiles;     // ceil(n / kBN)
+    int ntiles;     // ceil(n / BN)
 };
 
 struct ProjArgs {
     ProjMat mat[3];
     int M, K, kblocks, mtiles, tiles;
-    int split;      // CTAs per tile (cluster size); 1: persistent, whole K per CTA
+    int abox;       // token rows an x copy brings (all kBM once there are that many tokens)
+    int split;      // CTAs per tile (a cluster along K; 64-column tiles only), else 1
     int* status;
 };
 
@@ -138,10 +156,21 @@ __device__ __forceinline__ uint32_t cluster_rank()
     return r;
 }
 
-__device__ __forceinline__ void cluster_sync()
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank)
 {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+// bulk copy from this CTA's shared memory into another CTA's of the cluster, completing
+// on that CTA's barrier
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "r"(src), "r"(bytes), "r"(bar)
+        : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
@@ -151,6 +180,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
 }
 
 // tile t -> product j, its column tile and its token tile (token tiles innermost)
+template <int BN>
 __device__ __forceinline__ void tile_coords(const ProjArgs& a, int t, int& j, int& n0, int& m0)
 {
     j = 0;
@@ -163,20 +193,24 @@ __device__ __forceinline__ void tile_coords(const ProjArgs& a, int t, int& j, in
             ++j;
         }
     }
-    n0 = (rem / a.mtiles) * kBN;
+    n0 = (rem / a.mtiles) * BN;
     m0 = (rem % a.mtiles) * kBM;
 }
 
 // ------------------------------------------------------------------------ kernel
 
-// One kernel for both modes. split == 1: persistent, CTA b takes tiles b, b + grid, ...
-// over the whole K, two accumulators. split > 1: CTA rank r of cluster c takes tile c over
-// its share of the K blocks, one accumulator, then the cluster reduces the partials.
+// split == 1: CTA b takes tiles b, b + grid, ... over the whole K, two accumulators.
+// split > 1 (BN = 64): rank r of cluster c takes tile c over its share of the K blocks,
+// one accumulator, then the cluster exchanges and sums the partials.
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1) proj_tc_kernel(
     const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w0,
     const __grid_constant__ CUtensorMap map_w1, const __grid_constant__ CUtensorMap map_w2,
     ProjArgs a)
 {
+    using TL = Tile<BN>;
+    constexpr int kStages = TL::kStages;
+    constexpr uint32_t kStageBytes = TL::kStageBytes;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -184,17 +218,28 @@ __global__ void __launch_bounds__(kThreads, 1) proj_tc_kernel(
     uint64_t* bars = reinterpret_cast<uint64_t*>(sp + kStages * kStageBytes);
     // bars: [0, S) full, [S, 2S) empty, 2S + {0, 1} accumulator full, 2S + {2, 3} empty
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
+    uint64_t* rx = bars + 2 * kStages + 6;             // partials received (split > 1)
+    unsigned char* recv = sp + kStages * kStageBytes + (2 * kStages + 8) * 8;   // 16-aligned
     __shared__ int dead;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool split = a.split > 1;
+    const bool split = BN == 64 && a.split > 1;
     const uint32_t rank = split ? cluster_rank() : 0u;
     const int first_tile = split ? (int)(blockIdx.x / a.split) : (int)blockIdx.x;
-    const int tile_step = split ? a.tiles : (int)gridDim.x;     // split: one tile a cluster
+    const int tile_step = split ? a.tiles : (int)gridDim.x;      // split: one tile a cluster
     const int kb0 = split ? (int)((long long)a.kblocks * rank / a.split) : 0;
     const int kb1 = split ? (int)((long long)a.kblocks * (rank + 1) / a.split) : a.kblocks;
-    const int naccs = split ? 1 : 2;
-    const uint32_t tmem_cols = split ? 256u : 512u;
+    constexpr int naccs = 2;
+    constexpr uint32_t tmem_cols = TL::kTmemCols;
+    // split: the tile's rows, R of them a rank, and how many this rank owns
+    int rows = 0, R = 1, mine = 0;
+    if (split) {
+        int j_, n0_, m0_;
+        tile_coords<BN>(a, first_tile, j_, n0_, m0_);
+        rows = min(kBM, a.M - m0_);
+        R = (rows + a.split - 1) / a.split;
+        mine = max(0, min(R, rows - (int)rank * R));
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -206,6 +251,13 @@ __global__ void __launch_bounds__(kThreads, 1) proj_tc_kernel(
             mbar_init(smem_u32(bars + 2 * kStages + 2 + c), 4);
         }
         dead = 0;
+        if (split) {
+            // every other rank sends this one its rows: armed before the cluster barrier
+            // below lets any of them send
+            mbar_init(smem_u32(rx), 1);
+            fence_mbarrier_init();
+            mbar_arrive_expect_tx(smem_u32(rx), (uint32_t)((a.split - 1) * mine) * kXRow);
+        }
         fence_mbarrier_init();
     }
     if (warp == 1) {
@@ -218,6 +270,12 @@ __global__ void __launch_bounds__(kThreads, 1) proj_tc_kernel(
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (split)
+        asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    // inputs are read and outputs written only after the kernel before has completed (a
+    // programmatic launch starts earlier); the next kernel may then start its own prologue
+    griddep_wait();
+    griddep_launch();
     const uint32_t tmem = *tmem_slot;
     int* stat = a.status;
     auto waitb = [&](uint32_t bar, uint32_t parity) -> bool {
@@ -244,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_tc_kernel(
             bool ok = true;
             for (int t = first_tile; ok && t < a.tiles; t += tile_step) {
                 int j, n0, m0;
-                tile_coords(a, t, j, n0, m0);
+                tile_coords<BN>(a, t, j, n0, m0);
                 const CUtensorMap* mw = j == 0 ? &map_w0 : j == 1 ? &map_w1 : &map_w2;
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % kStages;
@@ -254,10 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1) proj_tc_kernel(
                     }
                     const uint32_t fb = smem_u32(bars + s);
                     const uint32_t sa = base + s * kStageBytes;
-                    mbar_arrive_expect_tx(fb, kStageBytes);
+                    mbar_arrive_expect_tx(fb, (uint32_t)a.abox * (kBK * 2) + TL::kBStage);
                     tma_load_2d(sa, &map_x, kb * kBK, m0, fb);
 #pragma unroll
-                    for (int c = 0; c < kBN / 64; ++c)
+                    for (int c = 0; c < BN / 64; ++c)
                         tma_load_2d(sa + kAStage + c * kBChunk, mw, n0 + c * 64, kb * kBK, fb);
                 }
             }
@@ -268,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_tc_kernel(
     } else if (warp == 1) {
         // ---------------- MMA issuer
         if (lane == 0 && nkb > 0) {
-            const uint32_t idesc = idesc_bf16_bt(kBM, kBN);
+            const uint32_t idesc = idesc_bf16_bt(kBM, BN);
             int it = 0, tl = 0;
             bool ok = true;
             int last_acc = -1;
@@ -280,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_tc_kernel(
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = tmem + acc * kBN;
+                const uint32_t d = tmem + acc * BN;
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % kStages;
                     if (!waitb(smem_u32(bars + s), (it / kStages) & 1)) {
@@ -321,14 +379,14 @@ __global__ void __launch_bounds__(kThreads, 1) proj_tc_kernel(
                 break;
             tc_fence_after();
             if (split)
-                break;                   // (the partial is read after the cluster barrier)
+                break;                   // (the partial is exchanged below)
             int j, n0, m0;
-            tile_coords(a, t, j, n0, m0);
+            tile_coords<BN>(a, t, j, n0, m0);
             const ProjMat& mat = a.mat[j];
             const int m = m0 + row;
             uint32_t v[32];
-            for (int c0 = 0; c0 < kBN; c0 += 32) {
-                tmem_ld32(trow + acc * kBN + c0, v);
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                tmem_ld32(trow + acc * BN + c0, v);
                 if (m >= a.M || n0 + c0 >= mat.n)
                     continue;
                 uint32_t w[16];
@@ -349,68 +407,102 @@ __global__ void __launch_bounds__(kThreads, 1) proj_tc_kernel(
         }
     }
     if (split) {
-        // Every CTA's MMAs are done once all have reached the barrier, so their stage
-        // memory is free. Rows [r R, (r+1) R) of the tile belong to rank r: each epilogue
-        // thread pushes its row of the fp32 partial, 32 columns at a time, into the owning
-        // rank's shared memory, slot [this rank][row - r R]; after a second barrier each rank
-        // sums its rows over the slots in rank order and stores them.
-        __syncthreads();
-        cluster_sync();
-        tc_fence_after();
+        // Every rank's partial is in its TMEM once its MMAs are done (the epilogue warps
+        // have seen the accumulator barrier), and its stages are free. The epilogue
+        // threads put the rows other ranks own into the stages ([owner][row - owner R]),
+        // thread 0 sends each owner its block with one bulk copy into the owner's receive
+        // buffer (slot of this rank among the others), and the owners sum in rank order.
+        __syncwarp();
+        asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
         int j, n0, m0;
-        tile_coords(a, first_tile, j, n0, m0);
+        tile_coords<BN>(a, first_tile, j, n0, m0);
         const ProjMat& mat = a.mat[j];
-        const int rows = min(kBM, a.M - m0);
-        const int R = (rows + a.split - 1) / a.split;
-        const uint32_t red0 = base;                     // [split][R][kRedStride] fp32
-        if (warp >= 2) {
-            const int q = warp & 3, row = q * 32 + lane;
-            const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-            if (q * 32 < rows) {                        // (warp-uniform)
-                const uint32_t owner = (uint32_t)(row / R);
-                const uint32_t slot =
-                    red0 + (uint32_t)((rank * R + (row - (int)owner * R)) * kRedStride) * 4u;
-                uint32_t remote = 0;
-                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(slot), "r"(owner));
-                for (int c0 = 0; c0 < kBN; c0 += 32) {
-                    uint32_t v[32];
-                    if (nkb > 0) {
-                        tmem_ld32(trow + c0, v);
+        const int q = warp & 3, row = q * 32 + lane;
+        const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+        const int owner = row / R;
+        const bool have = warp >= 2 && nkb > 0 && !*(volatile int*)&dead;
+        float own[BN];
+        if (warp >= 2 && q * 32 < rows) {                         // (warp-uniform)
+            uint32_t v[32];
+#pragma unroll
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                if (have) {
+                    tmem_ld32(trow + c0, v);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = 0u;                                // (no K blocks: zeros)
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    own[c0 + i] = __uint_as_float(v[i]);
+            }
+            if (row < rows && owner != (int)rank) {
+                float4* dst = reinterpret_cast<float4*>(sp + (size_t)(owner * R + row - owner * R) * kXRow);
+#pragma unroll
+                for (int i = 0; i < BN / 4; ++i)
+                    dst[i] = make_float4(own[4 * i], own[4 * i + 1], own[4 * i + 2], own[4 * i + 3]);
+            }
+        }
+        fence_proxy_async_shared();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int o = 0; o < a.split; ++o) {
+                const int orows = max(0, min(R, rows - o * R));
+                if (o == (int)rank || orows == 0)
+                    continue;
+                const uint32_t slot = (uint32_t)((int)rank < o ? rank : rank - 1);
+                bulk_s2cluster(cluster_addr(smem_u32(recv) + slot * (uint32_t)R * kXRow, (uint32_t)o),
+                               smem_u32(sp) + (uint32_t)(o * R) * kXRow, (uint32_t)orows * kXRow,
+                               cluster_addr(smem_u32(rx), (uint32_t)o));
+            }
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        if (warp >= 2 && q * 32 < rows) {
+            bool ok = mine == 0 || waitb(smem_u32(rx), 0);
+            if (row < rows && owner == (int)rank && ok) {
+                const int rl = row - (int)rank * R;
+                float sum[BN];
+#pragma unroll
+                for (int c = 0; c < BN; ++c)
+                    sum[c] = 0.f;
+                for (int src = 0; src < a.split; ++src) {
+                    if (src == (int)rank) {
+#pragma unroll
+                        for (int c = 0; c < BN; ++c)
+                            sum[c] += own[c];
                     } else {
+                        const int slot = src < (int)rank ? src : src - 1;
+                        const float4* pp = reinterpret_cast<const float4*>(recv + (size_t)(slot * R + rl) * kXRow);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[i] = 0u;                  // (a CTA without K blocks adds zeros)
-                    }
-                    if (row < rows) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                             remote + (uint32_t)(c0 + 4 * i) * 4u),
-                                         "r"(v[4 * i]), "r"(v[4 * i + 1]), "r"(v[4 * i + 2]),
-                                         "r"(v[4 * i + 3])
-                                         : "memory");
+                        for (int i = 0; i < BN / 4; ++i) {
+                            const float4 f = pp[i];
+                            sum[4 * i] += f.x;
+                            sum[4 * i + 1] += f.y;
+                            sum[4 * i + 2] += f.z;
+                            sum[4 * i + 3] += f.w;
+                        }
                     }
                 }
+                const int m = m0 + row;
+                if (m < a.M && n0 < mat.n) {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(mat.out) + (size_t)m * mat.n + n0);
+                    const int left = mat.n - n0;          // a multiple of 8 columns
+#pragma unroll
+                    for (int i = 0; i < BN / 8; ++i)
+                        if (8 * i < left)
+                            __stcs(dst + i, make_uint4(pack_bf16x2(sum[8 * i], sum[8 * i + 1]),
+                                                       pack_bf16x2(sum[8 * i + 2], sum[8 * i + 3]),
+                                                       pack_bf16x2(sum[8 * i + 4], sum[8 * i + 5]),
+                                                       pack_bf16x2(sum[8 * i + 6], sum[8 * i + 7])));
+                }
             }
+            if (!ok && lane == 0)
+                mbar_drain(smem_u32(rx), 0, kSpinLimitCycles);   // (late copies land first)
         }
-        cluster_sync();
-        const float* red = reinterpret_cast<const float*>(sp);
-        const int r0 = (int)rank * R, r1 = min(rows, r0 + R);
-        const int cols = min(kBN, mat.n - n0);          // a multiple of 8
-        const int groups = cols / 8;
-        for (int e = threadIdx.x; e < (r1 - r0) * groups; e += kThreads) {
-            const int rl = e / groups, c = (e % groups) * 8;
-            float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int src = 0; src < a.split; ++src) {
-                const float4* pp = reinterpret_cast<const float4*>(red + (size_t)(src * R + rl) * kRedStride + c);
-                const float4 p0 = pp[0], p1 = pp[1];
-                sum[0] += p0.x; sum[1] += p0.y; sum[2] += p0.z; sum[3] += p0.w;
-                sum[4] += p1.x; sum[5] += p1.y; sum[6] += p1.z; sum[7] += p1.w;
-            }
-            uint4 o = make_uint4(pack_bf16x2(sum[0], sum[1]), pack_bf16x2(sum[2], sum[3]),
-                                 pack_bf16x2(sum[4], sum[5]), pack_bf16x2(sum[6], sum[7]));
-            __stcs(reinterpret_cast<uint4*>(static_cast<bf16*>(mat.out) + (size_t)(m0 + r0 + rl) * mat.n + n0 + c), o);
-        }
+        // this CTA's copies are done (read and written) before it may end
+        if (threadIdx.x == 0)
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
@@ -519,28 +611,82 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uin
 
 }  // namespace
 
-static size_t proj_smem_bytes() { return 1024 + (size_t)kStages * kStageBytes + (2 * kStages + 4) * 8 + 16; }
-
-// CTAs per tile: a cluster per tile along K once the tiles of the whole-K kernel would
-// leave most SMs idle (few tokens). A function of the layer's shape and the token count
-// only (all three products counted, whichever a launch computes), so that the same shape
-// always takes the same path and gives the same bits.
-static int proj_split_for(const sdm_cfg& c, int64_t ntok)
+template <int BN>
+static size_t proj_smem_bytes()
 {
-    const int sms = num_sms_current_device();
+    using TL = Tile<BN>;
+    return 1024 + (size_t)TL::kStages * TL::kStageBytes + (2 * TL::kStages + 8) * 8 +
+           (BN == 64 ? kRecvBytes : 0);
+}
+
+// Tile width: 64 columns once 256-column tiles would leave most SMs idle (few tokens),
+// else 256. A function of the layer's shape and the token count only (all three products
+// counted, whichever a launch computes), so that the same shape always takes the same
+// path and gives the same bits.
+static bool proj_narrow(const sdm_cfg& c, int64_t ntok)
+{
     const int64_t mtiles = (ntok + kBM - 1) / kBM;
-    const int64_t tiles = mtiles * (2 * ((c.dk + kBN - 1) / kBN) + (c.d + kBN - 1) / kBN);
-    const int kblocks = (c.d + kBK - 1) / kBK;
-    if (tiles * 2 >= sms)
-        return 1;
-    int s = kMaxSplit;
-    while (s > 1 && (s > kblocks || tiles * s > 2 * sms))
-        s /= 2;
-    return s;
+    const int64_t tiles = mtiles * (2 * ((c.dk + 255) / 256) + (c.d + 255) / 256);
+    return tiles * 2 < num_sms_current_device();
+}
+
+template <int BN>
+static cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap (&mw)[3], ProjArgs a,
+                             cudaStream_t s, bool early, long long full_tiles)
+{
+    int ntiles = 0;
+    for (int q = 0; q < 3; ++q) {
+        a.mat[q].ntiles = a.mat[q].ntiles > 0 ? (a.mat[q].n + BN - 1) / BN : 0;
+        ntiles += a.mat[q].ntiles;
+    }
+    a.tiles = a.mtiles * ntiles;
+    // 64-column tiles: split along K while the clusters still fit the SMs (at least two K
+    // blocks a CTA); the count follows from the shape alone (all three products)
+    a.split = 1;
+    if (BN == 64) {
+        const int sms = num_sms_current_device();
+        for (int sp = kMaxSplit; sp > 1; --sp)
+            if ((long long)full_tiles * sp <= sms && a.kblocks >= 2 * sp) {
+                a.split = sp;
+                break;
+            }
+    }
+    const size_t smem = proj_smem_bytes<BN>();
+    auto kern = proj_tc_kernel<BN>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    int grid = num_sms_current_device();
+    if (grid > a.tiles)
+        grid = a.tiles;
+    if (a.split > 1)
+        grid = a.tiles * a.split;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (a.split > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)a.split;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (early) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = (unsigned)na;
+    return cudaLaunchKernelEx(&cfg, kern, mx, mw[0], mw[1], mw[2], a);
 }
 
 cudaError_t launch_project_tc(const sdm_cfg& c, const sdm_weights& w, const void* x, int64_t ntok,
-                              void* q_w, void* q_r, void* v, cudaStream_t s, int which)
+                              void* q_w, void* q_r, void* v, cudaStream_t s, int which, bool early)
 {
     if (ntok <= 0 || (which & 7) == 0)
         return cudaSuccess;
@@ -567,11 +713,15 @@ cudaError_t launch_project_tc(const sdm_cfg& c, const sdm_weights& w, const void
         proj_f32_kernel<<<grid, 256, 0, s>>>((const float*)x, fm, (int)ntok, c.d);
         return cudaGetLastError();
     }
+    // Fewer tokens than a tile: the x copies bring only the token rows (rounded up to the
+    // 8-row swizzle period); the MMA's other rows read whatever the stage holds, and the
+    // rows of the result they give are never stored (a row of the product depends on
+    // the same row of x alone).
     CUtensorMap mx, mw[3];
-    if (!make_map(&mx, x, (uint64_t)c.d, (uint64_t)ntok, kBM))
+    const int abox = ntok >= kBM ? kBM : (int)((ntok + 7) / 8 * 8);
+    if (!make_map(&mx, x, (uint64_t)c.d, (uint64_t)ntok, (uint32_t)abox))
         return cudaErrorInvalidValue;
     ProjArgs a;
-    int ntiles = 0;
     for (int q = 0; q < 3; ++q) {
         const bool used = q < nsel;
         const int j = sel[used ? q : 0];
@@ -579,41 +729,19 @@ cudaError_t launch_project_tc(const sdm_cfg& c, const sdm_weights& w, const void
             return cudaErrorInvalidValue;
         a.mat[q].out = outs[j];
         a.mat[q].n = ns[j];
-        a.mat[q].ntiles = used ? (ns[j] + kBN - 1) / kBN : 0;
-        ntiles += a.mat[q].ntiles;
+        a.mat[q].ntiles = used ? 1 : 0;   // (counted per tile width at launch)
     }
     a.M = (int)ntok;
     a.K = c.d;
     a.kblocks = (c.d + kBK - 1) / kBK;
     a.mtiles = (int)((ntok + kBM - 1) / kBM);
-    a.tiles = a.mtiles * ntiles;
+    a.abox = abox;
+    a.tiles = 0;
     a.status = nullptr;
-    a.split = proj_split_for(c, ntok);
-    const size_t smem = proj_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess)
-        return e;
-    if (a.split == 1) {
-        int grid = num_sms_current_device();
-        if (grid > a.tiles)
-            grid = a.tiles;
-        proj_tc_kernel<<<grid, kThreads, smem, s>>>(mx, mw[0], mw[1], mw[2], a);
-        return cudaGetLastError();
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(a.tiles * a.split), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)a.split;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, proj_tc_kernel, mx, mw[0], mw[1], mw[2], a);
+    // tiles of all three products, whichever this launch computes (the split count)
+    const long long full64 = (long long)a.mtiles * (2 * ((c.dk + 63) / 64) + (c.d + 63) / 64);
+    return proj_narrow(c, ntok) ? launch_tc<64>(mx, mw, a, s, early, full64)
+                                : launch_tc<256>(mx, mw, a, s, early, 0);
 }
 
 }  // namespace sdm

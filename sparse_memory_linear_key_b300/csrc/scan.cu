@@ -397,11 +397,13 @@ __device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
     };
     Ahead<JW> nx;
     fetch_ahead<W, JW>(a, claim(), nx);
+    // the abort flag, read one item ahead so that its load overlaps the fetch (the flags
+    // are clear at launch)
+    int ab = 0;
     for (int k = 0;; ++k) {
         const int p = k & 1;
         Meta& m = meta[p];
-        int aborted = lane == 0 ? ld_relaxed_gpu(a.abort_flag) : 0;
-        aborted = __shfl_sync(0xFFFFFFFFu, aborted, 0);
+        const int aborted = __shfl_sync(0xFFFFFFFFu, ab, 0);
         // the description slot (and read buffer) is free once item k-2 is done
         if (!uniform_wait(smem_u32(bars + kEmptyR + p), ((k >> 1) & 1) ^ 1, a))
             return;
@@ -415,10 +417,12 @@ __device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
         }
         const int t = nx.t, b = nx.b, rb = nx.rb;
         const int* fl = item_flag(a, b, rb, 0);
-        // window: tokens t-2*win+1 .. t-win of this stream are committed
+        // window: tokens t-2*win+1 .. t-win of this stream are committed (acquired, when
+        // there are any)
         if (!window_geq(a, fl, t - 2 * a.win + 1, t - a.win + 1, 3))
             return;
-        fence_acq_rel_gpu();
+        if (t - a.win + 1 > 0)
+            fence_acq_rel_gpu();
 
         unsigned long long wload = 0, rload = 0, fmask = 0, rdmask = 0, m0w = 0, m0r = 0;
         unsigned long long rvalid = 0;
@@ -497,6 +501,7 @@ __device__ void role_producer(const ScanArgs& a, Meta* meta, uint64_t* bars)
             mbar_arrive(smem_u32(bars + kPosted + p));  // consumers and D may start on it
 
         // ---- the next item
+        ab = lane == 0 ? ld_relaxed_gpu(a.abort_flag) : 0;
         fetch_ahead<W, JW>(a, claim(), nx);
     }
 }
@@ -643,7 +648,8 @@ __device__ void role_clear(const ScanArgs& a, const Meta* meta, uint64_t* bars)
         }
         if (!__all_sync(0xFFFFFFFFu, ok))
             return;
-        fence_acq_rel_gpu();
+        if ((war[0] | war[1]) != 0)   // (acquire what the flags published)
+            fence_acq_rel_gpu();
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_u32(bars + kWar + p));
@@ -657,7 +663,9 @@ __device__ void role_clear(const ScanArgs& a, const Meta* meta, uint64_t* bars)
 // values (the consumers' arrival, release at CTA scope, followed by this release at GPU
 // scope publishes their global writes). The three marks advance independently: the
 // warp polls whichever is next for each and never blocks one behind another (a later
-// item's bank loads may wait on other tokens' commits, this item's among them).
+// item's bank loads may wait on other tokens' commits, this item's among them). With one
+// token a sequence no item waits on another's flag, and the marks are only the CTA's own
+// barrier arrivals.
 __device__ void role_marks(const ScanArgs& a, const Meta* meta, uint64_t* bars)
 {
     const int lane = threadIdx.x & 31;
@@ -679,7 +687,8 @@ __device__ void role_marks(const ScanArgs& a, const Meta* meta, uint64_t* bars)
                             uniform_test(smem_u32(bars + kDepR + p), (kl >> 1) & 1))) {
                     // (without the ring, dependent references are bank loads too)
                     if (lane == 0) {
-                        red_max_release_gpu(item_flag(a, m.b, m.rb, m.t), 1);
+                        if (a.T > 1)
+                            red_max_release_gpu(item_flag(a, m.b, m.rb, m.t), 1);
                         mbar_arrive(smem_u32(bars + kLmark));
                     }
                     ++kl;
@@ -689,7 +698,7 @@ __device__ void role_marks(const ScanArgs& a, const Meta* meta, uint64_t* bars)
         }
         if (kp < kl && uniform_test(smem_u32(bars + kFwdw + (kp & 1)), (kp >> 1) & 1)) {
             const Meta& m = meta[kp & 1];
-            if (lane == 0)
+            if (lane == 0 && a.T > 1)
                 red_max_release_gpu(item_flag(a, m.b, m.rb, m.t), 2);  // ring entries visible
             ++kp;
             progress = true;
@@ -700,7 +709,8 @@ __device__ void role_marks(const ScanArgs& a, const Meta* meta, uint64_t* bars)
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(smem_u32(bars + kEmptyR + (kc & 1)));
-                red_max_release_gpu(flag, 3);  // bank stores visible
+                if (a.T > 1)
+                    red_max_release_gpu(flag, 3);  // bank stores visible
             }
             ++kc;
             progress = true;
@@ -805,7 +815,10 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
             mbar_arrive_expect_tx(fr, rb);
         }
         __syncwarp();
-        fence_proxy_async_global();
+        // this thread's bank stores of earlier items before the copies read the bank (with
+        // one token a sequence no item reads what another writes)
+        if (a.T > 1)
+            fence_proxy_async_global();
         const unsigned char* bank =
             a.banks + ((size_t)mn.b * a.N * a.d + (size_t)mn.rb * a.rb_rows) * sizeof(S);
         if (chunk) {
@@ -1164,6 +1177,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a)
             reinterpret_cast<uint4*>(rbuf)[e] = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_shared();   // (before bulk copies write the buffers)
     }
+    griddep_wait();   // (a programmatic launch: the kernel before has completed)
+    griddep_launch();
     __syncthreads();
     const int warp = threadIdx.x >> 5;
     // Register split: the block is launched with 96 registers a thread (640 x 96 =
@@ -1186,7 +1201,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a)
 }
 
 template <typename S, int W>
-cudaError_t launch_scan_t(const ScanArgs& a, cudaStream_t s)
+cudaError_t launch_scan_t(const ScanArgs& a, cudaStream_t s, bool early)
 {
     const size_t smem = (size_t)W * kStride + (size_t)2 * W * ScanShape<S, W>::kRStride +
                         2 * sizeof(Meta) + kNumBars * sizeof(uint64_t) +
@@ -1200,8 +1215,21 @@ cudaError_t launch_scan_t(const ScanArgs& a, cudaStream_t s)
     long long grid = num_sms_current_device();
     if (grid > a.items)
         grid = a.items;
-    kern<<<(unsigned)grid, kScanThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    if (!early) {
+        kern<<<(unsigned)grid, kScanThreads, smem, s>>>(a);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kScanThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -1247,15 +1275,17 @@ cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel,
                         const float* alpha, const float* beta, void* banks, float* y, int B,
                         int T, void* ws, size_t ws_bytes, int* status, cudaStream_t s,
                         const void* m0, const int32_t* first_write, void* tape,
-                        long long spin_limit, long long skip_item)
+                        long long spin_limit, long long skip_item, bool early)
 {
     if (B <= 0 || T <= 0)
         return cudaSuccess;
     const ScanWs L = scan_ws_layout(c, B, T);
     char* base = (char*)ws;
-    cudaError_t e = cudaMemsetAsync(base + L.flags, 0, L.flags_bytes, s);
-    if (e != cudaSuccess)
-        return e;
+    if (!early) {
+        const cudaError_t e = clear_scan_flags(c, B, T, ws, s);
+        if (e != cudaSuccess)
+            return e;
+    }
     ScanArgs a;
     a.banks = (unsigned char*)banks;
     a.idx = idx;
@@ -1288,12 +1318,18 @@ cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel,
     a.skip_item = skip_item;
     const bool bf = c.dtype == SDM_BF16;
     switch (c.w) {
-    case 8: return bf ? launch_scan_t<bf16, 8>(a, s) : launch_scan_t<float, 8>(a, s);
-    case 16: return bf ? launch_scan_t<bf16, 16>(a, s) : launch_scan_t<float, 16>(a, s);
-    case 32: return bf ? launch_scan_t<bf16, 32>(a, s) : launch_scan_t<float, 32>(a, s);
-    case 64: return bf ? launch_scan_t<bf16, 64>(a, s) : launch_scan_t<float, 64>(a, s);
+    case 8: return bf ? launch_scan_t<bf16, 8>(a, s, early) : launch_scan_t<float, 8>(a, s, early);
+    case 16: return bf ? launch_scan_t<bf16, 16>(a, s, early) : launch_scan_t<float, 16>(a, s, early);
+    case 32: return bf ? launch_scan_t<bf16, 32>(a, s, early) : launch_scan_t<float, 32>(a, s, early);
+    case 64: return bf ? launch_scan_t<bf16, 64>(a, s, early) : launch_scan_t<float, 64>(a, s, early);
     default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t clear_scan_flags(const sdm_cfg& c, int B, int T, void* ws, cudaStream_t s)
+{
+    const ScanWs L = scan_ws_layout(c, B, T);
+    return cudaMemsetAsync((char*)ws + L.flags, 0, L.flags_bytes, s);
 }
 
 }  // namespace sdm

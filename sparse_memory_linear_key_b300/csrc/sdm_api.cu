@@ -28,11 +28,12 @@ int num_sms_current_device()
 
 static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Few tokens (a decode step): only q_w and q_r are on the way to the addressing, so v is
-// projected on a side stream forked off the caller's stream and joined back before the
+// Few tokens, several a sequence: only q_w and q_r are on the way to the addressing, so v
+// is projected on a side stream forked off the caller's stream and joined back before the
 // scan (event record / wait, so that a captured graph gets a parallel branch). One side
 // stream and two events per device; the lock keeps another thread's call off them from
-// the fork until the join is enqueued.
+// the fork until the join is enqueued. (One token a sequence takes the early-launch chain
+// in prefill_impl instead.)
 constexpr int64_t kForkTokens = 256;
 
 struct ProjFork {
@@ -244,7 +245,8 @@ int sdm_address(const sdm_cfg* cfg, const void* K1, const void* K2, const void* 
 static int scan_impl(const sdm_cfg& c, const int32_t* idx, const float* wsel, const void* v,
                      const float* alpha, const float* beta, void* banks, float* y, int B, int T,
                      void* ws, size_t ws_bytes, int* dev_status, cudaStream_t s,
-                     const void* m0 = nullptr, const int32_t* first_write = nullptr)
+                     const void* m0 = nullptr, const int32_t* first_write = nullptr,
+                     bool early = false)
 {
     const ScanWs L = scan_ws_layout(c, B, T);
     char* base = (char*)ws;
@@ -255,7 +257,7 @@ static int scan_impl(const sdm_cfg& c, const int32_t* idx, const float* wsel, co
     if (e != cudaSuccess)
         return SDM_ECUDA;
     e = launch_scan(c, idx, wsel, v, alpha, beta, banks, y, B, T, ws, ws_bytes, dev_status, s, m0,
-                    first_write);
+                    first_write, nullptr, 0, -1, early);
     return cuda_status(e);
 }
 
@@ -461,7 +463,19 @@ static int prefill_impl(const sdm_cfg* cfg, const sdm_weights* w, const void* M0
     std::unique_lock<std::mutex> lock;
     ProjFork* f = nullptr;
     bool ok = true;
-    if (ntok <= kForkTokens) {
+    // One token a sequence (a decode step): projections -> addressing -> scan is a chain
+    // of three short kernels, each launched early (programmatic dependent launch): the
+    // projections set up while the kernel before them (the previous step's scan) ends, the
+    // addressing stages its sub-key table while the projections run, the scan sets up
+    // while the addressing runs. One projection launch for q and v, and the scan's flags
+    // cleared by the addressing kernel, so that each kernel has one kernel before it and
+    // nothing else lies between them.
+    const bool early = T == 1 && ntok <= kForkTokens;
+    void* scan_ws = base + L.scan;
+    const ScanWs SL = scan_ws_layout(*cfg, B, T);
+    if (early) {
+        ok = launch_project_tc(*cfg, *w, x, ntok, q_w, q_r, v, s, 7, true) == cudaSuccess;
+    } else if (ntok <= kForkTokens) {
         lock = std::unique_lock<std::mutex>(g_fork_mu);
         f = fork_state();
         if (f == nullptr)
@@ -479,7 +493,8 @@ static int prefill_impl(const sdm_cfg* cfg, const sdm_weights* w, const void* M0
     }
     ok = ok &&
          launch_address(*cfg, w->K1, w->K2, q_w, q_r, ntok, idx, wsel, base + L.addr, dev_status,
-                        s) == cudaSuccess &&
+                        s, ntok <= kForkTokens, early ? (char*)scan_ws + SL.flags : nullptr,
+                        early ? SL.flags_bytes : 0) == cudaSuccess &&
          (M0 == nullptr || launch_first_touch(*cfg, idx, B, T, first_write, s) == cudaSuccess);
     if (f != nullptr) {
         // v is ready for the scan
@@ -489,8 +504,8 @@ static int prefill_impl(const sdm_cfg* cfg, const sdm_weights* w, const void* M0
     }
     if (!ok)
         return SDM_ECUDA;
-    rc = scan_impl(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, base + L.scan,
-                   scan_ws_layout(*cfg, B, T).total, dev_status, s, M0, first_write);
+    rc = scan_impl(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, scan_ws, SL.total, dev_status,
+                   s, M0, first_write, early);
     if (rc != SDM_OK || M0 == nullptr)
         return rc;
     return cuda_status(launch_fill_untouched(*cfg, M0, first_write, banks, B, T, s));

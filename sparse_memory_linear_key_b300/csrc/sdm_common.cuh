@@ -225,6 +225,23 @@ __device__ __forceinline__ void fence_proxy_async_shared()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the kernel before it in the stream still runs, and
+// griddep_wait() blocks until that kernel has completed and its memory is visible; a
+// kernel launched without it passes straight through. griddep_launch() lets the next
+// kernel start once every CTA of this one has issued it (or exited). Kernels of this
+// library issue it only after their own wait, so a kernel that starts early overlaps
+// only the kernel right before it, never work further back in the stream.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
     return (uint32_t)__cvta_generic_to_shared(p);

@@ -25,8 +25,11 @@ cudaError_t launch_bank_init(const void* M0, void* banks, size_t bank_bytes, int
 // ---- projections (proj_tc.cu): q_w, q_r, v of ntok tokens in one launch (bf16: tcgen05
 // tensor cores; fp32: SIMT fp32)
 // which: bit 0 q_w, bit 1 q_r, bit 2 v (the products to compute)
+// early: the launch may overlap the kernel before it in the stream (programmatic
+// dependent launch); the kernel touches no global memory until that one has completed
 cudaError_t launch_project_tc(const sdm_cfg& c, const sdm_weights& w, const void* x, int64_t ntok,
-                              void* q_w, void* q_r, void* v, cudaStream_t s, int which = 7);
+                              void* q_w, void* q_r, void* v, cudaStream_t s, int which = 7,
+                              bool early = false);
 
 // ---- addressing (address.cu, score_tc.cu)
 // z with P(Z > z) = p for a standard normal Z (a starting bracket for exact top-W searches)
@@ -36,9 +39,14 @@ cudaError_t launch_score_tc(const sdm_cfg& c, const void* K1, const void* K2, co
                             const void* q_r, int64_t ntok, float* hv, int32_t* hi, int* status,
                             cudaStream_t s);
 size_t address_ws_bytes(const sdm_cfg& c, int64_t ntok);
+// early: the launch may overlap the kernel before it in the stream (programmatic
+// dependent launch), which must not write K1 or K2; only the few-token kernel uses it.
+// clear / clear_bytes (a multiple of 4): a buffer zeroed along the way, for the kernel
+// after (the scan's flags), so that no memset lies between the two
 cudaError_t launch_address(const sdm_cfg& c, const void* K1, const void* K2, const void* q_w,
                            const void* q_r, int64_t ntok, int32_t* idx, float* wsel, void* ws,
-                           int* status, cudaStream_t s);
+                           int* status, cudaStream_t s, bool early = false,
+                           void* clear = nullptr, size_t clear_bytes = 0);
 
 // ---- scan (scan.cu, scan_codes.cu)
 // Layout of the scan's workspace for B sequences of T tokens (byte offsets):
@@ -65,7 +73,11 @@ cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel,
                         int T, void* ws, size_t ws_bytes, int* status, cudaStream_t s,
                         const void* m0 = nullptr, const int32_t* first_write = nullptr,
                         void* tape = nullptr, long long spin_limit = 0,
-                        long long skip_item = -1);
+                        long long skip_item = -1, bool early = false);
+// early (above): the flags are already clear (clear_scan_flags, issued earlier on the
+// stream) and the kernel launches with programmatic dependent launch, overlapping the
+// kernel before it until its first global access
+cudaError_t clear_scan_flags(const sdm_cfg& c, int B, int T, void* ws, cudaStream_t s);
 
 // Backward of the recurrence (scan_bwd.cu): reverse token order over a gradient bank;
 // ws holds per-block partial sums (scan_backward_ws_bytes).
