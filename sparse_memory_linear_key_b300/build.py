@@ -13,9 +13,9 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "lib")
 LIB = os.path.join(OUT_DIR, "libsdm.so")
 SOURCES = ["sdm_api.cu", "bank_init.cu", "project.cu", "proj_tc.cu", "address.cu", "score_tc.cu",
-           "scan_codes.cu", "scan.cu", "scan_static.cu", "slot_stats.cu",
+           "scan_codes.cu", "scan.cu", "scan_step.cu", "scan_static.cu", "slot_stats.cu",
            "gdn_dense.cu", "scan_bwd.cu", "addr_bwd.cu"]
-HEADERS = ["sdm_common.cuh", "sdm_internal.h"]
+HEADERS = ["sdm_common.cuh", "sdm_internal.h", "scan_math.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -54,6 +54,7 @@
 // waits on another without a bound, so none can hang.
 #include <cstddef>
 
+#include "scan_math.cuh"
 #include "sdm_common.cuh"
 #include "sdm_internal.h"
 
@@ -73,7 +74,6 @@ static_assert(kCWarps * 32 * kConsumerRegs + 4 * 32 * kRoleRegs <= kScanThreads 
               "register split exceeds the block's launch allocation");
 static_assert(kCWarps % 4 == 0, "consumer warps must form whole warpgroups");
 constexpr int kMaxW = 64;
-constexpr int kSG = 8;             // slot groups (lanes sharing a row group)
 
 // With bf16 state and W >= 16 the read y = sum_j r_j M[R_j] runs on the tensor cores
 // (mma.sync m16n8k16 per 16 rows, the read chunks as A through ldmatrix.trans). The eight
@@ -158,61 +158,6 @@ enum {
     kFullW = 0, kWfree = 1, kFullR = 2, kEmptyR = 4, kDepB = 6, kPosted = 8, kWar = 10,
     kFwdw = 12, kStored = 14, kCbar = 16, kLmark = 17, kDepR = 18, kNumBars = 20
 };
-
-// 16 bytes of one slot vector (8 rows in bf16, 4 in fp32) as fp32 pairs, the operand
-// of the packed two-lane fp32 FMA.
-template <typename S>
-struct Pack16;
-
-template <>
-struct Pack16<bf16> {
-    static constexpr int R = 8;   // rows
-    static constexpr int H = 4;   // fp32 pairs
-    static __device__ __forceinline__ void unpack(const uint4& q, float2 (&f)[H])
-    {
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
-    }
-    // round-to-nearest-even, once per value
-    static __device__ __forceinline__ uint4 pack(const float2 (&f)[H])
-    {
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            __nv_bfloat162 h = __float22bfloat162_rn(f[i]);
-            w[i] = *reinterpret_cast<uint32_t*>(&h);
-        }
-        return make_uint4(w[0], w[1], w[2], w[3]);
-    }
-};
-
-template <>
-struct Pack16<float> {
-    static constexpr int R = 4;
-    static constexpr int H = 2;
-    static __device__ __forceinline__ void unpack(const uint4& q, float2 (&f)[H])
-    {
-        f[0] = make_float2(__uint_as_float(q.x), __uint_as_float(q.y));
-        f[1] = make_float2(__uint_as_float(q.z), __uint_as_float(q.w));
-    }
-    static __device__ __forceinline__ uint4 pack(const float2 (&f)[H])
-    {
-        return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y), __float_as_uint(f[1].x),
-                          __float_as_uint(f[1].y));
-    }
-};
-
-// sum of a pair over the eight slot groups of a row group (lanes 4 apart)
-__device__ __forceinline__ float2 slot_group_sum(float2 v)
-{
-#pragma unroll
-    for (int o = 4; o <= 16; o <<= 1)
-        v = __fadd2_rn(v, make_float2(__shfl_xor_sync(0xFFFFFFFFu, v.x, o),
-                                      __shfl_xor_sync(0xFFFFFFFFu, v.y, o)));
-    return v;
-}
 
 __device__ __forceinline__ bool uniform_wait(uint32_t bar, uint32_t parity, const ScanArgs& a)
 {
@@ -358,16 +303,6 @@ __device__ __forceinline__ void fetch_ahead(const ScanArgs& a, unsigned long lon
         n.war0 = many ? __ldg(a.masks + 2 * BT + 2 * tok) : 0ull;
         n.war1 = many ? __ldg(a.masks + 2 * BT + 2 * tok + 1) : 0ull;
     }
-}
-
-// the part of a weight that column `part` of the B fragment holds: 0 the nearest bf16, 1
-// the nearest bf16 of what that leaves (together about 16 bits of the fp32 weight)
-__device__ __forceinline__ uint32_t weight_part_bits(float w, int part)
-{
-    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(w - __bfloat162float(hi));
-    const __nv_bfloat16 v = part == 0 ? hi : lo;
-    return part < 2 ? (uint32_t)*reinterpret_cast<const unsigned short*>(&v) : 0u;
 }
 
 template <typename S, int W>
@@ -672,6 +607,7 @@ __device__ void role_marks(const ScanArgs& a, const Meta* meta, uint64_t* bars)
     int kl = 0, kp = 0, kc = 0;   // next item to mark loaded, ring-published, committed
     int end = -1;                 // item number of the empty end item, once seen
     long long idle = clock64();
+    long long next_poll = idle + kAbortPollCycles;
     while (true) {
         bool progress = false;
         if (end < 0) {
@@ -721,11 +657,16 @@ __device__ void role_marks(const ScanArgs& a, const Meta* meta, uint64_t* bars)
             idle = clock64();
             continue;
         }
+        __nanosleep(20);
+        const long long now = clock64();
+        if (now < next_poll)
+            continue;
+        next_poll = now + kAbortPollCycles;
         int stop = 0;
         if (lane == 0) {
             if (ld_relaxed_gpu(a.abort_flag) != 0) {
                 stop = 1;
-            } else if (clock64() - idle > a.spin_limit) {
+            } else if (now - idle > a.spin_limit) {
                 report(a.status, SDM_ETIMEOUT);
                 st_relaxed_gpu(a.abort_flag, 1);
                 stop = 1;
@@ -733,7 +674,6 @@ __device__ void role_marks(const ScanArgs& a, const Meta* meta, uint64_t* bars)
         }
         if (__shfl_sync(0xFFFFFFFFu, stop, 0))
             return;
-        __nanosleep(20);
     }
 }
 
@@ -1279,6 +1219,10 @@ cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel,
 {
     if (B <= 0 || T <= 0)
         return cudaSuccess;
+    // one token a sequence: independent items, all in one wave (scan_step.cu)
+    if (T == 1 && m0 == nullptr && first_write == nullptr && tape == nullptr && spin_limit <= 0 &&
+        skip_item < 0 && scan_step_supported(c))
+        return launch_scan_step(c, idx, wsel, v, alpha, beta, banks, y, B, status, s, early);
     const ScanWs L = scan_ws_layout(c, B, T);
     char* base = (char*)ws;
     if (!early) {

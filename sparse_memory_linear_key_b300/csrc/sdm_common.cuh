@@ -304,6 +304,12 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// How often a wait that goes on looks at the global abort flag and its own bound: a
+// read of the flag is a round trip to L2, and a wait that made one on every pass would
+// notice its own barrier only that much later. Aborts come from errors alone, so a few
+// microseconds' delay in seeing one costs nothing.
+constexpr long long kAbortPollCycles = 4096;
+
 // Bounded wait for the phase of parity `parity` of an mbarrier. Returns false if the
 // global abort flag is raised (abort may be null: not watched) or the wait ran out;
 // a wait that ran out records SDM_ETIMEOUT and raises the abort flag.
@@ -313,12 +319,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* ab
     if (mbar_try_wait(bar, parity))
         return true;
     const long long t0 = clock64();
+    long long next = t0 + kAbortPollCycles;
     while (true) {
         if (mbar_try_wait(bar, parity))
             return true;
+        const long long now = clock64();
+        if (now < next)
+            continue;
+        next = now + kAbortPollCycles;
         if (abort != nullptr && ld_relaxed_gpu(abort) != 0)
             return false;
-        if (clock64() - t0 > limit) {
+        if (now - t0 > limit) {
             report(status, SDM_ETIMEOUT);
             if (abort != nullptr)
                 st_relaxed_gpu(abort, 1);
@@ -335,13 +346,18 @@ __device__ __forceinline__ bool spin_geq_gpu(const int* f, int target, int* abor
     if (ld_relaxed_gpu(f) >= target)
         return true;
     const long long t0 = clock64();
+    long long next = t0 + kAbortPollCycles;
     while (true) {
-        __nanosleep(100);
+        __nanosleep(32);
         if (ld_relaxed_gpu(f) >= target)
             return true;
+        const long long now = clock64();
+        if (now < next)
+            continue;
+        next = now + kAbortPollCycles;
         if (ld_relaxed_gpu(abort) != 0)
             return false;
-        if (clock64() - t0 > limit) {
+        if (now - t0 > limit) {
             report(status, SDM_ETIMEOUT);
             st_relaxed_gpu(abort, 1);
             return false;

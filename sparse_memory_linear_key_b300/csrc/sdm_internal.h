@@ -78,6 +78,12 @@ cudaError_t launch_scan(const sdm_cfg& c, const int32_t* idx, const float* wsel,
 // stream) and the kernel launches with programmatic dependent launch, overlapping the
 // kernel before it until its first global access
 cudaError_t clear_scan_flags(const sdm_cfg& c, int B, int T, void* ws, cudaStream_t s);
+// One token a sequence (scan_step.cu): every (sequence, row block) item in one wave, same
+// arithmetic and bits as launch_scan; bf16 state with w >= 16, no M0, no tape.
+bool scan_step_supported(const sdm_cfg& c);
+cudaError_t launch_scan_step(const sdm_cfg& c, const int32_t* idx, const float* wsel, const void* v,
+                             const float* alpha, const float* beta, void* banks, float* y, int B,
+                             int* status, cudaStream_t s, bool early);
 
 // Backward of the recurrence (scan_bwd.cu): reverse token order over a gradient bank;
 // ws holds per-block partial sums (scan_backward_ws_bytes).

@@ -341,6 +341,71 @@ def test_single_token_and_single_sequence():
         assert tl.state_ok("bf16", y[b].cpu().numpy()[None], yr)[0]
 
 
+@pytest.mark.parametrize("B,N,W,d,seed", [
+    (64, 4096, 64, 2048, 11),     # the decode shape: 64 sequences x 4 row blocks
+    (37, 1024, 64, 1280, 12),     # row blocks of 512, 512 and 256 rows; many own reads
+    (9, 256, 32, 640, 13),
+    (200, 64, 16, 96, 14),        # more items than two CTAs an SM hold at once
+])
+def test_one_token_kernel_matches_persistent_scan(B, N, W, d, seed):
+    """With one token a sequence the scan runs every (sequence, row block) item in one wave
+    (scan_step.cu) with the persistent kernel's arithmetic. Against the persistent kernel
+    itself (the diagnostic entry point with an explicit wait bound takes it) on the same
+    inputs: the same bits, y and banks; against the oracle: every row of the first and
+    last sequences. A fifth of the tokens read exactly the slots they write, the others
+    share some (the new values must reach the read)."""
+    rng = np.random.default_rng(seed)
+    n = int(round(N ** 0.5))
+    cfg = sdm.make_cfg(d, n, 16, W, "bf16")
+    idx = np.zeros((B, 2, W), dtype=np.int32)
+    idx[:, 0] = _random_sets(rng, B, N, W)
+    idx[:, 1] = _random_sets(rng, B, N, W)
+    for b in range(B):
+        if rng.random() < 0.2:
+            idx[b, 1] = idx[b, 0]
+        else:                                   # share about a quarter of the write set
+            keep = rng.choice(W, W // 4, replace=False)
+            rest = np.setdiff1d(np.arange(N), idx[b, 0])
+            extra = rng.choice(rest, W - W // 4, replace=False)
+            idx[b, 1] = np.sort(np.concatenate([idx[b, 0, keep], extra]))
+    wts = (rng.random((B, 2, W)) + 0.05).astype(np.float32)
+    wts /= wts.sum(-1, keepdims=True)
+    v = torch.randn(B, d, generator=torch.Generator().manual_seed(seed)).to(torch.bfloat16)
+    M0 = (torch.randn(N, d, generator=torch.Generator().manual_seed(seed + 1)) * 0.1).to(torch.bfloat16)
+    alpha = torch.from_numpy(rng.uniform(0.5, 1.0, B).astype(np.float32))
+    beta = torch.from_numpy(rng.uniform(0.0, 1.0, B).astype(np.float32))
+    dev = [t.cuda().contiguous() for t in (torch.from_numpy(idx), torch.from_numpy(wts), v, alpha, beta)]
+    st = sdm.new_status()
+    ws = sdm.alloc_workspace(sdm.scan_workspace_bytes(cfg, B, 1))
+    outs = []
+    for persistent in (False, True):
+        banks = torch.empty((B,) + tuple(M0.shape), dtype=M0.dtype, device="cuda")
+        sdm.sdm_init_bank(cfg, M0.cuda(), banks)
+        y = torch.full((B, d), float("nan"), device="cuda")
+        sdm.sdm_scan_prepare(cfg, dev[0], B, 1, ws, st)
+        if persistent:
+            sdm.sdm_scan_run_diag(cfg, *dev, banks, y, B, 1, ws, 2 * 10 ** 9, -1, st)
+        else:
+            sdm.sdm_scan_run(cfg, *dev, banks, y, B, 1, ws, st)
+        torch.cuda.synchronize()
+        assert sdm.read_status(st) == 0
+        outs.append((y, banks))
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1], outs[1][1])
+    y, banks = outs[0]
+    for b in (0, B - 1):
+        M = np.ascontiguousarray(oracle.storage(M0)[0].copy())
+        yr = oracle.scan(M, oracle.storage(v[b:b + 1])[0], alpha[b:b + 1].numpy().astype(np.float64),
+                         beta[b:b + 1].numpy().astype(np.float64), idx[b:b + 1, 0],
+                         wts[b:b + 1, 0].astype(np.float64), idx[b:b + 1, 1],
+                         wts[b:b + 1, 1].astype(np.float64))
+        ok, m = tl.state_ok("bf16", y[b].cpu().numpy()[None], yr)
+        assert ok, ("y", b, m)
+        touched = np.union1d(idx[b, 0], idx[b, 1])
+        ok, m = tl.state_ok("bf16", oracle.to_f64(banks[b].cpu())[touched], oracle.to_f64(M)[touched])
+        assert ok, ("bank", b, m)
+
+
 def test_zero_tokens_is_a_no_op():
     wl = SMALL["ragged-bf16"]
     cfg = tl.cfg_of(wl)
