@@ -9,14 +9,14 @@
 // ordering (progress flags, forwarding ring, window) applies. One CTA per item, 16 warps
 // in scan.cu's consumer layout (a thread: 16 bytes of rows of the slots i*8 + its slot
 // group):
-//  1. the token's slot ids and weights into shared memory; each read of a slot the token
-//     also writes is matched to its write position (binary search over the ascending
-//     write set), and its row of the read buffer waits for the new value;
-//  2. the other read chunks are gathered from the bank into the read buffer by bulk
-//     copies (rows of out-of-range ids are zeroed: their weight is 0);
-//  3. each thread loads its write chunks from the bank into registers, forms u and the
-//     new values (rounded once), stores them to the bank and puts those the token also
-//     reads into the read buffer;
+//  1. the token's slot ids and weights into shared memory (v is loaded first);
+//  2. each read of a slot the token also writes is matched to its write position (binary
+//     search over the ascending write set); every other read chunk is gathered from the
+//     bank into the read buffer by bulk copies, at once (rows of out-of-range ids are
+//     zeroed: their weight is 0);
+//  3. each thread loads its write chunks from the bank into registers, forms u, the new
+//     values (rounded once) and their bank stores, and puts the new values of the token's
+//     own reads into their rows of the read buffer;
 //  4. y on the tensor cores (mma.sync over the read buffer, the read weights in two bf16
 //     parts), as scan.cu computes it.
 // A CTA holds the read buffer alone (about 69 KB) at 64 registers a thread, so two CTAs
@@ -85,6 +85,9 @@ __global__ void __launch_bounds__(kStepThreads, 2) scan_step_kernel(StepArgs a)
     griddep_wait();
     griddep_launch();
 
+    // v (independent of the slot sets) first
+    const uint4 vraw = act ? ld_u4(a.v + ((size_t)b * a.d + (size_t)rb * a.rb_rows) * sizeof(S) + rg * 16)
+                           : make_uint4(0u, 0u, 0u, 0u);
     // 1. slot ids and weights of the token (b: one token a sequence)
     const size_t tb = (size_t)b * 2 * W;
     if (ct < 2 * W) {
@@ -102,10 +105,13 @@ __global__ void __launch_bounds__(kStepThreads, 2) scan_step_kernel(StepArgs a)
         ab[1] = __ldg(a.beta + b);
     }
     __syncthreads();
-    // reads of slots the token writes: the write position of the same slot
-    int src = -1;
+    // 2. reads of slots the token writes: the write position of the same slot (their rows
+    // take the new values later); every other read chunk in range from the bank, at once
+    // (rows of out-of-range ids zeroed)
+    unsigned char* wrow = a.banks + ((size_t)b * a.N * a.d + (size_t)rb * a.rb_rows) * sizeof(S) + rg * 16;
     if (ct < W) {
         const int r = sid[W + ct];
+        int src = -1;
         if (r >= 0) {
             int lo = 0, hi = W;
             while (lo < hi) {
@@ -120,24 +126,10 @@ __global__ void __launch_bounds__(kStepThreads, 2) scan_step_kernel(StepArgs a)
         }
         if (src >= 0)
             wpub[src] = ct;
-    }
-    // the read's B fragments, [k-step][lane][2] flat, as scan.cu builds them
-    for (int e = ct; e < NB; e += kStepThreads) {
-        const int reg = e & 1, ln = (e >> 1) & 31, ks = e >> 6;
-        const int g = ln >> 2, j = 16 * ks + 2 * (ln & 3) + 8 * reg;
-        const float w0 = sid[W + j] >= 0 ? sw[W + j] : 0.f;
-        const float w1 = sid[W + j + 1] >= 0 ? sw[W + j + 1] : 0.f;
-        bfr[e] = weight_part_bits(w0, g) | (weight_part_bits(w1, g) << 16);
-    }
-    // 2. the read chunks from the bank (own writes and out-of-range ids excepted)
-    const unsigned char* bank =
-        a.banks + ((size_t)b * a.N * a.d + (size_t)rb * a.rb_rows) * sizeof(S);
-    if (ct < W) {
-        const int r = sid[W + ct];
         unsigned char* dst = rbuf + (size_t)ct * kStepRS;
         if (r >= 0 && src < 0) {
             mbar_arrive_expect_tx(smem_u32(bar), cb);
-            bulk_g2s(smem_u32(dst), bank + (size_t)r * a.d * sizeof(S), cb, smem_u32(bar));
+            bulk_g2s(smem_u32(dst), wrow - rg * 16 + (size_t)r * a.d * sizeof(S), cb, smem_u32(bar));
         } else {
             if (r < 0) {
                 for (uint32_t o = 0; o < cb; o += 16)
@@ -146,45 +138,46 @@ __global__ void __launch_bounds__(kStepThreads, 2) scan_step_kernel(StepArgs a)
             mbar_arrive(smem_u32(bar));
         }
     }
-    __syncthreads();   // (wpub complete)
-
-    // 3. u, the new values, the bank stores and the own reads. The write chunks are read
-    // twice -- for u, then again (from L1 or L2) for the new values -- so that no thread
-    // holds all of them while it forms the new ones: nothing writes a chunk before its
-    // thread's second read (each thread stores only its own pieces, after reading them).
-    unsigned char* wrow = a.banks + ((size_t)b * a.N * a.d + (size_t)rb * a.rb_rows) * sizeof(S) + rg * 16;
+    // 3. the write chunks of this thread (read twice -- for u, then again from L1 or L2 for
+    // the new values -- so that no thread holds all of them while it forms the new ones;
+    // nothing writes a chunk before its thread's second read, as each thread stores only its
+    // own pieces, after reading them)
+    uint4 q[SPL];
+#pragma unroll
+    for (int i = 0; i < SPL; ++i) {
+        const int id = sid[i * kSG + sg];
+        q[i] = act && id >= 0 ? ld_u4(wrow + (size_t)id * a.d * sizeof(S)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    // while they load: the read's B fragments, [k-step][lane][2] flat, as scan.cu builds them
+    for (int e = ct; e < NB; e += kStepThreads) {
+        const int reg = e & 1, ln = (e >> 1) & 31, ks = e >> 6;
+        const int g = ln >> 2, j = 16 * ks + 2 * (ln & 3) + 8 * reg;
+        const float w0 = sid[W + j] >= 0 ? sw[W + j] : 0.f;
+        const float w1 = sid[W + j + 1] >= 0 ? sw[W + j + 1] : 0.f;
+        bfr[e] = weight_part_bits(w0, g) | (weight_part_bits(w1, g) << 16);
+    }
     float2 u[HPL];
 #pragma unroll
     for (int h = 0; h < HPL; ++h)
         u[h] = make_float2(0.f, 0.f);
-    {
-        uint4 q[SPL];
 #pragma unroll
-        for (int i = 0; i < SPL; ++i) {
-            const int id = sid[i * kSG + sg];
-            q[i] = act && id >= 0 ? ld_u4(wrow + (size_t)id * a.d * sizeof(S)) : make_uint4(0u, 0u, 0u, 0u);
-        }
+    for (int i = 0; i < SPL; ++i) {
+        const float kw = sw[i * kSG + sg];
+        float2 f[HPL];
+        P::unpack(q[i], f);
 #pragma unroll
-        for (int i = 0; i < SPL; ++i) {
-            const float kw = sw[i * kSG + sg];
-            float2 f[HPL];
-            P::unpack(q[i], f);
-#pragma unroll
-            for (int h = 0; h < HPL; ++h)
-                u[h] = __ffma2_rn(make_float2(kw, kw), f[h], u[h]);
-        }
+        for (int h = 0; h < HPL; ++h)
+            u[h] = __ffma2_rn(make_float2(kw, kw), f[h], u[h]);
     }
     float2 vv[HPL];
-    P::unpack(act ? ld_u4(a.v + ((size_t)b * a.d + (size_t)rb * a.rb_rows) * sizeof(S) + rg * 16)
-                  : make_uint4(0u, 0u, 0u, 0u),
-              vv);
+    P::unpack(vraw, vv);
     const float al = ab[0], be = ab[1];
     const float2 al2 = make_float2(al, al), be2 = make_float2(be, be);
     float2 c[HPL];   // beta (v - alpha u)
 #pragma unroll
     for (int h = 0; h < HPL; ++h)
         c[h] = __fmul2_rn(be2, __ffma2_rn(make_float2(-al, -al), slot_group_sum(u[h]), vv[h]));
-    // M[S_j] <- alpha M[S_j] + k_j beta (v - alpha u), rounded once
+    // M[S_j] <- alpha M[S_j] + k_j beta (v - alpha u), rounded once, to the bank
 #pragma unroll
     for (int i = 0; i < SPL; ++i) {
         const int id = sid[i * kSG + sg];
@@ -194,18 +187,23 @@ __global__ void __launch_bounds__(kStepThreads, 2) scan_step_kernel(StepArgs a)
 #pragma unroll
         for (int h = 0; h < HPL; ++h)
             f[h] = __ffma2_rn(make_float2(kw, kw), c[h], __fmul2_rn(al2, f[h]));
-        const uint4 nv = P::pack(f);
+        q[i] = P::pack(f);
         if (act && id >= 0)
-            __stcg(reinterpret_cast<uint4*>(wrow + (size_t)id * a.d * sizeof(S)), nv);
+            __stcg(reinterpret_cast<uint4*>(wrow + (size_t)id * a.d * sizeof(S)), q[i]);
+    }
+    __syncthreads();   // (wpub complete)
+    // the reads of this token's own writes take the new values
+#pragma unroll
+    for (int i = 0; i < SPL; ++i) {
         const int jr = wpub[i * kSG + sg];
         if (act && jr >= 0)
-            *reinterpret_cast<uint4*>(rbuf + (size_t)jr * kStepRS + rg * 16) = nv;
+            *reinterpret_cast<uint4*>(rbuf + (size_t)jr * kStepRS + rg * 16) = q[i];
     }
     __syncthreads();   // (the own reads are in the read buffer)
+    const bool landed = mbar_wait(smem_u32(bar), 0, nullptr, a.status);
 
     // 4. y = sum_j r_j M[R_j] (post-write): warp w takes rows 32w .. 32w+31 in two 16-row
     // tiles, W / 16 steps of 16 slots, fp32 accumulation
-    const bool landed = mbar_wait(smem_u32(bar), 0, nullptr, a.status);
     if (landed) {
         const int gid = lane >> 2, tig = lane & 3;
         const uint32_t rbase = smem_u32(rbuf) + (uint32_t)(((lane & 7) + 8 * (lane >> 4)) * kStepRS) +
