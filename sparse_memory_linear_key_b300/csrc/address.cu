@@ -470,10 +470,12 @@ __device__ __forceinline__ KthSel group_kth(Group& g, const uint32_t (&key)[NK],
                 list[off + pos[i]] = mine[i];
         grp_sync(g);
         if (g.gw == 0) {
+            // (a fixed trip count, so that the loads are issued together)
             const uint64_t e = lane < m ? list[lane] : ~0ull;
             int rank = 0;
-            for (int j = 0; j < m; ++j)
-                rank += list[j] < e ? 1 : 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                rank += (j < m && list[j] < e) ? 1 : 0;
             const unsigned who = __ballot_sync(0xFFFFFFFFu, lane < m && rank == need - 1);
             const uint64_t pick = __shfl_sync(0xFFFFFFFFu, e, __ffs(who) - 1);
             if (lane == 0)
@@ -526,14 +528,13 @@ __device__ __forceinline__ int grp_compact(Group& g, const bool (&keep)[NK], con
 }
 
 // One query group: the W best of the n scores s[0..n) by (score desc, row asc), sorted,
-// into lv[0..W) / li[0..W), NK scores a thread (rows tid + kGT i). The first bracket is
-// what holds of mean + (z -+ 1/2) sd around the W-th score (the scores of a row are near
-// normal; z is the standard normal quantile of 1 - W/n), checked by one counting pass;
-// group_kth's search is exact either way. out: 64 entries, list: kKList entries of
-// scratch.
-template <int NK>
-__device__ __forceinline__ void group_topw(Group& g, const float* s, int n, int W, float z,
-                                           uint64_t* out, uint64_t* list, float* lv, int* li)
+// into lv[0..W) / li[0..W), NK scores a thread (rows tid + kGT i). The first bracket comes
+// from probes around mean + z sd (the scores of a row are near normal; z is the standard
+// normal quantile of 1 - W/n), checked by one counting pass; group_kth's search is exact
+// either way. out: 64 entries, list: kKList entries of scratch.
+template <int NK, int W>
+__device__ __forceinline__ void group_topw(Group& g, const float* s, int n, float z, uint64_t* out,
+                                           uint64_t* list, float* lv, int* li)
 {
     uint32_t key[NK], id[NK];
     uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
@@ -569,19 +570,25 @@ __device__ __forceinline__ void group_topw(Group& g, const float* s, int n, int 
     uint32_t lo = kmin, hi = kmax + 1u;
     int cnt_lo = n, cnt_hi = 0;
     {
+        // four probes, mean + (z -+ 1/2) sd and mean + (z -+ 1/10) sd: the W-th score lies
+        // within 1/10 sd of mean + z sd more often than not, and then at most about 20
+        // scores lie between the inner two, few enough to rank at once
         const float mean = sum / n;
         const float sd = sqrtf(fmaxf(sum2 / n - mean * mean, 0.f));
-        const uint32_t bl = float_order_bits(mean + (z - 0.5f) * sd);
-        const uint32_t bh = float_order_bits(mean + (z + 0.5f) * sd);
-        int c[2] = {0, 0};
+        uint32_t pb[4];
+        const float off[4] = {-0.5f, -0.1f, 0.1f, 0.5f};
+        int c[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int i = 0; i < NK; ++i) {
-            c[0] += key[i] >= bl ? 1 : 0;
-            c[1] += key[i] >= bh ? 1 : 0;
+        for (int q = 0; q < 4; ++q) {
+            pb[q] = float_order_bits(mean + (z + off[q]) * sd);
+#pragma unroll
+            for (int i = 0; i < NK; ++i)
+                c[q] += key[i] >= pb[q] ? 1 : 0;
         }
-        grp_sum<2>(g, c);
-        kth_narrow(bl, c[0], W, lo, hi, cnt_lo, cnt_hi);
-        kth_narrow(bh, c[1], W, lo, hi, cnt_lo, cnt_hi);
+        grp_sum<4>(g, c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            kth_narrow(pb[q], c[q], W, lo, hi, cnt_lo, cnt_hi);
     }
     const KthSel ks = group_kth<NK>(g, key, id, W, lo, hi, cnt_lo, cnt_hi, list);
     bool keep[NK];
@@ -596,7 +603,7 @@ __device__ __forceinline__ void group_topw(Group& g, const float* s, int n, int 
     if (g.tid < W) {
         const uint64_t e = out[g.tid];
         int place = 0;
-#pragma unroll 8
+#pragma unroll
         for (int j = 0; j < W; ++j)
             place += out[j] < e ? 1 : 0;
         lv[place] = key_score(e);
@@ -608,11 +615,10 @@ __device__ __forceinline__ void group_topw(Group& g, const float* s, int n, int 
 // One query group: select_candidates' merge, NC candidates a thread (candidate tid + kGT i);
 // the softmax normaliser is summed in a fixed order (each warp's butterfly, then the warps
 // in turn). sel: 64 entries, list: kKList entries of scratch.
-template <int NC>
+template <int NC, int W>
 __device__ __forceinline__ void group_merge(Group& g, const float* lv0, const int* li0, const float* lv1,
                                             const int* li1, const unsigned short* pairs, int C, int n,
-                                            int W, uint64_t* sel, uint64_t* list, int32_t* idx,
-                                            float* wsel)
+                                            uint64_t* sel, uint64_t* list, int32_t* idx, float* wsel)
 {
     uint32_t ck[NC], cs[NC];
     float cv[NC];
@@ -670,7 +676,7 @@ __device__ __forceinline__ void group_merge(Group& g, const float* lv0, const in
     if (g.tid < W) {
         const uint64_t e = sel[g.tid];
         int place = 0;
-#pragma unroll 8
+#pragma unroll
         for (int j = 0; j < W; ++j)
             place += sel[j] < e ? 1 : 0;
         idx[place] = (int32_t)(e >> 32);
@@ -828,6 +834,8 @@ __global__ void __launch_bounds__(kSmallThreads) address_small_kernel(
     __shared__ int npairs;
     __shared__ __align__(8) uint64_t kbar;
     const int warp = threadIdx.x >> 5;
+    // the set size, fixed by the candidate count a lane the launch picked
+    constexpr int WC = NC == 9 ? 64 : NC == 4 ? 32 : NC == 2 ? 16 : 8;
     const uint32_t half = cluster_rank_u();
     const int64_t q0 = (int64_t)(blockIdx.x >> 1) * kQG;      // first query of the group
     const int64_t nq = 2 * ntok;
@@ -912,7 +920,7 @@ __global__ void __launch_bounds__(kSmallThreads) address_small_kernel(
     uint64_t* glist = reinterpret_cast<uint64_t*>(sm + L.kl) + grp * kKList;
     constexpr int KPG = KPL >= 4 ? KPL / 4 : 1;      // scores a thread of the group
     if (ok && grp < kQG && q0 + grp < nq)
-        group_topw<KPG>(g, sc + grp * 32 * KPL, n, W, z, gout, glist, lv + grp * 64, li + grp * 64);
+        group_topw<KPG, WC>(g, sc + grp * 32 * KPL, n, z, gout, glist, lv + grp * 64, li + grp * 64);
     __syncthreads();
     cluster_sync_all();
     // 5. block 0 merges each query's halves: group j reads block 1's list of query j
@@ -926,8 +934,8 @@ __global__ void __launch_bounds__(kSmallThreads) address_small_kernel(
         grp_sync(g);
         const int64_t qi = q0 + grp;
         const size_t ob = ((size_t)(qi >> 1) * 2 + (qi & 1)) * W;
-        group_merge<(NC + 3) / 4>(g, lv + grp * 64, li + grp * 64, lv1, li1, pairs, npairs, n, W,
-                                  gout, glist, idx + ob, wsel + ob);
+        group_merge<(NC + 3) / 4, WC>(g, lv + grp * 64, li + grp * 64, lv1, li1, pairs, npairs, n,
+                                      gout, glist, idx + ob, wsel + ob);
     }
     // block 1 stays until block 0 has read its lists
     cluster_sync_all();
