@@ -14,8 +14,8 @@
 //   candidate_select_kernel  orders each half's list, then forms the outer sums of the
 //                          pairs of half-ranks (a, b) with (a+1)(b+1) <= W -- the only
 //                          pairs that can reach the top-W of all n^2 sums -- keeps their
-//                          top-W (warp_kth), takes the softmax, and reports the set in
-//                          ascending slot order.
+//                          top-W (bisection over the sums), takes the softmax, and reports
+//                          the set in ascending slot order.
 #include <algorithm>
 
 #include "sdm_common.cuh"
@@ -115,7 +115,7 @@ __device__ __forceinline__ void build_pairs(unsigned short* pairs, int* npairs, 
     }
 }
 
-// ------------------------------------------------------- exact top-W of a warp
+// ----------------------------------------------- exact top-W: shared pieces
 
 // An element's composite key: ascending = larger order key first, then smaller id.
 __device__ __forceinline__ uint64_t comp_key(uint32_t key, uint32_t id)
@@ -123,7 +123,7 @@ __device__ __forceinline__ uint64_t comp_key(uint32_t key, uint32_t id)
     return ((uint64_t)(~key) << 32) | id;
 }
 
-// Which elements warp_kth keeps: exact ? key >= lo : comp_key(key, id) <= e.
+// Which elements group_kth keeps: exact ? key >= lo : comp_key(key, id) <= e.
 struct KthSel {
     bool exact;
     uint32_t lo;
@@ -145,89 +145,13 @@ __device__ __forceinline__ void kth_narrow(uint32_t p, int c, int W, uint32_t& l
     }
 }
 
-// One warp, NK elements a lane: order keys key[] (0: no element) with distinct ids id[].
-// Finds the W best elements by (key desc, id asc) from a bracket [lo, hi) that holds
-// cnt_lo = #{key >= lo} >= W > cnt_hi = #{key >= hi}. Each round counts three probes:
-// two where a count falling linearly in the score between the ends of the bracket
-// would reach W, 12 elements' worth either side, and the middle of the key range, which
-// at least halves it. It stops when exactly W keys lie at or above lo, or at most 32
-// in the bracket: those are ranked directly, one a lane, and the e above is the
-// (W - cnt_hi)-th of them. Should more than 32 share one key value, the same rank among
-// their ids comes from a bisection over the ids. scratch: 32 entries.
-template <int NK>
-__device__ __forceinline__ KthSel warp_kth(const uint32_t (&key)[NK], const uint32_t (&id)[NK],
-                                           int W, uint32_t lo, uint32_t hi, int cnt_lo,
-                                           int cnt_hi, uint64_t* scratch)
-{
-    const int lane = threadIdx.x & 31;
-    const unsigned below = (1u << lane) - 1u;
-    auto count_ge = [&](uint32_t p) {
-        int c = 0;
-#pragma unroll
-        for (int i = 0; i < NK; ++i)
-            c += key[i] >= p ? 1 : 0;
-        return __reduce_add_sync(0xFFFFFFFFu, c);
-    };
-    for (int round = 0; round < 40 && cnt_lo != W && cnt_lo - cnt_hi > 32 && hi - lo > 1; ++round) {
-        const uint32_t mid = lo + ((hi - lo) >> 1);
-        const float vlo = float_from_order_bits(lo), vhi = float_from_order_bits(hi);
-        const float span = (float)(cnt_lo - cnt_hi);
-        const float f = (float)(cnt_lo - W) / span, dl = 12.0f / span;
-        const uint32_t pa = min(max(float_order_bits(vlo + (vhi - vlo) * (f - dl)), lo + 1), hi - 1);
-        const uint32_t pb = min(max(float_order_bits(vlo + (vhi - vlo) * (f + dl)), lo + 1), hi - 1);
-        const int ca = count_ge(pa), cb = count_ge(pb), cm = count_ge(mid);
-        kth_narrow(pa, ca, W, lo, hi, cnt_lo, cnt_hi);
-        kth_narrow(pb, cb, W, lo, hi, cnt_lo, cnt_hi);
-        kth_narrow(mid, cm, W, lo, hi, cnt_lo, cnt_hi);
-    }
-    KthSel r{cnt_lo == W, lo, 0ull};
-    if (r.exact)
-        return r;
-    const int m = cnt_lo - cnt_hi, need = W - cnt_hi;
-    if (m <= 32) {
-        int at = 0;
-#pragma unroll
-        for (int i = 0; i < NK; ++i) {
-            const bool in = key[i] >= lo && key[i] < hi;
-            const unsigned bal = __ballot_sync(0xFFFFFFFFu, in);
-            if (in)
-                scratch[at + __popc(bal & below)] = comp_key(key[i], id[i]);
-            at += __popc(bal);
-        }
-        __syncwarp();
-        const uint64_t e = lane < m ? scratch[lane] : ~0ull;
-        int rank = 0;
-        for (int j = 0; j < m; ++j)
-            rank += scratch[j] < e ? 1 : 0;
-        const unsigned who = __ballot_sync(0xFFFFFFFFu, lane < m && rank == need - 1);
-        r.e = __shfl_sync(0xFFFFFFFFu, e, __ffs(who) - 1);
-        __syncwarp();
-        return r;
-    }
-    // more than 32 left, all with key lo: the need-th lowest id among them
-    uint32_t ia = 0u, ib = 0xFFFFFFFFu;
-    for (int round = 0; round < 33 && ia < ib; ++round) {
-        const uint32_t md = ia + ((ib - ia) >> 1);
-        int c = 0;
-#pragma unroll
-        for (int i = 0; i < NK; ++i)
-            c += (key[i] == lo && id[i] <= md) ? 1 : 0;
-        c = __reduce_add_sync(0xFFFFFFFFu, c);
-        if (c >= need)
-            ib = md;
-        else
-            ia = md + 1u;
-    }
-    r.e = comp_key(lo, ia);
-    return r;
-}
-
 // One warp: given each half's W best (score, row) sorted by (score desc, row asc) in
 // lv0/li0 and lv1/li1, the W largest outer sums over the candidate pairs by (sum desc,
-// slot asc) (warp_kth, NC candidates a lane), then the softmax over them, and the set in
-// ascending slot order with its weights into idx[0..W) / wsel[0..W). sel: W entries of
-// scratch.
-template <int NC>
+// slot asc) -- a bisection over the order-preserving keys of the sums, NC candidates a
+// lane, stopping once exactly W keys lie at or above the probe, equal sums at the
+// threshold to the lower slot -- then the softmax over them, and the set in ascending
+// slot order with its weights into idx[0..W) / wsel[0..W). sel: W entries of scratch.
+template <int NC, int EW>
 __device__ __forceinline__ void select_candidates(const float* lv0, const int* li0, const float* lv1,
                                                   const int* li1, const unsigned short* pairs, int C,
                                                   int n, int W, uint64_t* sel, int32_t* idx,
@@ -254,46 +178,77 @@ __device__ __forceinline__ void select_candidates(const float* lv0, const int* l
     }
     kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
     kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
-    const KthSel ks = warp_kth<NC>(ck, cs, W, kmin, kmax + 1u, C, 0, sel);
+    uint32_t lo = kmin, hi = kmax + 1;
+    int cnt_hi = 0;
+    bool exact = false;
+    while (!exact && hi - lo > 1) {
+        const uint32_t mid = lo + ((hi - lo) >> 1);
+        int c = 0;
+#pragma unroll
+        for (int i = 0; i < NC; ++i)
+            c += ck[i] >= mid ? 1 : 0;
+        c = __reduce_add_sync(0xFFFFFFFFu, c);
+        if (c == W) {
+            lo = mid;
+            exact = true;
+        } else if (c > W) {
+            lo = mid;
+        } else {
+            hi = mid;
+            cnt_hi = c;
+        }
+    }
+    bool keep[NC];
+#pragma unroll
+    for (int i = 0; i < NC; ++i)
+        keep[i] = exact ? ck[i] >= lo : ck[i] >= hi;
+    for (int need = exact ? 0 : W - cnt_hi; need > 0; --need) {
+        // the lowest slot among the equal sums not yet kept
+        uint32_t best = 0xFFFFFFFFu;
+#pragma unroll
+        for (int i = 0; i < NC; ++i)
+            if (!keep[i] && ck[i] == lo)
+                best = min(best, cs[i]);
+        best = __reduce_min_sync(0xFFFFFFFFu, best);
+#pragma unroll
+        for (int i = 0; i < NC; ++i)
+            if (!keep[i] && ck[i] == lo && cs[i] == best)
+                keep[i] = true;
+    }
     // softmax over the kept sums (the largest one is the largest of all)
     const float mx = float_from_order_bits(kmax);
-    bool keep[NC];
-    float ev[NC];
     float part = 0.0f;
 #pragma unroll
-    for (int i = 0; i < NC; ++i) {
-        keep[i] = ck[i] != 0u && (ks.exact ? ck[i] >= ks.lo : comp_key(ck[i], cs[i]) <= ks.e);
-        ev[i] = keep[i] ? expf(cv[i] - mx) : 0.0f;
-        part += ev[i];
-    }
+    for (int i = 0; i < NC; ++i)
+        part += keep[i] ? expf(cv[i] - mx) : 0.0f;
     part = __reduce_add_sync_f(part);
-    int at = 0;
+    int base_pos = 0;
 #pragma unroll
     for (int i = 0; i < NC; ++i) {
         const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep[i]);
-        if (keep[i])
-            sel[at + __popc(bal & ((1u << lane) - 1u))] =
-                ((uint64_t)cs[i] << 32) | __float_as_uint(ev[i] / part);
-        at += __popc(bal);
+        if (keep[i]) {
+            const int pos = base_pos + __popc(bal & ((1u << lane) - 1u));
+            sel[pos] = ((uint64_t)cs[i] << 32) | __float_as_uint(expf(cv[i] - mx) / part);
+        }
+        base_pos += __popc(bal);
     }
     __syncwarp();
-    // the set in ascending slot order, weights alongside
-    uint64_t k2[2];
+    // report the set in ascending slot order, weights alongside
+    uint64_t k2[EW];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int e = lane * 2 + i;
-        k2[i] = e < W ? sel[e] : ~0ull;
+    for (int i = 0; i < EW; ++i) {
+        const int e = lane * EW + i;
+        k2[i] = (e < W) ? sel[e] : ~0ull;
     }
-    warp_bitonic_sort<2>(k2);
+    warp_bitonic_sort<EW>(k2);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int e = lane * 2 + i;
+    for (int i = 0; i < EW; ++i) {
+        const int e = lane * EW + i;
         if (e < W) {
             idx[e] = (int32_t)(k2[i] >> 32);
             wsel[e] = __uint_as_float((uint32_t)k2[i]);
         }
     }
-    __syncwarp();
 }
 
 // One warp per (token, kind). Candidate pairs (a, b) of half-ranks come from a table
@@ -339,8 +294,8 @@ __global__ void __launch_bounds__(256) candidate_select_kernel(
         }
         __syncwarp();
         const size_t ob = ((size_t)tok * 2 + kind) * W;
-        select_candidates<NC>(lv[warp][0], li[warp][0], lv[warp][1], li[warp][1], pairs, C, n,
-                                    W, sel[warp], idx + ob, wsel + ob);
+        select_candidates<NC, 2>(lv[warp][0], li[warp][0], lv[warp][1], li[warp][1], pairs, C, n,
+                                 W, sel[warp], idx + ob, wsel + ob);
     }
 }
 
@@ -416,8 +371,16 @@ __device__ __forceinline__ int grp_offset(Group& g, int c, int& total)
     return off;
 }
 
-// warp_kth for a group: NK elements a thread, counts summed over the group; the bracket's
-// last elements gathered in list (kKList entries) and ranked by the group's first warp.
+// Exact top-W for a query group of kGW warps, NK elements a thread: order keys key[] (0: no
+// element) with distinct ids id[]. Finds the W best elements by (key desc, id asc) from a
+// bracket [lo, hi) that holds cnt_lo = #{key >= lo} >= W > cnt_hi = #{key >= hi}. Each
+// round counts three probes over the group (one exchange): two where a count falling
+// linearly in the score between the ends of the bracket would reach W, 12 elements'
+// worth either side, and the middle of the key range, which at least halves it. It stops
+// when exactly W keys lie at or above lo, or at most 32 in the bracket: those are gathered
+// in list (kKList entries, warps in turn) and ranked by the group's first warp, and the
+// e of the result is the (W - cnt_hi)-th of them. Should more than 32 share one key value,
+// the same rank among their ids comes from a bisection over the ids.
 template <int NK>
 __device__ __forceinline__ KthSel group_kth(Group& g, const uint32_t (&key)[NK],
                                             const uint32_t (&id)[NK], int W, uint32_t lo,
