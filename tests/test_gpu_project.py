@@ -1,9 +1,11 @@
 """The projections (row a1: "Write & Read", the token embedding is projected to write keys
 and, separately, to read queries) on the hand-written GEMM, against the oracle's fp64
 products rounded once, at the widths of the pages' layers (d = 2048 and 3840, key width
-256) and token counts that take every path of the kernel: the persistent whole-K kernel
-(many tokens) and the split-K clusters of 2, 4 and 8 CTAs (few tokens), full and ragged
-128-token tiles, a single token."""
+256) and token counts that take every path of the kernel: 256-column tiles over the
+whole K (many tokens), 64-column tiles split along K over CTA pairs (few tokens: d = 2048
+with 1 to 127 tokens, d = 3840 and d = 1280 with 64 and 96), 64-column tiles over the
+whole K (129 and 300 tokens; a one-block K at d = 64), full and ragged 128-token tiles,
+x copies of fewer rows than a tile, a single token."""
 import numpy as np
 import pytest
 import torch
