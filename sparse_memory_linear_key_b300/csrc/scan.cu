@@ -593,10 +593,10 @@ __device__ void role_clear(const ScanArgs& a, const Meta* meta, uint64_t* bars)
 
 // ------------------------------------------------------------ M: progress marks
 
-// Raises each item's flag: to 1 as soon as its bank chunks have landed, to 2 once the
-// consumers have written its ring entries, to 3 once they have stored its new slot
-// values (the consumers' arrival, release at CTA scope, followed by this release at GPU
-// scope publishes their global writes). The three marks advance independently: the
+// Raises each item's flag: to 1 as soon as its bank chunks have landed and to 3 once the
+// consumers have stored its new slot values (the consumers' arrival, release at CTA
+// scope, followed by this release at GPU scope publishes their global writes); the
+// consumers raise it to 2 themselves once they have written its ring entries. The three marks advance independently: the
 // warp polls whichever is next for each and never blocks one behind another (a later
 // item's bank loads may wait on other tokens' commits, this item's among them). With one
 // token a sequence no item waits on another's flag, and the marks are only the CTA's own
@@ -633,10 +633,7 @@ __device__ void role_marks(const ScanArgs& a, const Meta* meta, uint64_t* bars)
             }
         }
         if (kp < kl && uniform_test(smem_u32(bars + kFwdw + (kp & 1)), (kp >> 1) & 1)) {
-            const Meta& m = meta[kp & 1];
-            if (lane == 0 && a.T > 1)
-                red_max_release_gpu(item_flag(a, m.b, m.rb, m.t), 2);  // ring entries visible
-            ++kp;
+            ++kp;                  // (the consumers published the ring entries: flag 2)
             progress = true;
         }
         if (kc < kp && uniform_test(smem_u32(bars + kStored + (kc & 1)), (kc >> 1) & 1)) {
@@ -681,7 +678,8 @@ __device__ void role_marks(const ScanArgs& a, const Meta* meta, uint64_t* bars)
 
 template <typename S, int W>
 __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned char* rbuf,
-                              const Meta* meta, uint64_t* bars, float* ybuf, uint32_t* bfr)
+                              const Meta* meta, uint64_t* bars, float* ybuf, uint32_t* bfr,
+                              int* fwdcnt)
 {
     constexpr int SPL = W / kSG;       // slots of each set per thread: i*8 + sg
     constexpr bool kMmaY = ScanShape<S, W>::kMmaY;
@@ -932,8 +930,23 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
                     __stcg(reinterpret_cast<uint4*>(re + (size_t)(i * kSG + sg) * a.chunk_bytes), Mv[i]);
         }
         __syncwarp();
-        if (lane == 0)
+        if (lane == 0) {
+            // The last consumer warp done with the item's ring entries publishes them at
+            // GPU scope itself (flag 2), one polling step sooner than the marks warp would:
+            // each warp's arrival is a release at CTA scope, the last one's an acquire,
+            // and its release at GPU scope carries the others' stores along. (With one
+            // token a sequence nothing reads the flags.)
+            if (a.T > 1) {
+                int old;
+                asm volatile("atom.acq_rel.cta.shared::cta.add.s32 %0, [%1], 1;"
+                             : "=r"(old)
+                             : "r"(smem_u32(fwdcnt + p))
+                             : "memory");
+                if (old % kCWarps == kCWarps - 1)
+                    red_max_release_gpu(item_flag(a, m.b, m.rb, m.t), 2);
+            }
             mbar_arrive(smem_u32(bars + kFwdw + p));
+        }
         if constexpr (kMmaY) {
             // reads of slots this token writes: the new values go into the read buffer at
             // their read positions (rows of this warp's row groups only)
@@ -1086,6 +1099,7 @@ template <typename S, int W>
 __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a)
 {
     extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ int fwdcnt[2];      // consumer warps done with an item's ring entries
     unsigned char* wbuf = smem;
     constexpr int RS = ScanShape<S, W>::kRStride;
     unsigned char* rbuf = smem + (size_t)W * kStride;
@@ -1107,6 +1121,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a)
             mbar_init(smem_u32(bars + kStored + p), kCWarps);
         }
         mbar_init(smem_u32(bars + kCbar), kCWarps);
+        fwdcnt[0] = fwdcnt[1] = 0;
         mbar_init(smem_u32(bars + kLmark), 1);
         fence_mbarrier_init();
     }
@@ -1126,7 +1141,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a)
     // warpgroup (warps 16..19) gives back down to 64 (128 x 64 = 8,192): 61,440 in all.
     if (warp < kCWarps) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kConsumerRegs) : "memory");
-        role_consumer<S, W>(a, wbuf, rbuf, meta, bars, ybuf, bfr);
+        role_consumer<S, W>(a, wbuf, rbuf, meta, bars, ybuf, bfr, fwdcnt);
         return;
     }
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRoleRegs) : "memory");

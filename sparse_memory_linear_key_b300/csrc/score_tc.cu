@@ -15,7 +15,8 @@
 //    each score in TMEM by its
 //    order-preserving integer image (tcgen05.st) and sums the row's scores and squares;
 //    a bracket around mean + z sd (the scores of a row are near normal; z is the normal
-//    quantile of 1 - W/n) is checked in one counting pass, and a bisection over the keys
+//    quantile of 1 - W/n; four probes, the inner two 1/10 sd either side) is checked in
+//    one counting pass, and a bisection over the keys
 //    inside what holds of the bracket (the whole range otherwise) finds the W-th
 //    largest, stopping early once exactly W keys lie at or above the probe; a last pass
 //    writes the kept (score, row) pairs, ties at the threshold by ascending row.
@@ -381,55 +382,54 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
                 sum += xs[xq + h * 32];
                 sum2 += xs2[xq + h * 32];
             }
-            // bracket the W-th largest score around mean + z sd (scores are near normal);
-            // one counting pass checks it, and the bisection starts from whatever of the
-            // bracket holds: at least W keys lie at or above lo, fewer than W at or above hi
+            // bracket the W-th largest score around mean + z sd (scores are near normal):
+            // one counting pass checks four probes, mean + (z -+ 1/2) sd and mean + (z -+
+            // 1/10) sd (the W-th score lies within 1/10 sd of mean + z sd more often than
+            // not), and the bisection starts from whatever of them holds: at least W keys
+            // lie at or above lo, fewer than W at or above hi
             const float mean = sum / a.n;
             const float sd = sqrtf(fmaxf(sum2 / a.n - mean * mean, 0.f));
-            const uint32_t bl = order_key(__float_as_uint(mean + (a.z - 0.5f) * sd));
-            const uint32_t bh = order_key(__float_as_uint(mean + (a.z + 0.5f) * sd));
+            const float off[4] = {-0.5f, -0.1f, 0.1f, 0.5f};
+            uint32_t pb[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                pb[q] = order_key(__float_as_uint(mean + (a.z + off[q]) * sd));
             uint32_t lo = kmin, hi = kmax + 1;
             int cnt_hi = 0;
             bool exact = false;
             {
-                int cl = 0, ch = 0;
+                // counts of the four probes in xb1, xb2, xa, xt (the last two are the
+                // emission's, free until then)
+                int* xp[4] = {xb1, xb2, xa, xt};
+                int cp[4] = {0, 0, 0, 0};
                 for (int c0 = cb; c0 < ce; c0 += 32) {
                     tmem_ld32(trow + c0, v);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        cl += v[j] >= bl ? 1 : 0;
-                        ch += v[j] >= bh ? 1 : 0;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            cp[q] += v[j] >= pb[q] ? 1 : 0;
                     }
                 }
-                xb1[xi] = cl;
-                xb2[xi] = ch;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    xp[q][xi] = cp[q];
                 bar_sync(bid, bn);
-                cl = 0;
-                ch = 0;
-                for (int h = 0; h < G; ++h) {
-                    cl += xb1[xq + h * 32];
-                    ch += xb2[xq + h * 32];
-                }
-                if (bl > lo && bl < hi) {
-                    if (cl == W) {
-                        lo = bl;
-                        exact = true;
-                    } else if (cl > W) {
-                        lo = bl;
-                    } else {
-                        hi = bl;
-                        cnt_hi = cl;
-                    }
-                }
-                if (!exact && bh > lo && bh < hi) {
-                    if (ch == W) {
-                        lo = bh;
-                        exact = true;
-                    } else if (ch > W) {
-                        lo = bh;
-                    } else {
-                        hi = bh;
-                        cnt_hi = ch;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    int c = 0;
+                    for (int h = 0; h < G; ++h)
+                        c += xp[q][xq + h * 32];
+                    if (!exact && pb[q] > lo && pb[q] < hi) {
+                        if (c == W) {
+                            lo = pb[q];
+                            exact = true;
+                        } else if (c > W) {
+                            lo = pb[q];
+                        } else {
+                            hi = pb[q];
+                            cnt_hi = c;
+                        }
                     }
                 }
             }
