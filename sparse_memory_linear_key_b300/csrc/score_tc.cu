@@ -44,6 +44,16 @@ constexpr int kEpiWarps = 16;             // four per TMEM lane quadrant, one co
 constexpr int kThreads = 32 * (2 + kEpiWarps);  // warp 0 TMA, warp 1 MMA, then the epilogue
 constexpr uint32_t kBBytes = kBRows * 128 * 2;        // two K atoms of 512 rows
 constexpr uint32_t kABytes = kTileM * 128 * 2;        // two K atoms of 128 rows
+// Top-W epilogue: probes a counting pass, their places around the expected W-th score in
+// rows (multiples of dz), and the capacity of a row's list of the scores inside its final
+// bracket (odd: the rows of a warp hit different banks)
+constexpr int kProbes = 6;
+constexpr int kLCap = 37;
+__constant__ float kProbeAt[kProbes] = {-35.f, -15.f, -7.f, 7.f, 15.f, 35.f};
+// exchange area after the barriers and the TMEM address: the bracket lists [128][kLCap]
+// (the row statistics of the first pass alias their start), probe counts [2][kProbes][512]
+// (the emission counts alias the first two), list sizes [512], W-th scores [128]
+constexpr uint32_t kXBytes = 128 * kLCap * 4 + 2 * kProbes * 512 * 2 + 512 * 2 + 128 * 4;
 
 struct ScoreArgs {
     int ntok, n, khalf, W, tiles_per_kind, ctas_per_half;
@@ -51,6 +61,7 @@ struct ScoreArgs {
                            // TMEM lane quadrants, so all 16 epilogue warps share its rows
     int qrows;             // queries a tile: 128 / rep
     float z;               // standard normal quantile of 1 - W/n (bracket of the W-th score)
+    float dz;              // 1 / (n phi(z)): standard deviations a score a row apart near z
     float* hv;
     int32_t* hi;
     int* status;
@@ -189,16 +200,17 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
     uint64_t* bars = reinterpret_cast<uint64_t*>(sp + kBBytes + 2 * kABytes);
     // bars: 0 B loaded, 1..2 A stage full, 3..4 A stage empty, 5 TMEM full, 6 TMEM empty
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
-    // exchange between the four epilogue warps of a quadrant: [quadrant][group][lane]
-    uint32_t* xmin = tmem_slot + 4;                  // 512 each
-    uint32_t* xmax = xmin + 512;
-    int* xcnt = reinterpret_cast<int*>(xmax + 512);  // [2 parities][512]
-    int* xa = xcnt + 1024;
-    int* xt = xa + 512;
-    float* xs = reinterpret_cast<float*>(xt + 512);   // [512] row sums, then [512] squares
-    float* xs2 = xs + 512;
-    int* xb1 = reinterpret_cast<int*>(xs2 + 512);      // bracket counts
-    int* xb2 = xb1 + 512;
+    // exchange between the epilogue warps sharing rows; per-thread slots [quadrant][group][lane]
+    float* xl = reinterpret_cast<float*>(tmem_slot + 4);   // [row slot][kLCap] bracket lists
+    float* xfmin = xl;                                     // [512] each: row minimum, maximum,
+    float* xfmax = xl + 512;                               // sum and sum of squares (first pass)
+    float* xs = xl + 1024;
+    float* xs2 = xl + 1536;
+    unsigned short* xpb = reinterpret_cast<unsigned short*>(xl + 128 * kLCap);  // [2][kProbes][512]
+    unsigned short* xa = xpb;                              // [512] emission counts: kept, ties
+    unsigned short* xt = xpb + 512;
+    unsigned short* xln = xpb + 2 * kProbes * 512;         // [512] list entries a thread
+    float* xtr = reinterpret_cast<float*>(xln + 512);      // [row slot] W-th score
     __shared__ int dead;                 // a role gave up: the others stop at their next wait
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -348,140 +360,192 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
             const int kind = tl / a.tiles_per_kind;
             const int tok = (tl % a.tiles_per_kind) * a.qrows + (a.rep == 1 ? q * 32 : 0) + lane;
             uint32_t v[32];
-            // keys in place of the scores (0 in padding columns), their range, and the
-            // row's mean and spread
-            uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-            float sum = 0.f, sum2 = 0.f;
+            const int nv_own = max(0, min(ce, a.n) - cb);          // valid columns here
+            // the row's range, mean and spread
+            float fmn = INFINITY, fmx = -INFINITY, sum = 0.f, sum2 = 0.f;
             for (int c0 = cb; c0 < ce; c0 += 32) {
                 tmem_ld32(trow + c0, v);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const bool valid = c0 + j < a.n;
-                    const float f = __uint_as_float(v[j]);
-                    const uint32_t k = valid ? order_key(v[j]) : 0u;
-                    if (valid) {
-                        kmin = min(kmin, k);
-                        kmax = max(kmax, k);
+                    if (c0 + j < a.n) {
+                        const float f = __uint_as_float(v[j]);
+                        fmn = fminf(fmn, f);
+                        fmx = fmaxf(fmx, f);
                         sum += f;
                         sum2 = fmaf(f, f, sum2);
                     }
-                    v[j] = k;
                 }
-                tmem_st32(trow + c0, v);
             }
-            xmin[xi] = kmin;
-            xmax[xi] = kmax;
+            xfmin[xi] = fmn;
+            xfmax[xi] = fmx;
             xs[xi] = sum;
             xs2[xi] = sum2;
             bar_sync(bid, bn);
             sum = 0.f;
             sum2 = 0.f;
             for (int h = 0; h < G; ++h) {
-                kmin = min(kmin, xmin[xq + h * 32]);
-                kmax = max(kmax, xmax[xq + h * 32]);
+                fmn = fminf(fmn, xfmin[xq + h * 32]);
+                fmx = fmaxf(fmx, xfmax[xq + h * 32]);
                 sum += xs[xq + h * 32];
                 sum2 += xs2[xq + h * 32];
             }
-            // bracket the W-th largest score around mean + z sd (scores are near normal):
-            // one counting pass checks four probes, mean + (z -+ 1/2) sd and mean + (z -+
-            // 1/10) sd (the W-th score lies within 1/10 sd of mean + z sd more often than
-            // not), and the bisection starts from whatever of them holds: at least W keys
-            // lie at or above lo, fewer than W at or above hi
-            const float mean = sum / a.n;
-            const float sd = sqrtf(fmaxf(sum2 / a.n - mean * mean, 0.f));
-            const float off[4] = {-0.5f, -0.1f, 0.1f, 0.5f};
-            uint32_t pb[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                pb[q] = order_key(__float_as_uint(mean + (a.z + off[q]) * sd));
-            uint32_t lo = kmin, hi = kmax + 1;
-            int cnt_hi = 0;
+            // Bracket [lo, hi) of the W-th largest score: c_lo >= W scores lie at or above
+            // lo (o_lo of them in this thread's columns), c_hi < W at or above hi (o_hi);
+            // exact: exactly W at or above lo. Counting passes narrow it with kProbes probes
+            // each: the first around mean + z sd (scores of a row are near normal), later
+            // ones around the interpolated place of the W-th score inside the bracket, one
+            // of them the midpoint of the bracket's order keys, which at least halves it.
+            // The passes end once every row of the warp's rows has exactly W, a bracket of
+            // one value, or at most kLCap scores inside its bracket.
+            float lo = fmn, hi = INFINITY;
+            int c_lo = a.n, c_hi = 0, o_lo = nv_own, o_hi = 0;
             bool exact = false;
+            float pr[kProbes];
             {
-                // counts of the four probes in xb1, xb2, xa, xt (the last two are the
-                // emission's, free until then)
-                int* xp[4] = {xb1, xb2, xa, xt};
-                int cp[4] = {0, 0, 0, 0};
+                const float mean = sum / a.n;
+                const float sd = sqrtf(fmaxf(sum2 / a.n - mean * mean, 0.f));
+#pragma unroll
+                for (int k = 0; k < kProbes; ++k)
+                    pr[k] = mean + (a.z + a.dz * kProbeAt[k]) * sd;
+            }
+            for (int pass = 0;; ++pass) {
+                unsigned short* xp = xpb + (pass & 1) * kProbes * 512;
+                int cp[kProbes];
+#pragma unroll
+                for (int k = 0; k < kProbes; ++k)
+                    cp[k] = 0;
                 for (int c0 = cb; c0 < ce; c0 += 32) {
                     tmem_ld32(trow + c0, v);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
+                        const float f = c0 + j < a.n ? __uint_as_float(v[j]) : -INFINITY;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            cp[q] += v[j] >= pb[q] ? 1 : 0;
+                        for (int k = 0; k < kProbes; ++k)
+                            cp[k] += f >= pr[k] ? 1 : 0;
                     }
                 }
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    xp[q][xi] = cp[q];
+                for (int k = 0; k < kProbes; ++k)
+                    xp[k * 512 + xi] = (unsigned short)cp[k];
                 bar_sync(bid, bn);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int k = 0; k < kProbes; ++k) {
                     int c = 0;
                     for (int h = 0; h < G; ++h)
-                        c += xp[q][xq + h * 32];
-                    if (!exact && pb[q] > lo && pb[q] < hi) {
-                        if (c == W) {
-                            lo = pb[q];
-                            exact = true;
-                        } else if (c > W) {
-                            lo = pb[q];
+                        c += xp[k * 512 + xq + h * 32];
+                    if (!exact && pr[k] > lo && pr[k] < hi) {
+                        if (c >= W) {
+                            lo = pr[k];
+                            c_lo = c;
+                            o_lo = cp[k];
+                            exact = c == W;
                         } else {
-                            hi = pb[q];
-                            cnt_hi = c;
+                            hi = pr[k];
+                            c_hi = c;
+                            o_hi = cp[k];
                         }
                     }
                 }
+                const uint32_t klo = order_key(__float_as_uint(lo));
+                const uint32_t khi = hi < INFINITY ? order_key(__float_as_uint(hi))
+                                                   : order_key(__float_as_uint(fmx)) + 1u;
+                const bool over = !exact && khi - klo > 1u && c_lo - c_hi > kLCap;
+                // (the same rows in every warp at this barrier: all leave together)
+                if (!__any_sync(0xFFFFFFFFu, over))
+                    break;
+                const float top = hi < INFINITY ? hi : fmx;
+                const float step = (top - lo) / (float)(c_lo - c_hi);
+                const float est = top - step * ((float)(W - c_hi) - 0.5f);
+                pr[0] = key_to_score(klo + ((khi - klo) >> 1));
+#pragma unroll
+                for (int k = 1; k < kProbes; ++k)
+                    pr[k] = est + step * (0.25f * kProbeAt[k]);
             }
-            for (int it = 1; __any_sync(0xFFFFFFFFu, !exact && hi - lo > 1); ++it) {
-                const bool active = !exact && hi - lo > 1;
-                const uint32_t mid = lo + ((hi - lo) >> 1);
-                int cnt = 0;
+            // The W-th largest score t. Keep: ex ? scores >= t : scores > t, and then the
+            // lowest-numbered rows among the scores equal to t up to W in all (ties are
+            // taken in column order, so a group takes ties only after lower columns' groups).
+            const uint32_t klo = order_key(__float_as_uint(lo));
+            const uint32_t khi = hi < INFINITY ? order_key(__float_as_uint(hi))
+                                               : order_key(__float_as_uint(fmx)) + 1u;
+            const bool listed = !exact && khi - klo > 1u;   // rank inside the bracket's list
+            const int m = c_lo - c_hi;
+            xln[xi] = (unsigned short)(listed ? o_lo - o_hi : 0);
+            bar_sync(bid, bn);
+            int off = 0;
+            for (int h = 0; h < g; ++h)
+                off += xln[xq + h * 32];
+            const int rslot = xs0 * 32 + lane;
+            float* L = xl + (size_t)rslot * kLCap;
+            const int own_end = off + (listed ? o_lo - o_hi : 0);
+            if (__any_sync(0xFFFFFFFFu, listed)) {
+                // this group's scores inside the bracket, in column order
+                int e = off;
                 for (int c0 = cb; c0 < ce; c0 += 32) {
                     tmem_ld32(trow + c0, v);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        cnt += v[j] >= mid ? 1 : 0;
-                }
-                int* xc = xcnt + (it & 1) * 512;
-                xc[xi] = cnt;
-                bar_sync(bid, bn);
-                cnt = 0;
-                for (int h = 0; h < G; ++h)
-                    cnt += xc[xq + h * 32];
-                if (active) {
-                    if (cnt == W) {
-                        lo = mid;
-                        exact = true;
-                    } else if (cnt > W) {
-                        lo = mid;
-                    } else {
-                        hi = mid;
-                        cnt_hi = cnt;
+                    for (int j = 0; j < 32; ++j) {
+                        const float f = c0 + j < a.n ? __uint_as_float(v[j]) : -INFINITY;
+                        if (listed && f >= lo && f < hi && e < own_end)
+                            L[e++] = f;
                     }
                 }
             }
-            // keep: keys >= lo when exactly W lie there, else keys >= hi and the
-            // lowest-numbered rows among those equal to lo (taken in column order, so a
-            // group takes ties only after the groups of lower columns)
-            const int need = exact ? 0 : W - cnt_hi;
-            int ka = 0, kt = 0;
-            for (int c0 = cb; c0 < ce; c0 += 32) {
-                tmem_ld32(trow + c0, v);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    ka += (exact ? v[j] >= lo : v[j] >= hi) ? 1 : 0;
-                    kt += (!exact && v[j] == lo) ? 1 : 0;
+            bar_sync(bid, bn);
+            const int need_b = W - c_hi;    // scores to take from inside the bracket
+            if (listed) {
+                // t is the listed score with fewer than need_b listed above it and at
+                // least need_b at or above it
+                for (int e = off; e < own_end; ++e) {
+                    const float x = L[e];
+                    int gt = 0, ge = 0;
+                    for (int e2 = 0; e2 < m; ++e2) {
+                        const float y = L[e2];
+                        gt += y > x ? 1 : 0;
+                        ge += y >= x ? 1 : 0;
+                    }
+                    if (gt < need_b && need_b <= ge)
+                        xtr[rslot] = x;
                 }
             }
-            xa[xi] = ka;
-            xt[xi] = kt;
+            bar_sync(bid, bn);
+            float t = lo;
+            bool ex = exact;
+            int ka, kt, cnt_above;
+            if (exact) {
+                ka = o_lo;
+                kt = 0;
+                cnt_above = W;
+            } else if (!listed) {
+                // one value in [lo, hi): scores above lo are those at or above hi
+                ka = o_hi;
+                kt = o_lo - o_hi;
+                cnt_above = c_hi;
+            } else {
+                t = xtr[rslot];
+                int gt = 0, ge = 0, og = 0, oe = 0;
+                for (int e2 = 0; e2 < m; ++e2) {
+                    const float y = L[e2];
+                    gt += y > t ? 1 : 0;
+                    ge += y >= t ? 1 : 0;
+                }
+                for (int e = off; e < own_end; ++e) {
+                    og += L[e] > t ? 1 : 0;
+                    oe += L[e] == t ? 1 : 0;
+                }
+                ex = c_hi + ge == W;
+                ka = o_hi + (ex ? og + oe : og);
+                kt = ex ? 0 : oe;
+                cnt_above = c_hi + gt;
+            }
+            xa[xi] = (unsigned short)ka;
+            xt[xi] = (unsigned short)kt;
             bar_sync(bid, bn);
             int pre_a = 0, pre_t = 0;
             for (int h = 0; h < g; ++h) {
                 pre_a += xa[xq + h * 32];
                 pre_t += xt[xq + h * 32];
             }
+            const int need = ex ? 0 : W - cnt_above;
             int pos = pre_a + min(pre_t, need);
             const int allow = max(0, min(kt, need - pre_t));
             int ties = 0;
@@ -491,14 +555,15 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
                 tmem_ld32(trow + c0, v);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const uint32_t k = v[j];
-                    bool keep = exact ? k >= lo : k >= hi;
-                    if (!keep && !exact && k == lo && ties < allow) {
+                    const bool valid = c0 + j < a.n;
+                    const float f = __uint_as_float(v[j]);
+                    bool keep = valid && (ex ? f >= t : f > t);
+                    if (!keep && valid && !ex && f == t && ties < allow) {
                         keep = true;
                         ++ties;
                     }
                     if (keep && row_ok && pos < W) {
-                        a.hv[ob + pos] = key_to_score(k);
+                        a.hv[ob + pos] = f + 0.0f;   // (-0 as +0)
                         a.hi[ob + pos] = c0 + j;
                         ++pos;
                     }
@@ -603,6 +668,7 @@ cudaError_t launch_score_tc(const sdm_cfg& c, const void* K1, const void* K2, co
     a.khalf = h;
     a.W = c.w;
     a.z = normal_upper_quantile((double)c.w / c.n_sub);
+    a.dz = (float)(1.0 / (c.n_sub * std::exp(-0.5 * (double)a.z * a.z) / std::sqrt(2.0 * M_PI)));
     a.rep = rep_;
     a.qrows = qrows;
     a.tiles_per_kind = (int)((ntok + qrows - 1) / qrows);
@@ -615,7 +681,7 @@ cudaError_t launch_score_tc(const sdm_cfg& c, const void* K1, const void* K2, co
     a.hv = hv;
     a.hi = hi;
     a.status = status;
-    const size_t smem = 1024 + kBBytes + 2 * kABytes + 8 * sizeof(uint64_t) + 16 + 4 * 5632;
+    const size_t smem = 1024 + kBBytes + 2 * kABytes + 8 * sizeof(uint64_t) + 16 + kXBytes;
     cudaError_t e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess)

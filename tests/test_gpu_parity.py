@@ -138,6 +138,41 @@ def test_address_tile_modes_agree():
     assert sdm.read_status(st) == 0
 
 
+@pytest.mark.parametrize("ntok", [200, 600, 2600])
+def test_address_exact_ties(ntok):
+    """Scores with exact ties everywhere: sub-keys and queries with entries in {-1, 0, 1},
+    so every half score and every combined score is a small integer, the same in fp32 and
+    fp64. The selection has no near-ties to excuse here, so the slot sets must equal the
+    oracle's exactly: per half, equal scores go to the lower row, and among the combined
+    scores, equal sums to the lower slot (the pages' top-k over the outer sum, read with
+    that order). One query in eight is all zero (every score equal). 2,600 tokens take
+    the tensor-core scorer's tiles of 128 queries, 600 tokens its replicated tiles of 32,
+    200 tokens the few-token kernel."""
+    n, dk, W = 480, 256, 64
+    cfg = sdm.make_cfg(64, n, dk, W, "bf16")
+    g = torch.Generator().manual_seed(17)
+
+    def tern(*shape):
+        return (torch.randint(0, 3, shape, generator=g) - 1).to(torch.bfloat16)
+
+    K1, K2 = tern(n, dk // 2), tern(n, dk // 2)
+    q_w, q_r = tern(ntok, dk), tern(ntok, dk)
+    q_w[::8] = 0
+    q_r[3::8] = 0
+    idx = torch.empty(ntok, 2, W, dtype=torch.int32, device="cuda")
+    w = torch.empty(ntok, 2, W, device="cuda")
+    ws = sdm.alloc_workspace(sdm.address_workspace_bytes(cfg, ntok))
+    st = sdm.new_status()
+    sdm.sdm_address(cfg, K1.cuda(), K2.cuda(), q_w.cuda(), q_r.cuda(), idx, w, ws, st)
+    torch.cuda.synchronize()
+    assert sdm.read_status(st) == 0
+    got = idx.cpu().numpy()
+    for kind, q in ((0, q_w), (1, q_r)):
+        S, _, _, _ = oracle.address(q, K1, K2, W)
+        bad = np.nonzero(np.any(np.sort(got[:, kind], axis=1) != np.sort(S, axis=1), axis=1))[0]
+        assert len(bad) == 0, (kind, bad[:5])
+
+
 @pytest.mark.parametrize("ntok", [1, 7, 64, 256])
 @pytest.mark.parametrize("shape", ["n480-w64", "w-eq-n", "ragged-f32-w8", "n96-w16"])
 def test_address_few_tokens(ntok, shape):
