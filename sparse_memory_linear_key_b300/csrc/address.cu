@@ -151,6 +151,9 @@ __device__ __forceinline__ void kth_narrow(uint32_t p, int c, int W, uint32_t& l
 // lane, stopping once exactly W keys lie at or above the probe, equal sums at the
 // threshold to the lower slot -- then the softmax over them, and the set in ascending
 // slot order with its weights into idx[0..W) / wsel[0..W). sel: W entries of scratch.
+// The bisection starts at a sum the W-th largest cannot be below: for ranks a, b with
+// (a+1)(b+1) >= W, the (a+1)(b+1) pairs of ranks at most a and at most b all sum to at
+// least lv0[a] + lv1[b].
 template <int NC, int EW>
 __device__ __forceinline__ void select_candidates(const float* lv0, const int* li0, const float* lv1,
                                                   const int* li1, const unsigned short* pairs, int C,
@@ -176,8 +179,15 @@ __device__ __forceinline__ void select_candidates(const float* lv0, const int* l
             kmax = max(kmax, ck[i]);
         }
     }
-    kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
     kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+    {
+        // floor: the largest lv0[a] + lv1[ceil(W / (a+1)) - 1] over the ranks a < W
+        uint32_t fl = 0u;
+        for (int a = lane; a < W; a += 32)
+            fl = max(fl, float_order_bits(lv0[a] + lv1[(W + a) / (a + 1) - 1]));
+        kmin = max(kmin, __reduce_max_sync(0xFFFFFFFFu, fl));
+        kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+    }
     uint32_t lo = kmin, hi = kmax + 1;
     int cnt_hi = 0;
     bool exact = false;
@@ -219,34 +229,44 @@ __device__ __forceinline__ void select_candidates(const float* lv0, const int* l
     const float mx = float_from_order_bits(kmax);
     float part = 0.0f;
 #pragma unroll
-    for (int i = 0; i < NC; ++i)
-        part += keep[i] ? expf(cv[i] - mx) : 0.0f;
+    for (int i = 0; i < NC; ++i) {
+        cv[i] = keep[i] ? expf(cv[i] - mx) : 0.0f;
+        part += cv[i];
+    }
     part = __reduce_add_sync_f(part);
+    // kept weights by position in sel (as floats); sort keys (slot << 6) | position (slots
+    // below 2^18, positions below 64)
+    float* selw = reinterpret_cast<float*>(sel);
+    uint32_t k2[EW];
+#pragma unroll
+    for (int i = 0; i < EW; ++i)
+        k2[i] = ~0u;
     int base_pos = 0;
 #pragma unroll
     for (int i = 0; i < NC; ++i) {
         const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep[i]);
         if (keep[i]) {
             const int pos = base_pos + __popc(bal & ((1u << lane) - 1u));
-            sel[pos] = ((uint64_t)cs[i] << 32) | __float_as_uint(expf(cv[i] - mx) / part);
+            selw[pos] = cv[i] / part;
+            reinterpret_cast<uint32_t*>(selw + 64)[pos] = (cs[i] << 6) | (uint32_t)pos;
         }
         base_pos += __popc(bal);
     }
     __syncwarp();
     // report the set in ascending slot order, weights alongside
-    uint64_t k2[EW];
 #pragma unroll
     for (int i = 0; i < EW; ++i) {
         const int e = lane * EW + i;
-        k2[i] = (e < W) ? sel[e] : ~0ull;
+        if (e < W)
+            k2[i] = reinterpret_cast<const uint32_t*>(selw + 64)[e];
     }
     warp_bitonic_sort<EW>(k2);
 #pragma unroll
     for (int i = 0; i < EW; ++i) {
         const int e = lane * EW + i;
         if (e < W) {
-            idx[e] = (int32_t)(k2[i] >> 32);
-            wsel[e] = __uint_as_float((uint32_t)k2[i]);
+            idx[e] = (int32_t)(k2[i] >> 6);
+            wsel[e] = selw[k2[i] & 63u];
         }
     }
 }
@@ -254,7 +274,7 @@ __device__ __forceinline__ void select_candidates(const float* lv0, const int* l
 // One warp per (token, kind). Candidate pairs (a, b) of half-ranks come from a table
 // built in shared memory at block start.
 template <int NC>
-__global__ void __launch_bounds__(256) candidate_select_kernel(
+__global__ void __launch_bounds__(256, 4) candidate_select_kernel(
     const float* __restrict__ hv, const int32_t* __restrict__ hi, int64_t ntok, int n, int W,
     int32_t* __restrict__ idx, float* __restrict__ wsel)
 {
@@ -262,7 +282,7 @@ __global__ void __launch_bounds__(256) candidate_select_kernel(
     __shared__ int npairs;
     __shared__ float lv[8][2][64];
     __shared__ int li[8][2][64];
-    __shared__ uint64_t sel[8][64];
+    __shared__ uint64_t sel[8][64];     // kept weights [64] and sort keys [64] a warp
     build_pairs(pairs, &npairs, W);
     __syncthreads();
     const int C = npairs;
@@ -272,23 +292,57 @@ __global__ void __launch_bounds__(256) candidate_select_kernel(
         const int kind = (int)(qi / ntok);
         const int64_t tok = qi % ntok;
         const size_t base = ((size_t)kind * ntok + tok) * 2 * W;
-        // each half's W best rows sorted by (score desc, row asc): the tensor-core scoring
-        // writes them in row order
+        // each half's W best rows sorted by (score desc, row asc). The lists come in
+        // ascending row order (the tensor-core scoring writes them so; the SIMT one
+        // already sorted), so a sort on the score's descending order key with its 6 low
+        // bits replaced by the list position keeps equal scores in row order. Only
+        // scores that differ in those 6 bits alone can come out of order; a list where
+        // that happened is sorted again on full (score, row) keys.
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            uint64_t hk[2];
+            const float* hvl = hv + base + h * W;
+            const int32_t* hil = hi + base + h * W;
+            uint32_t sk[2];
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int e = lane * 2 + i;
-                hk[i] = e < W ? desc_key(hv[base + h * W + e], (uint32_t)hi[base + h * W + e]) : ~0ull;
+                sk[i] = e < W ? ((~float_order_bits(hvl[e])) & ~63u) | (uint32_t)e : ~0u;
             }
-            warp_bitonic_sort<2>(hk);
+            warp_bitonic_sort<2>(sk);
+            float sv[2];
+            int si[2];
+            uint32_t ok[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int e = lane * 2 + i;
+                const int src = e < W ? (int)(sk[i] & 63u) : 0;
+                sv[i] = hvl[src];
+                si[i] = hil[src];
+                ok[i] = float_order_bits(sv[i]);
+            }
+            const uint32_t nxt = __shfl_down_sync(0xFFFFFFFFu, ok[0], 1);
+            const bool bad = (lane * 2 + 1 < W && ok[0] < ok[1]) ||
+                             (lane < 31 && lane * 2 + 2 < W && ok[1] < nxt);
+            if (__any_sync(0xFFFFFFFFu, bad)) {
+                uint64_t hk[2];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int e = lane * 2 + i;
+                    hk[i] = e < W ? desc_key(hvl[e], (uint32_t)hil[e]) : ~0ull;
+                }
+                warp_bitonic_sort<2>(hk);
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    sv[i] = key_score(hk[i]);
+                    si[i] = (int)key_id(hk[i]);
+                }
+            }
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int e = lane * 2 + i;
                 if (e < W) {
-                    lv[warp][h][e] = key_score(hk[i]);
-                    li[warp][h][e] = (int)key_id(hk[i]);
+                    lv[warp][h][e] = sv[i];
+                    li[warp][h][e] = si[i];
                 }
             }
         }

@@ -361,18 +361,40 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
             const int tok = (tl % a.tiles_per_kind) * a.qrows + (a.rep == 1 ? q * 32 : 0) + lane;
             uint32_t v[32];
             const int nv_own = max(0, min(ce, a.n) - cb);          // valid columns here
+            // 32 columns into v; in a chunk past the n-th column, -inf in the columns
+            // beyond it, below every probe and threshold
+            auto load = [&](int c0) {
+                tmem_ld32(trow + c0, v);
+                if (c0 + 32 > a.n) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (c0 + j >= a.n)
+                            v[j] = 0xFF800000u;
+                }
+            };
             // the row's range, mean and spread
             float fmn = INFINITY, fmx = -INFINITY, sum = 0.f, sum2 = 0.f;
             for (int c0 = cb; c0 < ce; c0 += 32) {
                 tmem_ld32(trow + c0, v);
+                if (c0 + 32 <= a.n) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    if (c0 + j < a.n) {
+                    for (int j = 0; j < 32; ++j) {
                         const float f = __uint_as_float(v[j]);
                         fmn = fminf(fmn, f);
                         fmx = fmaxf(fmx, f);
                         sum += f;
                         sum2 = fmaf(f, f, sum2);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (c0 + j < a.n) {
+                            const float f = __uint_as_float(v[j]);
+                            fmn = fminf(fmn, f);
+                            fmx = fmaxf(fmx, f);
+                            sum += f;
+                            sum2 = fmaf(f, f, sum2);
+                        }
                     }
                 }
             }
@@ -410,23 +432,28 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
             }
             for (int pass = 0;; ++pass) {
                 unsigned short* xp = xpb + (pass & 1) * kProbes * 512;
-                int cp[kProbes];
+                // (counted in floats, exact here: the additions go to the FMA pipe, the
+                // comparisons to the ALU pipe)
+                float cf[kProbes];
 #pragma unroll
                 for (int k = 0; k < kProbes; ++k)
-                    cp[k] = 0;
+                    cf[k] = 0.f;
                 for (int c0 = cb; c0 < ce; c0 += 32) {
-                    tmem_ld32(trow + c0, v);
+                    load(c0);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const float f = c0 + j < a.n ? __uint_as_float(v[j]) : -INFINITY;
+                        const float f = __uint_as_float(v[j]);
 #pragma unroll
                         for (int k = 0; k < kProbes; ++k)
-                            cp[k] += f >= pr[k] ? 1 : 0;
+                            cf[k] += f >= pr[k] ? 1.f : 0.f;
                     }
                 }
+                int cp[kProbes];
 #pragma unroll
-                for (int k = 0; k < kProbes; ++k)
+                for (int k = 0; k < kProbes; ++k) {
+                    cp[k] = (int)cf[k];
                     xp[k * 512 + xi] = (unsigned short)cp[k];
+                }
                 bar_sync(bid, bn);
 #pragma unroll
                 for (int k = 0; k < kProbes; ++k) {
@@ -479,14 +506,18 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
             const int own_end = off + (listed ? o_lo - o_hi : 0);
             if (__any_sync(0xFFFFFFFFu, listed)) {
                 // this group's scores inside the bracket, in column order
+                // (own_end = off in rows without a list: nothing written)
                 int e = off;
                 for (int c0 = cb; c0 < ce; c0 += 32) {
-                    tmem_ld32(trow + c0, v);
+                    load(c0);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const float f = c0 + j < a.n ? __uint_as_float(v[j]) : -INFINITY;
-                        if (listed && f >= lo && f < hi && e < own_end)
-                            L[e++] = f;
+                        const float f = __uint_as_float(v[j]);
+                        if (f >= lo && f < hi) {
+                            if (e < own_end)
+                                L[e] = f;
+                            ++e;
+                        }
                     }
                 }
             }
@@ -550,22 +581,27 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
             const int allow = max(0, min(kt, need - pre_t));
             int ties = 0;
             const size_t ob = (((size_t)kind * a.ntok + tok) * 2 + half) * W;
-            const bool row_ok = tok < a.ntok;
+            const int pmax = tok < a.ntok ? W : 0;
+            // scores at or above tk are kept outright, those equal to t (below tk unless
+            // ex) while ties remain (allow is 0 when ex)
+            const float tk = ex ? t : nextafterf(t, INFINITY);
+            float* hv_row = a.hv + ob;
+            int32_t* hi_row = a.hi + ob;
             for (int c0 = cb; c0 < ce; c0 += 32) {
-                tmem_ld32(trow + c0, v);
+                load(c0);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const bool valid = c0 + j < a.n;
                     const float f = __uint_as_float(v[j]);
-                    bool keep = valid && (ex ? f >= t : f > t);
-                    if (!keep && valid && !ex && f == t && ties < allow) {
-                        keep = true;
-                        ++ties;
-                    }
-                    if (keep && row_ok && pos < W) {
-                        a.hv[ob + pos] = f + 0.0f;   // (-0 as +0)
-                        a.hi[ob + pos] = c0 + j;
-                        ++pos;
+                    if (f >= t) {
+                        const bool tie = f < tk;
+                        if (!tie || ties < allow) {
+                            ties += tie ? 1 : 0;
+                            if (pos < pmax) {
+                                hv_row[pos] = f + 0.0f;   // (-0 as +0)
+                                hi_row[pos] = c0 + j;
+                            }
+                            ++pos;
+                        }
                     }
                 }
             }

@@ -143,8 +143,8 @@ __device__ __forceinline__ uint32_t key_id(uint64_t k) { return (uint32_t)k; }
 
 // Bitonic sort, ascending, of 32*E 64-bit keys held lane-major by one warp (lane l
 // holds elements l*E .. l*E+E-1 in k[0..E-1]). E is a power of two.
-template <int E>
-__device__ __forceinline__ void warp_bitonic_sort(uint64_t (&k)[E])
+template <int E, typename K>
+__device__ __forceinline__ void warp_bitonic_sort(K (&k)[E])
 {
     const int lane = threadIdx.x & 31;
     constexpr int P = 32 * E;
@@ -159,7 +159,7 @@ __device__ __forceinline__ void warp_bitonic_sort(uint64_t (&k)[E])
                     if (j > i) {
                         const int e = lane * E + i;
                         const bool up = (e & size) == 0;
-                        uint64_t a = k[i], b = k[j];
+                        K a = k[i], b = k[j];
                         const bool swap = up ? (a > b) : (a < b);
                         k[i] = swap ? b : a;
                         k[j] = swap ? a : b;
@@ -170,11 +170,11 @@ __device__ __forceinline__ void warp_bitonic_sort(uint64_t (&k)[E])
 #pragma unroll
                 for (int i = 0; i < E; ++i) {
                     const int e = lane * E + i;
-                    const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, k[i], lm);
+                    const K other = __shfl_xor_sync(0xFFFFFFFFu, k[i], lm);
                     const bool up = (e & size) == 0;
                     const bool lower = (e & stride) == 0;
-                    const uint64_t mn = k[i] < other ? k[i] : other;
-                    const uint64_t mx = k[i] < other ? other : k[i];
+                    const K mn = k[i] < other ? k[i] : other;
+                    const K mx = k[i] < other ? other : k[i];
                     k[i] = (up == lower) ? mn : mx;
                 }
             }
