@@ -22,8 +22,8 @@
 // sort places them in kBuckets hash buckets of (slot, token, kind, position) entries,
 // 6 bytes each. Each reference of the block then scans only its slot's bucket -- a handful
 // of entries, more for popular slots -- for the latest earlier writer and the earlier
-// referencing tokens. The window is indexed again by every block, so blocks take as many
-// tokens as shared memory allows while the grid still fills the GPU twice over.
+// referencing tokens. The window is indexed again by every block; the run length is the
+// one whose waves of blocks cost least (below).
 #include "sdm_common.cuh"
 #include "sdm_internal.h"
 
@@ -182,21 +182,33 @@ cudaError_t launch_scan_codes(const sdm_cfg& c, const int32_t* idx, int B, int T
     unsigned long long* deadmask = masks + (size_t)B * T;
     unsigned long long* warmask = masks + (size_t)B * T * 2;
     const int N = c.n_sub * c.n_sub;
-    // Tokens a block: every block indexes its run and the window before it, so the
-    // largest run whose index fits in shared memory (6 bytes a reference; at most 512
-    // tokens indexed, the reach of the 9-bit token field), as long as the grid keeps two
-    // blocks a SM busy; runs of at most 32 tokens always qualify.
+    // Tokens a block: every block indexes its run and the window before it (6 bytes a
+    // reference; at most 512 tokens indexed, the reach of the 9-bit token field). The
+    // kernel is bound by the latency of its index, so blocks resident together on an SM
+    // take about as long as one: a run of tb tokens costs its waves of blocks (as many
+    // blocks an SM as shared memory and threads allow) times the references a block
+    // handles, (tb + win) inserted and tb looked up. The cheapest run wins (the longer
+    // one on a tie). At 4 x 4,096 tokens with a window of 35 that is runs of 56, one
+    // wave, where the earlier rule (the longest run still giving two blocks an SM) took
+    // runs of 48, 344 blocks for 296 places.
     const int sms = num_sms_current_device();
     auto smem_for = [&](int tb_) {
         return (size_t)(2 * kBuckets + 4) * 4 + (size_t)(tb_ + win) * 2 * c.w * 6;
     };
     int tb = 8;
-    const int cand[] = {256, 192, 128, 96, 64, 48, 32, 16, 8};
-    for (int tb_ : cand) {
+    long long best = -1;
+    for (int tb_ = 256; tb_ >= 8; tb_ -= 8) {
+        const size_t sm = smem_for(tb_);
+        if (sm > kCodeSmemMax || tb_ + win > 512)
+            continue;
+        long long per_sm = (long long)(228 * 1024) / (long long)(sm + 1024);
+        per_sm = per_sm < 1 ? 1 : per_sm > 2048 / kCodeThreads ? 2048 / kCodeThreads : per_sm;
         const long long blocks = (long long)B * ((T + tb_ - 1) / tb_);
-        if (smem_for(tb_) <= kCodeSmemMax && tb_ + win <= 512 && (blocks >= 2LL * sms || tb_ <= 32)) {
+        const long long waves = (blocks + per_sm * sms - 1) / (per_sm * sms);
+        const long long cost = waves * (2LL * tb_ + win);
+        if (best < 0 || cost < best) {
+            best = cost;
             tb = tb_;
-            break;
         }
     }
     const size_t smem = smem_for(tb);
