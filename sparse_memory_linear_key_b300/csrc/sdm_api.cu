@@ -33,7 +33,10 @@ static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 // scan (event record / wait, so that a captured graph gets a parallel branch). One side
 // stream and two events per device; the lock keeps another thread's call off them from
 // the fork until the join is enqueued. (One token a sequence takes the early-launch chain
-// in prefill_impl instead.)
+// in prefill_impl instead.) From M0 with several tokens a sequence, the same side stream
+// takes the first-touch table and the fill of never-written slots while the caller's
+// stream computes the collision codes: both need only the slot ids, the fill (bound by
+// HBM) hides the codes (bound by the latency of their index), and the scan waits for both.
 constexpr int64_t kForkTokens = 256;
 
 struct ProjFork {
@@ -491,11 +494,14 @@ static int prefill_impl(const sdm_cfg* cfg, const sdm_weights* w, const void* M0
     } else {
         ok = launch_project_tc(*cfg, *w, x, ntok, q_w, q_r, v, s) == cudaSuccess;
     }
+    // from M0 with several tokens a sequence: first touch and fill beside the codes
+    const bool fill_beside = M0 != nullptr && T > 1;
     ok = ok &&
          launch_address(*cfg, w->K1, w->K2, q_w, q_r, ntok, idx, wsel, base + L.addr, dev_status,
                         s, ntok <= kForkTokens, early ? (char*)scan_ws + SL.flags : nullptr,
                         early ? SL.flags_bytes : 0) == cudaSuccess &&
-         (M0 == nullptr || launch_first_touch(*cfg, idx, B, T, first_write, s) == cudaSuccess);
+         (M0 == nullptr || fill_beside ||
+          launch_first_touch(*cfg, idx, B, T, first_write, s) == cudaSuccess);
     if (f != nullptr) {
         // v is ready for the scan
         const bool joined = cudaStreamWaitEvent(s, f->ev_v, 0) == cudaSuccess;
@@ -504,6 +510,29 @@ static int prefill_impl(const sdm_cfg* cfg, const sdm_weights* w, const void* M0
     }
     if (!ok)
         return SDM_ECUDA;
+    if (fill_beside) {
+        lock = std::unique_lock<std::mutex>(g_fork_mu);
+        f = fork_state();
+        if (f == nullptr)
+            return SDM_ECUDA;
+        if (cudaEventRecord(f->ev_fork, s) != cudaSuccess ||
+            cudaStreamWaitEvent(f->side, f->ev_fork, 0) != cudaSuccess)
+            return SDM_ECUDA;
+        ok = launch_first_touch(*cfg, idx, B, T, first_write, f->side) == cudaSuccess &&
+             launch_fill_untouched(*cfg, M0, first_write, banks, B, T, f->side) == cudaSuccess;
+        // the side stream is joined back whatever happened (a forked capture must rejoin)
+        if (cudaEventRecord(f->ev_v, f->side) != cudaSuccess)
+            return SDM_ECUDA;
+        ok = ok && launch_scan_codes(*cfg, idx, B, T, SL.win, (uint16_t*)((char*)scan_ws + SL.codes),
+                                     (unsigned long long*)((char*)scan_ws + SL.masks), dev_status,
+                                     s) == cudaSuccess;
+        const bool joined = cudaStreamWaitEvent(s, f->ev_v, 0) == cudaSuccess;
+        lock.unlock();
+        if (!ok || !joined)
+            return SDM_ECUDA;
+        return cuda_status(launch_scan(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, scan_ws,
+                                       SL.total, dev_status, s, M0, first_write));
+    }
     rc = scan_impl(*cfg, idx, wsel, v, alpha, beta, banks, y, B, T, scan_ws, SL.total, dev_status,
                    s, M0, first_write, early);
     if (rc != SDM_OK || M0 == nullptr)
