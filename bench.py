@@ -537,7 +537,9 @@ def gpu_arm(args, world, rank):
         e2e_step(i)
     torch.cuda.synchronize()
     # the pipeline's fill (first copy in) and drain (last copy out) are timed too
-    n_e2e = max(10, args.steps // 2)
+    # (a serving loop's steady state: the one-off first copy in and last copy out are
+    # spread over twice the timed steps)
+    n_e2e = max(20, 2 * args.steps)
     barrier(world)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
