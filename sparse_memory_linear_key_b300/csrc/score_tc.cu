@@ -48,12 +48,13 @@ constexpr uint32_t kABytes = kTileM * 128 * 2;        // two K atoms of 128 rows
 // rows (multiples of dz), and the capacity of a row's list of the scores inside its final
 // bracket (odd: the rows of a warp hit different banks)
 constexpr int kProbes = 6;
-constexpr int kLCap = 37;
+constexpr int kLCap = 31;
 __constant__ float kProbeAt[kProbes] = {-35.f, -15.f, -7.f, 7.f, 15.f, 35.f};
 // exchange area after the barriers and the TMEM address: the bracket lists [128][kLCap]
-// (the row statistics of the first pass alias their start), probe counts [2][kProbes][512]
-// (the emission counts alias the first two), list sizes [512], W-th scores [128]
-constexpr uint32_t kXBytes = 128 * kLCap * 4 + 2 * kProbes * 512 * 2 + 512 * 2 + 128 * 4;
+// of scores (the row statistics of the first pass alias their start) and of their
+// columns, probe counts [kProbes][512] (the emission counts alias the first two), list
+// sizes [512], counts of scores kept outright [512], W-th scores [128]
+constexpr uint32_t kXBytes = 128 * kLCap * (4 + 2) + kProbes * 512 * 2 + 2 * 512 * 2 + 128 * 4;
 
 struct ScoreArgs {
     int ntok, n, khalf, W, tiles_per_kind, ctas_per_half;
@@ -206,11 +207,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
     float* xfmax = xl + 512;                               // sum and sum of squares (first pass)
     float* xs = xl + 1024;
     float* xs2 = xl + 1536;
-    unsigned short* xpb = reinterpret_cast<unsigned short*>(xl + 128 * kLCap);  // [2][kProbes][512]
+    unsigned short* xlc = reinterpret_cast<unsigned short*>(xl + 128 * kLCap);  // [row slot][kLCap]
+    unsigned short* xpb = xlc + 128 * kLCap;               // [kProbes][512]
     unsigned short* xa = xpb;                              // [512] emission counts: kept, ties
     unsigned short* xt = xpb + 512;
-    unsigned short* xln = xpb + 2 * kProbes * 512;         // [512] list entries a thread
-    float* xtr = reinterpret_cast<float*>(xln + 512);      // [row slot] W-th score
+    unsigned short* xln = xpb + kProbes * 512;             // [512] list entries a thread
+    unsigned short* xab = xln + 512;                       // [512] scores kept outright
+    float* xtr = reinterpret_cast<float*>(xab + 512);      // [row slot] W-th score
     __shared__ int dead;                 // a role gave up: the others stop at their next wait
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -431,7 +434,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
                     pr[k] = mean + (a.z + a.dz * kProbeAt[k]) * sd;
             }
             for (int pass = 0;; ++pass) {
-                unsigned short* xp = xpb + (pass & 1) * kProbes * 512;
+                unsigned short* xp = xpb;
+                if (pass > 0)
+                    bar_sync(bid, bn);   // everyone has read the previous pass's counts
                 // (counted in floats, exact here: the additions go to the FMA pipe, the
                 // comparisons to the ALU pipe)
                 float cf[kProbes];
@@ -496,27 +501,50 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
                                                : order_key(__float_as_uint(fmx)) + 1u;
             const bool listed = !exact && khi - klo > 1u;   // rank inside the bracket's list
             const int m = c_lo - c_hi;
+            // Scores at or above ta are kept outright: all of the row's W when exact (ta =
+            // lo), else those at or above hi. The list pass writes them out (after the
+            // kept scores of lower groups: ab of them here) and lists the bracket's.
+            const float ta = exact ? lo : hi;
+            const int ab = exact ? o_lo : o_hi;
             xln[xi] = (unsigned short)(listed ? o_lo - o_hi : 0);
+            xab[xi] = (unsigned short)ab;
             bar_sync(bid, bn);
-            int off = 0;
-            for (int h = 0; h < g; ++h)
+            int off = 0, pre_ab = 0;
+            for (int h = 0; h < g; ++h) {
                 off += xln[xq + h * 32];
+                pre_ab += xab[xq + h * 32];
+            }
             const int rslot = xs0 * 32 + lane;
             float* L = xl + (size_t)rslot * kLCap;
+            unsigned short* Lc = xlc + (size_t)rslot * kLCap;
             const int own_end = off + (listed ? o_lo - o_hi : 0);
-            if (__any_sync(0xFFFFFFFFu, listed)) {
-                // this group's scores inside the bracket, in column order
-                // (own_end = off in rows without a list: nothing written)
-                int e = off;
+            const size_t ob = (((size_t)kind * a.ntok + tok) * 2 + half) * W;
+            const int pmax = tok < a.ntok ? W : 0;
+            float* hv_row = a.hv + ob;
+            int32_t* hi_row = a.hi + ob;
+            {
+                // scores kept outright to the output, in column order; the bracket's into
+                // this group's run of the list (own_end = off where the row has no list)
+                int e = off, pos = pre_ab;
                 for (int c0 = cb; c0 < ce; c0 += 32) {
                     load(c0);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const float f = __uint_as_float(v[j]);
-                        if (f >= lo && f < hi) {
-                            if (e < own_end)
-                                L[e] = f;
-                            ++e;
+                        if (f >= lo) {
+                            if (f >= ta) {
+                                if (pos < pmax) {
+                                    hv_row[pos] = f + 0.0f;   // (-0 as +0)
+                                    hi_row[pos] = c0 + j;
+                                }
+                                ++pos;
+                            } else {
+                                if (e < own_end) {
+                                    L[e] = f;
+                                    Lc[e] = (unsigned short)(c0 + j);
+                                }
+                                ++e;
+                            }
                         }
                     }
                 }
@@ -539,18 +567,16 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
                 }
             }
             bar_sync(bid, bn);
+            // Inside the bracket: kept outright ka (ex ? scores >= t : scores > t), ties kt
+            // (scores equal to t, taken by ascending row up to W in all). A row with one
+            // value in its bracket (not listed) keeps ties of lo.
             float t = lo;
             bool ex = exact;
-            int ka, kt, cnt_above;
+            int ka = 0, kt = 0, cnt_above = c_hi;
             if (exact) {
-                ka = o_lo;
-                kt = 0;
                 cnt_above = W;
             } else if (!listed) {
-                // one value in [lo, hi): scores above lo are those at or above hi
-                ka = o_hi;
                 kt = o_lo - o_hi;
-                cnt_above = c_hi;
             } else {
                 t = xtr[rslot];
                 int gt = 0, ge = 0, og = 0, oe = 0;
@@ -564,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
                     oe += L[e] == t ? 1 : 0;
                 }
                 ex = c_hi + ge == W;
-                ka = o_hi + (ex ? og + oe : og);
+                ka = ex ? og + oe : og;
                 kt = ex ? 0 : oe;
                 cnt_above = c_hi + gt;
             }
@@ -577,27 +603,39 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
                 pre_t += xt[xq + h * 32];
             }
             const int need = ex ? 0 : W - cnt_above;
-            int pos = pre_a + min(pre_t, need);
+            // after the c_hi outright scores of the row (the list pass wrote them)
+            int pos = c_hi + pre_a + min(pre_t, need);
             const int allow = max(0, min(kt, need - pre_t));
             int ties = 0;
-            const size_t ob = (((size_t)kind * a.ntok + tok) * 2 + half) * W;
-            const int pmax = tok < a.ntok ? W : 0;
-            // scores at or above tk are kept outright, those equal to t (below tk unless
-            // ex) while ties remain (allow is 0 when ex)
-            const float tk = ex ? t : nextafterf(t, INFINITY);
-            float* hv_row = a.hv + ob;
-            int32_t* hi_row = a.hi + ob;
-            for (int c0 = cb; c0 < ce; c0 += 32) {
-                load(c0);
+            if (listed) {
+                // this group's kept bracket scores from its run of the list, column order
+                for (int e = off; e < own_end; ++e) {
+                    const float f = L[e];
+                    const bool keep = ex ? f >= t : f > t;
+                    const bool tie = !keep && f == t && ties < allow;
+                    if (keep || tie) {
+                        ties += tie ? 1 : 0;
+                        if (pos < pmax) {
+                            hv_row[pos] = f + 0.0f;
+                            hi_row[pos] = Lc[e];
+                        }
+                        ++pos;
+                    }
+                }
+            }
+            if (__any_sync(0xFFFFFFFFu, !exact && !listed)) {
+                // rows whose bracket holds one value: its first ties by column order
+                // (rare: rows of equal scores, such as the zero queries of a last tile's
+                // rows past the tokens)
+                for (int c0 = cb; c0 < ce; c0 += 32) {
+                    load(c0);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float f = __uint_as_float(v[j]);
-                    if (f >= t) {
-                        const bool tie = f < tk;
-                        if (!tie || ties < allow) {
-                            ties += tie ? 1 : 0;
+                    for (int j = 0; j < 32; ++j) {
+                        const float f = __uint_as_float(v[j]);
+                        if (!exact && !listed && f == lo && ties < allow) {
+                            ++ties;
                             if (pos < pmax) {
-                                hv_row[pos] = f + 0.0f;   // (-0 as +0)
+                                hv_row[pos] = f + 0.0f;
                                 hi_row[pos] = c0 + j;
                             }
                             ++pos;
