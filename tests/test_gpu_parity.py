@@ -509,3 +509,36 @@ def test_decode_steps_captured_in_a_graph_match_eager():
     torch.cuda.synchronize()
     assert st.item() == 0
     assert torch.equal(y_g, y_e) and torch.equal(banks_g, banks_e)
+
+
+@pytest.mark.parametrize("B,T", [(3, 60), (2, 400)])
+def test_prefill_m0_captured_in_a_graph_matches_eager(B, T):
+    """sdm_prefill_m0 forks a side stream (the first-touch table and the fill beside the
+    collision codes; for a few tokens also the v projection beside q) and joins it back,
+    so a captured call becomes a graph with parallel branches. After a first call (which
+    creates the side stream), the captured call replayed gives the eager call's bits.
+    180 tokens take the few-token path, 800 the many-token one."""
+    wl = synth.Workload("gp", B=B, T=T, d=128, n=40, dk=64, W=16, dtype="bf16", seed=93)
+    p, tok = _inputs(wl)
+    cfg = tl.cfg_of(wl)
+    pd = tl.to_dev(p)
+    x, al, be = tok["x"].cuda(), tok["alpha"].cuda(), tok["beta"].cuda()
+    ws = sdm.alloc_workspace(sdm.prefill_m0_workspace_bytes(cfg, B, T))
+    st = sdm.new_status()
+
+    def run(banks, y):
+        sdm.sdm_prefill_m0(cfg, pd, pd["M0"], x, al, be, banks, y, ws, st)
+
+    banks_e = torch.empty(B, wl.N, wl.d, dtype=torch.bfloat16, device="cuda")
+    y_e = torch.empty(B, T, wl.d, device="cuda")
+    run(banks_e, y_e)
+    torch.cuda.synchronize()
+    banks_g = torch.zeros_like(banks_e)
+    y_g = torch.zeros_like(y_e)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run(banks_g, y_g)
+    g.replay()
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(y_g, y_e) and torch.equal(banks_g, banks_e)
