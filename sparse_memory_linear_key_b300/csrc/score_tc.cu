@@ -11,16 +11,18 @@
 //  * one thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M = 128, N = 256
 //    twice) into a 512-column TMEM accumulator: row r of the tile in TMEM lane r;
 //  * sixteen epilogue warps (four per TMEM lane quadrant, one column group each) keep,
-//    per row, the W largest scores by (score desc, row asc): a first pass replaces
-//    each score in TMEM by its
-//    order-preserving integer image (tcgen05.st) and sums the row's scores and squares;
-//    a bracket around mean + z sd (the scores of a row are near normal; z is the normal
-//    quantile of 1 - W/n; four probes, the inner two 1/10 sd either side) is checked in
-//    one counting pass, and a bisection over the keys
-//    inside what holds of the bracket (the whole range otherwise) finds the W-th
-//    largest, stopping early once exactly W keys lie at or above the probe; a last pass
-//    writes the kept (score, row) pairs, ties at the threshold by ascending row.
-// The per-half lists are written unsorted; the candidate kernel sorts them.
+//    per row, the W largest scores by (score desc, row asc), in three passes over TMEM:
+//    the row's range, mean and spread; counting passes of six probes narrowing a
+//    bracket [lo, hi) of the W-th largest score (the first around mean + z sd -- scores
+//    of a row are near normal, z the normal quantile of 1 - W/n -- later ones, run only
+//    while a row of the warp keeps too many scores inside its bracket, around the
+//    interpolated place of the W-th score and the midpoint of the bracket's order keys);
+//    and a pass that writes the scores kept outright and lists the bracket's scores
+//    (with their columns) in shared memory, where each thread ranks its own entries
+//    against the row's list to find the W-th largest, t. The kept bracket scores are
+//    then written from the list: those above t, then those equal to t by ascending row.
+// The per-half lists are written in ascending row order among equal scores; the
+// candidate kernel sorts them by score.
 // Every wait is bounded (status SDM_ETIMEOUT); on time-out a role stops issuing, the
 // CTA waits (bounded) for its copies and MMAs in flight and frees its TMEM.
 #include <cuda.h>
@@ -119,21 +121,6 @@ __device__ __forceinline__ bool bar_all(int id, int n, bool ok)
         : "r"((uint32_t)ok), "r"(id), "r"(n)
         : "memory");
     return r != 0;
-}
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32])
-{
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
-        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]),
-        "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]),
-        "r"(v[30]), "r"(v[31])
-        : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
