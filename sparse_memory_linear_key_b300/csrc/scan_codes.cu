@@ -20,7 +20,8 @@
 // Block: one sequence, a run of `tb` tokens [t0, t1). The references of the window
 // [t0 - win, t1) (slot ids are one contiguous run of idx) are indexed by slot: a counting
 // sort places them in kBuckets hash buckets of (slot, token, kind, position) entries,
-// 6 bytes each. Each reference of the block then scans only its slot's bucket -- a handful
+// 6 bytes each; bucket counts and offsets are 16-bit (two buckets a 32-bit word for the
+// atomics; a block indexes fewer than 65,536 references). Each reference of the block then scans only its slot's bucket -- a handful
 // of entries, more for popular slots -- for the latest earlier writer and the earlier
 // referencing tokens. The window is indexed again by every block; the run length is the
 // one whose waves of blocks cost least (below).
@@ -49,9 +50,9 @@ __global__ void __launch_bounds__(kCodeThreads) codes_kernel(const int32_t* __re
                                                              int* status)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    uint32_t* off = reinterpret_cast<uint32_t*>(smem_raw);           // [kBuckets + 1]
-    uint32_t* cur = off + kBuckets + 4;                               // [kBuckets] counts, cursors
-    int32_t* slot = reinterpret_cast<int32_t*>(cur + kBuckets);       // [nref window]
+    uint16_t* off = reinterpret_cast<uint16_t*>(smem_raw);           // [kBuckets + 1]
+    uint32_t* cur = reinterpret_cast<uint32_t*>(off + kBuckets + 8); // [kBuckets / 2] counts, cursors
+    int32_t* slot = reinterpret_cast<int32_t*>(cur + kBuckets / 2);   // [nref window]
     uint16_t* info = reinterpret_cast<uint16_t*>(slot + (tb + win) * 2 * W);  // tloc<<7|kind<<6|pos
     __shared__ uint32_t wsum[kCodeThreads / 32];
     const int b = blockIdx.y;
@@ -60,15 +61,17 @@ __global__ void __launch_bounds__(kCodeThreads) codes_kernel(const int32_t* __re
     const int base = max(0, t0 - win);
     const int nwin = (t1 - base) * 2 * W;
     const int32_t* wsrc = idx + ((size_t)b * T + base) * 2 * W;     // [token][write, read][W]
-    for (int i = threadIdx.x; i < kBuckets; i += blockDim.x)
+    for (int i = threadIdx.x; i < kBuckets / 2; i += blockDim.x)
         cur[i] = 0u;
     __syncthreads();
     for (int e = threadIdx.x; e < nwin; e += blockDim.x) {
         const int32_t s = __ldg(wsrc + e);
-        if (s >= 0 && s < N)
-            atomicAdd(&cur[bucket_of(s)], 1u);
-        else if (((e / W) & 1) == 0)
+        if (s >= 0 && s < N) {
+            const uint32_t bk = bucket_of(s);
+            atomicAdd(&cur[bk >> 1], 1u << (16 * (bk & 1)));
+        } else if (((e / W) & 1) == 0) {
             report(status, SDM_ERANGE);
+        }
     }
     __syncthreads();
     // exclusive prefix sum of the bucket sizes (8 buckets a thread)
@@ -78,7 +81,8 @@ __global__ void __launch_bounds__(kCodeThreads) codes_kernel(const int32_t* __re
         uint32_t v[PER], tot = 0;
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-            v[i] = cur[threadIdx.x * PER + i];
+            const int bk = threadIdx.x * PER + i;
+            v[i] = (cur[bk >> 1] >> (16 * (bk & 1))) & 0xFFFFu;
             tot += v[i];
         }
         uint32_t inc = tot;
@@ -95,20 +99,23 @@ __global__ void __launch_bounds__(kCodeThreads) codes_kernel(const int32_t* __re
         for (int w = 0; w < warp; ++w)
             pre += wsum[w];
         uint32_t run = pre + inc - tot;
+        __syncthreads();   // every count is read before the cursors replace them
 #pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            off[threadIdx.x * PER + i] = run;
-            cur[threadIdx.x * PER + i] = run;
-            run += v[i];
+        for (int i = 0; i < PER; i += 2) {
+            off[threadIdx.x * PER + i] = (uint16_t)run;
+            off[threadIdx.x * PER + i + 1] = (uint16_t)(run + v[i]);
+            cur[(threadIdx.x * PER + i) >> 1] = run | ((run + v[i]) << 16);
+            run += v[i] + v[i + 1];
         }
         if (threadIdx.x == blockDim.x - 1)
-            off[kBuckets] = run;
+            off[kBuckets] = (uint16_t)run;
     }
     __syncthreads();
     for (int e = threadIdx.x; e < nwin; e += blockDim.x) {
         const int32_t s = __ldg(wsrc + e);
         if (s >= 0 && s < N) {
-            const uint32_t at = atomicAdd(&cur[bucket_of(s)], 1u);
+            const uint32_t bk = bucket_of(s);
+            const uint32_t at = (atomicAdd(&cur[bk >> 1], 1u << (16 * (bk & 1))) >> (16 * (bk & 1))) & 0xFFFFu;
             slot[at] = s;
             info[at] = (uint16_t)(((e / (2 * W)) << 7) | (((e / W) & 1) << 6) | (e % W));
         }
@@ -193,13 +200,13 @@ cudaError_t launch_scan_codes(const sdm_cfg& c, const int32_t* idx, int B, int T
     // runs of 48, 344 blocks for 296 places.
     const int sms = num_sms_current_device();
     auto smem_for = [&](int tb_) {
-        return (size_t)(2 * kBuckets + 4) * 4 + (size_t)(tb_ + win) * 2 * c.w * 6;
+        return (size_t)(kBuckets + 8) * 2 + (size_t)kBuckets * 2 + (size_t)(tb_ + win) * 2 * c.w * 6;
     };
     int tb = 8;
     long long best = -1;
     for (int tb_ = 256; tb_ >= 8; tb_ -= 8) {
         const size_t sm = smem_for(tb_);
-        if (sm > kCodeSmemMax || tb_ + win > 512)
+        if (sm > kCodeSmemMax || tb_ + win > 512 || (long long)(tb_ + win) * 2 * c.w > 65535)
             continue;
         long long per_sm = (long long)(228 * 1024) / (long long)(sm + 1024);
         per_sm = per_sm < 1 ? 1 : per_sm > 2048 / kCodeThreads ? 2048 / kCodeThreads : per_sm;
