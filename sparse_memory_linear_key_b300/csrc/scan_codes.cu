@@ -208,8 +208,10 @@ cudaError_t launch_scan_codes(const sdm_cfg& c, const int32_t* idx, int B, int T
         const size_t sm = smem_for(tb_);
         if (sm > kCodeSmemMax || tb_ + win > 512 || (long long)(tb_ + win) * 2 * c.w > 65535)
             continue;
+        // at most two blocks an SM: in a prefill from M0 the codes run beside the
+        // first-touch table and the fill, which need room on the SMs as well
         long long per_sm = (long long)(228 * 1024) / (long long)(sm + 1024);
-        per_sm = per_sm < 1 ? 1 : per_sm > 2048 / kCodeThreads ? 2048 / kCodeThreads : per_sm;
+        per_sm = per_sm < 1 ? 1 : per_sm > 2 ? 2 : per_sm;
         const long long blocks = (long long)B * ((T + tb_ - 1) / tb_);
         const long long waves = (blocks + per_sm * sms - 1) / (per_sm * sms);
         const long long cost = waves * (2LL * tb_ + win);
