@@ -73,7 +73,9 @@ __global__ void __launch_bounds__(256) first_touch_kernel(const int32_t* __restr
 }
 
 // One warp per slot: the sequences that never wrote it (first_write >= T) get M0's row,
-// read once. Each lane moves 16 bytes a step, four steps in flight.
+// read once. Up to 32 sequences: a lane per sequence reads the first-writer table, one
+// slot ahead, and each lane has eight 16-byte loads in flight (a 4 KB row at once); more
+// sequences take them 32 at a time.
 __global__ void __launch_bounds__(256) fill_untouched_kernel(const uint4* __restrict__ M0,
                                                              const int32_t* __restrict__ first_write,
                                                              uint4* __restrict__ banks, int B, int T,
@@ -81,30 +83,49 @@ __global__ void __launch_bounds__(256) fill_untouched_kernel(const uint4* __rest
 {
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t sl = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); sl < N;
-         sl += warps) {
-        for (int b0 = 0; b0 < B; b0 += 32) {
-            const int b = b0 + lane;
-            const bool fresh = b < B && __ldg(first_write + (int64_t)b * N + sl) >= T;
-            unsigned mask = __ballot_sync(0xFFFFFFFFu, fresh);
-            if (mask == 0)
-                continue;
+    int64_t sl = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (B > 32) {
+        for (; sl < N; sl += warps) {
+            for (int b0 = 0; b0 < B; b0 += 32) {
+                const int b = b0 + lane;
+                const bool fresh = b < B && __ldg(first_write + (int64_t)b * N + sl) >= T;
+                unsigned mask = __ballot_sync(0xFFFFFFFFu, fresh);
+                if (mask == 0)
+                    continue;
+                const uint4* src = M0 + sl * row16;
+                for (int c0 = lane; c0 < row16; c0 += 32) {
+                    const uint4 v = __ldg(src + c0);
+                    for (unsigned m = mask; m != 0; m &= m - 1)
+                        __stcs(banks + ((int64_t)(b0 + __ffs(m) - 1) * N + sl) * row16 + c0, v);
+                }
+            }
+        }
+        return;
+    }
+    bool fresh = sl < N && lane < B && __ldg(first_write + (int64_t)lane * N + sl) >= T;
+    while (sl < N) {
+        const int64_t nx = sl + warps;
+        const bool fresh_n = nx < N && lane < B && __ldg(first_write + (int64_t)lane * N + nx) >= T;
+        const unsigned mask = __ballot_sync(0xFFFFFFFFu, fresh);
+        if (mask != 0) {
             const uint4* src = M0 + sl * row16;
-            for (int c0 = lane; c0 < row16; c0 += 4 * 32) {
-                uint4 v[4];
+            for (int c0 = lane; c0 < row16; c0 += 8 * 32) {
+                uint4 v[8];
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
+                for (int u = 0; u < 8; ++u)
                     if (c0 + u * 32 < row16)
                         v[u] = __ldg(src + c0 + u * 32);
                 for (unsigned m = mask; m != 0; m &= m - 1) {
-                    uint4* dst = banks + ((int64_t)(b0 + __ffs(m) - 1) * N + sl) * row16;
+                    uint4* dst = banks + ((int64_t)(__ffs(m) - 1) * N + sl) * row16;
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
+                    for (int u = 0; u < 8; ++u)
                         if (c0 + u * 32 < row16)
                             __stcs(dst + c0 + u * 32, v[u]);
                 }
             }
         }
+        sl = nx;
+        fresh = fresh_n;
     }
 }
 

@@ -28,10 +28,16 @@ def _garbage_like(t):
     return torch.randn(t.shape, generator=g, device="cuda").to(t.dtype) * 1e3
 
 
+# more sequences than a warp has lanes: the fill takes the first-writer table 32
+# sequences at a time
+MANY_SEQ = synth.Workload("many-seq", B=40, T=24, d=192, n=24, dk=32, W=8, dtype="bf16",
+                          seed=85)
+
+
 @pytest.mark.parametrize("name", ["tiny-f32", "ragged-bf16", "w64-small", "n480-full-tiles",
-                                  "multiblock-bf16", "multiblock-f32"])
+                                  "multiblock-bf16", "multiblock-f32", "many-seq"])
 def test_prefill_m0_matches_init_then_prefill(name):
-    wl = SMALL[name]
+    wl = MANY_SEQ if name == "many-seq" else SMALL[name]
     cfg = tl.cfg_of(wl)
     p = tl.to_dev(synth.make_params(wl))
     tok = synth.make_tokens(wl)
