@@ -935,8 +935,10 @@ __device__ void role_consumer(const ScanArgs& a, unsigned char* wbuf, unsigned c
             // GPU scope itself (flag 2), one polling step sooner than the marks warp would:
             // each warp's arrival is a release at CTA scope, the last one's an acquire,
             // and its release at GPU scope carries the others' stores along. (With one
-            // token a sequence nothing reads the flags.)
-            if (a.T > 1) {
+            // token a sequence nothing reads the flags; an item with no forwarded slot has
+            // no ring entry that a later token copies, and the flag 3 its commit raises
+            // answers every wait for flag 2.)
+            if (a.T > 1 && m.fwdmask != 0) {
                 int old;
                 asm volatile("atom.acq_rel.cta.shared::cta.add.s32 %0, [%1], 1;"
                              : "=r"(old)
