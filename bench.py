@@ -98,8 +98,8 @@ def max_over_ranks(world, x: float) -> float:
 # DRAM bytes (read + write) of one scan_kernel launch on this workload, from one ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum, 1 pass, full size). They hold
 # for the kernel sources they were taken on; any change to those makes them stale.
-SCAN_TRAFFIC = {"B": 4, "T": 4096, "bytes": 8440011520 + 4434076416,
-                "sources_sha256": {"scan.cu": "9c92877a537bfd53", "sdm_common.cuh": "1f984e99590cd1ea",
+SCAN_TRAFFIC = {"B": 4, "T": 4096, "bytes": 8439371776 + 4434630912,
+                "sources_sha256": {"scan.cu": "12e47d24b7e3e77e", "sdm_common.cuh": "1f984e99590cd1ea",
                                    "scan_math.cuh": "d17a68a734fe9bd2"}}
 
 
