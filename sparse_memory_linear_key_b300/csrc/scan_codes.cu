@@ -33,7 +33,7 @@ namespace sdm {
 namespace {
 
 constexpr int kBuckets = 4096;
-constexpr int kCodeThreads = 1024;
+constexpr int kCodeThreads = 512;
 constexpr size_t kCodeSmemMax = 225 * 1024;
 
 __device__ __forceinline__ uint32_t bucket_of(int32_t s)
