@@ -306,17 +306,21 @@ def gpu_arm(args, world, rank):
     stage_ms = stage_times(ev)
     ms_per_step = elapsed_ms / args.steps
     # the codes alone (outside the timed region): in the step they share the GPU with the
-    # fill, whose HBM traffic stretches them, but the scan waits for the fill anyway
-    # (the stream first sleeps for about a millisecond, so that the host has queued all
-    # five calls before the first one starts and no launch gap is timed)
+    # fill, whose HBM traffic stretches them, but the scan waits for the fill anyway.
+    # Five calls captured in a CUDA graph, so that no host launch gap is timed.
+    gc = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gc):
+        for _ in range(5):
+            sdm.sdm_scan_prepare(cfg, idx, B, T, ws_s, st)
+    gc.replay()
+    torch.cuda.synchronize()
     c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda._sleep(2_000_000)
     c0.record(stream)
-    for _ in range(5):
-        sdm.sdm_scan_prepare(cfg, idx, B, T, ws_s, st)
+    gc.replay()
     c1.record(stream)
     torch.cuda.synchronize()
     stage_ms["codes_alone"] = c0.elapsed_time(c1) / 5
+    del gc
     value = ntok * world * args.steps / (elapsed_ms / 1e3)
 
     # roofline of the scan kernel: algorithmic bytes per launch / launch duration
