@@ -98,3 +98,48 @@ def test_two_replicas_match_one_process(tmp_path):
         assert r["status"] == 0
         assert torch.equal(r["y"], y_ref.cpu()), rank
         assert torch.equal(r["banks"], banks_ref.cpu()), rank
+
+
+def test_concurrent_calls_from_two_host_threads():
+    """sdm_prefill_m0 forks its first-touch table and fill onto a side stream the library
+    owns (one a device, shared by all callers) and joins it back. Two host threads calling
+    it at once on their own streams, each with its own buffers, must each get the bits
+    of a call made alone: the lock keeps one thread's fork-to-join sequence whole, and
+    the events keep each call's work ordered on the device."""
+    import threading
+    y_ref, banks_ref, st = run_prefill()
+    assert st == 0
+    cfg = tl.cfg_of(WL)
+    p = tl.to_dev(synth.make_params(WL))
+    tok = synth.make_tokens(WL)
+    x, al, be = tok["x"].cuda(), tok["alpha"].cuda(), tok["beta"].cuda()
+    out = [None, None]
+    err = []
+
+    def worker(i):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                banks = torch.empty(WL.B, WL.N, WL.d, dtype=WL.torch_dtype, device="cuda")
+                y = torch.empty(WL.B, WL.T, WL.d, device="cuda")
+                ws = sdm.alloc_workspace(sdm.prefill_m0_workspace_bytes(cfg, WL.B, WL.T))
+                stt = sdm.new_status()
+                for _ in range(4):
+                    sdm.sdm_prefill_m0(cfg, p, p["M0"], x, al, be, banks, y, ws, stt, stream=s)
+            s.synchronize()
+            out[i] = (y.cpu(), banks.cpu(), sdm.read_status(stt))
+        except Exception as e:  # pragma: no cover - reported below
+            err.append(repr(e))
+
+    torch.cuda.synchronize()
+    th = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    assert not err, err
+    for i in range(2):
+        y, banks, st_i = out[i]
+        assert st_i == 0
+        assert torch.equal(y, y_ref.cpu()), i
+        assert torch.equal(banks, banks_ref.cpu()), i
