@@ -51,6 +51,11 @@ constexpr uint32_t kABytes = kTileM * 128 * 2;        // two K atoms of 128 rows
 // bracket (odd: the rows of a warp hit different banks)
 constexpr int kProbes = 6;
 constexpr int kLCap = 31;
+// Counting passes at most: each pass at least halves a bracket's order-key range, so
+// real scores need far fewer. A row still over the list capacity after them (reached
+// only by constructed scores) keeps its ties at lo, possibly fewer than W, and the
+// kernel reports SDM_EUNSUPPORTED.
+constexpr int kMaxPasses = 40;
 __constant__ float kProbeAt[kProbes] = {-35.f, -15.f, -7.f, 7.f, 15.f, 35.f};
 // exchange area after the barriers and the TMEM address: the bracket lists [128][kLCap]
 // of scores (the row statistics of the first pass alias their start) and of their
@@ -468,14 +473,26 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
                 const uint32_t klo = order_key(__float_as_uint(lo));
                 const uint32_t khi = hi < INFINITY ? order_key(__float_as_uint(hi))
                                                    : order_key(__float_as_uint(fmx)) + 1u;
-                const bool over = !exact && khi - klo > 1u && c_lo - c_hi > kLCap;
+                // one value in the bracket: no float strictly between lo and its top
+                const bool single =
+                    !(nextafterf(lo, INFINITY) < (hi < INFINITY ? hi : nextafterf(fmx, INFINITY)));
+                const bool over = !exact && !single && c_lo - c_hi > kLCap;
                 // (the same rows in every warp at this barrier: all leave together)
                 if (!__any_sync(0xFFFFFFFFu, over))
                     break;
+                if (pass + 1 >= kMaxPasses) {
+                    if (over)
+                        report(stat, SDM_EUNSUPPORTED);
+                    break;
+                }
                 const float top = hi < INFINITY ? hi : fmx;
                 const float step = (top - lo) / (float)(c_lo - c_hi);
                 const float est = top - step * ((float)(W - c_hi) - 0.5f);
+                // the midpoint of the bracket's order keys (-0 and +0 share a key: where the
+                // midpoint's float is not strictly inside, the float just above lo is)
                 pr[0] = key_to_score(klo + ((khi - klo) >> 1));
+                if (!(pr[0] > lo && pr[0] < hi))
+                    pr[0] = nextafterf(lo, INFINITY);
 #pragma unroll
                 for (int k = 1; k < kProbes; ++k)
                     pr[k] = est + step * (0.25f * kProbeAt[k]);
@@ -483,10 +500,11 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(
             // The W-th largest score t. Keep: ex ? scores >= t : scores > t, and then the
             // lowest-numbered rows among the scores equal to t up to W in all (ties are
             // taken in column order, so a group takes ties only after lower columns' groups).
-            const uint32_t klo = order_key(__float_as_uint(lo));
-            const uint32_t khi = hi < INFINITY ? order_key(__float_as_uint(hi))
-                                               : order_key(__float_as_uint(fmx)) + 1u;
-            const bool listed = !exact && khi - klo > 1u;   // rank inside the bracket's list
+            const bool single_v =
+                !(nextafterf(lo, INFINITY) < (hi < INFINITY ? hi : nextafterf(fmx, INFINITY)));
+            // rank inside the bracket's list (a row left over the capacity after the last
+            // pass keeps ties at lo instead)
+            const bool listed = !exact && !single_v && c_lo - c_hi <= kLCap;
             const int m = c_lo - c_hi;
             // Scores at or above ta are kept outright: all of the row's W when exact (ta =
             // lo), else those at or above hi. The list pass writes them out (after the
