@@ -24,7 +24,9 @@
 // atomics; a block indexes fewer than 65,536 references). Each reference of the block then scans only its slot's bucket -- a handful
 // of entries, more for popular slots -- for the latest earlier writer and the earlier
 // referencing tokens. The window is indexed again by every block; the run length is the
-// one whose waves of blocks cost least (below).
+// one whose waves of blocks cost least (below). In each phase a thread loads its slot ids
+// kBatch at a time before it uses any of them, so that their L2 round trips overlap
+// (one dependent load a reference made the kernel wait on L2 latency throughout).
 #include "sdm_common.cuh"
 #include "sdm_internal.h"
 
@@ -35,6 +37,9 @@ namespace {
 constexpr int kBuckets = 4096;
 constexpr int kCodeThreads = 512;
 constexpr size_t kCodeSmemMax = 225 * 1024;
+// slot ids a thread loads before it uses any of them: the loads of a batch are in flight
+// together instead of one L2 round trip per reference
+constexpr int kBatch = 8;
 
 __device__ __forceinline__ uint32_t bucket_of(int32_t s)
 {
@@ -64,13 +69,25 @@ __global__ void __launch_bounds__(kCodeThreads) codes_kernel(const int32_t* __re
     for (int i = threadIdx.x; i < kBuckets / 2; i += blockDim.x)
         cur[i] = 0u;
     __syncthreads();
-    for (int e = threadIdx.x; e < nwin; e += blockDim.x) {
-        const int32_t s = __ldg(wsrc + e);
-        if (s >= 0 && s < N) {
-            const uint32_t bk = bucket_of(s);
-            atomicAdd(&cur[bk >> 1], 1u << (16 * (bk & 1)));
-        } else if (((e / W) & 1) == 0) {
-            report(status, SDM_ERANGE);
+    for (int e0 = threadIdx.x; e0 < nwin; e0 += kCodeThreads * kBatch) {
+        int32_t sv[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int e = e0 + u * kCodeThreads;
+            sv[u] = e < nwin ? __ldg(wsrc + e) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int e = e0 + u * kCodeThreads;
+            const int32_t s = sv[u];
+            if (e >= nwin)
+                break;
+            if (s >= 0 && s < N) {
+                const uint32_t bk = bucket_of(s);
+                atomicAdd(&cur[bk >> 1], 1u << (16 * (bk & 1)));
+            } else if (((e / W) & 1) == 0) {
+                report(status, SDM_ERANGE);
+            }
         }
     }
     __syncthreads();
@@ -111,63 +128,86 @@ __global__ void __launch_bounds__(kCodeThreads) codes_kernel(const int32_t* __re
             off[kBuckets] = (uint16_t)run;
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < nwin; e += blockDim.x) {
-        const int32_t s = __ldg(wsrc + e);
-        if (s >= 0 && s < N) {
-            const uint32_t bk = bucket_of(s);
-            const uint32_t at = (atomicAdd(&cur[bk >> 1], 1u << (16 * (bk & 1))) >> (16 * (bk & 1))) & 0xFFFFu;
-            slot[at] = s;
-            info[at] = (uint16_t)(((e / (2 * W)) << 7) | (((e / W) & 1) << 6) | (e % W));
+    for (int e0 = threadIdx.x; e0 < nwin; e0 += kCodeThreads * kBatch) {
+        int32_t sv[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int e = e0 + u * kCodeThreads;
+            sv[u] = e < nwin ? __ldg(wsrc + e) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int e = e0 + u * kCodeThreads;
+            const int32_t s = sv[u];
+            if (s >= 0 && s < N) {
+                const uint32_t bk = bucket_of(s);
+                const uint32_t at = (atomicAdd(&cur[bk >> 1], 1u << (16 * (bk & 1))) >> (16 * (bk & 1))) & 0xFFFFu;
+                slot[at] = s;
+                info[at] = (uint16_t)(((e / (2 * W)) << 7) | (((e / W) & 1) << 6) | (e % W));
+            }
         }
     }
     __syncthreads();
     const int nref = (t1 - t0) * 2 * W;
-    for (int e = threadIdx.x; e < nref; e += blockDim.x) {
-        const int kind = (e / W) & 1;
-        const int t = t0 + e / (2 * W);
-        const size_t o = ((size_t)b * T + t0) * 2 * W + e;
-        const int32_t s = __ldg(idx + o);
-        uint16_t code = kNoFwd;
-        if (s >= 0 && s < N) {
-            const uint32_t bk = bucket_of(s);
-            int best_dt = 1 << 30, best_pos = 0;
-            unsigned long long war0 = 0, war1 = 0;
-            for (uint32_t q = off[bk]; q < off[bk + 1]; ++q) {
-                if (slot[q] != s)
-                    continue;
-                const uint32_t in = info[q];
-                const int dt = t - (base + (int)(in >> 7));
-                if (dt < 0 || dt > win)
-                    continue;
-                const bool is_w = ((in >> 6) & 1) == 0;
-                // writers: the latest one at or before t (a read sees its own token's
-                // write), strictly before t for a write
-                if (is_w && dt < best_dt && (kind ? dt >= 0 : dt >= 1)) {
-                    best_dt = dt;
-                    best_pos = (int)(in & 0x3F);
-                }
-                // a write waits for the bank loads of every earlier referencing token
-                if (!kind && dt >= 1) {
-                    if (dt <= 64)
-                        war0 |= 1ull << (dt - 1);
-                    else
-                        war1 |= 1ull << (dt - 65);
-                }
-            }
-            if (best_dt <= win) {
-                code = (uint16_t)((best_dt << 8) | best_pos);
-                if (best_dt > 0) {
-                    atomicOr(fwdmask + (size_t)b * T + t - best_dt, 1ull << best_pos);
-                    if (!kind)
-                        atomicOr(deadmask + (size_t)b * T + t - best_dt, 1ull << best_pos);
-                }
-            }
-            if (war0)
-                atomicOr(warmask + ((size_t)b * T + t) * 2, war0);
-            if (war1)
-                atomicOr(warmask + ((size_t)b * T + t) * 2 + 1, war1);
+    const int32_t* rsrc = idx + ((size_t)b * T + t0) * 2 * W;
+    for (int e0 = threadIdx.x; e0 < nref; e0 += kCodeThreads * kBatch) {
+        int32_t sv[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int e = e0 + u * kCodeThreads;
+            sv[u] = e < nref ? __ldg(rsrc + e) : -1;
         }
-        codes[o] = code;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int e = e0 + u * kCodeThreads;
+            if (e >= nref)
+                break;
+            const int kind = (e / W) & 1;
+            const int t = t0 + e / (2 * W);
+            const size_t o = ((size_t)b * T + t0) * 2 * W + e;
+            const int32_t s = sv[u];
+            uint16_t code = kNoFwd;
+            if (s >= 0 && s < N) {
+                const uint32_t bk = bucket_of(s);
+                int best_dt = 1 << 30, best_pos = 0;
+                unsigned long long war0 = 0, war1 = 0;
+                for (uint32_t q = off[bk]; q < off[bk + 1]; ++q) {
+                    if (slot[q] != s)
+                        continue;
+                    const uint32_t in = info[q];
+                    const int dt = t - (base + (int)(in >> 7));
+                    if (dt < 0 || dt > win)
+                        continue;
+                    const bool is_w = ((in >> 6) & 1) == 0;
+                    // writers: the latest one at or before t (a read sees its own token's
+                    // write), strictly before t for a write
+                    if (is_w && dt < best_dt && (kind ? dt >= 0 : dt >= 1)) {
+                        best_dt = dt;
+                        best_pos = (int)(in & 0x3F);
+                    }
+                    // a write waits for the bank loads of every earlier referencing token
+                    if (!kind && dt >= 1) {
+                        if (dt <= 64)
+                            war0 |= 1ull << (dt - 1);
+                        else
+                            war1 |= 1ull << (dt - 65);
+                    }
+                }
+                if (best_dt <= win) {
+                    code = (uint16_t)((best_dt << 8) | best_pos);
+                    if (best_dt > 0) {
+                        atomicOr(fwdmask + (size_t)b * T + t - best_dt, 1ull << best_pos);
+                        if (!kind)
+                            atomicOr(deadmask + (size_t)b * T + t - best_dt, 1ull << best_pos);
+                    }
+                }
+                if (war0)
+                    atomicOr(warmask + ((size_t)b * T + t) * 2, war0);
+                if (war1)
+                    atomicOr(warmask + ((size_t)b * T + t) * 2 + 1, war1);
+            }
+            codes[o] = code;
+        }
     }
 }
 
