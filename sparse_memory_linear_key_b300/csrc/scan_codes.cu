@@ -66,6 +66,9 @@ __global__ void __launch_bounds__(kCodeThreads) codes_kernel(const int32_t* __re
     const int base = max(0, t0 - win);
     const int nwin = (t1 - base) * 2 * W;
     const int32_t* wsrc = idx + ((size_t)b * T + base) * 2 * W;     // [token][write, read][W]
+    // W is a power of two (the host checks): reference e of a run is token e >> (lw + 1),
+    // set (e >> lw) & 1, position e & (W - 1) -- shifts, not divisions
+    const int lw = __ffs(W) - 1;
     for (int i = threadIdx.x; i < kBuckets / 2; i += blockDim.x)
         cur[i] = 0u;
     __syncthreads();
@@ -85,7 +88,7 @@ __global__ void __launch_bounds__(kCodeThreads) codes_kernel(const int32_t* __re
             if (s >= 0 && s < N) {
                 const uint32_t bk = bucket_of(s);
                 atomicAdd(&cur[bk >> 1], 1u << (16 * (bk & 1)));
-            } else if (((e / W) & 1) == 0) {
+            } else if (((e >> lw) & 1) == 0) {
                 report(status, SDM_ERANGE);
             }
         }
@@ -143,7 +146,7 @@ __global__ void __launch_bounds__(kCodeThreads) codes_kernel(const int32_t* __re
                 const uint32_t bk = bucket_of(s);
                 const uint32_t at = (atomicAdd(&cur[bk >> 1], 1u << (16 * (bk & 1))) >> (16 * (bk & 1))) & 0xFFFFu;
                 slot[at] = s;
-                info[at] = (uint16_t)(((e / (2 * W)) << 7) | (((e / W) & 1) << 6) | (e % W));
+                info[at] = (uint16_t)(((e >> (lw + 1)) << 7) | (((e >> lw) & 1) << 6) | (e & (W - 1)));
             }
         }
     }
@@ -162,8 +165,8 @@ __global__ void __launch_bounds__(kCodeThreads) codes_kernel(const int32_t* __re
             const int e = e0 + u * kCodeThreads;
             if (e >= nref)
                 break;
-            const int kind = (e / W) & 1;
-            const int t = t0 + e / (2 * W);
+            const int kind = (e >> lw) & 1;
+            const int t = t0 + (e >> (lw + 1));
             const size_t o = ((size_t)b * T + t0) * 2 * W + e;
             const int32_t s = sv[u];
             uint16_t code = kNoFwd;
@@ -221,6 +224,8 @@ cudaError_t launch_scan_codes(const sdm_cfg& c, const int32_t* idx, int B, int T
         return cudaSuccess;
     if (T == 1)   // one token a sequence: the scan matches reads to own writes itself
         return cudaSuccess;
+    if (c.w <= 0 || (c.w & (c.w - 1)) != 0 || c.w > 64)   // (the kernel's index arithmetic)
+        return cudaErrorInvalidValue;
     // masks: fwdmask [B*T], deadmask [B*T], warmask [B*T][2], all cleared first
     cudaError_t e = cudaMemsetAsync(masks, 0, (size_t)B * T * 4 * sizeof(unsigned long long), s);
     if (e != cudaSuccess)
