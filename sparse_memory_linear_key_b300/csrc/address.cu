@@ -50,8 +50,8 @@ __global__ void __launch_bounds__(256) subkey_topw_kernel(
     float* qw = qs + warp * h;
     const int64_t nq = 2 * ntok;
     for (int64_t qi = (int64_t)blockIdx.x * 8 + warp; qi < nq; qi += (int64_t)gridDim.x * 8) {
-        const int kind = (int)(qi / ntok);
-        const int64_t tok = qi % ntok;
+        const int kind = qi >= ntok ? 1 : 0;             // (qi < 2 ntok)
+        const int64_t tok = kind ? qi - ntok : qi;
         const IO* q = (kind ? q_r : q_w) + tok * dk + half * h;
         __syncwarp();
         for (int k = lane; k < h; k += 32)
@@ -157,8 +157,8 @@ __device__ __forceinline__ void kth_narrow(uint32_t p, int c, int W, uint32_t& l
 template <int NC, int EW>
 __device__ __forceinline__ void select_candidates(const float* lv0, const int* li0, const float* lv1,
                                                   const int* li1, const unsigned short* pairs, int C,
-                                                  int n, int W, uint64_t* sel, int32_t* idx,
-                                                  float* wsel)
+                                                  const unsigned char* fpart, int n, int W,
+                                                  uint64_t* sel, int32_t* idx, float* wsel)
 {
     const int lane = threadIdx.x & 31;
     uint32_t ck[NC], cs[NC];
@@ -181,10 +181,11 @@ __device__ __forceinline__ void select_candidates(const float* lv0, const int* l
     }
     kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
     {
-        // floor: the largest lv0[a] + lv1[ceil(W / (a+1)) - 1] over the ranks a < W
+        // floor: the largest lv0[a] + lv1[ceil(W / (a+1)) - 1] over the ranks a < W (the
+        // partner ranks from fpart)
         uint32_t fl = 0u;
         for (int a = lane; a < W; a += 32)
-            fl = max(fl, float_order_bits(lv0[a] + lv1[(W + a) / (a + 1) - 1]));
+            fl = max(fl, float_order_bits(lv0[a] + lv1[fpart[a]]));
         kmin = max(kmin, __reduce_max_sync(0xFFFFFFFFu, fl));
         kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
     }
@@ -283,14 +284,17 @@ __global__ void __launch_bounds__(256, 4) candidate_select_kernel(
     __shared__ float lv[8][2][64];
     __shared__ int li[8][2][64];
     __shared__ uint64_t sel[8][64];     // kept weights [64] and sort keys [64] a warp
+    __shared__ unsigned char fpart[64]; // ceil(W / (a+1)) - 1: the floor's partner rank of a
     build_pairs(pairs, &npairs, W);
+    if (threadIdx.x < W)
+        fpart[threadIdx.x] = (unsigned char)((W + (int)threadIdx.x) / ((int)threadIdx.x + 1) - 1);
     __syncthreads();
     const int C = npairs;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nq = 2 * ntok;
     for (int64_t qi = (int64_t)blockIdx.x * 8 + warp; qi < nq; qi += (int64_t)gridDim.x * 8) {
-        const int kind = (int)(qi / ntok);
-        const int64_t tok = qi % ntok;
+        const int kind = qi >= ntok ? 1 : 0;             // (qi < 2 ntok)
+        const int64_t tok = kind ? qi - ntok : qi;
         const size_t base = ((size_t)kind * ntok + tok) * 2 * W;
         // each half's W best rows sorted by (score desc, row asc). The lists come in
         // ascending row order (the tensor-core scoring writes them so; the SIMT one
@@ -348,8 +352,8 @@ __global__ void __launch_bounds__(256, 4) candidate_select_kernel(
         }
         __syncwarp();
         const size_t ob = ((size_t)tok * 2 + kind) * W;
-        select_candidates<NC, 2>(lv[warp][0], li[warp][0], lv[warp][1], li[warp][1], pairs, C, n,
-                                 W, sel[warp], idx + ob, wsel + ob);
+        select_candidates<NC, 2>(lv[warp][0], li[warp][0], lv[warp][1], li[warp][1], pairs, C, fpart,
+                                 n, W, sel[warp], idx + ob, wsel + ob);
     }
 }
 

@@ -59,16 +59,21 @@ cudaError_t launch_bank_init(const void* M0, void* banks, size_t bank_bytes, int
 // (scan.cu) and only the slots a sequence never writes need M0 in its bank afterwards.
 // first_write[b][s] is the first token of sequence b whose write set holds s.
 
+// W is a power of two and B * T < 2^31 (the host checks): the token of write reference e
+// is e >> lw, its position e & (W - 1), and the sequence a 32-bit division of the token
 __global__ void __launch_bounds__(256) first_touch_kernel(const int32_t* __restrict__ idx,
                                                           int64_t nref, int T, int W, int N,
                                                           int32_t* __restrict__ first_write)
 {
+    const int lw = __ffs(W) - 1;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nref; e += stride) {
-        const int64_t tok = e / W;                  // b * T + t
-        const int32_t s = __ldg(idx + tok * 2 * W + e % W);
-        if (s >= 0 && s < N)
-            atomicMin(first_write + (tok / T) * N + s, (int32_t)(tok % T));
+        const uint32_t tok = (uint32_t)(e >> lw);  // b * T + t
+        const int32_t s = __ldg(idx + ((int64_t)tok << (lw + 1)) + (e & (W - 1)));
+        if (s >= 0 && s < N) {
+            const uint32_t b = tok / (uint32_t)T;
+            atomicMin(first_write + (int64_t)b * N + s, (int32_t)(tok - b * (uint32_t)T));
+        }
     }
 }
 
@@ -139,6 +144,8 @@ cudaError_t launch_first_touch(const sdm_cfg& c, const int32_t* idx, int B, int 
     cudaError_t e = cudaMemsetAsync(first_write, 0x7F, (size_t)B * N * sizeof(int32_t), s);
     if (e != cudaSuccess || T <= 0)
         return e;
+    if ((int64_t)B * T > 0x7FFFFFFF || c.w <= 0 || (c.w & (c.w - 1)) != 0)
+        return cudaErrorInvalidValue;   // (the kernel's index arithmetic)
     const int64_t nref = (int64_t)B * T * c.w;
     int64_t blocks = (nref + 255) / 256;
     const int64_t cap = (int64_t)num_sms_current_device() * 8;
