@@ -899,13 +899,19 @@ __global__ void __launch_bounds__(kSmallThreads) address_small_kernel(
     for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < clear_words;
          e += (long long)gridDim.x * blockDim.x)
         clear[e] = 0u;
-    for (int e = threadIdx.x; e < 8 * h; e += blockDim.x) {
-        const int j = e / h, k = e % h;
-        const int64_t qi = q0 + j;                          // token-major: tok * 2 + kind
-        IO val = IO(0.0f);
-        if (j < kQG && qi < nq)
-            val = ((qi & 1) ? q_r : q_w)[(qi >> 1) * dk + half * h + k];
-        reinterpret_cast<IO*>(sm + L.qs + j * rs)[k] = val;
+    {
+        // 16-byte pieces: a query half is a whole number of them on this path ((h * es) %
+        // 16 == 0) and the q buffers are 16-byte aligned, so every piece is too; one load
+        // a thread, all in flight together
+        const int pieces = rowb / 16;
+        for (int e = threadIdx.x; e < 8 * pieces; e += blockDim.x) {
+            const int j = e / pieces, k = e - j * pieces;
+            const int64_t qi = q0 + j;                      // token-major: tok * 2 + kind
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (j < kQG && qi < nq)
+                val = reinterpret_cast<const uint4*>(((qi & 1) ? q_r : q_w) + (qi >> 1) * dk + half * h)[k];
+            *reinterpret_cast<uint4*>(sm + L.qs + j * rs + k * 16) = val;
+        }
     }
     ok = __syncthreads_and(ok) != 0;
     // 3. scores of this half
