@@ -21,15 +21,38 @@ namespace {
 __device__ __forceinline__ float to_f32(bf16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ float to_f32(float x) { return x; }
 
-// dst [rows, cols] fp32 <- src [rows, cols] (row-major, dst row stride ldd)
+// dst [total] fp32 <- src [total] (both contiguous). vec: both 16-byte aligned, and a
+// thread converts eight elements a step with 16- and 32-byte accesses; the tail (and
+// every element without vec) one by one.
 template <typename IO>
-__global__ void __launch_bounds__(256) widen_kernel(const IO* __restrict__ src, int64_t rows,
-                                                    int cols, float* __restrict__ dst, int ldd)
+__global__ void __launch_bounds__(256) widen_kernel(const IO* __restrict__ src, int64_t total,
+                                                    float* __restrict__ dst, bool vec)
 {
-    const int64_t total = rows * cols;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-         e += (int64_t)gridDim.x * blockDim.x)
-        dst[(e / cols) * ldd + e % cols] = to_f32(src[e]);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nv = vec ? total / 8 : 0;
+    for (int64_t v = i0; v < nv; v += stride) {
+        float f[8];
+        if constexpr (sizeof(IO) == 2) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4*>(src) + v);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                f[2 * i] = __uint_as_float(w[i] << 16);           // bf16 -> fp32: exact
+                f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+        } else {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(src) + 2 * v);
+            const float4 b = __ldg(reinterpret_cast<const float4*>(src) + 2 * v + 1);
+            f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+            f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+        }
+        float4* d = reinterpret_cast<float4*>(dst) + 2 * v;
+        d[0] = make_float4(f[0], f[1], f[2], f[3]);
+        d[1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+    for (int64_t e = nv * 8 + i0; e < total; e += stride)
+        dst[e] = to_f32(src[e]);
 }
 
 // one warp per (kind, token): softmax backward over the W kept pairs, scattered into the
@@ -45,8 +68,8 @@ __global__ void __launch_bounds__(256) select_bwd_kernel(const int32_t* __restri
     const int64_t q = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;   // kind * ntok + tok
     if (q >= 2 * ntok)
         return;   // whole warps
-    const int kind = (int)(q / ntok);
-    const int64_t tok = q % ntok;
+    const int kind = q >= ntok ? 1 : 0;                 // (q < 2 ntok)
+    const int64_t tok = kind ? q - ntok : q;
     const size_t base = ((size_t)tok * 2 + kind) * W;
     float sum = 0.f;
     for (int j = lane; j < W; j += 32)
@@ -92,9 +115,12 @@ AddrBwdWs addr_bwd_layout(const sdm_cfg& c, int64_t ntok)
 }
 
 template <typename IO>
-cudaError_t widen(const void* src, int64_t rows, int cols, float* dst, int ldd, cudaStream_t s)
+cudaError_t widen(const void* src, int64_t rows, int cols, float* dst, cudaStream_t s)
 {
-    widen_kernel<IO><<<grid_for(rows * cols), 256, 0, s>>>((const IO*)src, rows, cols, dst, ldd);
+    const int64_t total = rows * cols;
+    const bool vec = (((uintptr_t)src | (uintptr_t)dst) & 15u) == 0;
+    widen_kernel<IO><<<grid_for(vec ? (total + 7) / 8 : total), 256, 0, s>>>((const IO*)src, total,
+                                                                              dst, vec);
     return cudaGetLastError();
 }
 
@@ -125,14 +151,14 @@ int launch_address_backward(const sdm_cfg& c, const void* K1, const void* K2, co
     const bool bf = c.dtype == SDM_BF16;
     cudaError_t e = cudaMemsetAsync(ds1, 0, 2 * 2 * (size_t)ntok * n * sizeof(float), s);
     if (e == cudaSuccess)
-        e = bf ? widen<bf16>(q_w, ntok, dk, qf, dk, s) : widen<float>(q_w, ntok, dk, qf, dk, s);
+        e = bf ? widen<bf16>(q_w, ntok, dk, qf, s) : widen<float>(q_w, ntok, dk, qf, s);
     if (e == cudaSuccess)
-        e = bf ? widen<bf16>(q_r, ntok, dk, qf + (size_t)ntok * dk, dk, s)
-               : widen<float>(q_r, ntok, dk, qf + (size_t)ntok * dk, dk, s);
+        e = bf ? widen<bf16>(q_r, ntok, dk, qf + (size_t)ntok * dk, s)
+               : widen<float>(q_r, ntok, dk, qf + (size_t)ntok * dk, s);
     if (e == cudaSuccess)
-        e = bf ? widen<bf16>(K1, n, h, k1f, h, s) : widen<float>(K1, n, h, k1f, h, s);
+        e = bf ? widen<bf16>(K1, n, h, k1f, s) : widen<float>(K1, n, h, k1f, s);
     if (e == cudaSuccess)
-        e = bf ? widen<bf16>(K2, n, h, k2f, h, s) : widen<float>(K2, n, h, k2f, h, s);
+        e = bf ? widen<bf16>(K2, n, h, k2f, s) : widen<float>(K2, n, h, k2f, s);
     if (e == cudaSuccess) {
         select_bwd_kernel<<<grid_for(2 * ntok * 32), 256, 0, s>>>(idx, wsel, dwsel, ntok, c.w, n, ds1,
                                                                   ds2);
@@ -194,13 +220,13 @@ int launch_project_backward(const sdm_cfg& c, const sdm_weights& w, const void* 
     float* wv = wqr + (size_t)d * dk;
     const bool bf = c.dtype == SDM_BF16;
     const bool tc = bf;   // TF32 tensor cores for a bf16 layer
-    cudaError_t e = bf ? widen<bf16>(x, ntok, d, xf, d, s) : widen<float>(x, ntok, d, xf, d, s);
+    cudaError_t e = bf ? widen<bf16>(x, ntok, d, xf, s) : widen<float>(x, ntok, d, xf, s);
     if (e == cudaSuccess)
-        e = bf ? widen<bf16>(w.W_qw, d, dk, wqw, dk, s) : widen<float>(w.W_qw, d, dk, wqw, dk, s);
+        e = bf ? widen<bf16>(w.W_qw, d, dk, wqw, s) : widen<float>(w.W_qw, d, dk, wqw, s);
     if (e == cudaSuccess)
-        e = bf ? widen<bf16>(w.W_qr, d, dk, wqr, dk, s) : widen<float>(w.W_qr, d, dk, wqr, dk, s);
+        e = bf ? widen<bf16>(w.W_qr, d, dk, wqr, s) : widen<float>(w.W_qr, d, dk, wqr, s);
     if (e == cudaSuccess)
-        e = bf ? widen<bf16>(w.W_v, d, d, wv, d, s) : widen<float>(w.W_v, d, d, wv, d, s);
+        e = bf ? widen<bf16>(w.W_v, d, d, wv, s) : widen<float>(w.W_v, d, d, wv, s);
     if (e != cudaSuccess)
         return SDM_ECUDA;
     int rc = gemm_f32_rm(s, false, true, nt, d, dk, dq_w, dk, wqw, dk, dx, d, 0.f, tc);
