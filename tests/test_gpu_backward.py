@@ -211,6 +211,46 @@ def test_project_backward_matches_oracle(name):
         assert rel_err(got.cpu().numpy(), want) <= tol, name
 
 
+def _offset_copy(t):
+    """t's values in a buffer one element past a 16-byte boundary (a contiguous view)."""
+    buf = torch.empty(t.numel() + 8, dtype=t.dtype, device="cuda")
+    v = buf[1:1 + t.numel()].view(t.shape)
+    v.copy_(t)
+    assert v.data_ptr() % 16 != 0
+    return v
+
+
+@pytest.mark.parametrize("name", ["tiny-f32", "w64-small"])
+def test_project_backward_unaligned_inputs_match_aligned(name):
+    """The fp32 copies of x and the weights take their element-by-element path when a
+    pointer is not 16-byte aligned; the gradients are the same bits either way (the copies
+    are exact and the GEMMs read the same workspace)."""
+    wl = SMALL[name]
+    cfg = tl.cfg_of(wl)
+    p = tl.to_dev(synth.make_params(wl))
+    x = synth.make_tokens(wl)["x"].reshape(-1, wl.d).cuda()
+    ntok, d, dk = x.shape[0], wl.d, wl.dk
+    g = torch.Generator().manual_seed(17)
+    dqw, dqr, dvv = (torch.randn(ntok, dk, generator=g).cuda(), torch.randn(ntok, dk, generator=g).cuda(),
+                     torch.randn(ntok, d, generator=g).cuda())
+    ws = sdm.alloc_workspace(sdm.project_backward_workspace_bytes(cfg, ntok))
+    outs = []
+    for shifted in (False, True):
+        pp = dict(p)
+        xx = x
+        if shifted:
+            for k in ("W_qw", "W_qr", "W_v"):
+                pp[k] = _offset_copy(p[k])
+            xx = _offset_copy(x)
+        o = (torch.empty(ntok, d, device="cuda"), torch.empty(d, dk, device="cuda"),
+             torch.empty(d, dk, device="cuda"), torch.empty(d, d, device="cuda"))
+        sdm.sdm_project_backward(cfg, pp, xx, dqw, dqr, dvv, *o, ws)
+        torch.cuda.synchronize()
+        outs.append([t.cpu() for t in o])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b), name
+
+
 @pytest.mark.parametrize("name,tol", [("tiny-f32", 1e-4), ("w64-small", 2e-2)])
 def test_layer_backward_chain_matches_oracle(name, tol):
     """The whole layer's gradients: scan backward -> addressing backward -> projection
