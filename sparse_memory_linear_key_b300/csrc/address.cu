@@ -235,6 +235,8 @@ __device__ __forceinline__ void select_candidates(const float* lv0, const int* l
         part += cv[i];
     }
     part = __reduce_add_sync_f(part);
+    const float inv = 1.0f / part;   // (one division a query; a weight is within an ulp of
+                                     // the quotient)
     // kept weights by position in sel (as floats); sort keys (slot << 6) | position (slots
     // below 2^18, positions below 64)
     float* selw = reinterpret_cast<float*>(sel);
@@ -248,7 +250,7 @@ __device__ __forceinline__ void select_candidates(const float* lv0, const int* l
         const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep[i]);
         if (keep[i]) {
             const int pos = base_pos + __popc(bal & ((1u << lane) - 1u));
-            selw[pos] = cv[i] / part;
+            selw[pos] = cv[i] * inv;
             reinterpret_cast<uint32_t*>(selw + 64)[pos] = (cs[i] << 6) | (uint32_t)pos;
         }
         base_pos += __popc(bal);
